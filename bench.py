@@ -1,0 +1,473 @@
+"""Benchmark of the linear-recurrence state update on GB300.
+
+One step = both tier-1 scan forms (FMA and gated) over the large elementwise
+workload B=8 T=8192 N=2048 (inputs resident in HBM, 1.6 GB per form, larger
+than L2), through the C ABI.  Prints ONE JSON line with the contract keys,
+the roofline of the dominant kernel, the CPU-oracle baseline, the
+end-to-end figure (pinned host buffers, copies inside the timed region) and,
+under "forms", every other workload measured the same way.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+channels need no collective): "scaling": "weak", value = all ranks' bytes /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+SCAN = synth.CONFIGS["scan_large"]
+GB = 1e9
+
+
+def scan_bytes(B, T, N, has_s0=True):
+    """Algorithmic bytes of one scan: read a and b|u, write s_t (12 B per
+    element) plus s0 in and s_final out (8 B per channel)."""
+    return 12 * B * T * N + (8 if has_s0 else 4) * B * N
+
+
+# per-workload algorithmic bytes and flops ("Roofline accounting")
+def matrix_cost(name):
+    c = synth.CONFIGS[name]
+    B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+    th = B * T * H
+    state = B * H * dk * dv * 4
+    if name == "gla":
+        per_th, flop_e, s_in = (3 * dk + 2 * dv) * 4, 5, 0
+    elif name == "mamba2":
+        G = c["G"]
+        per_th, flop_e, s_in = (2 * dv + 1) * 4 + 2 * dk * 4 * G / H, 5, 0
+    elif name == "deltanet":
+        per_th, flop_e, s_in = (2 * dk + 2 * dv + 1) * 4, 6, 0
+    elif name == "rwkv7_prefill":
+        per_th, flop_e, s_in = (3 * dk + 2 * dv) * 4, 7, 0
+    else:  # rwkv7_decode: random initial state read and written
+        per_th, flop_e, s_in = (3 * dk + 2 * dv) * 4, 7, state
+    nbytes = th * per_th + state + s_in
+    flops = th * dk * dv * flop_e
+    return th, nbytes, flops
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def traffic_record(kernel):
+    """dram bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = open(os.path.join(ROOT, "scan_runtime_gb300", "csrc", "scan.cu"), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    for line in open(path):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("src_sha") == sha:
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, on):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(ts=ts, sm=float(parts[1]), max=float(parts[2]), hw=parts[5], hwt=parts[6],
+                                 swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inwin = [r for r in rows if self.t_on and self.t_off and self.t_on <= r["ts"] <= self.t_off]
+        use = inwin or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                          ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in use):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inwin)}
+
+
+# ---------------------------------------------------------------- CPU baseline
+def cpu_oracle_scan(a, b, u, s0, threads):
+    """Time the fp64 CPU oracle on both scan forms; the batch rows are
+    independent, so they run on `threads` Python threads (ctypes releases the
+    GIL).  Returns seconds."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle
+    B = a.shape[0]
+    s064 = s0.astype(np.float64)
+
+    def one(i):
+        oracle.scan_fma(a[i:i + 1], b[i:i + 1], s064[i:i + 1])
+        oracle.scan_gated(a[i:i + 1], u[i:i + 1], s064[i:i + 1])
+
+    oracle.scan_fma(a[:1, :8], b[:1, :8], s064[:1])           # load the library outside the timing
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(one, range(B)))
+    return time.perf_counter() - t0
+
+
+def cpu_sample_inputs(T_sample):
+    """A bounded sample of the large scan workload: all B and N, the first
+    T_sample steps (same distributions, CPU-generated)."""
+    x = synth.scan_inputs(SCAN["B"], T_sample, SCAN["N"], large=True)
+    return (x["a"].numpy(), x["b"].numpy(), x["u"].numpy(), x["s0"].numpy())
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on this arm's workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    T_s = 1024
+    a, b, u, s0 = cpu_sample_inputs(T_s)
+    threads = min(SCAN["B"], os.cpu_count() or 1)
+    for _ in range(args.warmup):
+        cpu_oracle_scan(a, b, u, s0, threads)
+    times = [cpu_oracle_scan(a, b, u, s0, threads) for _ in range(args.steps)]
+    per_step_bytes = 2 * scan_bytes(SCAN["B"], T_s, SCAN["N"])
+    total = sum(times)
+    value = args.steps * per_step_bytes / total / GB
+    sample = f"B=8 T={T_s} N=2048 (first {T_s} of 8192 steps), both forms, fp64 oracle"
+    line = {
+        "impl": "reference", "metric": "recurrence_scan_GBps", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "scan_large B=8 T=8192 N=2048, FMA + gated forms", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def time_form(torch, fn, warmup, reps, stream):
+    """Median ms of `fn` over `reps` launches (CUDA events on `stream`)."""
+    for _ in range(warmup):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for s, e in ev:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ts = sorted(s.elapsed_time(e) for s, e in ev)
+    return ts[len(ts) // 2]
+
+
+def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=3, reps=20):
+    """Every other workload, each on its own inputs, outside the main timed
+    region.  Returns a dict of per-form results."""
+    out = {}
+    s = stream
+    with torch.cuda.stream(stream):
+        # the chunked look-back kernel on the same large scan workload
+        x = synth.config_inputs("scan_large", device=dev)
+        B, T, N = SCAN["B"], SCAN["T"], SCAN["N"]
+        ctx.ensure_workspace(B, T, N)
+        so = torch.empty((B, T, N), device=dev)
+        sf = torch.empty((B, N), device=dev)
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+        for form, rhs in (("fma", "b"), ("gated", "u")):
+            f = sr.sn_scan_fma if form == "fma" else sr.sn_scan_gated
+            ms = time_form(torch, lambda: f(ctx.handle, B, T, N, x["a"], x[rhs], x["s0"], sf, so, s), warmup, reps, s)
+            nb = scan_bytes(B, T, N)
+            out[f"scan_{form}_lookback"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
+                                           "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+        del x, so, sf
+        for name in ("gla", "mamba2", "deltanet", "rwkv7_prefill", "rwkv7_decode"):
+            c = synth.CONFIGS[name]
+            x = synth.config_inputs(name, device=dev)
+            Bc, Tc, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+            o = torch.empty((Bc, Tc, H, dv), device=dev)
+            if name in ("gla", "mamba2"):
+                S = torch.empty((Bc, H, dk, dv), device=dev)
+                fn = lambda: sr.sn_recur_diag(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"], x["scale"],
+                                              x["q"], x["k"], x["v"], x["d"], None, S, o, s)
+            elif name == "deltanet":
+                S = torch.empty((Bc, H, dk, dv), device=dev)
+                fn = lambda: sr.sn_recur_delta(ctx.handle, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"], x["v"],
+                                               x["beta"], None, S, o, s)
+            else:
+                S = torch.empty((Bc, H, dv, dk), device=dev)
+                fn = lambda: sr.sn_recur_rwkv7(ctx.handle, Bc, Tc, H, dk, dv, x["q"], x["k"], x["v"], x["w"],
+                                               x["S0"], S, o, s)
+            st = fn()
+            if st != sr.SN_OK:
+                out[name] = {"error": sr.sn_status_str(st)}
+                continue
+            ms = time_form(torch, fn, warmup, reps, s)
+            th, nb, fl = matrix_cost(name)
+            gbps = nb / ms / 1e6
+            tflops = fl / ms / 1e9
+            r = {"ms": round(ms, 4), "tok_heads_per_s": round(th / ms * 1e3, 1), "GBps": round(gbps, 1),
+                 "hbm_frac": round(gbps / hbm_peak, 3), "TFLOPs_fp32": round(tflops, 2),
+                 "fp32_frac": round(tflops / fp32_peak_tflops, 3)}
+            r["bound"] = "hbm" if name == "rwkv7_decode" else "alu"
+            out[name] = r
+            del x, o, S
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    import scan_runtime_gb300 as sr
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    sr.build()
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    ctx = sr.Context(local)
+    stream = torch.cuda.Stream(dev)
+    peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    props = torch.cuda.get_device_properties(dev)
+    sm_count = props.multi_processor_count
+    fp32_peak = sm_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12   # TFLOP/s
+
+    B, T, N = SCAN["B"], SCAN["T"], SCAN["N"]
+    x = synth.config_inputs("scan_large", device=dev)
+    so_f = torch.empty((B, T, N), device=dev)
+    so_g = torch.empty((B, T, N), device=dev)
+    sf_f = torch.empty((B, N), device=dev)
+    sf_g = torch.empty((B, N), device=dev)
+    h = ctx.handle
+    per_form_bytes = scan_bytes(B, T, N)
+    step_bytes = 2 * per_form_bytes
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        st1 = sr.sn_scan_fma(h, B, T, N, x["a"], x["b"], x["s0"], sf_f, so_f, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        st2 = sr.sn_scan_gated(h, B, T, N, x["a"], x["u"], x["s0"], sf_g, so_g, stream)
+        if evs is not None:
+            evs[2].record(stream)
+        if st1 != sr.SN_OK or st2 != sr.SN_OK:
+            raise RuntimeError(f"scan failed: {st1} {st2}")
+
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk.mark(True)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk.mark(False)
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.1)
+    clk.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    launch_ms = [e[0].elapsed_time(e[1]) for e in evs] + [e[1].elapsed_time(e[2]) for e in evs]
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    value = world * args.steps * step_bytes / (ms_total / 1e3) / GB
+    achieved = per_form_bytes / (avg_launch_ms / 1e3) / GB
+
+    # end to end through the public API: pinned host inputs in, s_t out, every step
+    e2e = None
+    if not args.no_e2e:
+        ha = torch.empty((B, T, N), pin_memory=True)
+        hb = torch.empty((B, T, N), pin_memory=True)
+        hu = torch.empty((B, T, N), pin_memory=True)
+        hs0 = torch.empty((B, N), pin_memory=True)
+        ha.copy_(x["a"])
+        hb.copy_(x["b"])
+        hu.copy_(x["u"])
+        hs0.copy_(x["s0"])
+        hof = torch.empty((B, T, N), pin_memory=True)
+        hog = torch.empty((B, T, N), pin_memory=True)
+        hff = torch.empty((B, N), pin_memory=True)
+        hfg = torch.empty((B, N), pin_memory=True)
+        da, db, du, ds0 = (torch.empty_like(t, device=dev) for t in (ha, hb, hu, hs0))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                da.copy_(ha, non_blocking=True)
+                db.copy_(hb, non_blocking=True)
+                du.copy_(hu, non_blocking=True)
+                ds0.copy_(hs0, non_blocking=True)
+                s1 = sr.sn_scan_fma(h, B, T, N, da, db, ds0, sf_f, so_f, stream)
+                s2 = sr.sn_scan_gated(h, B, T, N, da, du, ds0, sf_g, so_g, stream)
+                hof.copy_(so_f, non_blocking=True)
+                hog.copy_(so_g, non_blocking=True)
+                hff.copy_(sf_f, non_blocking=True)
+                hfg.copy_(sf_g, non_blocking=True)
+            if s1 != sr.SN_OK or s2 != sr.SN_OK:
+                raise RuntimeError("scan failed in e2e step")
+
+        n_e2e = max(3, min(args.steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        h2d = 3 * B * T * N * 4 + B * N * 4
+        d2h = 2 * B * T * N * 4 + 2 * B * N * 4
+        e2e = {"value": round(step_bytes / (e2e_ms / 1e3) / GB, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)}
+        del ha, hb, hu, hof, hog, da, db, du
+
+    forms = None
+    if not args.no_forms:
+        forms = bench_forms(torch, sr, ctx, dev, stream, fp32_peak, hbm_peak)
+
+    # CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        T_s = 1024
+        a, b, u, s0 = cpu_sample_inputs(T_s)
+        threads = min(B, os.cpu_count() or 1)
+        secs = cpu_oracle_scan(a, b, u, s0, threads)
+        cpu = {"value": round(2 * scan_bytes(B, T_s, N) / secs / GB, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"B=8 T={T_s} N=2048 (first {T_s} of 8192 steps), both forms, fp64 oracle, "
+                         f"{secs:.2f} s"}
+
+    assert ctx.last_error() == sr.SN_OK
+    clocks = clk.summary()
+    traffic = traffic_record("scan_seq_tma")
+    line = {
+        "metric": "recurrence_scan_GBps", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "scan_large B=8 T=8192 N=2048, FMA + gated forms (sequential-in-T kernel)",
+                   "B": B, "T": T, "N": N, "bytes_per_step": step_bytes,
+                   "l2": "inputs (1.07 GB per form) larger than L2; no flush",
+                   "parallelism": f"dp{world}" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "kernel": "scan_seq_tma", "peak_source": f"{peak_src} hbm_gbs"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "forms": forms,
+        "fp32_peak_tflops": round(fp32_peak, 1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-forms", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

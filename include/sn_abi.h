@@ -1,0 +1,238 @@
+/*
+ * sn_abi.h -- stable C ABI of the GB300 linear-recurrence library (libsn).
+ *
+ * The library computes the unified linear-recurrence state update of O(N)
+ * sequence models on one NVIDIA GB300 GPU (sm_103a):
+ *   tier 1  per-channel first-order scans (FMA and gated forms);
+ *   tier 2  per-head matrix-state recurrences with readout (diagonal decay
+ *           for GLA / Mamba-2, the DeltaNet delta rule, RWKV-7 rank-1
+ *           removal), including batched single-step (T = 1) decode.
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "SunnyNet 工程化实录：一个 O(N) 架构如何长出自己的 C 推理运行时"
+ *   [P2] "我拿同一份权重和 llama.cpp 正面比了一场：我手写的 C 内核，慢了 1.1–1.7 倍"
+ *
+ * ABI conventions follow [P1] §6 (stable C ABI):
+ *   - every symbol carries the sn_ prefix; handles are opaque;
+ *   - the version is packed as (MAJOR << 16) | (MINOR << 8) | PATCH;
+ *   - capability bits SN_CAP_*; callers must ignore bits they do not know;
+ *   - sn_status is a fixed int32_t; array dimensions are int32_t;
+ *   - a caller passes SN_ABI_VERSION_MAJOR to sn_abi_check() and must refuse
+ *     the library when it returns SN_E_UNSUPPORTED.
+ *
+ * Memory and ownership (all compute calls):
+ *   - every tensor argument is a DEVICE pointer to contiguous, row-major fp32
+ *     data owned by the caller; the library never frees or retains it;
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Calls are asynchronous: they validate, enqueue the
+ *     kernel on `stream` and return.  Outputs are valid once the stream has
+ *     reached that point;
+ *   - compute calls never allocate device memory.  The only device memory the
+ *     library owns is a 256-byte status block per context (allocated by
+ *     sn_ctx_create) plus what the caller hands over with
+ *     sn_ctx_set_workspace;
+ *   - an initial-state pointer may be NULL (zero initial state); a final-state
+ *     or per-step output pointer may be NULL (not written);
+ *   - the initial and final state may be the same buffer (in-place
+ *     continuation); any other overlap between an output and an input or
+ *     another output is rejected with SN_E_INVAL.
+ *
+ * Errors:
+ *   - argument errors are detected on the host before anything is enqueued;
+ *     outputs are then left untouched;
+ *   - SN_E_DEVICE reports a CUDA runtime error at launch;
+ *   - device-side failures (a bounded wait that ran out) are recorded in the
+ *     context's status block; sn_ctx_last_error() returns and clears them
+ *     once the caller has synchronised the stream.
+ *
+ * Thread safety: a context may be used from one host thread at a time, and
+ * calls that use the context's workspace must be ordered on one stream.
+ */
+#ifndef SN_ABI_H
+#define SN_ABI_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SN_ABI_VERSION_MAJOR 1
+#define SN_ABI_VERSION_MINOR 0
+#define SN_ABI_VERSION_PATCH 0
+#define SN_ABI_VERSION \
+    ((SN_ABI_VERSION_MAJOR << 16) | (SN_ABI_VERSION_MINOR << 8) | SN_ABI_VERSION_PATCH)
+
+typedef int32_t sn_status;
+
+/* Status codes.  The first six are the ones [P1] §6 fixes; the last two are
+ * extensions of this library. */
+#define SN_OK             0
+#define SN_E_INVAL       (-1)  /* bad argument: NULL, dim <= 0, overlap, misalignment */
+#define SN_E_NOMEM       (-2)  /* workspace missing or too small */
+#define SN_E_IO          (-3)  /* reserved by the ABI (no file I/O here) */
+#define SN_E_FORMAT      (-4)  /* reserved by the ABI (no file formats here) */
+#define SN_E_UNSUPPORTED (-5)  /* major-version mismatch, head dim not compiled, device not sm_103 */
+#define SN_E_DEVICE      (-6)  /* CUDA runtime error (launch failure, bad stream, ...) */
+#define SN_E_TIMEOUT     (-7)  /* a bounded device-side wait ran out (see sn_ctx_last_error) */
+
+/* Capability bits returned by sn_abi_caps(). */
+#define SN_CAP_SCAN_FMA    (1u << 0)   /* sn_scan_fma */
+#define SN_CAP_SCAN_GATED  (1u << 1)   /* sn_scan_gated */
+#define SN_CAP_RECUR_DIAG  (1u << 2)   /* sn_recur_diag */
+#define SN_CAP_RECUR_DELTA (1u << 3)   /* sn_recur_delta */
+#define SN_CAP_RECUR_RWKV7 (1u << 4)   /* sn_recur_rwkv7 */
+#define SN_CAP_DECODE      (1u << 5)   /* dedicated T == 1 decode kernels */
+#define SN_CAP_SCAN_LOOKBACK (1u << 6) /* chunked scan with look-back carries */
+
+/* Decay layouts of sn_recur_diag. */
+#define SN_DECAY_PER_KEY  0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
+#define SN_DECAY_PER_HEAD 1   /* d is (B, T, H):     one scalar decay per head (Mamba-2) */
+
+/* Context options (sn_ctx_set_option / sn_ctx_get_option). */
+#define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back */
+#define SN_OPT_WAIT_LIMIT_US    2  /* bound on any device-side wait, microseconds (default 1e6) */
+#define SN_OPT_DEBUG_POISON     3  /* 1: look-back waits for a flag no chunk publishes (tests the bound) */
+#define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
+#define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
+
+#define SN_SCAN_KERNEL_AUTO       0
+#define SN_SCAN_KERNEL_SEQUENTIAL 1
+#define SN_SCAN_KERNEL_LOOKBACK   2
+
+/* Operation ids for sn_workspace_bytes(). */
+#define SN_OP_SCAN_FMA   1
+#define SN_OP_SCAN_GATED 2
+
+typedef struct SnCtx SnCtx;
+
+/* ---------------------------------------------------------------- meta */
+
+/* Packed version of the loaded library ((MAJOR << 16) | (MINOR << 8) | PATCH). */
+uint32_t sn_abi_version(void);
+
+/* SN_OK when `major` equals the library's major version, else
+ * SN_E_UNSUPPORTED (the caller must refuse the library).  [P1] §6. */
+sn_status sn_abi_check(int32_t major);
+
+/* Capability bits (SN_CAP_*).  Unknown bits must be ignored by callers. */
+uint32_t sn_abi_caps(void);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* sn_status_str(sn_status s);
+
+/* ---------------------------------------------------------------- context */
+
+/* Create a context bound to CUDA device `device`.  Allocates the context's
+ * 256-byte device status block on that device.  Errors: SN_E_INVAL (NULL
+ * out_ctx, bad device index), SN_E_UNSUPPORTED (device is not sm_103),
+ * SN_E_DEVICE (CUDA failure).  On error *out_ctx is set to NULL. */
+sn_status sn_ctx_create(int32_t device, SnCtx** out_ctx);
+
+/* Free a context (NULL is a no-op).  The caller must have synchronised all
+ * streams that still use it. */
+void sn_ctx_free(SnCtx* ctx);
+
+/* Hand the context a caller-owned device workspace (used only by the chunked
+ * look-back scan).  `dev_ptr` must be 256-byte aligned; `bytes` >= 0; a NULL
+ * pointer or 0 bytes removes it.  The library never frees it.  The first
+ * look-back launch after this call clears the flag area with one
+ * cudaMemsetAsync on that launch's stream. */
+sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes);
+
+/* Workspace bytes the chunked look-back scan needs for this problem
+ * (op = SN_OP_SCAN_FMA or SN_OP_SCAN_GATED); 0 for an op that needs none,
+ * -1 on invalid arguments. */
+int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N);
+
+/* Return and clear the first device-side error recorded in the context's
+ * status block (SN_OK if none).  Synchronous: call it after the stream that
+ * ran the work has been synchronised. */
+sn_status sn_ctx_last_error(SnCtx* ctx);
+
+/* Set / read a context option (SN_OPT_*).  SN_E_INVAL for an unknown key or
+ * out-of-range value; SN_OPT_LOOKBACK_CHUNK is read-only. */
+sn_status sn_ctx_set_option(SnCtx* ctx, int32_t key, int32_t value);
+sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value);
+
+/* ---------------------------------------------------------------- tier 1 */
+
+/* FMA-form scan, per channel n of each batch row b, for t = 0..T-1:
+ *     s_t = a_t * s_{t-1} + b_t,      s_{-1} = s0          ([P1] §2.1)
+ * evaluated in fp32 with one fused multiply-add per step.
+ *   a, b   : (B, T, N) inputs;      s_out  : (B, T, N) all states, may be NULL
+ *   s0     : (B, N), NULL = zeros;  s_final: (B, N) state after t = T-1, may be NULL
+ * The sequential kernel (the default whenever it fills the GPU) gives the
+ * same bits as the single-precision definition at every t, so splitting a
+ * sequence into segments and carrying s_final -> s0 reproduces the full run
+ * bit for bit ([P1] §4).  The chunked look-back kernel (chosen for few
+ * channels and long T, or forced by SN_OPT_SCAN_KERNEL) is deterministic and
+ * bit-exact under splits at multiples of SN_OPT_LOOKBACK_CHUNK.
+ * Pointers need 4-byte alignment; N % 4 == 0 with 16-byte aligned a, b and
+ * s_out enables the TMA path.  Errors: SN_E_INVAL, SN_E_NOMEM (look-back
+ * forced without enough workspace), SN_E_DEVICE. */
+sn_status sn_scan_fma(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
+                      const float* a, const float* b, const float* s0,
+                      float* s_final, float* s_out, void* stream);
+
+/* Gated-form scan ([P1] §2.1):
+ *     s_t = a_t * s_{t-1} + (1 - a_t) * u_t
+ * evaluated in fp32 as s = fma(a_t, s, (1 - a_t) * u_t) with the injection
+ * rounded after each of its two operations.  Arguments as sn_scan_fma with
+ * u in place of b. */
+sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
+                        const float* a, const float* u, const float* s0,
+                        float* s_final, float* s_out, void* stream);
+
+/* ---------------------------------------------------------------- tier 2 */
+
+/* Diagonal-decay matrix recurrence per (batch b, head h):
+ *     S_t = diag(d_t) S_{t-1} + k_t v_t^T,     o_t = scale * S_t^T q_t
+ * ([P1] §4.3 GLA with per-key decay; [P1] §4.1 / [P2] §3 Mamba-2 with one
+ * scalar decay dA = exp(dt*A) per head, B_g and C_g shared by a group of
+ * heads, dt folded into v by the caller).  Decays are linear (not log).
+ *   q, k : (B, T, G, dk)   head h reads group h / (H / G)
+ *   v, o : (B, T, H, dv)   o may be NULL
+ *   d    : (B, T, H, dk) for SN_DECAY_PER_KEY, (B, T, H) for SN_DECAY_PER_HEAD
+ *   S_in, S_out : (B, H, dk, dv), row = key index, column = value index;
+ *          S_in NULL = zeros; S_out may be NULL or equal S_in.
+ * Requires H % G == 0, dk in {64, 128}, dv in {64, 128} and 16-byte aligned
+ * pointers (else SN_E_UNSUPPORTED / SN_E_INVAL).  Deterministic; the result
+ * depends only on the inputs, so segment splits are bit-exact. */
+sn_status sn_recur_diag(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G,
+                        int32_t dk, int32_t dv, int32_t decay_kind, float scale,
+                        const float* q, const float* k, const float* v,
+                        const float* d, const float* S_in, float* S_out,
+                        float* o, void* stream);
+
+/* DeltaNet delta rule per (b, h) ([P1] §4.2, [P2] §3):
+ *     delta_t = (v_t - S_{t-1}^T k_t) * beta_t
+ *     S_t     = S_{t-1} + k_t delta_t^T,       o_t = scale * S_t^T q_t
+ *   q, k : (B, T, H, dk);  v, o : (B, T, H, dv);  beta : (B, T, H)
+ *   S_in, S_out : (B, H, dk, dv) as in sn_recur_diag.
+ * Requirements and guarantees as sn_recur_diag. */
+sn_status sn_recur_delta(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
+                         int32_t dk, int32_t dv, float scale,
+                         const float* q, const float* k, const float* v,
+                         const float* beta, const float* S_in, float* S_out,
+                         float* o, void* stream);
+
+/* RWKV-7 matrix state with rank-1 removal per (b, h) ([P1] §5.1):
+ *     S_t = S_{t-1} (.) w_t - (S_{t-1} k_t) k_t^T + v_t k_t^T,   o_t = S_t q_t
+ * with w_t scaling key column j of every row and the removal formed from the
+ * state before decay.
+ *   q, k, w : (B, T, H, dk);  v, o : (B, T, H, dv)
+ *   S_in, S_out : (B, H, dv, dk), row = value index, column = key index.
+ * T == 1 runs the batched single-step decode kernel (state-bandwidth bound,
+ * in place when S_in == S_out).  Requirements as sn_recur_diag. */
+sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
+                         int32_t dk, int32_t dv,
+                         const float* q, const float* k, const float* v,
+                         const float* w, const float* S_in, float* S_out,
+                         float* o, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SN_ABI_H */

@@ -1,0 +1,356 @@
+// abi.cu -- host side of the C ABI: version/caps/status, contexts, argument
+// validation, kernel selection and error surfacing.  No arithmetic of the
+// recurrences happens here; every step runs in the kernels.
+//
+// ABI style after "SunnyNet 工程化实录：一个 O(N) 架构如何长出自己的 C 推理运行时"
+// §6 (stable C ABI: sn_ prefix, opaque handles, packed version, capability
+// bits, int32 status codes and dimensions).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "sn_internal.h"
+
+using namespace sn;
+
+namespace {
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;   // sanity bound on one tensor (4 TB)
+constexpr int kDefaultWaitUs = 1000000;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool overlaps(const void* p, int64_t pbytes, const void* q, int64_t qbytes) {
+    if (p == nullptr || q == nullptr || pbytes <= 0 || qbytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + (uintptr_t)pbytes;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + (uintptr_t)qbytes;
+    return a0 < b1 && b0 < a1;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Buf {
+    const void* p;
+    int64_t bytes;
+    bool out;
+};
+
+// Outputs may not overlap any other buffer, except the declared in-place pair.
+bool any_bad_overlap(const Buf* bufs, int n, const void* inplace_in, const void* inplace_out) {
+    for (int i = 0; i < n; ++i) {
+        if (!bufs[i].out || bufs[i].p == nullptr) continue;
+        for (int j = 0; j < n; ++j) {
+            if (j == i || bufs[j].p == nullptr) continue;
+            if (bufs[j].out && j < i) continue;   // each output pair checked once
+            const bool pair_ok = (bufs[i].p == inplace_out && bufs[j].p == inplace_in && bufs[i].p == bufs[j].p &&
+                                  bufs[i].bytes == bufs[j].bytes);
+            if (!pair_ok && overlaps(bufs[i].p, bufs[i].bytes, bufs[j].p, bufs[j].bytes)) return true;
+        }
+    }
+    return false;
+}
+
+sn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SN_OK : SN_E_DEVICE; }
+
+// Make the context's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+uint64_t wait_ns(const SnCtx* c) { return (uint64_t)c->wait_limit_us * 1000ull; }
+
+}  // namespace
+
+namespace sn {
+bool encode_tiled(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box) {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base),
+                          reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                          reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+bool lookback_supported(const ScanArgs& x);
+}  // namespace sn
+
+extern "C" {
+
+uint32_t sn_abi_version(void) { return SN_ABI_VERSION; }
+
+sn_status sn_abi_check(int32_t major) { return major == SN_ABI_VERSION_MAJOR ? SN_OK : SN_E_UNSUPPORTED; }
+
+uint32_t sn_abi_caps(void) {
+    return SN_CAP_SCAN_FMA | SN_CAP_SCAN_GATED | SN_CAP_RECUR_DIAG | SN_CAP_RECUR_DELTA | SN_CAP_RECUR_RWKV7 |
+           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK;
+}
+
+const char* sn_status_str(sn_status s) {
+    switch (s) {
+        case SN_OK: return "ok";
+        case SN_E_INVAL: return "invalid argument";
+        case SN_E_NOMEM: return "workspace missing or too small";
+        case SN_E_IO: return "i/o error";
+        case SN_E_FORMAT: return "format error";
+        case SN_E_UNSUPPORTED: return "unsupported (version, shape or device)";
+        case SN_E_DEVICE: return "CUDA runtime error";
+        case SN_E_TIMEOUT: return "bounded device-side wait ran out";
+        default: return "unknown status";
+    }
+}
+
+sn_status sn_ctx_create(int32_t device, SnCtx** out_ctx) {
+    if (out_ctx == nullptr) return SN_E_INVAL;
+    *out_ctx = nullptr;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return SN_E_DEVICE;
+    if (device < 0 || device >= ndev) return SN_E_INVAL;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return SN_E_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return SN_E_UNSUPPORTED;
+    DeviceGuard g(device);
+    if (!g.ok) return SN_E_DEVICE;
+    SnCtx* c = new SnCtx();
+    std::memset(c, 0, sizeof(SnCtx));
+    c->device = device;
+    c->sm_count = prop.multiProcessorCount;
+    c->cc_major = prop.major;
+    c->cc_minor = prop.minor;
+    c->wait_limit_us = kDefaultWaitUs;
+    c->epoch = 0;
+    c->ws_dirty = true;
+    if (cudaMalloc(&c->dstatus, sizeof(SnDevStatus)) != cudaSuccess) {
+        delete c;
+        return SN_E_DEVICE;
+    }
+    if (cudaMemset(c->dstatus, 0, sizeof(SnDevStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(c->dstatus);
+        delete c;
+        return SN_E_DEVICE;
+    }
+    *out_ctx = c;
+    return SN_OK;
+}
+
+void sn_ctx_free(SnCtx* ctx) {
+    if (ctx == nullptr) return;
+    DeviceGuard g(ctx->device);
+    cudaFree(ctx->dstatus);
+    delete ctx;
+}
+
+sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes) {
+    if (ctx == nullptr || bytes < 0) return SN_E_INVAL;
+    if (dev_ptr == nullptr || bytes == 0) {
+        ctx->ws = nullptr;
+        ctx->ws_bytes = 0;
+        return SN_OK;
+    }
+    if (!aligned(dev_ptr, 256)) return SN_E_INVAL;
+    ctx->ws = dev_ptr;
+    ctx->ws_bytes = bytes;
+    ctx->ws_dirty = true;
+    return SN_OK;
+}
+
+int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N) {
+    if ((op != SN_OP_SCAN_FMA && op != SN_OP_SCAN_GATED) || B <= 0 || T <= 0 || N <= 0) return -1;
+    return lookback_ws_bytes(B, T, N);
+}
+
+sn_status sn_ctx_last_error(SnCtx* ctx) {
+    if (ctx == nullptr) return SN_E_INVAL;
+    DeviceGuard g(ctx->device);
+    int err = 0;
+    if (cudaMemcpy(&err, &ctx->dstatus->error, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SN_E_DEVICE;
+    if (err != 0) {
+        const int zero[2] = {0, 0};
+        if (cudaMemcpy(ctx->dstatus, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SN_E_DEVICE;
+    }
+    return err;
+}
+
+sn_status sn_ctx_set_option(SnCtx* ctx, int32_t key, int32_t value) {
+    if (ctx == nullptr) return SN_E_INVAL;
+    switch (key) {
+        case SN_OPT_SCAN_KERNEL:
+            if (value < SN_SCAN_KERNEL_AUTO || value > SN_SCAN_KERNEL_LOOKBACK) return SN_E_INVAL;
+            ctx->scan_kernel = value;
+            return SN_OK;
+        case SN_OPT_WAIT_LIMIT_US:
+            if (value < 1) return SN_E_INVAL;
+            ctx->wait_limit_us = value;
+            return SN_OK;
+        case SN_OPT_DEBUG_POISON:
+            if (value != 0 && value != 1) return SN_E_INVAL;
+            ctx->debug_poison = value;
+            return SN_OK;
+        case SN_OPT_RECUR_KERNEL:
+            if (value != 0 && value != 1) return SN_E_INVAL;
+            ctx->recur_kernel = value;
+            return SN_OK;
+        default: return SN_E_INVAL;
+    }
+}
+
+sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value) {
+    if (ctx == nullptr || value == nullptr) return SN_E_INVAL;
+    switch (key) {
+        case SN_OPT_SCAN_KERNEL: *value = ctx->scan_kernel; return SN_OK;
+        case SN_OPT_WAIT_LIMIT_US: *value = ctx->wait_limit_us; return SN_OK;
+        case SN_OPT_DEBUG_POISON: *value = ctx->debug_poison; return SN_OK;
+        case SN_OPT_LOOKBACK_CHUNK: *value = LB_TC; return SN_OK;
+        case SN_OPT_RECUR_KERNEL: *value = ctx->recur_kernel; return SN_OK;
+        default: return SN_E_INVAL;
+    }
+}
+
+// ------------------------------------------------------------------ scans
+static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* b,
+                             const float* s0, float* s_final, float* s_out, void* stream, bool gated) {
+    if (ctx == nullptr || a == nullptr || b == nullptr) return SN_E_INVAL;
+    if (B <= 0 || T <= 0 || N <= 0) return SN_E_INVAL;
+    const int64_t elems = (int64_t)B * T * N;
+    if (elems > kMaxElems) return SN_E_INVAL;
+    const void* ptrs[5] = {a, b, s0, s_final, s_out};
+    for (const void* p : ptrs)
+        if (p != nullptr && !aligned(p, 4)) return SN_E_INVAL;
+    const int64_t big = elems * 4, small = (int64_t)B * N * 4;
+    const Buf bufs[5] = {{a, big, false}, {b, big, false}, {s0, small, false}, {s_final, small, true},
+                         {s_out, big, true}};
+    // s0 and s_final may be the same buffer (in-place continuation)
+    if (any_bad_overlap(bufs, 5, s0, s_final)) return SN_E_INVAL;
+
+    ScanArgs x{B, T, N, a, b, s0, s_final, s_out};
+    int kernel = ctx->scan_kernel;
+    const int64_t need = lookback_ws_bytes(B, T, N);
+    if (kernel == SN_SCAN_KERNEL_LOOKBACK) {
+        if (!lookback_supported(x)) return SN_E_UNSUPPORTED;
+        if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
+    } else if (kernel == SN_SCAN_KERNEL_AUTO) {
+        // The sequential kernel keeps the exact per-step bits and is HBM-bound
+        // once there are enough channels; chunking along T pays only when the
+        // channel count leaves most SMs idle and T is long.
+        const int64_t seq_ctas = (int64_t)B * ((N + 63) / 64);
+        const bool few = seq_ctas < 2 * ctx->sm_count;
+        kernel = (few && T >= 8 * LB_TC && lookback_supported(x) && ctx->ws != nullptr && ctx->ws_bytes >= need)
+                     ? SN_SCAN_KERNEL_LOOKBACK
+                     : SN_SCAN_KERNEL_SEQUENTIAL;
+    }
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SN_E_DEVICE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kernel == SN_SCAN_KERNEL_LOOKBACK) {
+        const int64_t nflags = lookback_flag_count(B, T, N);
+        if (ctx->ws_dirty || ctx->epoch >= (1u << 29) || nflags != ctx->lb_last_flags) {
+            // fresh flag area: zero it once, on the caller's stream
+            if (cudaMemsetAsync(ctx->ws, 0, (size_t)nflags * 4, s) != cudaSuccess ||
+                cudaMemsetAsync(&ctx->dstatus->abort_tag, 0, sizeof(unsigned int), s) != cudaSuccess)
+                return SN_E_DEVICE;
+            ctx->ws_dirty = false;
+            ctx->epoch = 0;
+            ctx->lb_last_flags = nflags;
+        }
+        ctx->epoch += 1;
+        return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->epoch, ctx->debug_poison, ctx->dstatus,
+                                              wait_ns(ctx), ctx->sm_count, s));
+    }
+    return from_cuda(launch_scan_sequential(x, gated, ctx->dstatus, wait_ns(ctx), s));
+}
+
+sn_status sn_scan_fma(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* b,
+                      const float* s0, float* s_final, float* s_out, void* stream) {
+    return scan_common(ctx, B, T, N, a, b, s0, s_final, s_out, stream, false);
+}
+
+sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* u,
+                        const float* s0, float* s_final, float* s_out, void* stream) {
+    return scan_common(ctx, B, T, N, a, u, s0, s_final, s_out, stream, true);
+}
+
+// ------------------------------------------------------------------ matrix recurrences
+static bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
+    if (ctx == nullptr || x.q == nullptr || x.k == nullptr || x.v == nullptr || x.g == nullptr) return SN_E_INVAL;
+    if (x.B <= 0 || x.T <= 0 || x.H <= 0 || x.G <= 0 || x.dk <= 0 || x.dv <= 0) return SN_E_INVAL;
+    if (x.H % x.G != 0) return SN_E_INVAL;
+    if (!head_dim_ok(x.dk) || !head_dim_ok(x.dv)) return SN_E_UNSUPPORTED;
+    const int64_t rows = (int64_t)x.B * x.T;
+    if (rows * x.H * x.dk > kMaxElems || rows * x.H * x.dv > kMaxElems) return SN_E_INVAL;
+    const void* ptrs[7] = {x.q, x.k, x.v, x.g, x.S_in, x.S_out, x.o};
+    for (const void* p : ptrs)
+        if (p != nullptr && !aligned(p, 16)) return SN_E_INVAL;
+    const int64_t qk = rows * x.G * x.dk * 4, vo = rows * x.H * x.dv * 4;
+    const int64_t gb = (x.kind == RK_DIAG_KEY || x.kind == RK_RWKV7) ? rows * x.H * x.dk * 4 : rows * x.H * 4;
+    const int64_t sb = (int64_t)x.B * x.H * x.dk * x.dv * 4;
+    const Buf bufs[7] = {{x.q, qk, false},   {x.k, qk, false},     {x.v, vo, false}, {x.g, gb, false},
+                         {x.S_in, sb, false}, {x.S_out, sb, true}, {x.o, vo, true}};
+    if (any_bad_overlap(bufs, 7, x.S_in, x.S_out)) return SN_E_INVAL;
+
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SN_E_DEVICE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (x.T == 1 && ctx->recur_kernel == 0 && recur_decode_supported(x))
+        return from_cuda(launch_recur_decode(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+    return from_cuda(launch_recur_sequence(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+}
+
+sn_status sn_recur_diag(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G, int32_t dk, int32_t dv,
+                        int32_t decay_kind, float scale, const float* q, const float* k, const float* v,
+                        const float* d, const float* S_in, float* S_out, float* o, void* stream) {
+    if (decay_kind != SN_DECAY_PER_KEY && decay_kind != SN_DECAY_PER_HEAD) return SN_E_INVAL;
+    RecurArgs x{};
+    x.kind = decay_kind == SN_DECAY_PER_KEY ? RK_DIAG_KEY : RK_DIAG_HEAD;
+    x.B = B; x.T = T; x.H = H; x.G = G; x.dk = dk; x.dv = dv; x.scale = scale;
+    x.q = q; x.k = k; x.v = v; x.g = d; x.S_in = S_in; x.S_out = S_out; x.o = o;
+    x.state_transposed = false;
+    return recur_common(ctx, x, stream);
+}
+
+sn_status sn_recur_delta(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, float scale,
+                         const float* q, const float* k, const float* v, const float* beta, const float* S_in,
+                         float* S_out, float* o, void* stream) {
+    RecurArgs x{};
+    x.kind = RK_DELTA;
+    x.B = B; x.T = T; x.H = H; x.G = H; x.dk = dk; x.dv = dv; x.scale = scale;
+    x.q = q; x.k = k; x.v = v; x.g = beta; x.S_in = S_in; x.S_out = S_out; x.o = o;
+    x.state_transposed = false;
+    return recur_common(ctx, x, stream);
+}
+
+sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const float* q,
+                         const float* k, const float* v, const float* w, const float* S_in, float* S_out,
+                         float* o, void* stream) {
+    RecurArgs x{};
+    x.kind = RK_RWKV7;
+    x.B = B; x.T = T; x.H = H; x.G = H; x.dk = dk; x.dv = dv; x.scale = 1.0f;
+    x.q = q; x.k = k; x.v = v; x.g = w; x.S_in = S_in; x.S_out = S_out; x.o = o;
+    x.state_transposed = true;
+    return recur_common(ctx, x, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// sn_internal.h -- definitions shared by the host ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sn_abi.h"
+
+// Per-context device status block (256 bytes, zeroed at creation).
+struct SnDevStatus {
+    int error;   // first device-side error of any launch (SN_E_*), 0 = none
+    int site;    // where it happened: (kernel id << 16) | wait site
+    unsigned int abort_tag;   // tag of a look-back launch in which a tile gave up waiting
+    int pad[61];
+};
+static_assert(sizeof(SnDevStatus) == 256, "status block is 256 bytes");
+
+// Kernel ids used in SnDevStatus::site.
+enum SnKernelId : int {
+    SN_K_SCAN_SEQ = 1,
+    SN_K_SCAN_LOOKBACK = 2,
+    SN_K_RECUR_SEQ = 3,
+    SN_K_RECUR_DECODE = 4,
+};
+
+struct SnCtx {
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    SnDevStatus* dstatus;       // device status block (owned)
+    // caller-owned workspace for the chunked look-back scan
+    void* ws;
+    int64_t ws_bytes;
+    bool ws_dirty;              // flag area must be cleared before next use
+    uint32_t epoch;             // look-back epoch, incremented per launch
+    int64_t lb_last_flags;      // flag count of the last look-back launch
+    // options
+    int scan_kernel;
+    int wait_limit_us;
+    int debug_poison;
+    int recur_kernel;
+};
+
+namespace sn {
+
+// Layout of the chunked look-back scan (shared with the host for workspace
+// sizing): NC channels x TC time steps per tile.
+constexpr int LB_NC = 32;
+constexpr int LB_TC = 256;
+
+// Returns the workspace bytes of the look-back scan for (B, T, N).
+int64_t lookback_ws_bytes(int B, int T, int N);
+int64_t lookback_flag_count(int B, int T, int N);
+
+// tensor-map encoder (driver entry point fetched through the runtime)
+bool encode_tiled(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box);
+
+struct ScanArgs {
+    int B, T, N;
+    const float* a;
+    const float* b;   // b (FMA form) or u (gated form)
+    const float* s0;
+    float* s_final;
+    float* s_out;
+};
+
+// Launchers (return a CUDA error code; validation happens before).
+cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
+                                   cudaStream_t stream);
+cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32_t epoch, int poison,
+                                 SnDevStatus* st, uint64_t wait_ns, int sm_count, cudaStream_t stream);
+
+enum RecurKind : int { RK_DIAG_KEY = 0, RK_DIAG_HEAD = 1, RK_DELTA = 2, RK_RWKV7 = 3 };
+
+struct RecurArgs {
+    int kind;
+    int B, T, H, G, dk, dv;
+    float scale;
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* g;     // decay d (per key or per head), beta (delta) or w (rwkv7)
+    const float* S_in;
+    float* S_out;
+    float* o;
+    bool state_transposed;   // S stored (dv, dk) (RWKV-7) instead of (dk, dv)
+};
+
+cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                  cudaStream_t stream);
+cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                cudaStream_t stream);
+bool recur_decode_supported(const RecurArgs& x);
+
+}  // namespace sn

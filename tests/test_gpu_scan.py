@@ -1,0 +1,284 @@
+"""GPU parity of the tier-1 scans (through the C ABI) against the CPU oracle.
+
+Bar ("SunnyNet 工程化实录" §2.1 forms, §4 segment continuation):
+* the sequential kernel equals the single-precision definition bit for bit
+  (fp32 oracle with one fused multiply-add per step) and is split-invariant;
+* every kernel is within 1e-5 normwise of the fp64 oracle;
+* the look-back kernel is deterministic and bit-exact under splits at
+  multiples of its chunk length.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def sr():
+    import scan_runtime_gb300 as sr
+    sr.build()
+    return sr
+
+
+@pytest.fixture()
+def ctx(sr):
+    c = sr.Context(0)
+    yield c
+    assert c.last_error() == sr.SN_OK
+    c.close()
+
+
+def _nrel(x, r):
+    x = np.asarray(x, np.float64)
+    return float(np.max(np.abs(x - r)) / max(float(np.max(np.abs(r))), 1e-30))
+
+
+def _inputs(B, T, N, seed, large=True):
+    x = synth.scan_inputs(B, T, N, large=large, cid=50 + seed)
+    s0 = synth.normal((B, N), 9000 + seed)
+    return x["a"], x["b"], x["u"], s0
+
+
+def _run(ctx, form, a, rhs, s0, **kw):
+    fn = ctx.scan_fma if form == "fma" else ctx.scan_gated
+    so, sf = fn(a.cuda(), rhs.cuda(), None if s0 is None else s0.cuda(), **kw)
+    torch.cuda.synchronize()
+    return (None if so is None else so.cpu().numpy()), (None if sf is None else sf.cpu().numpy())
+
+
+def _ref(form, a, rhs, s0, prec):
+    fn = oracle.scan_fma if form == "fma" else oracle.scan_gated
+    if s0 is not None:
+        s0 = s0.numpy() if prec == "f32" else s0.numpy().astype(np.float64)
+    return fn(a.numpy(), rhs.numpy(), s0, prec=prec)
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+@pytest.mark.parametrize("shape", [(2, 128, 128), (3, 77, 100), (1, 1, 64), (2, 2, 8), (1, 300, 4),
+                                   (2, 65, 130), (1, 33, 7), (4, 40, 1)])
+def test_sequential_bit_exact_and_within_tolerance(ctx, form, shape):
+    B, T, N = shape
+    a, b, u, s0 = _inputs(B, T, N, hash(shape) % 97)
+    rhs = b if form == "fma" else u
+    so, sf = _run(ctx, form, a, rhs, s0)
+    r32, f32 = _ref(form, a, rhs, s0, "f32")
+    r64, f64 = _ref(form, a, rhs, s0, "f64")
+    assert np.array_equal(so.view(np.uint32), r32.view(np.uint32))
+    assert np.array_equal(sf.view(np.uint32), f32.view(np.uint32))
+    assert _nrel(so, r64) <= TOL and _nrel(sf, f64) <= TOL
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+def test_small_workload_config(ctx, form):
+    """B=2 T=128 N=128, a = sigmoid(N(0,1)), s0 = 0 (the pages' parity size)."""
+    x = synth.config_inputs("scan_small")
+    rhs = x["b"] if form == "fma" else x["u"]
+    so, sf = _run(ctx, form, x["a"], rhs, None)
+    r32, _ = _ref(form, x["a"], rhs, None, "f32")
+    r64, f64 = _ref(form, x["a"], rhs, None, "f64")
+    assert np.array_equal(so, r32)
+    assert _nrel(so, r64) <= TOL and _nrel(sf, f64) <= TOL
+
+
+def test_unaligned_views_take_the_plain_load_path(ctx):
+    B, T, N = 2, 50, 64
+    a, b, _, s0 = _inputs(B, T, N, 3)
+    big_a = torch.zeros(B * T * N + 1)
+    big_b = torch.zeros(B * T * N + 1)
+    big_a[1:] = a.reshape(-1)
+    big_b[1:] = b.reshape(-1)
+    ga, gb = big_a.cuda()[1:].view(B, T, N), big_b.cuda()[1:].view(B, T, N)
+    so, sf = ctx.scan_fma(ga, gb, s0.cuda())
+    r32, f32 = _ref("fma", a, b, s0, "f32")
+    assert np.array_equal(so.cpu().numpy(), r32) and np.array_equal(sf.cpu().numpy(), f32)
+
+
+def test_optional_outputs_and_in_place_state(ctx):
+    B, T, N = 2, 70, 64
+    a, b, _, s0 = _inputs(B, T, N, 4)
+    _, f32 = _ref("fma", a, b, s0, "f32")
+    so, sf = _run(ctx, "fma", a, b, s0, s_out=None)
+    assert so is None and np.array_equal(sf, f32)
+    st = s0.cuda().clone()
+    ctx.scan_fma(a.cuda(), b.cuda(), st, s_out=None, s_final=st)
+    torch.cuda.synchronize()
+    assert np.array_equal(st.cpu().numpy(), f32)
+    so, sf = _run(ctx, "fma", a, b, s0, s_final=None)
+    assert sf is None
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+@pytest.mark.parametrize("split", [1, 77, 150])
+def test_sequential_segment_split_bit_exact(ctx, form, split):
+    B, T, N = 2, 300, 192
+    a, b, u, s0 = _inputs(B, T, N, 5)
+    rhs = b if form == "fma" else u
+    full, ffull = _run(ctx, form, a, rhs, s0)
+    p1, f1 = _run(ctx, form, a[:, :split].contiguous(), rhs[:, :split].contiguous(), s0)
+    p2, f2 = _run(ctx, form, a[:, split:].contiguous(), rhs[:, split:].contiguous(), torch.from_numpy(f1))
+    assert np.array_equal(np.concatenate([p1, p2], 1), full) and np.array_equal(f2, ffull)
+
+
+# ------------------------------------------------------------------ look-back kernel
+@pytest.fixture()
+def lbctx(sr, ctx):
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+    return ctx
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+@pytest.mark.parametrize("shape", [(1, 4096, 32), (2, 1000, 64), (3, 257, 96), (1, 256, 32), (2, 5, 8),
+                                   (1, 70000, 64)])
+def test_lookback_within_tolerance(lbctx, form, shape):
+    B, T, N = shape
+    lbctx.ensure_workspace(B, T, N)
+    a, b, u, s0 = _inputs(B, T, N, 6 + T % 13)
+    rhs = b if form == "fma" else u
+    so, sf = _run(lbctx, form, a, rhs, s0)
+    r64, f64 = _ref(form, a, rhs, s0, "f64")
+    assert _nrel(so, r64) <= TOL and _nrel(sf, f64) <= TOL
+    assert np.array_equal(so[:, -1], sf)
+
+
+def test_lookback_deterministic(lbctx):
+    B, T, N = 1, 20000, 64
+    lbctx.ensure_workspace(B, T, N)
+    a, b, _, s0 = _inputs(B, T, N, 7)
+    r1 = _run(lbctx, "fma", a, b, s0)
+    r2 = _run(lbctx, "fma", a, b, s0)
+    assert np.array_equal(r1[0], r2[0]) and np.array_equal(r1[1], r2[1])
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+def test_lookback_split_at_chunk_multiple_bit_exact(sr, lbctx, form):
+    tc = lbctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK)
+    B, T, N = 2, 20 * tc + 17, 64
+    split = 12 * tc
+    lbctx.ensure_workspace(B, T, N)
+    a, b, u, s0 = _inputs(B, T, N, 8)
+    rhs = b if form == "fma" else u
+    full, ffull = _run(lbctx, form, a, rhs, s0)
+    p1, f1 = _run(lbctx, form, a[:, :split].contiguous(), rhs[:, :split].contiguous(), s0)
+    p2, f2 = _run(lbctx, form, a[:, split:].contiguous(), rhs[:, split:].contiguous(), torch.from_numpy(f1))
+    assert np.array_equal(np.concatenate([p1, p2], 1), full) and np.array_equal(f2, ffull)
+
+
+def test_lookback_bounded_wait_reports_timeout(sr, lbctx):
+    """A flag that no chunk publishes: every wait runs out after the limit, the
+    kernel returns normally and the context reports SN_E_TIMEOUT once."""
+    B, T, N = 1, 4 * 256, 32
+    lbctx.ensure_workspace(B, T, N)
+    lbctx.set_option(sr.SN_OPT_WAIT_LIMIT_US, 2000)
+    lbctx.set_option(sr.SN_OPT_DEBUG_POISON, 1)
+    a, b, _, s0 = _inputs(B, T, N, 9)
+    _run(lbctx, "fma", a, b, s0)
+    assert lbctx.last_error() == sr.SN_E_TIMEOUT
+    assert lbctx.last_error() == sr.SN_OK             # cleared
+    lbctx.set_option(sr.SN_OPT_DEBUG_POISON, 0)
+    so, sf = _run(lbctx, "fma", a, b, s0)              # context still usable
+    r64, f64 = _ref("fma", a, b, s0, "f64")
+    assert _nrel(so, r64) <= TOL
+
+
+def test_lookback_forced_without_workspace_is_nomem(sr, ctx):
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+    a = torch.zeros(1, 512, 32, device="cuda")
+    out = torch.full_like(a, 7.0)
+    s = sr.sn_scan_fma(ctx.handle, 1, 512, 32, a, a, None, None, out)
+    assert s == sr.SN_E_NOMEM
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())                     # untouched
+
+
+# ------------------------------------------------------------------ validation
+def test_invalid_arguments_leave_outputs_untouched(sr, ctx):
+    h = ctx.handle
+    a = torch.randn(2, 16, 64, device="cuda")
+    out = torch.full_like(a, 3.0)
+    fin = torch.full((2, 64), 3.0, device="cuda")
+    E = sr.SN_E_INVAL
+    assert sr.sn_scan_fma(h, 0, 16, 64, a, a, None, fin, out) == E
+    assert sr.sn_scan_fma(h, 2, -1, 64, a, a, None, fin, out) == E
+    assert sr.sn_scan_fma(h, 2, 16, 64, None, a, None, fin, out) == E
+    assert sr.sn_scan_fma(h, 2, 16, 64, a, a, None, fin, a) == E            # output aliases input
+    assert sr.sn_scan_fma(h, 2, 16, 64, a, a, None, out, out) == E          # two outputs overlap
+    assert sr.sn_scan_fma(h, 2, 16, 64, a.data_ptr() + 2, a, None, fin, out) == E   # misaligned
+    assert sr.sn_scan_gated(h, 1 << 20, 1 << 20, 1 << 20, a, a, None, fin, out) == E  # element-count bound
+    torch.cuda.synchronize()
+    assert bool((out == 3.0).all()) and bool((fin == 3.0).all())
+
+
+def test_options(sr, ctx):
+    assert ctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK) == 256
+    assert sr.sn_ctx_set_option(ctx.handle, sr.SN_OPT_LOOKBACK_CHUNK, 5) == sr.SN_E_INVAL
+    assert sr.sn_ctx_set_option(ctx.handle, sr.SN_OPT_SCAN_KERNEL, 9) == sr.SN_E_INVAL
+    assert sr.sn_ctx_set_option(ctx.handle, 12345, 0) == sr.SN_E_INVAL
+    ctx.set_option(sr.SN_OPT_WAIT_LIMIT_US, 500000)
+    assert ctx.get_option(sr.SN_OPT_WAIT_LIMIT_US) == 500000
+
+
+# ------------------------------------------------------------------ full-size workload
+@pytest.fixture(scope="module")
+def large_inputs():
+    return synth.config_inputs("scan_large")
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+def test_full_size_sequential_sampled_and_split(ctx, large_inputs, form):
+    """B=8 T=8192 N=2048 in the launch configuration the benchmark times;
+    sampled channels against the oracle and the 3000 + 5192 split."""
+    x = large_inputs
+    rhs = x["b"] if form == "fma" else x["u"]
+    B, T, N = x["a"].shape
+    ga, gr, gs0 = x["a"].cuda(), rhs.cuda(), x["s0"].cuda()
+    fn = ctx.scan_fma if form == "fma" else ctx.scan_gated
+    so, sf = fn(ga, gr, gs0)
+    rng = np.random.default_rng(11)
+    chans = [(int(rng.integers(B)), int(rng.integers(N))) for _ in range(24)] + [(0, 0), (B - 1, N - 1)]
+    so_s = {c: so[c[0], :, c[1]].cpu().numpy() for c in chans}
+    sf_h = sf.cpu().numpy()
+    for c in chans:
+        ac = np.ascontiguousarray(x["a"][c[0], :, c[1]].numpy()[None, :, None])
+        rc = np.ascontiguousarray(rhs[c[0], :, c[1]].numpy()[None, :, None])
+        s = x["s0"][c[0], c[1]].numpy().reshape(1, 1)
+        f = oracle.scan_fma if form == "fma" else oracle.scan_gated
+        r32, f32 = f(ac, rc, s, prec="f32")
+        r64, _ = f(ac, rc, s.astype(np.float64))
+        assert np.array_equal(so_s[c], r32[0, :, 0]) and sf_h[c] == f32[0, 0]
+        assert _nrel(so_s[c], r64[0, :, 0]) <= TOL
+    # split 3000 + 5192, state carried, equals the full run bit for bit
+    p1, f1 = fn(ga[:, :3000].contiguous(), gr[:, :3000].contiguous(), gs0)
+    p2, f2 = fn(ga[:, 3000:].contiguous(), gr[:, 3000:].contiguous(), f1)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([p1, p2], 1), so) and torch.equal(f2, sf)
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+def test_full_size_lookback_sampled_and_split(sr, ctx, large_inputs, form):
+    x = large_inputs
+    rhs = x["b"] if form == "fma" else x["u"]
+    B, T, N = x["a"].shape
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+    ctx.ensure_workspace(B, T, N)
+    ga, gr, gs0 = x["a"].cuda(), rhs.cuda(), x["s0"].cuda()
+    fn = ctx.scan_fma if form == "fma" else ctx.scan_gated
+    so, sf = fn(ga, gr, gs0)
+    rng = np.random.default_rng(12)
+    for _ in range(12):
+        bi, n = int(rng.integers(B)), int(rng.integers(N))
+        ac = np.ascontiguousarray(x["a"][bi, :, n].numpy()[None, :, None])
+        rc = np.ascontiguousarray(rhs[bi, :, n].numpy()[None, :, None])
+        s = x["s0"][bi, n].numpy().reshape(1, 1).astype(np.float64)
+        r64, f64 = (oracle.scan_fma if form == "fma" else oracle.scan_gated)(ac, rc, s)
+        assert _nrel(so[bi, :, n].cpu().numpy(), r64[0, :, 0]) <= TOL
+    split = 3072                                        # a multiple of the chunk length
+    p1, f1 = fn(ga[:, :split].contiguous(), gr[:, :split].contiguous(), gs0)
+    p2, f2 = fn(ga[:, split:].contiguous(), gr[:, split:].contiguous(), f1)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([p1, p2], 1), so) and torch.equal(f2, sf)
