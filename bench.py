@@ -451,6 +451,72 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ---------------------------------------------------------------- profiling cases
+PROFILE_CASES = {
+    # name: (description, workload builder)
+    "scan_seq": "sequential scan (FMA), B=8 T=2048 N=2048 (402 MB moved, > L2)",
+    "scan_lookback": "look-back scan (FMA), B=8 T=2048 N=2048",
+    "gla": "diag per-key, full GLA workload B=4 T=4096 H=4 dk=dv=128",
+    "mamba2": "diag per-head, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
+    "deltanet": "delta rule, full DeltaNet workload B=4 T=4096 H=8 dk=dv=128",
+    "rwkv7_prefill": "RWKV-7 sequence kernel, full prefill workload B=16 T=4096 H=12 64x64",
+    "rwkv7_decode": "RWKV-7 decode kernel, full decode workload B=1024 T=1 H=12 64x64",
+}
+
+
+def run_profile_case(args):
+    """Run one kernel `--steps` times after `--warmup` on its profiling case and
+    print its median time; used as the command under ncu."""
+    import torch
+
+    import scan_runtime_gb300 as sr
+    sr.build()
+    dev = torch.device("cuda:0")
+    ctx = sr.Context(0)
+    s = torch.cuda.Stream(dev)
+    name = args.profile_case
+    h = ctx.handle
+    if name.startswith("scan"):
+        B, T, N = 8, 2048, 2048
+        x = synth.scan_inputs(B, T, N, large=True, device=dev)
+        so = torch.empty((B, T, N), device=dev)
+        sf = torch.empty((B, N), device=dev)
+        if name == "scan_lookback":
+            ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+            ctx.ensure_workspace(B, T, N)
+        else:
+            ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_SEQUENTIAL)
+        fn = lambda: sr.sn_scan_fma(h, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
+        nbytes = scan_bytes(B, T, N)
+    else:
+        c = synth.CONFIGS[name]
+        x = synth.config_inputs(name, device=dev)
+        Bc, Tc, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+        o = torch.empty((Bc, Tc, H, dv), device=dev)
+        if name in ("gla", "mamba2"):
+            S = torch.empty((Bc, H, dk, dv), device=dev)
+            fn = lambda: sr.sn_recur_diag(h, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"], x["scale"], x["q"], x["k"],
+                                          x["v"], x["d"], None, S, o, s)
+        elif name == "deltanet":
+            S = torch.empty((Bc, H, dk, dv), device=dev)
+            fn = lambda: sr.sn_recur_delta(h, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"], x["v"], x["beta"],
+                                           None, S, o, s)
+        else:
+            S = torch.empty((Bc, H, dv, dk), device=dev)
+            fn = lambda: sr.sn_recur_rwkv7(h, Bc, Tc, H, dk, dv, x["q"], x["k"], x["v"], x["w"], x["S0"], S, o, s)
+        nbytes = matrix_cost(name)[1]
+    torch.cuda.synchronize()
+    def call():
+        st = fn()
+        if st != sr.SN_OK:
+            raise RuntimeError(f"{name}: {sr.sn_status_str(st)}")
+
+    ms = time_form(torch, call, args.warmup, args.steps, s)
+    assert ctx.last_error() == sr.SN_OK
+    print(json.dumps({"profile_case": name, "what": PROFILE_CASES[name], "median_ms": round(ms, 4),
+                      "GBps": round(nbytes / ms / 1e6, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -460,10 +526,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-forms", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run only this kernel on its profiling case (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -24,8 +24,9 @@
 // only on the inputs and segment splits are bit-exact.
 //
 // Decode kernel (RWKV-7, T == 1): four (batch, head) states per CTA move as
-// 16 KB bulk copies into shared memory, one thread per state row updates and
-// reads out, and the new states leave as bulk copies (in place allowed).
+// 16 KB bulk copies into shared memory, four lanes per state row update and
+// read out with the sequence kernel's arithmetic, and the new states leave as
+// bulk copies (in place allowed).
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -73,8 +74,76 @@ struct SeqParams {
 };
 
 __device__ __forceinline__ float group_sum(float x, int lpc) {
-    for (int o = lpc >> 1; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    for (int o = lpc >> 1; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
     return x;
+}
+
+// One time step of one state column held by a lane group of LPC lanes; each
+// lane owns rows (m * LPC + sub) * 4 + c of the column (m < R4, c < 4).
+// kr, gr, qr point at the step's k, per-key gate and q rows in shared memory;
+// vj is the column's value, gsc the per-head scalar (dA or beta).  Returns the
+// unscaled readout sum over the column (identical on all lanes of the group).
+// Every operation is an explicit round-to-nearest intrinsic, so any kernel
+// that calls this with the same lane layout produces the same bits.
+template <int KIND, int R4, int LPC>
+__device__ __forceinline__ float col_step(float (&P)[4 * R4], const float* kr, const float* gr,
+                                          const float* qr, float vj, float gsc, int sub, bool want_o) {
+    float kv[4 * R4];
+#pragma unroll
+    for (int m = 0; m < R4; ++m) {
+        const float4 x = *reinterpret_cast<const float4*>(kr + (m * LPC + sub) * 4);
+        kv[4 * m] = x.x; kv[4 * m + 1] = x.y; kv[4 * m + 2] = x.z; kv[4 * m + 3] = x.w;
+    }
+    if constexpr (KIND == RK_DIAG_KEY) {
+#pragma unroll
+        for (int m = 0; m < R4; ++m) {
+            const float4 d = *reinterpret_cast<const float4*>(gr + (m * LPC + sub) * 4);
+            P[4 * m] = __fmaf_rn(d.x, P[4 * m], __fmul_rn(kv[4 * m], vj));
+            P[4 * m + 1] = __fmaf_rn(d.y, P[4 * m + 1], __fmul_rn(kv[4 * m + 1], vj));
+            P[4 * m + 2] = __fmaf_rn(d.z, P[4 * m + 2], __fmul_rn(kv[4 * m + 2], vj));
+            P[4 * m + 3] = __fmaf_rn(d.w, P[4 * m + 3], __fmul_rn(kv[4 * m + 3], vj));
+        }
+    } else if constexpr (KIND == RK_DIAG_HEAD) {
+#pragma unroll
+        for (int r = 0; r < 4 * R4; ++r) P[r] = __fmaf_rn(gsc, P[r], __fmul_rn(kv[r], vj));
+    } else {
+        // u = column . k: four partial chains, then the lane group
+        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+        for (int m = 0; m < R4; ++m) {
+            u0 = __fmaf_rn(P[4 * m], kv[4 * m], u0);
+            u1 = __fmaf_rn(P[4 * m + 1], kv[4 * m + 1], u1);
+            u2 = __fmaf_rn(P[4 * m + 2], kv[4 * m + 2], u2);
+            u3 = __fmaf_rn(P[4 * m + 3], kv[4 * m + 3], u3);
+        }
+        const float u = group_sum(__fadd_rn(__fadd_rn(u0, u1), __fadd_rn(u2, u3)), LPC);
+        if constexpr (KIND == RK_DELTA) {
+            const float delta = __fmul_rn(__fsub_rn(vj, u), gsc);
+#pragma unroll
+            for (int r = 0; r < 4 * R4; ++r) P[r] = __fmaf_rn(kv[r], delta, P[r]);
+        } else {
+            const float delta = __fsub_rn(vj, u);
+#pragma unroll
+            for (int m = 0; m < R4; ++m) {
+                const float4 w = *reinterpret_cast<const float4*>(gr + (m * LPC + sub) * 4);
+                P[4 * m] = __fmaf_rn(kv[4 * m], delta, __fmul_rn(P[4 * m], w.x));
+                P[4 * m + 1] = __fmaf_rn(kv[4 * m + 1], delta, __fmul_rn(P[4 * m + 1], w.y));
+                P[4 * m + 2] = __fmaf_rn(kv[4 * m + 2], delta, __fmul_rn(P[4 * m + 2], w.z));
+                P[4 * m + 3] = __fmaf_rn(kv[4 * m + 3], delta, __fmul_rn(P[4 * m + 3], w.w));
+            }
+        }
+    }
+    if (!want_o) return 0.f;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int m = 0; m < R4; ++m) {
+        const float4 x = *reinterpret_cast<const float4*>(qr + (m * LPC + sub) * 4);
+        a0 = __fmaf_rn(P[4 * m], x.x, a0);
+        a1 = __fmaf_rn(P[4 * m + 1], x.y, a1);
+        a2 = __fmaf_rn(P[4 * m + 2], x.z, a2);
+        a3 = __fmaf_rn(P[4 * m + 3], x.w, a3);
+    }
+    return group_sum(__fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)), LPC);
 }
 
 template <int KIND, int DK, int LPC, int W>
@@ -176,75 +245,25 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         float* os = reinterpret_cast<float*>(smem + L::o_off + (kk % RS_OBUF) * L::o_bytes);
         const int tn = min(RS_TS, T - kk * RS_TS);
 
-        auto step = [&](int i) {
-            const float vj = vs[i * JT + jl];
-            float kv[R];
-#pragma unroll
-            for (int m = 0; m < R4; ++m) {
-                const float4 x = *reinterpret_cast<const float4*>(ks + i * DK + (m * LPC + sub) * 4);
-                kv[4 * m] = x.x; kv[4 * m + 1] = x.y; kv[4 * m + 2] = x.z; kv[4 * m + 3] = x.w;
-            }
-            if constexpr (KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD) {
-                if constexpr (KIND == RK_DIAG_KEY) {
-#pragma unroll
-                    for (int m = 0; m < R4; ++m) {
-                        const float4 d = *reinterpret_cast<const float4*>(gs + i * DK + (m * LPC + sub) * 4);
-                        P[4 * m] = __fmaf_rn(d.x, P[4 * m], __fmul_rn(kv[4 * m], vj));
-                        P[4 * m + 1] = __fmaf_rn(d.y, P[4 * m + 1], __fmul_rn(kv[4 * m + 1], vj));
-                        P[4 * m + 2] = __fmaf_rn(d.z, P[4 * m + 2], __fmul_rn(kv[4 * m + 2], vj));
-                        P[4 * m + 3] = __fmaf_rn(d.w, P[4 * m + 3], __fmul_rn(kv[4 * m + 3], vj));
-                    }
-                } else {
-                    const float dA = gs[i];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) P[r] = __fmaf_rn(dA, P[r], __fmul_rn(kv[r], vj));
-                }
-            } else {
-                // u = P^T k over this column: 4 partial sums, then the lane group
-                float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
-#pragma unroll
-                for (int m = 0; m < R4; ++m) {
-                    u0 = __fmaf_rn(P[4 * m], kv[4 * m], u0);
-                    u1 = __fmaf_rn(P[4 * m + 1], kv[4 * m + 1], u1);
-                    u2 = __fmaf_rn(P[4 * m + 2], kv[4 * m + 2], u2);
-                    u3 = __fmaf_rn(P[4 * m + 3], kv[4 * m + 3], u3);
-                }
-                const float u = group_sum((u0 + u1) + (u2 + u3), LPC);
-                if constexpr (KIND == RK_DELTA) {
-                    const float delta = __fmul_rn(vj - u, gs[i]);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) P[r] = __fmaf_rn(kv[r], delta, P[r]);
-                } else {
-                    const float delta = vj - u;
-#pragma unroll
-                    for (int m = 0; m < R4; ++m) {
-                        const float4 w = *reinterpret_cast<const float4*>(gs + i * DK + (m * LPC + sub) * 4);
-                        P[4 * m] = __fmaf_rn(kv[4 * m], delta, __fmul_rn(P[4 * m], w.x));
-                        P[4 * m + 1] = __fmaf_rn(kv[4 * m + 1], delta, __fmul_rn(P[4 * m + 1], w.y));
-                        P[4 * m + 2] = __fmaf_rn(kv[4 * m + 2], delta, __fmul_rn(P[4 * m + 2], w.z));
-                        P[4 * m + 3] = __fmaf_rn(kv[4 * m + 3], delta, __fmul_rn(P[4 * m + 3], w.w));
-                    }
-                }
-            }
-            if (p.has_o) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-                for (int m = 0; m < R4; ++m) {
-                    const float4 x = *reinterpret_cast<const float4*>(qs + i * DK + (m * LPC + sub) * 4);
-                    a0 = __fmaf_rn(P[4 * m], x.x, a0);
-                    a1 = __fmaf_rn(P[4 * m + 1], x.y, a1);
-                    a2 = __fmaf_rn(P[4 * m + 2], x.z, a2);
-                    a3 = __fmaf_rn(P[4 * m + 3], x.w, a3);
-                }
-                const float acc = group_sum((a0 + a1) + (a2 + a3), LPC);
-                if (sub == 0) os[i * JT + jl] = __fmul_rn(acc, p.scale);
-            }
-        };
+        const bool want_o = p.has_o != 0;
         if (tn == RS_TS) {
+            // readouts collect in registers and reach shared memory after the
+            // steps, so no store sits between one step's loads and the next
+            float ov[RS_TS];
 #pragma unroll
-            for (int i = 0; i < RS_TS; ++i) step(i);
+            for (int i = 0; i < RS_TS; ++i)
+                ov[i] = col_step<KIND, R4, LPC>(P, ks + i * DK, gs + i * DK, qs + i * DK, vs[i * JT + jl],
+                                                scalar_gate<KIND>() ? gs[i] : 0.f, sub, want_o);
+            if (want_o && sub == 0) {
+#pragma unroll
+                for (int i = 0; i < RS_TS; ++i) os[i * JT + jl] = __fmul_rn(ov[i], p.scale);
+            }
         } else {
-            for (int i = 0; i < tn; ++i) step(i);
+            for (int i = 0; i < tn; ++i) {
+                const float acc = col_step<KIND, R4, LPC>(P, ks + i * DK, gs + i * DK, qs + i * DK, vs[i * JT + jl],
+                                                          scalar_gate<KIND>() ? gs[i] : 0.f, sub, want_o);
+                if (want_o && sub == 0) os[i * JT + jl] = __fmul_rn(acc, p.scale);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -313,9 +332,18 @@ cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaS
     return cudaGetLastError();
 }
 
+// Two CTA widths per head dim: 4 consumer warps, or 2 when the (batch, head,
+// column tile) count would leave SMs idle.
 template <int KIND>
-cudaError_t dispatch_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaStream_t stream) {
-    if (x.dk == 128) return run_seq<KIND, 128, 8, 4>(x, st, wait_ns, stream);
+cudaError_t dispatch_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                         cudaStream_t stream) {
+    if (x.dk == 128) {
+        const int64_t ctas = (int64_t)x.B * x.H * (x.dv / 16);
+        if (ctas < 2 * sm_count) return run_seq<KIND, 128, 8, 2>(x, st, wait_ns, stream);
+        return run_seq<KIND, 128, 8, 4>(x, st, wait_ns, stream);
+    }
+    const int64_t ctas = (int64_t)x.B * x.H * (x.dv / 32);
+    if (ctas < 2 * sm_count) return run_seq<KIND, 64, 4, 2>(x, st, wait_ns, stream);
     return run_seq<KIND, 64, 4, 4>(x, st, wait_ns, stream);
 }
 
@@ -327,8 +355,9 @@ constexpr uint32_t DEC_V_BYTES = DEC_D * 4;
 // per tile: S (16 KB) then q, k, w, v rows (256 B each)
 constexpr uint32_t DEC_TILE_BYTES = DEC_S_BYTES + 4 * DEC_V_BYTES;
 constexpr size_t DEC_SMEM = DEC_TILES * DEC_TILE_BYTES + 8 + 128;
+constexpr int DEC_THREADS = DEC_D * 4;       // 4 lanes per state row
 
-__global__ void __launch_bounds__(DEC_TILES * DEC_D, 3)
+__global__ void __launch_bounds__(DEC_THREADS, 3)
 recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict__ k,
                    const float* __restrict__ v, const float* __restrict__ w, const float* S_in, float* S_out,
                    float* __restrict__ o, SnDevStatus* st, uint64_t wait_ns) {
@@ -365,50 +394,27 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
         }
         return;
     }
-    const int t = tid / DEC_D, i = tid % DEC_D;       // tile, state row (value index)
-    if (t < ntile) {
+    // Same lane layout and arithmetic as the sequence kernel for dk = 64
+    // (4 lanes per state row, 16 keys each, col_step), so one decode step and
+    // a one-step sequence call give identical bits.
+    const int i = tid >> 2, sub = tid & 3;            // state row (value index), lane in group
+    for (int t = 0; t < ntile; ++t) {
         float* S = reinterpret_cast<float*>(smem + t * DEC_TILE_BYTES);
         const float* qv = reinterpret_cast<const float*>(smem + t * DEC_TILE_BYTES + DEC_S_BYTES);
         const float* kv = qv + DEC_D;
         const float* wv = kv + DEC_D;
         const float* vv = wv + DEC_D;
-        float* row = S + i * DEC_D;
-        if (S_in == nullptr) {
+        float4* row = reinterpret_cast<float4*>(S + i * DEC_D);
+        float P[16];
 #pragma unroll
-            for (int c = 0; c < DEC_D / 4; ++c) reinterpret_cast<float4*>(row)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m < 4; ++m) {
+            const float4 x = (S_in != nullptr) ? row[m * 4 + sub] : make_float4(0.f, 0.f, 0.f, 0.f);
+            P[4 * m] = x.x; P[4 * m + 1] = x.y; P[4 * m + 2] = x.z; P[4 * m + 3] = x.w;
         }
-        // rotate the float4 chunk order by the row so 8 consecutive rows hit 8 distinct bank groups
-        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+        const float acc = col_step<RK_RWKV7, 4, 4>(P, kv, wv, qv, vv[i], 0.f, sub, o != nullptr);
 #pragma unroll
-        for (int c = 0; c < DEC_D / 4; ++c) {
-            const int cc = (c + i) & (DEC_D / 4 - 1);
-            const float4 s4 = reinterpret_cast<const float4*>(row)[cc];
-            const float4 k4 = reinterpret_cast<const float4*>(kv)[cc];
-            u0 = __fmaf_rn(s4.x, k4.x, u0);
-            u1 = __fmaf_rn(s4.y, k4.y, u1);
-            u2 = __fmaf_rn(s4.z, k4.z, u2);
-            u3 = __fmaf_rn(s4.w, k4.w, u3);
-        }
-        const float delta = vv[i] - ((u0 + u1) + (u2 + u3));
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < DEC_D / 4; ++c) {
-            const int cc = (c + i) & (DEC_D / 4 - 1);
-            float4 s4 = reinterpret_cast<const float4*>(row)[cc];
-            const float4 k4 = reinterpret_cast<const float4*>(kv)[cc];
-            const float4 w4 = reinterpret_cast<const float4*>(wv)[cc];
-            const float4 q4 = reinterpret_cast<const float4*>(qv)[cc];
-            s4.x = __fmaf_rn(k4.x, delta, __fmul_rn(s4.x, w4.x));
-            s4.y = __fmaf_rn(k4.y, delta, __fmul_rn(s4.y, w4.y));
-            s4.z = __fmaf_rn(k4.z, delta, __fmul_rn(s4.z, w4.z));
-            s4.w = __fmaf_rn(k4.w, delta, __fmul_rn(s4.w, w4.w));
-            reinterpret_cast<float4*>(row)[cc] = s4;
-            a0 = __fmaf_rn(s4.x, q4.x, a0);
-            a1 = __fmaf_rn(s4.y, q4.y, a1);
-            a2 = __fmaf_rn(s4.z, q4.z, a2);
-            a3 = __fmaf_rn(s4.w, q4.w, a3);
-        }
-        if (o != nullptr) o[(size_t)(tile0 + t) * DEC_D + i] = (a0 + a1) + (a2 + a3);
+        for (int m = 0; m < 4; ++m) row[m * 4 + sub] = make_float4(P[4 * m], P[4 * m + 1], P[4 * m + 2], P[4 * m + 3]);
+        if (o != nullptr && sub == 0) o[(size_t)(tile0 + t) * DEC_D + i] = __fmul_rn(acc, 1.0f);
     }
     if (S_out == nullptr) return;
     fence_proxy_async_smem();
@@ -425,12 +431,11 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
 
 cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                   cudaStream_t stream) {
-    (void)sm_count;
     switch (x.kind) {
-        case RK_DIAG_KEY: return dispatch_seq<RK_DIAG_KEY>(x, st, wait_ns, stream);
-        case RK_DIAG_HEAD: return dispatch_seq<RK_DIAG_HEAD>(x, st, wait_ns, stream);
-        case RK_DELTA: return dispatch_seq<RK_DELTA>(x, st, wait_ns, stream);
-        case RK_RWKV7: return dispatch_seq<RK_RWKV7>(x, st, wait_ns, stream);
+        case RK_DIAG_KEY: return dispatch_seq<RK_DIAG_KEY>(x, st, wait_ns, sm_count, stream);
+        case RK_DIAG_HEAD: return dispatch_seq<RK_DIAG_HEAD>(x, st, wait_ns, sm_count, stream);
+        case RK_DELTA: return dispatch_seq<RK_DELTA>(x, st, wait_ns, sm_count, stream);
+        case RK_RWKV7: return dispatch_seq<RK_RWKV7>(x, st, wait_ns, sm_count, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -451,7 +456,7 @@ cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wa
     }
     const int BH = x.B * x.H;
     const int grid = (BH + DEC_TILES - 1) / DEC_TILES;
-    recur_decode_rwkv7<<<grid, DEC_TILES * DEC_D, DEC_SMEM, stream>>>(BH, x.q, x.k, x.v, x.g, x.S_in, x.S_out,
+    recur_decode_rwkv7<<<grid, DEC_THREADS, DEC_SMEM, stream>>>(BH, x.q, x.k, x.v, x.g, x.S_in, x.S_out,
                                                                       x.o, st, wait_ns);
     return cudaGetLastError();
 }

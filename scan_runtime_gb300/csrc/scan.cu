@@ -13,13 +13,15 @@
 //    The LDG variant serves layouts TMA cannot describe (N % 4 != 0 or
 //    unaligned base pointers).
 //  * scan_lookback -- chunked associative scan over (A, B) pairs for few
-//    channels and long T.  Each tile is 32 channels x 256 steps: per-thread
-//    folds over 8 steps, a warp-shuffle Kogge-Stone scan over the warp's 4
+//    channels and long T.  Each tile is 32 channels x 128 steps: per-thread
+//    folds over 4 steps, a warp-shuffle Kogge-Stone scan over the warp's 4
 //    segments, a fixed-order fold across warps, and a decoupled look-back
 //    across T chunks.  Carries are defined by the forward fold
 //    C_k = fma(A_k, C_{k-1}, B_k), applied one chunk at a time whatever the
 //    timing, so the result is deterministic and bit-exact under splits at
-//    multiples of 256 steps.
+//    multiples of 128 steps.  Four tiles per CTA are in flight through a TMA
+//    ring; the persistent grid is launched cooperatively so every CTA a tile
+//    waits on is resident.
 #include <algorithm>
 #include <cstdio>
 
@@ -193,11 +195,12 @@ scan_seq_ldg(int T, int N, const float* __restrict__ a, const float* __restrict_
 // ============================================================ look-back
 namespace {
 constexpr int LB_THREADS = 256;                   // 8 warps
-constexpr int LB_SEG = LB_TC / 32;                // 8 steps per thread segment
+constexpr int LB_SEG = LB_TC / 32;                // steps per thread segment
 constexpr uint32_t LB_TILE = LB_TC * LB_NC;       // floats per tensor per tile
 constexpr uint32_t LB_TILE_BYTES = 2 * LB_TILE * 4;
 constexpr uint32_t LB_AGG = 1u, LB_INCL = 2u;
-constexpr size_t LB_SMEM = 2 * LB_TILE_BYTES + 2 * 8 + 16;
+constexpr int LB_STAGES = 4;                      // tiles in flight per CTA
+constexpr size_t LB_SMEM = LB_STAGES * LB_TILE_BYTES + LB_STAGES * 8 + 16;
 
 __device__ __forceinline__ float4 f4mul(float4 x, float4 y) {
     return make_float4(__fmul_rn(x.x, y.x), __fmul_rn(x.y, y.y), __fmul_rn(x.z, y.z), __fmul_rn(x.w, y.w));
@@ -248,17 +251,16 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
               const LookbackParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float* bufs = reinterpret_cast<float*>(smem);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * LB_TILE_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + LB_STAGES * LB_TILE_BYTES);
     __shared__ float4 wA[8][8], wB[8][8];          // per-warp aggregates [warp][quad]
     __shared__ float carry[LB_NC], cfin[LB_NC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane & 7, sub = lane >> 3;
-    const int seg = warp * 4 + sub;                 // 0..31, rows [seg*8, seg*8+8)
+    const int seg = warp * 4 + sub;                 // 0..31, rows [seg*LB_SEG, (seg+1)*LB_SEG)
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        for (int s = 0; s < LB_STAGES; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -279,30 +281,38 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     };
 
     int it = 0;
-    if (tid == 0 && (int)blockIdx.x < p.ntiles) issue(blockIdx.x, 0);
+    if (tid == 0) {
+        for (int s = 0; s < LB_STAGES - 1; ++s) {
+            const int ti = blockIdx.x + s * gridDim.x;
+            if (ti < p.ntiles) issue(ti, s);
+        }
+    }
     for (int ti = blockIdx.x; ti < p.ntiles; ti += gridDim.x, ++it) {
-        const int buf = it & 1;
-        if (tid == 0 && ti + (int)gridDim.x < p.ntiles) issue(ti + gridDim.x, buf ^ 1);
+        const int buf = it % LB_STAGES;
+        // refill the slot the previous iteration released
+        const int ahead = ti + (LB_STAGES - 1) * (int)gridDim.x;
+        if (tid == 0 && ahead < p.ntiles) issue(ahead, (it + LB_STAGES - 1) % LB_STAGES);
         int k, bi, cb;
         tile_coords(ti, k, bi, cb);
         const int t0 = k * LB_TC;
         const int n0 = cb * LB_NC;
         const int rows = min(LB_TC, p.T - t0);      // valid rows of this chunk
 
-        if (!__syncthreads_and(mbar_wait(&full[buf], (it >> 1) & 1, p.wait_ns))) {
+        if (!__syncthreads_and(mbar_wait(&full[buf], (it / LB_STAGES) & 1, p.wait_ns))) {
             // A copy never landed: report, wait (bounded) for this CTA's copies
             // still in flight, and retire the CTA.
             if (tid == 0) {
                 record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | 1);
-                (void)mbar_wait(&full[buf], (it >> 1) & 1, p.wait_ns);
-                if (ti + (int)gridDim.x < p.ntiles) (void)mbar_wait(&full[buf ^ 1], ((it + 1) >> 1) & 1, p.wait_ns);
+                for (int j = 0; j < LB_STAGES; ++j)
+                    if (ti + j * (int)gridDim.x < p.ntiles)
+                        (void)mbar_wait(&full[(it + j) % LB_STAGES], ((it + j) / LB_STAGES) & 1, p.wait_ns);
             }
             return;
         }
         const float* sa = bufs + buf * 2 * LB_TILE;
         const float* sb = sa + LB_TILE;
 
-        // ---- phase 1: fold this thread's 8 steps of its 4 channels
+        // ---- phase 1: fold this thread's LB_SEG steps of its 4 channels
         float4 A = make_float4(1.f, 1.f, 1.f, 1.f), Bc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < LB_SEG; ++i) {

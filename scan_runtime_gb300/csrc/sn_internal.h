@@ -47,7 +47,7 @@ namespace sn {
 // Layout of the chunked look-back scan (shared with the host for workspace
 // sizing): NC channels x TC time steps per tile.
 constexpr int LB_NC = 32;
-constexpr int LB_TC = 256;
+constexpr int LB_TC = 128;
 
 // Returns the workspace bytes of the look-back scan for (B, T, N).
 int64_t lookback_ws_bytes(int B, int T, int N);

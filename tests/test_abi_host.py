@@ -121,7 +121,7 @@ def test_ctx_create_without_gpu_fails_cleanly(abi):
 
 def test_workspace_bytes(abi):
     nb = abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 8, 8192, 2048)
-    tiles = 8 * (2048 // 32) * (8192 // 256)
+    tiles = 8 * (2048 // 32) * (8192 // 128)
     assert nb == ((tiles * 4 + 255) // 256) * 256 + tiles * 3 * 32 * 4
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_GATED, 1, 1, 1) > 0
     assert abi.sn_workspace_bytes(99, 1, 1, 1) == -1

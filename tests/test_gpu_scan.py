@@ -172,7 +172,7 @@ def test_lookback_split_at_chunk_multiple_bit_exact(sr, lbctx, form):
 def test_lookback_bounded_wait_reports_timeout(sr, lbctx):
     """A flag that no chunk publishes: every wait runs out after the limit, the
     kernel returns normally and the context reports SN_E_TIMEOUT once."""
-    B, T, N = 1, 4 * 256, 32
+    B, T, N = 1, 4 * 128, 32
     lbctx.ensure_workspace(B, T, N)
     lbctx.set_option(sr.SN_OPT_WAIT_LIMIT_US, 2000)
     lbctx.set_option(sr.SN_OPT_DEBUG_POISON, 1)
@@ -215,7 +215,7 @@ def test_invalid_arguments_leave_outputs_untouched(sr, ctx):
 
 
 def test_options(sr, ctx):
-    assert ctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK) == 256
+    assert ctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK) == 128
     assert sr.sn_ctx_set_option(ctx.handle, sr.SN_OPT_LOOKBACK_CHUNK, 5) == sr.SN_E_INVAL
     assert sr.sn_ctx_set_option(ctx.handle, sr.SN_OPT_SCAN_KERNEL, 9) == sr.SN_E_INVAL
     assert sr.sn_ctx_set_option(ctx.handle, 12345, 0) == sr.SN_E_INVAL
@@ -277,7 +277,7 @@ def test_full_size_lookback_sampled_and_split(sr, ctx, large_inputs, form):
         s = x["s0"][bi, n].numpy().reshape(1, 1).astype(np.float64)
         r64, f64 = (oracle.scan_fma if form == "fma" else oracle.scan_gated)(ac, rc, s)
         assert _nrel(so[bi, :, n].cpu().numpy(), r64[0, :, 0]) <= TOL
-    split = 3072                                        # a multiple of the chunk length
+    split = 3072                                        # a multiple of the 128-step chunk length
     p1, f1 = fn(ga[:, :split].contiguous(), gr[:, :split].contiguous(), gs0)
     p2, f2 = fn(ga[:, split:].contiguous(), gr[:, split:].contiguous(), f1)
     torch.cuda.synchronize()
