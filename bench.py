@@ -85,6 +85,24 @@ def traffic_record(kernel):
     return None
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(ms, device="cpu"):
+    """Largest per-rank time; the identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(step_bytes, steps, world, ms_total):
+    """Whole-job throughput: every rank moves `step_bytes` per step (weak
+    scaling), timed by the slowest rank."""
+    return world * steps * step_bytes / (ms_total / 1e3) / GB
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -347,14 +365,10 @@ def run_ours(args):
         torch.distributed.barrier()
     time.sleep(0.1)
     clk.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), dev)
     launch_ms = [e[0].elapsed_time(e[1]) for e in evs] + [e[1].elapsed_time(e[2]) for e in evs]
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
-    value = world * args.steps * step_bytes / (ms_total / 1e3) / GB
+    value = whole_job_gbps(step_bytes, args.steps, world, ms_total)
     achieved = per_form_bytes / (avg_launch_ms / 1e3) / GB
 
     # end to end through the public API: pinned host inputs in, s_t out, every step
@@ -455,6 +469,7 @@ def run_ours(args):
 PROFILE_CASES = {
     # name: (description, workload builder)
     "scan_seq": "sequential scan (FMA), B=8 T=2048 N=2048 (402 MB moved, > L2)",
+    "scan_seq_full": "sequential scan (FMA), full workload B=8 T=8192 N=2048 (1.61 GB moved)",
     "scan_lookback": "look-back scan (FMA), B=8 T=2048 N=2048",
     "gla": "diag per-key, full GLA workload B=4 T=4096 H=4 dk=dv=128",
     "mamba2": "diag per-head, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
@@ -477,7 +492,7 @@ def run_profile_case(args):
     name = args.profile_case
     h = ctx.handle
     if name.startswith("scan"):
-        B, T, N = 8, 2048, 2048
+        B, T, N = (8, 8192, 2048) if name.endswith("_full") else (8, 2048, 2048)
         x = synth.scan_inputs(B, T, N, large=True, device=dev)
         so = torch.empty((B, T, N), device=dev)
         sf = torch.empty((B, N), device=dev)

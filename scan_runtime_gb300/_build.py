@@ -15,8 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsn.so")
-SOURCES = ["abi.cu", "scan.cu", "recur.cu"]
-HEADERS = ["sn_internal.h", "ptx.cuh"]
+SOURCES = ["abi.cu", "scan.cu", "scan_lookback.cu", "recur.cu"]
+HEADERS = ["sn_internal.h", "ptx.cuh", "scan_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

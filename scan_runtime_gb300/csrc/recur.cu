@@ -269,7 +269,8 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         if (lane == 0) mbar_arrive(&empty[slot]);
         if (p.has_o) {
             fence_proxy_async_smem();
-            if (threadIdx.x == 0) bulk_wait_read_all();   // conservative: the store of 2 stages ago is done
+            // the store two stages back read the buffer the next stage writes
+            if (threadIdx.x == 0) bulk_wait_read_allbut1();
             named_bar_sync(1, W * 32);
             if (threadIdx.x == 0) {
                 tma_store_4d(&map_o, os, jt0, h, kk * RS_TS, b);
