@@ -95,6 +95,8 @@ typedef int32_t sn_status;
 #define SN_OPT_DEBUG_POISON     3  /* 1: look-back waits for a flag no chunk publishes (tests the bound) */
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
 #define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
+#define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA;
+                                      a width the value dimension does not divide fails with SN_E_DEVICE */
 
 #define SN_SCAN_KERNEL_AUTO       0
 #define SN_SCAN_KERNEL_SEQUENTIAL 1

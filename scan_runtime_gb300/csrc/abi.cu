@@ -212,6 +212,10 @@ sn_status sn_ctx_set_option(SnCtx* ctx, int32_t key, int32_t value) {
             if (value != 0 && value != 1) return SN_E_INVAL;
             ctx->recur_kernel = value;
             return SN_OK;
+        case SN_OPT_RECUR_TILE:
+            if (value != 0 && value != 2 && value != 4 && value != 8) return SN_E_INVAL;
+            ctx->recur_tile = value;
+            return SN_OK;
         default: return SN_E_INVAL;
     }
 }
@@ -224,6 +228,7 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value) {
         case SN_OPT_DEBUG_POISON: *value = ctx->debug_poison; return SN_OK;
         case SN_OPT_LOOKBACK_CHUNK: *value = LB_TC; return SN_OK;
         case SN_OPT_RECUR_KERNEL: *value = ctx->recur_kernel; return SN_OK;
+        case SN_OPT_RECUR_TILE: *value = ctx->recur_tile; return SN_OK;
         default: return SN_E_INVAL;
     }
 }
@@ -316,7 +321,7 @@ static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (x.T == 1 && ctx->recur_kernel == 0 && recur_decode_supported(x))
         return from_cuda(launch_recur_decode(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
-    return from_cuda(launch_recur_sequence(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+    return from_cuda(launch_recur_sequence(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, ctx->recur_tile, s));
 }
 
 sn_status sn_recur_diag(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G, int32_t dk, int32_t dv,

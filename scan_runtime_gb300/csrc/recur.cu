@@ -81,8 +81,10 @@ __device__ __forceinline__ float group_sum(float x, int lpc) {
 // One time step of one state column held by a lane group of LPC lanes; each
 // lane owns rows (m * LPC + sub) * 4 + c of the column (m < R4, c < 4).
 // kr, gr, qr point at the step's k, per-key gate and q rows in shared memory;
-// vj is the column's value, gsc the per-head scalar (dA or beta).  Returns the
-// unscaled readout sum over the column (identical on all lanes of the group).
+// vj is the column's value, gsc the per-head scalar (dA or beta).  Returns this
+// lane's partial of the unscaled readout; the caller reduces the partials over
+// the lane group (group_sum per step, or reduce_scatter per stage -- both use
+// the same addition tree, so the bits do not depend on which).
 // Every operation is an explicit round-to-nearest intrinsic, so any kernel
 // that calls this with the same lane layout produces the same bits.
 template <int KIND, int R4, int LPC>
@@ -143,7 +145,29 @@ __device__ __forceinline__ float col_step(float (&P)[4 * R4], const float* kr, c
         a2 = __fmaf_rn(P[4 * m + 2], x.z, a2);
         a3 = __fmaf_rn(P[4 * m + 3], x.w, a3);
     }
-    return group_sum(__fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)), LPC);
+    return __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
+}
+
+// Sum NV per-lane values over a group of LPC lanes by recursive halving: at
+// offset o a lane keeps the half of its values that its bit o selects and adds
+// its partner's copy of that half.  Afterwards v[e] (e < NV/LPC) holds the group
+// sum of value index sub * (NV/LPC) + e.  The pairing (offsets LPC/2 .. 1) is
+// the one group_sum uses, and addition is commutative, so every sum has the
+// bits group_sum would give it.
+template <int LPC, int NV>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int sub) {
+#pragma unroll
+    for (int lvl = 0; (LPC >> (lvl + 1)) >= 1; ++lvl) {
+        const int o = LPC >> (lvl + 1);
+        const int c = NV >> lvl;
+        const bool upper = (sub & o) != 0;
+#pragma unroll
+        for (int i = 0; i < c / 2; ++i) {
+            const float send = upper ? v[i] : v[i + c / 2];
+            const float keep = upper ? v[i + c / 2] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
 }
 
 template <int KIND, int DK, int LPC, int W>
@@ -247,22 +271,29 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
 
         const bool want_o = p.has_o != 0;
         if (tn == RS_TS) {
-            // readouts collect in registers and reach shared memory after the
-            // steps, so no store sits between one step's loads and the next
+            // Readout partials stay in registers for the whole stage and are
+            // reduced once over the lane group, so no shuffle chain or store
+            // sits between one step and the next.
             float ov[RS_TS];
 #pragma unroll
             for (int i = 0; i < RS_TS; ++i)
                 ov[i] = col_step<KIND, R4, LPC>(P, ks + i * DK, gs + i * DK, qs + i * DK, vs[i * JT + jl],
                                                 scalar_gate<KIND>() ? gs[i] : 0.f, sub, want_o);
-            if (want_o && sub == 0) {
+            if (want_o) {
+                reduce_scatter<LPC, RS_TS>(ov, sub);
+                constexpr int PER = RS_TS / LPC;
 #pragma unroll
-                for (int i = 0; i < RS_TS; ++i) os[i * JT + jl] = __fmul_rn(ov[i], p.scale);
+                for (int e = 0; e < PER; ++e) os[(sub * PER + e) * JT + jl] = __fmul_rn(ov[e], p.scale);
             }
         } else {
             for (int i = 0; i < tn; ++i) {
-                const float acc = col_step<KIND, R4, LPC>(P, ks + i * DK, gs + i * DK, qs + i * DK, vs[i * JT + jl],
-                                                          scalar_gate<KIND>() ? gs[i] : 0.f, sub, want_o);
-                if (want_o && sub == 0) os[i * JT + jl] = __fmul_rn(acc, p.scale);
+                const float part = col_step<KIND, R4, LPC>(P, ks + i * DK, gs + i * DK, qs + i * DK,
+                                                           vs[i * JT + jl], scalar_gate<KIND>() ? gs[i] : 0.f, sub,
+                                                           want_o);
+                if (want_o) {
+                    const float acc = group_sum(part, LPC);
+                    if (sub == 0) os[i * JT + jl] = __fmul_rn(acc, p.scale);
+                }
             }
         }
         __syncwarp();
@@ -333,19 +364,46 @@ cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaS
     return cudaGetLastError();
 }
 
-// Two CTA widths per head dim: 4 consumer warps, or 2 when the (batch, head,
-// column tile) count would leave SMs idle.
-template <int KIND>
-cudaError_t dispatch_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
-                         cudaStream_t stream) {
-    if (x.dk == 128) {
-        const int64_t ctas = (int64_t)x.B * x.H * (x.dv / 16);
-        if (ctas < 2 * sm_count) return run_seq<KIND, 128, 8, 2>(x, st, wait_ns, stream);
-        return run_seq<KIND, 128, 8, 4>(x, st, wait_ns, stream);
+// Lanes per column: the diagonal-decay kinds have no reduction on the
+// recurrence path, so they spread a column over more lanes (8 rows each) for
+// more warps per SM; delta and RWKV-7 keep 16 rows per lane to shorten the
+// per-step dot product that feeds the next state.  The CTA width (consumer
+// warps) is chosen so the grid covers the SMs, or forced by
+// SN_OPT_RECUR_TILE.
+template <int KIND, int DK>
+constexpr int lanes_per_col() {
+    return (KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD) ? DK / 8 : DK / 16;
+}
+
+template <int KIND, int DK>
+cudaError_t dispatch_width(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
+                           cudaStream_t stream) {
+    constexpr int LPC = lanes_per_col<KIND, DK>();
+    constexpr int CPW = 32 / LPC;                      // columns per warp
+    int w = force_w;
+    if (w == 0) {
+        // widest CTA that still gives at least one CTA per SM, else the narrowest
+        w = 2;
+        for (int cand : {8, 4}) {
+            if (x.dv % (cand * CPW) != 0) continue;
+            const int64_t ctas = (int64_t)x.B * x.H * (x.dv / (cand * CPW));
+            if (ctas >= sm_count) { w = cand; break; }
+        }
     }
-    const int64_t ctas = (int64_t)x.B * x.H * (x.dv / 32);
-    if (ctas < 2 * sm_count) return run_seq<KIND, 64, 4, 2>(x, st, wait_ns, stream);
-    return run_seq<KIND, 64, 4, 4>(x, st, wait_ns, stream);
+    if (x.dv % (w * CPW) != 0) return cudaErrorInvalidValue;
+    switch (w) {
+        case 2: return run_seq<KIND, DK, LPC, 2>(x, st, wait_ns, stream);
+        case 4: return run_seq<KIND, DK, LPC, 4>(x, st, wait_ns, stream);
+        case 8: return run_seq<KIND, DK, LPC, 8>(x, st, wait_ns, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int KIND>
+cudaError_t dispatch_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
+                         cudaStream_t stream) {
+    if (x.dk == 128) return dispatch_width<KIND, 128>(x, st, wait_ns, sm_count, force_w, stream);
+    return dispatch_width<KIND, 64>(x, st, wait_ns, sm_count, force_w, stream);
 }
 
 // ============================================================ decode (T == 1)
@@ -412,7 +470,7 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
             const float4 x = (S_in != nullptr) ? row[m * 4 + sub] : make_float4(0.f, 0.f, 0.f, 0.f);
             P[4 * m] = x.x; P[4 * m + 1] = x.y; P[4 * m + 2] = x.z; P[4 * m + 3] = x.w;
         }
-        const float acc = col_step<RK_RWKV7, 4, 4>(P, kv, wv, qv, vv[i], 0.f, sub, o != nullptr);
+        const float acc = group_sum(col_step<RK_RWKV7, 4, 4>(P, kv, wv, qv, vv[i], 0.f, sub, o != nullptr), 4);
 #pragma unroll
         for (int m = 0; m < 4; ++m) row[m * 4 + sub] = make_float4(P[4 * m], P[4 * m + 1], P[4 * m + 2], P[4 * m + 3]);
         if (o != nullptr && sub == 0) o[(size_t)(tile0 + t) * DEC_D + i] = __fmul_rn(acc, 1.0f);
@@ -431,12 +489,12 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
 }  // namespace
 
 cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
-                                  cudaStream_t stream) {
+                                  int force_w, cudaStream_t stream) {
     switch (x.kind) {
-        case RK_DIAG_KEY: return dispatch_seq<RK_DIAG_KEY>(x, st, wait_ns, sm_count, stream);
-        case RK_DIAG_HEAD: return dispatch_seq<RK_DIAG_HEAD>(x, st, wait_ns, sm_count, stream);
-        case RK_DELTA: return dispatch_seq<RK_DELTA>(x, st, wait_ns, sm_count, stream);
-        case RK_RWKV7: return dispatch_seq<RK_RWKV7>(x, st, wait_ns, sm_count, stream);
+        case RK_DIAG_KEY: return dispatch_seq<RK_DIAG_KEY>(x, st, wait_ns, sm_count, force_w, stream);
+        case RK_DIAG_HEAD: return dispatch_seq<RK_DIAG_HEAD>(x, st, wait_ns, sm_count, force_w, stream);
+        case RK_DELTA: return dispatch_seq<RK_DELTA>(x, st, wait_ns, sm_count, force_w, stream);
+        case RK_RWKV7: return dispatch_seq<RK_RWKV7>(x, st, wait_ns, sm_count, force_w, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -40,6 +40,7 @@ struct SnCtx {
     int wait_limit_us;
     int debug_poison;
     int recur_kernel;
+    int recur_tile;             // forced consumer warps per CTA of the sequence kernel (0 = auto)
 };
 
 namespace sn {
@@ -89,7 +90,7 @@ struct RecurArgs {
 };
 
 cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
-                                  cudaStream_t stream);
+                                  int force_width, cudaStream_t stream);
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);

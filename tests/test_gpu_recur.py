@@ -335,3 +335,24 @@ def test_full_size_rwkv7_decode(ctx):
     xs = {n: x[n][idx].contiguous() for n in ("q", "k", "v", "w", "S0")}
     ro, rS = ref_rwkv(xs, xs["S0"])
     assert _nrel(o[idx], ro) <= TOL and _nrel(S[idx], rS) <= TOL
+
+
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "rwkv"])
+def test_cta_widths_give_identical_bits(sr, ctx, kind):
+    """The CTA width only tiles the value columns; every width returns the
+    same bits, and matches the oracle."""
+    B, T, H = 2, 40, 2
+    dk = 64 if kind == "rwkv" else 128
+    dv = 128
+    x = make(kind, B, T, H, dk, dv, G=1 if kind == "mamba2" else None, seed=8)
+    S0 = synth.normal(state_shape(kind, B, H, dk, dv), 5400)
+    run, ref = RUN[kind]
+    outs = []
+    for w in (0, 2, 4, 8):
+        ctx.set_option(sr.SN_OPT_RECUR_TILE, w)
+        outs.append(run(ctx, x, S0))
+    ctx.set_option(sr.SN_OPT_RECUR_TILE, 0)
+    for o, S in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(S, outs[0][1])
+    ro, rS = ref(x, S0)
+    assert _nrel(outs[0][0], ro) <= TOL and _nrel(outs[0][1], rS) <= TOL
