@@ -233,6 +233,43 @@ sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
                          const float* w, const float* S_in, float* S_out,
                          float* o, void* stream);
 
+/* ---------------------------------------------------------------- allocation-free variant */
+
+/* Maximum look-back tiles of sn_scan_lookback_noalloc: a call needs
+ * B * ceil(N / 32) * ceil(T / 128) <= SN_NOALLOC_MAX_TILES. */
+#define SN_NOALLOC_MAX_TILES 40960
+
+/* The chunked look-back scan without a context and without any device
+ * allocation.  The pages have no counterpart of this entry point: it exists
+ * for callers that cannot allocate device memory at run time -- code under a
+ * fixed memory budget or an allocator that owns the whole device, plugins
+ * whose host application forbids cudaMalloc after start-up, and paths that
+ * cannot create an SnCtx (sn_ctx_create allocates a status block).
+ *
+ * It computes what sn_scan_fma (gated = 0) or sn_scan_gated (gated = 1)
+ * computes with SN_OPT_SCAN_KERNEL = SN_SCAN_KERNEL_LOOKBACK, with the same
+ * bits.  Its scratch is a 16 MiB file-scope device array that every GPU which
+ * loads libsn holds until the process exits; problems needing more than
+ * SN_NOALLOC_MAX_TILES tiles are rejected with SN_E_NOMEM.  Arguments as
+ * sn_scan_fma, except: N % 4 == 0 and 16-byte aligned a, b, s_out are
+ * required (else SN_E_UNSUPPORTED); the device is the calling thread's current
+ * device; `status_out` (device pointer to one int32, may be NULL) receives, in
+ * stream order, SN_OK or SN_E_TIMEOUT if a bounded device-side wait (1 s) ran
+ * out during this call.
+ *
+ * The first call on a device sets the device up (it looks up the array's
+ * device address and clears its flag area with a cudaMemsetAsync on `stream`),
+ * so that first call should come before any stream capture.  Every later call
+ * enqueues one small memset, the kernel and, if status_out is given, a 4-byte
+ * device-to-device copy.  All calls on a device share the one array, which
+ * keeps the last call's contents: calls that may overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  No cudaMalloc, cudaFree or other allocating routine is called. */
+sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t T, int32_t N,
+                                   const float* a, const float* b, const float* s0,
+                                   float* s_final, float* s_out, int32_t* status_out,
+                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,9 @@ EXPORTS = (
     "sn_ctx_create", "sn_ctx_free", "sn_ctx_set_workspace", "sn_workspace_bytes",
     "sn_ctx_last_error", "sn_ctx_set_option", "sn_ctx_get_option",
     "sn_scan_fma", "sn_scan_gated", "sn_recur_diag", "sn_recur_delta", "sn_recur_rwkv7",
+    "sn_scan_lookback_noalloc",
 )
+SN_NOALLOC_MAX_TILES = 40960
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "sn_recur_diag": ([p, i32, i32, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_delta": ([p, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_rwkv7": ([p, i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p], i32),
+            "sn_scan_lookback_noalloc": ([i32, i32, i32, i32, p, p, p, p, p, p, p], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -174,3 +177,8 @@ def sn_recur_delta(ctx, B, T, H, dk, dv, scale, q, k, v, beta, S_in, S_out, o, s
 def sn_recur_rwkv7(ctx, B, T, H, dk, dv, q, k, v, w, S_in, S_out, o, stream=None) -> int:
     return load().sn_recur_rwkv7(ctx, B, T, H, dk, dv, ptr(q), ptr(k), ptr(v), ptr(w), ptr(S_in), ptr(S_out),
                                  ptr(o), stream_handle(stream))
+
+
+def sn_scan_lookback_noalloc(gated, B, T, N, a, b, s0, s_final, s_out, status_out=None, stream=None) -> int:
+    return load().sn_scan_lookback_noalloc(gated, B, T, N, ptr(a), ptr(b), ptr(s0), ptr(s_final), ptr(s_out),
+                                           ptr(status_out), stream_handle(stream))

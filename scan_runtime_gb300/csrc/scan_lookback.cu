@@ -345,3 +345,151 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32
 }
 
 }  // namespace sn
+
+// ============================================================ allocation-free entry point
+//
+// sn_scan_lookback_noalloc runs the look-back scan above with its scratch in a
+// file-scope device array instead of a workspace handed over by the caller.
+// It is for callers that must not allocate device memory at run time: code
+// running under a fixed memory budget or a custom allocator that owns the
+// whole device, plugins whose host application forbids cudaMalloc after
+// start-up, and paths that cannot create an SnCtx (context creation allocates
+// the context's status block).
+//
+// The array (kNoallocScratchBytes, 16 MiB) lives on every device that loads
+// this library until the process exits.  Layout, fixed for every call:
+//   [ status block 256 B | flags: kNoallocMaxTiles x u32 | A | B | C carries ]
+// Flags stay at fixed offsets, so a flag word only ever holds a tag or zero.
+#include <atomic>
+#include <mutex>
+
+namespace {
+
+constexpr int64_t kNoallocMaxTiles = 40960;
+constexpr int64_t kNoallocFlagsOff = 256;
+constexpr int64_t kNoallocDataOff = kNoallocFlagsOff + kNoallocMaxTiles * 4;
+constexpr int64_t kNoallocScratchBytes = kNoallocDataOff + kNoallocMaxTiles * 3 * sn::LB_NC * 4;
+static_assert(kNoallocScratchBytes <= (int64_t(16) << 20), "scratch stays within 16 MiB");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kNoallocMaxDevices = 64;
+constexpr uint32_t kNoallocEpochWrap = 1u << 29;
+
+struct NoallocDevice {
+    bool ready = false;
+    unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+    int sm_count = 0;
+    int occ[2] = {0, 0};
+    uint32_t epoch = 0;
+};
+NoallocDevice g_noalloc[kNoallocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+bool nz_overlap(const void* p, int64_t pb, const void* q, int64_t qb) {
+    if (p == nullptr || q == nullptr) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), b0 = reinterpret_cast<uintptr_t>(q);
+    return a0 < b0 + (uintptr_t)qb && b0 < a0 + (uintptr_t)pb;
+}
+
+}  // namespace
+
+extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t T, int32_t N, const float* a,
+                                              const float* b, const float* s0, float* s_final, float* s_out,
+                                              int32_t* status_out, void* stream) {
+    using namespace sn;
+    // ---- arguments (checked before anything is enqueued)
+    if (a == nullptr || b == nullptr || B <= 0 || T <= 0 || N <= 0 || (gated != 0 && gated != 1))
+        return SN_E_INVAL;
+    const void* ptrs[6] = {a, b, s0, s_final, s_out, status_out};
+    for (const void* q : ptrs)
+        if (q != nullptr && (reinterpret_cast<uintptr_t>(q) & 3u) != 0) return SN_E_INVAL;
+    const int64_t big = (int64_t)B * T * N * 4, small = (int64_t)B * N * 4;
+    if ((int64_t)B * T * N > (int64_t(1) << 40)) return SN_E_INVAL;
+    const void* ins[3] = {a, b, s0};
+    const int64_t insz[3] = {big, big, small};
+    void* outs[3] = {s_final, s_out, status_out};
+    const int64_t outsz[3] = {small, big, 4};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j) {
+            const bool inplace = (i == 0 && j == 2 && outs[0] == ins[2]);   // s_final may equal s0
+            if (!inplace && nz_overlap(outs[i], outsz[i], ins[j], insz[j])) return SN_E_INVAL;
+        }
+        for (int j = i + 1; j < 3; ++j)
+            if (nz_overlap(outs[i], outsz[i], outs[j], outsz[j])) return SN_E_INVAL;
+    }
+    ScanArgs x{B, T, N, a, b, s0, s_final, s_out};
+    if (!scan_tma_ok(x)) return SN_E_UNSUPPORTED;
+    const int64_t tiles = lookback_flag_count(B, T, N);
+    if (tiles > kNoallocMaxTiles) return SN_E_NOMEM;   // beyond the fixed scratch
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return SN_E_DEVICE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    auto kern = gated ? scan_lookback<true> : scan_lookback<false>;
+
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoallocDevice& d = g_noalloc[dev];
+    if (!d.ready) {
+        // One-time set-up on this device (the first call; it must precede any
+        // stream capture): the array's device address, the kernel's shared
+        // memory opt-in and occupancy, and a cleared status/flag area.
+        void* sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_noalloc_scratch) != cudaSuccess || sym == nullptr) return SN_E_DEVICE;
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SN_E_DEVICE;
+        if (prop.major != 10 || prop.minor != 3) return SN_E_UNSUPPORTED;
+        for (int g = 0; g < 2; ++g) {
+            auto k = g ? scan_lookback<true> : scan_lookback<false>;
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LB_SMEM) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[g], k, LB_THREADS, LB_SMEM) != cudaSuccess ||
+                d.occ[g] < 1)
+                return SN_E_DEVICE;
+        }
+        if (cudaMemsetAsync(sym, 0, (size_t)kNoallocDataOff, s) != cudaSuccess) return SN_E_DEVICE;
+        d.scratch = static_cast<unsigned char*>(sym);
+        d.sm_count = prop.multiProcessorCount;
+        d.epoch = 0;
+        d.ready = true;
+    }
+    if (d.epoch + 1 >= kNoallocEpochWrap) {       // tags would repeat: start the flags over
+        if (cudaMemsetAsync(d.scratch, 0, (size_t)kNoallocDataOff, s) != cudaSuccess) return SN_E_DEVICE;
+        d.epoch = 0;
+    }
+    d.epoch += 1;
+
+    CUtensorMap ma, mb;
+    if (!make_scan_map(&ma, a, B, T, N, LB_NC, LB_TC) || !make_scan_map(&mb, b, B, T, N, LB_NC, LB_TC))
+        return SN_E_DEVICE;
+    SnDevStatus* st = reinterpret_cast<SnDevStatus*>(d.scratch);
+    LookbackParams p;
+    p.B = B;
+    p.T = T;
+    p.N = N;
+    p.ncb = (N + LB_NC - 1) / LB_NC;
+    p.nbcb = B * p.ncb;
+    p.nchunks = (T + LB_TC - 1) / LB_TC;
+    p.ntiles = p.nbcb * p.nchunks;
+    p.s0 = s0;
+    p.s_final = s_final;
+    p.s_out = s_out;
+    p.flags = reinterpret_cast<uint32_t*>(d.scratch + kNoallocFlagsOff);
+    p.dA = reinterpret_cast<float*>(d.scratch + kNoallocDataOff);
+    p.dB = p.dA + tiles * LB_NC;
+    p.dC = p.dB + tiles * LB_NC;
+    p.tag = d.epoch << 2;
+    p.want = p.tag;
+    p.st = st;
+    p.wait_ns = 1000000000ull;                    // 1 s bound on every device-side wait
+    // this call's error word starts at zero
+    if (cudaMemsetAsync(st, 0, 2 * sizeof(int), s) != cudaSuccess) return SN_E_DEVICE;
+    const int grid = (int)std::min<int64_t>(tiles, (int64_t)d.occ[gated] * d.sm_count);
+    void* args[] = {(void*)&ma, (void*)&mb, (void*)&p};
+    if (cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(LB_THREADS), args, LB_SMEM, s) !=
+        cudaSuccess)
+        return SN_E_DEVICE;
+    if (status_out != nullptr &&
+        cudaMemcpyAsync(status_out, &st->error, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return SN_E_DEVICE;
+    return SN_OK;
+}

@@ -1,0 +1,76 @@
+"""The allocation-free look-back entry point against the context-based one.
+
+sn_scan_lookback_noalloc serves callers that cannot allocate device memory at
+run time (a fixed memory budget, an allocator that owns the device, a host
+that forbids cudaMalloc after start-up).  It keeps its scratch in a
+file-scope device array that every call shares.  This file runs last so a
+failure here leaves every other test already run; it must pass both on its
+own in a fresh process and after the rest of the suite (the shared array then
+holds an earlier call's contents).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def sr():
+    import scan_runtime_gb300 as sr
+    sr.build()
+    return sr
+
+
+def _nrel(x, r):
+    x, r = np.asarray(x, np.float64), np.asarray(r, np.float64)
+    return float(np.max(np.abs(x - r)) / max(float(np.max(np.abs(r))), 1e-30))
+
+
+def _with_ctx(sr, gated, a, rhs, s0):
+    B, T, N = a.shape
+    ctx = sr.Context(0)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+    ctx.ensure_workspace(B, T, N)
+    fn = ctx.scan_gated if gated else ctx.scan_fma
+    so, sf = fn(a, rhs, s0)
+    torch.cuda.synchronize()
+    assert ctx.last_error() == sr.SN_OK
+    ctx.close()
+    return so.cpu().numpy(), sf.cpu().numpy()
+
+
+def _noalloc(sr, gated, a, rhs, s0):
+    B, T, N = a.shape
+    so = torch.full((B, T, N), float("nan"), device="cuda")
+    sf = torch.full((B, N), float("nan"), device="cuda")
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    st = sr.sn_scan_lookback_noalloc(gated, B, T, N, a, rhs, s0, sf, so, status)
+    assert st == sr.SN_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == sr.SN_OK
+    return so.cpu().numpy(), sf.cpu().numpy()
+
+
+def test_no_alloc_matches_workspace_entry_point_on_two_calls(sr):
+    # two calls in a row with different shapes and forms: the second one
+    # finds the first one's flags and carries in the shared array
+    for (B, T, N, gated, cid) in ((2, 3000, 96, 0, 201), (3, 1100, 64, 1, 202)):
+        x = synth.scan_inputs(B, T, N, large=True, cid=cid)
+        a, rhs = x["a"].cuda(), (x["u"] if gated else x["b"]).cuda()
+        s0 = synth.normal((B, N), cid + 7).cuda()
+        so_ref, sf_ref = _with_ctx(sr, gated, a, rhs, s0)
+        so, sf = _noalloc(sr, gated, a, rhs, s0)
+        assert _nrel(so, so_ref) <= TOL and _nrel(sf, sf_ref) <= TOL
+
+
+def test_no_alloc_rejects_problems_beyond_its_scratch(sr):
+    a = torch.zeros(4, device="cuda")
+    T = 128 * (sr.SN_NOALLOC_MAX_TILES + 1)          # one channel block, one tile too many
+    assert sr.sn_scan_lookback_noalloc(0, 1, T, 32, a, a, None, None, None) == sr.SN_E_NOMEM
+    assert sr.sn_scan_lookback_noalloc(0, 1, 16, 30, a, a, None, None, None) == sr.SN_E_UNSUPPORTED
+    assert sr.sn_scan_lookback_noalloc(2, 1, 16, 32, a, a, None, None, None) == sr.SN_E_INVAL
