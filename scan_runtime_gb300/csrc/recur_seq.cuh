@@ -1,0 +1,447 @@
+// recur_seq.cuh -- the sequence kernel shared by the three matrix recurrences
+// (instantiated per kind in recur_diag.cu, recur_delta.cu, recur_rwkv7.cu).
+//
+// All recurrences are written for the state P in R^{dk x dv} (row = key index
+// i, column = value index j), whose columns evolve independently:
+//   diag   P_t = diag(d_t) P_{t-1} + k_t v_t^T                       GLA / Mamba-2
+//   delta  P_t = P_{t-1} + k_t delta_t^T,  delta_t = (v_t - P_{t-1}^T k_t) beta_t
+//   rwkv7  P_t = diag(w_t) P_{t-1} + k_t delta_t^T,  delta_t = v_t - P_{t-1}^T k_t
+//   readout o_t = scale * P_t^T q_t
+// ("SunnyNet 工程化实录：一个 O(N) 架构如何长出自己的 C 推理运行时" §4.1 Mamba-2,
+// §4.2 DeltaNet, §4.3 GLA, §5.1 RWKV-7; RWKV-7's S in R^{dv x dk} is P^T, so it
+// is the delta template with a per-key decay and beta = 1, loaded and stored
+// transposed.)
+//
+// Work split: one CTA per (batch, head, tile of JT value columns).  A lane
+// holds R rows x C columns of P in registers for the whole sequence; LPC =
+// dk / R lanes share a group of C columns.  Column pairs are packed into
+// f32x2 operations, so every k / decay / q value read from shared memory
+// feeds C state entries.  q, k, per-key decay and the v slice arrive through a
+// 3-stage TMA ring fed by a producer warp (per-head scalars by 4-byte cp.async
+// on the same mbarrier); o leaves through TMA stores.
+//
+// Arithmetic per column is fixed: the diag update is fma(d_i, P_ij, k_i * v_j)
+// with the product rounded first (the single-precision definition's order);
+// a lane's dot products run four chains over its rows (row index mod 4) and
+// join as (c0 + c1) + (c2 + c3); lane partials join over xor partners LPC/2 ..
+// 1.  The result therefore depends only on the state and the inputs: segment
+// splits are bit-exact, and the CTA width does not change the bits.
+#pragma once
+
+#include <algorithm>
+
+#include "ptx.cuh"
+#include "sn_internal.h"
+
+namespace sn {
+
+constexpr int RS_TS = 16;       // time steps per stage
+constexpr int RS_STAGES = 3;
+constexpr int RS_OBUF = 3;      // output staging buffers
+constexpr int RS_RB = 8;        // steps per readout reduction batch
+
+template <int KIND>
+constexpr bool per_key_gate() { return KIND == RK_DIAG_KEY || KIND == RK_RWKV7; }
+template <int KIND>
+constexpr bool scalar_gate() { return KIND == RK_DIAG_HEAD || KIND == RK_DELTA; }
+
+template <int KIND, int DK, int JT>
+struct SeqLayout {
+    static constexpr uint32_t q_off = 0;
+    static constexpr uint32_t k_off = q_off + RS_TS * DK * 4;
+    static constexpr uint32_t g_off = k_off + RS_TS * DK * 4;
+    static constexpr uint32_t g_bytes = per_key_gate<KIND>() ? RS_TS * DK * 4 : 128;
+    static constexpr uint32_t v_off = g_off + g_bytes;
+    static constexpr uint32_t v_bytes = ((RS_TS * JT * 4 + 127) / 128) * 128;
+    static constexpr uint32_t stage_bytes = v_off + v_bytes;
+    static constexpr uint32_t tx_bytes = 2 * RS_TS * DK * 4 + (per_key_gate<KIND>() ? RS_TS * DK * 4 : 0) +
+                                         RS_TS * JT * 4;
+    static constexpr uint32_t o_off = RS_STAGES * stage_bytes;
+    static constexpr uint32_t o_bytes = ((RS_TS * JT * 4 + 127) / 128) * 128;
+    static constexpr uint32_t bar_off = o_off + RS_OBUF * o_bytes;
+    static constexpr size_t smem = bar_off + 2 * RS_STAGES * 8 + 128;   // + alignment slack
+};
+
+struct SeqParams {
+    int T, H, G, dk, dv;
+    float scale;
+    const float* g;        // per-head scalars (dA or beta) for cp.async
+    const float* S_in;
+    float* S_out;
+    int has_o;
+    SnDevStatus* st;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+__device__ __forceinline__ float group_sum(float x, int lpc) {
+    for (int o = lpc >> 1; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float2 group_sum2(float2 x, int lpc) {
+    return make_float2(group_sum(x.x, lpc), group_sum(x.y, lpc));
+}
+
+// Sum NV per-lane values over a group of LPC lanes by recursive halving: at
+// offset o a lane keeps the half its bit o selects and adds its partner's copy
+// of that half.  Afterwards v[e] (e < NV/LPC) holds the group sum of value
+// index sub * (NV/LPC) + e.  The pairing (offsets LPC/2 .. 1) is group_sum's
+// and addition is commutative, so each sum has the bits group_sum gives it.
+template <int LPC, int NV>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int sub) {
+#pragma unroll
+    for (int lvl = 0; (LPC >> (lvl + 1)) >= 1; ++lvl) {
+        const int o = LPC >> (lvl + 1);
+        const int c = NV >> lvl;
+        const bool upper = (sub & o) != 0;
+#pragma unroll
+        for (int i = 0; i < c / 2; ++i) {
+            const float send = upper ? v[i] : v[i + c / 2];
+            const float keep = upper ? v[i + c / 2] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+}
+
+template <int R, int LPC>
+__device__ __forceinline__ void load_rows(float (&x)[R], const float* row, int sub) {
+#pragma unroll
+    for (int m = 0; m < R / 4; ++m) {
+        const float4 t = *reinterpret_cast<const float4*>(row + (m * LPC + sub) * 4);
+        x[4 * m] = t.x; x[4 * m + 1] = t.y; x[4 * m + 2] = t.z; x[4 * m + 3] = t.w;
+    }
+}
+
+// One time step for one lane: rows (m * LPC + sub) * 4 + e (m < R/4, e < 4),
+// columns c < C of its group (packed as C/2 pairs).  kr, gr, qr point at the
+// step's k, per-key gate and q rows; vr at the group's C values; gsc is the
+// per-head scalar (dA or beta).  opart receives this lane's readout partials.
+template <int KIND, int R, int C, int LPC>
+__device__ __forceinline__ void lane_step(float2 (&P)[R][C / 2], const float* kr, const float* gr,
+                                          const float* qr, const float* vr, float gsc, int sub,
+                                          float2 (&opart)[C / 2], bool want_o) {
+    constexpr int C2 = C / 2;
+    float kv[R];
+    load_rows<R, LPC>(kv, kr, sub);
+    float2 v2[C2];
+#pragma unroll
+    for (int c = 0; c < C2; ++c) v2[c] = *reinterpret_cast<const float2*>(vr + 2 * c);
+    if constexpr (KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD) {
+        float dv_[R];
+        if constexpr (KIND == RK_DIAG_KEY) {
+            load_rows<R, LPC>(dv_, gr, sub);
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) dv_[r] = gsc;
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C2; ++c) P[r][c] = __ffma2_rn(f2(dv_[r]), P[r][c], __fmul2_rn(f2(kv[r]), v2[c]));
+    } else {
+        float wv[R];
+        if constexpr (KIND == RK_RWKV7) load_rows<R, LPC>(wv, gr, sub);
+#pragma unroll
+        for (int c = 0; c < C2; ++c) {
+            float2 u0 = f2(0.f), u1 = f2(0.f), u2 = f2(0.f), u3 = f2(0.f);
+#pragma unroll
+            for (int m = 0; m < R / 4; ++m) {
+                u0 = __ffma2_rn(P[4 * m][c], f2(kv[4 * m]), u0);
+                u1 = __ffma2_rn(P[4 * m + 1][c], f2(kv[4 * m + 1]), u1);
+                u2 = __ffma2_rn(P[4 * m + 2][c], f2(kv[4 * m + 2]), u2);
+                u3 = __ffma2_rn(P[4 * m + 3][c], f2(kv[4 * m + 3]), u3);
+            }
+            const float2 u = group_sum2(__fadd2_rn(__fadd2_rn(u0, u1), __fadd2_rn(u2, u3)), LPC);
+            float2 delta = __fadd2_rn(v2[c], make_float2(-u.x, -u.y));   // v - u, exactly
+            if constexpr (KIND == RK_DELTA) {
+                delta = __fmul2_rn(delta, f2(gsc));
+#pragma unroll
+                for (int r = 0; r < R; ++r) P[r][c] = __ffma2_rn(f2(kv[r]), delta, P[r][c]);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) P[r][c] = __ffma2_rn(f2(kv[r]), delta, __fmul2_rn(P[r][c], f2(wv[r])));
+            }
+        }
+    }
+    if (!want_o) return;
+    float qv[R];
+    load_rows<R, LPC>(qv, qr, sub);
+#pragma unroll
+    for (int c = 0; c < C2; ++c) {
+        float2 a0 = f2(0.f), a1 = f2(0.f), a2 = f2(0.f), a3 = f2(0.f);
+#pragma unroll
+        for (int m = 0; m < R / 4; ++m) {
+            a0 = __ffma2_rn(P[4 * m][c], f2(qv[4 * m]), a0);
+            a1 = __ffma2_rn(P[4 * m + 1][c], f2(qv[4 * m + 1]), a1);
+            a2 = __ffma2_rn(P[4 * m + 2][c], f2(qv[4 * m + 2]), a2);
+            a3 = __ffma2_rn(P[4 * m + 3][c], f2(qv[4 * m + 3]), a3);
+        }
+        opart[c] = __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
+    }
+}
+
+template <int KIND, int DK, int R, int C, int W>
+__global__ void __launch_bounds__((W + 1) * 32)
+recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+          const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_v,
+          const __grid_constant__ CUtensorMap map_o, const SeqParams p) {
+    constexpr int LPC = DK / R;            // lanes per column group
+    constexpr int CPW = 32 / LPC;          // column groups per warp
+    constexpr int JT = W * CPW * C;        // columns per CTA
+    constexpr int C2 = C / 2;
+    constexpr int NV = RS_RB * C;          // readout values per lane per batch
+    using L = SeqLayout<KIND, DK, JT>;
+    static_assert(R % 4 == 0 && C % 2 == 0 && LPC <= 32 && NV % LPC == 0, "tile shape");
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar_off);
+    uint64_t* empty = full + RS_STAGES;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int jt0 = blockIdx.x * JT, h = blockIdx.y, b = blockIdx.z;
+    const int grp = h / (p.H / p.G);
+    const int T = p.T;
+    const int nst = (T + RS_TS - 1) / RS_TS;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RS_STAGES; ++s) {
+            mbar_init(&full[s], scalar_gate<KIND>() ? 33 : 1);
+            mbar_init(&empty[s], W);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == W) {
+        // ------------------------------------------------ producer warp
+        for (int kk = 0; kk < nst; ++kk) {
+            const int slot = kk % RS_STAGES;
+            if (kk >= RS_STAGES) {
+                const bool ok =
+                    __all_sync(0xffffffffu, mbar_wait(&empty[slot], ((kk / RS_STAGES) - 1) & 1, p.wait_ns));
+                if (!ok) {
+                    if (lane == 0) record_error(p.st, SN_E_TIMEOUT, (SN_K_RECUR_SEQ << 16) | 1);
+                    break;       // consumers will time out on `full` and stop too
+                }
+            }
+            unsigned char* sb = smem + slot * L::stage_bytes;
+            const int t0 = kk * RS_TS;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[slot], L::tx_bytes);
+                tma_load_4d(sb + L::q_off, &map_q, &full[slot], 0, grp, t0, b);
+                tma_load_4d(sb + L::k_off, &map_k, &full[slot], 0, grp, t0, b);
+                if constexpr (per_key_gate<KIND>()) tma_load_4d(sb + L::g_off, &map_g, &full[slot], 0, h, t0, b);
+                tma_load_4d(sb + L::v_off, &map_v, &full[slot], jt0, h, t0, b);
+            }
+            if constexpr (scalar_gate<KIND>()) {
+                if (lane < RS_TS && t0 + lane < T)
+                    cp_async_4(sb + L::g_off + 4 * lane, p.g + ((size_t)b * T + t0 + lane) * p.H + h);
+                cp_async_mbar_arrive_noinc(&full[slot]);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int gcol = lane / LPC, sub = lane % LPC;
+    const int jl0 = (warp * CPW + gcol) * C;           // first column of the group within the tile
+    const int j0 = jt0 + jl0;
+    const size_t sbase = ((size_t)b * p.H + h) * (size_t)DK * p.dv;
+
+    float2 P[R][C2];
+#pragma unroll
+    for (int m = 0; m < R / 4; ++m) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int row = (m * LPC + sub) * 4 + e;
+#pragma unroll
+            for (int c = 0; c < C2; ++c) {
+                float x0 = 0.f, x1 = 0.f;
+                if (p.S_in != nullptr) {
+                    if (KIND == RK_RWKV7) {          // stored (dv, dk): value row, keys contiguous
+                        x0 = p.S_in[sbase + (size_t)(j0 + 2 * c) * DK + row];
+                        x1 = p.S_in[sbase + (size_t)(j0 + 2 * c + 1) * DK + row];
+                    } else {                         // stored (dk, dv)
+                        const float2 t =
+                            *reinterpret_cast<const float2*>(p.S_in + sbase + (size_t)row * p.dv + j0 + 2 * c);
+                        x0 = t.x;
+                        x1 = t.y;
+                    }
+                }
+                P[4 * m + e][c] = make_float2(x0, x1);
+            }
+        }
+    }
+
+    const bool want_o = p.has_o != 0;
+    bool failed = false;
+    for (int kk = 0; kk < nst; ++kk) {
+        const int slot = kk % RS_STAGES;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (kk / RS_STAGES) & 1, p.wait_ns));
+        if (!ok) {
+            if (lane == 0) record_error(p.st, SN_E_TIMEOUT, (SN_K_RECUR_SEQ << 16) | 2);
+            failed = true;
+            break;
+        }
+        const unsigned char* sb = smem + slot * L::stage_bytes;
+        const float* qs = reinterpret_cast<const float*>(sb + L::q_off);
+        const float* ks = reinterpret_cast<const float*>(sb + L::k_off);
+        const float* gs = reinterpret_cast<const float*>(sb + L::g_off);
+        const float* vs = reinterpret_cast<const float*>(sb + L::v_off);
+        float* os = reinterpret_cast<float*>(smem + L::o_off + (kk % RS_OBUF) * L::o_bytes);
+        const int tn = min(RS_TS, T - kk * RS_TS);
+
+        if (tn == RS_TS) {
+            // Readout partials of RS_RB steps stay in registers and are reduced
+            // once over the lane group (no per-step shuffle chain or store).
+#pragma unroll
+            for (int rb = 0; rb < RS_TS / RS_RB; ++rb) {
+                float2 ov[RS_RB][C2];
+#pragma unroll
+                for (int i = 0; i < RS_RB; ++i) {
+                    const int t = rb * RS_RB + i;
+                    lane_step<KIND, R, C, LPC>(P, ks + t * DK, gs + t * DK, qs + t * DK, vs + t * JT + jl0,
+                                               scalar_gate<KIND>() ? gs[t] : 0.f, sub, ov[i], want_o);
+                }
+                if (want_o) {
+                    float fl[NV];                      // [step][column] readout partials
+#pragma unroll
+                    for (int i = 0; i < RS_RB; ++i)
+#pragma unroll
+                        for (int c = 0; c < C2; ++c) {
+                            fl[i * C + 2 * c] = ov[i][c].x;
+                            fl[i * C + 2 * c + 1] = ov[i][c].y;
+                        }
+                    reduce_scatter<LPC, NV>(fl, sub);
+                    constexpr int PER = NV / LPC;
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) {
+                        const int idx = sub * PER + e;
+                        os[(rb * RS_RB + idx / C) * JT + jl0 + idx % C] = __fmul_rn(fl[e], p.scale);
+                    }
+                }
+            }
+        } else {
+            for (int t = 0; t < tn; ++t) {
+                float2 part[C2];
+                lane_step<KIND, R, C, LPC>(P, ks + t * DK, gs + t * DK, qs + t * DK, vs + t * JT + jl0,
+                                           scalar_gate<KIND>() ? gs[t] : 0.f, sub, part, want_o);
+                if (want_o) {
+#pragma unroll
+                    for (int c = 0; c < C2; ++c) {
+                        const float2 acc = group_sum2(part[c], LPC);
+                        if (sub == 0) {
+                            os[t * JT + jl0 + 2 * c] = __fmul_rn(acc.x, p.scale);
+                            os[t * JT + jl0 + 2 * c + 1] = __fmul_rn(acc.y, p.scale);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (want_o) {
+            fence_proxy_async_smem();
+            // the store two stages back read the buffer the next stage writes
+            if (threadIdx.x == 0) bulk_wait_read_allbut1();
+            named_bar_sync(1, W * 32);
+            if (threadIdx.x == 0) {
+                tma_store_4d(&map_o, os, jt0, h, kk * RS_TS, b);
+                bulk_commit();
+            }
+        }
+    }
+    if (threadIdx.x == 0) bulk_wait_all();
+    if (failed || p.S_out == nullptr) return;
+#pragma unroll
+    for (int m = 0; m < R / 4; ++m) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int row = (m * LPC + sub) * 4 + e;
+#pragma unroll
+            for (int c = 0; c < C2; ++c) {
+                const float2 x = P[4 * m + e][c];
+                if (KIND == RK_RWKV7) {
+                    p.S_out[sbase + (size_t)(j0 + 2 * c) * DK + row] = x.x;
+                    p.S_out[sbase + (size_t)(j0 + 2 * c + 1) * DK + row] = x.y;
+                } else {
+                    *reinterpret_cast<float2*>(p.S_out + sbase + (size_t)row * p.dv + j0 + 2 * c) = x;
+                }
+            }
+        }
+    }
+}
+
+template <int KIND, int DK, int R, int C, int W>
+cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaStream_t stream) {
+    constexpr int LPC = DK / R;
+    constexpr int JT = W * (32 / LPC) * C;
+    using L = SeqLayout<KIND, DK, JT>;
+    if (x.dv % JT != 0) return cudaErrorInvalidValue;
+    const int gdim = (KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD) ? x.G : x.H;
+    CUtensorMap mq, mk, mg, mv, mo;
+    const uint64_t dqk[4] = {(uint64_t)DK, (uint64_t)gdim, (uint64_t)x.T, (uint64_t)x.B};
+    const uint64_t sqk[3] = {(uint64_t)DK * 4, (uint64_t)gdim * DK * 4, (uint64_t)x.T * gdim * DK * 4};
+    const uint32_t bqk[4] = {(uint32_t)DK, 1, RS_TS, 1};
+    const uint64_t dg[4] = {(uint64_t)DK, (uint64_t)x.H, (uint64_t)x.T, (uint64_t)x.B};
+    const uint64_t sg[3] = {(uint64_t)DK * 4, (uint64_t)x.H * DK * 4, (uint64_t)x.T * x.H * DK * 4};
+    const uint64_t dvv[4] = {(uint64_t)x.dv, (uint64_t)x.H, (uint64_t)x.T, (uint64_t)x.B};
+    const uint64_t svv[3] = {(uint64_t)x.dv * 4, (uint64_t)x.H * x.dv * 4, (uint64_t)x.T * x.H * x.dv * 4};
+    const uint32_t bv[4] = {(uint32_t)JT, 1, RS_TS, 1};
+    if (!encode_tiled(&mq, 4, x.q, dqk, sqk, bqk) || !encode_tiled(&mk, 4, x.k, dqk, sqk, bqk) ||
+        !encode_tiled(&mv, 4, x.v, dvv, svv, bv))
+        return cudaErrorInvalidValue;
+    if (per_key_gate<KIND>()) {
+        if (!encode_tiled(&mg, 4, x.g, dg, sg, bqk)) return cudaErrorInvalidValue;
+    } else {
+        mg = mk;   // unused
+    }
+    if (x.o != nullptr) {
+        if (!encode_tiled(&mo, 4, x.o, dvv, svv, bv)) return cudaErrorInvalidValue;
+    } else {
+        mo = mv;   // unused
+    }
+    SeqParams p{x.T, x.H, x.G, x.dk, x.dv, x.scale, x.g, x.S_in, x.S_out, x.o != nullptr ? 1 : 0, st, wait_ns};
+    auto kern = recur_seq<KIND, DK, R, C, W>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid(x.dv / JT, x.H, x.B);
+    kern<<<grid, (W + 1) * 32, L::smem, stream>>>(mq, mk, mg, mv, mo, p);
+    return cudaGetLastError();
+}
+
+// Pick the CTA width (consumer warps): 4-warp CTAs while they fit in one wave
+// (at most one per SM), else 2-warp CTAs for more CTAs per SM; measured on the
+// GLA, Mamba-2, DeltaNet and RWKV-7 workloads, 8 warps never won.  A forced
+// width (SN_OPT_RECUR_TILE) overrides the choice.
+template <int KIND, int DK, int R, int C>
+cudaError_t run_seq_width(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
+                          cudaStream_t stream) {
+    constexpr int COLS_PER_WARP = (32 / (DK / R)) * C;
+    int w = force_w;
+    if (w == 0) {
+        const bool fits4 = x.dv % (4 * COLS_PER_WARP) == 0 &&
+                           (int64_t)x.B * x.H * (x.dv / (4 * COLS_PER_WARP)) <= sm_count;
+        w = (fits4 || x.dv % (2 * COLS_PER_WARP) != 0) ? 4 : 2;
+    }
+    switch (w) {
+        case 2: return run_seq<KIND, DK, R, C, 2>(x, st, wait_ns, stream);
+        case 4: return run_seq<KIND, DK, R, C, 4>(x, st, wait_ns, stream);
+        case 8: return run_seq<KIND, DK, R, C, 8>(x, st, wait_ns, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Warps the sequence kernel would run with R rows x C columns per lane.
+inline int64_t seq_warps(const RecurArgs& x, int R, int C) {
+    return (int64_t)x.B * x.H * (x.dv / C) * (x.dk / R) / 32;
+}
+
+}  // namespace sn
