@@ -76,11 +76,14 @@ def traffic_record(kernel):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = open(os.path.join(ROOT, "scan_runtime_gb300", "csrc", "scan.cu"), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
     for line in open(path):
+        if line.startswith("#"):
+            continue
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("src_sha") == sha:
+        if f.get("kernel") != kernel or "src" not in f:
+            continue
+        src = os.path.join(ROOT, f["src"])
+        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == f.get("src_sha"):
             return float(f["dram_bytes_per_launch"])
     return None
 
