@@ -66,6 +66,11 @@ def _load():
             lib.orc_recur_delta_f32.argtypes = [i32] * 5 + [f32] + [p] * 7
             lib.orc_recur_rwkv7_f64.argtypes = [i32] * 5 + [p] * 7
             lib.orc_recur_rwkv7_f32.argtypes = [i32] * 5 + [p] * 7
+            for prec in ("f64", "f32"):
+                getattr(lib, f"orc_scan_fma_bwd_{prec}").argtypes = [i32, i32, i32] + [p] * 8
+                getattr(lib, f"orc_scan_gated_bwd_{prec}").argtypes = [i32, i32, i32] + [p] * 9
+                getattr(lib, f"orc_scan_fma_bwd_{prec}").restype = None
+                getattr(lib, f"orc_scan_gated_bwd_{prec}").restype = None
             for name in ("orc_recur_diag_f64", "orc_recur_diag_f32", "orc_recur_delta_f64",
                          "orc_recur_delta_f32", "orc_recur_rwkv7_f64", "orc_recur_rwkv7_f32"):
                 getattr(lib, name).restype = None
@@ -116,6 +121,41 @@ def scan_fma(a, b, s0=None, prec="f64"):
 def scan_gated(a, u, s0=None, prec="f64"):
     """Gated-form scan; returns ``(s_out (B,T,N), s_final (B,N))``."""
     return _scan("gated", a, u, s0, prec)
+
+
+def _opt32(x, shape):
+    if x is None:
+        return None
+    x = _f32(x)
+    if x.shape != tuple(shape):
+        raise ValueError(f"shape {x.shape} != {tuple(shape)}")
+    return x
+
+
+def scan_backward(kind, a, s, s0=None, gs=None, gf=None, u=None, prec="f64"):
+    """Reverse (adjoint) scan: given the forward states s (B,T,N), the direct
+    gradients gs = dL/ds_t (B,T,N) and gf = dL/ds_final (B,N), return
+    ``(da, db_or_du, ds0)``.  ``kind`` is "fma" or "gated" (then u is needed)."""
+    a = _f32(a)
+    B, T, N = a.shape
+    dt = np.float64 if prec == "f64" else np.float32
+    s = np.ascontiguousarray(np.asarray(s, dtype=dt))
+    assert s.shape == (B, T, N)
+    s0 = _state(s0, prec, (B, N))
+    gs = _opt32(gs, (B, T, N))
+    gf = _opt32(gf, (B, N))
+    da = np.empty((B, T, N), dt)
+    dbu = np.empty((B, T, N), dt)
+    ds0 = np.empty((B, N), dt)
+    lib = _load()
+    if kind == "fma":
+        getattr(lib, f"orc_scan_fma_bwd_{prec}")(B, T, N, _ptr(a), _ptr(s0), _ptr(s), _ptr(gs), _ptr(gf),
+                                                _ptr(da), _ptr(dbu), _ptr(ds0))
+    else:
+        u = _f32(u)
+        getattr(lib, f"orc_scan_gated_bwd_{prec}")(B, T, N, _ptr(a), _ptr(u), _ptr(s0), _ptr(s), _ptr(gs),
+                                                  _ptr(gf), _ptr(da), _ptr(dbu), _ptr(ds0))
+    return da, dbu, ds0
 
 
 def recur_diag(q, k, v, d, S0=None, *, H, G, decay_kind, scale, prec="f64"):

@@ -368,3 +368,98 @@ void orc_recur_rwkv7_f32(i32 B, i32 T, i32 H, i32 dk, i32 dv,
     }
     free(S);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Tier 1 backward: the reverse (adjoint) scans of both forms.               */
+/* ------------------------------------------------------------------------ */
+/* With gs_t = dL/ds_t given for every t and gf = dL/ds_final, the total
+ * adjoint of the state runs backward in time:
+ *     g_{T-1} = gs_{T-1} + gf,     g_t = gs_t + a_{t+1} g_{t+1}   (t < T-1)
+ * and the input gradients follow from the forward step
+ * s_t = a_t s_{t-1} + b_t (b_t = (1 - a_t) u_t in the gated form):
+ *     FMA:   da_t = g_t s_{t-1},            db_t = g_t
+ *     gated: da_t = g_t (s_{t-1} - u_t),    du_t = g_t (1 - a_t)
+ *     ds0 = a_0 g_0,   with s_{-1} = s0.
+ * This is the reverse scan that the forward kernels of "SunnyNet 工程化实录"
+ * §8 (three entries: forward scan, reverse scan, single step) pair with.
+ * s holds the forward states s_t (B, T, N); gs, gf, s0 may be NULL (zeros);
+ * outputs may be NULL.  `u` is NULL for the FMA form. */
+static void orc_scan_bwd_f64(int gated, i32 B, i32 T, i32 N, const float* a, const float* u,
+                             const double* s0, const double* s, const float* gs, const float* gf,
+                             double* da, double* dbu, double* ds0)
+{
+    for (i64 bi = 0; bi < B; ++bi) {
+        for (i64 n = 0; n < N; ++n) {
+            double g = 0.0;
+            for (i64 t = T - 1; t >= 0; --t) {
+                i64 x = (bi * T + t) * N + n;
+                double gst = gs ? (double)gs[x] : 0.0;
+                if (t == T - 1) g = gst + (gf ? (double)gf[bi * N + n] : 0.0);
+                else g = gst + (double)a[x + N] * g;
+                double sprev = (t > 0) ? s[x - N] : (s0 ? s0[bi * N + n] : 0.0);
+                if (gated) {
+                    if (da) da[x] = g * (sprev - (double)u[x]);
+                    if (dbu) dbu[x] = g * (1.0 - (double)a[x]);
+                } else {
+                    if (da) da[x] = g * sprev;
+                    if (dbu) dbu[x] = g;
+                }
+            }
+            if (ds0) ds0[bi * N + n] = (double)a[bi * T * N + n] * g;
+        }
+    }
+}
+
+/* Float order: g_{T-1} = gs + gf (one add), g_t = fma(a_{t+1}, g_{t+1}, gs_t),
+ * each gradient product rounded once after its rounded difference. */
+static void orc_scan_bwd_f32(int gated, i32 B, i32 T, i32 N, const float* a, const float* u,
+                             const float* s0, const float* s, const float* gs, const float* gf,
+                             float* da, float* dbu, float* ds0)
+{
+    for (i64 bi = 0; bi < B; ++bi) {
+        for (i64 n = 0; n < N; ++n) {
+            float g = 0.0f;
+            for (i64 t = T - 1; t >= 0; --t) {
+                i64 x = (bi * T + t) * N + n;
+                float gst = gs ? gs[x] : 0.0f;
+                if (t == T - 1) g = gst + (gf ? gf[bi * N + n] : 0.0f);
+                else g = fmaf(a[x + N], g, gst);
+                float sprev = (t > 0) ? s[x - N] : (s0 ? s0[bi * N + n] : 0.0f);
+                if (gated) {
+                    if (da) da[x] = g * (sprev - u[x]);
+                    if (dbu) dbu[x] = g * (1.0f - a[x]);
+                } else {
+                    if (da) da[x] = g * sprev;
+                    if (dbu) dbu[x] = g;
+                }
+            }
+            if (ds0) ds0[bi * N + n] = a[bi * T * N + n] * g;
+        }
+    }
+}
+
+void orc_scan_fma_bwd_f64(i32 B, i32 T, i32 N, const float* a, const double* s0, const double* s,
+                          const float* gs, const float* gf, double* da, double* db, double* ds0)
+{
+    orc_scan_bwd_f64(0, B, T, N, a, NULL, s0, s, gs, gf, da, db, ds0);
+}
+
+void orc_scan_gated_bwd_f64(i32 B, i32 T, i32 N, const float* a, const float* u, const double* s0,
+                            const double* s, const float* gs, const float* gf, double* da, double* du,
+                            double* ds0)
+{
+    orc_scan_bwd_f64(1, B, T, N, a, u, s0, s, gs, gf, da, du, ds0);
+}
+
+void orc_scan_fma_bwd_f32(i32 B, i32 T, i32 N, const float* a, const float* s0, const float* s,
+                          const float* gs, const float* gf, float* da, float* db, float* ds0)
+{
+    orc_scan_bwd_f32(0, B, T, N, a, NULL, s0, s, gs, gf, da, db, ds0);
+}
+
+void orc_scan_gated_bwd_f32(i32 B, i32 T, i32 N, const float* a, const float* u, const float* s0,
+                            const float* s, const float* gs, const float* gf, float* da, float* du,
+                            float* ds0)
+{
+    orc_scan_bwd_f32(1, B, T, N, a, u, s0, s, gs, gf, da, du, ds0);
+}
