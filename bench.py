@@ -265,7 +265,25 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
             out[f"scan_{form}_lookback"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
                                            "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
-        del x, so, sf
+        # reverse scans (backward pass) on the same workload: read a, s, ds (+u),
+        # write da, db|du
+        gs_ = torch.empty((B, T, N), device=dev).normal_(generator=torch.Generator(dev).manual_seed(77))
+        da = torch.empty((B, T, N), device=dev)
+        db = torch.empty((B, T, N), device=dev)
+        d0 = torch.empty((B, N), device=dev)
+        sr.sn_scan_fma(ctx.handle, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
+        for form in ("fma", "gated"):
+            if form == "fma":
+                f = lambda: sr.sn_scan_fma_backward(ctx.handle, B, T, N, x["a"], x["s0"], so, gs_, None, da, db, d0, s)
+                nb = 20 * B * T * N + 8 * B * N
+            else:
+                f = lambda: sr.sn_scan_gated_backward(ctx.handle, B, T, N, x["a"], x["u"], x["s0"], so, gs_, None, da,
+                                                      db, d0, s)
+                nb = 24 * B * T * N + 8 * B * N
+            ms = time_form(torch, f, warmup, reps, s)
+            out[f"scan_{form}_backward"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
+                                            "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
+        del x, so, sf, gs_, da, db, d0
         for name in ("gla", "mamba2", "deltanet", "rwkv7_prefill", "rwkv7_decode"):
             c = synth.CONFIGS[name]
             x = synth.config_inputs(name, device=dev)

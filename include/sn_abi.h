@@ -84,6 +84,7 @@ typedef int32_t sn_status;
 #define SN_CAP_RECUR_RWKV7 (1u << 4)   /* sn_recur_rwkv7 */
 #define SN_CAP_DECODE      (1u << 5)   /* dedicated T == 1 decode kernels */
 #define SN_CAP_SCAN_LOOKBACK (1u << 6) /* chunked scan with look-back carries */
+#define SN_CAP_SCAN_BACKWARD (1u << 7) /* sn_scan_fma_backward, sn_scan_gated_backward */
 
 /* Decay layouts of sn_recur_diag. */
 #define SN_DECAY_PER_KEY  0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
@@ -185,6 +186,30 @@ sn_status sn_scan_fma(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
 sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
                         const float* a, const float* u, const float* s0,
                         float* s_final, float* s_out, void* stream);
+
+/* Reverse (adjoint) scan of the FMA form: the backward pass of sn_scan_fma
+ * (the pages' kernels pair a forward scan with a reverse scan, [P1] §8).
+ * Given the forward states and gs_t = dL/ds_t, gf = dL/ds_final:
+ *     g_{T-1} = gs_{T-1} + gf,    g_t = gs_t + a_{t+1} g_{t+1}  (one fma per step)
+ *     grad_a_t = g_t s_{t-1},     grad_b_t = g_t,     grad_s0 = a_0 g_0   (s_{-1} = s0)
+ *   a, s (forward states s_out), grad_s : (B, T, N), required
+ *   s0, grad_final : (B, N), NULL = zeros
+ *   grad_a, grad_b : (B, T, N), grad_s0 : (B, N), each may be NULL (not written)
+ * Runs T backwards per channel; N % 4 == 0 with 16-byte aligned tensors uses
+ * TMA, anything else plain loads.  Errors: SN_E_INVAL, SN_E_DEVICE. */
+sn_status sn_scan_fma_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
+                               const float* a, const float* s0, const float* s,
+                               const float* grad_s, const float* grad_final,
+                               float* grad_a, float* grad_b, float* grad_s0, void* stream);
+
+/* Reverse scan of the gated form (backward pass of sn_scan_gated): g as in
+ * sn_scan_fma_backward, then
+ *     grad_a_t = g_t (s_{t-1} - u_t),   grad_u_t = g_t (1 - a_t),   grad_s0 = a_0 g_0.
+ * u : (B, T, N) required; other arguments as sn_scan_fma_backward. */
+sn_status sn_scan_gated_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
+                                 const float* a, const float* u, const float* s0, const float* s,
+                                 const float* grad_s, const float* grad_final,
+                                 float* grad_a, float* grad_u, float* grad_s0, void* stream);
 
 /* ---------------------------------------------------------------- tier 2 */
 

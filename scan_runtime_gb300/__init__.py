@@ -97,6 +97,18 @@ class Context:
         _check(_abi.sn_scan_gated(self.handle, B, T, N, a, u, s0, sf, so, stream), "sn_scan_gated")
         return so, sf
 
+    def scan_backward(self, form, a, s, grad_s, *, s0=None, grad_final=None, u=None, stream=None):
+        """Reverse scan of `form` ("fma" or "gated"); returns (grad_a, grad_b|grad_u, grad_s0)."""
+        B, T, N = a.shape
+        ga, gb, g0 = self._out((B, T, N), True), self._out((B, T, N), True), self._out((B, N), True)
+        if form == "fma":
+            st = _abi.sn_scan_fma_backward(self.handle, B, T, N, a, s0, s, grad_s, grad_final, ga, gb, g0, stream)
+        else:
+            st = _abi.sn_scan_gated_backward(self.handle, B, T, N, a, u, s0, s, grad_s, grad_final, ga, gb, g0,
+                                             stream)
+        _check(st, f"sn_scan_{form}_backward")
+        return ga, gb, g0
+
     # ---------------------------------------------------------------- tier 2
     def recur_diag(self, q, k, v, d, S_in=None, *, H, G, decay_kind, scale, S_out=True, o=True, stream=None):
         B, T, _, dk = k.shape

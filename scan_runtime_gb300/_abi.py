@@ -20,7 +20,7 @@ SN_ABI_VERSION_MAJOR, SN_ABI_VERSION_MINOR, SN_ABI_VERSION_PATCH = 1, 0, 0
 SN_OK, SN_E_INVAL, SN_E_NOMEM, SN_E_IO, SN_E_FORMAT, SN_E_UNSUPPORTED, SN_E_DEVICE, SN_E_TIMEOUT = (
     0, -1, -2, -3, -4, -5, -6, -7)
 SN_CAP_SCAN_FMA, SN_CAP_SCAN_GATED, SN_CAP_RECUR_DIAG, SN_CAP_RECUR_DELTA = 1, 2, 4, 8
-SN_CAP_RECUR_RWKV7, SN_CAP_DECODE, SN_CAP_SCAN_LOOKBACK = 16, 32, 64
+SN_CAP_RECUR_RWKV7, SN_CAP_DECODE, SN_CAP_SCAN_LOOKBACK, SN_CAP_SCAN_BACKWARD = 16, 32, 64, 128
 SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD = 0, 1
 SN_OPT_SCAN_KERNEL, SN_OPT_WAIT_LIMIT_US, SN_OPT_DEBUG_POISON, SN_OPT_LOOKBACK_CHUNK, SN_OPT_RECUR_KERNEL = (
     1, 2, 3, 4, 5)
@@ -33,8 +33,8 @@ EXPORTS = (
     "sn_abi_version", "sn_abi_check", "sn_abi_caps", "sn_status_str",
     "sn_ctx_create", "sn_ctx_free", "sn_ctx_set_workspace", "sn_workspace_bytes",
     "sn_ctx_last_error", "sn_ctx_set_option", "sn_ctx_get_option",
-    "sn_scan_fma", "sn_scan_gated", "sn_recur_diag", "sn_recur_delta", "sn_recur_rwkv7",
-    "sn_scan_lookback_noalloc",
+    "sn_scan_fma", "sn_scan_gated", "sn_scan_fma_backward", "sn_scan_gated_backward",
+    "sn_recur_diag", "sn_recur_delta", "sn_recur_rwkv7", "sn_scan_lookback_noalloc",
 )
 SN_NOALLOC_MAX_TILES = 40960
 
@@ -67,6 +67,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "sn_ctx_get_option": ([p, i32, ctypes.POINTER(i32)], i32),
             "sn_scan_fma": ([p, i32, i32, i32, p, p, p, p, p, p], i32),
             "sn_scan_gated": ([p, i32, i32, i32, p, p, p, p, p, p], i32),
+            "sn_scan_fma_backward": ([p, i32, i32, i32] + [p] * 9, i32),
+            "sn_scan_gated_backward": ([p, i32, i32, i32] + [p] * 10, i32),
             "sn_recur_diag": ([p, i32, i32, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_delta": ([p, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_rwkv7": ([p, i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p], i32),
@@ -162,6 +164,18 @@ def sn_scan_fma(ctx, B, T, N, a, b, s0, s_final, s_out, stream=None) -> int:
 def sn_scan_gated(ctx, B, T, N, a, u, s0, s_final, s_out, stream=None) -> int:
     return load().sn_scan_gated(ctx, B, T, N, ptr(a), ptr(u), ptr(s0), ptr(s_final), ptr(s_out),
                                 stream_handle(stream))
+
+
+def sn_scan_fma_backward(ctx, B, T, N, a, s0, s, grad_s, grad_final, grad_a, grad_b, grad_s0, stream=None) -> int:
+    return load().sn_scan_fma_backward(ctx, B, T, N, ptr(a), ptr(s0), ptr(s), ptr(grad_s), ptr(grad_final),
+                                       ptr(grad_a), ptr(grad_b), ptr(grad_s0), stream_handle(stream))
+
+
+def sn_scan_gated_backward(ctx, B, T, N, a, u, s0, s, grad_s, grad_final, grad_a, grad_u, grad_s0,
+                           stream=None) -> int:
+    return load().sn_scan_gated_backward(ctx, B, T, N, ptr(a), ptr(u), ptr(s0), ptr(s), ptr(grad_s),
+                                         ptr(grad_final), ptr(grad_a), ptr(grad_u), ptr(grad_s0),
+                                         stream_handle(stream))
 
 
 def sn_recur_diag(ctx, B, T, H, G, dk, dv, decay_kind, scale, q, k, v, d, S_in, S_out, o, stream=None) -> int:

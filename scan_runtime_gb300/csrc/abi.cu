@@ -104,7 +104,7 @@ sn_status sn_abi_check(int32_t major) { return major == SN_ABI_VERSION_MAJOR ? S
 
 uint32_t sn_abi_caps(void) {
     return SN_CAP_SCAN_FMA | SN_CAP_SCAN_GATED | SN_CAP_RECUR_DIAG | SN_CAP_RECUR_DELTA | SN_CAP_RECUR_RWKV7 |
-           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK;
+           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK | SN_CAP_SCAN_BACKWARD;
 }
 
 const char* sn_status_str(sn_status s) {
@@ -294,6 +294,40 @@ sn_status sn_scan_fma(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* 
 sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* u,
                         const float* s0, float* s_final, float* s_out, void* stream) {
     return scan_common(ctx, B, T, N, a, u, s0, s_final, s_out, stream, true);
+}
+
+// ------------------------------------------------------------------ reverse scans
+static sn_status scan_backward_common(SnCtx* ctx, BwdArgs& x, bool gated, void* stream) {
+    if (ctx == nullptr || x.a == nullptr || x.s == nullptr || x.gs == nullptr || (gated && x.u == nullptr))
+        return SN_E_INVAL;
+    if (x.B <= 0 || x.T <= 0 || x.N <= 0) return SN_E_INVAL;
+    const int64_t elems = (int64_t)x.B * x.T * x.N;
+    if (elems > kMaxElems) return SN_E_INVAL;
+    const void* ptrs[9] = {x.a, x.u, x.s0, x.s, x.gs, x.gf, x.da, x.dbu, x.ds0};
+    for (const void* p : ptrs)
+        if (p != nullptr && !aligned(p, 4)) return SN_E_INVAL;
+    const int64_t big = elems * 4, small = (int64_t)x.B * x.N * 4;
+    const Buf bufs[9] = {{x.a, big, false}, {x.u, big, false},   {x.s0, small, false},
+                         {x.s, big, false}, {x.gs, big, false},  {x.gf, small, false},
+                         {x.da, big, true}, {x.dbu, big, true},  {x.ds0, small, true}};
+    if (any_bad_overlap(bufs, 9, nullptr, nullptr)) return SN_E_INVAL;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SN_E_DEVICE;
+    return from_cuda(launch_scan_backward(x, gated, ctx->dstatus, wait_ns(ctx), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sn_status sn_scan_fma_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* s0,
+                               const float* s, const float* grad_s, const float* grad_final, float* grad_a,
+                               float* grad_b, float* grad_s0, void* stream) {
+    BwdArgs x{B, T, N, a, nullptr, s0, s, grad_s, grad_final, grad_a, grad_b, grad_s0};
+    return scan_backward_common(ctx, x, false, stream);
+}
+
+sn_status sn_scan_gated_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* u,
+                                 const float* s0, const float* s, const float* grad_s, const float* grad_final,
+                                 float* grad_a, float* grad_u, float* grad_s0, void* stream) {
+    BwdArgs x{B, T, N, a, u, s0, s, grad_s, grad_final, grad_a, grad_u, grad_s0};
+    return scan_backward_common(ctx, x, true, stream);
 }
 
 // ------------------------------------------------------------------ matrix recurrences

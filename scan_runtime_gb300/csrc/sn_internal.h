@@ -67,7 +67,25 @@ struct ScanArgs {
     float* s_out;
 };
 
+// Reverse (adjoint) scan arguments: forward states s (B, T, N), direct
+// gradients gs (B, T, N), final-state gradient gf (B, N), outputs da, db|du
+// (B, T, N) and ds0 (B, N); u only for the gated form.
+struct BwdArgs {
+    int B, T, N;
+    const float* a;
+    const float* u;
+    const float* s0;
+    const float* s;
+    const float* gs;
+    const float* gf;
+    float* da;
+    float* dbu;
+    float* ds0;
+};
+
 // Launchers (return a CUDA error code; validation happens before).
+cudaError_t launch_scan_backward(const BwdArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
+                                 cudaStream_t stream);
 cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
                                    cudaStream_t stream);
 cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32_t epoch, int poison,

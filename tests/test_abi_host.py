@@ -78,9 +78,9 @@ def test_version_packing_and_check(abi):
 def test_caps_bits(abi):
     caps = abi.sn_abi_caps()
     for bit in (abi.SN_CAP_SCAN_FMA, abi.SN_CAP_SCAN_GATED, abi.SN_CAP_RECUR_DIAG, abi.SN_CAP_RECUR_DELTA,
-                abi.SN_CAP_RECUR_RWKV7, abi.SN_CAP_DECODE, abi.SN_CAP_SCAN_LOOKBACK):
+                abi.SN_CAP_RECUR_RWKV7, abi.SN_CAP_DECODE, abi.SN_CAP_SCAN_LOOKBACK, abi.SN_CAP_SCAN_BACKWARD):
         assert caps & bit
-    assert caps & ~0x7F == 0            # no undocumented bits set
+    assert caps & ~0xFF == 0            # no undocumented bits set
 
 
 def test_status_strings(abi):
@@ -97,6 +97,8 @@ def test_null_context_is_rejected_before_any_device_work(abi):
     assert abi.sn_recur_diag(None, 1, 1, 1, 1, 64, 64, 0, 1.0, x, x, x, x, None, None, x, 0) == E
     assert abi.sn_recur_delta(None, 1, 1, 1, 64, 64, 1.0, x, x, x, x, None, None, x, 0) == E
     assert abi.sn_recur_rwkv7(None, 1, 1, 1, 64, 64, x, x, x, x, None, None, x, 0) == E
+    assert abi.sn_scan_fma_backward(None, 1, 1, 4, x, None, x, x, None, x, x, x, 0) == E
+    assert abi.sn_scan_gated_backward(None, 1, 1, 4, x, x, None, x, x, None, x, x, x, 0) == E
     assert abi.sn_ctx_set_option(None, abi.SN_OPT_SCAN_KERNEL, 0) == E
     assert abi.sn_ctx_get_option(None, abi.SN_OPT_SCAN_KERNEL)[0] == E
     assert abi.sn_ctx_last_error(None) == E
