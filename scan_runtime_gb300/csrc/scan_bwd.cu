@@ -9,8 +9,8 @@
 //   gated: da_t = g_t (s_{t-1} - u_t),   du_t = g_t (1 - a_t)
 //   ds0 = a_0 g_0                        (s_{-1} = s0)
 // The kernel runs T backwards per channel, like the forward sequential
-// kernel: a producer warp streams [32 x 64] tiles of a, gs, the forward
-// states shifted one step (s_{t-1}) and u through a 3-stage TMA ring, from
+// kernel: a producer warp streams [32 x 32] tiles of a, gs, the forward
+// states shifted one step (s_{t-1}) and u through a 3- or 4-stage TMA ring, from
 // the end of the sequence (the last tile may start at a negative row, which
 // TMA fills with zeros); the consumer warp carries g through the steps and
 // writes da and db|du with streaming stores.  Every operation is one explicit
@@ -22,10 +22,13 @@
 namespace sn {
 
 namespace {
-constexpr int SB_NC = 64;                    // channels per CTA
+constexpr int SB_NC = 32;                    // channels per CTA (one per consumer lane)
 constexpr int SB_TS = 32;                    // time steps per stage
-constexpr int SB_STAGES = 3;
-constexpr int SB_THREADS = 64;               // warp 0 consumes (2 ch/lane), warp 1 produces
+// Stages per form: 48 KB of ring per CTA either way, so four CTAs fit per SM
+// and the grid (32-channel CTAs) runs in one wave.
+template <bool GATED>
+constexpr int sb_stages() { return GATED ? 3 : 4; }
+constexpr int SB_THREADS = 64;               // warp 0 consumes, warp 1 produces
 constexpr uint32_t SB_TILE = SB_TS * SB_NC;  // floats per tensor per stage
 
 template <bool GATED>
@@ -33,7 +36,7 @@ constexpr int sb_tensors() { return GATED ? 4 : 3; }   // a, gs, s_{t-1}, (u)
 template <bool GATED>
 constexpr uint32_t sb_stage_bytes() { return sb_tensors<GATED>() * SB_TILE * 4; }
 template <bool GATED>
-constexpr size_t sb_smem() { return SB_STAGES * sb_stage_bytes<GATED>() + 2 * SB_STAGES * 8 + 16; }
+constexpr size_t sb_smem() { return sb_stages<GATED>() * sb_stage_bytes<GATED>() + 2 * sb_stages<GATED>() * 8 + 16; }
 }  // namespace
 
 template <bool GATED>
@@ -43,6 +46,7 @@ scan_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ 
              const float* __restrict__ s0, const float* __restrict__ gf, float* __restrict__ da,
              float* __restrict__ dbu, float* __restrict__ ds0, SnDevStatus* st, uint64_t wait_ns) {
     constexpr int NT = sb_tensors<GATED>();
+    constexpr int SB_STAGES = sb_stages<GATED>();
     extern __shared__ __align__(128) unsigned char smem[];
     float* tiles = reinterpret_cast<float*>(smem);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SB_STAGES * sb_stage_bytes<GATED>());
@@ -95,20 +99,35 @@ scan_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ 
             ctl[1] = k;
         }
     } else {
-        const int c = n0 + 2 * lane;                  // this lane's two channels
-        const bool live = c < N;                      // N % 4 == 0 here, so c + 1 < N too
-        float gf0 = 0.f, gf1 = 0.f, s00 = 0.f, s01 = 0.f;
+        const int c = n0 + lane;                      // this lane's channel
+        const bool live = c < N;
+        float gfv = 0.f, s0v = 0.f;
         if (live) {
-            if (gf != nullptr) {
-                gf0 = gf[(size_t)bi * N + c];
-                gf1 = gf[(size_t)bi * N + c + 1];
-            }
-            if (s0 != nullptr) {
-                s00 = s0[(size_t)bi * N + c];
-                s01 = s0[(size_t)bi * N + c + 1];
-            }
+            if (gf != nullptr) gfv = gf[(size_t)bi * N + c];
+            if (s0 != nullptr) s0v = s0[(size_t)bi * N + c];
         }
-        float g0 = 0.f, g1 = 0.f, an0 = 0.f, an1 = 0.f;   // running adjoint, a_{t+1}
+        float g = 0.f, an = 0.f;                      // running adjoint, a_{t+1}
+        auto row = [&](const float* A, const float* Gs, const float* Sp, const float* U, int i, int t, bool edge) {
+            const float av = A[i * SB_NC], gv = Gs[i * SB_NC];
+            float sp = Sp[i * SB_NC];
+            if (edge && t == 0) sp = s0v;
+            if (edge && t == T - 1) g = __fadd_rn(gv, gfv);
+            else g = __fmaf_rn(an, g, gv);
+            float oa, ob;
+            if constexpr (GATED) {
+                oa = __fmul_rn(g, __fsub_rn(sp, U[i * SB_NC]));
+                ob = __fmul_rn(g, __fsub_rn(1.0f, av));
+            } else {
+                oa = __fmul_rn(g, sp);
+                ob = g;
+            }
+            if (live) {
+                const size_t off = ((size_t)bi * T + t) * N + c;
+                if (da != nullptr) st_cs(da + off, oa);
+                if (dbu != nullptr) st_cs(dbu + off, ob);
+            }
+            an = av;
+        };
         for (int k = 0; k < nst; ++k) {
             const int slot = k % SB_STAGES;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (k / SB_STAGES) & 1, wait_ns));
@@ -119,50 +138,23 @@ scan_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ 
                 }
                 break;
             }
-            const float* A = tiles + (size_t)slot * NT * SB_TILE + 2 * lane;
+            const float* A = tiles + (size_t)slot * NT * SB_TILE + lane;
             const float* Gs = A + SB_TILE;
             const float* Sp = A + 2 * SB_TILE;
             const float* U = A + 3 * SB_TILE;
             const int r0 = T - (k + 1) * SB_TS;
-            const int ilo = max(0, -r0);
-            for (int i = SB_TS - 1; i >= ilo; --i) {
-                const int t = r0 + i;
-                const float2 av = *reinterpret_cast<const float2*>(A + i * SB_NC);
-                const float2 gv = *reinterpret_cast<const float2*>(Gs + i * SB_NC);
-                float2 sp = *reinterpret_cast<const float2*>(Sp + i * SB_NC);
-                if (t == 0) sp = make_float2(s00, s01);
-                if (t == T - 1) {
-                    g0 = __fadd_rn(gv.x, gf0);
-                    g1 = __fadd_rn(gv.y, gf1);
-                } else {
-                    g0 = __fmaf_rn(an0, g0, gv.x);
-                    g1 = __fmaf_rn(an1, g1, gv.y);
-                }
-                float2 oa, ob;
-                if constexpr (GATED) {
-                    const float2 uv = *reinterpret_cast<const float2*>(U + i * SB_NC);
-                    oa = make_float2(__fmul_rn(g0, __fsub_rn(sp.x, uv.x)), __fmul_rn(g1, __fsub_rn(sp.y, uv.y)));
-                    ob = make_float2(__fmul_rn(g0, __fsub_rn(1.0f, av.x)), __fmul_rn(g1, __fsub_rn(1.0f, av.y)));
-                } else {
-                    oa = make_float2(__fmul_rn(g0, sp.x), __fmul_rn(g1, sp.y));
-                    ob = make_float2(g0, g1);
-                }
-                if (live) {
-                    const size_t off = ((size_t)bi * T + t) * N + c;
-                    if (da != nullptr) st_cs(reinterpret_cast<float2*>(da + off), oa);
-                    if (dbu != nullptr) st_cs(reinterpret_cast<float2*>(dbu + off), ob);
-                }
-                an0 = av.x;
-                an1 = av.y;
+            if (k > 0 && r0 >= 1) {
+                // interior stage: neither t = T-1 nor t = 0 occurs, all rows valid
+#pragma unroll
+                for (int i = SB_TS - 1; i >= 0; --i) row(A, Gs, Sp, U, i, r0 + i, false);
+            } else {
+                for (int i = SB_TS - 1; i >= max(0, -r0); --i) row(A, Gs, Sp, U, i, r0 + i, true);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             ++consumed;
         }
-        if (ds0 != nullptr && live && consumed == nst) {
-            ds0[(size_t)bi * N + c] = __fmul_rn(an0, g0);        // a_0 g_0
-            ds0[(size_t)bi * N + c + 1] = __fmul_rn(an1, g1);
-        }
+        if (ds0 != nullptr && live && consumed == nst) ds0[(size_t)bi * N + c] = __fmul_rn(an, g);   // a_0 g_0
     }
     __syncthreads();
     if (warp == 0 && lane == 0 && ctl[0]) {
@@ -205,8 +197,7 @@ scan_bwd_ldg(int T, int N, const float* __restrict__ a, const float* __restrict_
 cudaError_t launch_scan_backward(const BwdArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
                                  cudaStream_t stream) {
     auto al16 = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    const bool tma = (x.N % 4 == 0) && al16(x.a) && al16(x.gs) && al16(x.s) && al16(x.u) && al16(x.da) &&
-                     al16(x.dbu);
+    const bool tma = (x.N % 4 == 0) && al16(x.a) && al16(x.gs) && al16(x.s) && al16(x.u);
     if (tma) {
         CUtensorMap ma, mg, ms, mu;
         if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, SB_NC, SB_TS) ||
