@@ -8,8 +8,9 @@
 //    channels' state through all T with one fused multiply-add per step, so the
 //    result has the bits of the single-precision definition at every t and is
 //    invariant under any segment split ("SunnyNet 工程化实录" §4).  The TMA
-//    variant streams [32 x 64] tiles of a and b through a 4-stage shared-memory
-//    ring fed by a producer warp; s_t leaves as coalesced streaming stores.
+//    variant streams [32 x S1_NC] tiles of a and b through an S1_STAGES-deep
+//    shared-memory ring fed by a producer warp; s_t leaves as coalesced
+//    streaming stores.
 //    The LDG variant serves layouts TMA cannot describe (N % 4 != 0 or
 //    unaligned base pointers).
 //  * the chunked look-back kernel lives in scan_lookback.cu.
@@ -22,12 +23,22 @@ namespace sn {
 
 // ============================================================ sequential (TMA)
 namespace {
-constexpr int S1_NC = 64;                         // channels per CTA
+// Compile-time shape of the TMA kernel: S1_VEC channels per consumer lane
+// (S1_NC = 32 * S1_VEC per CTA), S1_TS steps per stage, S1_STAGES stages.
+#ifndef SN_SEQ_VEC
+#define SN_SEQ_VEC 2
+#endif
+#ifndef SN_SEQ_STAGES
+#define SN_SEQ_STAGES 4
+#endif
+constexpr int S1_VEC = SN_SEQ_VEC;
+constexpr int S1_NC = 32 * S1_VEC;                // channels per CTA
 constexpr int S1_TS = 32;                         // time steps per stage
-constexpr int S1_STAGES = 4;
-constexpr int S1_THREADS = 64;                    // warp 0 consumes (2 ch/lane), warp 1 produces
+constexpr int S1_STAGES = SN_SEQ_STAGES;
+constexpr int S1_THREADS = 64;                    // warp 0 consumes, warp 1 produces
 constexpr uint32_t S1_TILE = S1_TS * S1_NC;       // floats per tensor per stage
 constexpr uint32_t S1_STAGE_BYTES = 2 * S1_TILE * 4;
+static_assert(S1_VEC == 1 || S1_VEC == 2, "one or two channels per lane");
 constexpr size_t S1_SMEM = S1_STAGES * S1_STAGE_BYTES + 2 * S1_STAGES * 8 + 16;
 
 }  // namespace
@@ -86,13 +97,28 @@ scan_seq_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ 
             ctl[1] = k;
         }
     } else {
-        const int c = n0 + 2 * lane;                  // this lane's two channels
-        const bool live = c < N;                      // N % 4 == 0 here, so c + 1 < N too
-        float x0 = 0.0f, x1 = 0.0f;
-        if (s0 != nullptr && live) {
-            x0 = s0[(size_t)bi * N + c];
-            x1 = s0[(size_t)bi * N + c + 1];
-        }
+        const int c = n0 + S1_VEC * lane;             // this lane's first channel
+        const bool live = c < N;                      // N % 4 == 0 here, so a live lane owns all S1_VEC
+        float x[S1_VEC];
+#pragma unroll
+        for (int v = 0; v < S1_VEC; ++v) x[v] = (s0 != nullptr && live) ? s0[(size_t)bi * N + c + v] : 0.0f;
+        auto row = [&](const float* A, const float* Bv, float* out, int i) {
+            float av[S1_VEC], bv[S1_VEC];
+            if constexpr (S1_VEC == 2) {
+                const float2 a2 = *reinterpret_cast<const float2*>(A + i * S1_NC);
+                const float2 b2 = *reinterpret_cast<const float2*>(Bv + i * S1_NC);
+                av[0] = a2.x; av[1] = a2.y; bv[0] = b2.x; bv[1] = b2.y;
+            } else {
+                av[0] = A[i * S1_NC];
+                bv[0] = Bv[i * S1_NC];
+            }
+#pragma unroll
+            for (int v = 0; v < S1_VEC; ++v) x[v] = __fmaf_rn(av[v], x[v], inj<GATED>(av[v], bv[v]));
+            if (out) {
+                if constexpr (S1_VEC == 2) st_cs(reinterpret_cast<float2*>(out + (size_t)i * N), make_float2(x[0], x[1]));
+                else st_cs(out + (size_t)i * N, x[0]);
+            }
+        };
         for (int k = 0; k < nst; ++k) {
             const int slot = k % S1_STAGES;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (k / S1_STAGES) & 1, wait_ns));
@@ -103,36 +129,24 @@ scan_seq_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ 
                 }
                 break;
             }
-            const float* A = tiles + slot * 2 * S1_TILE + 2 * lane;
+            const float* A = tiles + slot * 2 * S1_TILE + S1_VEC * lane;
             const float* Bv = A + S1_TILE;
             const int t0 = k * S1_TS;
             const int tn = min(S1_TS, T - t0);
             float* out = (s_out != nullptr && live) ? s_out + ((size_t)bi * T + t0) * N + c : nullptr;
             if (tn == S1_TS) {
 #pragma unroll
-                for (int i = 0; i < S1_TS; ++i) {
-                    const float2 av = *reinterpret_cast<const float2*>(A + i * S1_NC);
-                    const float2 bv = *reinterpret_cast<const float2*>(Bv + i * S1_NC);
-                    x0 = __fmaf_rn(av.x, x0, inj<GATED>(av.x, bv.x));
-                    x1 = __fmaf_rn(av.y, x1, inj<GATED>(av.y, bv.y));
-                    if (out) st_cs(reinterpret_cast<float2*>(out + (size_t)i * N), make_float2(x0, x1));
-                }
+                for (int i = 0; i < S1_TS; ++i) row(A, Bv, out, i);
             } else {
-                for (int i = 0; i < tn; ++i) {
-                    const float2 av = *reinterpret_cast<const float2*>(A + i * S1_NC);
-                    const float2 bv = *reinterpret_cast<const float2*>(Bv + i * S1_NC);
-                    x0 = __fmaf_rn(av.x, x0, inj<GATED>(av.x, bv.x));
-                    x1 = __fmaf_rn(av.y, x1, inj<GATED>(av.y, bv.y));
-                    if (out) st_cs(reinterpret_cast<float2*>(out + (size_t)i * N), make_float2(x0, x1));
-                }
+                for (int i = 0; i < tn; ++i) row(A, Bv, out, i);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             ++consumed;
         }
         if (s_final != nullptr && live && consumed == nst) {
-            s_final[(size_t)bi * N + c] = x0;
-            s_final[(size_t)bi * N + c + 1] = x1;
+#pragma unroll
+            for (int v = 0; v < S1_VEC; ++v) s_final[(size_t)bi * N + c + v] = x[v];
         }
     }
     // After an abort, wait (bounded) for copies still in flight into this
