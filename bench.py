@@ -194,34 +194,29 @@ def cpu_oracle_scan(a, b, u, s0, threads):
     return time.perf_counter() - t0
 
 
-def cpu_sample_inputs(T_sample):
-    """A bounded sample of the large scan workload: all B and N, the first
-    T_sample steps (same distributions, CPU-generated)."""
-    x = synth.scan_inputs(SCAN["B"], T_sample, SCAN["N"], large=True)
-    return (x["a"].numpy(), x["b"].numpy(), x["u"].numpy(), x["s0"].numpy())
-
-
 def run_reference(args):
-    """The reference arm: the CPU oracle as it stands, on this arm's workload."""
+    """The reference arm: the CPU oracle as it stands, on this arm's workload
+    (the full B=8 T=8192 N=2048 scan, both forms, inputs drawn on the CPU)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    T_s = 1024
-    a, b, u, s0 = cpu_sample_inputs(T_s)
-    threads = min(SCAN["B"], os.cpu_count() or 1)
+    x = synth.config_inputs("scan_large")
+    a, b, u, s0 = (x[n].numpy() for n in ("a", "b", "u", "s0"))
+    B, T, N = a.shape
+    threads = min(B, os.cpu_count() or 1)
     for _ in range(args.warmup):
         cpu_oracle_scan(a, b, u, s0, threads)
     times = [cpu_oracle_scan(a, b, u, s0, threads) for _ in range(args.steps)]
-    per_step_bytes = 2 * scan_bytes(SCAN["B"], T_s, SCAN["N"])
+    per_step_bytes = 2 * scan_bytes(B, T, N)
     total = sum(times)
     value = args.steps * per_step_bytes / total / GB
-    sample = f"B=8 T={T_s} N=2048 (first {T_s} of 8192 steps), both forms, fp64 oracle"
+    sample = f"the full workload B=8 T=8192 N=2048 per step, both forms, fp64 oracle, batch rows on {threads} threads"
     line = {
         "impl": "reference", "metric": "recurrence_scan_GBps", "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "scan_large B=8 T=8192 N=2048, FMA + gated forms", "sample": sample},
+        "config": {"workload": "scan_large B=8 T=8192 N=2048, FMA + gated forms"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -392,70 +387,53 @@ def run_ours(args):
     value = whole_job_gbps(step_bytes, args.steps, world, ms_total)
     achieved = per_form_bytes / (avg_launch_ms / 1e3) / GB
 
-    # end to end through the public API: pinned host inputs in, s_t out, every step
+    # end to end through the public API (Context.scan_host): pinned host inputs
+    # in, both forms' s_t and s_final out, every step; wall clock per step
     e2e = None
     if not args.no_e2e:
-        ha = torch.empty((B, T, N), pin_memory=True)
-        hb = torch.empty((B, T, N), pin_memory=True)
-        hu = torch.empty((B, T, N), pin_memory=True)
-        hs0 = torch.empty((B, N), pin_memory=True)
-        ha.copy_(x["a"])
-        hb.copy_(x["b"])
-        hu.copy_(x["u"])
-        hs0.copy_(x["s0"])
-        hof = torch.empty((B, T, N), pin_memory=True)
-        hog = torch.empty((B, T, N), pin_memory=True)
-        hff = torch.empty((B, N), pin_memory=True)
-        hfg = torch.empty((B, N), pin_memory=True)
-        da, db, du, ds0 = (torch.empty_like(t, device=dev) for t in (ha, hb, hu, hs0))
+        host = {n: torch.empty_like(x[n], device="cpu").pin_memory() for n in ("a", "b", "u", "s0")}
+        for n in host:
+            host[n].copy_(x[n])
+        hout = {f: (torch.empty((B, T, N), pin_memory=True), torch.empty((B, N), pin_memory=True))
+                for f in ("fma", "gated")}
 
         def e2e_step():
-            with torch.cuda.stream(stream):
-                da.copy_(ha, non_blocking=True)
-                db.copy_(hb, non_blocking=True)
-                du.copy_(hu, non_blocking=True)
-                ds0.copy_(hs0, non_blocking=True)
-                s1 = sr.sn_scan_fma(h, B, T, N, da, db, ds0, sf_f, so_f, stream)
-                s2 = sr.sn_scan_gated(h, B, T, N, da, du, ds0, sf_g, so_g, stream)
-                hof.copy_(so_f, non_blocking=True)
-                hog.copy_(so_g, non_blocking=True)
-                hff.copy_(sf_f, non_blocking=True)
-                hfg.copy_(sf_g, non_blocking=True)
-            if s1 != sr.SN_OK or s2 != sr.SN_OK:
-                raise RuntimeError("scan failed in e2e step")
+            ctx.scan_host(host["a"], host["b"], host["u"], host["s0"], out=hout, rows_per_chunk=1, nstreams=3)
 
         n_e2e = max(3, min(args.steps, 20))
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
         for _ in range(n_e2e):
             e2e_step()
-        e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dev)
         h2d = 3 * B * T * N * 4 + B * N * 4
         d2h = 2 * B * T * N * 4 + 2 * B * N * 4
-        e2e = {"value": round(step_bytes / (e2e_ms / 1e3) / GB, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)}
-        del ha, hb, hu, hof, hog, da, db, du
+        e2e = {"value": round(whole_job_gbps(step_bytes, 1, world, e2e_ms), 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+               "api": "Context.scan_host (3 streams, one batch row per chunk)"}
+        del host, hout
 
     forms = None
     if not args.no_forms:
         forms = bench_forms(torch, sr, ctx, dev, stream, fp32_peak, hbm_peak)
 
-    # CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N=1 only)
+    # CPU baseline: the fp64 oracle on this run's own inputs (the full
+    # workload, copied to the host), rank 0 at N=1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        T_s = 1024
-        a, b, u, s0 = cpu_sample_inputs(T_s)
+        a, b, u, s0 = (x[n].cpu().numpy() for n in ("a", "b", "u", "s0"))
         threads = min(B, os.cpu_count() or 1)
         secs = cpu_oracle_scan(a, b, u, s0, threads)
-        cpu = {"value": round(2 * scan_bytes(B, T_s, N) / secs / GB, 4), "unit": "GB/s", "cores": threads,
+        cpu = {"value": round(2 * scan_bytes(B, T, N) / secs / GB, 4), "unit": "GB/s", "cores": threads,
                "kind": "oracle",
-               "sample": f"B=8 T={T_s} N=2048 (first {T_s} of 8192 steps), both forms, fp64 oracle, "
-                         f"{secs:.2f} s"}
+               "sample": f"the full workload B=8 T=8192 N=2048 (this run's inputs), both forms, fp64 oracle, "
+                         f"batch rows on {threads} threads, {secs:.2f} s"}
+        del a, b, u, s0
 
     assert ctx.last_error() == sr.SN_OK
     clocks = clk.summary()

@@ -7,7 +7,9 @@
 // bits, int32 status codes and dimensions).
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include <cudaTypedefs.h>
 
@@ -94,6 +96,40 @@ bool encode_tiled(CUtensorMap* map, int rank, const void* base, const uint64_t* 
     return r == CUDA_SUCCESS;
 }
 bool lookback_supported(const ScanArgs& x);
+
+namespace {
+std::mutex g_attr_mutex;
+std::map<std::pair<const void*, int>, int> g_attr;     // (kernel, device) -> occupancy (0 = attr only)
+}  // namespace
+
+cudaError_t set_smem_attr_once(const void* kern, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    const auto key = std::make_pair(kern, dev);
+    if (g_attr.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) g_attr[key] = 0;
+    return e;
+}
+
+cudaError_t occupancy_once(const void* kern, int threads, size_t smem, int* out) {
+    cudaError_t e = set_smem_attr_once(kern, smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    int& occ = g_attr[std::make_pair(kern, dev)];
+    if (occ == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+    }
+    *out = occ;
+    return cudaSuccess;
+}
 }  // namespace sn
 
 extern "C" {

@@ -129,13 +129,8 @@ bool recur_decode_supported(const RecurArgs& x) {
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream) {
     (void)sm_count;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e =
-            cudaFuncSetAttribute(recur_decode_rwkv7, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    cudaError_t e = set_smem_attr_once((const void*)recur_decode_rwkv7, DEC_SMEM);
+    if (e != cudaSuccess) return e;
     const int BH = x.B * x.H;
     const int grid = (BH + DEC_TILES - 1) / DEC_TILES;
     recur_decode_rwkv7<<<grid, DEC_THREADS, DEC_SMEM, stream>>>(BH, x.q, x.k, x.v, x.g, x.S_in, x.S_out, x.o, st,

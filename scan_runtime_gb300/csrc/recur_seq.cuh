@@ -406,12 +406,8 @@ cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaS
     }
     SeqParams p{x.T, x.H, x.G, x.dk, x.dv, x.scale, x.g, x.S_in, x.S_out, x.o != nullptr ? 1 : 0, st, wait_ns};
     auto kern = recur_seq<KIND, DK, R, C, W>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    cudaError_t e = set_smem_attr_once((const void*)kern, L::smem);
+    if (e != cudaSuccess) return e;
     dim3 grid(x.dv / JT, x.H, x.B);
     kern<<<grid, (W + 1) * 32, L::smem, stream>>>(mq, mk, mg, mv, mo, p);
     return cudaGetLastError();

@@ -201,12 +201,8 @@ cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* s
             !make_scan_map(&mb, x.b, x.B, x.T, x.N, S1_NC, S1_TS))
             return cudaErrorInvalidValue;
         auto kern = gated ? scan_seq_tma<true> : scan_seq_tma<false>;
-        static bool attr_set[2] = {false, false};
-        if (!attr_set[gated]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S1_SMEM);
-            if (e != cudaSuccess) return e;
-            attr_set[gated] = true;
-        }
+        cudaError_t e = set_smem_attr_once((const void*)kern, S1_SMEM);
+        if (e != cudaSuccess) return e;
         dim3 grid((x.N + S1_NC - 1) / S1_NC, x.B);
         kern<<<grid, S1_THREADS, S1_SMEM, stream>>>(ma, mb, x.T, x.N, x.s0, x.s_final, x.s_out, st, wait_ns);
     } else {

@@ -211,12 +211,8 @@ cudaError_t launch_scan_backward(const BwdArgs& x, bool gated, SnDevStatus* st, 
         }
         auto kern = gated ? scan_bwd_tma<true> : scan_bwd_tma<false>;
         const size_t smem = gated ? sb_smem<true>() : sb_smem<false>();
-        static bool attr_set[2] = {false, false};
-        if (!attr_set[gated]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            attr_set[gated] = true;
-        }
+        cudaError_t e = set_smem_attr_once((const void*)kern, smem);
+        if (e != cudaSuccess) return e;
         dim3 grid((x.N + SB_NC - 1) / SB_NC, x.B);
         kern<<<grid, SB_THREADS, smem, stream>>>(ma, mg, ms, mu, x.T, x.N, x.s0, x.gf, x.da, x.dbu, x.ds0, st,
                                                  wait_ns);

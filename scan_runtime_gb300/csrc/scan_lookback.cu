@@ -326,17 +326,10 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32
     p.wait_ns = wait_ns;
 
     auto kern = gated ? scan_lookback<true> : scan_lookback<false>;
-    static bool attr_set[2] = {false, false};
-    static int occ[2] = {0, 0};
-    if (!attr_set[gated]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LB_SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[gated], kern, LB_THREADS, LB_SMEM);
-        if (e != cudaSuccess) return e;
-        if (occ[gated] < 1) return cudaErrorInvalidConfiguration;
-        attr_set[gated] = true;
-    }
-    const int grid = std::min<int64_t>(tiles, (int64_t)occ[gated] * sm_count);
+    int occ = 0;
+    cudaError_t oe = occupancy_once((const void*)kern, LB_THREADS, LB_SMEM, &occ);
+    if (oe != cudaSuccess) return oe;
+    const int grid = std::min<int64_t>(tiles, (int64_t)occ * sm_count);
     void* args[] = {(void*)&ma, (void*)&mb, (void*)&p};
     cudaError_t e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(LB_THREADS), args, LB_SMEM,
                                                 stream);

@@ -282,3 +282,17 @@ def test_full_size_lookback_sampled_and_split(sr, ctx, large_inputs, form):
     p2, f2 = fn(ga[:, split:].contiguous(), gr[:, split:].contiguous(), f1)
     torch.cuda.synchronize()
     assert torch.equal(torch.cat([p1, p2], 1), so) and torch.equal(f2, sf)
+
+
+def test_scan_host_pipeline_matches_device_path(ctx):
+    """Context.scan_host (host buffers streamed through the GPU in batch-row
+    chunks on three streams) returns the device path's bits for both forms."""
+    B, T, N = 5, 300, 192
+    a, b, u, s0 = _inputs(B, T, N, 12)
+    outs = ctx.scan_host(a.pin_memory(), b.pin_memory(), u.pin_memory(), s0.pin_memory(), rows_per_chunk=2)
+    for form, rhs in (("fma", b), ("gated", u)):
+        so, sf = _run(ctx, form, a, rhs, s0)
+        assert np.array_equal(outs[form][0].numpy(), so) and np.array_equal(outs[form][1].numpy(), sf)
+    only = ctx.scan_host(a, u=u, s0=None)
+    r32, _ = _ref("gated", a, u, None, "f32")
+    assert set(only) == {"gated"} and np.array_equal(only["gated"][0].numpy(), r32)
