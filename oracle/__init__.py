@@ -37,6 +37,8 @@ _lib = None
 
 DECAY_PER_KEY = 0
 DECAY_PER_HEAD = 1
+DECAY_PER_KEY_GATED = 2
+DECAY_PER_HEAD_GATED = 3
 
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
@@ -160,12 +162,13 @@ def scan_backward(kind, a, s, s0=None, gs=None, gf=None, u=None, prec="f64"):
 
 def recur_diag(q, k, v, d, S0=None, *, H, G, decay_kind, scale, prec="f64"):
     """Diagonal-decay recurrence; q,k (B,T,G,dk), v (B,T,H,dv), d per key
-    (B,T,H,dk) or per head (B,T,H).  Returns ``(o (B,T,H,dv), S (B,H,dk,dv))``."""
+    (B,T,H,dk) or per head (B,T,H); the gated kinds scale the injection by
+    (1 - d).  Returns ``(o (B,T,H,dv), S (B,H,dk,dv))``."""
     q, k, v, d = _f32(q), _f32(k), _f32(v), _f32(d)
     B, T, G_, dk = k.shape
     dv = v.shape[3]
     assert G_ == G and q.shape == k.shape and v.shape == (B, T, H, dv)
-    assert d.shape == ((B, T, H, dk) if decay_kind == DECAY_PER_KEY else (B, T, H))
+    assert d.shape == ((B, T, H, dk) if decay_kind in (DECAY_PER_KEY, DECAY_PER_KEY_GATED) else (B, T, H))
     dt = np.float64 if prec == "f64" else np.float32
     S0 = _state(S0, prec, (B, H, dk, dv))
     o = np.empty((B, T, H, dv), dt)

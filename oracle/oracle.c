@@ -38,8 +38,10 @@
 typedef int32_t i32;
 typedef int64_t i64;
 
-#define ORC_DECAY_PER_KEY  0
-#define ORC_DECAY_PER_HEAD 1
+#define ORC_DECAY_PER_KEY        0
+#define ORC_DECAY_PER_HEAD       1
+#define ORC_DECAY_PER_KEY_GATED  2
+#define ORC_DECAY_PER_HEAD_GATED 3
 
 /* ------------------------------------------------------------------------ */
 /* Tier 1: per-channel first-order scans.                                    */
@@ -125,7 +127,10 @@ void orc_scan_gated_f32(i32 B, i32 T, i32 N, const float* a, const float* u,
 /* ------------------------------------------------------------------------ */
 
 /* Diagonal decay (GLA per-key decay, Mamba-2 per-head scalar decay):
- *   S_t = diag(d_t) S_{t-1} + k_t v_t^T,   o_t = scale * S_t^T q_t.
+ *   S_t = diag(d_t) S_{t-1} + k_t v_t^T,   o_t = scale * S_t^T q_t,
+ * and its gated (convex-combination) form, the matrix-valued association
+ * memory of [P2] §8 and HGRN2's structure ([P2] §4):
+ *   S_t = diag(p_t) S_{t-1} + diag(1 - p_t) k_t v_t^T     (decay kinds 2, 3).
  * [P1] §4.3 (GLA: decay on the key dimension, readout S^T q with scale),
  * [P1] §4.1 and [P2] §3 (Mamba-2: scalar dA per head, B_g shared by the heads
  * of a group, dt folded into the injected value by the caller).
@@ -148,11 +153,13 @@ void orc_recur_diag_f64(i32 B, i32 T, i32 H, i32 G, i32 dk, i32 dv,
                 const float* kt = k + ((bi * T + t) * G + g) * dk;
                 const float* vt = v + ((bi * T + t) * H + h) * dv;
                 for (i64 i = 0; i < dk; ++i) {
-                    double di = (decay_kind == ORC_DECAY_PER_KEY)
-                                    ? (double)d[((bi * T + t) * H + h) * dk + i]
-                                    : (double)d[(bi * T + t) * H + h];
+                    int per_key = (decay_kind == ORC_DECAY_PER_KEY || decay_kind == ORC_DECAY_PER_KEY_GATED);
+                    int gated = (decay_kind == ORC_DECAY_PER_KEY_GATED || decay_kind == ORC_DECAY_PER_HEAD_GATED);
+                    double di = per_key ? (double)d[((bi * T + t) * H + h) * dk + i]
+                                        : (double)d[(bi * T + t) * H + h];
+                    double ki = gated ? (1.0 - di) * (double)kt[i] : (double)kt[i];
                     for (i64 j = 0; j < dv; ++j)
-                        S[i * dv + j] = di * S[i * dv + j] + (double)kt[i] * (double)vt[j];
+                        S[i * dv + j] = di * S[i * dv + j] + ki * (double)vt[j];
                 }
                 if (o) {
                     for (i64 j = 0; j < dv; ++j) {
@@ -169,7 +176,8 @@ void orc_recur_diag_f64(i32 B, i32 T, i32 H, i32 G, i32 dk, i32 dv,
 }
 
 /* Float diagonal decay.  Canonical update order: the injection k_i * v_j is
- * rounded first, then one fused multiply-add applies the decay,
+ * rounded first (gated kinds: ((1 - p_i) * k_i) * v_j, each product rounded),
+ * then one fused multiply-add applies the decay,
  * S_ij = fma(d_i, S_ij, k_i * v_j) -- exactly the FMA-form scan of [P1] §2.1
  * with a = d_i and b = k_i * v_j, which is the elementwise decomposition that
  * [P1] §4.3 states for GLA.  The readout sums over i in increasing order. */
@@ -191,11 +199,12 @@ void orc_recur_diag_f32(i32 B, i32 T, i32 H, i32 G, i32 dk, i32 dv,
                 const float* kt = k + ((bi * T + t) * G + g) * dk;
                 const float* vt = v + ((bi * T + t) * H + h) * dv;
                 for (i64 i = 0; i < dk; ++i) {
-                    float di = (decay_kind == ORC_DECAY_PER_KEY)
-                                   ? d[((bi * T + t) * H + h) * dk + i]
-                                   : d[(bi * T + t) * H + h];
+                    int per_key = (decay_kind == ORC_DECAY_PER_KEY || decay_kind == ORC_DECAY_PER_KEY_GATED);
+                    int gated = (decay_kind == ORC_DECAY_PER_KEY_GATED || decay_kind == ORC_DECAY_PER_HEAD_GATED);
+                    float di = per_key ? d[((bi * T + t) * H + h) * dk + i] : d[(bi * T + t) * H + h];
+                    float ki = gated ? (1.0f - di) * kt[i] : kt[i];
                     for (i64 j = 0; j < dv; ++j) {
-                        float inj = kt[i] * vt[j];
+                        float inj = ki * vt[j];
                         S[i * dv + j] = fmaf(di, S[i * dv + j], inj);
                     }
                 }

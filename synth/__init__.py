@@ -47,6 +47,8 @@ CONFIGS = {
 
 DECAY_PER_KEY = 0
 DECAY_PER_HEAD = 1
+DECAY_PER_KEY_GATED = 2
+DECAY_PER_HEAD_GATED = 3
 
 
 def _gen(seed: int, device):
@@ -127,6 +129,21 @@ def rwkv7_inputs(B, T, H, dk, dv, *, random_state=False, cid=6, device="cpu"):
     q = normal((B, T, H, dk), s + 4, device=device)
     S0 = normal((B, H, dv, dk), s + 5, device=device) if random_state else None
     return dict(q=q, k=k, v=v, w=w, S0=S0)
+
+
+def gated_memory_inputs(B, T, H, dk, dv, *, per_key=True, cid=8, device="cpu"):
+    """Gated matrix state S = p (.) S + (1 - p) (.) (k v^T): the GLA-shaped
+    inputs with the gate p = sigmoid(N(2,1)) (mostly retaining), per key or
+    per head, scale dk^-1/2."""
+    s = 1000 * cid
+    r = 1.0 / math.sqrt(dk)
+    q = normal((B, T, H, dk), s + 1, device=device) * r
+    k = normal((B, T, H, dk), s + 2, device=device) * r
+    v = normal((B, T, H, dv), s + 3, device=device)
+    shape = (B, T, H, dk) if per_key else (B, T, H)
+    p = torch.sigmoid(normal(shape, s + 4, 2.0, 1.0, device))
+    return dict(q=q.contiguous(), k=k.contiguous(), v=v, d=p.contiguous(), S0=None, H=H, G=H,
+                decay_kind=DECAY_PER_KEY_GATED if per_key else DECAY_PER_HEAD_GATED, scale=dk ** -0.5)
 
 
 def config_inputs(name, device="cpu", **override):

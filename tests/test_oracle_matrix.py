@@ -408,3 +408,89 @@ def test_fp32_oracle_error_vs_fp64(fn):
     o64, S64 = f("f64")
     o32, S32 = f("f32")
     assert _nrel(o32, o64) < 1e-5 and _nrel(S32, S64) < 1e-5
+
+
+# ------------------------------------------------------------------ gated matrix state
+def _gated_inputs(seed, B, T, H, dk, dv, per_key=True):
+    rng = _rng(seed)
+    q = rng.standard_normal((B, T, H, dk)).astype(np.float32)
+    k = rng.standard_normal((B, T, H, dk)).astype(np.float32)
+    v = rng.standard_normal((B, T, H, dv)).astype(np.float32)
+    p = _sig(rng.standard_normal((B, T, H, dk) if per_key else (B, T, H)) + 1.0)
+    S0 = rng.standard_normal((B, H, dk, dv)) * 3
+    return q, k, v, p, S0
+
+
+@pytest.mark.parametrize("prec", ["f64", "f32"])
+def test_gated_hand_fixture(prec):
+    g = _golden.load("diag_gated_dyadic.txt")
+    B, T, H, G, dk, dv = g["shape"]
+    o, S = oracle.recur_diag(_golden.f32(g["q"], (B, T, G, dk)), _golden.f32(g["k"], (B, T, G, dk)),
+                             _golden.f32(g["v"], (B, T, H, dv)), _golden.f32(g["d"], (B, T, H, dk)),
+                             np.asarray(g["S0"]).reshape(B, H, dk, dv), H=H, G=G,
+                             decay_kind=int(g["decay_kind"][0]), scale=1.0, prec=prec)
+    assert np.array_equal(o, np.asarray(g["o"]).reshape(B, T, H, dv))
+    assert np.array_equal(S, np.asarray(g["S"]).reshape(B, H, dk, dv))
+
+
+@pytest.mark.parametrize("per_key", [True, False])
+def test_gated_state_contracts_to_constant_injection(per_key):
+    """Constant k, v: S_t - k v^T = diag(prod p) (S0 - k v^T) (convex
+    combination with a fixed point, "我拿同一份权重…" §8: S stays bounded)."""
+    B, T, H, dk, dv = 1, 60, 2, 6, 4
+    q, k, v, p, S0 = _gated_inputs(50, B, T, H, dk, dv, per_key)
+    k[:] = k[:, :1]
+    v[:] = v[:, :1]
+    kind = oracle.DECAY_PER_KEY_GATED if per_key else oracle.DECAY_PER_HEAD_GATED
+    _, S = oracle.recur_diag(q, k, v, p, S0, H=H, G=H, decay_kind=kind, scale=1.0)
+    for h in range(H):
+        fixed = _outer(k[0, 0, h], v[0, 0, h])
+        pr = np.prod(p[0, :, h].astype(np.float64), axis=0)
+        P = pr[:, None] if per_key else pr
+        assert np.max(np.abs(S[0, h] - (fixed + P * (S0[0, h] - fixed)))) < 1e-12
+
+
+def test_gated_state_stays_in_convex_hull():
+    B, T, H, dk, dv = 1, 200, 1, 5, 3
+    q, k, v, p, S0 = _gated_inputs(51, B, T, H, dk, dv)
+    _, S = oracle.recur_diag(q, k, v, p, S0, H=H, G=H, decay_kind=oracle.DECAY_PER_KEY_GATED, scale=1.0)
+    inj = k[0, :, 0, :, None].astype(np.float64) * v[0, :, 0, None, :]
+    lo = np.minimum(inj.min(axis=0), S0[0, 0])
+    hi = np.maximum(inj.max(axis=0), S0[0, 0])
+    assert np.all(S[0, 0] >= lo - 1e-12) and np.all(S[0, 0] <= hi + 1e-12)
+
+
+def test_gated_bruteforce_unrolled():
+    """T <= 6: S_T = (prod D_t) S0 + sum_j (prod_{t>j} D_t) diag(1 - p_j) k_j v_j^T."""
+    B, T, H, dk, dv = 1, 6, 2, 4, 3
+    q, k, v, p, S0 = _gated_inputs(52, B, T, H, dk, dv)
+    _, S = oracle.recur_diag(q, k, v, p, S0, H=H, G=H, decay_kind=oracle.DECAY_PER_KEY_GATED, scale=1.0)
+    for h in range(H):
+        D = [np.diag(p[0, t, h].astype(np.float64)) for t in range(T)]
+        acc = np.eye(dk)
+        for t in range(T):
+            acc = D[t] @ acc
+        ref = acc @ S0[0, h]
+        for j in range(T):
+            P = np.eye(dk)
+            for t in range(j + 1, T):
+                P = D[t] @ P
+            ref = ref + P @ np.diag(1.0 - p[0, j, h].astype(np.float64)) @ _outer(k[0, j, h], v[0, j, h])
+        assert _nrel(S[0, h], ref) < 1e-13
+
+
+def test_gated_f32_decomposes_into_fma_scans():
+    """Each entry of the fp32 gated state is the FMA-form scan with a = p_i and
+    b = fl(fl(fl(1 - p_i) k_i) v_j), bit for bit."""
+    B, T, H, dk, dv = 1, 40, 1, 6, 4
+    q, k, v, p, S0 = _gated_inputs(53, B, T, H, dk, dv)
+    S0 = S0.astype(np.float32)
+    _, S = oracle.recur_diag(q, k, v, p, S0, H=H, G=H, decay_kind=oracle.DECAY_PER_KEY_GATED, scale=1.0,
+                             prec="f32")
+    kg = ((np.float32(1) - p[0, :, 0]) * k[0, :, 0]).astype(np.float32)
+    bb = (kg[:, :, None] * v[0, :, 0, None, :]).astype(np.float32)
+    a = np.repeat(p[0, :, 0, :, None], dv, axis=2)
+    _, sf = oracle.scan_fma(np.ascontiguousarray(a.reshape(1, T, dk * dv)),
+                            np.ascontiguousarray(bb.reshape(1, T, dk * dv)), S0[0, 0].reshape(1, dk * dv),
+                            prec="f32")
+    assert np.array_equal(sf.reshape(dk, dv).view(np.uint32), S[0, 0].view(np.uint32))
