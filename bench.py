@@ -46,7 +46,7 @@ def matrix_cost(name):
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
     th = B * T * H
     state = B * H * dk * dv * 4
-    if name == "gla":
+    if name in ("gla", "gated_memory"):
         per_th, flop_e, s_in = (3 * dk + 2 * dv) * 4, 5, 0
     elif name == "mamba2":
         G = c["G"]
@@ -279,12 +279,12 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
             out[f"scan_{form}_backward"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
                                             "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
         del x, so, sf, gs_, da, db, d0
-        for name in ("gla", "mamba2", "deltanet", "rwkv7_prefill", "rwkv7_decode"):
+        for name in ("gla", "mamba2", "deltanet", "rwkv7_prefill", "rwkv7_decode", "gated_memory"):
             c = synth.CONFIGS[name]
             x = synth.config_inputs(name, device=dev)
             Bc, Tc, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
             o = torch.empty((Bc, Tc, H, dv), device=dev)
-            if name in ("gla", "mamba2"):
+            if name in ("gla", "mamba2", "gated_memory"):
                 S = torch.empty((Bc, H, dk, dv), device=dev)
                 fn = lambda: sr.sn_recur_diag(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"], x["scale"],
                                               x["q"], x["k"], x["v"], x["d"], None, S, o, s)

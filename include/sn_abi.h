@@ -87,8 +87,10 @@ typedef int32_t sn_status;
 #define SN_CAP_SCAN_BACKWARD (1u << 7) /* sn_scan_fma_backward, sn_scan_gated_backward */
 
 /* Decay layouts of sn_recur_diag. */
-#define SN_DECAY_PER_KEY  0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
-#define SN_DECAY_PER_HEAD 1   /* d is (B, T, H):     one scalar decay per head (Mamba-2) */
+#define SN_DECAY_PER_KEY        0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
+#define SN_DECAY_PER_HEAD       1   /* d is (B, T, H):     one scalar decay per head (Mamba-2) */
+#define SN_DECAY_PER_KEY_GATED  2   /* as PER_KEY, injection weighted by (1 - d_i)             */
+#define SN_DECAY_PER_HEAD_GATED 3   /* as PER_HEAD, injection weighted by (1 - d)              */
 
 /* Context options (sn_ctx_set_option / sn_ctx_get_option). */
 #define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back */
@@ -223,6 +225,10 @@ sn_status sn_scan_gated_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
  *   d    : (B, T, H, dk) for SN_DECAY_PER_KEY, (B, T, H) for SN_DECAY_PER_HEAD
  *   S_in, S_out : (B, H, dk, dv), row = key index, column = value index;
  *          S_in NULL = zeros; S_out may be NULL or equal S_in.
+ * The gated layouts give the convex-combination state
+ *     S_t = diag(d_t) S_{t-1} + diag(1 - d_t) k_t v_t^T
+ * of the association-memory branch ([P2] §8; HGRN2's recurrence structure,
+ * [P2] §4), computed as S = fma(d_i, S, ((1 - d_i) * k_i) * v_j).
  * Requires H % G == 0, dk in {64, 128}, dv in {64, 128} and 16-byte aligned
  * pointers (else SN_E_UNSUPPORTED / SN_E_INVAL).  Deterministic; the result
  * depends only on the inputs, so segment splits are bit-exact. */

@@ -21,7 +21,7 @@ SN_OK, SN_E_INVAL, SN_E_NOMEM, SN_E_IO, SN_E_FORMAT, SN_E_UNSUPPORTED, SN_E_DEVI
     0, -1, -2, -3, -4, -5, -6, -7)
 SN_CAP_SCAN_FMA, SN_CAP_SCAN_GATED, SN_CAP_RECUR_DIAG, SN_CAP_RECUR_DELTA = 1, 2, 4, 8
 SN_CAP_RECUR_RWKV7, SN_CAP_DECODE, SN_CAP_SCAN_LOOKBACK, SN_CAP_SCAN_BACKWARD = 16, 32, 64, 128
-SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD = 0, 1
+SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD, SN_DECAY_PER_KEY_GATED, SN_DECAY_PER_HEAD_GATED = 0, 1, 2, 3
 SN_OPT_SCAN_KERNEL, SN_OPT_WAIT_LIMIT_US, SN_OPT_DEBUG_POISON, SN_OPT_LOOKBACK_CHUNK, SN_OPT_RECUR_KERNEL = (
     1, 2, 3, 4, 5)
 SN_OPT_RECUR_TILE = 6

@@ -380,7 +380,8 @@ static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
     for (const void* p : ptrs)
         if (p != nullptr && !aligned(p, 16)) return SN_E_INVAL;
     const int64_t qk = rows * x.G * x.dk * 4, vo = rows * x.H * x.dv * 4;
-    const int64_t gb = (x.kind == RK_DIAG_KEY || x.kind == RK_RWKV7) ? rows * x.H * x.dk * 4 : rows * x.H * 4;
+    const bool per_key = x.kind == RK_DIAG_KEY || x.kind == RK_RWKV7 || x.kind == RK_DIAG_KEY_GATED;
+    const int64_t gb = per_key ? rows * x.H * x.dk * 4 : rows * x.H * 4;
     const int64_t sb = (int64_t)x.B * x.H * x.dk * x.dv * 4;
     const Buf bufs[7] = {{x.q, qk, false},   {x.k, qk, false},     {x.v, vo, false}, {x.g, gb, false},
                          {x.S_in, sb, false}, {x.S_out, sb, true}, {x.o, vo, true}};
@@ -397,9 +398,14 @@ static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
 sn_status sn_recur_diag(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G, int32_t dk, int32_t dv,
                         int32_t decay_kind, float scale, const float* q, const float* k, const float* v,
                         const float* d, const float* S_in, float* S_out, float* o, void* stream) {
-    if (decay_kind != SN_DECAY_PER_KEY && decay_kind != SN_DECAY_PER_HEAD) return SN_E_INVAL;
     RecurArgs x{};
-    x.kind = decay_kind == SN_DECAY_PER_KEY ? RK_DIAG_KEY : RK_DIAG_HEAD;
+    switch (decay_kind) {
+        case SN_DECAY_PER_KEY: x.kind = RK_DIAG_KEY; break;
+        case SN_DECAY_PER_HEAD: x.kind = RK_DIAG_HEAD; break;
+        case SN_DECAY_PER_KEY_GATED: x.kind = RK_DIAG_KEY_GATED; break;
+        case SN_DECAY_PER_HEAD_GATED: x.kind = RK_DIAG_HEAD_GATED; break;
+        default: return SN_E_INVAL;
+    }
     x.B = B; x.T = T; x.H = H; x.G = G; x.dk = dk; x.dv = dv; x.scale = scale;
     x.q = q; x.k = k; x.v = v; x.g = d; x.S_in = S_in; x.S_out = S_out; x.o = o;
     x.state_transposed = false;

@@ -41,9 +41,15 @@ constexpr int RS_OBUF = 3;      // output staging buffers
 constexpr int RS_RB = 8;        // steps per readout reduction batch
 
 template <int KIND>
-constexpr bool per_key_gate() { return KIND == RK_DIAG_KEY || KIND == RK_RWKV7; }
+constexpr bool per_key_gate() { return KIND == RK_DIAG_KEY || KIND == RK_RWKV7 || KIND == RK_DIAG_KEY_GATED; }
 template <int KIND>
-constexpr bool scalar_gate() { return KIND == RK_DIAG_HEAD || KIND == RK_DELTA; }
+constexpr bool scalar_gate() { return KIND == RK_DIAG_HEAD || KIND == RK_DELTA || KIND == RK_DIAG_HEAD_GATED; }
+template <int KIND>
+constexpr bool diag_kind() {
+    return KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD || KIND == RK_DIAG_KEY_GATED || KIND == RK_DIAG_HEAD_GATED;
+}
+template <int KIND>
+constexpr bool gated_injection() { return KIND == RK_DIAG_KEY_GATED || KIND == RK_DIAG_HEAD_GATED; }
 
 template <int KIND, int DK, int JT>
 struct SeqLayout {
@@ -127,13 +133,18 @@ __device__ __forceinline__ void lane_step(float2 (&P)[R][C / 2], const float* kr
     float2 v2[C2];
 #pragma unroll
     for (int c = 0; c < C2; ++c) v2[c] = *reinterpret_cast<const float2*>(vr + 2 * c);
-    if constexpr (KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD) {
+    if constexpr (diag_kind<KIND>()) {
         float dv_[R];
-        if constexpr (KIND == RK_DIAG_KEY) {
+        if constexpr (per_key_gate<KIND>()) {
             load_rows<R, LPC>(dv_, gr, sub);
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) dv_[r] = gsc;
+        }
+        if constexpr (gated_injection<KIND>()) {
+            // convex combination: the injection k_i v_j enters with weight 1 - p_i
+#pragma unroll
+            for (int r = 0; r < R; ++r) kv[r] = __fmul_rn(__fsub_rn(1.0f, dv_[r]), kv[r]);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -381,7 +392,7 @@ cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaS
     constexpr int JT = W * (32 / LPC) * C;
     using L = SeqLayout<KIND, DK, JT>;
     if (x.dv % JT != 0) return cudaErrorInvalidValue;
-    const int gdim = (KIND == RK_DIAG_KEY || KIND == RK_DIAG_HEAD) ? x.G : x.H;
+    const int gdim = diag_kind<KIND>() ? x.G : x.H;
     CUtensorMap mq, mk, mg, mv, mo;
     const uint64_t dqk[4] = {(uint64_t)DK, (uint64_t)gdim, (uint64_t)x.T, (uint64_t)x.B};
     const uint64_t sqk[3] = {(uint64_t)DK * 4, (uint64_t)gdim * DK * 4, (uint64_t)x.T * gdim * DK * 4};

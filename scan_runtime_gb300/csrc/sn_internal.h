@@ -97,7 +97,14 @@ cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* s
 cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32_t epoch, int poison,
                                  SnDevStatus* st, uint64_t wait_ns, int sm_count, cudaStream_t stream);
 
-enum RecurKind : int { RK_DIAG_KEY = 0, RK_DIAG_HEAD = 1, RK_DELTA = 2, RK_RWKV7 = 3 };
+enum RecurKind : int {
+    RK_DIAG_KEY = 0,
+    RK_DIAG_HEAD = 1,
+    RK_DELTA = 2,
+    RK_RWKV7 = 3,
+    RK_DIAG_KEY_GATED = 4,     // injection scaled by (1 - d_i): convex-combination state
+    RK_DIAG_HEAD_GATED = 5,
+};
 
 struct RecurArgs {
     int kind;

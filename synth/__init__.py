@@ -43,6 +43,9 @@ CONFIGS = {
     "deltanet": dict(cid=5, B=4, T=4096, H=8, dk=128, dv=128),
     "rwkv7_prefill": dict(cid=6, B=16, T=4096, H=12, dk=64, dv=64),
     "rwkv7_decode": dict(cid=7, B=1024, T=1, H=12, dk=64, dv=64),
+    # not a benchmark configuration of the pages: the GLA shape run through the
+    # gated (convex-combination) matrix state
+    "gated_memory": dict(cid=8, B=4, T=4096, H=4, G=4, dk=128, dv=128),
 }
 
 DECAY_PER_KEY = 0
@@ -159,6 +162,8 @@ def config_inputs(name, device="cpu", **override):
         return mamba2_inputs(c["B"], c["T"], c["H"], c["G"], c["dk"], c["dv"], cid=cid, device=device)
     if name == "deltanet":
         return deltanet_inputs(c["B"], c["T"], c["H"], c["dk"], c["dv"], cid=cid, device=device)
+    if name == "gated_memory":
+        return gated_memory_inputs(c["B"], c["T"], c["H"], c["dk"], c["dv"], cid=cid, device=device)
     if name.startswith("rwkv7"):
         return rwkv7_inputs(c["B"], c["T"], c["H"], c["dk"], c["dv"],
                             random_state=(name == "rwkv7_decode"), cid=cid, device=device)

@@ -88,6 +88,8 @@ def ref_rwkv(x, S0=None):
 
 
 def make(kind, B, T, H, dk, dv, G=None, seed=0):
+    if kind in ("gated_key", "gated_head"):
+        return synth.gated_memory_inputs(B, T, H, dk, dv, per_key=(kind == "gated_key"), cid=100 + seed)
     if kind == "gla":
         return synth.gla_inputs(B, T, H, dk, dv, cid=60 + seed)
     if kind == "mamba2":
@@ -98,7 +100,7 @@ def make(kind, B, T, H, dk, dv, G=None, seed=0):
 
 
 RUN = {"gla": (run_diag, ref_diag), "mamba2": (run_diag, ref_diag), "delta": (run_delta, ref_delta),
-       "rwkv": (run_rwkv, ref_rwkv)}
+       "rwkv": (run_rwkv, ref_rwkv), "gated_key": (run_diag, ref_diag), "gated_head": (run_diag, ref_diag)}
 
 
 def state_shape(kind, B, H, dk, dv):
@@ -106,7 +108,7 @@ def state_shape(kind, B, H, dk, dv):
 
 
 # ------------------------------------------------------------------ parity
-@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "rwkv"])
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "rwkv", "gated_key", "gated_head"])
 @pytest.mark.parametrize("dims", [(128, 128), (128, 64), (64, 128), (64, 64)])
 @pytest.mark.parametrize("T", [1, 2, 37, 100])
 def test_parity_small(ctx, kind, dims, T):
@@ -120,7 +122,7 @@ def test_parity_small(ctx, kind, dims, T):
     assert _nrel(o, ro) <= TOL and _nrel(S, rS) <= TOL
 
 
-@pytest.mark.parametrize("kind", ["gla", "mamba2"])
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "gated_key", "gated_head"])
 def test_diag_state_is_bit_exact_with_single_precision_definition(ctx, kind):
     x = make(kind, 2, 50, 4, 128, 64, G=1, seed=3)
     S0 = synth.normal((2, 4, 128, 64), 5100)
@@ -153,7 +155,7 @@ def test_optional_outputs_and_in_place_state(ctx, kind):
     assert _nrel(st.cpu().numpy(), rS) <= TOL
 
 
-@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "rwkv"])
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "rwkv", "gated_key"])
 @pytest.mark.parametrize("split", [1, 19, 48])
 def test_segment_split_bit_exact(ctx, kind, split):
     B, T, H, dk, dv = 2, 64, 2, 128 if kind != "rwkv" else 64, 64
@@ -161,8 +163,8 @@ def test_segment_split_bit_exact(ctx, kind, split):
     run, _ = RUN[kind]
     S0 = synth.normal(state_shape(kind, B, H, dk, dv), 5300)
     of, Sf = run(ctx, x, S0)
-    tk = ("q", "k", "v", "d") if kind in ("gla", "mamba2") else ("q", "k", "v", "beta") if kind == "delta" \
-        else ("q", "k", "v", "w")
+    tk = ("q", "k", "v", "d") if kind in ("gla", "mamba2", "gated_key") else ("q", "k", "v", "beta") \
+        if kind == "delta" else ("q", "k", "v", "w")
     x1 = dict(x, **{n: x[n][:, :split].contiguous() for n in tk})
     x2 = dict(x, **{n: x[n][:, split:].contiguous() for n in tk})
     o1, S1 = run(ctx, x1, S0)
@@ -223,6 +225,17 @@ def test_hand_fixtures_exact(ctx):
              v=_embed(g["v"], (B, T, H, dv), (B, T, H, D)), d=_embed(g["d"], (B, T, H), (B, T, H)),
              H=H, G=G, decay_kind=1, scale=1.0)
     o, S = run_diag(ctx, x)
+    assert np.array_equal(o[..., :dv].ravel(), np.asarray(g["o"], np.float32))
+    assert np.array_equal(S[:, :, :dk, :dv].ravel(), np.asarray(g["S"], np.float32))
+
+    g = _golden.load("diag_gated_dyadic.txt")
+    B, T, H, G, dk, dv = g["shape"]
+    x = dict(q=_embed(g["q"], (B, T, G, dk), (B, T, G, D)), k=_embed(g["k"], (B, T, G, dk), (B, T, G, D)),
+             v=_embed(g["v"], (B, T, H, dv), (B, T, H, D)), H=H, G=G, decay_kind=2, scale=1.0)
+    d = np.ones((B, T, H, D), np.float32)
+    d[..., :dk] = np.asarray(g["d"], np.float32).reshape(B, T, H, dk)
+    x["d"] = torch.from_numpy(d)
+    o, S = run_diag(ctx, x, _embed(g["S0"], (B, H, dk, dv), (B, H, D, D)))
     assert np.array_equal(o[..., :dv].ravel(), np.asarray(g["o"], np.float32))
     assert np.array_equal(S[:, :, :dk, :dv].ravel(), np.asarray(g["S"], np.float32))
 
