@@ -309,8 +309,44 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                  "fp32_frac": round(tflops / fp32_peak_tflops, 3)}
             r["bound"] = "hbm" if name == "rwkv7_decode" else "alu"
             out[name] = r
+            if name in ("gla", "mamba2"):
+                # the chunked tensor-core form of the same workload (tf32 operands)
+                ctx.ensure_workspace_bytes(sr.sn_recur_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
+                fc = lambda: sr.sn_recur_diag_chunked(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"],
+                                                      x["scale"], x["q"], x["k"], x["v"], x["d"], None, S, o, s)
+                st = fc()
+                if st != sr.SN_OK:
+                    out[name + "_chunked_tc"] = {"error": sr.sn_status_str(st)}
+                else:
+                    ms = time_form(torch, fc, warmup, reps, s)
+                    tf = chunked_tensor_flops(Bc, Tc, H, dk, dv) / ms / 1e9
+                    out[name + "_chunked_tc"] = {
+                        "ms": round(ms, 4), "tok_heads_per_s": round(th / ms * 1e3, 1),
+                        "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
+                        "TFLOPs_tf32": round(tf, 2), "tf32_frac": round(tf / tf32_peak_tflops(), 4),
+                        "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "hbm",
+                        "tolerance": 2e-3}
+                assert ctx.last_error() == sr.SN_OK
             del x, o, S
     return out
+
+
+CHUNK = 128
+
+
+def chunked_tensor_flops(B, T, H, dk, dv):
+    """Tensor-core flops of the chunked form: per chunk of C tokens the
+    products Q K^T (C x C x dk), Q S (C x dv x dk), A V (C x dv x C) and
+    Khat^T V (dk x dv x C)."""
+    nch = B * H * ((T + CHUNK - 1) // CHUNK)
+    C = CHUNK
+    return nch * 2 * (C * C * dk + C * dv * dk + C * dv * C + dk * dv * C)
+
+
+def tf32_peak_tflops():
+    """Dense tf32 peak: the measured bf16 burst peak times the nominal
+    tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)."""
+    return load_peaks()[0]["bf16_tflops"] * (1.1 / 2.25)
 
 
 def run_ours(args):
@@ -475,6 +511,8 @@ PROFILE_CASES = {
     "deltanet": "delta rule, full DeltaNet workload B=4 T=4096 H=8 dk=dv=128",
     "rwkv7_prefill": "RWKV-7 sequence kernel, full prefill workload B=16 T=4096 H=12 64x64",
     "rwkv7_decode": "RWKV-7 decode kernel, full decode workload B=1024 T=1 H=12 64x64",
+    "gla_chunked": "chunked tensor-core form, full GLA workload B=4 T=4096 H=4 dk=dv=128",
+    "mamba2_chunked": "chunked tensor-core form, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
 }
 
 
@@ -502,6 +540,17 @@ def run_profile_case(args):
             ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_SEQUENTIAL)
         fn = lambda: sr.sn_scan_fma(h, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
         nbytes = scan_bytes(B, T, N)
+    elif name.endswith("_chunked"):
+        base = name[:-len("_chunked")]
+        c = synth.CONFIGS[base]
+        x = synth.config_inputs(base, device=dev)
+        Bc, Tc, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+        o = torch.empty((Bc, Tc, H, dv), device=dev)
+        S = torch.empty((Bc, H, dk, dv), device=dev)
+        ctx.ensure_workspace_bytes(sr.sn_recur_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
+        fn = lambda: sr.sn_recur_diag_chunked(h, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"], x["scale"], x["q"],
+                                              x["k"], x["v"], x["d"], None, S, o, s)
+        nbytes = matrix_cost(base)[1]
     else:
         c = synth.CONFIGS[name]
         x = synth.config_inputs(name, device=dev)

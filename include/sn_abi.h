@@ -65,7 +65,7 @@ extern "C" {
 
 typedef int32_t sn_status;
 
-/* Status codes.  The first six are the ones [P1] §6 fixes; the last two are
+/* Status codes.  The first six are the ones [P1] §6 fixes; the last three are
  * extensions of this library. */
 #define SN_OK             0
 #define SN_E_INVAL       (-1)  /* bad argument: NULL, dim <= 0, overlap, misalignment */
@@ -75,6 +75,7 @@ typedef int32_t sn_status;
 #define SN_E_UNSUPPORTED (-5)  /* major-version mismatch, head dim not compiled, device not sm_103 */
 #define SN_E_DEVICE      (-6)  /* CUDA runtime error (launch failure, bad stream, ...) */
 #define SN_E_TIMEOUT     (-7)  /* a bounded device-side wait ran out (see sn_ctx_last_error) */
+#define SN_E_RANGE       (-8)  /* an input value outside what a kernel supports (see sn_recur_diag_chunked) */
 
 /* Capability bits returned by sn_abi_caps(). */
 #define SN_CAP_SCAN_FMA    (1u << 0)   /* sn_scan_fma */
@@ -85,6 +86,7 @@ typedef int32_t sn_status;
 #define SN_CAP_DECODE      (1u << 5)   /* dedicated T == 1 decode kernels */
 #define SN_CAP_SCAN_LOOKBACK (1u << 6) /* chunked scan with look-back carries */
 #define SN_CAP_SCAN_BACKWARD (1u << 7) /* sn_scan_fma_backward, sn_scan_gated_backward */
+#define SN_CAP_RECUR_CHUNKED (1u << 8) /* sn_recur_diag_chunked (tensor-core chunked form) */
 
 /* Decay layouts of sn_recur_diag. */
 #define SN_DECAY_PER_KEY        0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
@@ -263,6 +265,43 @@ sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
                          const float* q, const float* k, const float* v,
                          const float* w, const float* S_in, float* S_out,
                          float* o, void* stream);
+
+/* Chunked tensor-core form of sn_recur_diag for the two plain decay layouts
+ * (SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD): the same recurrence and readout,
+ * evaluated T-parallel in chunks of 128 tokens.  The state is carried from
+ * chunk to chunk ([P2] §8 keeps the association memory "chunk-scannable";
+ * [P1] §4.3 GLA, §4.1 Mamba-2), and inside a chunk
+ *     S_{n+1} = diag(D_n) S_n + sum_j diag(D_n / D_j) k_j v_j^T
+ *     o_t     = scale * ( (q_t (.) D_t)^T S_n + sum_{j <= t} (q_t (.) D_t / D_j)^T k_j v_j )
+ * with D_t the product of the chunk's decays up to token t (computed in log2
+ * space), as three dense contractions per chunk on the tensor cores
+ * (tcgen05, tf32 operands rounded to nearest, fp32 accumulation) plus an
+ * fp32 chain over the chunk states.
+ *
+ * Arguments, layouts and state conventions are those of sn_recur_diag.
+ * Accuracy: tf32 rounding of the operands, about 1e-3 relative (the
+ * sequence kernel of sn_recur_diag is exact fp32 per step); results do not
+ * depend on timing, but a segment split changes the chunk grid and so the
+ * rounding.
+ * Requirements: decay_kind SN_DECAY_PER_KEY or SN_DECAY_PER_HEAD, dk == 128,
+ * dv in {64, 128} (else SN_E_UNSUPPORTED); 16-byte aligned pointers; a
+ * context workspace of at least sn_recur_chunked_workspace_bytes() bytes
+ * (else SN_E_NOMEM), which the call overwrites (a later look-back scan on the
+ * same context clears its flag area again).  Decays must be positive; with
+ * per-key decays the product of the decays between any token of a chunk and
+ * the chunk's token 63 must lie in [2^-60, 2^60] -- a chunk outside that
+ * range records SN_E_RANGE in the context's status block (outputs are then
+ * unspecified; use sn_recur_diag). */
+sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G,
+                                int32_t dk, int32_t dv, int32_t decay_kind, float scale,
+                                const float* q, const float* k, const float* v,
+                                const float* d, const float* S_in, float* S_out,
+                                float* o, void* stream);
+
+/* Workspace bytes sn_recur_diag_chunked needs: B * H * ceil(T / 128) chunk
+ * states of dk x dv floats plus one decay vector of dk floats per chunk
+ * (each part rounded up to 256 bytes); -1 on invalid arguments. */
+int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* ---------------------------------------------------------------- allocation-free variant */
 

@@ -77,6 +77,13 @@ class Context:
         self._ws = self._torch.empty(max(need, 256), dtype=self._torch.uint8, device=f"cuda:{self.device}")
         _check(_abi.sn_ctx_set_workspace(self.handle, self._ws, self._ws.numel()), "sn_ctx_set_workspace")
 
+    def ensure_workspace_bytes(self, need: int) -> None:
+        """Give the context a workspace of at least `need` bytes."""
+        if self._ws is not None and self._ws.numel() >= need:
+            return
+        self._ws = self._torch.empty(max(need, 256), dtype=self._torch.uint8, device=f"cuda:{self.device}")
+        _check(_abi.sn_ctx_set_workspace(self.handle, self._ws, self._ws.numel()), "sn_ctx_set_workspace")
+
     def _out(self, shape, want):
         if want is None or want is False:
             return None
@@ -172,6 +179,21 @@ class Context:
         So, oo = self._out((B, H, dk, dv), S_out), self._out((B, T, H, dv), o)
         _check(_abi.sn_recur_diag(self.handle, B, T, H, G, dk, dv, decay_kind, scale, q, k, v, d, S_in, So, oo,
                                   stream), "sn_recur_diag")
+        return oo, So
+
+    def recur_diag_chunked(self, q, k, v, d, S_in=None, *, H, G, decay_kind, scale, S_out=True, o=True,
+                           stream=None):
+        """Chunked tensor-core form of recur_diag (tf32 operands); sizes the
+        context workspace on first use."""
+        B, T, _, dk = k.shape
+        dv = v.shape[3]
+        need = _abi.sn_recur_chunked_workspace_bytes(B, T, H, dk, dv)
+        if need < 0:
+            raise SnError(_abi.SN_E_INVAL, "sn_recur_chunked_workspace_bytes")
+        self.ensure_workspace_bytes(need)
+        So, oo = self._out((B, H, dk, dv), S_out), self._out((B, T, H, dv), o)
+        _check(_abi.sn_recur_diag_chunked(self.handle, B, T, H, G, dk, dv, decay_kind, scale, q, k, v, d, S_in, So,
+                                          oo, stream), "sn_recur_diag_chunked")
         return oo, So
 
     def recur_delta(self, q, k, v, beta, S_in=None, *, scale, S_out=True, o=True, stream=None):

@@ -19,8 +19,10 @@ LIB_PATH = os.path.join(HERE, "libsn.so")
 SN_ABI_VERSION_MAJOR, SN_ABI_VERSION_MINOR, SN_ABI_VERSION_PATCH = 1, 0, 0
 SN_OK, SN_E_INVAL, SN_E_NOMEM, SN_E_IO, SN_E_FORMAT, SN_E_UNSUPPORTED, SN_E_DEVICE, SN_E_TIMEOUT = (
     0, -1, -2, -3, -4, -5, -6, -7)
+SN_E_RANGE = -8
 SN_CAP_SCAN_FMA, SN_CAP_SCAN_GATED, SN_CAP_RECUR_DIAG, SN_CAP_RECUR_DELTA = 1, 2, 4, 8
 SN_CAP_RECUR_RWKV7, SN_CAP_DECODE, SN_CAP_SCAN_LOOKBACK, SN_CAP_SCAN_BACKWARD = 16, 32, 64, 128
+SN_CAP_RECUR_CHUNKED = 256
 SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD, SN_DECAY_PER_KEY_GATED, SN_DECAY_PER_HEAD_GATED = 0, 1, 2, 3
 SN_OPT_SCAN_KERNEL, SN_OPT_WAIT_LIMIT_US, SN_OPT_DEBUG_POISON, SN_OPT_LOOKBACK_CHUNK, SN_OPT_RECUR_KERNEL = (
     1, 2, 3, 4, 5)
@@ -35,6 +37,7 @@ EXPORTS = (
     "sn_ctx_last_error", "sn_ctx_set_option", "sn_ctx_get_option",
     "sn_scan_fma", "sn_scan_gated", "sn_scan_fma_backward", "sn_scan_gated_backward",
     "sn_recur_diag", "sn_recur_delta", "sn_recur_rwkv7", "sn_scan_lookback_noalloc",
+    "sn_recur_diag_chunked", "sn_recur_chunked_workspace_bytes",
 )
 SN_NOALLOC_MAX_TILES = 40960
 
@@ -73,6 +76,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "sn_recur_delta": ([p, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_rwkv7": ([p, i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p], i32),
             "sn_scan_lookback_noalloc": ([i32, i32, i32, i32, p, p, p, p, p, p, p], i32),
+            "sn_recur_diag_chunked": ([p, i32, i32, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
+            "sn_recur_chunked_workspace_bytes": ([i32, i32, i32, i32, i32], i64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -196,3 +201,13 @@ def sn_recur_rwkv7(ctx, B, T, H, dk, dv, q, k, v, w, S_in, S_out, o, stream=None
 def sn_scan_lookback_noalloc(gated, B, T, N, a, b, s0, s_final, s_out, status_out=None, stream=None) -> int:
     return load().sn_scan_lookback_noalloc(gated, B, T, N, ptr(a), ptr(b), ptr(s0), ptr(s_final), ptr(s_out),
                                            ptr(status_out), stream_handle(stream))
+
+
+def sn_recur_diag_chunked(ctx, B, T, H, G, dk, dv, decay_kind, scale, q, k, v, d, S_in, S_out, o,
+                          stream=None) -> int:
+    return load().sn_recur_diag_chunked(ctx, B, T, H, G, dk, dv, decay_kind, scale, ptr(q), ptr(k), ptr(v),
+                                        ptr(d), ptr(S_in), ptr(S_out), ptr(o), stream_handle(stream))
+
+
+def sn_recur_chunked_workspace_bytes(B, T, H, dk, dv) -> int:
+    return load().sn_recur_chunked_workspace_bytes(B, T, H, dk, dv)

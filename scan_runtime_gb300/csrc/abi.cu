@@ -140,7 +140,7 @@ sn_status sn_abi_check(int32_t major) { return major == SN_ABI_VERSION_MAJOR ? S
 
 uint32_t sn_abi_caps(void) {
     return SN_CAP_SCAN_FMA | SN_CAP_SCAN_GATED | SN_CAP_RECUR_DIAG | SN_CAP_RECUR_DELTA | SN_CAP_RECUR_RWKV7 |
-           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK | SN_CAP_SCAN_BACKWARD;
+           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK | SN_CAP_SCAN_BACKWARD | SN_CAP_RECUR_CHUNKED;
 }
 
 const char* sn_status_str(sn_status s) {
@@ -153,6 +153,7 @@ const char* sn_status_str(sn_status s) {
         case SN_E_UNSUPPORTED: return "unsupported (version, shape or device)";
         case SN_E_DEVICE: return "CUDA runtime error";
         case SN_E_TIMEOUT: return "bounded device-side wait ran out";
+        case SN_E_RANGE: return "input value outside the range the kernel supports";
         default: return "unknown status";
     }
 }
@@ -369,7 +370,8 @@ sn_status sn_scan_gated_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N, co
 // ------------------------------------------------------------------ matrix recurrences
 static bool head_dim_ok(int d) { return d == 64 || d == 128; }
 
-static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
+// Argument checks shared by every matrix-recurrence entry point.
+static sn_status recur_validate(SnCtx* ctx, const RecurArgs& x) {
     if (ctx == nullptr || x.q == nullptr || x.k == nullptr || x.v == nullptr || x.g == nullptr) return SN_E_INVAL;
     if (x.B <= 0 || x.T <= 0 || x.H <= 0 || x.G <= 0 || x.dk <= 0 || x.dv <= 0) return SN_E_INVAL;
     if (x.H % x.G != 0) return SN_E_INVAL;
@@ -386,7 +388,12 @@ static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
     const Buf bufs[7] = {{x.q, qk, false},   {x.k, qk, false},     {x.v, vo, false}, {x.g, gb, false},
                          {x.S_in, sb, false}, {x.S_out, sb, true}, {x.o, vo, true}};
     if (any_bad_overlap(bufs, 7, x.S_in, x.S_out)) return SN_E_INVAL;
+    return SN_OK;
+}
 
+static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
+    const sn_status v = recur_validate(ctx, x);
+    if (v != SN_OK) return v;
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -432,6 +439,37 @@ sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dk
     x.q = q; x.k = k; x.v = v; x.g = w; x.S_in = S_in; x.S_out = S_out; x.o = o;
     x.state_transposed = true;
     return recur_common(ctx, x, stream);
+}
+
+sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G, int32_t dk, int32_t dv,
+                                int32_t decay_kind, float scale, const float* q, const float* k, const float* v,
+                                const float* d, const float* S_in, float* S_out, float* o, void* stream) {
+    RecurArgs x{};
+    switch (decay_kind) {
+        case SN_DECAY_PER_KEY: x.kind = RK_DIAG_KEY; break;
+        case SN_DECAY_PER_HEAD: x.kind = RK_DIAG_HEAD; break;
+        case SN_DECAY_PER_KEY_GATED:
+        case SN_DECAY_PER_HEAD_GATED: return SN_E_UNSUPPORTED;
+        default: return SN_E_INVAL;
+    }
+    x.B = B; x.T = T; x.H = H; x.G = G; x.dk = dk; x.dv = dv; x.scale = scale;
+    x.q = q; x.k = k; x.v = v; x.g = d; x.S_in = S_in; x.S_out = S_out; x.o = o;
+    x.state_transposed = false;
+    const sn_status st = recur_validate(ctx, x);
+    if (st != SN_OK) return st;
+    if (!chunked_supported(x)) return SN_E_UNSUPPORTED;
+    const int64_t need = chunked_ws_bytes(B, T, H, dk, dv);
+    if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SN_E_DEVICE;
+    ctx->ws_dirty = true;   // the chunk states overwrite the look-back flag area
+    return from_cuda(launch_recur_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {
+    if (B <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    return chunked_ws_bytes(B, T, H, dk, dv);
 }
 
 }  // extern "C"

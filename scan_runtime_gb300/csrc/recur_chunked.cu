@@ -1,0 +1,923 @@
+// recur_chunked.cu -- chunked tensor-core form of the diagonal-decay matrix
+// recurrence
+//     S_t = diag(d_t) S_{t-1} + k_t v_t^T,      o_t = scale * S_t^T q_t
+// for per-key decays (GLA, "SunnyNet 工程化实录" §4.3) and per-head decays
+// (Mamba-2, same page §4.1), the T-parallel counterpart of the sequence kernel
+// in recur_seq.cuh.  The pages keep this state "chunk-scannable" ("我拿同一份
+// 权重和 llama.cpp 正面比了一场" §8); this file evaluates it chunk by chunk with
+// dense contractions on the fifth-generation tensor cores.
+//
+// Chunk n holds tokens t = 0..C-1 (C = 128, global index nC + t) and starts
+// from state S_n.  With lam_t = sum_{s <= t} log2 d_s (per key, or one scalar
+// per head) the chunk's tokens satisfy
+//   S_{n+1} = diag(2^{lam_{C-1}}) S_n + sum_j diag(2^{lam_{C-1} - lam_j}) k_j v_j^T
+//   o_t     = scale * ( sum_i q_ti 2^{lam_ti} S_n[i, :]
+//                     + sum_{j <= t} ( sum_i q_ti k_ji 2^{lam_ti - lam_ji} ) v_j )
+// which three kernels evaluate:
+//   chunk_state   one CTA per chunk: dS_n^T = V^T Khat with Khat_j = k_j
+//                 2^{lam_{C-1} - lam_j} (one tcgen05 product, M = dv), the chunk
+//                 decay gamma_n = 2^{lam_{C-1}} and the anchor factor below;
+//   chunk_carry   one thread per state entry: S_{n+1} = gamma_n S_n + dS_n over
+//                 the chunks in order (fp32 FMA); the operand S'_n of the chunk
+//                 (below, rounded to tf32) is written over dS_n;
+//   chunk_output  one CTA per chunk: A = Qt Kt^T masked to j <= t, P = Qt S',
+//                 O = A V (three M = C tcgen05 products), o = scale (f_t P + O).
+// Per-key decays cannot be pulled out of the dot product over keys, so the
+// pair weight 2^{lam_ti - lam_ji} is split through an anchor token m = C/2 - 1:
+// Qt = q 2^{lam_t - lam_m}, Kt = k 2^{lam_m - lam_j}, S' = diag(2^{lam_m}) S_n
+// and f_t = 1.  Those factors stay within 2^{+-60} as long as the decay
+// product between any token of the chunk and the anchor is at least 2^-60 (and
+// every decay is positive); a launch that sees a chunk outside that range
+// records SN_E_RANGE.  Per-head decays are scalars per token, so Qt = q, Kt =
+// k, S' = S_n, the exact weight 2^{lam_t - lam_j} multiplies A after the
+// product and f_t = 2^{lam_t}; they only need positive decays.
+//
+// Operands are rounded to tf32 (to nearest) and products accumulate in fp32
+// in tensor memory, so results carry tf32 rounding (about 1e-3 relative)
+// instead of the sequence kernel's exact per-step fp32 arithmetic.
+//
+// Data movement: every tile a CTA needs is requested before any of it is
+// used.  Tiles whose layout matches the operand (q, k rows) arrive by 16-byte
+// cp.async straight into the operand layout; tiles that must be transposed
+// (k, d and v in chunk_state, the v slice of chunk_output) arrive by 4-byte
+// cp.async or plain loads, with lanes covering 8 operand rows x 4 tokens so
+// the scattered shared-memory writes are conflict-free; the chunk's S'
+// operand is one contiguous bulk copy, because chunk_state and chunk_carry
+// keep the chunk states in the operand layout.
+//
+// Shared-memory operands use the K-major no-swizzle core-matrix layout of
+// tc.cuh with K extent 128 (every contraction here has K = 128: keys, or the
+// chunk's tokens).
+#include <cmath>
+
+#include "ptx.cuh"
+#include "sn_internal.h"
+#include "tc.cuh"
+
+namespace sn {
+namespace {
+
+constexpr int CH = 128;                 // tokens per chunk
+constexpr int DKC = 128;                // key dimension
+constexpr int NT = 256;                 // threads per CTA
+constexpr int ANCHOR = CH / 2 - 1;      // anchor token of the per-key factors
+constexpr float RANGE_LOG2 = 60.0f;     // bound on |lam_t - lam_anchor| (log2 units)
+constexpr int OPF = CH * DKC;           // floats per 128 x 128 operand
+constexpr unsigned FULL = 0xffffffffu;
+
+struct ChunkArgs {
+    int B, T, H, G, NC;
+    float scale;
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* d;
+    const float* S_in;
+    float* S_out;
+    float* o;
+    float* W;       // per (b, h, chunk) a dv x dk tile in operand layout: dS^T, then S'^T
+    float* gam;     // (B, H, NC, dk): chunk decay gamma_n per key
+    float* anc;     // (B, H, NC, dk): anchor factor 2^{lam_m} (1 for per-head decays)
+    SnDevStatus* st;
+    uint64_t wait_ns;
+};
+
+// sites recorded with SN_E_TIMEOUT / SN_E_RANGE
+constexpr int SITE_STATE_WAIT = 1, SITE_OUT_WAIT1 = 2, SITE_OUT_WAIT2 = 3, SITE_RANGE_KEY = 4,
+              SITE_RANGE_HEAD = 5, SITE_OUT_COPY = 6;
+
+__device__ __forceinline__ int off128(int r, int k) {
+    return (r >> 3) * 1024 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3);
+}
+
+__device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 tf32x4(float a, float b, float c, float d) {
+    return make_float4(tc::to_tf32(a), tc::to_tf32(b), tc::to_tf32(c), tc::to_tf32(d));
+}
+__device__ __forceinline__ float4 tf32x4(float4 x) { return tf32x4(x.x, x.y, x.z, x.w); }
+
+// cp.async of 4 / 16 bytes; `valid` false writes zeros (the source is not read).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Base-2 exponential and logarithm from the SFU instructions (ex2.approx /
+// lg2.approx, relative error ~2^-22; subnormals flush to zero): far below the
+// tf32 rounding of the operands they scale.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float* align128(unsigned char* p) {
+    return reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p) + 127) & ~uintptr_t(127));
+}
+
+struct ChunkIdx {
+    int b, h, n, g, t0, nval;
+    size_t bh;
+};
+
+__device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a) {
+    ChunkIdx c;
+    c.h = blockIdx.x % a.H;
+    const int bn = blockIdx.x / a.H;
+    c.n = bn % a.NC;
+    c.b = bn / a.NC;
+    c.g = c.h / (a.H / a.G);
+    c.t0 = c.n * CH;
+    c.nval = min(CH, a.T - c.t0);
+    c.bh = (size_t)c.b * a.H + c.h;
+    return c;
+}
+
+// Transposing copy of a (tokens x R) slab of a row-major global array into the
+// operand layout (rows = the R columns of the array, K = tokens): element
+// (t, r) of rows base[t * rs + r] lands at off128(r, t).  Lanes cover 8 rows x
+// 4 tokens (32 distinct banks); tokens >= nval are zero.
+template <int R>
+__device__ __forceinline__ void copy_transposed(float* dst, const float* base, size_t rs, int nval, int warp,
+                                                int lane) {
+    const int rl = lane & 7, tq = lane >> 3;
+    constexpr int RB = R / 8;
+#pragma unroll 8
+    for (int p = warp; p < RB * (CH / 4); p += NT / 32) {
+        const int r = (p % RB) * 8 + rl;
+        const int t = (p / RB) * 4 + tq;
+        const bool ok = t < nval;
+        cp_async4(dst + off128(r, t), base + (size_t)(ok ? t : 0) * rs + r, ok);
+    }
+}
+
+// ------------------------------------------------------------------ chunk_state
+template <bool PER_KEY, int DV>
+struct StateSmem {
+    static constexpr int k_off = 0;                                   // k^T, then Khat^T: rows i, K = t
+    static constexpr int d_off = OPF;                                 // d^T (per key): rows i, K = t
+    static constexpr int v_off = d_off + (PER_KEY ? OPF : 0);         // v^T: rows c, K = t
+    static constexpr int tot_off = v_off + DV * CH;                   // [2][DKC] half sums
+    static constexpr int mu_off = tot_off + 2 * DKC;                  // [CH] suffix sums (per head)
+    static constexpr int misc_off = mu_off + CH;                      // total, barrier, tmem slot
+    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+};
+
+template <bool PER_KEY, int DV>
+__global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = StateSmem<PER_KEY, DV>;
+    float* base = align128(smem_raw);
+    float* Ks = base + L::k_off;
+    float* Ds = base + L::d_off;
+    float* Vs = base + L::v_off;
+    float* tot = base + L::tot_off;
+    float* mu = base + L::mu_off;
+    float* total_s = base + L::misc_off;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const ChunkIdx c = chunk_index(a);
+
+    if (warp == 0) tc::tmem_alloc(slot, DKC);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+
+    const size_t krs = (size_t)a.G * DKC, drs = (size_t)a.H * DKC, vrs = (size_t)a.H * DV;
+    const size_t row0 = (size_t)c.b * a.T + c.t0;
+    copy_transposed<DKC>(Ks, a.k + row0 * krs + (size_t)c.g * DKC, krs, c.nval, warp, lane);
+    if (PER_KEY) copy_transposed<DKC>(Ds, a.d + row0 * drs + (size_t)c.h * DKC, drs, c.nval, warp, lane);
+    copy_transposed<DV>(Vs, a.v + row0 * vrs + (size_t)c.h * DV, vrs, c.nval, warp, lane);
+    cp_async_commit();
+
+    if (!PER_KEY && warp == 0) {
+        // exclusive suffix sums mu[t] = sum_{s > t} log2 d_s of the per-head decays
+        float lg[4], s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * lane + r;
+            lg[r] = t < c.nval ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
+            s += lg[r];
+        }
+        float x = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_down_sync(FULL, x, off);
+            if (lane + off < 32) x += y;
+        }
+        float acc = x - s;
+#pragma unroll
+        for (int r = 3; r >= 0; --r) {
+            mu[4 * lane + r] = acc;
+            acc += lg[r];
+        }
+        if (lane == 0) {
+            total_s[0] = x;
+            if (!isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // Khat^T in place: thread = key row i, half of the tokens
+    const int i = tid & (DKC - 1), half = tid >> 7;
+    const int tbeg = (CH / 2) * half;
+    float gam, anc;
+    if (PER_KEY) {
+        // log2 of the decays, kept in place of the decays
+        float sum = 0.f;
+#pragma unroll 4
+        for (int t4 = 0; t4 < CH / 8; ++t4) {
+            const int tb = tbeg + 4 * t4;
+            const int o = off128(i, tb);
+            const float4 dd = ld4(Ds + o);
+            const float4 lg = make_float4(tb + 0 < c.nval ? lg2(dd.x) : 0.f, tb + 1 < c.nval ? lg2(dd.y) : 0.f,
+                                          tb + 2 < c.nval ? lg2(dd.z) : 0.f, tb + 3 < c.nval ? lg2(dd.w) : 0.f);
+            st4(Ds + o, lg);
+            sum += (lg.x + lg.y) + (lg.z + lg.w);
+        }
+        tot[half * DKC + i] = sum;
+        __syncthreads();
+        float m = half == 0 ? tot[DKC + i] : 0.f;   // sum over the later tokens
+#pragma unroll 4
+        for (int t4 = CH / 8 - 1; t4 >= 0; --t4) {
+            const int tb = tbeg + 4 * t4;
+            const int o = off128(i, tb);
+            const float4 dd = ld4(Ds + o), kk = ld4(Ks + o);
+            float out[4];
+            const float dv4[4] = {dd.x, dd.y, dd.z, dd.w}, kv4[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+            for (int r = 3; r >= 0; --r) {
+                out[r] = kv4[r] * ex2(m);
+                m += dv4[r];
+            }
+            st4(Ks + o, tf32x4(out[0], out[1], out[2], out[3]));
+        }
+        gam = ex2(m);                       // half 0: the whole chunk's log2 decay
+        anc = ex2(tot[i]);                  // 2^{lam at the anchor token C/2 - 1}
+    } else {
+        const float total = total_s[0];
+#pragma unroll 4
+        for (int t4 = 0; t4 < CH / 8; ++t4) {
+            const int tb = tbeg + 4 * t4;
+            const int o = off128(i, tb);
+            const float4 kk = ld4(Ks + o);
+            st4(Ks + o, tf32x4(kk.x * ex2(mu[tb]), kk.y * ex2(mu[tb + 1]), kk.z * ex2(mu[tb + 2]),
+                               kk.w * ex2(mu[tb + 3])));
+        }
+        gam = ex2(total);
+        anc = 1.f;
+    }
+    if (half == 0) {
+        const size_t gi = (c.bh * a.NC + c.n) * DKC + i;
+        a.gam[gi] = gam;
+        a.anc[gi] = anc;
+    }
+    // v^T rounded in place
+    for (int f = tid; f < DV * CH / 4; f += NT) st4(Vs + 4 * f, tf32x4(ld4(Vs + 4 * f)));
+
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    if (tid == 0) {
+        // dS^T (M = dv rows c, N = dk columns i) = v^T (K = t) x Khat^T (K = t)
+        tc::gemm_tf32(tmem, Vs, Ks, CH, tc::idesc_tf32(DV, DKC), false);
+        tc::commit(bar);
+    }
+    const bool ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
+    tc::fence_after_sync();
+    if (ok) {
+        // M = 128: row c in lane c.  M = 64: rows 16q..16q+15 in lanes 32q..32q+15.
+        const int lq = warp & 3, ih = warp >> 2;
+        const int row = DV == 128 ? 32 * lq + lane : 16 * lq + (lane & 15);
+        const bool mine = DV == 128 || lane < 16;
+        float* wt = a.W + (c.bh * a.NC + c.n) * (size_t)DV * DKC;
+#pragma unroll
+        for (int i0 = 64 * ih; i0 < 64 * ih + 64; i0 += 16) {
+            float x[16];
+            tc::ld16(tmem + ((uint32_t)(32 * lq) << 16) + i0, x);
+            if (mine) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st4(wt + off128(row, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+            }
+        }
+    } else if (tid == 0) {
+        record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_STATE_WAIT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, DKC);
+}
+
+// ------------------------------------------------------------------ chunk_carry
+// One thread per entry of a head's dv x dk state tile, in the operand layout.
+// S_0 = S_in; for each chunk: W[n] <- tf32(anc_n (.) S_n), S_{n+1} = gamma_n (.) S_n + dS_n.
+__global__ void __launch_bounds__(256) chunk_carry(const ChunkArgs a, int dv) {
+    const size_t per_head = (size_t)DKC * dv;
+    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (size_t)a.B * a.H * per_head) return;
+    const size_t bh = e / per_head;
+    const int f = (int)(e % per_head);
+    const int i = ((f >> 5) & 31) * 4 + (f & 3);        // key (K index of the operand)
+    const int col = (f >> 10) * 8 + ((f >> 2) & 7);     // value (row of the operand)
+    const size_t nat = bh * per_head + (size_t)i * dv + col;
+    float s = a.S_in != nullptr ? a.S_in[nat] : 0.f;
+    float* w = a.W + bh * a.NC * per_head + f;
+    const float* gm = a.gam + bh * a.NC * DKC + i;
+    const float* an = a.anc + bh * a.NC * DKC + i;
+    constexpr int U = 8;
+    int n = 0;
+    for (; n + U <= a.NC; n += U) {
+        float ds[U], gg[U], aa[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            ds[u] = w[(size_t)(n + u) * per_head];
+            gg[u] = __ldg(gm + (size_t)(n + u) * DKC);
+            aa[u] = __ldg(an + (size_t)(n + u) * DKC);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            w[(size_t)(n + u) * per_head] = tc::to_tf32(aa[u] * s);
+            s = fmaf(gg[u], s, ds[u]);
+        }
+    }
+    for (; n < a.NC; ++n) {
+        const float ds = w[(size_t)n * per_head];
+        w[(size_t)n * per_head] = tc::to_tf32(__ldg(an + (size_t)n * DKC) * s);
+        s = fmaf(__ldg(gm + (size_t)n * DKC), s, ds);
+    }
+    if (a.S_out != nullptr) a.S_out[nat] = s;
+}
+
+// ------------------------------------------------------------------ chunk_output
+template <int DV>
+struct OutSmem {
+    static constexpr int q_off = 0;              // Qt, later the masked A
+    static constexpr int k_off = OPF;            // Kt, later v^T
+    static constexpr int s_off = 2 * OPF;        // S'^T (rows c, K = i)
+    static constexpr int lam_off = s_off + DV * DKC;   // [CH] per-head lam
+    static constexpr int misc_off = lam_off + CH;
+    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+};
+
+template <bool PER_KEY, int DV>
+__global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = OutSmem<DV>;
+    float* base = align128(smem_raw);
+    float* bufQ = base + L::q_off;
+    float* bufK = base + L::k_off;
+    float* bufS = base + L::s_off;
+    float* lam_s = base + L::lam_off;
+    uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);
+    uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const ChunkIdx c = chunk_index(a);
+
+    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (tid == 0) {
+        mbar_init(barS, 1);
+        mbar_init(barM, 1);
+        fence_mbar_init();
+        // the chunk's S' operand: one contiguous tile written by chunk_carry
+        mbar_arrive_expect_tx(barS, DV * DKC * 4);
+        bulk_load(bufS, a.W + (c.bh * a.NC + c.n) * (size_t)DV * DKC, DV * DKC * 4, barS);
+    }
+    __syncthreads();   // barriers initialised before any thread polls them
+
+    // q, k rows straight into the operand layout: warp = 16 key columns,
+    // lane = (token mod 8, 4-column group)
+    const int tl = lane & 7, ig = lane >> 3;
+    const int ic = 16 * warp + 4 * ig;
+    const size_t qrs = (size_t)a.G * DKC;
+    const size_t row0 = (size_t)c.b * a.T + c.t0;
+    const float* qb = a.q + row0 * qrs + (size_t)c.g * DKC + ic;
+    const float* kb = a.k + row0 * qrs + (size_t)c.g * DKC + ic;
+#pragma unroll
+    for (int tb = 0; tb < CH / 8; ++tb) {
+        const int t = 8 * tb + tl;
+        const bool ok = t < c.nval;
+        const size_t src = (size_t)(ok ? t : 0) * qrs;
+        cp_async16(bufQ + off128(t, ic), qb + src, ok);
+        cp_async16(bufK + off128(t, ic), kb + src, ok);
+    }
+    cp_async_commit();
+
+    // v slice for the last product, in registers: thread = value column, a run of tokens
+    constexpr int TP = CH / (NT / DV);
+    const int col = tid % DV, part = tid / DV;
+    float vr[TP];
+    {
+        const size_t vrs = (size_t)a.H * DV;
+        const float* vcol = a.v + row0 * vrs + (size_t)c.h * DV + col;
+#pragma unroll
+        for (int r = 0; r < TP; ++r) {
+            const int t = part * TP + r;
+            vr[r] = t < c.nval ? __ldg(vcol + (size_t)t * vrs) : 0.f;
+        }
+    }
+
+    // decay prefix sums: per key in registers (same lane mapping), per head in shared memory
+    float4 lam[CH / 8];
+    float4 lm = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (PER_KEY) {
+        const size_t drs = (size_t)a.H * DKC;
+        const float* db = a.d + row0 * drs + (size_t)c.h * DKC + ic;
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            const int t = 8 * tb + tl;
+            lam[tb] = t < c.nval ? ldg4(db + (size_t)t * drs) : make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+        float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 lmax = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float4 lmin = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            float4 x = make_float4(lg2(lam[tb].x), lg2(lam[tb].y), lg2(lam[tb].z), lg2(lam[tb].w));
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                const float yx = __shfl_up_sync(FULL, x.x, off, 8), yy = __shfl_up_sync(FULL, x.y, off, 8);
+                const float yz = __shfl_up_sync(FULL, x.z, off, 8), yw = __shfl_up_sync(FULL, x.w, off, 8);
+                if (tl >= off) {
+                    x.x += yx; x.y += yy; x.z += yz; x.w += yw;
+                }
+            }
+            x.x += carry.x; x.y += carry.y; x.z += carry.z; x.w += carry.w;
+            carry = make_float4(__shfl_sync(FULL, x.x, 7, 8), __shfl_sync(FULL, x.y, 7, 8),
+                                __shfl_sync(FULL, x.z, 7, 8), __shfl_sync(FULL, x.w, 7, 8));
+            if (tb == ANCHOR / 8) lm = carry;
+            lmax = make_float4(fmaxf(lmax.x, x.x), fmaxf(lmax.y, x.y), fmaxf(lmax.z, x.z), fmaxf(lmax.w, x.w));
+            lmin = make_float4(fminf(lmin.x, x.x), fminf(lmin.y, x.y), fminf(lmin.z, x.z), fminf(lmin.w, x.w));
+            lam[tb] = x;
+        }
+        // the anchor factors must stay within 2^{+-RANGE}: NaN (decay <= 0) fails too
+        const bool in_range = (lmax.x - lm.x <= RANGE_LOG2) && (lm.x - lmin.x <= RANGE_LOG2) &&
+                              (lmax.y - lm.y <= RANGE_LOG2) && (lm.y - lmin.y <= RANGE_LOG2) &&
+                              (lmax.z - lm.z <= RANGE_LOG2) && (lm.z - lmin.z <= RANGE_LOG2) &&
+                              (lmax.w - lm.w <= RANGE_LOG2) && (lm.w - lmin.w <= RANGE_LOG2);
+        if (!__all_sync(FULL, in_range) && lane == 0)
+            record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_KEY);
+    } else if (warp == 0) {
+        // inclusive prefix sums of log2 d (per head) into lam_s
+        float lg[4], s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * lane + r;
+            lg[r] = t < c.nval ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
+            s += lg[r];
+        }
+        float x = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(FULL, x, off);
+            if (lane >= off) x += y;
+        }
+        float acc = x - s;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            acc += lg[r];
+            lam_s[4 * lane + r] = acc;
+        }
+        const float total = __shfl_sync(FULL, x, 31);
+        if (lane == 0 && !isfinite(total))
+            record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
+    }
+
+    // Qt, Kt in place (each thread rescales the rows its own copies wrote)
+    cp_async_wait_all();
+#pragma unroll
+    for (int tb = 0; tb < CH / 8; ++tb) {
+        const int o = off128(8 * tb + tl, ic);
+        const float4 q4 = ld4(bufQ + o), k4 = ld4(bufK + o);
+        if (PER_KEY) {
+            const float4 x = lam[tb];
+            st4(bufQ + o, tf32x4(q4.x * ex2(x.x - lm.x), q4.y * ex2(x.y - lm.y), q4.z * ex2(x.z - lm.z),
+                                 q4.w * ex2(x.w - lm.w)));
+            st4(bufK + o, tf32x4(k4.x * ex2(lm.x - x.x), k4.y * ex2(lm.y - x.y), k4.z * ex2(lm.z - x.z),
+                                 k4.w * ex2(lm.w - x.w)));
+        } else {
+            st4(bufQ + o, tf32x4(q4));
+            st4(bufK + o, tf32x4(k4));
+        }
+    }
+
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    bool ok = __syncthreads_and(mbar_wait(barS, 0, a.wait_ns));
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    if (!ok) {
+        if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
+            mbar_wait(barS, 0, a.wait_ns);   // let a late copy land before the CTA exits
+        }
+    } else if (tid == 0) {
+        tc::gemm_tf32(tmem, bufQ, bufK, DKC, tc::idesc_tf32(128, 128), false);        // A (cols 0..127)
+        tc::gemm_tf32(tmem + 128, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);   // P (cols 128..)
+        tc::commit(barM);
+    }
+
+    const int lq = warp & 3, hf = warp >> 2;
+    const int t = 32 * lq + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    if (ok) {
+        ok = __syncthreads_and(mbar_wait(barM, 0, a.wait_ns));
+        tc::fence_after_sync();
+        if (ok) {
+            const float lt = PER_KEY ? 0.f : lam_s[t];
+            // masked (and, per head, decay-weighted) A into the Q buffer as the next A operand
+#pragma unroll
+            for (int j0 = 64 * hf; j0 < 64 * hf + 64; j0 += 16) {
+                float x[16];
+                tc::ld16(lane_base + j0, x);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = j0 + jj;
+                    const float w = j <= t ? (PER_KEY ? 1.f : ex2(lt - lam_s[j])) : 0.f;
+                    x[jj] *= w;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st4(bufQ + off128(t, j0 + 4 * q), tf32x4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+            }
+#pragma unroll
+            for (int t4 = 0; t4 < TP / 4; ++t4)
+                st4(bufK + off128(col, part * TP + 4 * t4),
+                    tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
+        } else if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT1);
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    if (ok) {
+        if (tid == 0) {
+            tc::gemm_tf32(tmem, bufQ, bufK, CH, tc::idesc_tf32(128, DV), false);   // O (cols 0..DV-1)
+            tc::commit(barM);
+        }
+        ok = __syncthreads_and(mbar_wait(barM, 1, a.wait_ns));
+        tc::fence_after_sync();
+        if (ok) {
+            const float fp = PER_KEY ? 1.f : ex2(lam_s[t]);
+            const bool store = t < c.nval && a.o != nullptr;
+            float* orow = a.o + (row0 + t) * a.H * DV + (size_t)c.h * DV;
+#pragma unroll
+            for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
+                float p[16], x[16];
+                tc::ld16(lane_base + 128 + c0, p);
+                tc::ld16(lane_base + c0, x);
+                if (store) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_cs(reinterpret_cast<float4*>(orow + c0 + 4 * q),
+                              make_float4(a.scale * fmaf(fp, p[4 * q], x[4 * q]),
+                                          a.scale * fmaf(fp, p[4 * q + 1], x[4 * q + 1]),
+                                          a.scale * fmaf(fp, p[4 * q + 2], x[4 * q + 2]),
+                                          a.scale * fmaf(fp, p[4 * q + 3], x[4 * q + 3])));
+                }
+            }
+        } else if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------ chunk_output_heads
+// Per-head decays where several heads share q and k (Mamba-2's groups): one
+// CTA per (batch, chunk, block of hb heads of one group).  Q K^T does not
+// depend on the head, so the CTA forms it once in tensor memory and, head by
+// head, weights a copy of it with that head's decays, then adds the head's
+// state and value products.  The next head's S' tile, v slice and decay sums
+// are fetched while the current head's products run.  dv = 64.
+template <int DV>
+struct HeadsSmem {
+    static constexpr int q_off = 0;                  // Q (tf32)
+    static constexpr int a_off = OPF;                // K, then the weighted A of the current head
+    static constexpr int s_off = 2 * OPF;            // S'^T of the current head
+    static constexpr int v_off = s_off + DV * DKC;   // v^T of the current head
+    static constexpr int lam_off = v_off + DV * CH;  // [2][CH] decay prefix sums (two heads)
+    static constexpr int misc_off = lam_off + 2 * CH;
+    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+};
+
+template <int DV>
+__global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, int hb) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = HeadsSmem<DV>;
+    float* base = align128(smem_raw);
+    float* bufQ = base + L::q_off;
+    float* bufA = base + L::a_off;
+    float* bufS = base + L::s_off;
+    float* bufV = base + L::v_off;
+    float* lam2 = base + L::lam_off;
+    uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);
+    uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nhb = a.H / hb;
+    const int hblk = blockIdx.x % nhb;
+    const int bn = blockIdx.x / nhb;
+    const int n = bn % a.NC, b = bn / a.NC;
+    const int h0 = hblk * hb;
+    const int g = h0 / (a.H / a.G);
+    const int t0 = n * CH, nval = min(CH, a.T - t0);
+    const size_t row0 = (size_t)b * a.T + t0;
+    const size_t tile_floats = (size_t)DV * DKC;
+    auto tile = [&](int h) { return a.W + (((size_t)b * a.H + h) * a.NC + n) * tile_floats; };
+
+    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (tid == 0) {
+        mbar_init(barS, 1);
+        mbar_init(barM, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(barS, DV * DKC * 4);
+        bulk_load(bufS, tile(h0), DV * DKC * 4, barS);
+    }
+    __syncthreads();
+
+    // q, k rows straight into the operand layout
+    {
+        const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
+        const size_t qrs = (size_t)a.G * DKC;
+        const float* qb = a.q + row0 * qrs + (size_t)g * DKC + ic;
+        const float* kb = a.k + row0 * qrs + (size_t)g * DKC + ic;
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            const int t = 8 * tb + tl;
+            const bool ok = t < nval;
+            const size_t src = (size_t)(ok ? t : 0) * qrs;
+            cp_async16(bufQ + off128(t, ic), qb + src, ok);
+            cp_async16(bufA + off128(t, ic), kb + src, ok);
+        }
+        cp_async_commit();
+    }
+
+    constexpr int TP = CH / (NT / DV);
+    const int col = tid % DV, part = tid / DV;
+    float vr[TP];
+    const size_t vrs = (size_t)a.H * DV;
+    auto load_v = [&](int h) {
+        const float* vcol = a.v + row0 * vrs + (size_t)h * DV + col;
+#pragma unroll
+        for (int r = 0; r < TP; ++r) {
+            const int t = part * TP + r;
+            vr[r] = t < nval ? __ldg(vcol + (size_t)t * vrs) : 0.f;
+        }
+    };
+    // warp 0: inclusive prefix sums of log2 d of head h into dst
+    auto head_lam = [&](int h, float* dst) {
+        float lg[4], s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * lane + r;
+            lg[r] = t < nval ? lg2(__ldg(a.d + (row0 + t) * a.H + h)) : 0.f;
+            s += lg[r];
+        }
+        float x = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(FULL, x, off);
+            if (lane >= off) x += y;
+        }
+        float acc = x - s;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            acc += lg[r];
+            dst[4 * lane + r] = acc;
+        }
+        if (lane == 31 && !isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
+    };
+    load_v(h0);
+    if (warp == 0) head_lam(h0, lam2);
+
+    cp_async_wait_all();
+    {
+        const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            const int o = off128(8 * tb + tl, ic);
+            st4(bufQ + o, tf32x4(ld4(bufQ + o)));
+            st4(bufA + o, tf32x4(ld4(bufA + o)));
+        }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    bool ok = __syncthreads_and(mbar_wait(barS, 0, a.wait_ns));
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    constexpr uint32_t COL_P = 128, COL_O = 128 + DV;   // tensor-memory columns: A, P, O
+    if (!ok) {
+        if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
+            mbar_wait(barS, 0, a.wait_ns);
+        }
+    } else if (tid == 0) {
+        tc::gemm_tf32(tmem, bufQ, bufA, DKC, tc::idesc_tf32(128, 128), false);        // Q K^T
+        tc::gemm_tf32(tmem + COL_P, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false); // P of the first head
+        tc::commit(barM);
+    }
+
+    const int lq = warp & 3, hf = warp >> 2;
+    const int t = 32 * lq + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    uint32_t mpar = 0;
+    for (int hi = 0; hi < hb && ok; ++hi) {
+        const int h = h0 + hi;
+        const float* lam = lam2 + (hi & 1) * CH;
+        ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
+        mpar ^= 1;
+        tc::fence_after_sync();
+        if (!ok) {
+            if (tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT1);
+            break;
+        }
+        if (tid == 0 && hi + 1 < hb) {   // the S' buffer is free again
+            mbar_arrive_expect_tx(barS, DV * DKC * 4);
+            bulk_load(bufS, tile(h + 1), DV * DKC * 4, barS);
+        }
+        const float lt = lam[t];
+#pragma unroll
+        for (int j0 = 64 * hf; j0 < 64 * hf + 64; j0 += 16) {
+            float x[16];
+            tc::ld16(lane_base + j0, x);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j = j0 + jj;
+                x[jj] *= j <= t ? ex2(lt - lam[j]) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st4(bufA + off128(t, j0 + 4 * q), tf32x4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+        }
+#pragma unroll
+        for (int t4 = 0; t4 < TP / 4; ++t4)
+            st4(bufV + off128(col, part * TP + 4 * t4),
+                tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            tc::gemm_tf32(tmem + COL_O, bufA, bufV, CH, tc::idesc_tf32(128, DV), false);
+            tc::commit(barM);
+        }
+        if (hi + 1 < hb) {   // next head's v and decay sums while the product runs
+            load_v(h + 1);
+            if (warp == 0) head_lam(h + 1, lam2 + ((hi + 1) & 1) * CH);
+        }
+        ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
+        mpar ^= 1;
+        tc::fence_after_sync();
+        if (!ok) {
+            if (tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
+            break;
+        }
+        {
+            const float fp = ex2(lt);
+            const bool store = t < nval && a.o != nullptr;
+            float* orow = a.o + (row0 + t) * a.H * DV + (size_t)h * DV;
+#pragma unroll
+            for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
+                float p[16], x[16];
+                tc::ld16(lane_base + COL_P + c0, p);
+                tc::ld16(lane_base + COL_O + c0, x);
+                if (store) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_cs(reinterpret_cast<float4*>(orow + c0 + 4 * q),
+                              make_float4(a.scale * fmaf(fp, p[4 * q], x[4 * q]),
+                                          a.scale * fmaf(fp, p[4 * q + 1], x[4 * q + 1]),
+                                          a.scale * fmaf(fp, p[4 * q + 2], x[4 * q + 2]),
+                                          a.scale * fmaf(fp, p[4 * q + 3], x[4 * q + 3])));
+                }
+            }
+        }
+        if (hi + 1 < hb) {
+            tc::fence_before_sync();
+            ok = __syncthreads_and(mbar_wait(barS, (hi + 1) & 1, a.wait_ns));
+            tc::fence_after_sync();
+            if (!ok) {
+                if (tid == 0) {
+                    record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
+                    mbar_wait(barS, (hi + 1) & 1, a.wait_ns);
+                }
+                break;
+            }
+            if (tid == 0) {
+                tc::gemm_tf32(tmem + COL_P, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);
+                tc::commit(barM);
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// Heads per CTA of chunk_output_heads: the largest block of one group's heads
+// that still gives every SM two CTAs.
+int heads_per_cta(const ChunkArgs& a, int sm_count) {
+    const int per_group = a.H / a.G;
+    for (int hb : {8, 6, 4, 3, 2}) {
+        if (per_group % hb != 0) continue;
+        if ((int64_t)a.B * a.NC * (a.H / hb) >= 2 * (int64_t)sm_count) return hb;
+    }
+    return 1;
+}
+
+template <bool PER_KEY, int DV>
+cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
+    constexpr bool HEADS = !PER_KEY && DV == 64;   // per-head decays: heads of a group share Q K^T
+    const size_t st_bytes = StateSmem<PER_KEY, DV>::bytes;
+    size_t out_bytes;
+    cudaError_t e = set_smem_attr_once((const void*)chunk_state<PER_KEY, DV>, st_bytes);
+    if (e != cudaSuccess) return e;
+    if constexpr (HEADS) {
+        out_bytes = HeadsSmem<DV>::bytes;
+        e = set_smem_attr_once((const void*)chunk_output_heads<DV>, out_bytes);
+    } else {
+        out_bytes = OutSmem<DV>::bytes;
+        e = set_smem_attr_once((const void*)chunk_output<PER_KEY, DV>, out_bytes);
+    }
+    if (e != cudaSuccess) return e;
+    const unsigned chunks = (unsigned)((size_t)a.B * a.H * a.NC);
+    chunk_state<PER_KEY, DV><<<chunks, NT, st_bytes, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t entries = (size_t)a.B * a.H * DKC * DV;
+    chunk_carry<<<(unsigned)((entries + 255) / 256), 256, 0, s>>>(a, DV);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if constexpr (HEADS) {
+        const int hb = heads_per_cta(a, sm_count);
+        chunk_output_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, out_bytes, s>>>(a, hb);
+    } else {
+        chunk_output<PER_KEY, DV><<<chunks, NT, out_bytes, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
+    const int64_t nc = (T + CH - 1) / CH;
+    return round256((int64_t)B * H * nc * dk * dv * 4) + 2 * round256((int64_t)B * H * nc * dk * 4);
+}
+
+bool chunked_supported(const RecurArgs& x) {
+    return (x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_HEAD) && x.dk == DKC && (x.dv == 64 || x.dv == 128);
+}
+
+cudaError_t launch_recur_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                 cudaStream_t s) {
+    ChunkArgs a{};
+    a.B = x.B; a.T = x.T; a.H = x.H; a.G = x.G;
+    a.NC = (x.T + CH - 1) / CH;
+    a.scale = x.scale;
+    a.q = x.q; a.k = x.k; a.v = x.v; a.d = x.g;
+    a.S_in = x.S_in; a.S_out = x.S_out; a.o = x.o;
+    char* p = static_cast<char*>(ws);
+    a.W = reinterpret_cast<float*>(p);
+    p += round256((int64_t)x.B * x.H * a.NC * x.dk * x.dv * 4);
+    a.gam = reinterpret_cast<float*>(p);
+    p += round256((int64_t)x.B * x.H * a.NC * x.dk * 4);
+    a.anc = reinterpret_cast<float*>(p);
+    a.st = st;
+    a.wait_ns = wait_ns;
+    const bool per_key = x.kind == RK_DIAG_KEY;
+    if (x.dv == 128) return per_key ? run_chunked<true, 128>(a, sm_count, s) : run_chunked<false, 128>(a, sm_count, s);
+    return per_key ? run_chunked<true, 64>(a, sm_count, s) : run_chunked<false, 64>(a, sm_count, s);
+}
+
+}  // namespace sn

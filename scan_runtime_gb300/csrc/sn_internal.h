@@ -22,6 +22,7 @@ enum SnKernelId : int {
     SN_K_SCAN_LOOKBACK = 2,
     SN_K_RECUR_SEQ = 3,
     SN_K_RECUR_DECODE = 4,
+    SN_K_RECUR_CHUNK = 5,
 };
 
 struct SnCtx {
@@ -125,5 +126,11 @@ cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t 
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);
+
+// Chunked tensor-core form of the diagonal-decay recurrence (recur_chunked.cu).
+int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv);
+bool chunked_supported(const RecurArgs& x);
+cudaError_t launch_recur_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                 cudaStream_t stream);
 
 }  // namespace sn

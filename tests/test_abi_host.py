@@ -78,13 +78,14 @@ def test_version_packing_and_check(abi):
 def test_caps_bits(abi):
     caps = abi.sn_abi_caps()
     for bit in (abi.SN_CAP_SCAN_FMA, abi.SN_CAP_SCAN_GATED, abi.SN_CAP_RECUR_DIAG, abi.SN_CAP_RECUR_DELTA,
-                abi.SN_CAP_RECUR_RWKV7, abi.SN_CAP_DECODE, abi.SN_CAP_SCAN_LOOKBACK, abi.SN_CAP_SCAN_BACKWARD):
+                abi.SN_CAP_RECUR_RWKV7, abi.SN_CAP_DECODE, abi.SN_CAP_SCAN_LOOKBACK, abi.SN_CAP_SCAN_BACKWARD,
+                abi.SN_CAP_RECUR_CHUNKED):
         assert caps & bit
-    assert caps & ~0xFF == 0            # no undocumented bits set
+    assert caps & ~0x1FF == 0           # no undocumented bits set
 
 
 def test_status_strings(abi):
-    for s in (0, -1, -2, -3, -4, -5, -6, -7):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert abi.sn_status_str(s) and abi.sn_status_str(s) != "unknown status"
     assert abi.sn_status_str(-99) == "unknown status"
 
