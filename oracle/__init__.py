@@ -73,6 +73,11 @@ def _load():
                 getattr(lib, f"orc_scan_gated_bwd_{prec}").argtypes = [i32, i32, i32] + [p] * 9
                 getattr(lib, f"orc_scan_fma_bwd_{prec}").restype = None
                 getattr(lib, f"orc_scan_gated_bwd_{prec}").restype = None
+            i64 = ctypes.c_int64
+            lib.orc_readout_norm_gate_f64.argtypes = [i64, i32, p, p, p, f64, p]
+            lib.orc_readout_norm_gate_f64.restype = None
+            lib.orc_readout_dskip_f64.argtypes = [i64, i32, i32, p, p, p, p]
+            lib.orc_readout_dskip_f64.restype = None
             for name in ("orc_recur_diag_f64", "orc_recur_diag_f32", "orc_recur_delta_f64",
                          "orc_recur_delta_f32", "orc_recur_rwkv7_f64", "orc_recur_rwkv7_f32"):
                 getattr(lib, name).restype = None
@@ -209,3 +214,28 @@ def recur_rwkv7(q, k, v, w, S0=None, *, prec="f64"):
     getattr(_load(), f"orc_recur_rwkv7_{prec}")(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                                                   _ptr(w), _ptr(S0), _ptr(S), _ptr(o))
     return o, S
+
+
+def readout_norm_gate(o, g, w=None, *, eps):
+    """GLA readout epilogue y = RMSNorm(o) * w * silu(g) over the last axis
+    (normalised first, gated after); o, g (..., dv), w (dv,) or None.
+    Returns y in float64."""
+    o, g = _f32(o), _f32(g)
+    assert o.shape == g.shape
+    dv = o.shape[-1]
+    w = None if w is None else _f32(w)
+    assert w is None or w.shape == (dv,)
+    y = np.empty(o.shape, np.float64)
+    _load().orc_readout_norm_gate_f64(o.size // dv, dv, _ptr(o), _ptr(g), _ptr(w), float(eps), _ptr(y))
+    return y
+
+
+def readout_dskip(o, x, D):
+    """Mamba-2 skip connection y = o + D_h x; o, x (B, T, H, dv), D (H,).
+    Returns y in float64."""
+    o, x, D = _f32(o), _f32(x), _f32(D)
+    assert o.shape == x.shape and o.ndim == 4 and D.shape == (o.shape[2],)
+    H, dv = o.shape[2], o.shape[3]
+    y = np.empty(o.shape, np.float64)
+    _load().orc_readout_dskip_f64(o.size // dv, H, dv, _ptr(o), _ptr(x), _ptr(D), _ptr(y))
+    return y

@@ -472,3 +472,41 @@ void orc_scan_gated_bwd_f32(i32 B, i32 T, i32 N, const float* a, const float* u,
 {
     orc_scan_bwd_f32(1, B, T, N, a, u, s0, s, gs, gf, da, du, ds0);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Readout epilogues: the step applied to the readout o_t.                   */
+/* ------------------------------------------------------------------------ */
+/* GLA output: y = RMSNorm(o) * silu(g), normalised first and gated after
+ * ([P1] §4.3).  Per row of dv values (one (b, t, h)):
+ *     ms  = (1 / dv) * sum_j o_j^2
+ *     y_j = o_j / sqrt(ms + eps) * w_j * g_j / (1 + exp(-g_j))
+ * with w the norm's per-channel weight (NULL = 1).  In double. */
+void orc_readout_norm_gate_f64(i64 rows, i32 dv, const float* o, const float* g, const float* w,
+                               double eps, double* y)
+{
+    for (i64 r = 0; r < rows; ++r) {
+        const float* orow = o + r * dv;
+        const float* grow = g + r * dv;
+        double ms = 0.0;
+        for (i32 j = 0; j < dv; ++j) ms += (double)orow[j] * (double)orow[j];
+        ms /= (double)dv;
+        const double inv = 1.0 / sqrt(ms + eps);
+        for (i32 j = 0; j < dv; ++j) {
+            const double gj = (double)grow[j];
+            const double silu = gj / (1.0 + exp(-gj));
+            const double wj = w ? (double)w[j] : 1.0;
+            y[r * dv + j] = (double)orow[j] * inv * wj * silu;
+        }
+    }
+}
+
+/* Mamba-2 skip connection: y = o + D_h * x for every row (b, t, h) of dv
+ * values, h = row mod H (rows ordered (b, t, h)).  In double. */
+void orc_readout_dskip_f64(i64 rows, i32 H, i32 dv, const float* o, const float* x, const float* D, double* y)
+{
+    for (i64 r = 0; r < rows; ++r) {
+        const double dh = (double)D[r % H];
+        for (i32 j = 0; j < dv; ++j)
+            y[r * dv + j] = (double)o[r * dv + j] + dh * (double)x[r * dv + j];
+    }
+}
