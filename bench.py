@@ -225,13 +225,18 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU arm
-def time_form(torch, fn, warmup, reps, stream):
-    """Median ms of `fn` over `reps` launches (CUDA events on `stream`)."""
+def time_form(torch, fn, warmup, reps, stream, flush=None):
+    """Median ms of `fn` over `reps` launches (CUDA events on `stream`).
+    `flush` (a tensor larger than L2) is overwritten on the stream before every
+    timed launch, outside the events, for workloads that would fit in L2."""
     for _ in range(warmup):
         fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     torch.cuda.synchronize()
     for s, e in ev:
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
         s.record(stream)
         fn()
         e.record(stream)
@@ -328,6 +333,31 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                         "tolerance": 2e-3}
                 assert ctx.last_error() == sr.SN_OK
             del x, o, S
+        # readout epilogues on the GLA and Mamba-2 output shapes (12 B per element);
+        # L2 is flushed before each timed launch (the GLA tensors fit in it)
+        flush = torch.empty(64 << 20, device=dev)          # 256 MB
+        gen = torch.Generator(dev).manual_seed(91)
+        for name, (Bc, Tc, H, dv) in (("gla_readout_norm_gate", (4, 4096, 4, 128)),
+                                      ("mamba2_readout_dskip", (4, 4096, 24, 64))):
+            o = torch.empty((Bc, Tc, H, dv), device=dev).normal_(generator=gen)
+            z = torch.empty((Bc, Tc, H, dv), device=dev).normal_(generator=gen)
+            y = torch.empty_like(o)
+            if name.endswith("norm_gate"):
+                w = torch.ones(dv, device=dev)
+                fn = lambda: sr.sn_readout_norm_gate(ctx.handle, Bc, Tc, H, dv, o, z, w, 1e-6, y, s)
+            else:
+                D = torch.ones(H, device=dev)
+                fn = lambda: sr.sn_readout_dskip(ctx.handle, Bc, Tc, H, dv, o, z, D, y, s)
+            st = fn()
+            if st != sr.SN_OK:
+                out[name] = {"error": sr.sn_status_str(st)}
+                continue
+            ms = time_form(torch, fn, warmup, reps, s, flush=flush)
+            nb = 12 * o.numel()
+            out[name] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
+                         "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm", "l2": "flushed"}
+            del o, z, y
+        del flush
     return out
 
 
@@ -513,6 +543,8 @@ PROFILE_CASES = {
     "rwkv7_decode": "RWKV-7 decode kernel, full decode workload B=1024 T=1 H=12 64x64",
     "gla_chunked": "chunked tensor-core form, full GLA workload B=4 T=4096 H=4 dk=dv=128",
     "mamba2_chunked": "chunked tensor-core form, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
+    "readout_norm_gate": "GLA readout epilogue RMSNorm(o)*w*silu(g), B=4 T=4096 H=24 dv=128 (fills past L2)",
+    "readout_dskip": "Mamba-2 skip connection o + D*x, B=4 T=4096 H=24 dv=64",
 }
 
 
@@ -540,6 +572,19 @@ def run_profile_case(args):
             ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_SEQUENTIAL)
         fn = lambda: sr.sn_scan_fma(h, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
         nbytes = scan_bytes(B, T, N)
+    elif name.startswith("readout_"):
+        Bc, Tc, H, dv = (4, 4096, 24, 128) if name.endswith("norm_gate") else (4, 4096, 24, 64)
+        gen = torch.Generator(dev).manual_seed(92)
+        o = torch.empty((Bc, Tc, H, dv), device=dev).normal_(generator=gen)
+        z = torch.empty((Bc, Tc, H, dv), device=dev).normal_(generator=gen)
+        y = torch.empty_like(o)
+        if name.endswith("norm_gate"):
+            w = torch.ones(dv, device=dev)
+            fn = lambda: sr.sn_readout_norm_gate(h, Bc, Tc, H, dv, o, z, w, 1e-6, y, s)
+        else:
+            D = torch.ones(H, device=dev)
+            fn = lambda: sr.sn_readout_dskip(h, Bc, Tc, H, dv, o, z, D, y, s)
+        nbytes = 12 * o.numel()
     elif name.endswith("_chunked"):
         base = name[:-len("_chunked")]
         c = synth.CONFIGS[base]

@@ -87,6 +87,7 @@ typedef int32_t sn_status;
 #define SN_CAP_SCAN_LOOKBACK (1u << 6) /* chunked scan with look-back carries */
 #define SN_CAP_SCAN_BACKWARD (1u << 7) /* sn_scan_fma_backward, sn_scan_gated_backward */
 #define SN_CAP_RECUR_CHUNKED (1u << 8) /* sn_recur_diag_chunked (tensor-core chunked form) */
+#define SN_CAP_READOUT       (1u << 9) /* sn_readout_norm_gate, sn_readout_dskip */
 
 /* Decay layouts of sn_recur_diag. */
 #define SN_DECAY_PER_KEY        0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
@@ -302,6 +303,30 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
  * states of dk x dv floats plus one decay vector of dk floats per chunk
  * (each part rounded up to 256 bytes); -1 on invalid arguments. */
 int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
+
+/* ---------------------------------------------------------------- readout epilogues */
+
+/* GLA readout epilogue ([P1] §4.3: the readout is followed by RMSNorm(o) and
+ * the output gate, normalised first and gated after), one pass per element:
+ *     y_j = o_j / sqrt(mean_j(o_j^2) + eps) * w_j * silu(g_j),
+ *     silu(z) = z / (1 + exp(-z)),
+ * with the mean over the dv values of each (b, t, h).
+ *   o, g, y : (B, T, H, dv); y may equal o (in place), no other overlap
+ *   w       : (dv,) norm weight shared by the heads, NULL = 1
+ *   eps     : >= 0 (eps = 0 and an all-zero row give NaN, as the definition)
+ * fp32 (rsqrt and exp from the CUDA math library); within 1e-5 normwise of
+ * the fp64 definition.  Requires dv in {64, 128} (else SN_E_UNSUPPORTED) and
+ * 16-byte aligned pointers.  Errors: SN_E_INVAL, SN_E_UNSUPPORTED, SN_E_DEVICE. */
+sn_status sn_readout_norm_gate(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dv,
+                               const float* o, const float* g, const float* w, float eps,
+                               float* y, void* stream);
+
+/* Mamba-2 skip connection added to each head's readout:
+ *     y = o + D_h * x,   one fused multiply-add per element.
+ *   o, x, y : (B, T, H, dv); y may equal o;  D : (H,)
+ * Requirements and errors as sn_readout_norm_gate. */
+sn_status sn_readout_dskip(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dv,
+                           const float* o, const float* x, const float* D, float* y, void* stream);
 
 /* ---------------------------------------------------------------- allocation-free variant */
 

@@ -196,6 +196,21 @@ class Context:
                                           oo, stream), "sn_recur_diag_chunked")
         return oo, So
 
+    def readout_norm_gate(self, o, g, w=None, *, eps, y=True, stream=None):
+        """GLA readout epilogue y = RMSNorm(o) * w * silu(g); o, g (B, T, H, dv).
+        Pass y=o to write in place."""
+        B, T, H, dv = o.shape
+        yy = self._out((B, T, H, dv), y)
+        _check(_abi.sn_readout_norm_gate(self.handle, B, T, H, dv, o, g, w, eps, yy, stream), "sn_readout_norm_gate")
+        return yy
+
+    def readout_dskip(self, o, x, D, *, y=True, stream=None):
+        """Mamba-2 skip connection y = o + D_h x; o, x (B, T, H, dv), D (H,)."""
+        B, T, H, dv = o.shape
+        yy = self._out((B, T, H, dv), y)
+        _check(_abi.sn_readout_dskip(self.handle, B, T, H, dv, o, x, D, yy, stream), "sn_readout_dskip")
+        return yy
+
     def recur_delta(self, q, k, v, beta, S_in=None, *, scale, S_out=True, o=True, stream=None):
         B, T, H, dk = k.shape
         dv = v.shape[3]

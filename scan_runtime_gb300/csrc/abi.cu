@@ -6,6 +6,7 @@
 // §6 (stable C ABI: sn_ prefix, opaque handles, packed version, capability
 // bits, int32 status codes and dimensions).
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -140,7 +141,8 @@ sn_status sn_abi_check(int32_t major) { return major == SN_ABI_VERSION_MAJOR ? S
 
 uint32_t sn_abi_caps(void) {
     return SN_CAP_SCAN_FMA | SN_CAP_SCAN_GATED | SN_CAP_RECUR_DIAG | SN_CAP_RECUR_DELTA | SN_CAP_RECUR_RWKV7 |
-           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK | SN_CAP_SCAN_BACKWARD | SN_CAP_RECUR_CHUNKED;
+           SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK | SN_CAP_SCAN_BACKWARD | SN_CAP_RECUR_CHUNKED |
+           SN_CAP_READOUT;
 }
 
 const char* sn_status_str(sn_status s) {
@@ -464,6 +466,48 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
     if (!g.ok) return SN_E_DEVICE;
     ctx->ws_dirty = true;   // the chunk states overwrite the look-back flag area
     return from_cuda(launch_recur_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ readout epilogues
+static sn_status readout_check(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dv, const void* const* ptrs,
+                               int nptr) {
+    if (ctx == nullptr || B <= 0 || T <= 0 || H <= 0 || dv <= 0) return SN_E_INVAL;
+    if ((int64_t)B * T * H * dv > kMaxElems) return SN_E_INVAL;
+    if (dv != 64 && dv != 128) return SN_E_UNSUPPORTED;
+    for (int i = 0; i < nptr; ++i)
+        if (ptrs[i] != nullptr && !aligned(ptrs[i], 16)) return SN_E_INVAL;
+    return SN_OK;
+}
+
+sn_status sn_readout_norm_gate(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dv, const float* o,
+                               const float* g, const float* w, float eps, float* y, void* stream) {
+    if (o == nullptr || g == nullptr || y == nullptr || !(eps >= 0.0f) || !std::isfinite(eps)) return SN_E_INVAL;
+    const void* ptrs[4] = {o, g, w, y};
+    const sn_status st = readout_check(ctx, B, T, H, dv, ptrs, 4);
+    if (st != SN_OK) return st;
+    const int64_t rows = (int64_t)B * T * H, big = rows * dv * 4;
+    const Buf bufs[4] = {{o, big, false}, {g, big, false}, {w, (int64_t)dv * 4, false}, {y, big, true}};
+    if (any_bad_overlap(bufs, 4, o, y)) return SN_E_INVAL;
+    DeviceGuard gd(ctx->device);
+    if (!gd.ok) return SN_E_DEVICE;
+    return from_cuda(launch_readout_norm_gate(rows, dv, o, g, w, eps, y, ctx->sm_count,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sn_status sn_readout_dskip(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dv, const float* o,
+                           const float* x, const float* D, float* y, void* stream) {
+    if (o == nullptr || x == nullptr || D == nullptr || y == nullptr) return SN_E_INVAL;
+    const void* ptrs[3] = {o, x, y};
+    const sn_status st = readout_check(ctx, B, T, H, dv, ptrs, 3);
+    if (st != SN_OK) return st;
+    if (!aligned(D, 4)) return SN_E_INVAL;
+    const int64_t rows = (int64_t)B * T * H, big = rows * dv * 4;
+    const Buf bufs[4] = {{o, big, false}, {x, big, false}, {D, (int64_t)H * 4, false}, {y, big, true}};
+    if (any_bad_overlap(bufs, 4, o, y)) return SN_E_INVAL;
+    DeviceGuard gd(ctx->device);
+    if (!gd.ok) return SN_E_DEVICE;
+    return from_cuda(launch_readout_dskip(rows, H, dv, o, x, D, y, ctx->sm_count,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -127,6 +127,12 @@ cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wa
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);
 
+// Readout epilogues (readout.cu).
+cudaError_t launch_readout_norm_gate(int64_t rows, int dv, const float* o, const float* g, const float* w, float eps,
+                                     float* y, int sm_count, cudaStream_t stream);
+cudaError_t launch_readout_dskip(int64_t rows, int H, int dv, const float* o, const float* x, const float* D,
+                                 float* y, int sm_count, cudaStream_t stream);
+
 // Chunked tensor-core form of the diagonal-decay recurrence (recur_chunked.cu).
 int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv);
 bool chunked_supported(const RecurArgs& x);
