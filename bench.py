@@ -314,6 +314,24 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                  "fp32_frac": round(tflops / fp32_peak_tflops, 3)}
             r["bound"] = "hbm" if name == "rwkv7_decode" else "alu"
             out[name] = r
+            if name == "deltanet":
+                # the chunked tensor-core delta rule on the same workload (tf32 operands)
+                ctx.ensure_workspace_bytes(sr.sn_recur_delta_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
+                fc = lambda: sr.sn_recur_delta_chunked(ctx.handle, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"],
+                                                       x["v"], x["beta"], None, S, o, s)
+                st = fc()
+                if st != sr.SN_OK:
+                    out["deltanet_chunked_tc"] = {"error": sr.sn_status_str(st)}
+                else:
+                    ms = time_form(torch, fc, warmup, reps, s)
+                    tf = delta_tensor_flops(Bc, Tc, H, dk, dv) / ms / 1e9
+                    out["deltanet_chunked_tc"] = {
+                        "ms": round(ms, 4), "tok_heads_per_s": round(th / ms * 1e3, 1),
+                        "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
+                        "TFLOPs_tf32": round(tf, 2), "tf32_frac": round(tf / tf32_peak_tflops(), 4),
+                        "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "latency",
+                        "tolerance": 2e-3}
+                assert ctx.last_error() == sr.SN_OK
             if name in ("gla", "mamba2"):
                 # the chunked tensor-core form of the same workload (tf32 operands)
                 ctx.ensure_workspace_bytes(sr.sn_recur_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
@@ -371,6 +389,18 @@ def chunked_tensor_flops(B, T, H, dk, dv):
     nch = B * H * ((T + CHUNK - 1) // CHUNK)
     C = CHUNK
     return nch * 2 * (C * C * dk + C * dv * dk + C * dv * C + dk * dv * C)
+
+
+def delta_tensor_flops(B, T, H, dk, dv):
+    """Tensor-core flops of the chunked delta rule per chunk of C tokens: the
+    Gram matrix K K^T three times (hi/lo split), W = T K, U = T V, W S_n,
+    K^T Delta, and the output products Q K^T, Q S_n and A Delta."""
+    nch = B * H * ((T + CHUNK - 1) // CHUNK)
+    C = CHUNK
+    prep = 3 * C * C * dk + C * C * dk + C * C * dv
+    chain = C * dk * dv + dk * C * dv
+    out = C * C * dk + C * dk * dv + C * C * dv
+    return nch * 2 * (prep + chain + out)
 
 
 def tf32_peak_tflops():
@@ -543,6 +573,7 @@ PROFILE_CASES = {
     "rwkv7_decode": "RWKV-7 decode kernel, full decode workload B=1024 T=1 H=12 64x64",
     "gla_chunked": "chunked tensor-core form, full GLA workload B=4 T=4096 H=4 dk=dv=128",
     "mamba2_chunked": "chunked tensor-core form, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
+    "deltanet_chunked": "chunked tensor-core delta rule, full DeltaNet workload B=4 T=4096 H=8 dk=dv=128",
     "readout_norm_gate": "GLA readout epilogue RMSNorm(o)*w*silu(g), B=4 T=4096 H=24 dv=128 (fills past L2)",
     "readout_dskip": "Mamba-2 skip connection o + D*x, B=4 T=4096 H=24 dv=64",
 }
@@ -585,6 +616,16 @@ def run_profile_case(args):
             D = torch.ones(H, device=dev)
             fn = lambda: sr.sn_readout_dskip(h, Bc, Tc, H, dv, o, z, D, y, s)
         nbytes = 12 * o.numel()
+    elif name == "deltanet_chunked":
+        c = synth.CONFIGS["deltanet"]
+        x = synth.config_inputs("deltanet", device=dev)
+        Bc, Tc, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
+        o = torch.empty((Bc, Tc, H, dv), device=dev)
+        S = torch.empty((Bc, H, dk, dv), device=dev)
+        ctx.ensure_workspace_bytes(sr.sn_recur_delta_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
+        fn = lambda: sr.sn_recur_delta_chunked(h, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"], x["v"], x["beta"],
+                                               None, S, o, s)
+        nbytes = matrix_cost("deltanet")[1]
     elif name.endswith("_chunked"):
         base = name[:-len("_chunked")]
         c = synth.CONFIGS[base]

@@ -88,6 +88,7 @@ typedef int32_t sn_status;
 #define SN_CAP_SCAN_BACKWARD (1u << 7) /* sn_scan_fma_backward, sn_scan_gated_backward */
 #define SN_CAP_RECUR_CHUNKED (1u << 8) /* sn_recur_diag_chunked (tensor-core chunked form) */
 #define SN_CAP_READOUT       (1u << 9) /* sn_readout_norm_gate, sn_readout_dskip */
+#define SN_CAP_DELTA_CHUNKED (1u << 10) /* sn_recur_delta_chunked (tensor-core chunked delta rule) */
 
 /* Decay layouts of sn_recur_diag. */
 #define SN_DECAY_PER_KEY        0   /* d is (B, T, H, dk): one decay per key row (GLA)        */
@@ -303,6 +304,33 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
  * states of dk x dv floats plus one decay vector of dk floats per chunk
  * (each part rounded up to 256 bytes); -1 on invalid arguments. */
 int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
+
+/* Chunked tensor-core form of sn_recur_delta: the same delta rule and readout
+ * ([P1] §4.2), evaluated T-parallel in chunks of 128 tokens.  Inside a chunk
+ * the deltas solve a unit lower-triangular system (the WY form of the chunk's
+ * rank-1 updates):
+ *     T = (I + diag(beta) L)^{-1} diag(beta),   L = strictly lower part of K K^T
+ *     Delta = T V - (T K) S_n,   S_{n+1} = S_n + K^T Delta,
+ *     O = scale * (Q S_n + tril(Q K^T) Delta)
+ * The Gram matrix uses a hi/lo tf32 split and the triangular inverse runs in
+ * fp32; the remaining products use tf32 operands with fp32 accumulation, and
+ * the state crosses chunks in fp32.
+ * Arguments and layouts as sn_recur_delta.  Accuracy about 1e-3 relative
+ * (tf32); splits at multiples of 128 tokens are bit-exact.  Requires dk = dv
+ * = 128 (else SN_E_UNSUPPORTED), 16-byte aligned pointers and a context
+ * workspace of at least sn_recur_delta_chunked_workspace_bytes() bytes (else
+ * SN_E_NOMEM), which the call overwrites. */
+sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
+                                 int32_t dk, int32_t dv, float scale,
+                                 const float* q, const float* k, const float* v,
+                                 const float* beta, const float* S_in, float* S_out,
+                                 float* o, void* stream);
+
+/* Workspace bytes sn_recur_delta_chunked needs: four tiles of dk x dv floats
+ * per chunk of 128 tokens and head (W, K^T, U and the chunk state) plus the
+ * deltas (B * T * H * dv floats), each part rounded up to 256 bytes; -1 on
+ * invalid arguments. */
+int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* ---------------------------------------------------------------- readout epilogues */
 

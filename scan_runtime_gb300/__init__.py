@@ -211,6 +211,20 @@ class Context:
         _check(_abi.sn_readout_dskip(self.handle, B, T, H, dv, o, x, D, yy, stream), "sn_readout_dskip")
         return yy
 
+    def recur_delta_chunked(self, q, k, v, beta, S_in=None, *, scale, S_out=True, o=True, stream=None):
+        """Chunked tensor-core form of recur_delta (tf32 operands); sizes the
+        context workspace on first use."""
+        B, T, H, dk = k.shape
+        dv = v.shape[3]
+        need = _abi.sn_recur_delta_chunked_workspace_bytes(B, T, H, dk, dv)
+        if need < 0:
+            raise SnError(_abi.SN_E_INVAL, "sn_recur_delta_chunked_workspace_bytes")
+        self.ensure_workspace_bytes(need)
+        So, oo = self._out((B, H, dk, dv), S_out), self._out((B, T, H, dv), o)
+        _check(_abi.sn_recur_delta_chunked(self.handle, B, T, H, dk, dv, scale, q, k, v, beta, S_in, So, oo, stream),
+               "sn_recur_delta_chunked")
+        return oo, So
+
     def recur_delta(self, q, k, v, beta, S_in=None, *, scale, S_out=True, o=True, stream=None):
         B, T, H, dk = k.shape
         dv = v.shape[3]

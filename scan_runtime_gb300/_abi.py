@@ -22,7 +22,7 @@ SN_OK, SN_E_INVAL, SN_E_NOMEM, SN_E_IO, SN_E_FORMAT, SN_E_UNSUPPORTED, SN_E_DEVI
 SN_E_RANGE = -8
 SN_CAP_SCAN_FMA, SN_CAP_SCAN_GATED, SN_CAP_RECUR_DIAG, SN_CAP_RECUR_DELTA = 1, 2, 4, 8
 SN_CAP_RECUR_RWKV7, SN_CAP_DECODE, SN_CAP_SCAN_LOOKBACK, SN_CAP_SCAN_BACKWARD = 16, 32, 64, 128
-SN_CAP_RECUR_CHUNKED, SN_CAP_READOUT = 256, 512
+SN_CAP_RECUR_CHUNKED, SN_CAP_READOUT, SN_CAP_DELTA_CHUNKED = 256, 512, 1024
 SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD, SN_DECAY_PER_KEY_GATED, SN_DECAY_PER_HEAD_GATED = 0, 1, 2, 3
 SN_OPT_SCAN_KERNEL, SN_OPT_WAIT_LIMIT_US, SN_OPT_DEBUG_POISON, SN_OPT_LOOKBACK_CHUNK, SN_OPT_RECUR_KERNEL = (
     1, 2, 3, 4, 5)
@@ -38,6 +38,7 @@ EXPORTS = (
     "sn_scan_fma", "sn_scan_gated", "sn_scan_fma_backward", "sn_scan_gated_backward",
     "sn_recur_diag", "sn_recur_delta", "sn_recur_rwkv7", "sn_scan_lookback_noalloc",
     "sn_recur_diag_chunked", "sn_recur_chunked_workspace_bytes", "sn_readout_norm_gate", "sn_readout_dskip",
+    "sn_recur_delta_chunked", "sn_recur_delta_chunked_workspace_bytes",
 )
 SN_NOALLOC_MAX_TILES = 40960
 
@@ -80,6 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "sn_recur_chunked_workspace_bytes": ([i32, i32, i32, i32, i32], i64),
             "sn_readout_norm_gate": ([p, i32, i32, i32, i32, p, p, p, f32, p, p], i32),
             "sn_readout_dskip": ([p, i32, i32, i32, i32, p, p, p, p, p], i32),
+            "sn_recur_delta_chunked": ([p, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
+            "sn_recur_delta_chunked_workspace_bytes": ([i32, i32, i32, i32, i32], i64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -221,3 +224,12 @@ def sn_readout_norm_gate(ctx, B, T, H, dv, o, g, w, eps, y, stream=None) -> int:
 
 def sn_readout_dskip(ctx, B, T, H, dv, o, x, D, y, stream=None) -> int:
     return load().sn_readout_dskip(ctx, B, T, H, dv, ptr(o), ptr(x), ptr(D), ptr(y), stream_handle(stream))
+
+
+def sn_recur_delta_chunked(ctx, B, T, H, dk, dv, scale, q, k, v, beta, S_in, S_out, o, stream=None) -> int:
+    return load().sn_recur_delta_chunked(ctx, B, T, H, dk, dv, scale, ptr(q), ptr(k), ptr(v), ptr(beta), ptr(S_in),
+                                         ptr(S_out), ptr(o), stream_handle(stream))
+
+
+def sn_recur_delta_chunked_workspace_bytes(B, T, H, dk, dv) -> int:
+    return load().sn_recur_delta_chunked_workspace_bytes(B, T, H, dk, dv)

@@ -142,7 +142,7 @@ sn_status sn_abi_check(int32_t major) { return major == SN_ABI_VERSION_MAJOR ? S
 uint32_t sn_abi_caps(void) {
     return SN_CAP_SCAN_FMA | SN_CAP_SCAN_GATED | SN_CAP_RECUR_DIAG | SN_CAP_RECUR_DELTA | SN_CAP_RECUR_RWKV7 |
            SN_CAP_DECODE | SN_CAP_SCAN_LOOKBACK | SN_CAP_SCAN_BACKWARD | SN_CAP_RECUR_CHUNKED |
-           SN_CAP_READOUT;
+           SN_CAP_READOUT | SN_CAP_DELTA_CHUNKED;
 }
 
 const char* sn_status_str(sn_status s) {
@@ -467,6 +467,30 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
     ctx->ws_dirty = true;   // the chunk states overwrite the look-back flag area
     return from_cuda(launch_recur_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, float scale,
+                                 const float* q, const float* k, const float* v, const float* beta,
+                                 const float* S_in, float* S_out, float* o, void* stream) {
+    RecurArgs x{};
+    x.kind = RK_DELTA;
+    x.B = B; x.T = T; x.H = H; x.G = H; x.dk = dk; x.dv = dv; x.scale = scale;
+    x.q = q; x.k = k; x.v = v; x.g = beta; x.S_in = S_in; x.S_out = S_out; x.o = o;
+    x.state_transposed = false;
+    const sn_status st = recur_validate(ctx, x);
+    if (st != SN_OK) return st;
+    if (!delta_chunked_supported(x)) return SN_E_UNSUPPORTED;
+    const int64_t need = delta_chunked_ws_bytes(B, T, H, dk, dv);
+    if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SN_E_DEVICE;
+    ctx->ws_dirty = true;   // the chunk tiles overwrite the look-back flag area
+    return from_cuda(launch_delta_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {
+    if (B <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    return delta_chunked_ws_bytes(B, T, H, dk, dv);
 }
 
 // ------------------------------------------------------------------ readout epilogues

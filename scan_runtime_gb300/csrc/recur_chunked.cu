@@ -48,123 +48,12 @@
 // Shared-memory operands use the K-major no-swizzle core-matrix layout of
 // tc.cuh with K extent 128 (every contraction here has K = 128: keys, or the
 // chunk's tokens).
-#include <cmath>
-
-#include "ptx.cuh"
-#include "sn_internal.h"
-#include "tc.cuh"
+#include "chunk_common.cuh"
 
 namespace sn {
 namespace {
 
-constexpr int CH = 128;                 // tokens per chunk
-constexpr int DKC = 128;                // key dimension
-constexpr int NT = 256;                 // threads per CTA
-constexpr int ANCHOR = CH / 2 - 1;      // anchor token of the per-key factors
-constexpr float RANGE_LOG2 = 60.0f;     // bound on |lam_t - lam_anchor| (log2 units)
-constexpr int OPF = CH * DKC;           // floats per 128 x 128 operand
-constexpr unsigned FULL = 0xffffffffu;
-
-struct ChunkArgs {
-    int B, T, H, G, NC;
-    float scale;
-    const float* q;
-    const float* k;
-    const float* v;
-    const float* d;
-    const float* S_in;
-    float* S_out;
-    float* o;
-    float* W;       // per (b, h, chunk) a dv x dk tile in operand layout: dS^T, then S'^T
-    float* gam;     // (B, H, NC, dk): chunk decay gamma_n per key
-    float* anc;     // (B, H, NC, dk): anchor factor 2^{lam_m} (1 for per-head decays)
-    SnDevStatus* st;
-    uint64_t wait_ns;
-};
-
-// sites recorded with SN_E_TIMEOUT / SN_E_RANGE
-constexpr int SITE_STATE_WAIT = 1, SITE_OUT_WAIT1 = 2, SITE_OUT_WAIT2 = 3, SITE_RANGE_KEY = 4,
-              SITE_RANGE_HEAD = 5, SITE_OUT_COPY = 6;
-
-__device__ __forceinline__ int off128(int r, int k) {
-    return (r >> 3) * 1024 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3);
-}
-
-__device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 tf32x4(float a, float b, float c, float d) {
-    return make_float4(tc::to_tf32(a), tc::to_tf32(b), tc::to_tf32(c), tc::to_tf32(d));
-}
-__device__ __forceinline__ float4 tf32x4(float4 x) { return tf32x4(x.x, x.y, x.z, x.w); }
-
-// cp.async of 4 / 16 bytes; `valid` false writes zeros (the source is not read).
-__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(valid ? 4 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// Base-2 exponential and logarithm from the SFU instructions (ex2.approx /
-// lg2.approx, relative error ~2^-22; subnormals flush to zero): far below the
-// tf32 rounding of the operands they scale.
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float lg2(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float* align128(unsigned char* p) {
-    return reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p) + 127) & ~uintptr_t(127));
-}
-
-struct ChunkIdx {
-    int b, h, n, g, t0, nval;
-    size_t bh;
-};
-
-__device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a) {
-    ChunkIdx c;
-    c.h = blockIdx.x % a.H;
-    const int bn = blockIdx.x / a.H;
-    c.n = bn % a.NC;
-    c.b = bn / a.NC;
-    c.g = c.h / (a.H / a.G);
-    c.t0 = c.n * CH;
-    c.nval = min(CH, a.T - c.t0);
-    c.bh = (size_t)c.b * a.H + c.h;
-    return c;
-}
-
-// Transposing copy of a (tokens x R) slab of a row-major global array into the
-// operand layout (rows = the R columns of the array, K = tokens): element
-// (t, r) of rows base[t * rs + r] lands at off128(r, t).  Lanes cover 8 rows x
-// 4 tokens (32 distinct banks); tokens >= nval are zero.
-template <int R>
-__device__ __forceinline__ void copy_transposed(float* dst, const float* base, size_t rs, int nval, int warp,
-                                                int lane) {
-    const int rl = lane & 7, tq = lane >> 3;
-    constexpr int RB = R / 8;
-#pragma unroll 8
-    for (int p = warp; p < RB * (CH / 4); p += NT / 32) {
-        const int r = (p % RB) * 8 + rl;
-        const int t = (p / RB) * 4 + tq;
-        const bool ok = t < nval;
-        cp_async4(dst + off128(r, t), base + (size_t)(ok ? t : 0) * rs + r, ok);
-    }
-}
+using namespace chunk;
 
 // ------------------------------------------------------------------ chunk_state
 template <bool PER_KEY, int DV>
@@ -214,7 +103,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * lane + r;
-            lg[r] = t < c.nval ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
+            lg[r] = (t < c.nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
             s += lg[r];
         }
         float x = s;
@@ -486,7 +375,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * lane + r;
-            lg[r] = t < c.nval ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
+            lg[r] = (t < c.nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
             s += lg[r];
         }
         float x = s;
@@ -699,7 +588,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * lane + r;
-            lg[r] = t < nval ? lg2(__ldg(a.d + (row0 + t) * a.H + h)) : 0.f;
+            lg[r] = (t < nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + h)) : 0.f;
             s += lg[r];
         }
         float x = s;
@@ -889,6 +778,17 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
+
+// The output stage alone with unit decays (a.d == nullptr, per-head path):
+// o = scale (Q S_n + tril(Q K^T) V) for every chunk, with V and the chunk
+// states S_n (operand layout, tf32) supplied by the caller; dv = 128.
+cudaError_t chunk::launch_output_unit_decay(const ChunkArgs& a, cudaStream_t s) {
+    const size_t bytes = OutSmem<128>::bytes;
+    const cudaError_t e = set_smem_attr_once((const void*)chunk_output<false, 128>, bytes);
+    if (e != cudaSuccess) return e;
+    chunk_output<false, 128><<<(unsigned)((size_t)a.B * a.H * a.NC), NT, bytes, s>>>(a);
+    return cudaGetLastError();
+}
 
 int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;

@@ -1,0 +1,467 @@
+// recur_delta_chunked.cu -- chunked tensor-core form of the DeltaNet delta rule
+//     delta_t = beta_t (v_t - S_{t-1}^T k_t),   S_t = S_{t-1} + k_t delta_t^T,
+//     o_t = scale * S_t^T q_t
+// ("SunnyNet 工程化实录" §4.2, "我拿同一份权重和 llama.cpp 正面比了一场" §3),
+// the T-parallel counterpart of recur_seq<RK_DELTA>.
+//
+// Within a chunk of C = 128 tokens starting from state S_n, the deltas solve a
+// unit lower-triangular system: delta_t = beta_t (v_t - S_n^T k_t -
+// sum_{j<t} (k_t . k_j) delta_j).  With L the strictly lower part of K K^T,
+//     T = (I + diag(beta) L)^{-1} diag(beta),   W = T K,   U = T V
+//     Delta   = U - W S_n                     (the chunk's deltas, C x dv)
+//     S_{n+1} = S_n + K^T Delta
+//     O       = scale * (Q S_n + tril(Q K^T) Delta)      (j <= t)
+// (the WY / UT form of a product of rank-1 updates).  Three launches:
+//   delta_prep    one CTA per chunk: the Gram matrix K K^T on tcgen05 with a
+//                 hi/lo tf32 split (three products, close to fp32), the
+//                 triangular inverse in fp32 on the CUDA cores (16 x 16
+//                 diagonal blocks by forward substitution, then block rows),
+//                 W = T K and U = T V on tcgen05; writes W, U and K^T tiles;
+//   delta_chain   one CTA per (batch, head), chunks in order: the state S^T
+//                 stays in fp32 registers; per chunk the products W S_n and
+//                 K^T Delta run on tcgen05 (tf32 operands); writes every
+//                 chunk's Delta (in v's layout) and S_n (operand layout);
+//   chunk_output  the output kernel of the diagonal-decay form with unit
+//                 decays (recur_chunked.cu), with Delta in place of v.
+// Supported: dk = dv = 128.  Results carry tf32 rounding (about 1e-3
+// relative); splits at multiples of 128 tokens are bit-exact because the state
+// crosses chunks in fp32.
+#include "chunk_common.cuh"
+
+namespace sn {
+namespace {
+
+using namespace chunk;
+
+constexpr int LD = CH + 1;          // row stride of the fp32 triangular matrices
+constexpr int BSZ = 16;             // diagonal block size of the inverse
+constexpr int NBLK = CH / BSZ;
+constexpr int SITE_PREP_WAIT1 = 7, SITE_PREP_WAIT2 = 8, SITE_CHAIN_WAIT = 9;
+
+struct DeltaArgs {
+    int B, T, H, NC;
+    const float* k;
+    const float* v;
+    const float* beta;
+    const float* S_in;
+    float* S_out;
+    float* Wt;      // per chunk: W (rows t, K = key), operand layout, tf32
+    float* KTt;     // per chunk: K^T (rows key, K = t), operand layout, tf32
+    float* Ut;      // per chunk: U, row-major [t][value]
+    float* Dl;      // the deltas, (B, T, H, dv) like v
+    float* St;      // per chunk: S_n^T (rows value, K = key), operand layout, tf32
+    SnDevStatus* st;
+    uint64_t wait_ns;
+};
+
+// ------------------------------------------------------------------ delta_prep
+struct PrepSmem {
+    static constexpr int b0 = 0;                 // K (hi), then K^T operand
+    static constexpr int b1 = OPF;               // K (lo), then A (fp32, stride LD), then V^T operand
+    static constexpr int b2 = OPF + CH * LD;     // X = (I + A)^{-1} (fp32, stride LD), then T operand
+    static constexpr int rt = OPF + 2 * CH * LD; // one block row of partial products (16 x LD)
+    static constexpr int beta = rt + BSZ * LD;
+    static constexpr int misc = beta + CH;
+    static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
+};
+
+__global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = PrepSmem;
+    float* base = align128(smem_raw);
+    float* buf0 = base + L::b0;
+    float* buf1 = base + L::b1;
+    float* buf2 = base + L::b2;
+    float* Rt = base + L::rt;
+    float* beta_s = base + L::beta;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x % a.H;
+    const int bn = blockIdx.x / a.H;
+    const int n = bn % a.NC, b = bn / a.NC;
+    const int t0 = n * CH, nval = min(CH, a.T - t0);
+    const size_t bh = (size_t)b * a.H + h;
+    const size_t row0 = (size_t)b * a.T + t0;
+    const size_t tile = (bh * a.NC + n) * (size_t)OPF;
+    const size_t krs = (size_t)a.H * DKC;
+
+    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+
+    // K rows straight into the operand layout (rows t, K = key); beta
+    const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
+    {
+        const float* kb = a.k + row0 * krs + (size_t)h * DKC + ic;
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            const int t = 8 * tb + tl;
+            const bool ok = t < nval;
+            cp_async16(buf0 + off128(t, ic), kb + (size_t)(ok ? t : 0) * krs, ok);
+        }
+        cp_async_commit();
+    }
+    if (tid < CH) beta_s[tid] = tid < nval ? __ldg(a.beta + (row0 + tid) * a.H + h) : 0.f;
+    cp_async_wait_all();
+    __syncthreads();
+
+    // K = hi + lo, both tf32: K K^T ~ hi hi^T + hi lo^T + lo hi^T
+#pragma unroll
+    for (int tb = 0; tb < CH / 8; ++tb) {
+        const int o = off128(8 * tb + tl, ic);
+        const float4 x = ld4(buf0 + o);
+        const float4 hi = tf32x4(x);
+        st4(buf0 + o, hi);
+        st4(buf1 + o, tf32x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w));
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    if (tid == 0) {
+        const uint32_t id = tc::idesc_tf32(128, 128);
+        tc::gemm_tf32(tmem, buf0, buf0, DKC, id, false);
+        tc::gemm_tf32(tmem, buf0, buf1, DKC, id, true);
+        tc::gemm_tf32(tmem, buf1, buf0, DKC, id, true);
+        tc::commit(bar);
+    }
+    bool ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
+    tc::fence_after_sync();
+    const int lq = warp & 3, hf = warp >> 2;
+    const int tr = 32 * lq + lane;                           // tensor-memory row of this thread
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    if (ok) {
+        // the K^T operand can stream in now (buf0's hi part is consumed)
+        copy_transposed<DKC>(buf0, a.k + row0 * krs + (size_t)h * DKC, krs, nval, warp, lane);
+        cp_async_commit();
+
+        // A = diag(beta) strict_lower(K K^T) in fp32; X = I
+        float* Am = buf1;
+        float* Xm = buf2;
+        const float bt = beta_s[tr];
+#pragma unroll
+        for (int j0 = 64 * hf; j0 < 64 * hf + 64; j0 += 16) {
+            float x[16];
+            tc::ld16(lane_base + j0, x);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) Am[tr * LD + j0 + jj] = j0 + jj < tr ? bt * x[jj] : 0.f;
+        }
+        for (int e = tid; e < CH * LD; e += NT) Xm[e] = (e / LD == e % LD) ? 1.f : 0.f;
+        __syncthreads();
+
+        // diagonal blocks of X = (I + A)^{-1}: forward substitution, warp w -> block w,
+        // X[r][c] = -sum_{c <= m < r} A[r][m] X[m][c]
+        {
+            const int r0 = BSZ * warp;
+            for (int r = 1; r < BSZ; ++r) {
+                if (lane < r) {
+                    float acc = 0.f;
+                    for (int m = lane; m < r; ++m)
+                        acc = fmaf(Am[(r0 + r) * LD + r0 + m], Xm[(r0 + m) * LD + r0 + lane], acc);
+                    Xm[(r0 + r) * LD + r0 + lane] = -acc;
+                }
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        // block rows: X_ij = -X_ii sum_{j <= k < i} A_ik X_kj
+        for (int i = 1; i < NBLK; ++i) {
+            for (int e = tid; e < i * BSZ * BSZ; e += NT) {
+                const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                float acc = 0.f;
+                for (int k = j; k < i; ++k)
+#pragma unroll
+                    for (int m = 0; m < BSZ; ++m)
+                        acc = fmaf(Am[(BSZ * i + r) * LD + BSZ * k + m], Xm[(BSZ * k + m) * LD + BSZ * j + cc], acc);
+                Rt[r * LD + BSZ * j + cc] = acc;
+            }
+            __syncthreads();
+            for (int e = tid; e < i * BSZ * BSZ; e += NT) {
+                const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                float acc = 0.f;
+                for (int m = 0; m <= r; ++m)
+                    acc = fmaf(Xm[(BSZ * i + r) * LD + BSZ * i + m], Rt[m * LD + BSZ * j + cc], acc);
+                Xm[(BSZ * i + r) * LD + BSZ * j + cc] = -acc;
+            }
+            __syncthreads();
+        }
+
+        // A is consumed: the V^T operand streams into its buffer
+        copy_transposed<128>(buf1, a.v + row0 * (size_t)a.H * 128 + (size_t)h * 128, (size_t)a.H * 128, nval, warp,
+                             lane);
+        cp_async_commit();
+
+        // T = X diag(beta) as the tf32 operand (rows t, K = j), in place through registers
+        float4 tv[CH / 8];
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            const int t = 8 * tb + tl;
+            const float* xr = Xm + t * LD + ic;
+            tv[tb] = tf32x4(xr[0] * beta_s[ic], xr[1] * beta_s[ic + 1], xr[2] * beta_s[ic + 2], xr[3] * beta_s[ic + 3]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) st4(buf2 + off128(8 * tb + tl, ic), tv[tb]);
+
+        cp_async_wait_all();
+        __syncthreads();
+        for (int f = tid; f < OPF / 4; f += NT) {
+            st4(buf0 + 4 * f, tf32x4(ld4(buf0 + 4 * f)));
+            st4(buf1 + 4 * f, tf32x4(ld4(buf1 + 4 * f)));
+        }
+    } else if (tid == 0) {
+        record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_PREP_WAIT1);
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (ok) {
+        if (tid == 0) {
+            const uint32_t id = tc::idesc_tf32(128, 128);
+            tc::gemm_tf32(tmem, buf2, buf0, CH, id, false);          // W = T K   (cols 0..127)
+            tc::gemm_tf32(tmem + 128, buf2, buf1, CH, id, false);    // U = T V   (cols 128..255)
+            tc::commit(bar);
+        }
+        ok = __syncthreads_and(mbar_wait(bar, 1, a.wait_ns));
+        tc::fence_after_sync();
+        if (ok) {
+            float* wt = a.Wt + tile;
+            float* ut = a.Ut + tile;
+#pragma unroll
+            for (int i0 = 64 * hf; i0 < 64 * hf + 64; i0 += 16) {
+                float x[16];
+                tc::ld16(lane_base + i0, x);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st4(wt + off128(tr, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+                tc::ld16(lane_base + 128 + i0, x);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st4(ut + tr * 128 + i0 + 4 * q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+            }
+            if (tid == 0) {   // the K^T operand as it stands (tf32) for the chain kernel
+                bulk_store(a.KTt + tile, buf0, OPF * 4);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+        } else if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_PREP_WAIT2);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------ delta_chain
+struct ChainSmem {
+    static constexpr int w_off = 0;          // W_n (rows t, K = key)
+    static constexpr int kt_off = OPF;       // K_n^T (rows key, K = t)
+    static constexpr int su_off = 2 * OPF;   // S_n^T (rows value, K = key), then Delta^T (rows value, K = t)
+    static constexpr int misc = 3 * OPF;
+    static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
+};
+
+__global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = ChainSmem;
+    float* base = align128(smem_raw);
+    float* Wb = base + L::w_off;
+    float* KTb = base + L::kt_off;
+    float* SUb = base + L::su_off;
+    uint64_t* barW = reinterpret_cast<uint64_t*>(base + L::misc);
+    uint64_t* barK = reinterpret_cast<uint64_t*>(base + L::misc + 2);
+    uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc + 4);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 6);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const size_t bh = blockIdx.x;
+    const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+    const int c = tid & 127, part = tid >> 7;     // value column, half of the keys / tokens
+    const int lq = warp & 3;                      // tensor-memory lanes 32 lq .. : rows c
+    const int NC = a.NC;
+    auto tile = [&](const float* p, int n) { return p + (bh * NC + n) * (size_t)OPF; };
+
+    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (tid == 0) {
+        mbar_init(barW, 1);
+        mbar_init(barK, 1);
+        mbar_init(barM, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(barW, OPF * 4);
+        bulk_load(Wb, tile(a.Wt, 0), OPF * 4, barW);
+        mbar_arrive_expect_tx(barK, OPF * 4);
+        bulk_load(KTb, tile(a.KTt, 0), OPF * 4, barK);
+    }
+
+    // S^T[c][i] for this part's 64 keys, fp32 in registers for the whole sequence
+    float sreg[64];
+    const size_t sbase = bh * (size_t)(DKC * 128);
+#pragma unroll
+    for (int r = 0; r < 64; ++r) sreg[r] = a.S_in != nullptr ? a.S_in[sbase + (size_t)(64 * part + r) * 128 + c] : 0.f;
+    auto put_state = [&](int n) {   // tf32 S_n^T into the operand buffer and the chunk's state tile
+        float* stile = a.St + (bh * NC + n) * (size_t)OPF;
+#pragma unroll
+        for (int r4 = 0; r4 < 16; ++r4) {
+            const int i = 64 * part + 4 * r4;
+            const float4 v = tf32x4(sreg[4 * r4], sreg[4 * r4 + 1], sreg[4 * r4 + 2], sreg[4 * r4 + 3]);
+            st4(SUb + off128(c, i), v);
+            st4(stile + off128(c, i), v);
+        }
+    };
+    float u[64];
+    auto load_u = [&](int n) {
+        const float* ut = tile(a.Ut, n);
+#pragma unroll
+        for (int r = 0; r < 64; ++r) u[r] = ut[(64 * part + r) * 128 + c];
+    };
+    put_state(0);
+    load_u(0);
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    const uint32_t id = tc::idesc_tf32(128, 128);
+    uint32_t mpar = 0;
+    int w_loads = 1, k_loads = 1;   // bulk loads issued on barW / barK (thread 0's count)
+    bool ok = true;
+    int n = 0;
+    for (; n < NC; ++n) {
+        ok = __syncthreads_and(mbar_wait(barW, n & 1, a.wait_ns));
+        if (!ok) break;
+        if (tid == 0) {   // P[c][t] = sum_i S^T[c][i] W[t][i]  (= (W S_n)^T)
+            tc::gemm_tf32(tmem, SUb, Wb, DKC, id, false);
+            tc::commit(barM);
+        }
+        ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
+        mpar ^= 1;
+        tc::fence_after_sync();
+        if (!ok) break;
+        if (tid == 0 && n + 1 < NC) {
+            mbar_arrive_expect_tx(barW, OPF * 4);
+            bulk_load(Wb, tile(a.Wt, n + 1), OPF * 4, barW);
+            ++w_loads;
+        }
+        // Delta^T[c][t] = U[t][c] - P[c][t] for this part's tokens
+        const int t0 = n * CH;
+#pragma unroll
+        for (int q0 = 0; q0 < 64; q0 += 16) {
+            float x[16];
+            tc::ld16(lane_base + 64 * part + q0, x);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                x[jj] = u[q0 + jj] - x[jj];
+                const int t = 64 * part + q0 + jj;
+                if (t0 + t < a.T) a.Dl[(((size_t)b * a.T + t0 + t) * a.H + h) * 128 + c] = x[jj];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st4(SUb + off128(c, 64 * part + q0 + 4 * q),
+                    tf32x4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        ok = __syncthreads_and(mbar_wait(barK, n & 1, a.wait_ns));
+        tc::fence_after_sync();
+        if (!ok) break;
+        if (tid == 0) {   // D[c][i] = sum_t Delta^T[c][t] K^T[i][t]  (= (K^T Delta)^T)
+            tc::gemm_tf32(tmem + 128, SUb, KTb, CH, id, false);
+            tc::commit(barM);
+        }
+        if (n + 1 < NC) load_u(n + 1);
+        ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
+        mpar ^= 1;
+        tc::fence_after_sync();
+        if (!ok) break;
+        if (tid == 0 && n + 1 < NC) {
+            mbar_arrive_expect_tx(barK, OPF * 4);
+            bulk_load(KTb, tile(a.KTt, n + 1), OPF * 4, barK);
+            ++k_loads;
+        }
+#pragma unroll
+        for (int q0 = 0; q0 < 64; q0 += 16) {
+            float x[16];
+            tc::ld16(lane_base + 128 + 64 * part + q0, x);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) sreg[q0 + jj] += x[jj];
+        }
+        if (n + 1 < NC) put_state(n + 1);
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    if (!ok) {
+        if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_CHAIN_WAIT);
+            // let copies still in flight land before the CTA exits
+            mbar_wait(barW, (w_loads - 1) & 1, a.wait_ns);
+            mbar_wait(barK, (k_loads - 1) & 1, a.wait_ns);
+        }
+    } else if (a.S_out != nullptr) {
+#pragma unroll
+        for (int r = 0; r < 64; ++r) a.S_out[sbase + (size_t)(64 * part + r) * 128 + c] = sreg[r];
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
+    const int64_t nc = (T + CH - 1) / CH;
+    return 4 * round256((int64_t)B * H * nc * dk * dv * 4) + round256((int64_t)B * T * H * dv * 4);
+}
+
+bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && x.dk == DKC && x.dv == 128; }
+
+cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, cudaStream_t s) {
+    DeltaArgs d{};
+    d.B = x.B; d.T = x.T; d.H = x.H;
+    d.NC = (x.T + CH - 1) / CH;
+    d.k = x.k; d.v = x.v; d.beta = x.g;
+    d.S_in = x.S_in; d.S_out = x.S_out;
+    const int64_t tile_bytes = round256((int64_t)x.B * x.H * d.NC * OPF * 4);
+    char* p = static_cast<char*>(ws);
+    d.Wt = reinterpret_cast<float*>(p);
+    d.KTt = reinterpret_cast<float*>(p + tile_bytes);
+    d.Ut = reinterpret_cast<float*>(p + 2 * tile_bytes);
+    d.St = reinterpret_cast<float*>(p + 3 * tile_bytes);
+    d.Dl = reinterpret_cast<float*>(p + 4 * tile_bytes);
+    d.st = st;
+    d.wait_ns = wait_ns;
+
+    cudaError_t e = set_smem_attr_once((const void*)delta_prep, PrepSmem::bytes);
+    if (e != cudaSuccess) return e;
+    e = set_smem_attr_once((const void*)delta_chain, ChainSmem::bytes);
+    if (e != cudaSuccess) return e;
+    delta_prep<<<(unsigned)((size_t)x.B * x.H * d.NC), NT, PrepSmem::bytes, s>>>(d);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    delta_chain<<<(unsigned)((size_t)x.B * x.H), NT, ChainSmem::bytes, s>>>(d);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || x.o == nullptr) return e;
+
+    ChunkArgs c{};
+    c.B = x.B; c.T = x.T; c.H = x.H; c.G = x.H; c.NC = d.NC;
+    c.scale = x.scale;
+    c.q = x.q; c.k = x.k; c.v = d.Dl; c.d = nullptr;
+    c.S_in = nullptr; c.S_out = nullptr; c.o = x.o;
+    c.W = d.St; c.gam = nullptr; c.anc = nullptr;
+    c.st = st;
+    c.wait_ns = wait_ns;
+    return launch_output_unit_decay(c, s);
+}
+
+}  // namespace sn

@@ -127,6 +127,11 @@ cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wa
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);
 
+// Chunked tensor-core form of the delta rule (recur_delta_chunked.cu).
+int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv);
+bool delta_chunked_supported(const RecurArgs& x);
+cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, cudaStream_t stream);
+
 // Readout epilogues (readout.cu).
 cudaError_t launch_readout_norm_gate(int64_t rows, int dv, const float* o, const float* g, const float* w, float eps,
                                      float* y, int sm_count, cudaStream_t stream);

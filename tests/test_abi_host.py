@@ -79,9 +79,9 @@ def test_caps_bits(abi):
     caps = abi.sn_abi_caps()
     for bit in (abi.SN_CAP_SCAN_FMA, abi.SN_CAP_SCAN_GATED, abi.SN_CAP_RECUR_DIAG, abi.SN_CAP_RECUR_DELTA,
                 abi.SN_CAP_RECUR_RWKV7, abi.SN_CAP_DECODE, abi.SN_CAP_SCAN_LOOKBACK, abi.SN_CAP_SCAN_BACKWARD,
-                abi.SN_CAP_RECUR_CHUNKED, abi.SN_CAP_READOUT):
+                abi.SN_CAP_RECUR_CHUNKED, abi.SN_CAP_READOUT, abi.SN_CAP_DELTA_CHUNKED):
         assert caps & bit
-    assert caps & ~0x3FF == 0           # no undocumented bits set
+    assert caps & ~0x7FF == 0           # no undocumented bits set
 
 
 def test_status_strings(abi):

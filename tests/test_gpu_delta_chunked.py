@@ -1,0 +1,133 @@
+"""GPU parity of the chunked tensor-core delta rule (sn_recur_delta_chunked)
+against the fp64 oracle.
+
+Bar: o and the final state within 2e-3 normwise of the fp64 oracle (tf32
+operands, as for the chunked diagonal-decay form); splits at multiples of the
+128-token chunk bit-exact within the GPU path; beta = 1 with unit keys keeps
+the retrieval identity S_t^T k_t = v_t that the oracle's pins fix.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+CHUNK = 128
+
+
+@pytest.fixture(scope="module")
+def sr():
+    import scan_runtime_gb300 as sr
+    sr.build()
+    return sr
+
+
+@pytest.fixture()
+def ctx(sr):
+    c = sr.Context(0)
+    yield c
+    assert c.last_error() == sr.SN_OK
+    c.close()
+
+
+def _nrel(x, r):
+    x = np.asarray(x, np.float64)
+    r = np.asarray(r, np.float64)
+    return float(np.max(np.abs(x - r)) / max(float(np.max(np.abs(r))), 1e-30))
+
+
+def cu(t):
+    return None if t is None else t.cuda()
+
+
+def run(ctx, x, S0=None, **kw):
+    o, S = ctx.recur_delta_chunked(*(cu(x[n]) for n in ("q", "k", "v", "beta")), cu(S0), scale=x["scale"], **kw)
+    torch.cuda.synchronize()
+    return (None if o is None else o.cpu().numpy()), (None if S is None else S.cpu().numpy())
+
+
+def ref(x, S0=None):
+    return oracle.recur_delta(*(x[n].numpy() for n in ("q", "k", "v", "beta")),
+                              None if S0 is None else S0.numpy().astype(np.float64), scale=x["scale"])
+
+
+@pytest.mark.parametrize("T", [1, 5, 127, 128, 129, 300, 640])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_parity(ctx, T, with_state):
+    B, H = 2, 3
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=400 + T % 7)
+    S0 = synth.normal((B, H, 128, 128), 8000 + T) * 0.5 if with_state else None
+    o, S = run(ctx, x, S0)
+    ro, rS = ref(x, S0)
+    assert _nrel(o, ro) <= TOL
+    assert _nrel(S, rS) <= TOL
+
+
+def test_unit_beta_retrieves_the_value(ctx):
+    """beta = 1 and |k| = 1: S_t^T k_t = v_t after every step, so the last
+    token's key reads back its value from the final state."""
+    B, T, H = 1, 200, 2
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=410)
+    x = dict(x, beta=torch.ones_like(x["beta"]))
+    _, S = run(ctx, x)
+    k_last = x["k"][:, -1].numpy().astype(np.float64)           # (B, H, dk)
+    got = np.einsum("bhij,bhi->bhj", S.astype(np.float64), k_last)
+    assert _nrel(got, x["v"][:, -1].numpy()) <= TOL
+
+
+@pytest.mark.parametrize("split", [CHUNK, 2 * CHUNK])
+def test_split_at_chunk_multiple_is_bit_exact(ctx, split):
+    B, T, H = 2, 600, 2
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=420)
+    S0 = synth.normal((B, H, 128, 128), 8100) * 0.5
+    o, S = run(ctx, x, S0)
+    first = {n: (x[n][:, :split].contiguous() if n in ("q", "k", "v", "beta") else x[n]) for n in x}
+    rest = {n: (x[n][:, split:].contiguous() if n in ("q", "k", "v", "beta") else x[n]) for n in x}
+    o1, S1 = run(ctx, first, S0)
+    o2, S2 = run(ctx, rest, torch.from_numpy(S1))
+    assert np.array_equal(np.concatenate([o1, o2], axis=1), o)
+    assert np.array_equal(S2, S)
+
+
+def test_optional_outputs(ctx):
+    x = synth.deltanet_inputs(1, 300, 2, 128, 128, cid=430)
+    o, S = run(ctx, x)
+    o2, S2 = run(ctx, x, o=False)
+    assert o2 is None and np.array_equal(S2, S)
+    o3, S3 = run(ctx, x, S_out=False)
+    assert S3 is None and np.array_equal(o3, o)
+
+
+def test_full_size_sampled_heads(ctx):
+    """The full DeltaNet workload (B4 T4096 H8 128x128) in the launch
+    configuration the benchmark times; sampled heads recomputed by the oracle."""
+    x = synth.config_inputs("deltanet")
+    o, S = run(ctx, x)
+    rng = np.random.default_rng(41)
+    heads = sorted({(int(rng.integers(4)), int(rng.integers(8))) for _ in range(3)} | {(0, 0), (3, 7)})
+    for (b, h) in heads:
+        xs = {n: x[n][b:b + 1, :, h:h + 1].contiguous() for n in ("q", "k", "v", "beta")}
+        xs["scale"] = x["scale"]
+        ro, rS = ref(xs)
+        assert _nrel(o[b:b + 1, :, h:h + 1], ro) <= TOL
+        assert _nrel(S[b:b + 1, h:h + 1], rS) <= TOL
+
+
+def test_unsupported_and_missing_workspace(ctx, sr):
+    abi = sr._abi
+    x = synth.deltanet_inputs(1, 16, 1, 64, 64, cid=440)
+    q, k, v, beta = (cu(x[n]) for n in ("q", "k", "v", "beta"))
+    o = torch.empty((1, 16, 1, 64), device="cuda")
+    assert abi.sn_recur_delta_chunked(ctx.handle, 1, 16, 1, 64, 64, 1.0, q, k, v, beta, None, None, o) == \
+        sr.SN_E_UNSUPPORTED
+    x = synth.deltanet_inputs(1, 16, 1, 128, 128, cid=441)
+    q, k, v, beta = (cu(x[n]) for n in ("q", "k", "v", "beta"))
+    o = torch.empty((1, 16, 1, 128), device="cuda")
+    assert abi.sn_recur_delta_chunked(ctx.handle, 1, 16, 1, 128, 128, 1.0, q, k, v, beta, None, None, o) == \
+        sr.SN_E_NOMEM
+    assert abi.sn_recur_delta_chunked_workspace_bytes(1, 0, 1, 128, 128) == -1
+    torch.cuda.synchronize()
