@@ -15,8 +15,9 @@
 //   delta_prep    one CTA per chunk: the Gram matrix K K^T on tcgen05 with a
 //                 hi/lo tf32 split (three products, close to fp32), the
 //                 triangular inverse in fp32 on the CUDA cores (16 x 16
-//                 diagonal blocks by forward substitution, then block rows),
-//                 W = T K and U = T V on tcgen05; writes W, U and K^T tiles;
+//                 diagonal blocks by column-wise substitution in registers,
+//                 then block rows as register-tiled strips), W = T K and
+//                 U = T V on tcgen05; writes W, U and K^T tiles;
 //   delta_chain   one CTA per (batch, head), chunks in order: the state S^T
 //                 stays in fp32 registers; per chunk the products W S_n and
 //                 K^T Delta run on tcgen05 (tf32 operands); writes every
@@ -33,7 +34,7 @@ namespace {
 
 using namespace chunk;
 
-constexpr int LD = CH + 1;          // row stride of the fp32 triangular matrices
+constexpr int LDX = CH + 4;         // row stride of A^T and X (rows of float4)
 constexpr int BSZ = 16;             // diagonal block size of the inverse
 constexpr int NBLK = CH / BSZ;
 constexpr int SITE_PREP_WAIT1 = 7, SITE_PREP_WAIT2 = 8, SITE_CHAIN_WAIT = 9;
@@ -57,10 +58,9 @@ struct DeltaArgs {
 // ------------------------------------------------------------------ delta_prep
 struct PrepSmem {
     static constexpr int b0 = 0;                 // K (hi), then K^T operand
-    static constexpr int b1 = OPF;               // K (lo), then A (fp32, stride LD), then V^T operand
-    static constexpr int b2 = OPF + CH * LD;     // X = (I + A)^{-1} (fp32, stride LD), then T operand
-    static constexpr int rt = OPF + 2 * CH * LD; // one block row of partial products (16 x LD)
-    static constexpr int beta = rt + BSZ * LD;
+    static constexpr int b1 = OPF;               // K (lo), then A^T (fp32, stride LDX), then V^T operand
+    static constexpr int b2 = b1 + CH * LDX;     // X = (I + A)^{-1} (fp32, stride LDX), then T operand
+    static constexpr int beta = b2 + CH * LDX;
     static constexpr int misc = beta + CH;
     static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
 };
@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
     float* buf0 = base + L::b0;
     float* buf1 = base + L::b1;
     float* buf2 = base + L::b2;
-    float* Rt = base + L::rt;
     float* beta_s = base + L::beta;
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 2);
@@ -140,8 +139,8 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
         copy_transposed<DKC>(buf0, a.k + row0 * krs + (size_t)h * DKC, krs, nval, warp, lane);
         cp_async_commit();
 
-        // A = diag(beta) strict_lower(K K^T) in fp32; X = I
-        float* Am = buf1;
+        // A = diag(beta) strict_lower(K K^T) in fp32, stored transposed: AT[j][t] = A[t][j]
+        float* AT = buf1;
         float* Xm = buf2;
         const float bt = beta_s[tr];
 #pragma unroll
@@ -149,44 +148,78 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
             float x[16];
             tc::ld16(lane_base + j0, x);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) Am[tr * LD + j0 + jj] = j0 + jj < tr ? bt * x[jj] : 0.f;
+            for (int jj = 0; jj < 16; ++jj) AT[(j0 + jj) * LDX + tr] = j0 + jj < tr ? bt * x[jj] : 0.f;
         }
-        for (int e = tid; e < CH * LD; e += NT) Xm[e] = (e / LD == e % LD) ? 1.f : 0.f;
         __syncthreads();
 
-        // diagonal blocks of X = (I + A)^{-1}: forward substitution, warp w -> block w,
-        // X[r][c] = -sum_{c <= m < r} A[r][m] X[m][c]
+        // diagonal blocks of X = (I + A)^{-1}, warp w -> block w, in registers: a
+        // lane holds column c of rows rb, rb + 2, ..., and column by column
+        // X[r][c] -= A[r][m] X[m][c] for r > m once X[m][c] is final
         {
-            const int r0 = BSZ * warp;
-            for (int r = 1; r < BSZ; ++r) {
-                if (lane < r) {
-                    float acc = 0.f;
-                    for (int m = lane; m < r; ++m)
-                        acc = fmaf(Am[(r0 + r) * LD + r0 + m], Xm[(r0 + m) * LD + r0 + lane], acc);
-                    Xm[(r0 + r) * LD + r0 + lane] = -acc;
+            const int r0 = BSZ * warp, c = lane & 15, rb = lane >> 4;
+            float xr[BSZ / 2];
+#pragma unroll
+            for (int jj = 0; jj < BSZ / 2; ++jj) xr[jj] = (rb + 2 * jj == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < BSZ - 1; ++m) {
+                const float xm = __shfl_sync(FULL, xr[m >> 1], (m & 1) * 16 + c);
+#pragma unroll
+                for (int jj = 0; jj < BSZ / 2; ++jj) {
+                    const int r = rb + 2 * jj;
+                    if (r > m) xr[jj] = fmaf(-AT[(r0 + m) * LDX + r0 + r], xm, xr[jj]);
                 }
-                __syncwarp();
             }
+#pragma unroll
+            for (int jj = 0; jj < BSZ / 2; ++jj) Xm[(r0 + rb + 2 * jj) * LDX + r0 + c] = xr[jj];
         }
         __syncthreads();
-        // block rows: X_ij = -X_ii sum_{j <= k < i} A_ik X_kj
+        // block rows: X_ij = -X_ii sum_{j <= k < i} A_ik X_kj.  A group of KS = 8
+        // adjacent lanes owns one 16 x 4 column strip of the block row: the
+        // lanes split the sum over k (one float4 of X and four of A^T feed 64
+        // FMAs), join it with xor shuffles, and each lane then multiplies two
+        // rows of X_ii into the strip.  One barrier per block row.
         for (int i = 1; i < NBLK; ++i) {
-            for (int e = tid; e < i * BSZ * BSZ; e += NT) {
-                const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-                float acc = 0.f;
-                for (int k = j; k < i; ++k)
+            constexpr int KS = 8;
+            const int cq = 4 * i;                          // column quads (strips) of the block row
+            if (tid < cq * KS) {                           // 32 i threads: whole warps
+                const int s4 = tid / KS, part = tid % KS;
+                float acc[BSZ][4] = {};
+                for (int kk = BSZ * (s4 >> 2) + part; kk < BSZ * i; kk += KS) {
+                    const float4 x4 = ld4(Xm + kk * LDX + 4 * s4);
+                    const float* ap = AT + kk * LDX + BSZ * i;       // A[16 i + r][kk], r = 0..15
 #pragma unroll
-                    for (int m = 0; m < BSZ; ++m)
-                        acc = fmaf(Am[(BSZ * i + r) * LD + BSZ * k + m], Xm[(BSZ * k + m) * LD + BSZ * j + cc], acc);
-                Rt[r * LD + BSZ * j + cc] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < i * BSZ * BSZ; e += NT) {
-                const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m)
-                    acc = fmaf(Xm[(BSZ * i + r) * LD + BSZ * i + m], Rt[m * LD + BSZ * j + cc], acc);
-                Xm[(BSZ * i + r) * LD + BSZ * j + cc] = -acc;
+                    for (int r4 = 0; r4 < BSZ / 4; ++r4) {
+                        const float4 a4 = ld4(ap + 4 * r4);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float* o = acc[4 * r4 + q];
+                            o[0] = fmaf(av[q], x4.x, o[0]); o[1] = fmaf(av[q], x4.y, o[1]);
+                            o[2] = fmaf(av[q], x4.z, o[2]); o[3] = fmaf(av[q], x4.w, o[3]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int off = KS / 2; off > 0; off >>= 1)
+#pragma unroll
+                    for (int r = 0; r < BSZ; ++r)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[r][c] += __shfl_xor_sync(FULL, acc[r][c], off);
+#pragma unroll
+                for (int rr = 0; rr < BSZ / KS; ++rr) {
+                    const int r = part * (BSZ / KS) + rr;
+                    const float* xd = Xm + (BSZ * i + r) * LDX + BSZ * i;   // row r of X_ii
+                    float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int m = 0; m < BSZ; ++m) {
+                        if (m <= r) {
+                            const float xv = xd[m];
+                            out.x = fmaf(xv, acc[m][0], out.x); out.y = fmaf(xv, acc[m][1], out.y);
+                            out.z = fmaf(xv, acc[m][2], out.z); out.w = fmaf(xv, acc[m][3], out.w);
+                        }
+                    }
+                    st4(Xm + (BSZ * i + r) * LDX + 4 * s4, make_float4(-out.x, -out.y, -out.z, -out.w));
+                }
             }
             __syncthreads();
         }
@@ -201,8 +234,13 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
 #pragma unroll
         for (int tb = 0; tb < CH / 8; ++tb) {
             const int t = 8 * tb + tl;
-            const float* xr = Xm + t * LD + ic;
-            tv[tb] = tf32x4(xr[0] * beta_s[ic], xr[1] * beta_s[ic + 1], xr[2] * beta_s[ic + 2], xr[3] * beta_s[ic + 3]);
+            // blocks right of the diagonal block are never written: X is zero there
+            if ((ic >> 4) > (t >> 4)) {
+                tv[tb] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                const float4 x4 = ld4(Xm + t * LDX + ic), b4 = ld4(beta_s + ic);
+                tv[tb] = tf32x4(x4.x * b4.x, x4.y * b4.y, x4.z * b4.z, x4.w * b4.w);
+            }
         }
         __syncthreads();
 #pragma unroll
