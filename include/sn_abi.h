@@ -326,10 +326,10 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
                                  const float* beta, const float* S_in, float* S_out,
                                  float* o, void* stream);
 
-/* Workspace bytes sn_recur_delta_chunked needs: four tiles of dk x dv floats
- * per chunk of 128 tokens and head (W, K^T, U and the chunk state) plus the
- * deltas (B * T * H * dv floats), each part rounded up to 256 bytes; -1 on
- * invalid arguments. */
+/* Workspace bytes sn_recur_delta_chunked needs: five tiles of dk x dv floats
+ * per chunk of 128 tokens and head (W, K^T, U, the chunk state and the
+ * chunk's deltas), each kind rounded up to 256 bytes; -1 on invalid
+ * arguments. */
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* ---------------------------------------------------------------- readout epilogues */

@@ -34,6 +34,8 @@ struct ChunkArgs {
     float* W;       // per (b, h, chunk) a dv x dk tile in operand layout: dS^T, then S'^T
     float* gam;     // (B, H, NC, dk): chunk decay gamma_n per key
     float* anc;     // (B, H, NC, dk): anchor factor 2^{lam_m} (1 for per-head decays)
+    const float* vt;   // optional: per chunk a v^T operand tile (rows value, K = token, tf32)
+                       // that replaces v in the output stage (bulk-loaded)
     SnDevStatus* st;
     uint64_t wait_ns;
 };

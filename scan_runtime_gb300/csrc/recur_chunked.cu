@@ -316,10 +316,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
     cp_async_commit();
 
     // v slice for the last product, in registers: thread = value column, a run of tokens
+    // (unless the caller supplies the v^T operand tiles)
     constexpr int TP = CH / (NT / DV);
     const int col = tid % DV, part = tid / DV;
     float vr[TP];
-    {
+    if (a.vt == nullptr) {
         const size_t vrs = (size_t)a.H * DV;
         const float* vcol = a.v + row0 * vrs + (size_t)c.h * DV + col;
 #pragma unroll
@@ -435,6 +436,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
     if (ok) {
         ok = __syncthreads_and(mbar_wait(barM, 0, a.wait_ns));
         tc::fence_after_sync();
+        if (ok && a.vt != nullptr && tid == 0) {   // the K buffer is free: the v^T tile streams in
+            mbar_arrive_expect_tx(barS, DV * CH * 4);
+            bulk_load(bufK, a.vt + (c.bh * a.NC + c.n) * (size_t)DV * CH, DV * CH * 4, barS);
+        }
         if (ok) {
             const float lt = PER_KEY ? 0.f : lam_s[t];
             // masked (and, per head, decay-weighted) A into the Q buffer as the next A operand
@@ -452,17 +457,26 @@ __global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
                 for (int q = 0; q < 4; ++q)
                     st4(bufQ + off128(t, j0 + 4 * q), tf32x4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
             }
+            if (a.vt == nullptr) {
 #pragma unroll
-            for (int t4 = 0; t4 < TP / 4; ++t4)
-                st4(bufK + off128(col, part * TP + 4 * t4),
-                    tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
+                for (int t4 = 0; t4 < TP / 4; ++t4)
+                    st4(bufK + off128(col, part * TP + 4 * t4),
+                        tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
+            }
         } else if (tid == 0) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT1);
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
+        const bool vok = __syncthreads_and(!ok || a.vt == nullptr || mbar_wait(barS, 1, a.wait_ns));
         tc::fence_after_sync();
+        if (ok && !vok) {
+            if (tid == 0) {
+                record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
+                mbar_wait(barS, 1, a.wait_ns);   // let a late copy land before the CTA exits
+            }
+            ok = false;
+        }
     }
     if (ok) {
         if (tid == 0) {

@@ -20,10 +20,10 @@
 //                 U = T V on tcgen05; writes W, U and K^T tiles;
 //   delta_chain   one CTA per (batch, head), chunks in order: the state S^T
 //                 stays in fp32 registers; per chunk the products W S_n and
-//                 K^T Delta run on tcgen05 (tf32 operands); writes every
-//                 chunk's Delta (in v's layout) and S_n (operand layout);
+//                 K^T Delta run on tcgen05 (tf32 operands); the operand tiles
+//                 of every chunk's Delta^T and S_n^T leave by bulk stores;
 //   chunk_output  the output kernel of the diagonal-decay form with unit
-//                 decays (recur_chunked.cu), with Delta in place of v.
+//                 decays (recur_chunked.cu), bulk-loading Delta^T in place of v.
 // Supported: dk = dv = 128.  Results carry tf32 rounding (about 1e-3
 // relative); splits at multiples of 128 tokens are bit-exact because the state
 // crosses chunks in fp32.
@@ -49,7 +49,7 @@ struct DeltaArgs {
     float* Wt;      // per chunk: W (rows t, K = key), operand layout, tf32
     float* KTt;     // per chunk: K^T (rows key, K = t), operand layout, tf32
     float* Ut;      // per chunk: U, row-major [t][value]
-    float* Dl;      // the deltas, (B, T, H, dv) like v
+    float* DTt;     // per chunk: Delta^T (rows value, K = t), operand layout, tf32
     float* St;      // per chunk: S_n^T (rows value, K = key), operand layout, tf32
     SnDevStatus* st;
     uint64_t wait_ns;
@@ -320,7 +320,6 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const size_t bh = blockIdx.x;
-    const int b = (int)(bh / a.H), h = (int)(bh % a.H);
     const int c = tid & 127, part = tid >> 7;     // value column, half of the keys / tokens
     const int lq = warp & 3;                      // tensor-memory lanes 32 lq .. : rows c
     const int NC = a.NC;
@@ -343,15 +342,16 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
     const size_t sbase = bh * (size_t)(DKC * 128);
 #pragma unroll
     for (int r = 0; r < 64; ++r) sreg[r] = a.S_in != nullptr ? a.S_in[sbase + (size_t)(64 * part + r) * 128 + c] : 0.f;
-    auto put_state = [&](int n) {   // tf32 S_n^T into the operand buffer and the chunk's state tile
-        float* stile = a.St + (bh * NC + n) * (size_t)OPF;
+    auto put_state = [&]() {   // tf32 S_n^T into the operand buffer (then bulk-stored as the chunk's tile)
 #pragma unroll
         for (int r4 = 0; r4 < 16; ++r4) {
             const int i = 64 * part + 4 * r4;
-            const float4 v = tf32x4(sreg[4 * r4], sreg[4 * r4 + 1], sreg[4 * r4 + 2], sreg[4 * r4 + 3]);
-            st4(SUb + off128(c, i), v);
-            st4(stile + off128(c, i), v);
+            st4(SUb + off128(c, i), tf32x4(sreg[4 * r4], sreg[4 * r4 + 1], sreg[4 * r4 + 2], sreg[4 * r4 + 3]));
         }
+    };
+    auto store_tile = [&](float* tiles, int n) {   // thread 0: the operand buffer -> a chunk's tile
+        bulk_store(tiles + (bh * NC + n) * (size_t)OPF, SUb, OPF * 4);
+        bulk_commit();
     };
     float u[64];
     auto load_u = [&](int n) {
@@ -359,12 +359,13 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
 #pragma unroll
         for (int r = 0; r < 64; ++r) u[r] = ut[(64 * part + r) * 128 + c];
     };
-    put_state(0);
+    put_state();
     load_u(0);
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (tid == 0) store_tile(a.St, 0);
     const uint32_t tmem = *slot;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     const uint32_t id = tc::idesc_tf32(128, 128);
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         if (tid == 0) {   // P[c][t] = sum_i S^T[c][i] W[t][i]  (= (W S_n)^T)
             tc::gemm_tf32(tmem, SUb, Wb, DKC, id, false);
             tc::commit(barM);
+            bulk_wait_read_all();   // the S_n tile store has read the buffer the deltas overwrite
         }
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
@@ -389,17 +391,12 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
             ++w_loads;
         }
         // Delta^T[c][t] = U[t][c] - P[c][t] for this part's tokens
-        const int t0 = n * CH;
 #pragma unroll
         for (int q0 = 0; q0 < 64; q0 += 16) {
             float x[16];
             tc::ld16(lane_base + 64 * part + q0, x);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                x[jj] = u[q0 + jj] - x[jj];
-                const int t = 64 * part + q0 + jj;
-                if (t0 + t < a.T) a.Dl[(((size_t)b * a.T + t0 + t) * a.H + h) * 128 + c] = x[jj];
-            }
+            for (int jj = 0; jj < 16; ++jj) x[jj] = u[q0 + jj] - x[jj];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 st4(SUb + off128(c, 64 * part + q0 + 4 * q),
@@ -413,8 +410,10 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         if (tid == 0) {   // D[c][i] = sum_t Delta^T[c][t] K^T[i][t]  (= (K^T Delta)^T)
             tc::gemm_tf32(tmem + 128, SUb, KTb, CH, id, false);
             tc::commit(barM);
+            store_tile(a.DTt, n);
         }
         if (n + 1 < NC) load_u(n + 1);
+        if (tid == 0) bulk_wait_read_all();   // the Delta^T tile store has read the buffer
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
         tc::fence_after_sync();
@@ -431,12 +430,14 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) sreg[q0 + jj] += x[jj];
         }
-        if (n + 1 < NC) put_state(n + 1);
+        if (n + 1 < NC) put_state();
         fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
+        if (tid == 0 && n + 1 < NC) store_tile(a.St, n + 1);
     }
+    if (tid == 0) bulk_wait_all();   // every tile store complete before the CTA exits
     if (!ok) {
         if (tid == 0) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_CHAIN_WAIT);
@@ -459,7 +460,7 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;
-    return 4 * round256((int64_t)B * H * nc * dk * dv * 4) + round256((int64_t)B * T * H * dv * 4);
+    return 5 * round256((int64_t)B * H * nc * dk * dv * 4);
 }
 
 bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && x.dk == DKC && x.dv == 128; }
@@ -476,7 +477,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     d.KTt = reinterpret_cast<float*>(p + tile_bytes);
     d.Ut = reinterpret_cast<float*>(p + 2 * tile_bytes);
     d.St = reinterpret_cast<float*>(p + 3 * tile_bytes);
-    d.Dl = reinterpret_cast<float*>(p + 4 * tile_bytes);
+    d.DTt = reinterpret_cast<float*>(p + 4 * tile_bytes);
     d.st = st;
     d.wait_ns = wait_ns;
 
@@ -494,7 +495,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     ChunkArgs c{};
     c.B = x.B; c.T = x.T; c.H = x.H; c.G = x.H; c.NC = d.NC;
     c.scale = x.scale;
-    c.q = x.q; c.k = x.k; c.v = d.Dl; c.d = nullptr;
+    c.q = x.q; c.k = x.k; c.v = nullptr; c.vt = d.DTt; c.d = nullptr;
     c.S_in = nullptr; c.S_out = nullptr; c.o = x.o;
     c.W = d.St; c.gam = nullptr; c.anc = nullptr;
     c.st = st;
