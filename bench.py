@@ -225,6 +225,42 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU arm
+def link_bandwidth(torch, dev, nbytes=1 << 30, reps=4):
+    """Pinned host <-> device copy rates of this machine (GB/s): each direction
+    alone and both at once on two streams.  They bound the end-to-end step."""
+    n = nbytes // 4
+    h_in, h_out = torch.empty(n, pin_memory=True), torch.empty(n, pin_memory=True)
+    d_in, d_out = torch.empty(n, device=dev), torch.empty(n, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    gb = nbytes / 1e9
+    out = {"h2d_GBps": round(gb / timed(h2d), 1), "d2h_GBps": round(gb / timed(d2h), 1),
+           "concurrent_each_GBps": round(gb / timed(both), 1)}
+    del h_in, h_out, d_in, d_out
+    return out
+
+
 def time_form(torch, fn, warmup, reps, stream, flush=None):
     """Median ms of `fn` over `reps` launches (CUDA events on `stream`).
     `flush` (a tensor larger than L2) is overwritten on the stream before every
@@ -509,9 +545,14 @@ def run_ours(args):
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dev)
         h2d = 3 * B * T * N * 4 + B * N * 4
         d2h = 2 * B * T * N * 4 + 2 * B * N * 4
+        link = link_bandwidth(torch, dev)
+        # the step cannot beat moving its bytes over the host link, both directions at once
+        bound_ms = max(h2d, d2h) / (link["concurrent_each_GBps"] * 1e6)
         e2e = {"value": round(whole_job_gbps(step_bytes, 1, world, e2e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-               "api": "Context.scan_host (3 streams, one batch row per chunk)"}
+               "api": "Context.scan_host (3 streams, one batch row per chunk)",
+               "link": link, "link_bound_ms_per_step": round(bound_ms, 3),
+               "link_frac": round(bound_ms / e2e_ms, 3)}
         del host, hout
 
     forms = None
