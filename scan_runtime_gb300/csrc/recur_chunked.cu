@@ -596,13 +596,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
             vr[r] = t < nval ? __ldg(vcol + (size_t)t * vrs) : 0.f;
         }
     };
-    // warp 0: inclusive prefix sums of log2 d of head h into dst
-    auto head_lam = [&](int h, float* dst) {
-        float lg[4], s = 0.f;
+    // warp 0: a head's decays, four tokens per lane, loaded one step ahead of
+    // their prefix sums so that the load latency hides behind other work
+    float dr[4];
+    auto head_d = [&](int h) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * lane + r;
-            lg[r] = (t < nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + h)) : 0.f;
+            dr[r] = (t < nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + h) : 1.f;
+        }
+    };
+    // warp 0: inclusive prefix sums of log2 d of the loaded head into dst
+    auto head_lam = [&](float* dst) {
+        float lg[4], s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            lg[r] = lg2(dr[r]);
             s += lg[r];
         }
         float x = s;
@@ -620,7 +629,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
         if (lane == 31 && !isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
     };
     load_v(h0);
-    if (warp == 0) head_lam(h0, lam2);
+    if (warp == 0) {
+        head_d(h0);
+        head_lam(lam2);
+    }
 
     cp_async_wait_all();
     {
@@ -656,6 +668,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     for (int hi = 0; hi < hb && ok; ++hi) {
         const int h = h0 + hi;
         const float* lam = lam2 + (hi & 1) * CH;
+        if (warp == 0 && hi + 1 < hb) head_d(h + 1);
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
         tc::fence_after_sync();
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
         }
         if (hi + 1 < hb) {   // next head's v and decay sums while the product runs
             load_v(h + 1);
-            if (warp == 0) head_lam(h + 1, lam2 + ((hi + 1) & 1) * CH);
+            if (warp == 0) head_lam(lam2 + ((hi + 1) & 1) * CH);
         }
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
