@@ -607,6 +607,8 @@ PROFILE_CASES = {
     "scan_seq": "sequential scan (FMA), B=8 T=2048 N=2048 (402 MB moved, > L2)",
     "scan_seq_full": "sequential scan (FMA), full workload B=8 T=8192 N=2048 (1.61 GB moved)",
     "scan_lookback": "look-back scan (FMA), B=8 T=2048 N=2048",
+    "scan_bwd_fma": "reverse scan (FMA form), B=8 T=2048 N=2048 (20 B per element)",
+    "scan_bwd_gated": "reverse scan (gated form), B=8 T=2048 N=2048 (24 B per element)",
     "gla": "diag per-key, full GLA workload B=4 T=4096 H=4 dk=dv=128",
     "mamba2": "diag per-head, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
     "deltanet": "delta rule, full DeltaNet workload B=4 T=4096 H=8 dk=dv=128",
@@ -632,7 +634,22 @@ def run_profile_case(args):
     s = torch.cuda.Stream(dev)
     name = args.profile_case
     h = ctx.handle
-    if name.startswith("scan"):
+    if name.startswith("scan_bwd"):
+        B, T, N = 8, 2048, 2048
+        x = synth.scan_inputs(B, T, N, large=True, device=dev)
+        so = torch.empty((B, T, N), device=dev)
+        sf = torch.empty((B, N), device=dev)
+        sr.sn_scan_fma(h, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
+        gs_ = torch.empty((B, T, N), device=dev).normal_(generator=torch.Generator(dev).manual_seed(77))
+        da, db = torch.empty((B, T, N), device=dev), torch.empty((B, T, N), device=dev)
+        d0 = torch.empty((B, N), device=dev)
+        if name.endswith("gated"):
+            fn = lambda: sr.sn_scan_gated_backward(h, B, T, N, x["a"], x["u"], x["s0"], so, gs_, None, da, db, d0, s)
+            nbytes = 24 * B * T * N + 8 * B * N
+        else:
+            fn = lambda: sr.sn_scan_fma_backward(h, B, T, N, x["a"], x["s0"], so, gs_, None, da, db, d0, s)
+            nbytes = 20 * B * T * N + 8 * B * N
+    elif name.startswith("scan"):
         B, T, N = (8, 8192, 2048) if name.endswith("_full") else (8, 2048, 2048)
         x = synth.scan_inputs(B, T, N, large=True, device=dev)
         so = torch.empty((B, T, N), device=dev)

@@ -37,6 +37,31 @@ template <bool GATED>
 constexpr uint32_t sb_stage_bytes() { return sb_tensors<GATED>() * SB_TILE * 4; }
 template <bool GATED>
 constexpr size_t sb_smem() { return sb_stages<GATED>() * sb_stage_bytes<GATED>() + 2 * sb_stages<GATED>() * 8 + 16; }
+// One interior stage of the consumer (no sequence edge inside, every row
+// valid), rows SB_TS - 1 down to 0, in the same operation order as the edge
+// path.  WA / WB select whether grad_a and grad_b|u are stored; pa, pb point
+// at this lane's element of the stage's first row, rows N floats apart.
+template <bool GATED, bool WA, bool WB>
+__device__ __forceinline__ void bwd_stage(const float* A, const float* Gs, const float* Sp, const float* U,
+                                          float* pa, float* pb, size_t N, float& g, float& an) {
+#pragma unroll
+    for (int i = SB_TS - 1; i >= 0; --i) {
+        const float av = A[i * SB_NC], gv = Gs[i * SB_NC], sp = Sp[i * SB_NC];
+        g = __fmaf_rn(an, g, gv);
+        float oa, ob;
+        if constexpr (GATED) {
+            oa = __fmul_rn(g, __fsub_rn(sp, U[i * SB_NC]));
+            ob = __fmul_rn(g, __fsub_rn(1.0f, av));
+        } else {
+            oa = __fmul_rn(g, sp);
+            ob = g;
+        }
+        if constexpr (WA) st_cs(pa + (size_t)i * N, oa);
+        if constexpr (WB) st_cs(pb + (size_t)i * N, ob);
+        an = av;
+    }
+}
+
 }  // namespace
 
 template <bool GATED>
@@ -144,9 +169,16 @@ scan_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ 
             const float* U = A + 3 * SB_TILE;
             const int r0 = T - (k + 1) * SB_TS;
             if (k > 0 && r0 >= 1) {
-                // interior stage: neither t = T-1 nor t = 0 occurs, all rows valid
-#pragma unroll
-                for (int i = SB_TS - 1; i >= 0; --i) row(A, Gs, Sp, U, i, r0 + i, false);
+                // interior stage: neither t = T-1 nor t = 0 occurs, all rows valid;
+                // which outputs this lane stores is decided once per stage
+                const size_t base = ((size_t)bi * T + r0) * N + c;
+                const bool wa = live && da != nullptr, wb = live && dbu != nullptr;
+                float* pa = wa ? da + base : nullptr;
+                float* pb = wb ? dbu + base : nullptr;
+                if (wa && wb) bwd_stage<GATED, true, true>(A, Gs, Sp, U, pa, pb, N, g, an);
+                else if (wa) bwd_stage<GATED, true, false>(A, Gs, Sp, U, pa, pb, N, g, an);
+                else if (wb) bwd_stage<GATED, false, true>(A, Gs, Sp, U, pa, pb, N, g, an);
+                else bwd_stage<GATED, false, false>(A, Gs, Sp, U, pa, pb, N, g, an);
             } else {
                 for (int i = SB_TS - 1; i >= max(0, -r0); --i) row(A, Gs, Sp, U, i, r0 + i, true);
             }
