@@ -116,7 +116,7 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
         for (int tt = 0; tt < ntile; ++tt)
             bulk_store(S_out + (size_t)(tile0 + tt) * DEC_D * DEC_D, smem + tt * DEC_TILE_BYTES, DEC_S_BYTES);
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read_all();   // shared memory must outlive the copies' reads; the writes finish on their own
     }
 }
 
