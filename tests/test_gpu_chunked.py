@@ -243,3 +243,30 @@ def test_head_blocks_sharing_one_group(ctx, G):
             ro, rS = ref(xs, S0[b:b + 1, h:h + 1].contiguous())
             assert _nrel(o[b:b + 1, :, h:h + 1], ro) <= TOL, (b, h)
             assert _nrel(S[b:b + 1, h:h + 1], rS) <= TOL, (b, h)
+
+
+@pytest.mark.parametrize("kind", ["gla", "mamba2"])
+def test_in_place_state(ctx, kind):
+    """S_in and S_out may be the same buffer (continuation in place)."""
+    B, T, H, dv = 2, 300, 2, 128
+    x = make(kind, B, T, H, dv, seed=1)
+    S0 = synth.normal((B, H, 128, dv), 7300) * 0.5
+    o_ref, S_ref = run_chunked(ctx, x, S0)
+    Sd = S0.cuda()
+    o, S = ctx.recur_diag_chunked(*(cu(x[n]) for n in ("q", "k", "v", "d")), Sd, H=x["H"], G=x["G"],
+                                  decay_kind=x["decay_kind"], scale=x["scale"], S_out=Sd)
+    torch.cuda.synchronize()
+    assert S.data_ptr() == Sd.data_ptr()
+    assert np.array_equal(Sd.cpu().numpy(), S_ref) and np.array_equal(o.cpu().numpy(), o_ref)
+
+
+def test_grouped_keys_with_per_key_decay(ctx):
+    """Per-key decays with q, k shared by groups of heads (G < H)."""
+    B, T, H, G, dv = 2, 260, 4, 2, 64
+    x = make("gla", B, T, H, dv, seed=2)
+    q = synth.normal((B, T, G, 128), 7400) * 0.088
+    k = synth.normal((B, T, G, 128), 7401) * 0.088
+    x = dict(x, q=q, k=k, G=G)
+    o, S = run_chunked(ctx, x)
+    ro, rS = ref(x)
+    assert _nrel(o, ro) <= TOL and _nrel(S, rS) <= TOL

@@ -131,3 +131,14 @@ def test_unsupported_and_missing_workspace(ctx, sr):
         sr.SN_E_NOMEM
     assert abi.sn_recur_delta_chunked_workspace_bytes(1, 0, 1, 128, 128) == -1
     torch.cuda.synchronize()
+
+
+def test_in_place_state(ctx):
+    x = synth.deltanet_inputs(2, 300, 2, 128, 128, cid=450)
+    S0 = synth.normal((2, 2, 128, 128), 8200) * 0.5
+    o_ref, S_ref = run(ctx, x, S0)
+    Sd = S0.cuda()
+    o, S = ctx.recur_delta_chunked(*(cu(x[n]) for n in ("q", "k", "v", "beta")), Sd, scale=x["scale"], S_out=Sd)
+    torch.cuda.synchronize()
+    assert S.data_ptr() == Sd.data_ptr()
+    assert np.array_equal(Sd.cpu().numpy(), S_ref) and np.array_equal(o.cpu().numpy(), o_ref)
