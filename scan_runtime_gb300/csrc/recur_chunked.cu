@@ -219,6 +219,144 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, DKC);
 }
 
+// ------------------------------------------------------------------ chunk_state_heads
+// Per-head decays with heads sharing k (Mamba-2's groups): the token weight
+// 2^{mu_t} is a scalar per token, so it is applied to v instead of k,
+// dS^T = (v (.) 2^{mu})^T k, and the transposed k tile is the same for every
+// head of the group.  One CTA per (batch, chunk, block of hb heads of one
+// group) loads it once and loops over the heads.  dv = 64.
+template <int DV>
+struct StateHeadsSmem {
+    static constexpr int k_off = 0;                  // k^T (rows key, K = t), tf32
+    static constexpr int v_off = OPF;                // the head's v^T (rows value, K = t), scaled, tf32
+    static constexpr int mu_off = v_off + DV * CH;   // [CH] suffix sums of log2 d of the head
+    static constexpr int misc_off = mu_off + CH;     // total, barrier, tmem slot
+    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+};
+
+template <int DV>
+__global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, int hb) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = StateHeadsSmem<DV>;
+    float* base = align128(smem_raw);
+    float* Ks = base + L::k_off;
+    float* Vs = base + L::v_off;
+    float* mu = base + L::mu_off;
+    float* total_s = base + L::misc_off;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nhb = a.H / hb;
+    const int hblk = blockIdx.x % nhb;
+    const int bn = blockIdx.x / nhb;
+    const int n = bn % a.NC, b = bn / a.NC;
+    const int h0 = hblk * hb;
+    const int g = h0 / (a.H / a.G);
+    const int t0 = n * CH, nval = min(CH, a.T - t0);
+    const size_t row0 = (size_t)b * a.T + t0;
+    const size_t krs = (size_t)a.G * DKC, vrs = (size_t)a.H * DV;
+
+    if (warp == 0) tc::tmem_alloc(slot, DKC);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    copy_transposed<DKC>(Ks, a.k + row0 * krs + (size_t)g * DKC, krs, nval, warp, lane);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int f = tid; f < OPF / 4; f += NT) st4(Ks + 4 * f, tf32x4(ld4(Ks + 4 * f)));
+
+    uint32_t mpar = 0;
+    bool ok = true;
+    uint32_t tmem = 0;
+    for (int hi = 0; hi < hb && ok; ++hi) {
+        const int h = h0 + hi;
+        copy_transposed<DV>(Vs, a.v + row0 * vrs + (size_t)h * DV, vrs, nval, warp, lane);
+        cp_async_commit();
+        if (warp == 0) {
+            // exclusive suffix sums mu[t] = sum_{s > t} log2 d_s of this head
+            float lg[4], sm = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * lane + r;
+                lg[r] = (t < nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + h)) : 0.f;
+                sm += lg[r];
+            }
+            float x = sm;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_down_sync(FULL, x, off);
+                if (lane + off < 32) x += y;
+            }
+            float acc = x - sm;
+#pragma unroll
+            for (int r = 3; r >= 0; --r) {
+                mu[4 * lane + r] = acc;
+                acc += lg[r];
+            }
+            if (lane == 0) {
+                total_s[0] = x;
+                if (!isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // v^T (.) 2^{mu_t}, rounded: a float4 of the operand holds four consecutive tokens
+        for (int f = tid; f < DV * CH / 4; f += NT) {
+            const int tq = ((4 * f) >> 5 & 31) * 4;
+            const float4 x = ld4(Vs + 4 * f);
+            st4(Vs + 4 * f, tf32x4(x.x * ex2(mu[tq]), x.y * ex2(mu[tq + 1]), x.z * ex2(mu[tq + 2]),
+                                   x.w * ex2(mu[tq + 3])));
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        tmem = *slot;
+        if (tid == 0) {
+            // dS^T (M = dv rows value, N = dk columns key) = (v 2^mu)^T (K = t) x k^T (K = t)
+            tc::gemm_tf32(tmem, Vs, Ks, CH, tc::idesc_tf32(DV, DKC), false);
+            tc::commit(bar);
+        }
+        ok = __syncthreads_and(mbar_wait(bar, mpar, a.wait_ns));
+        mpar ^= 1;
+        tc::fence_after_sync();
+        if (ok) {
+            // M = 64: rows 16q .. 16q + 15 in lanes 32q .. 32q + 15
+            const int lq = warp & 3, ih = warp >> 2;
+            const int row = 16 * lq + (lane & 15);
+            const bool mine = lane < 16;
+            const size_t bh = (size_t)b * a.H + h;
+            float* wt = a.W + (bh * a.NC + n) * (size_t)DV * DKC;
+#pragma unroll
+            for (int i0 = 64 * ih; i0 < 64 * ih + 64; i0 += 16) {
+                float x[16];
+                tc::ld16(tmem + ((uint32_t)(32 * lq) << 16) + i0, x);
+                if (mine) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st4(wt + off128(row, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+                }
+            }
+            if (tid < DKC) {
+                const size_t gi = (bh * a.NC + n) * DKC + tid;
+                a.gam[gi] = ex2(total_s[0]);
+                a.anc[gi] = 1.f;
+            }
+        } else if (tid == 0) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_STATE_WAIT);
+        }
+        tc::fence_before_sync();
+        __syncthreads();   // tensor memory, the v buffer and mu are reused by the next head
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(*slot, DKC);
+}
+
 // ------------------------------------------------------------------ chunk_carry
 // One thread per entry of a head's dv x dk state tile, in the operand layout.
 // S_0 = S_in; for each chunk: W[n] <- tf32(anc_n (.) S_n), S_{n+1} = gamma_n (.) S_n + dS_n.
@@ -773,9 +911,16 @@ int heads_per_cta(const ChunkArgs& a, int sm_count) {
 template <bool PER_KEY, int DV>
 cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     constexpr bool HEADS = !PER_KEY && DV == 64;   // per-head decays: heads of a group share Q K^T
-    const size_t st_bytes = StateSmem<PER_KEY, DV>::bytes;
+    size_t st_bytes;
     size_t out_bytes;
-    cudaError_t e = set_smem_attr_once((const void*)chunk_state<PER_KEY, DV>, st_bytes);
+    cudaError_t e;
+    if constexpr (HEADS) {
+        st_bytes = StateHeadsSmem<DV>::bytes;
+        e = set_smem_attr_once((const void*)chunk_state_heads<DV>, st_bytes);
+    } else {
+        st_bytes = StateSmem<PER_KEY, DV>::bytes;
+        e = set_smem_attr_once((const void*)chunk_state<PER_KEY, DV>, st_bytes);
+    }
     if (e != cudaSuccess) return e;
     if constexpr (HEADS) {
         out_bytes = HeadsSmem<DV>::bytes;
@@ -786,7 +931,12 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     }
     if (e != cudaSuccess) return e;
     const unsigned chunks = (unsigned)((size_t)a.B * a.H * a.NC);
-    chunk_state<PER_KEY, DV><<<chunks, NT, st_bytes, s>>>(a);
+    if constexpr (HEADS) {
+        const int hb = heads_per_cta(a, sm_count);
+        chunk_state_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, st_bytes, s>>>(a, hb);
+    } else {
+        chunk_state<PER_KEY, DV><<<chunks, NT, st_bytes, s>>>(a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t entries = (size_t)a.B * a.H * DKC * DV;
