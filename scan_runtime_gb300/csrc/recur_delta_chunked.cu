@@ -16,7 +16,7 @@
 //                 hi/lo tf32 split (three products, close to fp32), the
 //                 triangular inverse in fp32 on the CUDA cores (16 x 16
 //                 diagonal blocks by column-wise substitution in registers,
-//                 then block rows as register-tiled strips), W = T K and
+//                 then doubling levels 16 -> 32 -> 64 -> 128), W = T K and
 //                 U = T V on tcgen05; writes W, U and K^T tiles;
 //   delta_chain   one CTA per (batch, head), chunks in order: the state S^T
 //                 stays in fp32 registers; per chunk the products W S_n and
@@ -36,7 +36,6 @@ using namespace chunk;
 
 constexpr int LDX = CH + 4;         // row stride of A^T and X (rows of float4)
 constexpr int BSZ = 16;             // diagonal block size of the inverse
-constexpr int NBLK = CH / BSZ;
 constexpr int SITE_PREP_WAIT1 = 7, SITE_PREP_WAIT2 = 8, SITE_CHAIN_WAIT = 9;
 
 struct DeltaArgs {
@@ -64,6 +63,74 @@ struct PrepSmem {
     static constexpr int misc = beta + CH;
     static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
 };
+
+// One doubling level of the lower-triangular inverse X = (I + A)^{-1}: for
+// every 2S x 2S diagonal block, whose two S x S diagonal blocks X_A (upper
+// left) and X_D (lower right) are already inverted, the lower-left block is
+//     X_C = -X_D (A_C X_A)
+// with A_C the matching block of A (read from A^T).  The product Y = A_C X_A
+// is parked in the upper-right S x S block, which X never uses (X is zero
+// there and the T operand masks it).  Every thread owns RT = S / 16 rows x 4
+// columns of one pair's block, so all 256 threads work at every level.  The
+// sums skip X_A's and X_D's zero triangles in steps of four; the few entries
+// past the triangle that a step still touches sit in a diagonal 16 x 16 block
+// above its diagonal, where X holds exact zeros.
+template <int S>
+__device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int tid) {
+    constexpr int RT = S / 16, NCT = S / 4;
+    const int ct = tid % NCT, rt = (tid / NCT) % 16;
+    const int o = 2 * S * (tid / (16 * NCT));
+    const int r0 = RT * rt, c0 = 4 * ct;
+    float acc[RT][4] = {};
+    // Y[r][c] = sum_{m >= c} A[o + S + r][o + m] X[o + m][o + c]
+    for (int m = c0; m < S; m += 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 x = ld4(Xm + (o + m + i) * LDX + o + c0);
+            const float* ap = AT + (o + m + i) * LDX + o + S + r0;
+            float av[RT];
+            if constexpr (RT == 4) {
+                const float4 t = ld4(ap);
+                av[0] = t.x; av[1] = t.y; av[2] = t.z; av[3] = t.w;
+            } else if constexpr (RT == 2) {
+                const float2 t = *reinterpret_cast<const float2*>(ap);
+                av[0] = t.x; av[1] = t.y;
+            } else {
+                av[0] = ap[0];
+            }
+#pragma unroll
+            for (int j = 0; j < RT; ++j) {
+                acc[j][0] = fmaf(av[j], x.x, acc[j][0]); acc[j][1] = fmaf(av[j], x.y, acc[j][1]);
+                acc[j][2] = fmaf(av[j], x.z, acc[j][2]); acc[j][3] = fmaf(av[j], x.w, acc[j][3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < RT; ++j)
+        st4(Xm + (o + r0 + j) * LDX + o + S + c0, make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
+    __syncthreads();
+    // X_C[r][c] = -sum_{m <= r} X[o + S + r][o + S + m] Y[m][c]
+    float out[RT][4] = {};
+    for (int m = 0; m < r0 + RT; m += 4) {
+        float4 xd[RT];
+#pragma unroll
+        for (int j = 0; j < RT; ++j) xd[j] = ld4(Xm + (o + S + r0 + j) * LDX + o + S + m);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 y = ld4(Xm + (o + m + i) * LDX + o + S + c0);
+#pragma unroll
+            for (int j = 0; j < RT; ++j) {
+                const float xv = i == 0 ? xd[j].x : i == 1 ? xd[j].y : i == 2 ? xd[j].z : xd[j].w;
+                out[j][0] = fmaf(xv, y.x, out[j][0]); out[j][1] = fmaf(xv, y.y, out[j][1]);
+                out[j][2] = fmaf(xv, y.z, out[j][2]); out[j][3] = fmaf(xv, y.w, out[j][3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < RT; ++j)
+        st4(Xm + (o + S + r0 + j) * LDX + o + c0, make_float4(-out[j][0], -out[j][1], -out[j][2], -out[j][3]));
+    __syncthreads();
+}
 
 __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -173,56 +240,10 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
             for (int jj = 0; jj < BSZ / 2; ++jj) Xm[(r0 + rb + 2 * jj) * LDX + r0 + c] = xr[jj];
         }
         __syncthreads();
-        // block rows: X_ij = -X_ii sum_{j <= k < i} A_ik X_kj.  A group of KS = 8
-        // adjacent lanes owns one 16 x 4 column strip of the block row: the
-        // lanes split the sum over k (one float4 of X and four of A^T feed 64
-        // FMAs), join it with xor shuffles, and each lane then multiplies two
-        // rows of X_ii into the strip.  One barrier per block row.
-        for (int i = 1; i < NBLK; ++i) {
-            constexpr int KS = 8;
-            const int cq = 4 * i;                          // column quads (strips) of the block row
-            if (tid < cq * KS) {                           // 32 i threads: whole warps
-                const int s4 = tid / KS, part = tid % KS;
-                float acc[BSZ][4] = {};
-                for (int kk = BSZ * (s4 >> 2) + part; kk < BSZ * i; kk += KS) {
-                    const float4 x4 = ld4(Xm + kk * LDX + 4 * s4);
-                    const float* ap = AT + kk * LDX + BSZ * i;       // A[16 i + r][kk], r = 0..15
-#pragma unroll
-                    for (int r4 = 0; r4 < BSZ / 4; ++r4) {
-                        const float4 a4 = ld4(ap + 4 * r4);
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float* o = acc[4 * r4 + q];
-                            o[0] = fmaf(av[q], x4.x, o[0]); o[1] = fmaf(av[q], x4.y, o[1]);
-                            o[2] = fmaf(av[q], x4.z, o[2]); o[3] = fmaf(av[q], x4.w, o[3]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int off = KS / 2; off > 0; off >>= 1)
-#pragma unroll
-                    for (int r = 0; r < BSZ; ++r)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[r][c] += __shfl_xor_sync(FULL, acc[r][c], off);
-#pragma unroll
-                for (int rr = 0; rr < BSZ / KS; ++rr) {
-                    const int r = part * (BSZ / KS) + rr;
-                    const float* xd = Xm + (BSZ * i + r) * LDX + BSZ * i;   // row r of X_ii
-                    float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int m = 0; m < BSZ; ++m) {
-                        if (m <= r) {
-                            const float xv = xd[m];
-                            out.x = fmaf(xv, acc[m][0], out.x); out.y = fmaf(xv, acc[m][1], out.y);
-                            out.z = fmaf(xv, acc[m][2], out.z); out.w = fmaf(xv, acc[m][3], out.w);
-                        }
-                    }
-                    st4(Xm + (BSZ * i + r) * LDX + 4 * s4, make_float4(-out.x, -out.y, -out.z, -out.w));
-                }
-            }
-            __syncthreads();
-        }
+        // the inverse by doubling, 16 -> 32 -> 64 -> 128 (one product pair per level)
+        inverse_level<16>(Xm, AT, tid);
+        inverse_level<32>(Xm, AT, tid);
+        inverse_level<64>(Xm, AT, tid);
 
         // A is consumed: the V^T operand streams into its buffer
         copy_transposed<128>(buf1, a.v + row0 * (size_t)a.H * 128 + (size_t)h * 128, (size_t)a.H * 128, nval, warp,
