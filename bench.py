@@ -383,7 +383,7 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                         "ms": round(ms, 4), "tok_heads_per_s": round(th / ms * 1e3, 1),
                         "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
                         "TFLOPs_tf32": round(tf, 2), "tf32_frac": round(tf / tf32_peak_tflops(), 4),
-                        "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "hbm",
+                        "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "latency",
                         "tolerance": 2e-3}
                 assert ctx.last_error() == sr.SN_OK
             del x, o, S

@@ -104,6 +104,8 @@ typedef int32_t sn_status;
 #define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
 #define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA;
                                       a width the value dimension does not divide fails with SN_E_DEVICE */
+#define SN_OPT_DELTA_SEGMENTS   7  /* sn_recur_delta_chunked: 0 auto (default), or 1..8 segments of the
+                                      chunk sequence run as a pipeline (same bits for every value) */
 
 #define SN_SCAN_KERNEL_AUTO       0
 #define SN_SCAN_KERNEL_SEQUENTIAL 1
@@ -319,7 +321,14 @@ int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_
  * (tf32); splits at multiples of 128 tokens are bit-exact.  Requires dk = dv
  * = 128 (else SN_E_UNSUPPORTED), 16-byte aligned pointers and a context
  * workspace of at least sn_recur_delta_chunked_workspace_bytes() bytes (else
- * SN_E_NOMEM), which the call overwrites. */
+ * SN_E_NOMEM), which the call overwrites.
+ * Streams: for more than a few chunks the call splits the sequence into
+ * segments (SN_OPT_DELTA_SEGMENTS) and runs the chain of one segment beside
+ * the preparation of the next on two side streams the context owns.  The
+ * side streams wait for `stream`'s earlier work and `stream` waits for them
+ * before its later work, so to the caller the call is ordered on `stream`
+ * like any other (also under stream capture).  A context is not for use from
+ * two host threads at once. */
 sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
                                  int32_t dk, int32_t dv, float scale,
                                  const float* q, const float* k, const float* v,
@@ -328,8 +337,8 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
 
 /* Workspace bytes sn_recur_delta_chunked needs: five tiles of dk x dv floats
  * per chunk of 128 tokens and head (W, K^T, U, the chunk state and the
- * chunk's deltas), each kind rounded up to 256 bytes; -1 on invalid
- * arguments. */
+ * chunk's deltas) plus one fp32 dk x dv state per head (carried between
+ * segments), each kind rounded up to 256 bytes; -1 on invalid arguments. */
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* ---------------------------------------------------------------- readout epilogues */

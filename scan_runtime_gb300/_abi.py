@@ -27,6 +27,7 @@ SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD, SN_DECAY_PER_KEY_GATED, SN_DECAY_PER_HEAD_G
 SN_OPT_SCAN_KERNEL, SN_OPT_WAIT_LIMIT_US, SN_OPT_DEBUG_POISON, SN_OPT_LOOKBACK_CHUNK, SN_OPT_RECUR_KERNEL = (
     1, 2, 3, 4, 5)
 SN_OPT_RECUR_TILE = 6
+SN_OPT_DELTA_SEGMENTS = 7
 SN_SCAN_KERNEL_AUTO, SN_SCAN_KERNEL_SEQUENTIAL, SN_SCAN_KERNEL_LOOKBACK = 0, 1, 2
 SN_OP_SCAN_FMA, SN_OP_SCAN_GATED = 1, 2
 

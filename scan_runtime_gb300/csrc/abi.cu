@@ -196,6 +196,13 @@ sn_status sn_ctx_create(int32_t device, SnCtx** out_ctx) {
 void sn_ctx_free(SnCtx* ctx) {
     if (ctx == nullptr) return;
     DeviceGuard g(ctx->device);
+    if (ctx->pipe_ready) {
+        for (cudaStream_t st : {ctx->pipe_prep, ctx->pipe_chain, ctx->pipe_out}) {
+            cudaStreamSynchronize(st);
+            cudaStreamDestroy(st);
+        }
+        for (cudaEvent_t ev : ctx->pipe_ev) cudaEventDestroy(ev);
+    }
     cudaFree(ctx->dstatus);
     delete ctx;
 }
@@ -255,6 +262,10 @@ sn_status sn_ctx_set_option(SnCtx* ctx, int32_t key, int32_t value) {
             if (value != 0 && value != 2 && value != 4 && value != 8) return SN_E_INVAL;
             ctx->recur_tile = value;
             return SN_OK;
+        case SN_OPT_DELTA_SEGMENTS:
+            if (value < 0 || value > DELTA_MAX_SEGMENTS) return SN_E_INVAL;
+            ctx->delta_segments = value;
+            return SN_OK;
         default: return SN_E_INVAL;
     }
 }
@@ -268,6 +279,7 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value) {
         case SN_OPT_LOOKBACK_CHUNK: *value = LB_TC; return SN_OK;
         case SN_OPT_RECUR_KERNEL: *value = ctx->recur_kernel; return SN_OK;
         case SN_OPT_RECUR_TILE: *value = ctx->recur_tile; return SN_OK;
+        case SN_OPT_DELTA_SEGMENTS: *value = ctx->delta_segments; return SN_OK;
         default: return SN_E_INVAL;
     }
 }
@@ -485,7 +497,33 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, in
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
     ctx->ws_dirty = true;   // the chunk tiles overwrite the look-back flag area
-    return from_cuda(launch_delta_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), reinterpret_cast<cudaStream_t>(stream)));
+    const int nseg = delta_segments((T + 127) / 128, B * H, ctx->sm_count, ctx->delta_segments);
+    if (nseg > 1 && !ctx->pipe_ready) {
+        // priorities: chain > preparation > output, so the serial chain starts as soon as SMs
+        // free up and the preparation that feeds it runs ahead of the outputs
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return SN_E_DEVICE;
+        const int mid = greatest < least - 1 ? greatest + 1 : greatest;
+        cudaStream_t* sts[3] = {&ctx->pipe_chain, &ctx->pipe_prep, &ctx->pipe_out};
+        const int prio[3] = {greatest, mid, least};
+        int made_s = 0;
+        for (; made_s < 3; ++made_s)
+            if (cudaStreamCreateWithPriority(sts[made_s], cudaStreamNonBlocking, prio[made_s]) != cudaSuccess) break;
+        int made_e = 0;
+        if (made_s == 3)
+            for (; made_e < 20; ++made_e)
+                if (cudaEventCreateWithFlags(&ctx->pipe_ev[made_e], cudaEventDisableTiming) != cudaSuccess) break;
+        if (made_e < 20) {
+            for (int i = 0; i < made_e; ++i) cudaEventDestroy(ctx->pipe_ev[i]);
+            for (int i = 0; i < made_s; ++i) cudaStreamDestroy(*sts[i]);
+            return SN_E_DEVICE;
+        }
+        ctx->pipe_ready = true;
+    }
+    DeltaPipe pipe{};
+    if (ctx->pipe_ready) pipe = DeltaPipe{ctx->pipe_prep, ctx->pipe_chain, ctx->pipe_out, ctx->pipe_ev, 20};
+    return from_cuda(launch_delta_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, ctx->delta_segments, pipe,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {

@@ -38,6 +38,7 @@ struct ChunkArgs {
                        // that replaces v in the output stage (bulk-loaded)
     SnDevStatus* st;
     uint64_t wait_ns;
+    int n0, nsg;       // the output kernel alone: chunks [n0, n0 + nsg) (nsg = 0: all NC chunks)
 };
 
 // sites recorded with SN_E_TIMEOUT / SN_E_RANGE
@@ -97,8 +98,9 @@ __device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a) {
     ChunkIdx c;
     c.h = blockIdx.x % a.H;
     const int bn = blockIdx.x / a.H;
-    c.n = bn % a.NC;
-    c.b = bn / a.NC;
+    const int nsg = a.nsg > 0 ? a.nsg : a.NC;
+    c.n = a.n0 + bn % nsg;
+    c.b = bn / nsg;
     c.g = c.h / (a.H / a.G);
     c.t0 = c.n * CH;
     c.nval = min(CH, a.T - c.t0);
@@ -125,8 +127,11 @@ __device__ __forceinline__ void copy_transposed(float* dst, const float* base, s
 }
 
 // recur_chunked.cu: the output kernel alone with unit decays (d == nullptr),
-// dv = 128 (used by the chunked delta rule).
+// dv = 128 (used by the chunked delta rule), over chunks [n0, n0 + nsg); the
+// kernel and its shared-memory size, for opting in before the launches.
 cudaError_t launch_output_unit_decay(const ChunkArgs& a, cudaStream_t s);
+const void* output_unit_decay_kernel();
+size_t output_unit_decay_smem();
 
 }  // namespace chunk
 }  // namespace sn

@@ -963,9 +963,13 @@ cudaError_t chunk::launch_output_unit_decay(const ChunkArgs& a, cudaStream_t s) 
     const size_t bytes = OutSmem<128>::bytes;
     const cudaError_t e = set_smem_attr_once((const void*)chunk_output<false, 128>, bytes);
     if (e != cudaSuccess) return e;
-    chunk_output<false, 128><<<(unsigned)((size_t)a.B * a.H * a.NC), NT, bytes, s>>>(a);
+    const int nsg = a.nsg > 0 ? a.nsg : a.NC;
+    chunk_output<false, 128><<<(unsigned)((size_t)a.B * a.H * nsg), NT, bytes, s>>>(a);
     return cudaGetLastError();
 }
+
+const void* chunk::output_unit_decay_kernel() { return (const void*)chunk_output<false, 128>; }
+size_t chunk::output_unit_decay_smem() { return OutSmem<128>::bytes; }
 
 int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;

@@ -29,6 +29,8 @@
 // crosses chunks in fp32.
 #include "chunk_common.cuh"
 
+#include <algorithm>
+
 namespace sn {
 namespace {
 
@@ -40,16 +42,17 @@ constexpr int SITE_PREP_WAIT1 = 7, SITE_PREP_WAIT2 = 8, SITE_CHAIN_WAIT = 9;
 
 struct DeltaArgs {
     int B, T, H, NC;
+    int n0, n1;     // chunks [n0, n1) of this launch (a segment of the sequence)
     const float* k;
     const float* v;
     const float* beta;
-    const float* S_in;
-    float* S_out;
     float* Wt;      // per chunk: W (rows t, K = key), operand layout, tf32
     float* KTt;     // per chunk: K^T (rows key, K = t), operand layout, tf32
     float* Ut;      // per chunk: U, row-major [t][value]
     float* DTt;     // per chunk: Delta^T (rows value, K = t), operand layout, tf32
     float* St;      // per chunk: S_n^T (rows value, K = key), operand layout, tf32
+    const float* S_from;   // delta_chain: fp32 state entering chunk n0 (NULL = zeros)
+    float* S_to;           // delta_chain: fp32 state after chunk n1 - 1 (NULL = not written)
     SnDevStatus* st;
     uint64_t wait_ns;
 };
@@ -146,7 +149,8 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x % a.H;
     const int bn = blockIdx.x / a.H;
-    const int n = bn % a.NC, b = bn / a.NC;
+    const int nsg = a.n1 - a.n0;
+    const int n = a.n0 + bn % nsg, b = bn / nsg;
     const int t0 = n * CH, nval = min(CH, a.T - t0);
     const size_t bh = (size_t)b * a.H + h;
     const size_t row0 = (size_t)b * a.T + t0;
@@ -353,16 +357,16 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         mbar_init(barM, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(barW, OPF * 4);
-        bulk_load(Wb, tile(a.Wt, 0), OPF * 4, barW);
+        bulk_load(Wb, tile(a.Wt, a.n0), OPF * 4, barW);
         mbar_arrive_expect_tx(barK, OPF * 4);
-        bulk_load(KTb, tile(a.KTt, 0), OPF * 4, barK);
+        bulk_load(KTb, tile(a.KTt, a.n0), OPF * 4, barK);
     }
 
     // S^T[c][i] for this part's 64 keys, fp32 in registers for the whole sequence
     float sreg[64];
     const size_t sbase = bh * (size_t)(DKC * 128);
 #pragma unroll
-    for (int r = 0; r < 64; ++r) sreg[r] = a.S_in != nullptr ? a.S_in[sbase + (size_t)(64 * part + r) * 128 + c] : 0.f;
+    for (int r = 0; r < 64; ++r) sreg[r] = a.S_from != nullptr ? a.S_from[sbase + (size_t)(64 * part + r) * 128 + c] : 0.f;
     auto put_state = [&]() {   // tf32 S_n^T into the operand buffer (then bulk-stored as the chunk's tile)
 #pragma unroll
         for (int r4 = 0; r4 < 16; ++r4) {
@@ -381,21 +385,21 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         for (int r = 0; r < 64; ++r) u[r] = ut[(64 * part + r) * 128 + c];
     };
     put_state();
-    load_u(0);
+    load_u(a.n0);
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) store_tile(a.St, 0);
+    if (tid == 0) store_tile(a.St, a.n0);
     const uint32_t tmem = *slot;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     const uint32_t id = tc::idesc_tf32(128, 128);
     uint32_t mpar = 0;
     int w_loads = 1, k_loads = 1;   // bulk loads issued on barW / barK (thread 0's count)
     bool ok = true;
-    int n = 0;
-    for (; n < NC; ++n) {
-        ok = __syncthreads_and(mbar_wait(barW, n & 1, a.wait_ns));
+    for (int n = a.n0; n < a.n1; ++n) {
+        const uint32_t ph = (uint32_t)(n - a.n0) & 1;   // phase of this launch's n-th tile loads
+        ok = __syncthreads_and(mbar_wait(barW, ph, a.wait_ns));
         if (!ok) break;
         if (tid == 0) {   // P[c][t] = sum_i S^T[c][i] W[t][i]  (= (W S_n)^T)
             tc::gemm_tf32(tmem, SUb, Wb, DKC, id, false);
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         mpar ^= 1;
         tc::fence_after_sync();
         if (!ok) break;
-        if (tid == 0 && n + 1 < NC) {
+        if (tid == 0 && n + 1 < a.n1) {
             mbar_arrive_expect_tx(barW, OPF * 4);
             bulk_load(Wb, tile(a.Wt, n + 1), OPF * 4, barW);
             ++w_loads;
@@ -425,7 +429,7 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        ok = __syncthreads_and(mbar_wait(barK, n & 1, a.wait_ns));
+        ok = __syncthreads_and(mbar_wait(barK, ph, a.wait_ns));
         tc::fence_after_sync();
         if (!ok) break;
         if (tid == 0) {   // D[c][i] = sum_t Delta^T[c][t] K^T[i][t]  (= (K^T Delta)^T)
@@ -433,13 +437,13 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
             tc::commit(barM);
             store_tile(a.DTt, n);
         }
-        if (n + 1 < NC) load_u(n + 1);
+        if (n + 1 < a.n1) load_u(n + 1);
         if (tid == 0) bulk_wait_read_all();   // the Delta^T tile store has read the buffer
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
         tc::fence_after_sync();
         if (!ok) break;
-        if (tid == 0 && n + 1 < NC) {
+        if (tid == 0 && n + 1 < a.n1) {
             mbar_arrive_expect_tx(barK, OPF * 4);
             bulk_load(KTb, tile(a.KTt, n + 1), OPF * 4, barK);
             ++k_loads;
@@ -451,12 +455,12 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) sreg[q0 + jj] += x[jj];
         }
-        if (n + 1 < NC) put_state();
+        if (n + 1 < a.n1) put_state();
         fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (tid == 0 && n + 1 < NC) store_tile(a.St, n + 1);
+        if (tid == 0 && n + 1 < a.n1) store_tile(a.St, n + 1);
     }
     if (tid == 0) bulk_wait_all();   // every tile store complete before the CTA exits
     if (!ok) {
@@ -466,9 +470,9 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
             mbar_wait(barW, (w_loads - 1) & 1, a.wait_ns);
             mbar_wait(barK, (k_loads - 1) & 1, a.wait_ns);
         }
-    } else if (a.S_out != nullptr) {
+    } else if (a.S_to != nullptr) {
 #pragma unroll
-        for (int r = 0; r < 64; ++r) a.S_out[sbase + (size_t)(64 * part + r) * 128 + c] = sreg[r];
+        for (int r = 0; r < 64; ++r) a.S_to[sbase + (size_t)(64 * part + r) * 128 + c] = sreg[r];
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -481,17 +485,37 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;
-    return 5 * round256((int64_t)B * H * nc * dk * dv * 4);
+    return 5 * round256((int64_t)B * H * nc * dk * dv * 4) + round256((int64_t)B * H * dk * dv * 4);
 }
 
 bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && x.dk == DKC && x.dv == 128; }
 
-cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, cudaStream_t s) {
+// Auto: two segments when the chain (one CTA per head) leaves at least half
+// the SMs to the preparation and there are chunks enough to split; more
+// segments measured slower (each chain segment waits for SMs held by the
+// next segment's preparation, whose CTAs run about 30 us).
+int delta_segments(int NC, int BH, int sm_count, int requested) {
+    int nseg = requested > 0 ? requested : (NC >= 8 && 2 * BH <= sm_count ? 2 : 1);
+    nseg = std::min(nseg, NC);
+    const int len = (NC + nseg - 1) / nseg;
+    return (NC + len - 1) / len;
+}
+
+// Segments of the chunk sequence run as a pipeline over three side streams:
+// the per-chunk preparation on `pipe.prep`, the chain on `pipe.chain` once
+// the segment's tiles exist, and the output on `pipe.out` once the chain has
+// produced the segment's deltas and states.  The chain of one segment thus
+// runs beside the preparation of the next; the chain stream has the highest
+// priority and the output stream the lowest.  The fp32 state crosses
+// segments through the workspace, so every segmentation gives the same bits.
+// Events order the stages (fork from and join to the caller's stream); no
+// kernel waits on another.
+cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                 int segments, const DeltaPipe& pipe, cudaStream_t s) {
     DeltaArgs d{};
     d.B = x.B; d.T = x.T; d.H = x.H;
     d.NC = (x.T + CH - 1) / CH;
     d.k = x.k; d.v = x.v; d.beta = x.g;
-    d.S_in = x.S_in; d.S_out = x.S_out;
     const int64_t tile_bytes = round256((int64_t)x.B * x.H * d.NC * OPF * 4);
     char* p = static_cast<char*>(ws);
     d.Wt = reinterpret_cast<float*>(p);
@@ -499,6 +523,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     d.Ut = reinterpret_cast<float*>(p + 2 * tile_bytes);
     d.St = reinterpret_cast<float*>(p + 3 * tile_bytes);
     d.DTt = reinterpret_cast<float*>(p + 4 * tile_bytes);
+    float* S_mid = reinterpret_cast<float*>(p + 5 * tile_bytes);
     d.st = st;
     d.wait_ns = wait_ns;
 
@@ -506,12 +531,31 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     if (e != cudaSuccess) return e;
     e = set_smem_attr_once((const void*)delta_chain, ChainSmem::bytes);
     if (e != cudaSuccess) return e;
-    delta_prep<<<(unsigned)((size_t)x.B * x.H * d.NC), NT, PrepSmem::bytes, s>>>(d);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    delta_chain<<<(unsigned)((size_t)x.B * x.H), NT, ChainSmem::bytes, s>>>(d);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || x.o == nullptr) return e;
+    if (x.o != nullptr) {
+        e = set_smem_attr_once(output_unit_decay_kernel(), output_unit_decay_smem());
+        if (e != cudaSuccess) return e;
+    }
+
+    const int nseg = delta_segments(d.NC, x.B * x.H, sm_count, segments);
+    const int len = (d.NC + nseg - 1) / nseg;
+    const bool piped = nseg > 1;
+    if (piped && (pipe.prep == nullptr || pipe.chain == nullptr || pipe.out == nullptr || pipe.nev < 2 * nseg + 4))
+        return cudaErrorInvalidValue;
+    cudaStream_t sp = piped ? pipe.prep : s, sc = piped ? pipe.chain : s, so = piped ? pipe.out : s;
+    int ev = 0;
+    auto order = [&](cudaStream_t from, cudaStream_t to) -> cudaError_t {   // `to` waits for `from`'s work so far
+        if (from == to) return cudaSuccess;
+        cudaError_t r = cudaEventRecord(pipe.ev[ev], from);
+        if (r == cudaSuccess) r = cudaStreamWaitEvent(to, pipe.ev[ev], 0);
+        ++ev;
+        return r;
+    };
+    e = cudaSuccess;
+    if (piped) {   // fork: the side streams wait for the caller's earlier work
+        e = cudaEventRecord(pipe.ev[ev++], s);
+        for (cudaStream_t side : {sp, sc, so})
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(side, pipe.ev[0], 0);
+    }
 
     ChunkArgs c{};
     c.B = x.B; c.T = x.T; c.H = x.H; c.G = x.H; c.NC = d.NC;
@@ -521,7 +565,31 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     c.W = d.St; c.gam = nullptr; c.anc = nullptr;
     c.st = st;
     c.wait_ns = wait_ns;
-    return launch_output_unit_decay(c, s);
+
+    for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
+        d.n0 = g * len;
+        d.n1 = std::min(d.NC, d.n0 + len);
+        delta_prep<<<(unsigned)((size_t)x.B * x.H * (d.n1 - d.n0)), NT, PrepSmem::bytes, sp>>>(d);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) e = order(sp, sc);
+        if (e != cudaSuccess) break;
+        d.S_from = g == 0 ? x.S_in : S_mid;
+        d.S_to = g == nseg - 1 ? x.S_out : S_mid;
+        delta_chain<<<(unsigned)((size_t)x.B * x.H), NT, ChainSmem::bytes, sc>>>(d);
+        e = cudaGetLastError();
+        if (e != cudaSuccess || x.o == nullptr) continue;
+        e = order(sc, so);
+        if (e != cudaSuccess) break;
+        c.n0 = d.n0;
+        c.nsg = d.n1 - d.n0;
+        e = launch_output_unit_decay(c, so);
+    }
+    // join: the caller's stream waits for the side streams, also after an error
+    for (cudaStream_t side : {sp, sc, so}) {
+        const cudaError_t ej = order(side, s);
+        if (e == cudaSuccess) e = ej;
+    }
+    return e;
 }
 
 }  // namespace sn

@@ -42,6 +42,11 @@ struct SnCtx {
     int debug_poison;
     int recur_kernel;
     int recur_tile;             // forced consumer warps per CTA of the sequence kernel (0 = auto)
+    int delta_segments;         // segments of the pipelined chunked delta rule (0 = auto)
+    // side streams and events of the pipelined chunked delta rule (created on first use)
+    cudaStream_t pipe_prep, pipe_chain, pipe_out;
+    cudaEvent_t pipe_ev[20];
+    bool pipe_ready;
 };
 
 namespace sn {
@@ -130,7 +135,18 @@ bool recur_decode_supported(const RecurArgs& x);
 // Chunked tensor-core form of the delta rule (recur_delta_chunked.cu).
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv);
 bool delta_chunked_supported(const RecurArgs& x);
-cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, cudaStream_t stream);
+// At most DELTA_MAX_SEGMENTS segments; a pipeline of n segments uses 2 n + 4
+// events.  delta_segments: the segment count used for NC chunks of BH heads
+// (requested 0 = auto).
+constexpr int DELTA_MAX_SEGMENTS = 8;
+struct DeltaPipe {
+    cudaStream_t prep, chain, out;
+    cudaEvent_t* ev;
+    int nev;
+};
+int delta_segments(int NC, int BH, int sm_count, int requested);
+cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                 int segments, const DeltaPipe& pipe, cudaStream_t stream);
 
 // Readout epilogues (readout.cu).
 cudaError_t launch_readout_norm_gate(int64_t rows, int dv, const float* o, const float* g, const float* w, float eps,

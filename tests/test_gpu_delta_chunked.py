@@ -142,3 +142,51 @@ def test_in_place_state(ctx):
     torch.cuda.synchronize()
     assert S.data_ptr() == Sd.data_ptr()
     assert np.array_equal(Sd.cpu().numpy(), S_ref) and np.array_equal(o.cpu().numpy(), o_ref)
+
+
+@pytest.mark.parametrize("segments", [2, 3, 4, 8, 0])
+def test_segments_give_the_same_bits(ctx, sr, segments):
+    """The pipelined call (segments of chunks over side streams) against one
+    segment: the state crosses segments in fp32, so the bits must agree.  T =
+    1100 leaves a ragged last chunk of 76 tokens."""
+    B, T, H = 2, 1100, 3
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=460)
+    S0 = synth.normal((B, H, 128, 128), 8300) * 0.5
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 1)
+    o1, S1 = run(ctx, x, S0)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, segments)
+    assert ctx.get_option(sr.SN_OPT_DELTA_SEGMENTS) == segments
+    o, S = run(ctx, x, S0)
+    assert np.array_equal(o, o1) and np.array_equal(S, S1)
+    _, S_only = run(ctx, x, S0, o=False)
+    assert np.array_equal(S_only, S1)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
+
+
+def test_segments_in_place_on_a_side_stream(ctx, sr):
+    """Pipelined call issued on a non-default stream, state in place: the
+    results are ordered on that stream."""
+    B, T, H = 1, 1300, 2
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=470)
+    S0 = synth.normal((B, H, 128, 128), 8400) * 0.5
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 1)
+    o_ref, S_ref = run(ctx, x, S0)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 4)
+    side = torch.cuda.Stream()
+    ins = [cu(x[n]) for n in ("q", "k", "v", "beta")]
+    Sd = S0.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        o, S = ctx.recur_delta_chunked(*ins, Sd, scale=x["scale"], S_out=Sd, stream=side)
+        o_host = o.to("cpu", non_blocking=False)
+        S_host = Sd.to("cpu", non_blocking=False)
+    torch.cuda.synchronize()
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
+    assert np.array_equal(o_host.numpy(), o_ref) and np.array_equal(S_host.numpy(), S_ref)
+
+
+def test_segment_option_range(ctx, sr):
+    for bad in (-1, 9):
+        with pytest.raises(sr.SnError):
+            ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, bad)
+    assert ctx.get_option(sr.SN_OPT_DELTA_SEGMENTS) == 0
