@@ -281,12 +281,41 @@ def time_form(torch, fn, warmup, reps, stream, flush=None):
     return ts[len(ts) // 2]
 
 
+GRAPH_CALLS = 16   # scan calls captured in one CUDA graph for the small-workload latency
+
+
 def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=3, reps=20):
     """Every other workload, each on its own inputs, outside the main timed
     region.  Returns a dict of per-form results."""
     out = {}
     s = stream
     with torch.cuda.stream(stream):
+        # the small scan workload (0.4 MB, fits in L2): per-call latency of both
+        # forms, launched directly and replayed from a CUDA graph of GRAPH_CALLS
+        # calls; L2 is flushed before every timed call or replay
+        c = synth.CONFIGS["scan_small"]
+        Bs, Ts, Ns = c["B"], c["T"], c["N"]
+        xs = synth.config_inputs("scan_small", device=dev)
+        sos = torch.empty((Bs, Ts, Ns), device=dev)
+        sfs = torch.empty((Bs, Ns), device=dev)
+        flush = torch.empty(64 << 20, device=dev)          # 256 MB
+        small = {"workload": f"B={Bs} T={Ts} N={Ns}", "bytes_per_call": scan_bytes(Bs, Ts, Ns), "l2": "flushed",
+                 "graph_calls": GRAPH_CALLS}
+        for form, rhs in (("fma", "b"), ("gated", "u")):
+            f = sr.sn_scan_fma if form == "fma" else sr.sn_scan_gated
+            call = lambda: f(ctx.handle, Bs, Ts, Ns, xs["a"], xs[rhs], xs["s0"], sfs, sos, s)
+            direct = time_form(torch, call, warmup, reps, s, flush=flush)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(GRAPH_CALLS):
+                    call()
+            replay = time_form(torch, g.replay, warmup, reps, s, flush=flush)
+            small[form] = {"us_per_call": round(direct * 1e3, 2),
+                           "us_per_call_graph": round(replay * 1e3 / GRAPH_CALLS, 2)}
+            del g
+        out["scan_small"] = small
+        del flush, xs, sos, sfs
         # the chunked look-back kernel on the same large scan workload
         x = synth.config_inputs("scan_large", device=dev)
         B, T, N = SCAN["B"], SCAN["T"], SCAN["N"]

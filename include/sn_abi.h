@@ -178,7 +178,9 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value);
  * sequence into segments and carrying s_final -> s0 reproduces the full run
  * bit for bit ([P1] §4).  The chunked look-back kernel (chosen for few
  * channels and long T, or forced by SN_OPT_SCAN_KERNEL) is deterministic and
- * bit-exact under splits at multiples of SN_OPT_LOOKBACK_CHUNK.
+ * bit-exact under splits at multiples of SN_OPT_LOOKBACK_CHUNK.  Calls may be
+ * captured in a CUDA graph and replayed: the look-back kernel keeps its launch
+ * epoch in device memory, so every replay tags its chunk flags afresh.
  * Pointers need 4-byte alignment; N % 4 == 0 with 16-byte aligned a, b and
  * s_out enables the TMA path.  Errors: SN_E_INVAL, SN_E_NOMEM (look-back
  * forced without enough workspace), SN_E_DEVICE. */

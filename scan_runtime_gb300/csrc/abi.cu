@@ -178,7 +178,6 @@ sn_status sn_ctx_create(int32_t device, SnCtx** out_ctx) {
     c->cc_major = prop.major;
     c->cc_minor = prop.minor;
     c->wait_limit_us = kDefaultWaitUs;
-    c->epoch = 0;
     c->ws_dirty = true;
     if (cudaMalloc(&c->dstatus, sizeof(SnDevStatus)) != cudaSuccess) {
         delete c;
@@ -321,18 +320,18 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (kernel == SN_SCAN_KERNEL_LOOKBACK) {
         const int64_t nflags = lookback_flag_count(B, T, N);
-        if (ctx->ws_dirty || ctx->epoch >= (1u << 29) || nflags != ctx->lb_last_flags) {
-            // fresh flag area: zero it once, on the caller's stream
+        if (ctx->ws_dirty || nflags != ctx->lb_last_flags) {
+            // fresh flag area: zero it once, on the caller's stream.  Between
+            // clears every launch rewrites all its flags, and the launch epoch
+            // (kept on the device) differs from the previous launch's.
             if (cudaMemsetAsync(ctx->ws, 0, (size_t)nflags * 4, s) != cudaSuccess ||
                 cudaMemsetAsync(&ctx->dstatus->abort_tag, 0, sizeof(unsigned int), s) != cudaSuccess)
                 return SN_E_DEVICE;
             ctx->ws_dirty = false;
-            ctx->epoch = 0;
             ctx->lb_last_flags = nflags;
         }
-        ctx->epoch += 1;
-        return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->epoch, ctx->debug_poison, ctx->dstatus,
-                                              wait_ns(ctx), ctx->sm_count, s));
+        return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->debug_poison, ctx->dstatus, wait_ns(ctx),
+                                              ctx->sm_count, s));
     }
     return from_cuda(launch_scan_sequential(x, gated, ctx->dstatus, wait_ns(ctx), s));
 }

@@ -24,6 +24,7 @@ constexpr uint32_t LB_TILE = LB_TC * LB_NC;       // floats per tensor per tile
 constexpr uint32_t LB_TILE_BYTES = 2 * LB_TILE * 4;
 constexpr uint32_t LB_AGG = 1u, LB_INCL = 2u;
 constexpr int LB_STAGES = 2;                      // tiles in flight per CTA (3 CTAs per SM)
+constexpr uint32_t LB_EPOCH_WRAP = 1u << 29;      // epochs run 1 .. 2^29 - 1 (tags are epoch << 2)
 constexpr size_t LB_SMEM = LB_STAGES * LB_TILE_BYTES + LB_STAGES * 8 + 16;
 
 __device__ __forceinline__ float4 f4mul(float4 x, float4 y) {
@@ -63,9 +64,8 @@ struct LookbackParams {
     float* dA;
     float* dB;
     float* dC;
-    uint32_t tag;        // (epoch << 2) written with each state
-    uint32_t want;       // tag the waiters look for (differs from `tag` in poison mode)
-    SnDevStatus* st;
+    uint32_t poison;     // 1: waiters look for a tag no tile publishes (tests the bound)
+    SnDevStatus* st;     // error word, abort tag and the launch epoch (lb_epoch, lb_done)
     uint64_t wait_ns;
 };
 
@@ -83,11 +83,22 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     const int quad = lane & 7, sub = lane >> 3;
     const int seg = warp * 4 + sub;                 // 0..31, rows [seg*LB_SEG, (seg+1)*LB_SEG)
 
+    // The launch epoch lives in device memory: lb_epoch holds the last launch's
+    // (0 = none yet), this launch uses the next one, and the launch's last CTA
+    // stores it.  A launch replayed from a CUDA graph thus still gets a fresh
+    // tag.  Epochs run 1 .. LB_EPOCH_WRAP - 1, so no tag is 0, the value of
+    // cleared flags and of a cleared abort tag.
+    __shared__ uint32_t s_epoch;
     if (tid == 0) {
         for (int s = 0; s < LB_STAGES; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        const uint32_t last = *reinterpret_cast<volatile const uint32_t*>(&p.st->lb_epoch);
+        s_epoch = last + 1 >= LB_EPOCH_WRAP ? 1u : last + 1;
     }
     __syncthreads();
+    const uint32_t epoch = s_epoch;
+    const uint32_t tag = epoch << 2;                          // written with each state
+    const uint32_t want = p.poison ? (epoch + 1u) << 2 : tag; // what the waiters look for
 
     auto tile_coords = [&](int ti, int& k, int& bi, int& cb) {
         k = ti / p.nbcb;
@@ -131,7 +142,7 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                     if (ti + j * (int)gridDim.x < p.ntiles)
                         (void)mbar_wait(&full[(it + j) % LB_STAGES], ((it + j) / LB_STAGES) & 1, p.wait_ns);
             }
-            return;
+            break;
         }
         const float* sa = bufs + buf * 2 * LB_TILE;
         const float* sb = sa + LB_TILE;
@@ -208,7 +219,7 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                     uint32_t state = LB_INCL;         // chunks before 0 act as "inclusive = s0"
                     if (jl >= 0) {
                         const uint32_t f = ld_acquire_gpu(p.flags + (size_t)jl * p.nbcb + base);
-                        state = ((f & ~3u) == p.want) ? (f & 3u) : 0u;
+                        state = ((f & ~3u) == want) ? (f & 3u) : 0u;
                     }
                     const uint32_t incl = __ballot_sync(0xffffffffu, state == LB_INCL);
                     const uint32_t none = __ballot_sync(0xffffffffu, state == 0u);
@@ -227,13 +238,13 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                         p.dA[me] = CA;
                         p.dB[me] = CB;
                         __syncwarp();
-                        if (lane == 0) st_release_gpu(p.flags + ti, p.tag | LB_AGG);
+                        if (lane == 0) st_release_gpu(p.flags + ti, tag | LB_AGG);
                         published = true;
                     }
                     // give up after the limit, or at once if another tile of this
                     // launch already gave up (its successors would only wait too)
                     if (global_ns() - tstart > p.wait_ns ||
-                        *reinterpret_cast<volatile const uint32_t*>(&p.st->abort_tag) == p.tag) {
+                        *reinterpret_cast<volatile const uint32_t*>(&p.st->abort_tag) == tag) {
                         timed_out = true;
                         break;
                     }
@@ -242,7 +253,7 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                 if (timed_out) {
                     if (lane == 0) {
                         record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | 2);
-                        atomicExch(&p.st->abort_tag, p.tag);
+                        atomicExch(&p.st->abort_tag, tag);
                     }
                     cin = 0.f;
                 } else {
@@ -268,7 +279,7 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
             const float Ck = __fmaf_rn(CA, cin, CB);
             p.dC[(size_t)ti * LB_NC + lane] = Ck;
             __syncwarp();       // the lanes' stores precede lane 0's release (cumulative)
-            if (lane == 0) st_release_gpu(p.flags + ti, p.tag | LB_INCL);
+            if (lane == 0) st_release_gpu(p.flags + ti, tag | LB_INCL);
             carry[lane] = cin;
             cfin[lane] = Ck;
             if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
@@ -293,12 +304,23 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         }
         __syncthreads();                              // buffer `buf` free for the next prefetch
     }
+    // every CTA ends here (also after a copy timeout): the last one records
+    // this launch's epoch for the next launch
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&p.st->lb_done, 1u) == gridDim.x - 1) {
+            p.st->lb_done = 0;
+            p.st->lb_epoch = epoch;
+            __threadfence();
+        }
+    }
 }
 
 bool lookback_supported(const ScanArgs& x) { return scan_tma_ok(x); }
 
-cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32_t epoch, int poison,
-                                 SnDevStatus* st, uint64_t wait_ns, int sm_count, cudaStream_t stream) {
+cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,
+                                 uint64_t wait_ns, int sm_count, cudaStream_t stream) {
     CUtensorMap ma, mb;
     if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, LB_NC, LB_TC) ||
         !make_scan_map(&mb, x.b, x.B, x.T, x.N, LB_NC, LB_TC))
@@ -320,8 +342,7 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32
     p.dA = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + flag_bytes);
     p.dB = p.dA + tiles * LB_NC;
     p.dC = p.dB + tiles * LB_NC;
-    p.tag = epoch << 2;
-    p.want = poison ? ((epoch + 1u) << 2) : p.tag;
+    p.poison = poison ? 1u : 0u;
     p.st = st;
     p.wait_ns = wait_ns;
 
@@ -367,14 +388,12 @@ static_assert(kNoallocScratchBytes <= (int64_t(16) << 20), "scratch stays within
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kNoallocMaxDevices = 64;
-constexpr uint32_t kNoallocEpochWrap = 1u << 29;
 
 struct NoallocDevice {
     bool ready = false;
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
     int sm_count = 0;
     int occ[2] = {0, 0};
-    uint32_t epoch = 0;
 };
 NoallocDevice g_noalloc[kNoallocMaxDevices];
 std::mutex g_noalloc_mutex;
@@ -442,14 +461,8 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
         if (cudaMemsetAsync(sym, 0, (size_t)kNoallocDataOff, s) != cudaSuccess) return SN_E_DEVICE;
         d.scratch = static_cast<unsigned char*>(sym);
         d.sm_count = prop.multiProcessorCount;
-        d.epoch = 0;
         d.ready = true;
     }
-    if (d.epoch + 1 >= kNoallocEpochWrap) {       // tags would repeat: start the flags over
-        if (cudaMemsetAsync(d.scratch, 0, (size_t)kNoallocDataOff, s) != cudaSuccess) return SN_E_DEVICE;
-        d.epoch = 0;
-    }
-    d.epoch += 1;
 
     CUtensorMap ma, mb;
     if (!make_scan_map(&ma, a, B, T, N, LB_NC, LB_TC) || !make_scan_map(&mb, b, B, T, N, LB_NC, LB_TC))
@@ -470,9 +483,8 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
     p.dA = reinterpret_cast<float*>(d.scratch + kNoallocDataOff);
     p.dB = p.dA + tiles * LB_NC;
     p.dC = p.dB + tiles * LB_NC;
-    p.tag = d.epoch << 2;
-    p.want = p.tag;
-    p.st = st;
+    p.poison = 0;
+    p.st = st;                                    // also holds the launch epoch
     p.wait_ns = 1000000000ull;                    // 1 s bound on every device-side wait
     // this call's error word starts at zero
     if (cudaMemsetAsync(st, 0, 2 * sizeof(int), s) != cudaSuccess) return SN_E_DEVICE;

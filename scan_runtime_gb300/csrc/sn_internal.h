@@ -12,7 +12,9 @@ struct SnDevStatus {
     int error;   // first device-side error of any launch (SN_E_*), 0 = none
     int site;    // where it happened: (kernel id << 16) | wait site
     unsigned int abort_tag;   // tag of a look-back launch in which a tile gave up waiting
-    int pad[61];
+    unsigned int lb_epoch;    // epoch of the last look-back launch, 0 = none (stored by its last CTA)
+    unsigned int lb_done;     // CTAs of the running look-back launch that have finished
+    int pad[59];
 };
 static_assert(sizeof(SnDevStatus) == 256, "status block is 256 bytes");
 
@@ -34,7 +36,6 @@ struct SnCtx {
     void* ws;
     int64_t ws_bytes;
     bool ws_dirty;              // flag area must be cleared before next use
-    uint32_t epoch;             // look-back epoch, incremented per launch
     int64_t lb_last_flags;      // flag count of the last look-back launch
     // options
     int scan_kernel;
@@ -100,8 +101,8 @@ cudaError_t launch_scan_backward(const BwdArgs& x, bool gated, SnDevStatus* st, 
                                  cudaStream_t stream);
 cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
                                    cudaStream_t stream);
-cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, uint32_t epoch, int poison,
-                                 SnDevStatus* st, uint64_t wait_ns, int sm_count, cudaStream_t stream);
+cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,
+                                 uint64_t wait_ns, int sm_count, cudaStream_t stream);
 
 enum RecurKind : int {
     RK_DIAG_KEY = 0,

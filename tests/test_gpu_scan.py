@@ -155,6 +155,46 @@ def test_lookback_deterministic(lbctx):
     assert np.array_equal(r1[0], r2[0]) and np.array_equal(r1[1], r2[1])
 
 
+def _replay_matches(sr, call, ins, expect):
+    """Capture `call` (on fixed device buffers) in a CUDA graph, then replay it
+    on each input set twice over: the outputs must equal `expect` bit for bit."""
+    B, T, N = ins[0][0].shape
+    a_d = torch.empty((B, T, N), device="cuda")
+    b_d = torch.empty_like(a_d)
+    s0_d = torch.empty((B, N), device="cuda")
+    so = torch.empty_like(a_d)
+    sf = torch.empty_like(s0_d)
+    a_d.copy_(ins[0][0])
+    b_d.copy_(ins[0][1])
+    s0_d.copy_(ins[0][2])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert call(a_d, b_d, s0_d, sf, so) == sr.SN_OK
+    for _ in range(2):
+        for (a, b, s0), (eo, ef) in zip(ins, expect):
+            a_d.copy_(a)
+            b_d.copy_(b)
+            s0_d.copy_(s0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(so.cpu().numpy(), eo) and np.array_equal(sf.cpu().numpy(), ef)
+
+
+def test_lookback_replayed_from_a_cuda_graph(sr, lbctx):
+    """A captured look-back call replayed on new inputs: every replay must
+    publish its chunk flags under a fresh tag (the launch epoch is kept and
+    advanced on the device), else a replay would take the previous replay's
+    carries as published.  Each replay equals an uncaptured call."""
+    B, T, N = 1, 8192, 64
+    lbctx.ensure_workspace(B, T, N)
+    ins = [(a, b, s0) for a, b, _, s0 in (_inputs(B, T, N, 30 + i) for i in range(3))]
+    expect = [_run(lbctx, "fma", a, b, s0) for a, b, s0 in ins]
+    call = lambda a, b, s0, sf, so: sr.sn_scan_fma(lbctx.handle, B, T, N, a, b, s0, sf, so)
+    _replay_matches(sr, call, ins, expect)
+    assert lbctx.last_error() == sr.SN_OK
+
+
 @pytest.mark.parametrize("form", ["fma", "gated"])
 def test_lookback_split_at_chunk_multiple_bit_exact(sr, lbctx, form):
     tc = lbctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK)

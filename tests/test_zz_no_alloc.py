@@ -74,3 +74,35 @@ def test_no_alloc_rejects_problems_beyond_its_scratch(sr):
     assert sr.sn_scan_lookback_noalloc(0, 1, T, 32, a, a, None, None, None) == sr.SN_E_NOMEM
     assert sr.sn_scan_lookback_noalloc(0, 1, 16, 30, a, a, None, None, None) == sr.SN_E_UNSUPPORTED
     assert sr.sn_scan_lookback_noalloc(2, 1, 16, 32, a, a, None, None, None) == sr.SN_E_INVAL
+
+
+def test_no_alloc_replayed_from_a_cuda_graph(sr):
+    """The allocation-free entry point captured in a CUDA graph (after a first,
+    uncaptured call has set the device up) and replayed on new inputs: each
+    replay equals an uncaptured call, because the launch epoch advances on
+    the device."""
+    B, T, N = 1, 8192, 64
+    ins = []
+    for i in range(3):
+        x = synth.scan_inputs(B, T, N, large=True, cid=90 + i)
+        ins.append((x["a"].cuda(), x["b"].cuda(), synth.normal((B, N), 9900 + i).cuda()))
+    expect = [_noalloc(sr, 0, a, b, s0) for a, b, s0 in ins]
+    a_d = torch.empty((B, T, N), device="cuda")
+    b_d = torch.empty_like(a_d)
+    s0_d = torch.empty((B, N), device="cuda")
+    so = torch.empty_like(a_d)
+    sf = torch.empty_like(s0_d)
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert sr.sn_scan_lookback_noalloc(0, B, T, N, a_d, b_d, s0_d, sf, so, status) == sr.SN_OK
+    for _ in range(2):
+        for (a, b, s0), (eo, ef) in zip(ins, expect):
+            a_d.copy_(a)
+            b_d.copy_(b)
+            s0_d.copy_(s0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert int(status.item()) == sr.SN_OK
+            assert np.array_equal(so.cpu().numpy(), eo) and np.array_equal(sf.cpu().numpy(), ef)
