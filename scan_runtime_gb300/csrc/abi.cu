@@ -78,7 +78,7 @@ uint64_t wait_ns(const SnCtx* c) { return (uint64_t)c->wait_limit_us * 1000ull; 
 
 namespace sn {
 bool encode_tiled(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
-                  const uint64_t* strides_bytes, const uint32_t* box) {
+                  const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
     std::call_once(g_encode_once, [] {
         cudaDriverEntryPointQueryResult q;
         void* fn = nullptr;
@@ -92,7 +92,8 @@ bool encode_tiled(CUtensorMap* map, int rank, const void* base, const uint64_t* 
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base),
                           reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
                           reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -49,6 +49,13 @@ __device__ __forceinline__ int off128(int r, int k) {
     return (r >> 3) * 1024 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3);
 }
 
+// Float offset of element (r, k) of a 128 x 128 operand in the 128-byte-swizzled
+// K-major layout (tc.cuh): atom k / 32 (16 KB), row r (128 B), 16-byte chunk
+// (k mod 32) / 4 XOR (r mod 8).
+__device__ __forceinline__ int off_sw(int r, int k) {
+    return (k >> 5) * 4096 + r * 32 + ((((k & 31) >> 2) ^ (r & 7)) << 2) + (k & 3);
+}
+
 __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
@@ -94,10 +101,13 @@ struct ChunkIdx {
     size_t bh;
 };
 
-__device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a) {
+// Units (one chunk of one head each) of a launch: B * H * (nsg or NC).
+__device__ __forceinline__ int chunk_units(const ChunkArgs& a) { return a.B * a.H * (a.nsg > 0 ? a.nsg : a.NC); }
+
+__device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a, int unit) {
     ChunkIdx c;
-    c.h = blockIdx.x % a.H;
-    const int bn = blockIdx.x / a.H;
+    c.h = unit % a.H;
+    const int bn = unit / a.H;
     const int nsg = a.nsg > 0 ? a.nsg : a.NC;
     c.n = a.n0 + bn % nsg;
     c.b = bn / nsg;
@@ -107,6 +117,8 @@ __device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a) {
     c.bh = (size_t)c.b * a.H + c.h;
     return c;
 }
+
+__device__ __forceinline__ ChunkIdx chunk_index(const ChunkArgs& a) { return chunk_index(a, (int)blockIdx.x); }
 
 // Transposing copy of a (tokens x R) slab of a row-major global array into the
 // operand layout (rows = the R columns of the array, K = tokens): element
@@ -127,9 +139,10 @@ __device__ __forceinline__ void copy_transposed(float* dst, const float* base, s
 }
 
 // recur_chunked.cu: the output kernel alone with unit decays (d == nullptr),
-// dv = 128 (used by the chunked delta rule), over chunks [n0, n0 + nsg); the
-// kernel and its shared-memory size, for opting in before the launches.
-cudaError_t launch_output_unit_decay(const ChunkArgs& a, cudaStream_t s);
+// dv = 128 (used by the chunked delta rule), over chunks [n0, n0 + nsg) on at
+// most max_ctas CTAs (fewer CTAs than units: persistent CTAs); the kernel and
+// its shared-memory size, for opting in before the launches.
+cudaError_t launch_output_unit_decay(const ChunkArgs& a, int max_ctas, cudaStream_t s);
 const void* output_unit_decay_kernel();
 size_t output_unit_decay_smem();
 

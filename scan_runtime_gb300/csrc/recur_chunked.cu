@@ -398,6 +398,14 @@ __global__ void __launch_bounds__(256) chunk_carry(const ChunkArgs a, int dv) {
 }
 
 // ------------------------------------------------------------------ chunk_output
+// Persistent: CTA i takes units i, i + grid, ... (a unit is one chunk of one
+// head), and the next unit's operands stream in as the current unit frees
+// their space: its decays into registers after the rescaling, its S' tile
+// into the S buffer after the first two products, its v slice into registers
+// after the first epilogue, and its q and k rows into the Q and K buffers
+// after the last product.  q and k arrive by TMA in the 128-byte-swizzled
+// K-major layout (four 32-key x 128-token boxes each; rows past T are filled
+// with zeros), which the first two products read directly.
 template <int DV>
 struct OutSmem {
     static constexpr int q_off = 0;              // Qt, later the masked A
@@ -405,180 +413,231 @@ struct OutSmem {
     static constexpr int s_off = 2 * OPF;        // S'^T (rows c, K = i)
     static constexpr int lam_off = s_off + DV * DKC;   // [CH] per-head lam
     static constexpr int misc_off = lam_off + CH;
-    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 1024;
 };
 
 template <bool PER_KEY, int DV>
-__global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
+__global__ void __launch_bounds__(NT, 1)
+chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, const ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     using L = OutSmem<DV>;
-    float* base = align128(smem_raw);
+    float* base = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* bufQ = base + L::q_off;
     float* bufK = base + L::k_off;
     float* bufS = base + L::s_off;
     float* lam_s = base + L::lam_off;
-    uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);
-    uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+    uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);       // S' tiles, one per unit
+    uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);   // products, two per unit
+    uint64_t* barV = reinterpret_cast<uint64_t*>(base + L::misc_off + 4);   // v^T tiles, one per unit
+    uint64_t* barQ = reinterpret_cast<uint64_t*>(base + L::misc_off + 6);   // q and k tiles, one pair per unit
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const ChunkIdx c = chunk_index(a);
+    const int units = chunk_units(a);
+    // rescaling of q, k (and the per-key decays): warp = 16 key columns,
+    // lane = (token mod 8, 4-column group)
+    const int tl = lane & 7, ig = lane >> 3;
+    const int ic = 16 * warp + 4 * ig;
+    // v slice for the last product, in registers: thread = value column, a run
+    // of tokens (unless the caller supplies the v^T operand tiles)
+    constexpr int TP = CH / (NT / DV);
+    const int col = tid % DV, part = tid / DV;
+    // tensor-memory rows: warp quarter lq, token t
+    const int lq = warp & 3, hf = warp >> 2;
+    const int t = 32 * lq + lane;
 
     if (warp == 0) tc::tmem_alloc(slot, 256);
     if (tid == 0) {
         mbar_init(barS, 1);
         mbar_init(barM, 1);
+        mbar_init(barV, 1);
+        mbar_init(barQ, 1);
         fence_mbar_init();
-        // the chunk's S' operand: one contiguous tile written by chunk_carry
-        mbar_arrive_expect_tx(barS, DV * DKC * 4);
-        bulk_load(bufS, a.W + (c.bh * a.NC + c.n) * (size_t)DV * DKC, DV * DKC * 4, barS);
     }
     __syncthreads();   // barriers initialised before any thread polls them
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
 
-    // q, k rows straight into the operand layout: warp = 16 key columns,
-    // lane = (token mod 8, 4-column group)
-    const int tl = lane & 7, ig = lane >> 3;
-    const int ic = 16 * warp + 4 * ig;
-    const size_t qrs = (size_t)a.G * DKC;
-    const size_t row0 = (size_t)c.b * a.T + c.t0;
-    const float* qb = a.q + row0 * qrs + (size_t)c.g * DKC + ic;
-    const float* kb = a.k + row0 * qrs + (size_t)c.g * DKC + ic;
-#pragma unroll
-    for (int tb = 0; tb < CH / 8; ++tb) {
-        const int t = 8 * tb + tl;
-        const bool ok = t < c.nval;
-        const size_t src = (size_t)(ok ? t : 0) * qrs;
-        cp_async16(bufQ + off128(t, ic), qb + src, ok);
-        cp_async16(bufK + off128(t, ic), kb + src, ok);
-    }
-    cp_async_commit();
-
-    // v slice for the last product, in registers: thread = value column, a run of tokens
-    // (unless the caller supplies the v^T operand tiles)
-    constexpr int TP = CH / (NT / DV);
-    const int col = tid % DV, part = tid / DV;
+    // operands of the unit being loaded (registers are filled by the loads in flight)
     float vr[TP];
-    if (a.vt == nullptr) {
+    float4 draw[CH / 8];   // per-key decays, lane mapping of q and k
+    float lgh[4];          // per-head decays of tokens 4 lane .. 4 lane + 3 (warp 0)
+    int s_loads = 0, v_loads = 0, q_loads = 0;   // copies issued on barS / barV / barQ (thread 0's count)
+
+    auto issue_s = [&](const ChunkIdx& c) {   // thread 0: the chunk's S' operand, one contiguous tile
+        mbar_arrive_expect_tx(barS, DV * DKC * 4);
+        bulk_load(bufS, a.W + (c.bh * a.NC + c.n) * (size_t)DV * DKC, DV * DKC * 4, barS);
+        ++s_loads;
+    };
+    auto issue_qk = [&](const ChunkIdx& c) {   // thread 0: q and k tiles, four swizzled 32-key boxes each
+        mbar_arrive_expect_tx(barQ, 2 * OPF * 4);
+#pragma unroll
+        for (int at = 0; at < DKC / 32; ++at) {
+            tma_load_3d(bufQ + at * 4096, &map_q, barQ, c.g * DKC + 32 * at, c.t0, c.b);
+            tma_load_3d(bufK + at * 4096, &map_k, barQ, c.g * DKC + 32 * at, c.t0, c.b);
+        }
+        ++q_loads;
+    };
+    auto issue_v = [&](const ChunkIdx& c) {   // all threads: the v slice into registers
+        if (a.vt != nullptr) return;
+        const size_t row0 = (size_t)c.b * a.T + c.t0;
         const size_t vrs = (size_t)a.H * DV;
         const float* vcol = a.v + row0 * vrs + (size_t)c.h * DV + col;
 #pragma unroll
         for (int r = 0; r < TP; ++r) {
-            const int t = part * TP + r;
-            vr[r] = t < c.nval ? __ldg(vcol + (size_t)t * vrs) : 0.f;
+            const int tt = part * TP + r;
+            vr[r] = tt < c.nval ? __ldg(vcol + (size_t)tt * vrs) : 0.f;
         }
-    }
-
-    // decay prefix sums: per key in registers (same lane mapping), per head in shared memory
-    float4 lam[CH / 8];
-    float4 lm = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (PER_KEY) {
-        const size_t drs = (size_t)a.H * DKC;
-        const float* db = a.d + row0 * drs + (size_t)c.h * DKC + ic;
-#pragma unroll
-        for (int tb = 0; tb < CH / 8; ++tb) {
-            const int t = 8 * tb + tl;
-            lam[tb] = t < c.nval ? ldg4(db + (size_t)t * drs) : make_float4(1.f, 1.f, 1.f, 1.f);
-        }
-        float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 lmax = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        float4 lmin = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
-#pragma unroll
-        for (int tb = 0; tb < CH / 8; ++tb) {
-            float4 x = make_float4(lg2(lam[tb].x), lg2(lam[tb].y), lg2(lam[tb].z), lg2(lam[tb].w));
-#pragma unroll
-            for (int off = 1; off < 8; off <<= 1) {
-                const float yx = __shfl_up_sync(FULL, x.x, off, 8), yy = __shfl_up_sync(FULL, x.y, off, 8);
-                const float yz = __shfl_up_sync(FULL, x.z, off, 8), yw = __shfl_up_sync(FULL, x.w, off, 8);
-                if (tl >= off) {
-                    x.x += yx; x.y += yy; x.z += yz; x.w += yw;
-                }
-            }
-            x.x += carry.x; x.y += carry.y; x.z += carry.z; x.w += carry.w;
-            carry = make_float4(__shfl_sync(FULL, x.x, 7, 8), __shfl_sync(FULL, x.y, 7, 8),
-                                __shfl_sync(FULL, x.z, 7, 8), __shfl_sync(FULL, x.w, 7, 8));
-            if (tb == ANCHOR / 8) lm = carry;
-            lmax = make_float4(fmaxf(lmax.x, x.x), fmaxf(lmax.y, x.y), fmaxf(lmax.z, x.z), fmaxf(lmax.w, x.w));
-            lmin = make_float4(fminf(lmin.x, x.x), fminf(lmin.y, x.y), fminf(lmin.z, x.z), fminf(lmin.w, x.w));
-            lam[tb] = x;
-        }
-        // the anchor factors must stay within 2^{+-RANGE}: NaN (decay <= 0) fails too
-        const bool in_range = (lmax.x - lm.x <= RANGE_LOG2) && (lm.x - lmin.x <= RANGE_LOG2) &&
-                              (lmax.y - lm.y <= RANGE_LOG2) && (lm.y - lmin.y <= RANGE_LOG2) &&
-                              (lmax.z - lm.z <= RANGE_LOG2) && (lm.z - lmin.z <= RANGE_LOG2) &&
-                              (lmax.w - lm.w <= RANGE_LOG2) && (lm.w - lmin.w <= RANGE_LOG2);
-        if (!__all_sync(FULL, in_range) && lane == 0)
-            record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_KEY);
-    } else if (warp == 0) {
-        // inclusive prefix sums of log2 d (per head) into lam_s
-        float lg[4], s = 0.f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int t = 4 * lane + r;
-            lg[r] = (t < c.nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
-            s += lg[r];
-        }
-        float x = s;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(FULL, x, off);
-            if (lane >= off) x += y;
-        }
-        float acc = x - s;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            acc += lg[r];
-            lam_s[4 * lane + r] = acc;
-        }
-        const float total = __shfl_sync(FULL, x, 31);
-        if (lane == 0 && !isfinite(total))
-            record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
-    }
-
-    // Qt, Kt in place (each thread rescales the rows its own copies wrote)
-    cp_async_wait_all();
-#pragma unroll
-    for (int tb = 0; tb < CH / 8; ++tb) {
-        const int o = off128(8 * tb + tl, ic);
-        const float4 q4 = ld4(bufQ + o), k4 = ld4(bufK + o);
+    };
+    auto issue_d = [&](const ChunkIdx& c) {   // the decays into registers
+        const size_t row0 = (size_t)c.b * a.T + c.t0;
         if (PER_KEY) {
-            const float4 x = lam[tb];
-            st4(bufQ + o, tf32x4(q4.x * ex2(x.x - lm.x), q4.y * ex2(x.y - lm.y), q4.z * ex2(x.z - lm.z),
-                                 q4.w * ex2(x.w - lm.w)));
-            st4(bufK + o, tf32x4(k4.x * ex2(lm.x - x.x), k4.y * ex2(lm.y - x.y), k4.z * ex2(lm.z - x.z),
-                                 k4.w * ex2(lm.w - x.w)));
-        } else {
-            st4(bufQ + o, tf32x4(q4));
-            st4(bufK + o, tf32x4(k4));
+            const size_t drs = (size_t)a.H * DKC;
+            const float* db = a.d + row0 * drs + (size_t)c.h * DKC + ic;
+#pragma unroll
+            for (int tb = 0; tb < CH / 8; ++tb) {
+                const int tt = 8 * tb + tl;
+                draw[tb] = tt < c.nval ? ldg4(db + (size_t)tt * drs) : make_float4(1.f, 1.f, 1.f, 1.f);
+            }
+        } else if (warp == 0) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int tt = 4 * lane + r;
+                lgh[r] = (tt < c.nval && a.d != nullptr) ? __ldg(a.d + (row0 + tt) * a.H + c.h) : 1.f;
+            }
         }
-    }
+    };
 
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    bool ok = __syncthreads_and(mbar_wait(barS, 0, a.wait_ns));
-    tc::fence_after_sync();
-    const uint32_t tmem = *slot;
-    if (!ok) {
+    bool ok = true;
+    int site = 0;
+    if ((int)blockIdx.x < units) {
+        const ChunkIdx c0 = chunk_index(a, blockIdx.x);
         if (tid == 0) {
-            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
-            mbar_wait(barS, 0, a.wait_ns);   // let a late copy land before the CTA exits
+            issue_s(c0);
+            issue_qk(c0);
         }
-    } else if (tid == 0) {
-        tc::gemm_tf32(tmem, bufQ, bufK, DKC, tc::idesc_tf32(128, 128), false);        // A (cols 0..127)
-        tc::gemm_tf32(tmem + 128, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);   // P (cols 128..)
-        tc::commit(barM);
+        issue_v(c0);
+        issue_d(c0);
     }
+    int it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+        const ChunkIdx c = chunk_index(a, u);
+        const bool has_next = u + (int)gridDim.x < units;
+        const ChunkIdx cn = chunk_index(a, has_next ? u + (int)gridDim.x : u);
+        const size_t row0 = (size_t)c.b * a.T + c.t0;
+        const uint32_t ph = (uint32_t)it & 1;
 
-    const int lq = warp & 3, hf = warp >> 2;
-    const int t = 32 * lq + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
-    if (ok) {
+        // decay prefix sums: per key in registers (the q, k lane mapping), per head in shared memory
+        float4 lam[CH / 8];
+        float4 lm = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (PER_KEY) {
+            float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 lmax = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            float4 lmin = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+#pragma unroll
+            for (int tb = 0; tb < CH / 8; ++tb) {
+                float4 x = make_float4(lg2(draw[tb].x), lg2(draw[tb].y), lg2(draw[tb].z), lg2(draw[tb].w));
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1) {
+                    const float yx = __shfl_up_sync(FULL, x.x, off, 8), yy = __shfl_up_sync(FULL, x.y, off, 8);
+                    const float yz = __shfl_up_sync(FULL, x.z, off, 8), yw = __shfl_up_sync(FULL, x.w, off, 8);
+                    if (tl >= off) {
+                        x.x += yx; x.y += yy; x.z += yz; x.w += yw;
+                    }
+                }
+                x.x += carry.x; x.y += carry.y; x.z += carry.z; x.w += carry.w;
+                carry = make_float4(__shfl_sync(FULL, x.x, 7, 8), __shfl_sync(FULL, x.y, 7, 8),
+                                    __shfl_sync(FULL, x.z, 7, 8), __shfl_sync(FULL, x.w, 7, 8));
+                if (tb == ANCHOR / 8) lm = carry;
+                lmax = make_float4(fmaxf(lmax.x, x.x), fmaxf(lmax.y, x.y), fmaxf(lmax.z, x.z), fmaxf(lmax.w, x.w));
+                lmin = make_float4(fminf(lmin.x, x.x), fminf(lmin.y, x.y), fminf(lmin.z, x.z), fminf(lmin.w, x.w));
+                lam[tb] = x;
+            }
+            // the anchor factors must stay within 2^{+-RANGE}: NaN (decay <= 0) fails too
+            const bool in_range = (lmax.x - lm.x <= RANGE_LOG2) && (lm.x - lmin.x <= RANGE_LOG2) &&
+                                  (lmax.y - lm.y <= RANGE_LOG2) && (lm.y - lmin.y <= RANGE_LOG2) &&
+                                  (lmax.z - lm.z <= RANGE_LOG2) && (lm.z - lmin.z <= RANGE_LOG2) &&
+                                  (lmax.w - lm.w <= RANGE_LOG2) && (lm.w - lmin.w <= RANGE_LOG2);
+            if (!__all_sync(FULL, in_range) && lane == 0)
+                record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_KEY);
+        } else if (warp == 0) {
+            // inclusive prefix sums of log2 d (per head) into lam_s
+            float lg[4], sm = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                lg[r] = lg2(lgh[r]);
+                sm += lg[r];
+            }
+            float x = sm;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(FULL, x, off);
+                if (lane >= off) x += y;
+            }
+            float acc = x - sm;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                acc += lg[r];
+                lam_s[4 * lane + r] = acc;
+            }
+            const float total = __shfl_sync(FULL, x, 31);
+            if (lane == 0 && !isfinite(total))
+                record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
+        }
+
+        // Qt, Kt in place, in the swizzled layout
+        ok = __syncthreads_and(mbar_wait(barQ, ph, a.wait_ns));
+        if (!ok) {
+            site = SITE_OUT_COPY;
+            break;
+        }
+#pragma unroll
+        for (int tb = 0; tb < CH / 8; ++tb) {
+            const int o = off_sw(8 * tb + tl, ic);
+            const float4 q4 = ld4(bufQ + o), k4 = ld4(bufK + o);
+            if (PER_KEY) {
+                const float4 x = lam[tb];
+                st4(bufQ + o, tf32x4(q4.x * ex2(x.x - lm.x), q4.y * ex2(x.y - lm.y), q4.z * ex2(x.z - lm.z),
+                                     q4.w * ex2(x.w - lm.w)));
+                st4(bufK + o, tf32x4(k4.x * ex2(lm.x - x.x), k4.y * ex2(lm.y - x.y), k4.z * ex2(lm.z - x.z),
+                                     k4.w * ex2(lm.w - x.w)));
+            } else {
+                st4(bufQ + o, tf32x4(q4));
+                st4(bufK + o, tf32x4(k4));
+            }
+        }
+
+        if (has_next) issue_d(cn);   // this unit's decays are consumed: the next unit's stream in
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        ok = __syncthreads_and(mbar_wait(barS, ph, a.wait_ns));
+        tc::fence_after_sync();
+        if (!ok) {
+            site = SITE_OUT_COPY;
+            break;
+        }
+        if (tid == 0) {
+            tc::gemm_tf32_sw_sw(tmem, bufQ, bufK, tc::idesc_tf32(128, 128), false);          // A (cols 0..127)
+            tc::gemm_tf32_sw_plain(tmem + 128, bufQ, bufS, tc::idesc_tf32(128, DV), false);  // P (cols 128..)
+            tc::commit(barM);
+        }
         ok = __syncthreads_and(mbar_wait(barM, 0, a.wait_ns));
         tc::fence_after_sync();
-        if (ok && a.vt != nullptr && tid == 0) {   // the K buffer is free: the v^T tile streams in
-            mbar_arrive_expect_tx(barS, DV * CH * 4);
-            bulk_load(bufK, a.vt + (c.bh * a.NC + c.n) * (size_t)DV * CH, DV * CH * 4, barS);
+        if (!ok) {
+            site = SITE_OUT_WAIT1;
+            break;
         }
-        if (ok) {
+        if (tid == 0) {
+            // the K buffer is free: the v^T tile streams in; the S buffer is free: the next unit's S'
+            if (a.vt != nullptr) {
+                mbar_arrive_expect_tx(barV, DV * CH * 4);
+                bulk_load(bufK, a.vt + (c.bh * a.NC + c.n) * (size_t)DV * CH, DV * CH * 4, barV);
+                ++v_loads;
+            }
+            if (has_next) issue_s(cn);
+        }
+        {
             const float lt = PER_KEY ? 0.f : lam_s[t];
             // masked (and, per head, decay-weighted) A into the Q buffer as the next A operand
 #pragma unroll
@@ -601,29 +660,29 @@ __global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
                     st4(bufK + off128(col, part * TP + 4 * t4),
                         tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
             }
-        } else if (tid == 0) {
-            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT1);
         }
+        if (has_next) issue_v(cn);   // this unit's v slice is in the K buffer: the next unit's streams in
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        const bool vok = __syncthreads_and(!ok || a.vt == nullptr || mbar_wait(barS, 1, a.wait_ns));
+        ok = __syncthreads_and(a.vt == nullptr || mbar_wait(barV, ph, a.wait_ns));
         tc::fence_after_sync();
-        if (ok && !vok) {
-            if (tid == 0) {
-                record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
-                mbar_wait(barS, 1, a.wait_ns);   // let a late copy land before the CTA exits
-            }
-            ok = false;
+        if (!ok) {
+            site = SITE_OUT_COPY;
+            break;
         }
-    }
-    if (ok) {
         if (tid == 0) {
             tc::gemm_tf32(tmem, bufQ, bufK, CH, tc::idesc_tf32(128, DV), false);   // O (cols 0..DV-1)
             tc::commit(barM);
         }
         ok = __syncthreads_and(mbar_wait(barM, 1, a.wait_ns));
         tc::fence_after_sync();
-        if (ok) {
+        if (!ok) {
+            site = SITE_OUT_WAIT2;
+            break;
+        }
+        // the Q and K buffers are free: the next unit's q and k stream in
+        if (has_next && tid == 0) issue_qk(cn);
+        {
             const float fp = PER_KEY ? 1.f : ex2(lam_s[t]);
             const bool store = t < c.nval && a.o != nullptr;
             float* orow = a.o + (row0 + t) * a.H * DV + (size_t)c.h * DV;
@@ -642,9 +701,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_output(const ChunkArgs a) {
                                           a.scale * fmaf(fp, p[4 * q + 3], x[4 * q + 3])));
                 }
             }
-        } else if (tid == 0) {
-            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
         }
+        // tensor memory and the per-head sums are reused by the next unit
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    if (!ok && tid == 0) {
+        record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
+        // at most one copy per barrier can still be in flight: let it land
+        if (s_loads > 0) (void)mbar_wait(barS, (uint32_t)(s_loads - 1) & 1, a.wait_ns);
+        if (v_loads > 0) (void)mbar_wait(barV, (uint32_t)(v_loads - 1) & 1, a.wait_ns);
+        if (q_loads > 0) (void)mbar_wait(barQ, (uint32_t)(q_loads - 1) & 1, a.wait_ns);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -908,6 +976,15 @@ int heads_per_cta(const ChunkArgs& a, int sm_count) {
     return 1;
 }
 
+// TMA maps of q and k for the output kernel: (B, T, G * dk) row-major, boxes
+// of 32 keys x 128 tokens, 128-byte swizzle.
+bool make_qk_maps(const ChunkArgs& a, CUtensorMap* mq, CUtensorMap* mk) {
+    const uint64_t dims[3] = {(uint64_t)a.G * DKC, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t strides[2] = {(uint64_t)a.G * DKC * 4, (uint64_t)a.T * a.G * DKC * 4};
+    const uint32_t box[3] = {32, (uint32_t)CH, 1};
+    return encode_tiled(mq, 3, a.q, dims, strides, box, true) && encode_tiled(mk, 3, a.k, dims, strides, box, true);
+}
+
 template <bool PER_KEY, int DV>
 cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     constexpr bool HEADS = !PER_KEY && DV == 64;   // per-head decays: heads of a group share Q K^T
@@ -947,7 +1024,9 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
         const int hb = heads_per_cta(a, sm_count);
         chunk_output_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, out_bytes, s>>>(a, hb);
     } else {
-        chunk_output<PER_KEY, DV><<<chunks, NT, out_bytes, s>>>(a);
+        CUtensorMap mq, mk;
+        if (!make_qk_maps(a, &mq, &mk)) return cudaErrorInvalidValue;
+        chunk_output<PER_KEY, DV><<<(unsigned)std::min<size_t>(chunks, (size_t)sm_count), NT, out_bytes, s>>>(mq, mk, a);
     }
     return cudaGetLastError();
 }
@@ -959,12 +1038,15 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 // The output stage alone with unit decays (a.d == nullptr, per-head path):
 // o = scale (Q S_n + tril(Q K^T) V) for every chunk, with V and the chunk
 // states S_n (operand layout, tf32) supplied by the caller; dv = 128.
-cudaError_t chunk::launch_output_unit_decay(const ChunkArgs& a, cudaStream_t s) {
+cudaError_t chunk::launch_output_unit_decay(const ChunkArgs& a, int max_ctas, cudaStream_t s) {
     const size_t bytes = OutSmem<128>::bytes;
     const cudaError_t e = set_smem_attr_once((const void*)chunk_output<false, 128>, bytes);
     if (e != cudaSuccess) return e;
     const int nsg = a.nsg > 0 ? a.nsg : a.NC;
-    chunk_output<false, 128><<<(unsigned)((size_t)a.B * a.H * nsg), NT, bytes, s>>>(a);
+    const size_t units = (size_t)a.B * a.H * nsg;
+    CUtensorMap mq, mk;
+    if (!make_qk_maps(a, &mq, &mk)) return cudaErrorInvalidValue;
+    chunk_output<false, 128><<<(unsigned)std::min<size_t>(units, (size_t)max_ctas), NT, bytes, s>>>(mq, mk, a);
     return cudaGetLastError();
 }
 

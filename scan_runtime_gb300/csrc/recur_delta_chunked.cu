@@ -582,7 +582,9 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
         if (e != cudaSuccess) break;
         c.n0 = d.n0;
         c.nsg = d.n1 - d.n0;
-        e = launch_output_unit_decay(c, so);
+        // pipelined: one CTA per unit, so the output CTAs fill whatever SMs the other
+        // stages leave (persistent CTAs, assigned their units up front, measured slower)
+        e = launch_output_unit_decay(c, piped ? INT32_MAX : sm_count, so);
     }
     // join: the caller's stream waits for the side streams, also after an error
     for (cudaStream_t side : {sp, sc, so}) {

@@ -33,6 +33,23 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// 128-byte-swizzled K-major operand (the layout a TMA copy with 128-byte
+// swizzle writes): atoms of 32 K elements (128 B) x R rows, rows 128 B apart,
+// 8-row groups 1024 B apart, the 16-byte chunks of each row permuted by XOR
+// with (row mod 8).  Atoms must start at 1024-byte boundaries.  Within an atom
+// one kind::tf32 MMA (K = 8) advances the start by 32 bytes; the next atom is
+// R * 128 bytes further.  Fields: leading offset 16 B (unused), stride offset
+// 1024 B, version 1, swizzle mode 128 B (value 2 in bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::tf32: fp32 accumulator, tf32 A and B, both
 // K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -85,6 +102,29 @@ __device__ __forceinline__ void gemm_tf32(uint32_t d_tmem, const float* A, const
     for (int kk = 0; kk < KD / 8; ++kk)
         mma_tf32(d_tmem, smem_desc(a0 + kk * 256, 128, sbo), smem_desc(b0 + kk * 256, 128, sbo), idesc,
                  accumulate || kk > 0);
+}
+
+// D = A * B^T with K = 128, M = N = 128 rows, A and B both 128-byte-swizzled
+// (four atoms of 32 K elements, 16 KB apart).
+__device__ __forceinline__ void gemm_tf32_sw_sw(uint32_t d_tmem, const float* A, const float* B, uint32_t idesc,
+                                                bool accumulate) {
+    const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+    for (int kk = 0; kk < 16; ++kk) {
+        const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+        mma_tf32(d_tmem, smem_desc_sw128(a0 + off), smem_desc_sw128(b0 + off), idesc, accumulate || kk > 0);
+    }
+}
+
+// D = A * B^T with K = 128: A 128-byte-swizzled (128 rows, atoms 16 KB apart),
+// B in the plain K-major layout above.
+__device__ __forceinline__ void gemm_tf32_sw_plain(uint32_t d_tmem, const float* A, const float* B, uint32_t idesc,
+                                                   bool accumulate) {
+    const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+    for (int kk = 0; kk < 16; ++kk) {
+        const uint32_t aoff = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+        mma_tf32(d_tmem, smem_desc_sw128(a0 + aoff), smem_desc(b0 + kk * 256, 128, 32 * 128), idesc,
+                 accumulate || kk > 0);
+    }
 }
 
 // Warp-collective load of 16 consecutive fp32 columns of this warp's 32 lanes.
