@@ -60,8 +60,9 @@ struct DeltaArgs {
 // ------------------------------------------------------------------ delta_prep
 struct PrepSmem {
     static constexpr int b0 = 0;                 // K (hi), then K^T operand
-    static constexpr int b1 = OPF;               // K (lo), then A^T (fp32, stride LDX), then V^T operand
-    static constexpr int b2 = b1 + CH * LDX;     // X = (I + A)^{-1} (fp32, stride LDX), then T operand
+    static constexpr int b1 = OPF;               // K (lo), then V^T operand
+    static constexpr int b2 = 2 * OPF;           // A^T above the diagonal and X = (I + A)^{-1} on and
+                                                 // below it (fp32, stride LDX), then T operand
     static constexpr int beta = b2 + CH * LDX;
     static constexpr int misc = beta + CH;
     static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
@@ -71,9 +72,11 @@ struct PrepSmem {
 // every 2S x 2S diagonal block, whose two S x S diagonal blocks X_A (upper
 // left) and X_D (lower right) are already inverted, the lower-left block is
 //     X_C = -X_D (A_C X_A)
-// with A_C the matching block of A (read from A^T).  The product Y = A_C X_A
-// is parked in the upper-right S x S block, which X never uses (X is zero
-// there and the T operand masks it).  Every thread owns RT = S / 16 rows x 4
+// with A_C the matching block of A (read from A^T).  A^T and X share one
+// array (A^T strictly above the diagonal, X on and below it), and the product
+// Y = A_C X_A is parked over A_C itself, the upper-right S x S block, once
+// every thread has read A_C (no later level reads it; X is zero there and the
+// T operand masks it).  Every thread owns RT = S / 16 rows x 4
 // columns of one pair's block, so all 256 threads work at every level.  The
 // sums skip X_A's and X_D's zero triangles in steps of four; the few entries
 // past the triangle that a step still touches sit in a diagonal 16 x 16 block
@@ -108,6 +111,7 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
             }
         }
     }
+    __syncthreads();   // A_C is read: Y goes over it
 #pragma unroll
     for (int j = 0; j < RT; ++j)
         st4(Xm + (o + r0 + j) * LDX + o + S + c0, make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
@@ -206,12 +210,16 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
     const int tr = 32 * lq + lane;                           // tensor-memory row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     if (ok) {
-        // the K^T operand can stream in now (buf0's hi part is consumed)
+        // the K^T and V^T operands can stream in now (the Gram products have
+        // read the hi and lo parts of K) while the inverse runs
         copy_transposed<DKC>(buf0, a.k + row0 * krs + (size_t)h * DKC, krs, nval, warp, lane);
+        copy_transposed<128>(buf1, a.v + row0 * (size_t)a.H * 128 + (size_t)h * 128, (size_t)a.H * 128, nval, warp,
+                             lane);
         cp_async_commit();
 
         // A = diag(beta) strict_lower(K K^T) in fp32, stored transposed: AT[j][t] = A[t][j]
-        float* AT = buf1;
+        // (zeros on and below the diagonal, where X goes next)
+        float* AT = buf2;
         float* Xm = buf2;
         const float bt = beta_s[tr];
 #pragma unroll
@@ -240,6 +248,7 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
                     if (r > m) xr[jj] = fmaf(-AT[(r0 + m) * LDX + r0 + r], xm, xr[jj]);
                 }
             }
+            __syncwarp();   // the block's A^T entries are read: its X (zeros above the diagonal) goes over them
 #pragma unroll
             for (int jj = 0; jj < BSZ / 2; ++jj) Xm[(r0 + rb + 2 * jj) * LDX + r0 + c] = xr[jj];
         }
@@ -248,11 +257,6 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
         inverse_level<16>(Xm, AT, tid);
         inverse_level<32>(Xm, AT, tid);
         inverse_level<64>(Xm, AT, tid);
-
-        // A is consumed: the V^T operand streams into its buffer
-        copy_transposed<128>(buf1, a.v + row0 * (size_t)a.H * 128 + (size_t)h * 128, (size_t)a.H * 128, nval, warp,
-                             lane);
-        cp_async_commit();
 
         // T = X diag(beta) as the tf32 operand (rows t, K = j), in place through registers
         float4 tv[CH / 8];
