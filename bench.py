@@ -330,6 +330,26 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
             out[f"scan_{form}_lookback"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
                                            "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+        # few channels, long T (B=1 T=262144 N=64, the chunked kernels' regime):
+        # the automatic choice (reduce-then-scan) and the look-back kernel
+        Bf, Tf, Nf = 1, 262144, 64
+        xf = synth.scan_inputs(Bf, Tf, Nf, large=True, cid=6)
+        af, bf, s0f = xf["a"].to(dev), xf["b"].to(dev), xf["s0"].to(dev)
+        sof = torch.empty_like(af)
+        sff = torch.empty_like(s0f)
+        ctx.ensure_workspace(Bf, Tf, Nf)
+        few = {"workload": f"B={Bf} T={Tf} N={Nf}", "bytes_per_call": scan_bytes(Bf, Tf, Nf)}
+        for label, kern in (("reduce_scan", sr.SN_SCAN_KERNEL_REDUCE_SCAN), ("lookback", sr.SN_SCAN_KERNEL_LOOKBACK),
+                            ("sequential", sr.SN_SCAN_KERNEL_SEQUENTIAL)):
+            ctx.set_option(sr.SN_OPT_SCAN_KERNEL, kern)
+            ms = time_form(torch, lambda: sr.sn_scan_fma(ctx.handle, Bf, Tf, Nf, af, bf, s0f, sff, sof, s), warmup,
+                           reps, s)
+            few[label] = {"ms": round(ms, 4), "GBps": round(scan_bytes(Bf, Tf, Nf) / ms / 1e6, 1),
+                          "hbm_frac": round(scan_bytes(Bf, Tf, Nf) / ms / 1e6 / hbm_peak, 3)}
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+        few["auto_picks"] = "reduce_scan"
+        out["scan_fma_few_channels"] = few
+        del xf, af, bf, s0f, sof, sff
         # reverse scans (backward pass) on the same workload: read a, s, ds (+u),
         # write da, db|du
         gs_ = torch.empty((B, T, N), device=dev).normal_(generator=torch.Generator(dev).manual_seed(77))

@@ -97,7 +97,8 @@ typedef int32_t sn_status;
 #define SN_DECAY_PER_HEAD_GATED 3   /* as PER_HEAD, injection weighted by (1 - d)              */
 
 /* Context options (sn_ctx_set_option / sn_ctx_get_option). */
-#define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back */
+#define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back,
+                                      3 chunked reduce-then-scan */
 #define SN_OPT_WAIT_LIMIT_US    2  /* bound on any device-side wait, microseconds (default 1e6) */
 #define SN_OPT_DEBUG_POISON     3  /* 1: look-back waits for a flag no chunk publishes (tests the bound) */
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
@@ -110,6 +111,7 @@ typedef int32_t sn_status;
 #define SN_SCAN_KERNEL_AUTO       0
 #define SN_SCAN_KERNEL_SEQUENTIAL 1
 #define SN_SCAN_KERNEL_LOOKBACK   2
+#define SN_SCAN_KERNEL_REDUCE_SCAN 3   /* the look-back kernel's results in three flag-free passes */
 
 /* Operation ids for sn_workspace_bytes(). */
 #define SN_OP_SCAN_FMA   1
@@ -176,11 +178,13 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value);
  * The sequential kernel (the default whenever it fills the GPU) gives the
  * same bits as the single-precision definition at every t, so splitting a
  * sequence into segments and carrying s_final -> s0 reproduces the full run
- * bit for bit ([P1] §4).  The chunked look-back kernel (chosen for few
- * channels and long T, or forced by SN_OPT_SCAN_KERNEL) is deterministic and
- * bit-exact under splits at multiples of SN_OPT_LOOKBACK_CHUNK.  Calls may be
- * captured in a CUDA graph and replayed: the look-back kernel keeps its launch
- * epoch in device memory, so every replay tags its chunk flags afresh.
+ * bit for bit ([P1] §4).  For few channels and long T the call chunks T
+ * instead: the reduce-then-scan path (chosen automatically there) or the
+ * decoupled look-back kernel (SN_OPT_SCAN_KERNEL); the two give the same bits,
+ * are deterministic and are bit-exact under splits at multiples of
+ * SN_OPT_LOOKBACK_CHUNK.  Calls may be captured in a CUDA graph and replayed:
+ * the look-back kernel keeps its launch epoch in device memory, so every
+ * replay tags its chunk flags afresh.
  * Pointers need 4-byte alignment; N % 4 == 0 with 16-byte aligned a, b and
  * s_out enables the TMA path.  Errors: SN_E_INVAL, SN_E_NOMEM (look-back
  * forced without enough workspace), SN_E_DEVICE. */

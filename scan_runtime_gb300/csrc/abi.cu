@@ -243,7 +243,7 @@ sn_status sn_ctx_set_option(SnCtx* ctx, int32_t key, int32_t value) {
     if (ctx == nullptr) return SN_E_INVAL;
     switch (key) {
         case SN_OPT_SCAN_KERNEL:
-            if (value < SN_SCAN_KERNEL_AUTO || value > SN_SCAN_KERNEL_LOOKBACK) return SN_E_INVAL;
+            if (value < SN_SCAN_KERNEL_AUTO || value > SN_SCAN_KERNEL_REDUCE_SCAN) return SN_E_INVAL;
             ctx->scan_kernel = value;
             return SN_OK;
         case SN_OPT_WAIT_LIMIT_US:
@@ -303,17 +303,19 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     ScanArgs x{B, T, N, a, b, s0, s_final, s_out};
     int kernel = ctx->scan_kernel;
     const int64_t need = lookback_ws_bytes(B, T, N);
-    if (kernel == SN_SCAN_KERNEL_LOOKBACK) {
+    if (kernel == SN_SCAN_KERNEL_LOOKBACK || kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
         if (!lookback_supported(x)) return SN_E_UNSUPPORTED;
         if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
     } else if (kernel == SN_SCAN_KERNEL_AUTO) {
         // The sequential kernel keeps the exact per-step bits and is HBM-bound
         // once there are enough channels; chunking along T pays only when the
-        // channel count leaves most SMs idle and T is long.
+        // channel count leaves most SMs idle and T is long.  Of the two chunked
+        // paths (same bits), reduce-then-scan measured faster whenever the
+        // channels are that few: the look-back folds hundreds of chunks deep.
         const int64_t seq_ctas = (int64_t)B * ((N + 63) / 64);
         const bool few = seq_ctas < 2 * ctx->sm_count;
         kernel = (few && T >= 8 * LB_TC && lookback_supported(x) && ctx->ws != nullptr && ctx->ws_bytes >= need)
-                     ? SN_SCAN_KERNEL_LOOKBACK
+                     ? SN_SCAN_KERNEL_REDUCE_SCAN
                      : SN_SCAN_KERNEL_SEQUENTIAL;
     }
     DeviceGuard g(ctx->device);
@@ -334,6 +336,8 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->debug_poison, ctx->dstatus, wait_ns(ctx),
                                               ctx->sm_count, s));
     }
+    if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN)
+        return from_cuda(launch_scan_reduce_scan(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
     return from_cuda(launch_scan_sequential(x, gated, ctx->dstatus, wait_ns(ctx), s));
 }
 

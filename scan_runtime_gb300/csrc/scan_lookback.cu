@@ -42,6 +42,102 @@ template <bool GATED>
 __device__ __forceinline__ float4 inj4(float4 a, float4 u) {
     return make_float4(inj<GATED>(a.x, u.x), inj<GATED>(a.y, u.y), inj<GATED>(a.z, u.z), inj<GATED>(a.w, u.w));
 }
+// Local scan of one tile (LB_TC steps x LB_NC channels in shared memory, row
+// major): every thread folds its LB_SEG steps of 4 channels, the warp scans
+// its four segments, and the earlier warps' aggregates are folded in warp
+// order.  Returns this thread's exclusive prefix (EA, EB); wA / wB keep the
+// warps' aggregates.  Contains one __syncthreads.
+template <bool GATED>
+__device__ __forceinline__ void tile_local_scan(const float* sa, const float* sb, int rows, float4 (*wA)[8],
+                                                float4 (*wB)[8], float4& EA, float4& EB) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = lane & 7, sub = lane >> 3;
+    const int seg = warp * 4 + sub;                 // 0..31, rows [seg*LB_SEG, (seg+1)*LB_SEG)
+    // ---- phase 1: fold this thread's LB_SEG steps of its 4 channels
+    float4 A = make_float4(1.f, 1.f, 1.f, 1.f), Bc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < LB_SEG; ++i) {
+        const int r = seg * LB_SEG + i;
+        float4 av = *reinterpret_cast<const float4*>(sa + r * LB_NC + 4 * quad);
+        float4 bv = inj4<GATED>(av, *reinterpret_cast<const float4*>(sb + r * LB_NC + 4 * quad));
+        if (r >= rows) {                         // past T: identity step
+            av = make_float4(1.f, 1.f, 1.f, 1.f);
+            bv = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        Bc = f4fma(av, Bc, bv);
+        A = f4mul(av, A);
+    }
+    // ---- phase 2a: inclusive scan over the warp's 4 segments (same quad)
+#pragma unroll
+    for (int d = 8; d < 32; d <<= 1) {
+        const float4 Ap = f4shfl_up(A, d), Bp = f4shfl_up(Bc, d);
+        if (lane >= d) {
+            Bc = f4fma(A, Bp, Bc);
+            A = f4mul(A, Ap);
+        }
+    }
+    float4 eA = f4shfl_up(A, 8), eB = f4shfl_up(Bc, 8);   // exclusive within the warp
+    if (sub == 0) {
+        eA = make_float4(1.f, 1.f, 1.f, 1.f);
+        eB = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (sub == 3) {
+        wA[warp][quad] = A;
+        wB[warp][quad] = Bc;
+    }
+    __syncthreads();
+    // ---- phase 2b: fold the earlier warps' aggregates in warp order
+    float4 PA = make_float4(1.f, 1.f, 1.f, 1.f), PB = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < warp; ++j) {
+        PB = f4fma(wA[j][quad], PB, wB[j][quad]);
+        PA = f4mul(wA[j][quad], PA);
+    }
+    EB = f4fma(eA, PB, eB);                     // exclusive prefix of this segment
+    EA = f4mul(eA, PA);
+}
+
+// The whole tile's aggregate (A, B) for channel `lane` (warp 0): the warps'
+// aggregates folded in warp order.
+__device__ __forceinline__ void tile_aggregate(const float4 (*wA)[8], const float4 (*wB)[8], int lane, float& CA,
+                                               float& CB) {
+    CA = 1.f;
+    CB = 0.f;
+    const float* pA = reinterpret_cast<const float*>(&wA[0][0]) + lane;
+    const float* pB = reinterpret_cast<const float*>(&wB[0][0]) + lane;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        CB = __fmaf_rn(pA[j * 32], CB, pB[j * 32]);
+        CA = __fmul_rn(pA[j * 32], CA);
+    }
+}
+
+// States of this thread's segment from its exclusive prefix and the tile's
+// incoming carries (carry[]); the tile's last state is the outgoing carry
+// itself (cfin[]), so a split at a multiple of LB_TC continues bit-exactly.
+// `out` points at state (t0, n0) of the tile; rows of N floats.
+template <bool GATED>
+__device__ __forceinline__ void tile_outputs(const float* sa, const float* sb, int rows, const float* carry,
+                                             const float* cfin, float4 EA, float4 EB, float* out, int N,
+                                             bool active) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = lane & 7, sub = lane >> 3;
+    const int seg = warp * 4 + sub;
+    if (!active) return;
+    const float4 cc = *reinterpret_cast<const float4*>(&carry[4 * quad]);
+    float4 s = f4fma(EA, cc, EB);
+    out += 4 * quad;
+#pragma unroll
+    for (int i = 0; i < LB_SEG; ++i) {
+        const int r = seg * LB_SEG + i;
+        if (r < rows) {
+            const float4 av = *reinterpret_cast<const float4*>(sa + r * LB_NC + 4 * quad);
+            const float4 bv = inj4<GATED>(av, *reinterpret_cast<const float4*>(sb + r * LB_NC + 4 * quad));
+            s = f4fma(av, s, bv);
+            if (r == rows - 1) s = *reinterpret_cast<const float4*>(&cfin[4 * quad]);
+            st_cs(reinterpret_cast<float4*>(out + (size_t)r * N), s);
+        }
+    }
+}
 }  // namespace
 
 int64_t lookback_flag_count(int B, int T, int N) {
@@ -147,59 +243,15 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         const float* sa = bufs + buf * 2 * LB_TILE;
         const float* sb = sa + LB_TILE;
 
-        // ---- phase 1: fold this thread's LB_SEG steps of its 4 channels
-        float4 A = make_float4(1.f, 1.f, 1.f, 1.f), Bc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < LB_SEG; ++i) {
-            const int r = seg * LB_SEG + i;
-            float4 av = *reinterpret_cast<const float4*>(sa + r * LB_NC + 4 * quad);
-            float4 bv = inj4<GATED>(av, *reinterpret_cast<const float4*>(sb + r * LB_NC + 4 * quad));
-            if (r >= rows) {                         // past T: identity step
-                av = make_float4(1.f, 1.f, 1.f, 1.f);
-                bv = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            Bc = f4fma(av, Bc, bv);
-            A = f4mul(av, A);
-        }
-        // ---- phase 2a: inclusive scan over the warp's 4 segments (same quad)
-#pragma unroll
-        for (int d = 8; d < 32; d <<= 1) {
-            const float4 Ap = f4shfl_up(A, d), Bp = f4shfl_up(Bc, d);
-            if (lane >= d) {
-                Bc = f4fma(A, Bp, Bc);
-                A = f4mul(A, Ap);
-            }
-        }
-        float4 eA = f4shfl_up(A, 8), eB = f4shfl_up(Bc, 8);   // exclusive within the warp
-        if (sub == 0) {
-            eA = make_float4(1.f, 1.f, 1.f, 1.f);
-            eB = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (sub == 3) {
-            wA[warp][quad] = A;
-            wB[warp][quad] = Bc;
-        }
-        __syncthreads();
-        // ---- phase 2b: fold the earlier warps' aggregates in warp order
-        float4 PA = make_float4(1.f, 1.f, 1.f, 1.f), PB = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < warp; ++j) {
-            PB = f4fma(wA[j][quad], PB, wB[j][quad]);
-            PA = f4mul(wA[j][quad], PA);
-        }
-        const float4 EB = f4fma(eA, PB, eB);        // exclusive prefix of this segment
-        const float4 EA = f4mul(eA, PA);
+        // ---- phases 1 and 2: the tile's local scan
+        float4 EA, EB;
+        tile_local_scan<GATED>(sa, sb, rows, wA, wB, EA, EB);
 
         // ---- phase 3: chunk aggregate and look-back (warp 0, lane = channel)
         if (warp == 0) {
             const int n = n0 + lane;
-            float CA = 1.f, CB = 0.f;
-            const float* pA = reinterpret_cast<const float*>(&wA[0][0]) + lane;
-            const float* pB = reinterpret_cast<const float*>(&wB[0][0]) + lane;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                CB = __fmaf_rn(pA[j * 32], CB, pB[j * 32]);
-                CA = __fmul_rn(pA[j * 32], CA);
-            }
+            float CA, CB;
+            tile_aggregate(wA, wB, lane, CA, CB);
             const int base = bi * p.ncb + cb;
             float cin;
             if (k == 0) {
@@ -286,22 +338,8 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         }
         __syncthreads();
         // ---- phase 4: states of this thread's segment from its exclusive prefix
-        if (p.s_out != nullptr && n0 + 4 * quad < p.N) {
-            const float4 cc = *reinterpret_cast<const float4*>(&carry[4 * quad]);
-            float4 s = f4fma(EA, cc, EB);
-            float* out = p.s_out + ((size_t)bi * p.T + t0) * p.N + n0 + 4 * quad;
-#pragma unroll
-            for (int i = 0; i < LB_SEG; ++i) {
-                const int r = seg * LB_SEG + i;
-                if (r < rows) {
-                    const float4 av = *reinterpret_cast<const float4*>(sa + r * LB_NC + 4 * quad);
-                    const float4 bv = inj4<GATED>(av, *reinterpret_cast<const float4*>(sb + r * LB_NC + 4 * quad));
-                    s = f4fma(av, s, bv);
-                    if (r == rows - 1) s = *reinterpret_cast<const float4*>(&cfin[4 * quad]);
-                    st_cs(reinterpret_cast<float4*>(out + (size_t)r * p.N), s);
-                }
-            }
-        }
+        tile_outputs<GATED>(sa, sb, rows, carry, cfin, EA, EB, p.s_out + ((size_t)bi * p.T + t0) * p.N + n0, p.N,
+                            p.s_out != nullptr && n0 + 4 * quad < p.N);
         __syncthreads();                              // buffer `buf` free for the next prefetch
     }
     // every CTA ends here (also after a copy timeout): the last one records
@@ -318,6 +356,272 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 bool lookback_supported(const ScanArgs& x) { return scan_tma_ok(x); }
+
+// ============================================================ reduce-then-scan
+// For few channel tiles and long T the look-back folds deep: with hundreds of
+// a column's chunks in flight at once, each chunk's carry must be folded
+// forward through hundreds of predecessors' aggregates, one L2 round trip per
+// batch.  This path takes the carries out of the tiles instead:
+//   scan_pass<.., false>  every tile's aggregate (A_k, B_k) per channel;
+//   scan_chain            per column, the carries C_k = fma(A_k, C_{k-1}, B_k)
+//                         over all chunks in order, with the aggregates staged
+//                         through shared memory by bulk copies;
+//   scan_pass<.., true>   every tile's states from its incoming carry.
+// The local scan, the aggregates and the carry chain are the look-back
+// kernel's own operations in the same order, so both paths give the same bits.
+// a and b are read twice (20 bytes per element instead of 12).
+// Workspace: the look-back's A, B and C arrays, indexed [column][chunk][channel].
+namespace {
+
+constexpr int PASS_STAGES = 2;                    // tiles in flight per CTA of the two passes (3 CTAs
+                                                  // per SM; deeper rings with fewer CTAs measured slower)
+constexpr size_t PASS_SMEM = PASS_STAGES * LB_TILE_BYTES + PASS_STAGES * 8 + 16;
+
+struct PassParams {
+    int B, T, N, ncb, nbcb, nchunks, ntiles;
+    const float* s0;
+    float* s_final;
+    float* s_out;
+    float* dA;
+    float* dB;
+    float* dC;
+    SnDevStatus* st;
+    uint64_t wait_ns;
+};
+
+template <bool GATED, bool OUT>
+__global__ void __launch_bounds__(LB_THREADS, 3)
+scan_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const PassParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* bufs = reinterpret_cast<float*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + PASS_STAGES * LB_TILE_BYTES);
+    __shared__ float4 wA[8][8], wB[8][8];
+    __shared__ float carry[LB_NC], cfin[LB_NC];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = lane & 7;
+
+    if (tid == 0) {
+        for (int s = 0; s < PASS_STAGES; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // tiles column-major within a chunk row, as the look-back kernel
+    auto tile_coords = [&](int ti, int& k, int& bi, int& cb) {
+        k = ti / p.nbcb;
+        const int r = ti - k * p.nbcb;
+        bi = r / p.ncb;
+        cb = r - bi * p.ncb;
+    };
+    auto issue = [&](int ti, int buf) {
+        int k, bi, cb;
+        tile_coords(ti, k, bi, cb);
+        mbar_arrive_expect_tx(&full[buf], LB_TILE_BYTES);
+        float* dst = bufs + buf * 2 * LB_TILE;
+        tma_load_3d(dst, &map_a, &full[buf], cb * LB_NC, k * LB_TC, bi);
+        tma_load_3d(dst + LB_TILE, &map_b, &full[buf], cb * LB_NC, k * LB_TC, bi);
+    };
+    int it = 0;
+    if (tid == 0) {
+        for (int s = 0; s < PASS_STAGES - 1; ++s) {
+            const int ti = blockIdx.x + s * gridDim.x;
+            if (ti < p.ntiles) issue(ti, s);
+        }
+    }
+    for (int ti = blockIdx.x; ti < p.ntiles; ti += gridDim.x, ++it) {
+        const int buf = it % PASS_STAGES;
+        const int ahead = ti + (PASS_STAGES - 1) * (int)gridDim.x;
+        if (tid == 0 && ahead < p.ntiles) issue(ahead, (it + PASS_STAGES - 1) % PASS_STAGES);
+        int k, bi, cb;
+        tile_coords(ti, k, bi, cb);
+        const int t0 = k * LB_TC, n0 = cb * LB_NC;
+        const int rows = min(LB_TC, p.T - t0);
+        if (!__syncthreads_and(mbar_wait(&full[buf], (it / PASS_STAGES) & 1, p.wait_ns))) {
+            if (tid == 0) {
+                record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | 3);
+                for (int j = 0; j < PASS_STAGES; ++j)
+                    if (ti + j * (int)gridDim.x < p.ntiles)
+                        (void)mbar_wait(&full[(it + j) % PASS_STAGES], ((it + j) / PASS_STAGES) & 1, p.wait_ns);
+            }
+            return;
+        }
+        const float* sa = bufs + buf * 2 * LB_TILE;
+        const float* sb = sa + LB_TILE;
+        float4 EA, EB;
+        tile_local_scan<GATED>(sa, sb, rows, wA, wB, EA, EB);
+        const size_t col = (size_t)bi * p.ncb + cb;
+        const size_t me = (col * p.nchunks + k) * LB_NC + lane;
+        if (warp == 0) {
+            float CA, CB;
+            tile_aggregate(wA, wB, lane, CA, CB);
+            if (!OUT) {
+                p.dA[me] = CA;
+                p.dB[me] = CB;
+            } else {
+                const int n = n0 + lane;
+                const float cin = k == 0 ? ((p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f)
+                                         : __ldg(p.dC + me - LB_NC);
+                const float Ck = __fmaf_rn(CA, cin, CB);
+                carry[lane] = cin;
+                cfin[lane] = Ck;
+                if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
+            }
+        }
+        if (OUT) {
+            __syncthreads();
+            tile_outputs<GATED>(sa, sb, rows, carry, cfin, EA, EB, p.s_out + ((size_t)bi * p.T + t0) * p.N + n0,
+                                p.N, p.s_out != nullptr && n0 + 4 * quad < p.N);
+        }
+        __syncthreads();                              // buffer `buf` free for the next prefetch
+    }
+}
+
+// One warp per column: C_k = fma(A_k, C_{k-1}, B_k) over the chunks in order,
+// C_{-1} = s0 (lane = channel).  The column's aggregates arrive in blocks of
+// CHAIN_BLK chunks by bulk copies, CHAIN_STAGES blocks in flight.  Within a
+// full block the aggregates of CHAIN_U chunks are read into registers one
+// batch ahead of the FMAs that consume them (two batches in turn, all offsets
+// fixed), so a step costs two shared loads, the FMA and a store, and the
+// dependent chain is not held up by load latency.
+constexpr int CHAIN_BLK = 128;
+constexpr int CHAIN_STAGES = 4;
+constexpr int CHAIN_U = 16;
+constexpr uint32_t CHAIN_BLK_FLOATS = CHAIN_BLK * LB_NC;          // one block of one array
+constexpr size_t CHAIN_SMEM = (size_t)CHAIN_STAGES * 2 * CHAIN_BLK_FLOATS * 4 + CHAIN_STAGES * 8 + 16;
+
+__global__ void __launch_bounds__(32) scan_chain(const PassParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* bufs = reinterpret_cast<float*>(smem);                 // [stage][A | B][CHAIN_BLK][LB_NC]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)CHAIN_STAGES * 2 * CHAIN_BLK_FLOATS * 4);
+    const int lane = threadIdx.x;
+    const size_t col = blockIdx.x;
+    const int bi = (int)(col / p.ncb), cb = (int)(col % p.ncb);
+    const int n = cb * LB_NC + lane;
+    const size_t colbase = col * p.nchunks * LB_NC;
+    const int nblk = (p.nchunks + CHAIN_BLK - 1) / CHAIN_BLK;
+    auto issue = [&](int blk) {   // lane 0
+        const int c0 = blk * CHAIN_BLK, st = blk % CHAIN_STAGES;
+        const uint32_t bytes = (uint32_t)min(CHAIN_BLK, p.nchunks - c0) * LB_NC * 4;
+        mbar_arrive_expect_tx(&bar[st], 2 * bytes);
+        bulk_load(bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS, p.dA + colbase + (size_t)c0 * LB_NC, bytes, &bar[st]);
+        bulk_load(bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS + CHAIN_BLK_FLOATS, p.dB + colbase + (size_t)c0 * LB_NC,
+                  bytes, &bar[st]);
+    };
+    int issued = 0;
+    if (lane == 0) {
+        for (int st = 0; st < CHAIN_STAGES; ++st) mbar_init(&bar[st], 1);
+        fence_mbar_init();
+        for (; issued < min(nblk, CHAIN_STAGES); ++issued) issue(issued);
+    }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    float c = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
+    bool ok = true;
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int st = blk % CHAIN_STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[st], (uint32_t)(blk / CHAIN_STAGES) & 1, p.wait_ns));
+        if (!ok) break;
+        const float* sA = bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS + lane;
+        const float* sB = sA + CHAIN_BLK_FLOATS;
+        float* dC = p.dC + colbase + (size_t)blk * CHAIN_BLK * LB_NC + lane;
+        const int cnt = min(CHAIN_BLK, p.nchunks - blk * CHAIN_BLK);
+        if (cnt == CHAIN_BLK) {
+            // a full block: two register batches in turn, every offset fixed
+            float a0[CHAIN_U], b0[CHAIN_U], a1[CHAIN_U], b1[CHAIN_U];
+#pragma unroll
+            for (int u = 0; u < CHAIN_U; ++u) {
+                a0[u] = sA[u * LB_NC];
+                b0[u] = sB[u * LB_NC];
+            }
+#pragma unroll
+            for (int i0 = 0; i0 < CHAIN_BLK; i0 += 2 * CHAIN_U) {
+#pragma unroll
+                for (int u = 0; u < CHAIN_U; ++u) {
+                    a1[u] = sA[(i0 + CHAIN_U + u) * LB_NC];
+                    b1[u] = sB[(i0 + CHAIN_U + u) * LB_NC];
+                }
+#pragma unroll
+                for (int u = 0; u < CHAIN_U; ++u) {
+                    c = __fmaf_rn(a0[u], c, b0[u]);
+                    dC[(i0 + u) * LB_NC] = c;
+                }
+                if (i0 + 2 * CHAIN_U < CHAIN_BLK) {
+#pragma unroll
+                    for (int u = 0; u < CHAIN_U; ++u) {
+                        a0[u] = sA[(i0 + 2 * CHAIN_U + u) * LB_NC];
+                        b0[u] = sB[(i0 + 2 * CHAIN_U + u) * LB_NC];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < CHAIN_U; ++u) {
+                    c = __fmaf_rn(a1[u], c, b1[u]);
+                    dC[(i0 + CHAIN_U + u) * LB_NC] = c;
+                }
+            }
+        } else {
+            for (int i = 0; i < cnt; ++i) {   // the last, partial block
+                c = __fmaf_rn(sA[i * LB_NC], c, sB[i * LB_NC]);
+                dC[(size_t)i * LB_NC] = c;
+            }
+        }
+        __syncwarp();                                 // the stage is read
+        if (lane == 0 && issued < nblk) issue(issued);
+        if (issued < nblk) ++issued;
+    }
+    if (!ok && lane == 0) {
+        record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | 4);
+        // let this warp's loads still in flight land: the last CHAIN_STAGES issued
+        for (int blk = max(0, issued - CHAIN_STAGES); blk < issued; ++blk)
+            (void)mbar_wait(&bar[blk % CHAIN_STAGES], (uint32_t)(blk / CHAIN_STAGES) & 1, p.wait_ns);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
+                                    int sm_count, cudaStream_t stream) {
+    CUtensorMap ma, mb;
+    if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, LB_NC, LB_TC) ||
+        !make_scan_map(&mb, x.b, x.B, x.T, x.N, LB_NC, LB_TC))
+        return cudaErrorInvalidValue;
+    PassParams p;
+    p.B = x.B;
+    p.T = x.T;
+    p.N = x.N;
+    p.ncb = (x.N + LB_NC - 1) / LB_NC;
+    p.nbcb = x.B * p.ncb;
+    p.nchunks = (x.T + LB_TC - 1) / LB_TC;
+    p.ntiles = p.nbcb * p.nchunks;
+    p.s0 = x.s0;
+    p.s_final = x.s_final;
+    p.s_out = x.s_out;
+    const int64_t tiles = p.ntiles;
+    const int64_t flag_bytes = ((tiles * 4 + 255) / 256) * 256;
+    p.dA = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + flag_bytes);
+    p.dB = p.dA + tiles * LB_NC;
+    p.dC = p.dB + tiles * LB_NC;
+    p.st = st;
+    p.wait_ns = wait_ns;
+
+    auto k_agg = gated ? scan_pass<true, false> : scan_pass<false, false>;
+    auto k_out = gated ? scan_pass<true, true> : scan_pass<false, true>;
+    int occ = 0;
+    cudaError_t e = occupancy_once((const void*)k_agg, LB_THREADS, PASS_SMEM, &occ);
+    if (e != cudaSuccess) return e;
+    e = occupancy_once((const void*)k_out, LB_THREADS, PASS_SMEM, &occ);
+    if (e != cudaSuccess) return e;
+    e = set_smem_attr_once((const void*)scan_chain, CHAIN_SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(tiles, (int64_t)occ * sm_count);
+    k_agg<<<grid, LB_THREADS, PASS_SMEM, stream>>>(ma, mb, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    scan_chain<<<(unsigned)p.nbcb, 32, CHAIN_SMEM, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_out<<<grid, LB_THREADS, PASS_SMEM, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+
 
 cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,
                                  uint64_t wait_ns, int sm_count, cudaStream_t stream) {

@@ -103,6 +103,10 @@ cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* s
                                    cudaStream_t stream);
 cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,
                                  uint64_t wait_ns, int sm_count, cudaStream_t stream);
+// Reduce-then-scan (scan_lookback.cu): the look-back kernel's results in three
+// launches without flags, for few channel tiles and long T; same workspace.
+cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
+                                    int sm_count, cudaStream_t stream);
 
 enum RecurKind : int {
     RK_DIAG_KEY = 0,

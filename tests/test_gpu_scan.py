@@ -226,6 +226,47 @@ def test_lookback_bounded_wait_reports_timeout(sr, lbctx):
     assert _nrel(so, r64) <= TOL
 
 
+@pytest.mark.parametrize("form", ["fma", "gated"])
+@pytest.mark.parametrize("shape", [(1, 4096, 32), (2, 1000, 64), (3, 257, 96), (2, 5, 8), (1, 70000, 64),
+                                   (1, 40000, 36)])
+def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
+    """The reduce-then-scan path runs the look-back kernel's local scans,
+    aggregates and carry chain in the same order, so its results equal the
+    look-back's bit for bit; T = 70000 and 40000 span several blocks of the
+    carry chain, N = 36 a ragged channel tile."""
+    B, T, N = shape
+    ctx.ensure_workspace(B, T, N)
+    a, b, u, s0 = _inputs(B, T, N, 40 + T % 11)
+    rhs = b if form == "fma" else u
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+    lo, lf = _run(ctx, form, a, rhs, s0)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    ro, rf = _run(ctx, form, a, rhs, s0)
+    ro0, rf0 = _run(ctx, form, a, rhs, None)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    assert np.array_equal(ro, lo) and np.array_equal(rf, lf)
+    r64, f64 = _ref(form, a, rhs, s0, "f64")
+    assert _nrel(ro, r64) <= TOL and _nrel(rf, f64) <= TOL
+    z64, zf64 = _ref(form, a, rhs, None, "f64")
+    assert _nrel(ro0, z64) <= TOL and _nrel(rf0, zf64) <= TOL
+
+
+def test_reduce_scan_optional_outputs_and_split(sr, ctx):
+    tc = ctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK)
+    B, T, N = 2, 300 * tc + 9, 64
+    split = 140 * tc
+    ctx.ensure_workspace(B, T, N)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    a, b, _, s0 = _inputs(B, T, N, 41)
+    full, ffull = _run(ctx, "fma", a, b, s0)
+    none_out, f_only = _run(ctx, "fma", a, b, s0, s_out=False)
+    p1, f1 = _run(ctx, "fma", a[:, :split].contiguous(), b[:, :split].contiguous(), s0)
+    p2, f2 = _run(ctx, "fma", a[:, split:].contiguous(), b[:, split:].contiguous(), torch.from_numpy(f1))
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    assert none_out is None and np.array_equal(f_only, ffull)
+    assert np.array_equal(np.concatenate([p1, p2], 1), full) and np.array_equal(f2, ffull)
+
+
 def test_lookback_forced_without_workspace_is_nomem(sr, ctx):
     ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
     a = torch.zeros(1, 512, 32, device="cuda")
