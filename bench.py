@@ -349,7 +349,22 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
         few["auto_picks"] = "reduce_scan"
         out["scan_fma_few_channels"] = few
-        del xf, af, bf, s0f, sof, sff
+        # and its reverse scan (read a, s, ds; write da, db): sequential against chunked
+        sr.sn_scan_fma(ctx.handle, Bf, Tf, Nf, af, bf, s0f, sff, sof, s)
+        gsf = torch.empty_like(af).normal_(generator=torch.Generator(dev).manual_seed(78))
+        daf, dbf, d0f = torch.empty_like(af), torch.empty_like(af), torch.empty_like(s0f)
+        nbb = 20 * Bf * Tf * Nf + 8 * Bf * Nf
+        fewb = {"workload": f"B={Bf} T={Tf} N={Nf}", "bytes_per_call": nbb}
+        for label, kern in (("chunked", sr.SN_SCAN_KERNEL_REDUCE_SCAN), ("sequential", sr.SN_SCAN_KERNEL_SEQUENTIAL)):
+            ctx.set_option(sr.SN_OPT_SCAN_KERNEL, kern)
+            ms = time_form(torch, lambda: sr.sn_scan_fma_backward(ctx.handle, Bf, Tf, Nf, af, s0f, sof, gsf, None,
+                                                                   daf, dbf, d0f, s), warmup, reps, s)
+            fewb[label] = {"ms": round(ms, 4), "GBps": round(nbb / ms / 1e6, 1),
+                           "hbm_frac": round(nbb / ms / 1e6 / hbm_peak, 3)}
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+        fewb["auto_picks"] = "chunked"
+        out["scan_fma_backward_few_channels"] = fewb
+        del xf, af, bf, s0f, sof, sff, gsf, daf, dbf, d0f
         # reverse scans (backward pass) on the same workload: read a, s, ds (+u),
         # write da, db|du
         gs_ = torch.empty((B, T, N), device=dev).normal_(generator=torch.Generator(dev).manual_seed(77))

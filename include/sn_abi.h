@@ -209,8 +209,15 @@ sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
  *   a, s (forward states s_out), grad_s : (B, T, N), required
  *   s0, grad_final : (B, N), NULL = zeros
  *   grad_a, grad_b : (B, T, N), grad_s0 : (B, N), each may be NULL (not written)
- * Runs T backwards per channel; N % 4 == 0 with 16-byte aligned tensors uses
- * TMA, anything else plain loads.  Errors: SN_E_INVAL, SN_E_DEVICE. */
+ * Runs T backwards per channel (the fp32 definition's bits); N % 4 == 0 with
+ * 16-byte aligned tensors uses TMA, anything else plain loads.  For few
+ * channels and long T, with a context workspace of sn_workspace_bytes() bytes
+ * set, the call instead chunks T (per-chunk reverse aggregates, a carry chain,
+ * then the gradients): chosen automatically there, forced by either chunked
+ * SN_OPT_SCAN_KERNEL value (then SN_E_NOMEM without the workspace, and
+ * SN_E_UNSUPPORTED unless N % 4 == 0 and every tensor is 16-byte aligned).  It
+ * rounds in a different order (within 1e-5 of the definition, deterministic)
+ * and overwrites the workspace.  Errors: SN_E_INVAL, SN_E_DEVICE, and those. */
 sn_status sn_scan_fma_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
                                const float* a, const float* s0, const float* s,
                                const float* grad_s, const float* grad_final,

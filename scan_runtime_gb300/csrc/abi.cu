@@ -366,9 +366,29 @@ static sn_status scan_backward_common(SnCtx* ctx, BwdArgs& x, bool gated, void* 
                          {x.s, big, false}, {x.gs, big, false},  {x.gf, small, false},
                          {x.da, big, true}, {x.dbu, big, true},  {x.ds0, small, true}};
     if (any_bad_overlap(bufs, 9, nullptr, nullptr)) return SN_E_INVAL;
+    // kernel: the sequential reverse scan, or for few channels and long T the
+    // chunked one (SN_OPT_SCAN_KERNEL: either chunked value forces it)
+    const int64_t need = scan_backward_chunked_ws_bytes(x.B, x.T, x.N);
+    bool chunked;
+    if (ctx->scan_kernel == SN_SCAN_KERNEL_LOOKBACK || ctx->scan_kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
+        if (!scan_backward_chunked_supported(x)) return SN_E_UNSUPPORTED;
+        if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
+        chunked = true;
+    } else if (ctx->scan_kernel == SN_SCAN_KERNEL_AUTO) {
+        const int64_t seq_ctas = (int64_t)x.B * ((x.N + 31) / 32);
+        chunked = seq_ctas < 2 * ctx->sm_count && x.T >= 8 * LB_TC && scan_backward_chunked_supported(x) &&
+                  ctx->ws != nullptr && ctx->ws_bytes >= need;
+    } else {
+        chunked = false;
+    }
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
-    return from_cuda(launch_scan_backward(x, gated, ctx->dstatus, wait_ns(ctx), reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (chunked) {
+        ctx->ws_dirty = true;   // the carries overwrite the look-back flag area
+        return from_cuda(launch_scan_backward_chunked(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+    }
+    return from_cuda(launch_scan_backward(x, gated, ctx->dstatus, wait_ns(ctx), s));
 }
 
 sn_status sn_scan_fma_backward(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float* a, const float* s0,

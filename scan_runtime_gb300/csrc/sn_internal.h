@@ -99,6 +99,13 @@ struct BwdArgs {
 // Launchers (return a CUDA error code; validation happens before).
 cudaError_t launch_scan_backward(const BwdArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
                                  cudaStream_t stream);
+// Chunked reverse scans (scan_bwd_chunked.cu), for few channels and long T:
+// 16-byte aligned tensors with N % 4 == 0; workspace bytes (at the start of
+// the context workspace, which the look-back scan's sizes cover).
+bool scan_backward_chunked_supported(const BwdArgs& x);
+int64_t scan_backward_chunked_ws_bytes(int B, int T, int N);
+cudaError_t launch_scan_backward_chunked(const BwdArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
+                                         int sm_count, cudaStream_t stream);
 cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
                                    cudaStream_t stream);
 cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,

@@ -129,3 +129,49 @@ def test_full_size_backward_sampled(ctx, form):
         assert np.array_equal(ga[bi, :, n].cpu().numpy(), r32[0][0, :, 0])
         assert np.array_equal(gb[bi, :, n].cpu().numpy(), r32[1][0, :, 0])
         assert g0[bi, n].item() == r32[2][0, 0]
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
+@pytest.mark.parametrize("shape", [(1, 4096, 32), (2, 1000, 64), (1, 40000, 36), (3, 257, 96), (2, 5, 8)])
+@pytest.mark.parametrize("opts", [(True, True), (False, False)])
+def test_chunked_backward_within_tolerance(sr, ctx, form, shape, opts):
+    """The chunked reverse scan (few channels, long T): per-tile reverse
+    aggregates, a carry chain from the last chunk down, then the gradients.
+    Its rounding order differs from the sequential kernel's, so it is held to
+    the fp64 definition's tolerance, and two runs must agree bit for bit.
+    T = 40000 spans several blocks of the carry chain and a ragged last chunk;
+    T = 5 a single partial chunk."""
+    B, T, N = shape
+    x, s0, gs, gf = _case(B, T, N, 17 + T % 13, *opts)
+    s = _forward32(form, x, s0)
+    ctx.ensure_workspace(B, T, N)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    first = _run(ctx, form, x, s, s0, gs, gf)
+    second = _run(ctx, form, x, s, s0, gs, gf)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    u = x["u"].numpy() if form == "gated" else None
+    r64 = oracle.scan_backward(form, x["a"].numpy(), s.numpy().astype(np.float64),
+                               None if s0 is None else s0.numpy().astype(np.float64), gs.numpy(),
+                               None if gf is None else gf.numpy(), u=u)
+    for got, again, e64 in zip(first, second, r64):
+        assert np.array_equal(got, again)
+        assert _nrel(got, e64) <= TOL
+
+
+def test_chunked_backward_optional_outputs_and_auto(sr, ctx):
+    """grad_a, grad_b and grad_s0 may each be NULL; with a workspace set and few
+    channels the automatic choice takes the chunked path (same bits as forcing it)."""
+    B, T, N = 1, 3000, 32
+    x, s0, gs, gf = _case(B, T, N, 23)
+    s = _forward32("fma", x, s0)
+    ctx.ensure_workspace(B, T, N)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    ga, gb, g0 = _run(ctx, "fma", x, s, s0, gs, gf)
+    a, sd, gsd, s0d, gfd = (t.cuda() for t in (x["a"], s, gs, s0, gf))
+    only_b = torch.full((B, T, N), 7.0, device="cuda")
+    assert sr.sn_scan_fma_backward(ctx.handle, B, T, N, a, s0d, sd, gsd, gfd, None, only_b, None) == sr.SN_OK
+    torch.cuda.synchronize()
+    assert np.array_equal(only_b.cpu().numpy(), gb)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    ga2, gb2, g02 = _run(ctx, "fma", x, s, s0, gs, gf)
+    assert np.array_equal(ga2, ga) and np.array_equal(gb2, gb) and np.array_equal(g02, g0)
