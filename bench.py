@@ -451,6 +451,32 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                         "tolerance": 2e-3}
                 assert ctx.last_error() == sr.SN_OK
             del x, o, S
+        # single-step decode of the other kinds (column decode kernel), B=1024 T=1,
+        # random states: each step reads and writes every state once
+        for name, maker, (Bc, H, G, dk, dv) in (
+                ("gla_decode", lambda c: synth.gla_inputs(1024, 1, 4, 128, 128, cid=c, device=dev), (1024, 4, 4, 128, 128)),
+                ("mamba2_decode", lambda c: synth.mamba2_inputs(1024, 1, 24, 1, 128, 64, cid=c, device=dev),
+                 (1024, 24, 1, 128, 64)),
+                ("deltanet_decode", lambda c: synth.deltanet_inputs(1024, 1, 8, 128, 128, cid=c, device=dev),
+                 (1024, 8, 8, 128, 128))):
+            x = maker(97)
+            S = torch.empty((Bc, H, dk, dv), device=dev).normal_(generator=torch.Generator(dev).manual_seed(98))
+            o = torch.empty((Bc, 1, H, dv), device=dev)
+            if name == "deltanet_decode":
+                fn = lambda: sr.sn_recur_delta(ctx.handle, Bc, 1, H, dk, dv, x["scale"], x["q"], x["k"], x["v"],
+                                               x["beta"], S, S, o, s)
+                gbytes = x["beta"].numel() * 4
+            else:
+                fn = lambda: sr.sn_recur_diag(ctx.handle, Bc, 1, H, G, dk, dv, x["decay_kind"], x["scale"], x["q"],
+                                              x["k"], x["v"], x["d"], S, S, o, s)
+                gbytes = x["d"].numel() * 4
+            nb = 2 * S.numel() * 4 + (x["q"].numel() + x["k"].numel() + x["v"].numel() + o.numel()) * 4 + gbytes
+            ms = time_form(torch, fn, warmup, reps, s)   # in place: the states (>= 268 MB) exceed L2
+            out[name] = {"ms": round(ms, 4), "tok_heads_per_s": round(Bc * H / ms * 1e3, 1),
+                         "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
+                         "bound": "hbm", "workload": f"B={Bc} T=1 H={H} dk={dk} dv={dv}"}
+            assert ctx.last_error() == sr.SN_OK
+            del x, S, o
         # readout epilogues on the GLA and Mamba-2 output shapes (12 B per element);
         # L2 is flushed before each timed launch (the GLA tensors fit in it)
         flush = torch.empty(64 << 20, device=dev)          # 256 MB

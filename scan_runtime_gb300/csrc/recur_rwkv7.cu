@@ -123,12 +123,12 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
 }  // namespace
 
 bool recur_decode_supported(const RecurArgs& x) {
-    return x.kind == RK_RWKV7 && x.T == 1 && x.dk == DEC_D && x.dv == DEC_D;
+    return (x.kind == RK_RWKV7 && x.T == 1 && x.dk == DEC_D && x.dv == DEC_D) || recur_decode_cols_supported(x);
 }
 
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream) {
-    (void)sm_count;
+    if (x.kind != RK_RWKV7) return launch_recur_decode_cols(x, sm_count, stream);   // recur_decode.cu
     cudaError_t e = set_smem_attr_once((const void*)recur_decode_rwkv7, DEC_SMEM);
     if (e != cudaSuccess) return e;
     const int BH = x.B * x.H;

@@ -143,6 +143,9 @@ cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t 
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);
+// recur_decode.cu: T == 1 of the diagonal-decay kinds and the delta rule
+bool recur_decode_cols_supported(const RecurArgs& x);
+cudaError_t launch_recur_decode_cols(const RecurArgs& x, int sm_count, cudaStream_t stream);
 
 // Chunked tensor-core form of the delta rule (recur_delta_chunked.cu).
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv);

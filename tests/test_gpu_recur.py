@@ -285,6 +285,50 @@ def test_decode_matches_sequence_kernel_at_t1(sr, ctx):
     assert _nrel(o1, ro) <= TOL and _nrel(o2, ro) <= TOL and _nrel(S2, rS) <= TOL
 
 
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "gated_key", "gated_head"])
+@pytest.mark.parametrize("dims", [(128, 128), (128, 64), (64, 64)])
+def test_column_decode_matches_sequence_kernel_bit_for_bit(sr, ctx, kind, dims):
+    """T = 1 of the diagonal kinds and the delta rule runs the column decode
+    kernel, which sums in the sequence kernel's 8-rows-per-lane order; at this
+    batch the sequence kernel runs 8 rows per lane too, so a forced one-step
+    sequence call must give the same bits for o and the state."""
+    dk, dv = dims
+    B, H = 64, 4
+    x = make(kind, B, 1, H, dk, dv, G=2 if kind == "mamba2" else None, seed=11)
+    S0 = synth.normal(state_shape(kind, B, H, dk, dv), 5300) * 0.5
+    run, ref = RUN[kind]
+    o1, S1 = run(ctx, x, S0)
+    ctx.set_option(sr.SN_OPT_RECUR_KERNEL, 1)
+    o2, S2 = run(ctx, x, S0)
+    ctx.set_option(sr.SN_OPT_RECUR_KERNEL, 0)
+    assert np.array_equal(S1, S2) and np.array_equal(o1, o2)
+    ro, rS = ref(x, S0)
+    assert _nrel(o1, ro) <= TOL and _nrel(S1, rS) <= TOL
+
+
+@pytest.mark.parametrize("kind", ["gla", "delta", "gated_head"])
+def test_column_decode_in_place_and_optional_outputs(ctx, kind):
+    B, H, dk, dv = 5, 3, 128, 128
+    x = make(kind, B, 1, H, dk, dv, seed=12)
+    S0 = synth.normal(state_shape(kind, B, H, dk, dv), 5400) * 0.5
+    run, ref = RUN[kind]
+    o, S = run(ctx, x, S0)
+    st = S0.cuda()
+    names = ("q", "k", "v", "d") if kind != "delta" else ("q", "k", "v", "beta")
+    args = [cu(x[n]) for n in names]
+    if kind == "delta":
+        o2, _ = ctx.recur_delta(*args, st, scale=x["scale"], S_out=st)
+    else:
+        o2, _ = ctx.recur_diag(*args, st, H=x["H"], G=x["G"], decay_kind=x["decay_kind"], scale=x["scale"], S_out=st)
+    torch.cuda.synchronize()
+    assert np.array_equal(st.cpu().numpy(), S) and np.array_equal(o2.cpu().numpy(), o)
+    o3, S3 = run(ctx, x, S0, o=False)
+    assert o3 is None and np.array_equal(S3, S)
+    o4, S4 = run(ctx, x, None)
+    ro4, rS4 = ref(x, None)
+    assert _nrel(o4, ro4) <= TOL and _nrel(S4, rS4) <= TOL
+
+
 # ------------------------------------------------------------------ validation
 def test_invalid_arguments(sr, ctx):
     h = ctx.handle
