@@ -432,7 +432,7 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                         "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "latency",
                         "tolerance": 2e-3}
                 assert ctx.last_error() == sr.SN_OK
-            if name in ("gla", "mamba2"):
+            if name in ("gla", "mamba2", "gated_memory"):
                 # the chunked tensor-core form of the same workload (tf32 operands)
                 ctx.ensure_workspace_bytes(sr.sn_recur_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
                 fc = lambda: sr.sn_recur_diag_chunked(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"],

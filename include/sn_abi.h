@@ -283,9 +283,10 @@ sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
                          const float* w, const float* S_in, float* S_out,
                          float* o, void* stream);
 
-/* Chunked tensor-core form of sn_recur_diag for the two plain decay layouts
- * (SN_DECAY_PER_KEY, SN_DECAY_PER_HEAD): the same recurrence and readout,
- * evaluated T-parallel in chunks of 128 tokens.  The state is carried from
+/* Chunked tensor-core form of sn_recur_diag for all four decay layouts: the
+ * same recurrence and readout, evaluated T-parallel in chunks of 128 tokens
+ * (the gated layouts are the same recurrence with every key weighted by
+ * 1 - d, [P2] §8).  The state is carried from
  * chunk to chunk ([P2] §8 keeps the association memory "chunk-scannable";
  * [P1] §4.3 GLA, §4.1 Mamba-2), and inside a chunk
  *     S_{n+1} = diag(D_n) S_n + sum_j diag(D_n / D_j) k_j v_j^T
@@ -300,8 +301,7 @@ sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
  * sequence kernel of sn_recur_diag is exact fp32 per step); results do not
  * depend on timing, but a segment split changes the chunk grid and so the
  * rounding.
- * Requirements: decay_kind SN_DECAY_PER_KEY or SN_DECAY_PER_HEAD, dk == 128,
- * dv in {64, 128} (else SN_E_UNSUPPORTED); 16-byte aligned pointers; a
+ * Requirements: dk == 128, dv in {64, 128} (else SN_E_UNSUPPORTED); 16-byte aligned pointers; a
  * context workspace of at least sn_recur_chunked_workspace_bytes() bytes
  * (else SN_E_NOMEM), which the call overwrites (a later look-back scan on the
  * same context clears its flag area again).  Decays must be positive; with

@@ -486,8 +486,8 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
     switch (decay_kind) {
         case SN_DECAY_PER_KEY: x.kind = RK_DIAG_KEY; break;
         case SN_DECAY_PER_HEAD: x.kind = RK_DIAG_HEAD; break;
-        case SN_DECAY_PER_KEY_GATED:
-        case SN_DECAY_PER_HEAD_GATED: return SN_E_UNSUPPORTED;
+        case SN_DECAY_PER_KEY_GATED: x.kind = RK_DIAG_KEY_GATED; break;
+        case SN_DECAY_PER_HEAD_GATED: x.kind = RK_DIAG_HEAD_GATED; break;
         default: return SN_E_INVAL;
     }
     x.B = B; x.T = T; x.H = H; x.G = G; x.dk = dk; x.dv = dv; x.scale = scale;

@@ -39,6 +39,7 @@ struct ChunkArgs {
     SnDevStatus* st;
     uint64_t wait_ns;
     int n0, nsg;       // the output kernel alone: chunks [n0, n0 + nsg) (nsg = 0: all NC chunks)
+    int gated;         // gated injection: key i of token t enters weighted by 1 - d (per key or per head)
 };
 
 // sites recorded with SN_E_TIMEOUT / SN_E_RANGE

@@ -63,7 +63,8 @@ struct StateSmem {
     static constexpr int v_off = d_off + (PER_KEY ? OPF : 0);         // v^T: rows c, K = t
     static constexpr int tot_off = v_off + DV * CH;                   // [2][DKC] half sums
     static constexpr int mu_off = tot_off + 2 * DKC;                  // [CH] suffix sums (per head)
-    static constexpr int misc_off = mu_off + CH;                      // total, barrier, tmem slot
+    static constexpr int om_off = mu_off + CH;                        // [CH] injection weights (per head)
+    static constexpr int misc_off = om_off + CH;                      // total, barrier, tmem slot
     static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
 };
 
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     float* Vs = base + L::v_off;
     float* tot = base + L::tot_off;
     float* mu = base + L::mu_off;
+    float* om = base + L::om_off;
     float* total_s = base + L::misc_off;
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
@@ -103,7 +105,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * lane + r;
-            lg[r] = (t < c.nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + c.h)) : 0.f;
+            const float dt = (t < c.nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + c.h) : 1.f;
+            lg[r] = (t < c.nval && a.d != nullptr) ? lg2(dt) : 0.f;
+            om[t] = a.gated ? 1.f - dt : 1.f;
             s += lg[r];
         }
         float x = s;
@@ -141,6 +145,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
             const float4 lg = make_float4(tb + 0 < c.nval ? lg2(dd.x) : 0.f, tb + 1 < c.nval ? lg2(dd.y) : 0.f,
                                           tb + 2 < c.nval ? lg2(dd.z) : 0.f, tb + 3 < c.nval ? lg2(dd.w) : 0.f);
             st4(Ds + o, lg);
+            if (a.gated) {   // the injection k_i v_j enters with weight 1 - d_i
+                const float4 kk = ld4(Ks + o);
+                st4(Ks + o, make_float4(kk.x * (1.f - dd.x), kk.y * (1.f - dd.y), kk.z * (1.f - dd.z),
+                                        kk.w * (1.f - dd.w)));
+            }
             sum += (lg.x + lg.y) + (lg.z + lg.w);
         }
         tot[half * DKC + i] = sum;
@@ -169,8 +178,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
             const int tb = tbeg + 4 * t4;
             const int o = off128(i, tb);
             const float4 kk = ld4(Ks + o);
-            st4(Ks + o, tf32x4(kk.x * ex2(mu[tb]), kk.y * ex2(mu[tb + 1]), kk.z * ex2(mu[tb + 2]),
-                               kk.w * ex2(mu[tb + 3])));
+            st4(Ks + o, tf32x4(kk.x * ex2(mu[tb]) * om[tb], kk.y * ex2(mu[tb + 1]) * om[tb + 1],
+                               kk.z * ex2(mu[tb + 2]) * om[tb + 2], kk.w * ex2(mu[tb + 3]) * om[tb + 3]));
         }
         gam = ex2(total);
         anc = 1.f;
@@ -230,7 +239,8 @@ struct StateHeadsSmem {
     static constexpr int k_off = 0;                  // k^T (rows key, K = t), tf32
     static constexpr int v_off = OPF;                // the head's v^T (rows value, K = t), scaled, tf32
     static constexpr int mu_off = v_off + DV * CH;   // [CH] suffix sums of log2 d of the head
-    static constexpr int misc_off = mu_off + CH;     // total, barrier, tmem slot
+    static constexpr int om_off = mu_off + CH;       // [CH] injection weights of the head
+    static constexpr int misc_off = om_off + CH;     // total, barrier, tmem slot
     static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
 };
 
@@ -242,6 +252,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, in
     float* Ks = base + L::k_off;
     float* Vs = base + L::v_off;
     float* mu = base + L::mu_off;
+    float* om = base + L::om_off;
     float* total_s = base + L::misc_off;
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
@@ -281,7 +292,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, in
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * lane + r;
-                lg[r] = (t < nval && a.d != nullptr) ? lg2(__ldg(a.d + (row0 + t) * a.H + h)) : 0.f;
+                const float dt = (t < nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + h) : 1.f;
+                lg[r] = (t < nval && a.d != nullptr) ? lg2(dt) : 0.f;
+                om[t] = a.gated ? 1.f - dt : 1.f;
                 sm += lg[r];
             }
             float x = sm;
@@ -307,8 +320,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, in
         for (int f = tid; f < DV * CH / 4; f += NT) {
             const int tq = ((4 * f) >> 5 & 31) * 4;
             const float4 x = ld4(Vs + 4 * f);
-            st4(Vs + 4 * f, tf32x4(x.x * ex2(mu[tq]), x.y * ex2(mu[tq + 1]), x.z * ex2(mu[tq + 2]),
-                                   x.w * ex2(mu[tq + 3])));
+            st4(Vs + 4 * f, tf32x4(x.x * ex2(mu[tq]) * om[tq], x.y * ex2(mu[tq + 1]) * om[tq + 1],
+                                   x.z * ex2(mu[tq + 2]) * om[tq + 2], x.w * ex2(mu[tq + 3]) * om[tq + 3]));
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
@@ -412,7 +425,8 @@ struct OutSmem {
     static constexpr int k_off = OPF;            // Kt, later v^T
     static constexpr int s_off = 2 * OPF;        // S'^T (rows c, K = i)
     static constexpr int lam_off = s_off + DV * DKC;   // [CH] per-head lam
-    static constexpr int misc_off = lam_off + CH;
+    static constexpr int om_off = lam_off + CH;        // [CH] per-head injection weights
+    static constexpr int misc_off = om_off + CH;
     static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 1024;
 };
 
@@ -426,6 +440,7 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     float* bufK = base + L::k_off;
     float* bufS = base + L::s_off;
     float* lam_s = base + L::lam_off;
+    float* om_s = base + L::om_off;
     uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);       // S' tiles, one per unit
     uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);   // products, two per unit
     uint64_t* barV = reinterpret_cast<uint64_t*>(base + L::misc_off + 4);   // v^T tiles, one per unit
@@ -567,6 +582,7 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 lg[r] = lg2(lgh[r]);
+                om_s[4 * lane + r] = a.gated ? 1.f - lgh[r] : 1.f;
                 sm += lg[r];
             }
             float x = sm;
@@ -598,13 +614,18 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             const float4 q4 = ld4(bufQ + o), k4 = ld4(bufK + o);
             if (PER_KEY) {
                 const float4 x = lam[tb];
+                // gated: the key enters with weight 1 - d (the raw decays are still in draw)
+                const float4 w = a.gated ? make_float4(1.f - draw[tb].x, 1.f - draw[tb].y, 1.f - draw[tb].z,
+                                                       1.f - draw[tb].w)
+                                         : make_float4(1.f, 1.f, 1.f, 1.f);
                 st4(bufQ + o, tf32x4(q4.x * ex2(x.x - lm.x), q4.y * ex2(x.y - lm.y), q4.z * ex2(x.z - lm.z),
                                      q4.w * ex2(x.w - lm.w)));
-                st4(bufK + o, tf32x4(k4.x * ex2(lm.x - x.x), k4.y * ex2(lm.y - x.y), k4.z * ex2(lm.z - x.z),
-                                     k4.w * ex2(lm.w - x.w)));
+                st4(bufK + o, tf32x4(k4.x * ex2(lm.x - x.x) * w.x, k4.y * ex2(lm.y - x.y) * w.y,
+                                     k4.z * ex2(lm.z - x.z) * w.z, k4.w * ex2(lm.w - x.w) * w.w));
             } else {
+                const float w = om_s[8 * tb + tl];
                 st4(bufQ + o, tf32x4(q4));
-                st4(bufK + o, tf32x4(k4));
+                st4(bufK + o, tf32x4(k4.x * w, k4.y * w, k4.z * w, k4.w * w));
             }
         }
 
@@ -733,7 +754,8 @@ struct HeadsSmem {
     static constexpr int s_off = 2 * OPF;            // S'^T of the current head
     static constexpr int v_off = s_off + DV * DKC;   // v^T of the current head
     static constexpr int lam_off = v_off + DV * CH;  // [2][CH] decay prefix sums (two heads)
-    static constexpr int misc_off = lam_off + 2 * CH;
+    static constexpr int om_off = lam_off + 2 * CH;  // [2][CH] injection weights (two heads)
+    static constexpr int misc_off = om_off + 2 * CH;
     static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
 };
 
@@ -747,6 +769,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     float* bufS = base + L::s_off;
     float* bufV = base + L::v_off;
     float* lam2 = base + L::lam_off;
+    float* om2 = base + L::om_off;
     uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);
     uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
@@ -812,12 +835,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
             dr[r] = (t < nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + h) : 1.f;
         }
     };
-    // warp 0: inclusive prefix sums of log2 d of the loaded head into dst
+    // warp 0: inclusive prefix sums of log2 d of the loaded head into dst, and
+    // the keys' injection weights (1 - d when gated) into dst + (om2 - lam2)
     auto head_lam = [&](float* dst) {
         float lg[4], s = 0.f;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             lg[r] = lg2(dr[r]);
+            dst[(om2 - lam2) + 4 * lane + r] = a.gated ? 1.f - dr[r] : 1.f;
             s += lg[r];
         }
         float x = s;
@@ -874,6 +899,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     for (int hi = 0; hi < hb && ok; ++hi) {
         const int h = h0 + hi;
         const float* lam = lam2 + (hi & 1) * CH;
+        const float* omh = om2 + (hi & 1) * CH;
         if (warp == 0 && hi + 1 < hb) head_d(h + 1);
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
@@ -894,7 +920,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = j0 + jj;
-                x[jj] *= j <= t ? ex2(lt - lam[j]) : 0.f;
+                x[jj] *= j <= t ? ex2(lt - lam[j]) * omh[j] : 0.f;
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -1059,7 +1085,9 @@ int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
 }
 
 bool chunked_supported(const RecurArgs& x) {
-    return (x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_HEAD) && x.dk == DKC && (x.dv == 64 || x.dv == 128);
+    return (x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_HEAD || x.kind == RK_DIAG_KEY_GATED ||
+            x.kind == RK_DIAG_HEAD_GATED) &&
+           x.dk == DKC && (x.dv == 64 || x.dv == 128);
 }
 
 cudaError_t launch_recur_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
@@ -1078,7 +1106,8 @@ cudaError_t launch_recur_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     a.anc = reinterpret_cast<float*>(p);
     a.st = st;
     a.wait_ns = wait_ns;
-    const bool per_key = x.kind == RK_DIAG_KEY;
+    const bool per_key = x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_KEY_GATED;
+    a.gated = x.kind == RK_DIAG_KEY_GATED || x.kind == RK_DIAG_HEAD_GATED;
     if (x.dv == 128) return per_key ? run_chunked<true, 128>(a, sm_count, s) : run_chunked<false, 128>(a, sm_count, s);
     return per_key ? run_chunked<true, 64>(a, sm_count, s) : run_chunked<false, 64>(a, sm_count, s);
 }

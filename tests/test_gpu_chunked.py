@@ -171,6 +171,44 @@ def test_per_key_range_limit_is_reported(ctx, sr):
     assert ctx.last_error() == sr.SN_OK                    # read once, cleared
 
 
+@pytest.mark.parametrize("per_key", [True, False])
+@pytest.mark.parametrize("dv", [128, 64])
+@pytest.mark.parametrize("T", [5, 128, 300])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_gated_parity(ctx, per_key, dv, T, with_state):
+    """Gated injection S = p (.) S + (1 - p) (.) (k v^T): the diagonal
+    recurrence with keys weighted by 1 - p, which every kernel of the chunked
+    form applies where it scales the keys (per-head gates with dv = 64 run the
+    block-of-heads kernels)."""
+    B, H = 2, 3
+    x = synth.gated_memory_inputs(B, T, H, 128, dv, per_key=per_key, cid=340 + T % 5)
+    S0 = synth.normal((B, H, 128, dv), 9700 + T) * 0.5 if with_state else None
+    o, S = run_chunked(ctx, x, S0)
+    ro, rS = ref(x, S0)
+    assert _nrel(o, ro) <= TOL
+    assert _nrel(S, rS) <= TOL
+
+
+def test_gated_per_head_blocks_sharing_one_group(ctx):
+    """Per-head gates with grouped keys: the output kernel weights each head's
+    copy of Q K^T by that head's decays and gates (two heads per CTA here)."""
+    B, T, H, G, dv = 4, 2048, 8, 2, 64
+    x = synth.mamba2_inputs(B, T, H, G, 128, dv, cid=350)
+    x = dict(x, decay_kind=synth.DECAY_PER_HEAD_GATED)
+    S0 = synth.normal((B, H, 128, dv), 9800) * 0.5
+    o, S = run_chunked(ctx, x, S0)
+    per = H // G
+    for b in (0, B - 1):
+        for h in range(H):
+            g = h // per
+            xs = dict(x, q=x["q"][b:b + 1, :, g:g + 1].contiguous(), k=x["k"][b:b + 1, :, g:g + 1].contiguous(),
+                      v=x["v"][b:b + 1, :, h:h + 1].contiguous(), d=x["d"][b:b + 1, :, h:h + 1].contiguous(),
+                      H=1, G=1)
+            ro, rS = ref(xs, S0[b:b + 1, h:h + 1].contiguous())
+            assert _nrel(o[b:b + 1, :, h:h + 1], ro) <= TOL, (b, h)
+            assert _nrel(S[b:b + 1, h:h + 1], rS) <= TOL, (b, h)
+
+
 @pytest.mark.parametrize("kind", ["gla", "mamba2"])
 def test_zero_decay_is_reported(ctx, sr, kind):
     B, T, H, dv = 1, 64, 1, 64
@@ -191,9 +229,6 @@ def test_unsupported_shapes_and_missing_workspace(ctx, sr):
     assert abi.sn_recur_diag_chunked(ctx.handle, 1, 16, 1, 1, 128, 64, sr.SN_DECAY_PER_KEY, 1.0, q, k, v, d,
                                      None, S, o) == sr.SN_E_NOMEM
     ctx.ensure_workspace_bytes(abi.sn_recur_chunked_workspace_bytes(1, 16, 1, 128, 64))
-    for kind in (sr.SN_DECAY_PER_KEY_GATED, sr.SN_DECAY_PER_HEAD_GATED):
-        assert abi.sn_recur_diag_chunked(ctx.handle, 1, 16, 1, 1, 128, 64, kind, 1.0, q, k, v, d,
-                                         None, S, o) == sr.SN_E_UNSUPPORTED
     assert abi.sn_recur_diag_chunked(ctx.handle, 1, 16, 1, 1, 128, 64, 7, 1.0, q, k, v, d,
                                      None, S, o) == sr.SN_E_INVAL
     x64 = synth.gla_inputs(1, 16, 1, 64, 64, cid=320)
