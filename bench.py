@@ -171,27 +171,47 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU baseline
-def cpu_oracle_scan(a, b, u, s0, threads):
-    """Time the fp64 CPU oracle on both scan forms; the batch rows are
-    independent, so they run on `threads` Python threads (ctypes releases the
-    GIL).  Returns seconds."""
+def cpu_oracle_scan(a, b, u, s0, threads, prec="f64"):
+    """Time the CPU oracle (fp64 or fp32) on both scan forms; the batch rows
+    are independent, so they run on `threads` Python threads (ctypes releases
+    the GIL).  Returns seconds."""
     import concurrent.futures as cf
 
     import numpy as np
 
     import oracle
     B = a.shape[0]
-    s064 = s0.astype(np.float64)
+    s0p = s0.astype(np.float64) if prec == "f64" else s0
 
     def one(i):
-        oracle.scan_fma(a[i:i + 1], b[i:i + 1], s064[i:i + 1])
-        oracle.scan_gated(a[i:i + 1], u[i:i + 1], s064[i:i + 1])
+        oracle.scan_fma(a[i:i + 1], b[i:i + 1], s0p[i:i + 1], prec=prec)
+        oracle.scan_gated(a[i:i + 1], u[i:i + 1], s0p[i:i + 1], prec=prec)
 
-    oracle.scan_fma(a[:1, :8], b[:1, :8], s064[:1])           # load the library outside the timing
+    oracle.scan_fma(a[:1, :8], b[:1, :8], s0p[:1], prec=prec)   # load the library outside the timing
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:
         list(ex.map(one, range(B)))
     return time.perf_counter() - t0
+
+
+def cpu_model():
+    """The host CPU's name from /proc/cpuinfo (model name, or the Arm
+    implementer / part codes), else the platform string."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.processor() or platform.machine()
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args):
@@ -660,7 +680,20 @@ def run_ours(args):
                "kind": "oracle",
                "sample": f"the full workload B=8 T=8192 N=2048 (this run's inputs), both forms, fp64 oracle, "
                          f"batch rows on {threads} threads, {secs:.2f} s"}
-        del a, b, u, s0
+        # the same oracle single-threaded (one batch row) and in fp32 (all rows,
+        # and one row), with the host it ran on
+        row = (a[:1], b[:1], u[:1], s0[:1])
+        s1 = cpu_oracle_scan(*row, 1)
+        s32 = cpu_oracle_scan(a, b, u, s0, threads, prec="f32")
+        s321 = cpu_oracle_scan(*row, 1, prec="f32")
+        cpu["detail"] = {
+            "cpu_model": cpu_model(), "logical_cpus": os.cpu_count(),
+            "fp64_all_threads_GBps": cpu["value"],
+            "fp64_1_thread_GBps": round(2 * scan_bytes(1, T, N) / s1 / GB, 4),
+            "fp32_all_threads_GBps": round(2 * scan_bytes(B, T, N) / s32 / GB, 4),
+            "fp32_1_thread_GBps": round(2 * scan_bytes(1, T, N) / s321 / GB, 4),
+            "sample_1_thread": "one batch row (T=8192 N=2048), both forms"}
+        del a, b, u, s0, row
 
     assert ctx.last_error() == sr.SN_OK
     clocks = clk.summary()
