@@ -38,37 +38,59 @@ struct DecodeParams {
     float* o;            // (B, 1, H, dv), may be NULL
 };
 
-// sum_i p[i] x[i] in the sequence kernel's order with R rows per lane
-template <int DK, int R>
-__device__ __forceinline__ float seq_dot(const float (&p)[DK], const float* x) {
-    constexpr int LPC = DK / R;
-    float lane[LPC];
+// sum_i p[i] x[i] in the sequence kernel's order with R rows per lane.  With
+// HV = 2 a column is split over two threads (lanes l and l ^ 16): this thread
+// holds the rows of the virtual lanes s in [hv * LPC/2, (hv + 1) * LPC/2) in
+// p[0 .. DK/2), and the first join (offset LPC/2) is the pair's shuffle.
+template <int DK, int R, int HV>
+__device__ __forceinline__ float seq_dot(const float (&p)[DK / HV], const float* x, int hv) {
+    constexpr int LPC = DK / R, LS = LPC / HV;
+    float lane[LS];
 #pragma unroll
-    for (int s = 0; s < LPC; ++s) {
+    for (int sl = 0; sl < LS; ++sl) {
+        const int s = hv * LS + sl;
         float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int m = 0; m < R / 4; ++m)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = (m * LPC + s) * 4 + e;
-                a[e] = __fmaf_rn(p[r], x[r], a[e]);
+                const int r = (m * LPC + s) * 4 + e;           // row of the state
+                a[e] = __fmaf_rn(p[(m * LS + sl) * 4 + e], x[r], a[e]);
             }
-        lane[s] = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+        lane[sl] = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+    }
+    if (HV == 2) {
+#pragma unroll
+        for (int sl = 0; sl < LS; ++sl) lane[sl] = __fadd_rn(lane[sl], __shfl_xor_sync(0xffffffffu, lane[sl], 16));
     }
 #pragma unroll
-    for (int o = LPC / 2; o > 0; o >>= 1)
+    for (int o = LS / 2; o > 0; o >>= 1)
 #pragma unroll
-        for (int s = 0; s < o; ++s) lane[s] = __fadd_rn(lane[s], lane[s + o]);
+        for (int sl = 0; sl < o; ++sl) lane[sl] = __fadd_rn(lane[sl], lane[sl + o]);
     return lane[0];
 }
 
+// Thread layout: HV threads per value column (2 for dk = 128, so a thread
+// holds 64 entries); in a warp, lanes 0-15 and 16-31 take the two halves of
+// the same 16 columns.
 template <int KIND, int DK, int DV, int R>
-__global__ void __launch_bounds__(DD_THREADS, 1) recur_decode_cols(const DecodeParams p) {
-    constexpr int SPC = DD_THREADS / DV;   // states per CTA step
+__global__ void __launch_bounds__(DD_THREADS, 2) recur_decode_cols(const DecodeParams p) {
+    constexpr int HV = DK == 128 ? 2 : 1;
+    constexpr int PR = DK / HV;                       // state entries per thread
+    constexpr int LPC = DK / R, LS = LPC / HV;
+    constexpr int SPC = DD_THREADS / (HV * DV);       // states per CTA step
     __shared__ float sk[SPC][DK], sq[SPC][DK], sd[SPC][per_key_gate<KIND>() ? DK : 1];
-    const int tid = threadIdx.x, slot = tid / DV, j = tid % DV;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hv = HV == 2 ? lane >> 4 : 0;
+    const int cl = HV == 2 ? warp * 16 + (lane & 15) : tid;   // column-thread index in the CTA
+    const int slot = cl / DV, j = cl % DV;
     const int BH = p.B * p.H;
     const int hpg = p.H / p.G;
+    // row of this thread's e-th entry: entry (m * LS + sl) * 4 + e is row (m * LPC + hv * LS + sl) * 4 + e
+    auto row_of = [&](int idx) {
+        const int e = idx & 3, q = idx >> 2, m = q / LS, sl = q % LS;
+        return (m * LPC + hv * LS + sl) * 4 + e;
+    };
     for (int base = blockIdx.x * SPC; base < BH; base += gridDim.x * SPC) {
         __syncthreads();   // the previous step's readers are done with the staged vectors
         for (int idx = tid; idx < SPC * DK; idx += DD_THREADS) {
@@ -83,32 +105,36 @@ __global__ void __launch_bounds__(DD_THREADS, 1) recur_decode_cols(const DecodeP
         }
         __syncthreads();
         const int bh = base + slot;
-        if (bh >= BH) continue;
+        if (bh >= BH) continue;                       // a whole pair of lanes leaves together
         const size_t sbase = (size_t)bh * DK * DV + j;
-        float pc[DK];
+        float pc[PR];
 #pragma unroll
-        for (int i = 0; i < DK; ++i) pc[i] = p.S_in != nullptr ? p.S_in[sbase + (size_t)i * DV] : 0.f;
+        for (int t = 0; t < PR; ++t) pc[t] = p.S_in != nullptr ? p.S_in[sbase + (size_t)row_of(t) * DV] : 0.f;
         const float vj = __ldg(p.v + (size_t)bh * DV + j);
         const float* kx = sk[slot];
         if constexpr (diag_kind<KIND>()) {
             const float dh = per_key_gate<KIND>() ? 0.f : __ldg(p.g + bh);
 #pragma unroll
-            for (int i = 0; i < DK; ++i) {
+            for (int t = 0; t < PR; ++t) {
+                const int i = row_of(t);
                 const float di = per_key_gate<KIND>() ? sd[slot][i] : dh;
                 float ki = kx[i];
                 if constexpr (gated_injection<KIND>()) ki = __fmul_rn(__fsub_rn(1.0f, di), ki);
-                pc[i] = __fmaf_rn(di, pc[i], __fmul_rn(ki, vj));
+                pc[t] = __fmaf_rn(di, pc[t], __fmul_rn(ki, vj));
             }
         } else {   // RK_DELTA
-            const float u = seq_dot<DK, R>(pc, kx);
+            const float u = seq_dot<DK, R, HV>(pc, kx, hv);
             const float delta = __fmul_rn(__fadd_rn(vj, -u), __ldg(p.g + bh));
 #pragma unroll
-            for (int i = 0; i < DK; ++i) pc[i] = __fmaf_rn(kx[i], delta, pc[i]);
+            for (int t = 0; t < PR; ++t) pc[t] = __fmaf_rn(kx[row_of(t)], delta, pc[t]);
         }
-        if (p.o != nullptr) p.o[(size_t)bh * DV + j] = __fmul_rn(seq_dot<DK, R>(pc, sq[slot]), p.scale);
+        if (p.o != nullptr) {
+            const float acc = seq_dot<DK, R, HV>(pc, sq[slot], hv);
+            if (hv == 0) p.o[(size_t)bh * DV + j] = __fmul_rn(acc, p.scale);
+        }
         if (p.S_out != nullptr) {
 #pragma unroll
-            for (int i = 0; i < DK; ++i) p.S_out[sbase + (size_t)i * DV] = pc[i];
+            for (int t = 0; t < PR; ++t) p.S_out[sbase + (size_t)row_of(t) * DV] = pc[t];
         }
     }
 }
@@ -117,8 +143,8 @@ template <int KIND, int R>
 cudaError_t run_decode_rows(const RecurArgs& x, const DecodeParams& p, int sm_count, cudaStream_t s) {
     const int BH = x.B * x.H;
     auto go = [&](auto kern, int dv) -> cudaError_t {
-        const int spc = DD_THREADS / dv;
-        const int grid = std::min((BH + spc - 1) / spc, 2 * sm_count);
+        const int spc = DD_THREADS / ((x.dk == 128 ? 2 : 1) * dv);
+        const int grid = std::min((BH + spc - 1) / spc, 4 * sm_count);
         kern<<<grid, DD_THREADS, 0, s>>>(p);
         return cudaGetLastError();
     };
@@ -133,8 +159,12 @@ cudaError_t run_decode_rows(const RecurArgs& x, const DecodeParams& p, int sm_co
 // single steps and longer segments gives the same bits.
 template <int KIND>
 cudaError_t run_decode_kind(const RecurArgs& x, const DecodeParams& p, int sm_count, cudaStream_t s) {
-    if (KIND == RK_DELTA || seq_warps(x, 8, 4) >= 4 * (int64_t)sm_count) return run_decode_rows<KIND, 8>(x, p, sm_count, s);
-    return run_decode_rows<KIND, 4>(x, p, sm_count, s);
+    if constexpr (KIND == RK_DELTA) {
+        return run_decode_rows<KIND, 8>(x, p, sm_count, s);
+    } else {
+        if (seq_warps(x, 8, 4) >= 4 * (int64_t)sm_count) return run_decode_rows<KIND, 8>(x, p, sm_count, s);
+        return run_decode_rows<KIND, 4>(x, p, sm_count, s);
+    }
 }
 
 }  // namespace
