@@ -24,6 +24,9 @@
 //                 of every chunk's Delta^T and S_n^T leave by bulk stores;
 //   chunk_output  the output kernel of the diagonal-decay form with unit
 //                 decays (recur_chunked.cu), bulk-loading Delta^T in place of v.
+// For longer sequences the chunks are split into segments that run as a
+// pipeline on three side streams (launch_delta_chunked), so the chain of one
+// segment overlaps the preparation of the next.
 // Supported: dk = dv = 128.  Results carry tf32 rounding (about 1e-3
 // relative); splits at multiples of 128 tokens are bit-exact because the state
 // crosses chunks in fp32.

@@ -1,5 +1,7 @@
-// scan_lookback.cu -- chunked associative scan with decoupled look-back
-// (tier 1 for few channels and long T), sm_103a.
+// scan_lookback.cu -- chunked associative scans of tier 1 for few channels and
+// long T, sm_103a: the decoupled look-back kernel, and the reduce-then-scan
+// path (further below) that gives the same bits in three flag-free launches;
+// the allocation-free entry point runs the look-back kernel.
 //
 // Forms as in scan.cu ("SunnyNet 工程化实录" §2.1).  Each tile is 32 channels
 // x 128 steps: per-thread folds over 4 steps into (A, B) pairs, a warp-shuffle
