@@ -94,7 +94,7 @@ __device__ __forceinline__ float lg2(float x) {
 }
 
 __device__ __forceinline__ float* align128(unsigned char* p) {
-    return reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p) + 127) & ~uintptr_t(127));
+    return reinterpret_cast<float*>(smem_align<128>(p));
 }
 
 struct ChunkIdx {

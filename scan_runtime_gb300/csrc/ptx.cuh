@@ -17,6 +17,24 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first A-byte aligned address at or after raw, a pointer into the
+// dynamic shared memory.  The offset is added to raw itself (not formed from
+// an integer), so the compiler still sees a shared-memory pointer and reads
+// through it with shared-memory loads rather than generic ones.
+template <uint32_t A>
+__device__ __forceinline__ unsigned char* smem_align(unsigned char* raw) {
+    const uint32_t s = smem_u32(raw);
+    return raw + (((s + (A - 1)) & ~(A - 1)) - s);
+}
+
+// The same address formed from an integer: the compiler no longer knows the
+// pointer is shared and reads through it with generic loads, which it
+// schedules as long-latency loads (issued further ahead of their use).
+template <uint32_t A>
+__device__ __forceinline__ unsigned char* smem_align_generic(unsigned char* raw) {
+    return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(raw) + (A - 1)) & ~uintptr_t(A - 1));
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(NT, 1)
 chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, const ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     using L = OutSmem<DV>;
-    float* base = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* base = reinterpret_cast<float*>(smem_align<1024>(smem_raw));
     float* bufQ = base + L::q_off;
     float* bufK = base + L::k_off;
     float* bufS = base + L::s_off;

@@ -36,8 +36,7 @@ recur_decode_rwkv7(int BH, const float* __restrict__ q, const float* __restrict_
                    const float* __restrict__ v, const float* __restrict__ w, const float* S_in, float* S_out,
                    float* __restrict__ o, SnDevStatus* st, uint64_t wait_ns) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    unsigned char* smem = smem_align<128>(smem_raw);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + DEC_TILES * DEC_TILE_BYTES);
     const int tid = threadIdx.x;
     const int tile0 = blockIdx.x * DEC_TILES;

@@ -206,8 +206,10 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     static_assert(R % 4 == 0 && C % 2 == 0 && LPC <= 32 && NV % LPC == 0, "tile shape");
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    // With 4 rows per lane a step has little arithmetic to hide its operand
+    // loads behind, and the kernel measured faster with the loads scheduled as
+    // generic (long-latency) ones; with 8 rows, shared-memory loads are faster.
+    unsigned char* smem = R >= 8 ? smem_align<128>(smem_raw) : smem_align_generic<128>(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar_off);
     uint64_t* empty = full + RS_STAGES;
 

@@ -137,7 +137,8 @@ __device__ __forceinline__ void tile_outputs(const float* sa, const float* sb, i
 // full block the aggregates of CHAIN_U chunks are read into registers one
 // batch ahead of the FMAs that consume them (two batches in turn, all offsets
 // fixed), so a step costs two shared loads, the FMA and a store, and the
-// dependent chain is not held up by load latency.
+// dependent chain is not held up by load latency.  The carries are stored as
+// global stores (st.global), which cannot alias the shared-memory operands.
 constexpr int CHAIN_BLK = 128;
 constexpr int CHAIN_STAGES = 4;
 constexpr int CHAIN_U = 16;
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(32) scan_chain(const ChainParams p) {
 #pragma unroll
                 for (int u = 0; u < CHAIN_U; ++u) {
                     c = __fmaf_rn(a0[u], c, b0[u]);
-                    dC[SN_CHAIN_IX(i0 + u) * LB_NC] = c;
+                    __stcg(&dC[SN_CHAIN_IX(i0 + u) * LB_NC], c);
                 }
                 if (i0 + 2 * CHAIN_U < CHAIN_BLK) {
 #pragma unroll
@@ -226,14 +227,14 @@ __global__ void __launch_bounds__(32) scan_chain(const ChainParams p) {
 #pragma unroll
                 for (int u = 0; u < CHAIN_U; ++u) {
                     c = __fmaf_rn(a1[u], c, b1[u]);
-                    dC[SN_CHAIN_IX(i0 + CHAIN_U + u) * LB_NC] = c;
+                    __stcg(&dC[SN_CHAIN_IX(i0 + CHAIN_U + u) * LB_NC], c);
                 }
             }
         } else {
             for (int q = 0; q < cnt; ++q) {   // the partial block (the sequence's last)
                 const int i = REV ? cnt - 1 - q : q;
                 c = __fmaf_rn(sA[i * LB_NC], c, sB[i * LB_NC]);
-                dC[(size_t)i * LB_NC] = c;
+                __stcg(&dC[(size_t)i * LB_NC], c);
             }
         }
 #undef SN_CHAIN_IX
