@@ -149,13 +149,15 @@ void sn_ctx_free(SnCtx* ctx);
 /* Hand the context a caller-owned device workspace (used only by the chunked
  * look-back scan).  `dev_ptr` must be 256-byte aligned; `bytes` >= 0; a NULL
  * pointer or 0 bytes removes it.  The library never frees it.  The first
- * look-back launch after this call clears the flag area with one
- * cudaMemsetAsync on that launch's stream. */
+ * look-back launch after this call (or after another chunked path used the
+ * workspace) clears the flag and carry-word areas with cudaMemsetAsync on that
+ * launch's stream. */
 sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes);
 
-/* Workspace bytes the chunked look-back scan needs for this problem
- * (op = SN_OP_SCAN_FMA or SN_OP_SCAN_GATED); 0 for an op that needs none,
- * -1 on invalid arguments. */
+/* Workspace bytes the chunked scans need for this problem (op =
+ * SN_OP_SCAN_FMA or SN_OP_SCAN_GATED): with tiles = B * ceil(N / 32) *
+ * ceil(T / 128), a flag word per tile rounded up to 256 bytes plus 512 bytes
+ * per tile; 0 for an op that needs none, -1 on invalid arguments. */
 int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N);
 
 /* Return and clear the first device-side error recorded in the context's
@@ -393,8 +395,8 @@ sn_status sn_readout_dskip(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t 
  *
  * It computes what sn_scan_fma (gated = 0) or sn_scan_gated (gated = 1)
  * computes with SN_OPT_SCAN_KERNEL = SN_SCAN_KERNEL_LOOKBACK, with the same
- * bits.  Its scratch is a 16 MiB file-scope device array that every GPU which
- * loads libsn holds until the process exits; problems needing more than
+ * bits.  Its scratch is a file-scope device array of about 20 MiB that every
+ * GPU which loads libsn holds until the process exits; problems needing more than
  * SN_NOALLOC_MAX_TILES tiles are rejected with SN_E_NOMEM.  Arguments as
  * sn_scan_fma, except: N % 4 == 0 and 16-byte aligned a, b, s_out are
  * required (else SN_E_UNSUPPORTED); the device is the calling thread's current

@@ -324,10 +324,13 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     if (kernel == SN_SCAN_KERNEL_LOOKBACK) {
         const int64_t nflags = lookback_flag_count(B, T, N);
         if (ctx->ws_dirty || nflags != ctx->lb_last_flags) {
-            // fresh flag area: zero it once, on the caller's stream.  Between
-            // clears every launch rewrites all its flags, and the launch epoch
-            // (kept on the device) differs from the previous launch's.
+            // fresh flag and carry-word areas: zero them once, on the caller's
+            // stream.  Between clears every launch rewrites all its flags and
+            // carry words, and the launch epoch (kept on the device) differs
+            // from the previous launch's.
+            const int64_t cw_off = lookback_cw_offset(B, T, N);
             if (cudaMemsetAsync(ctx->ws, 0, (size_t)nflags * 4, s) != cudaSuccess ||
+                cudaMemsetAsync(static_cast<char*>(ctx->ws) + cw_off, 0, (size_t)(need - cw_off), s) != cudaSuccess ||
                 cudaMemsetAsync(&ctx->dstatus->abort_tag, 0, sizeof(unsigned int), s) != cudaSuccess)
                 return SN_E_DEVICE;
             ctx->ws_dirty = false;
@@ -336,8 +339,10 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->debug_poison, ctx->dstatus, wait_ns(ctx),
                                               ctx->sm_count, s));
     }
-    if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN)
+    if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
+        ctx->ws_dirty = true;   // its carries overwrite the look-back's carry words
         return from_cuda(launch_scan_reduce_scan(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+    }
     return from_cuda(launch_scan_sequential(x, gated, ctx->dstatus, wait_ns(ctx), s));
 }
 

@@ -32,10 +32,16 @@ int64_t lookback_flag_count(int B, int T, int N) {
     return (int64_t)B * ncb * nch;
 }
 
-int64_t lookback_ws_bytes(int B, int T, int N) {
+// Look-back workspace: [ flags: u32 per tile | A | B: f32 per channel and tile |
+// carry words: u64 per channel and tile ].  The reduce-then-scan path uses the
+// same region as three f32 arrays after the flags.
+int64_t lookback_cw_offset(int B, int T, int N) {
     const int64_t tiles = lookback_flag_count(B, T, N);
-    const int64_t flag_bytes = ((tiles * 4 + 255) / 256) * 256;
-    return flag_bytes + tiles * 3 * LB_NC * 4;
+    return ((tiles * 4 + 255) / 256) * 256 + tiles * 2 * LB_NC * 4;
+}
+
+int64_t lookback_ws_bytes(int B, int T, int N) {
+    return lookback_cw_offset(B, T, N) + lookback_flag_count(B, T, N) * LB_NC * 8;
 }
 
 struct LookbackParams {
@@ -46,7 +52,7 @@ struct LookbackParams {
     uint32_t* flags;
     float* dA;
     float* dB;
-    float* dC;
+    unsigned long long* cw;   // per tile and channel: (tag | LB_INCL) << 32 | bits of the carry
     uint32_t poison;     // 1: waiters look for a tag no tile publishes (tests the bound)
     SnDevStatus* st;     // error word, abort tag and the launch epoch (lb_epoch, lb_done)
     uint64_t wait_ns;
@@ -140,85 +146,115 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
             float CA, CB;
             tile_aggregate(wA, wB, lane, CA, CB);
             const int base = bi * p.ncb + cb;
+            const uint32_t want_c = want | LB_INCL;   // tag of a carry word this launch wrote
             float cin;
             if (k == 0) {
                 cin = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
             } else {
-                // Windowed look-back: lane l inspects chunk (j - l).  Success =
-                // the nearest inclusive carry m with every chunk in (m, k)
-                // published.  The aggregate is published only if the first
-                // probe does not already succeed.
-                int j = k - 1;
-                int m = -2;                           // chunk whose inclusive carry we take (-1 = s0)
-                bool published = false;
-                const uint64_t tstart = global_ns();
-                bool timed_out = false;
-                while (true) {
-                    const int jl = j - lane;
-                    uint32_t state = LB_INCL;         // chunks before 0 act as "inclusive = s0"
-                    if (jl >= 0) {
-                        const uint32_t f = ld_acquire_gpu(p.flags + (size_t)jl * p.nbcb + base);
-                        state = ((f & ~3u) == want) ? (f & 3u) : 0u;
-                    }
-                    const uint32_t incl = __ballot_sync(0xffffffffu, state == LB_INCL);
-                    const uint32_t none = __ballot_sync(0xffffffffu, state == 0u);
-                    if (incl != 0u) {
-                        const int l = __ffs(incl) - 1;
-                        if ((none & ((1u << l) - 1u)) == 0u) {   // all nearer chunks published
-                            m = j - l;
+                // Usually the predecessor has already published its carry: one
+                // load of its carry words (value and tag in one word) finds it.
+                unsigned long long w = ld_relaxed_gpu_u64(p.cw + ((size_t)(k - 1) * p.nbcb + base) * LB_NC + lane);
+                if (__all_sync(0xffffffffu, (uint32_t)(w >> 32) == want_c)) {
+                    cin = __uint_as_float((uint32_t)w);
+                } else {
+                    // Windowed look-back: lane l inspects chunk (j - l).  Success =
+                    // the nearest inclusive carry m with every chunk in (m, k)
+                    // published.  The aggregate is published the first time a
+                    // probe does not succeed.
+                    int j = k - 1;
+                    int m = -2;                       // chunk whose inclusive carry we take (-1 = s0)
+                    bool published = false;
+                    const uint64_t tstart = global_ns();
+                    bool timed_out = false;
+                    auto give_up = [&]() {
+                        return global_ns() - tstart > p.wait_ns ||
+                               *reinterpret_cast<volatile const uint32_t*>(&p.st->abort_tag) == tag;
+                    };
+                    while (true) {
+                        const int jl = j - lane;
+                        uint32_t state = LB_INCL;     // chunks before 0 act as "inclusive = s0"
+                        if (jl >= 0) {
+                            const uint32_t f = ld_acquire_gpu(p.flags + (size_t)jl * p.nbcb + base);
+                            state = ((f & ~3u) == want) ? (f & 3u) : 0u;
+                        }
+                        const uint32_t incl = __ballot_sync(0xffffffffu, state == LB_INCL);
+                        const uint32_t none = __ballot_sync(0xffffffffu, state == 0u);
+                        if (incl != 0u) {
+                            const int l = __ffs(incl) - 1;
+                            if ((none & ((1u << l) - 1u)) == 0u) {   // all nearer chunks published
+                                m = j - l;
+                                break;
+                            }
+                        } else if (none == 0u) {      // 32 aggregates: look further back
+                            j -= 32;
+                            continue;
+                        }
+                        if (!published) {             // let successors fold through this chunk
+                            const size_t me = (size_t)ti * LB_NC + lane;
+                            p.dA[me] = CA;
+                            p.dB[me] = CB;
+                            __syncwarp();
+                            if (lane == 0) st_release_gpu(p.flags + ti, tag | LB_AGG);
+                            published = true;
+                        }
+                        // give up after the limit, or at once if another tile of this
+                        // launch already gave up (its successors would only wait too)
+                        if (give_up()) {
+                            timed_out = true;
                             break;
                         }
-                    } else if (none == 0u) {          // 32 aggregates: look further back
-                        j -= 32;
-                        continue;
                     }
-                    if (!published) {                 // let successors fold through this chunk
-                        const size_t me = (size_t)ti * LB_NC + lane;
-                        p.dA[me] = CA;
-                        p.dB[me] = CB;
-                        __syncwarp();
-                        if (lane == 0) st_release_gpu(p.flags + ti, tag | LB_AGG);
-                        published = true;
-                    }
-                    // give up after the limit, or at once if another tile of this
-                    // launch already gave up (its successors would only wait too)
-                    if (global_ns() - tstart > p.wait_ns ||
-                        *reinterpret_cast<volatile const uint32_t*>(&p.st->abort_tag) == tag) {
-                        timed_out = true;
-                        break;
-                    }
-                }
-                __syncwarp();
-                if (timed_out) {
-                    if (lane == 0) {
-                        record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | 2);
-                        atomicExch(&p.st->abort_tag, tag);
-                    }
-                    cin = 0.f;
-                } else {
-                    // forward fold from the inclusive carry at m through m+1 .. k-1,
-                    // one chunk at a time (loads batched eight chunks ahead)
-                    if (m < 0) cin = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
-                    else cin = __ldcg(p.dC + ((size_t)m * p.nbcb + base) * LB_NC + lane);
-                    for (int i0 = m + 1; i0 < k; i0 += 8) {
-                        float fa[8], fb[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int i = i0 + u < k ? i0 + u : k - 1;
-                            const size_t o = ((size_t)i * p.nbcb + base) * LB_NC + lane;
-                            fa[u] = __ldcg(p.dA + o);
-                            fb[u] = __ldcg(p.dB + o);
+                    if (!timed_out) {
+                        if (m < 0) {
+                            cin = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
+                        } else {
+                            // chunk m's flag announced its carry; the carry words
+                            // themselves may land a moment later
+                            const unsigned long long* cm = p.cw + ((size_t)m * p.nbcb + base) * LB_NC + lane;
+                            while (true) {
+                                w = ld_relaxed_gpu_u64(cm);
+                                if (__all_sync(0xffffffffu, (uint32_t)(w >> 32) == want_c)) break;
+                                if (give_up()) {
+                                    timed_out = true;
+                                    break;
+                                }
+                            }
+                            cin = __uint_as_float((uint32_t)w);
                         }
+                    }
+                    __syncwarp();
+                    if (timed_out) {
+                        if (lane == 0) {
+                            record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | 2);
+                            atomicExch(&p.st->abort_tag, tag);
+                        }
+                        cin = 0.f;
+                    } else {
+                        // forward fold from the inclusive carry at m through m+1 .. k-1,
+                        // one chunk at a time (loads batched eight chunks ahead)
+                        for (int i0 = m + 1; i0 < k; i0 += 8) {
+                            float fa[8], fb[8];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            if (i0 + u < k) cin = __fmaf_rn(fa[u], cin, fb[u]);
+                            for (int u = 0; u < 8; ++u) {
+                                const int i = i0 + u < k ? i0 + u : k - 1;
+                                const size_t o = ((size_t)i * p.nbcb + base) * LB_NC + lane;
+                                fa[u] = __ldcg(p.dA + o);
+                                fb[u] = __ldcg(p.dB + o);
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                if (i0 + u < k) cin = __fmaf_rn(fa[u], cin, fb[u]);
+                        }
                     }
                 }
             }
             const float Ck = __fmaf_rn(CA, cin, CB);
-            p.dC[(size_t)ti * LB_NC + lane] = Ck;
-            __syncwarp();       // the lanes' stores precede lane 0's release (cumulative)
-            if (lane == 0) st_release_gpu(p.flags + ti, tag | LB_INCL);
+            // The carry word is self-validating (its tag), so it needs no
+            // release; the flag only tells a deep look-back where it lies.
+            st_relaxed_gpu_u64(p.cw + (size_t)ti * LB_NC + lane,
+                               ((unsigned long long)(tag | LB_INCL) << 32) | __float_as_uint(Ck));
+            __syncwarp();
+            if (lane == 0) st_relaxed_gpu(p.flags + ti, tag | LB_INCL);
             carry[lane] = cin;
             cfin[lane] = Ck;
             if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
@@ -434,7 +470,7 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int po
     p.flags = reinterpret_cast<uint32_t*>(ws);
     p.dA = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + flag_bytes);
     p.dB = p.dA + tiles * LB_NC;
-    p.dC = p.dB + tiles * LB_NC;
+    p.cw = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + lookback_cw_offset(x.B, x.T, x.N));
     p.poison = poison ? 1u : 0u;
     p.st = st;
     p.wait_ns = wait_ns;
@@ -463,10 +499,12 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int po
 // start-up, and paths that cannot create an SnCtx (context creation allocates
 // the context's status block).
 //
-// The array (kNoallocScratchBytes, 16 MiB) lives on every device that loads
-// this library until the process exits.  Layout, fixed for every call:
-//   [ status block 256 B | flags: kNoallocMaxTiles x u32 | A | B | C carries ]
-// Flags stay at fixed offsets, so a flag word only ever holds a tag or zero.
+// The array (kNoallocScratchBytes, about 20 MiB) lives on every device that
+// loads this library until the process exits.  Layout, fixed for every call:
+//   [ status block 256 B | flags: kNoallocMaxTiles x u32 | A | B aggregates |
+//     carry words: kNoallocMaxTiles x 32 x u64 ]
+// Flags and carry words stay at fixed offsets, so such a word only ever holds
+// a tagged value or zero.
 #include <atomic>
 #include <mutex>
 
@@ -475,8 +513,9 @@ namespace {
 constexpr int64_t kNoallocMaxTiles = 40960;
 constexpr int64_t kNoallocFlagsOff = 256;
 constexpr int64_t kNoallocDataOff = kNoallocFlagsOff + kNoallocMaxTiles * 4;
-constexpr int64_t kNoallocScratchBytes = kNoallocDataOff + kNoallocMaxTiles * 3 * sn::LB_NC * 4;
-static_assert(kNoallocScratchBytes <= (int64_t(16) << 20), "scratch stays within 16 MiB");
+constexpr int64_t kNoallocCwOff = kNoallocDataOff + kNoallocMaxTiles * 2 * sn::LB_NC * 4;
+constexpr int64_t kNoallocScratchBytes = kNoallocCwOff + kNoallocMaxTiles * sn::LB_NC * 8;
+static_assert(kNoallocScratchBytes <= (int64_t(24) << 20), "scratch stays within 24 MiB");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -538,7 +577,7 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
     if (!d.ready) {
         // One-time set-up on this device (the first call; it must precede any
         // stream capture): the array's device address, the kernel's shared
-        // memory opt-in and occupancy, and a cleared status/flag area.
+        // memory opt-in and occupancy, and cleared status, flag and carry areas.
         void* sym = nullptr;
         if (cudaGetSymbolAddress(&sym, g_noalloc_scratch) != cudaSuccess || sym == nullptr) return SN_E_DEVICE;
         cudaDeviceProp prop;
@@ -551,7 +590,10 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
                 d.occ[g] < 1)
                 return SN_E_DEVICE;
         }
-        if (cudaMemsetAsync(sym, 0, (size_t)kNoallocDataOff, s) != cudaSuccess) return SN_E_DEVICE;
+        if (cudaMemsetAsync(sym, 0, (size_t)kNoallocDataOff, s) != cudaSuccess ||
+            cudaMemsetAsync(static_cast<unsigned char*>(sym) + kNoallocCwOff, 0,
+                            (size_t)(kNoallocScratchBytes - kNoallocCwOff), s) != cudaSuccess)
+            return SN_E_DEVICE;
         d.scratch = static_cast<unsigned char*>(sym);
         d.sm_count = prop.multiProcessorCount;
         d.ready = true;
@@ -575,7 +617,7 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
     p.flags = reinterpret_cast<uint32_t*>(d.scratch + kNoallocFlagsOff);
     p.dA = reinterpret_cast<float*>(d.scratch + kNoallocDataOff);
     p.dB = p.dA + tiles * LB_NC;
-    p.dC = p.dB + tiles * LB_NC;
+    p.cw = reinterpret_cast<unsigned long long*>(d.scratch + kNoallocCwOff);
     p.poison = 0;
     p.st = st;                                    // also holds the launch epoch
     p.wait_ns = 1000000000ull;                    // 1 s bound on every device-side wait

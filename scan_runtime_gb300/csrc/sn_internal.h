@@ -59,6 +59,7 @@ constexpr int LB_TC = 128;
 
 // Returns the workspace bytes of the look-back scan for (B, T, N).
 int64_t lookback_ws_bytes(int B, int T, int N);
+int64_t lookback_cw_offset(int B, int T, int N);
 int64_t lookback_flag_count(int B, int T, int N);
 
 // Opt `kern` into `bytes` of dynamic shared memory on the current device (once

@@ -125,7 +125,8 @@ def test_ctx_create_without_gpu_fails_cleanly(abi):
 def test_workspace_bytes(abi):
     nb = abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 8, 8192, 2048)
     tiles = 8 * (2048 // 32) * (8192 // 128)
-    assert nb == ((tiles * 4 + 255) // 256) * 256 + tiles * 3 * 32 * 4
+    # flags, the A and B aggregates (f32) and the tagged carry words (u64)
+    assert nb == ((tiles * 4 + 255) // 256) * 256 + tiles * (2 * 32 * 4 + 32 * 8)
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_GATED, 1, 1, 1) > 0
     assert abi.sn_workspace_bytes(99, 1, 1, 1) == -1
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 0, 1, 1) == -1
