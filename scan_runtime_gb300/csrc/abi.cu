@@ -309,11 +309,14 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     } else if (kernel == SN_SCAN_KERNEL_AUTO) {
         // The sequential kernel keeps the exact per-step bits and is HBM-bound
         // once there are enough channels; chunking along T pays only when the
-        // channel count leaves most SMs idle and T is long.  Of the two chunked
-        // paths (same bits), reduce-then-scan measured faster whenever the
-        // channels are that few: the look-back folds hundreds of chunks deep.
+        // channel count leaves most SMs idle and T is long.  Measured at 2^25
+        // elements: a sequential CTA (64 channels) streams about 37 GB/s and
+        // reduce-then-scan about 3.3 TB/s, so the two cross near 0.6 CTAs per
+        // SM (64 CTAs: 0.156 against 0.123 ms; 128 CTAs: 0.084 against
+        // 0.123 ms).  Of the two chunked paths (same bits), reduce-then-scan
+        // measured faster wherever the channels are that few.
         const int64_t seq_ctas = (int64_t)B * ((N + 63) / 64);
-        const bool few = seq_ctas < 2 * ctx->sm_count;
+        const bool few = 5 * seq_ctas < 3 * (int64_t)ctx->sm_count;
         kernel = (few && T >= 8 * LB_TC && lookback_supported(x) && ctx->ws != nullptr && ctx->ws_bytes >= need)
                      ? SN_SCAN_KERNEL_REDUCE_SCAN
                      : SN_SCAN_KERNEL_SEQUENTIAL;
@@ -380,8 +383,11 @@ static sn_status scan_backward_common(SnCtx* ctx, BwdArgs& x, bool gated, void* 
         if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
         chunked = true;
     } else if (ctx->scan_kernel == SN_SCAN_KERNEL_AUTO) {
+        // A sequential reverse-scan CTA covers 32 channels.  Measured at 2^25
+        // elements, the chunked path (about 0.165 ms) wins up to about one such
+        // CTA per SM (128 CTAs: 0.208 ms sequential; 192 CTAs: 0.143 ms).
         const int64_t seq_ctas = (int64_t)x.B * ((x.N + 31) / 32);
-        chunked = seq_ctas < 2 * ctx->sm_count && x.T >= 8 * LB_TC && scan_backward_chunked_supported(x) &&
+        chunked = seq_ctas <= ctx->sm_count && x.T >= 8 * LB_TC && scan_backward_chunked_supported(x) &&
                   ctx->ws != nullptr && ctx->ws_bytes >= need;
     } else {
         chunked = false;

@@ -23,6 +23,8 @@ namespace {
 constexpr uint32_t LB_AGG = 1u, LB_INCL = 2u;
 constexpr int LB_STAGES = 2;                      // tiles in flight per CTA (3 CTAs per SM)
 constexpr uint32_t LB_EPOCH_WRAP = 1u << 29;      // epochs run 1 .. 2^29 - 1 (tags are epoch << 2)
+constexpr int LB_FOLD_SOLO = 8;                   // deeper folds are staged by the whole CTA
+constexpr int LB_FOLD_B = 24;                     // chunks per staged batch (6 KB of shared memory)
 constexpr size_t LB_SMEM = LB_STAGES * LB_TILE_BYTES + LB_STAGES * 8 + 16;
 
 }  // namespace
@@ -67,6 +69,8 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + LB_STAGES * LB_TILE_BYTES);
     __shared__ float4 wA[8][8], wB[8][8];          // per-warp aggregates [warp][quad]
     __shared__ float carry[LB_NC], cfin[LB_NC];
+    __shared__ __align__(16) float stA[LB_FOLD_B][LB_NC], stB[LB_FOLD_B][LB_NC];   // staged aggregates
+    __shared__ int s_fold[2];                       // chunks [lo, hi) of a staged fold; hi = 0: none
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane & 7, sub = lane >> 3;
@@ -141,13 +145,26 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         tile_local_scan<GATED>(sa, sb, rows, wA, wB, EA, EB);
 
         // ---- phase 3: chunk aggregate and look-back (warp 0, lane = channel)
+        const int n = n0 + lane;
+        const int base = bi * p.ncb + cb;
+        float CA = 1.f, CB = 0.f, cin = 0.f;
+        // warp 0: this tile's carry and its outgoing carry words
+        auto publish = [&]() {
+            const float Ck = __fmaf_rn(CA, cin, CB);
+            // The carry word is self-validating (its tag), so it needs no
+            // release; the flag only tells a deep look-back where it lies.
+            st_relaxed_gpu_u64(p.cw + (size_t)ti * LB_NC + lane,
+                               ((unsigned long long)(tag | LB_INCL) << 32) | __float_as_uint(Ck));
+            __syncwarp();
+            if (lane == 0) st_relaxed_gpu(p.flags + ti, tag | LB_INCL);
+            carry[lane] = cin;
+            cfin[lane] = Ck;
+            if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
+        };
         if (warp == 0) {
-            const int n = n0 + lane;
-            float CA, CB;
             tile_aggregate(wA, wB, lane, CA, CB);
-            const int base = bi * p.ncb + cb;
             const uint32_t want_c = want | LB_INCL;   // tag of a carry word this launch wrote
-            float cin;
+            bool staged = false;
             if (k == 0) {
                 cin = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
             } else {
@@ -229,6 +246,13 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                             atomicExch(&p.st->abort_tag, tag);
                         }
                         cin = 0.f;
+                    } else if (k - 1 - m > LB_FOLD_SOLO) {
+                        // a deep fold: the whole CTA stages the aggregates below
+                        staged = true;
+                        if (lane == 0) {
+                            s_fold[0] = m + 1;
+                            s_fold[1] = k;
+                        }
                     } else {
                         // forward fold from the inclusive carry at m through m+1 .. k-1,
                         // one chunk at a time (loads batched eight chunks ahead)
@@ -248,18 +272,35 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                     }
                 }
             }
-            const float Ck = __fmaf_rn(CA, cin, CB);
-            // The carry word is self-validating (its tag), so it needs no
-            // release; the flag only tells a deep look-back where it lies.
-            st_relaxed_gpu_u64(p.cw + (size_t)ti * LB_NC + lane,
-                               ((unsigned long long)(tag | LB_INCL) << 32) | __float_as_uint(Ck));
-            __syncwarp();
-            if (lane == 0) st_relaxed_gpu(p.flags + ti, tag | LB_INCL);
-            carry[lane] = cin;
-            cfin[lane] = Ck;
-            if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
+            if (!staged) {
+                if (lane == 0) s_fold[1] = 0;
+                publish();
+            }
         }
         __syncthreads();
+        if (s_fold[1] != 0) {
+            // Deep fold (many chunks of one column in flight): the CTA loads the
+            // aggregates of LB_FOLD_B chunks at a time into shared memory (one
+            // L2 round trip per batch), and warp 0 folds them one chunk at a
+            // time, C = fma(A_i, C, B_i), as the short fold does.  The flags of
+            // these chunks were read with acquire by warp 0 before the barrier.
+            const int lo = s_fold[0], hi = s_fold[1];
+            const int u = tid >> 3, q4 = tid & 7;   // chunk of the batch, quarter of its 32 channels
+            for (int c0 = lo; c0 < hi; c0 += LB_FOLD_B) {
+                const int cnt = min(LB_FOLD_B, hi - c0);
+                if (u < cnt) {
+                    const size_t o = ((size_t)(c0 + u) * p.nbcb + base) * LB_NC + 4 * q4;
+                    *reinterpret_cast<float4*>(&stA[u][4 * q4]) = __ldcg(reinterpret_cast<const float4*>(p.dA + o));
+                    *reinterpret_cast<float4*>(&stB[u][4 * q4]) = __ldcg(reinterpret_cast<const float4*>(p.dB + o));
+                }
+                __syncthreads();
+                if (warp == 0)
+                    for (int v = 0; v < cnt; ++v) cin = __fmaf_rn(stA[v][lane], cin, stB[v][lane]);
+                __syncthreads();
+            }
+            if (warp == 0) publish();
+            __syncthreads();
+        }
         // ---- phase 4: states of this thread's segment from its exclusive prefix
         tile_outputs<GATED>(sa, sb, rows, carry, cfin, EA, EB, p.s_out + ((size_t)bi * p.T + t0) * p.N + n0, p.N,
                             p.s_out != nullptr && n0 + 4 * quad < p.N);

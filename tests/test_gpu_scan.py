@@ -277,6 +277,24 @@ def test_lookback_forced_without_workspace_is_nomem(sr, ctx):
     assert bool((out == 7.0).all())                     # untouched
 
 
+def test_auto_choice_by_channel_count(sr, ctx):
+    """With a workspace set, the automatic choice chunks along T only when the
+    channels leave most SMs idle: one channel tile takes reduce-then-scan, eight
+    batches of 2048 channels stay on the sequential kernel.  The two kernels
+    round differently, so the bits show which one ran."""
+    auto, seq, rs = sr.SN_SCAN_KERNEL_AUTO, sr.SN_SCAN_KERNEL_SEQUENTIAL, sr.SN_SCAN_KERNEL_REDUCE_SCAN
+    for (B, T, N), want in (((1, 4096, 32), rs), ((8, 1024, 2048), seq)):
+        a, b, _, s0 = _inputs(B, T, N, 61)
+        ctx.ensure_workspace(B, T, N)
+        outs = {}
+        for k in (auto, seq, rs):
+            ctx.set_option(sr.SN_OPT_SCAN_KERNEL, k)
+            outs[k] = _run(ctx, "fma", a, b, s0)[0]
+        assert not np.array_equal(outs[seq], outs[rs])
+        assert np.array_equal(outs[auto], outs[want])
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, auto)
+
+
 # ------------------------------------------------------------------ validation
 def test_invalid_arguments_leave_outputs_untouched(sr, ctx):
     h = ctx.handle

@@ -175,3 +175,20 @@ def test_chunked_backward_optional_outputs_and_auto(sr, ctx):
     ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
     ga2, gb2, g02 = _run(ctx, "fma", x, s, s0, gs, gf)
     assert np.array_equal(ga2, ga) and np.array_equal(gb2, gb) and np.array_equal(g02, g0)
+
+
+def test_auto_keeps_sequential_for_many_channels(sr, ctx):
+    """Eight batches of 2048 channels give the sequential reverse scan enough
+    CTAs: with a workspace set, the automatic choice still takes it (its bits,
+    which differ from the chunked path's)."""
+    B, T, N = 8, 1024, 2048
+    x, s0, gs, gf = _case(B, T, N, 29)
+    s = _forward32("fma", x, s0)
+    ctx.ensure_workspace(B, T, N)
+    outs = {}
+    for k in (sr.SN_SCAN_KERNEL_AUTO, sr.SN_SCAN_KERNEL_SEQUENTIAL, sr.SN_SCAN_KERNEL_REDUCE_SCAN):
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, k)
+        outs[k] = _run(ctx, "fma", x, s, s0, gs, gf)[0]
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    assert not np.array_equal(outs[sr.SN_SCAN_KERNEL_SEQUENTIAL], outs[sr.SN_SCAN_KERNEL_REDUCE_SCAN])
+    assert np.array_equal(outs[sr.SN_SCAN_KERNEL_AUTO], outs[sr.SN_SCAN_KERNEL_SEQUENTIAL])
