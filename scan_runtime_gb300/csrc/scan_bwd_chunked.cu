@@ -70,8 +70,11 @@ bwd_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
         fence_mbar_init();
     }
     __syncthreads();
-    // tiles column-major within a chunk row
+    // tiles column-major within a chunk row; the output pass visits them in the
+    // opposite order, so it starts on the tiles the aggregate pass read last,
+    // which are still in L2
     auto tile_coords = [&](int ti, int& k, int& bi, int& cb) {
+        if (OUT) ti = p.ntiles - 1 - ti;
         k = ti / p.nbcb;
         const int r = ti - k * p.nbcb;
         bi = r / p.ncb;

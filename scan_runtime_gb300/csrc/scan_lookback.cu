@@ -369,8 +369,11 @@ scan_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         fence_mbar_init();
     }
     __syncthreads();
-    // tiles column-major within a chunk row, as the look-back kernel
+    // tiles column-major within a chunk row, as the look-back kernel; the output pass visits them in the
+    // opposite order, so it starts on the tiles the aggregate pass read last,
+    // which are still in L2
     auto tile_coords = [&](int ti, int& k, int& bi, int& cb) {
+        if (OUT) ti = p.ntiles - 1 - ti;
         k = ti / p.nbcb;
         const int r = ti - k * p.nbcb;
         bi = r / p.ncb;
