@@ -730,6 +730,7 @@ PROFILE_CASES = {
     "scan_seq": "sequential scan (FMA), B=8 T=2048 N=2048 (402 MB moved, > L2)",
     "scan_seq_full": "sequential scan (FMA), full workload B=8 T=8192 N=2048 (1.61 GB moved)",
     "scan_lookback": "look-back scan (FMA), B=8 T=2048 N=2048",
+    "scan_few_channels": "reduce-then-scan (FMA, the automatic choice), few channels B=1 T=262144 N=64",
     "scan_bwd_fma": "reverse scan (FMA form), B=8 T=2048 N=2048 (20 B per element)",
     "scan_bwd_gated": "reverse scan (gated form), B=8 T=2048 N=2048 (24 B per element)",
     "gla": "diag per-key, full GLA workload B=4 T=4096 H=4 dk=dv=128",
@@ -757,7 +758,15 @@ def run_profile_case(args):
     s = torch.cuda.Stream(dev)
     name = args.profile_case
     h = ctx.handle
-    if name.startswith("scan_bwd"):
+    if name == "scan_few_channels":
+        B, T, N = 1, 262144, 64
+        x = synth.scan_inputs(B, T, N, large=True, cid=6, device=dev)
+        so = torch.empty((B, T, N), device=dev)
+        sf = torch.empty((B, N), device=dev)
+        ctx.ensure_workspace(B, T, N)
+        fn = lambda: sr.sn_scan_fma(h, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
+        nbytes = scan_bytes(B, T, N)
+    elif name.startswith("scan_bwd"):
         B, T, N = 8, 2048, 2048
         x = synth.scan_inputs(B, T, N, large=True, device=dev)
         so = torch.empty((B, T, N), device=dev)

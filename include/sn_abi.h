@@ -155,9 +155,12 @@ void sn_ctx_free(SnCtx* ctx);
 sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes);
 
 /* Workspace bytes the chunked scans need for this problem (op =
- * SN_OP_SCAN_FMA or SN_OP_SCAN_GATED): with tiles = B * ceil(N / 32) *
- * ceil(T / 128), a flag word per tile rounded up to 256 bytes plus 512 bytes
- * per tile; 0 for an op that needs none, -1 on invalid arguments. */
+ * SN_OP_SCAN_FMA or SN_OP_SCAN_GATED): with columns = B * ceil(N / 32),
+ * chunks = ceil(T / 128) and tiles = columns * chunks, a flag word per tile
+ * rounded up to 256 bytes, plus the larger of 512 bytes per tile and
+ * columns * (1536 * ceil(chunks / 4) + 128) bytes (the second only for
+ * sequences of fewer than ten chunks); 0 for an op that needs none, -1 on
+ * invalid arguments. */
 int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N);
 
 /* Return and clear the first device-side error recorded in the context's

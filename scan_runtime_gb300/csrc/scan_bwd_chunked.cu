@@ -44,7 +44,7 @@ struct BwdPassParams {
     float* da;
     float* dbu;
     float* ds0;
-    float* dA;           // [column][chunk][channel] aggregates, then the chain's h_k in dC
+    float* dA;           // aggregates at agg_index (chunks in groups of four), then the chain's h_k in dC
     float* dB;
     float* dC;
     SnDevStatus* st;
@@ -132,7 +132,8 @@ bwd_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
         float4 EA, EB;
         tile_local_scan<false, true>(sa + LB_NC, sg, rows, wA, wB, EA, EB);   // alpha_t = a_{t+1}
         const size_t col = (size_t)bi * p.ncb + cb;
-        const size_t me = (col * p.nchunks + k) * LB_NC + lane;
+        const int nq = chunk_quads(p.nchunks);
+        const size_t me = agg_index(col, nq, k, lane);
         if (warp == 0) {
             if (!OUT) {
                 float CA, CB;
@@ -143,7 +144,7 @@ bwd_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
                 const int n = n0 + lane;
                 // g entering the tile from above (h_{k+1}), and the tile's own first g (h_k)
                 carry[lane] = k == p.nchunks - 1 ? ((p.gf != nullptr && n < p.N) ? p.gf[(size_t)bi * p.N + n] : 0.f)
-                                                 : __ldg(p.dC + me + LB_NC);
+                                                 : __ldg(p.dC + agg_index(col, nq, k + 1, lane));
                 cfin[lane] = __ldg(p.dC + me);
             }
         }
@@ -206,8 +207,9 @@ bool scan_backward_chunked_supported(const BwdArgs& x) {
 }
 
 int64_t scan_backward_chunked_ws_bytes(int B, int T, int N) {
-    const int64_t tiles = lookback_flag_count(B, T, N);
-    return tiles * 3 * LB_NC * 4;
+    // A, B and C arrays at agg_index: per column, chunks in groups of four
+    const int64_t nbcb = (int64_t)B * ((N + LB_NC - 1) / LB_NC);
+    return 3 * nbcb * chunk_quads((T + LB_TC - 1) / LB_TC) * LB_NC * 4 * 4;
 }
 
 cudaError_t launch_scan_backward_chunked(const BwdArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
@@ -233,9 +235,10 @@ cudaError_t launch_scan_backward_chunked(const BwdArgs& x, bool gated, void* ws,
     p.dbu = x.dbu;
     p.ds0 = x.ds0;
     const int64_t tiles = p.ntiles;
+    const int64_t arr = (int64_t)p.nbcb * chunk_quads(p.nchunks) * LB_NC * 4;   // floats per array
     p.dA = static_cast<float*>(ws);
-    p.dB = p.dA + tiles * LB_NC;
-    p.dC = p.dB + tiles * LB_NC;
+    p.dB = p.dA + arr;
+    p.dC = p.dB + arr;
     p.st = st;
     p.wait_ns = wait_ns;
 
@@ -254,7 +257,7 @@ cudaError_t launch_scan_backward_chunked(const BwdArgs& x, bool gated, void* ws,
                                                                                                           mu, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const ChainParams cp{p.N, p.ncb, p.nchunks, x.gf, p.dA, p.dB, p.dC, st, wait_ns};
+    const ChainParams cp{p.N, p.ncb, p.nchunks, x.gf, p.dA, p.dB, p.dC, nullptr, st, wait_ns};
     scan_chain<true><<<(unsigned)p.nbcb, 32, CHAIN_SMEM, stream>>>(cp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

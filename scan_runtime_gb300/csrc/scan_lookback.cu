@@ -36,14 +36,21 @@ int64_t lookback_flag_count(int B, int T, int N) {
 
 // Look-back workspace: [ flags: u32 per tile | A | B: f32 per channel and tile |
 // carry words: u64 per channel and tile ].  The reduce-then-scan path uses the
-// same region as three f32 arrays after the flags.
+// region after the flags for its A, B and C arrays (chunks in groups of four,
+// agg_index) and the columns' initial carries; the larger need sets the size.
 int64_t lookback_cw_offset(int B, int T, int N) {
     const int64_t tiles = lookback_flag_count(B, T, N);
     return ((tiles * 4 + 255) / 256) * 256 + tiles * 2 * LB_NC * 4;
 }
 
 int64_t lookback_ws_bytes(int B, int T, int N) {
-    return lookback_cw_offset(B, T, N) + lookback_flag_count(B, T, N) * LB_NC * 8;
+    const int64_t tiles = lookback_flag_count(B, T, N);
+    const int64_t flag_bytes = ((tiles * 4 + 255) / 256) * 256;
+    const int64_t nbcb = (int64_t)B * ((N + LB_NC - 1) / LB_NC);
+    const int64_t nq = chunk_quads((T + LB_TC - 1) / LB_TC);
+    const int64_t lookback = tiles * (2 * LB_NC * 4 + LB_NC * 8);
+    const int64_t reduce_scan = (3 * nbcb * nq * LB_NC * 4 + nbcb * LB_NC) * 4;   // A, B, C groups + cin0
+    return flag_bytes + std::max(lookback, reduce_scan);
 }
 
 struct LookbackParams {
@@ -222,22 +229,18 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                         }
                     }
                     if (!timed_out) {
-                        if (m < 0) {
-                            cin = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
-                        } else {
-                            // chunk m's flag announced its carry; the carry words
-                            // themselves may land a moment later
-                            const unsigned long long* cm = p.cw + ((size_t)m * p.nbcb + base) * LB_NC + lane;
-                            while (true) {
-                                w = ld_relaxed_gpu_u64(cm);
-                                if (__all_sync(0xffffffffu, (uint32_t)(w >> 32) == want_c)) break;
-                                if (give_up()) {
-                                    timed_out = true;
-                                    break;
-                                }
+                        // chunk m's flag announced its carry; the carry words
+                        // themselves may land a moment later
+                        const unsigned long long* cm = p.cw + ((size_t)m * p.nbcb + base) * LB_NC + lane;
+                        while (true) {
+                            w = ld_relaxed_gpu_u64(cm);
+                            if (__all_sync(0xffffffffu, (uint32_t)(w >> 32) == want_c)) break;
+                            if (give_up()) {
+                                timed_out = true;
+                                break;
                             }
-                            cin = __uint_as_float((uint32_t)w);
                         }
+                        cin = __uint_as_float((uint32_t)w);
                     }
                     __syncwarp();
                     if (timed_out) {
@@ -334,7 +337,9 @@ bool lookback_supported(const ScanArgs& x) { return scan_tma_ok(x); }
 // The local scan, the aggregates and the carry chain are the look-back
 // kernel's own operations in the same order, so both paths give the same bits.
 // a and b are read twice (20 bytes per element instead of 12).
-// Workspace: the look-back's A, B and C arrays, indexed [column][chunk][channel].
+// Workspace: A, B and C arrays at agg_index (per column, chunks in groups of
+// four), then the columns' initial carries as the chain read them (the output
+// pass takes its first chunk's carry there, since s_final may be s0's buffer).
 namespace {
 
 constexpr int PASS_STAGES = 2;                    // tiles in flight per CTA of the two passes (3 CTAs
@@ -349,6 +354,7 @@ struct PassParams {
     float* dA;
     float* dB;
     float* dC;
+    float* cin0;         // [column][channel] initial carries, written by the chain
     SnDevStatus* st;
     uint64_t wait_ns;
 };
@@ -416,7 +422,8 @@ scan_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         float4 EA, EB;
         tile_local_scan<GATED>(sa, sb, rows, wA, wB, EA, EB);
         const size_t col = (size_t)bi * p.ncb + cb;
-        const size_t me = (col * p.nchunks + k) * LB_NC + lane;
+        const int nq = chunk_quads(p.nchunks);
+        const size_t me = agg_index(col, nq, k, lane);
         if (warp == 0) {
             float CA, CB;
             tile_aggregate(wA, wB, lane, CA, CB);
@@ -425,8 +432,9 @@ scan_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                 p.dB[me] = CB;
             } else {
                 const int n = n0 + lane;
-                const float cin = k == 0 ? ((p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f)
-                                         : __ldg(p.dC + me - LB_NC);
+                // s0 itself is not read here: a call may write its final states over it
+                const float cin =
+                    k == 0 ? __ldg(p.cin0 + col * LB_NC + lane) : __ldg(p.dC + agg_index(col, nq, k - 1, lane));
                 const float Ck = __fmaf_rn(CA, cin, CB);
                 carry[lane] = cin;
                 cfin[lane] = Ck;
@@ -463,9 +471,11 @@ cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnD
     p.s_out = x.s_out;
     const int64_t tiles = p.ntiles;
     const int64_t flag_bytes = ((tiles * 4 + 255) / 256) * 256;
+    const int64_t arr = (int64_t)p.nbcb * chunk_quads(p.nchunks) * LB_NC * 4;   // floats per array
     p.dA = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + flag_bytes);
-    p.dB = p.dA + tiles * LB_NC;
-    p.dC = p.dB + tiles * LB_NC;
+    p.dB = p.dA + arr;
+    p.dC = p.dB + arr;
+    p.cin0 = p.dC + arr;             // nbcb * 32 floats
     p.st = st;
     p.wait_ns = wait_ns;
 
@@ -482,7 +492,7 @@ cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnD
     k_agg<<<grid, LB_THREADS, PASS_SMEM, stream>>>(ma, mb, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const ChainParams cp{p.N, p.ncb, p.nchunks, x.s0, p.dA, p.dB, p.dC, st, wait_ns};
+    const ChainParams cp{p.N, p.ncb, p.nchunks, x.s0, p.dA, p.dB, p.dC, p.cin0, st, wait_ns};
     scan_chain<false><<<(unsigned)p.nbcb, 32, CHAIN_SMEM, stream>>>(cp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

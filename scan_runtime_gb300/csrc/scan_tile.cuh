@@ -129,19 +129,30 @@ __device__ __forceinline__ void tile_outputs(const float* sa, const float* sb, i
     }
 }
 
+// Aggregates (A_k, B_k) and carries C_k of the chunked scans' passes, per
+// column (channel tile) in groups of four chunks: group g of column col holds
+// [channel][chunk 4g .. 4g + 3], 16 bytes per channel.  A column holds
+// chunk_quads(nchunks) groups; the slots past the last chunk are padding.
+__host__ __device__ __forceinline__ int chunk_quads(int nchunks) { return (nchunks + 3) >> 2; }
+__host__ __device__ __forceinline__ size_t agg_index(size_t col, int nq, int k, int ch) {
+    return ((col * nq + (k >> 2)) * LB_NC + ch) * 4 + (k & 3);
+}
+
 // Carries of the chunked scans, one warp per column (lane = channel):
 //   forward (REV = false): C_k = fma(A_k, C_{k-1}, B_k), k = 0 .. nchunks - 1, C_{-1} = init;
 //   reverse (REV = true):  C_k = fma(A_k, C_{k+1}, B_k), k = nchunks - 1 .. 0, C_{nchunks} = init;
-// with (A_k, B_k) and C_k at [column][chunk][channel].  The column's aggregates arrive in blocks of
-// CHAIN_BLK chunks by bulk copies, CHAIN_STAGES blocks in flight.  Within a
-// full block the aggregates of CHAIN_U chunks are read into registers one
-// batch ahead of the FMAs that consume them (two batches in turn, all offsets
-// fixed), so a step costs two shared loads, the FMA and a store, and the
-// dependent chain is not held up by load latency.  The carries are stored as
-// global stores (st.global), which cannot alias the shared-memory operands.
-constexpr int CHAIN_BLK = 128;
+// with (A_k, B_k) and C_k at agg_index.  The column's aggregates arrive in
+// blocks of CHAIN_BLK chunks by bulk copies, CHAIN_STAGES blocks in flight.
+// A lane reads four chunks of its channel with one 16-byte shared load per
+// array and stores their four carries with one 16-byte global store; within
+// a full block the groups are read into registers one batch ahead of the
+// FMAs that consume them (two batches in turn, all offsets fixed), so the
+// dependent chain is held up neither by load latency nor by a store per
+// step.  The stores are global (st.global), so they cannot alias the
+// shared-memory operands.
+constexpr int CHAIN_BLK = 128;                                    // chunks per block (32 groups)
 constexpr int CHAIN_STAGES = 4;
-constexpr int CHAIN_U = 16;
+constexpr int CHAIN_QB = 4;                                       // groups per register batch
 constexpr uint32_t CHAIN_BLK_FLOATS = CHAIN_BLK * LB_NC;          // one block of one array
 constexpr size_t CHAIN_SMEM = (size_t)CHAIN_STAGES * 2 * CHAIN_BLK_FLOATS * 4 + CHAIN_STAGES * 8 + 16;
 
@@ -151,27 +162,48 @@ struct ChainParams {
     const float* dA;
     const float* dB;
     float* dC;
+    float* cin0;         // [column][channel]: the initial carry as read, for the output pass (or NULL)
     SnDevStatus* st;
     uint64_t wait_ns;
 };
 
+// Four steps of the chain over one group, in visiting order; returns the
+// group's carries in chunk order.
+template <bool REV>
+__device__ __forceinline__ float4 chain_group(float4 a, float4 b, float& c) {
+    float4 r;
+    if (!REV) {
+        c = __fmaf_rn(a.x, c, b.x); r.x = c;
+        c = __fmaf_rn(a.y, c, b.y); r.y = c;
+        c = __fmaf_rn(a.z, c, b.z); r.z = c;
+        c = __fmaf_rn(a.w, c, b.w); r.w = c;
+    } else {
+        c = __fmaf_rn(a.w, c, b.w); r.w = c;
+        c = __fmaf_rn(a.z, c, b.z); r.z = c;
+        c = __fmaf_rn(a.y, c, b.y); r.y = c;
+        c = __fmaf_rn(a.x, c, b.x); r.x = c;
+    }
+    return r;
+}
+
 template <bool REV>
 __global__ void __launch_bounds__(32) scan_chain(const ChainParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    float* bufs = reinterpret_cast<float*>(smem);                 // [stage][A | B][CHAIN_BLK][LB_NC]
+    float* bufs = reinterpret_cast<float*>(smem);                 // [stage][A | B][CHAIN_BLK / 4][LB_NC][4]
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)CHAIN_STAGES * 2 * CHAIN_BLK_FLOATS * 4);
     const int lane = threadIdx.x;
     const size_t col = blockIdx.x;
     const int bi = (int)(col / p.ncb), cb = (int)(col % p.ncb);
     const int n = cb * LB_NC + lane;
-    const size_t colbase = col * p.nchunks * LB_NC;
+    const int nq = chunk_quads(p.nchunks);
+    const size_t colbase = agg_index(col, nq, 0, 0);
     const int nblk = (p.nchunks + CHAIN_BLK - 1) / CHAIN_BLK;
     // the j-th block visited (0-based) is block blk_of(j); stage j % CHAIN_STAGES
     auto blk_of = [&](int j) { return REV ? nblk - 1 - j : j; };
     auto issue = [&](int j) {   // lane 0
         const int blk = blk_of(j);
         const int c0 = blk * CHAIN_BLK, st = j % CHAIN_STAGES;
-        const uint32_t bytes = (uint32_t)min(CHAIN_BLK, p.nchunks - c0) * LB_NC * 4;
+        const uint32_t bytes = (uint32_t)chunk_quads(min(CHAIN_BLK, p.nchunks - c0)) * LB_NC * 16;
         mbar_arrive_expect_tx(&bar[st], 2 * bytes);
         bulk_load(bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS, p.dA + colbase + (size_t)c0 * LB_NC, bytes, &bar[st]);
         bulk_load(bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS + CHAIN_BLK_FLOATS, p.dB + colbase + (size_t)c0 * LB_NC,
@@ -185,59 +217,64 @@ __global__ void __launch_bounds__(32) scan_chain(const ChainParams p) {
     }
     issued = __shfl_sync(0xffffffffu, issued, 0);
     float c = (p.init != nullptr && n < p.N) ? p.init[(size_t)bi * p.N + n] : 0.f;
+    // The output pass takes its first chunk's carry from here, not from init:
+    // init may be the buffer that pass writes its final states to.
+    if (p.cin0 != nullptr) p.cin0[col * LB_NC + lane] = c;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
         const int blk = blk_of(j);
         const int st = j % CHAIN_STAGES;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar[st], (uint32_t)(j / CHAIN_STAGES) & 1, p.wait_ns));
         if (!ok) break;
-        const float* sA = bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS + lane;
-        const float* sB = sA + CHAIN_BLK_FLOATS;
-        float* dC = p.dC + colbase + (size_t)blk * CHAIN_BLK * LB_NC + lane;
+        const float4* sA = reinterpret_cast<const float4*>(bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS) + lane;
+        const float4* sB = sA + CHAIN_BLK_FLOATS / 4;
+        float4* dC = reinterpret_cast<float4*>(p.dC + colbase + (size_t)blk * CHAIN_BLK * LB_NC) + lane;
         const int cnt = min(CHAIN_BLK, p.nchunks - blk * CHAIN_BLK);
-        // step q of the block (0-based, in visiting order) is chunk row ix(q) of it
-#define SN_CHAIN_IX(q) (REV ? CHAIN_BLK - 1 - (q) : (q))
+        // group q of the block (0-based, in visiting order) is group gx(q) of it
+#define SN_CHAIN_GX(q) (REV ? CHAIN_BLK / 4 - 1 - (q) : (q))
         if (cnt == CHAIN_BLK) {
             // a full block: two register batches in turn, every offset fixed
-            float a0[CHAIN_U], b0[CHAIN_U], a1[CHAIN_U], b1[CHAIN_U];
+            constexpr int NG = CHAIN_BLK / 4;
+            float4 a0[CHAIN_QB], b0[CHAIN_QB], a1[CHAIN_QB], b1[CHAIN_QB];
 #pragma unroll
-            for (int u = 0; u < CHAIN_U; ++u) {
-                a0[u] = sA[SN_CHAIN_IX(u) * LB_NC];
-                b0[u] = sB[SN_CHAIN_IX(u) * LB_NC];
+            for (int u = 0; u < CHAIN_QB; ++u) {
+                a0[u] = sA[SN_CHAIN_GX(u) * LB_NC];
+                b0[u] = sB[SN_CHAIN_GX(u) * LB_NC];
             }
 #pragma unroll
-            for (int i0 = 0; i0 < CHAIN_BLK; i0 += 2 * CHAIN_U) {
+            for (int q0 = 0; q0 < NG; q0 += 2 * CHAIN_QB) {
 #pragma unroll
-                for (int u = 0; u < CHAIN_U; ++u) {
-                    a1[u] = sA[SN_CHAIN_IX(i0 + CHAIN_U + u) * LB_NC];
-                    b1[u] = sB[SN_CHAIN_IX(i0 + CHAIN_U + u) * LB_NC];
+                for (int u = 0; u < CHAIN_QB; ++u) {
+                    a1[u] = sA[SN_CHAIN_GX(q0 + CHAIN_QB + u) * LB_NC];
+                    b1[u] = sB[SN_CHAIN_GX(q0 + CHAIN_QB + u) * LB_NC];
                 }
 #pragma unroll
-                for (int u = 0; u < CHAIN_U; ++u) {
-                    c = __fmaf_rn(a0[u], c, b0[u]);
-                    __stcg(&dC[SN_CHAIN_IX(i0 + u) * LB_NC], c);
-                }
-                if (i0 + 2 * CHAIN_U < CHAIN_BLK) {
+                for (int u = 0; u < CHAIN_QB; ++u)
+                    __stcg(&dC[SN_CHAIN_GX(q0 + u) * LB_NC], chain_group<REV>(a0[u], b0[u], c));
+                if (q0 + 2 * CHAIN_QB < NG) {
 #pragma unroll
-                    for (int u = 0; u < CHAIN_U; ++u) {
-                        a0[u] = sA[SN_CHAIN_IX(i0 + 2 * CHAIN_U + u) * LB_NC];
-                        b0[u] = sB[SN_CHAIN_IX(i0 + 2 * CHAIN_U + u) * LB_NC];
+                    for (int u = 0; u < CHAIN_QB; ++u) {
+                        a0[u] = sA[SN_CHAIN_GX(q0 + 2 * CHAIN_QB + u) * LB_NC];
+                        b0[u] = sB[SN_CHAIN_GX(q0 + 2 * CHAIN_QB + u) * LB_NC];
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < CHAIN_U; ++u) {
-                    c = __fmaf_rn(a1[u], c, b1[u]);
-                    __stcg(&dC[SN_CHAIN_IX(i0 + CHAIN_U + u) * LB_NC], c);
-                }
+                for (int u = 0; u < CHAIN_QB; ++u)
+                    __stcg(&dC[SN_CHAIN_GX(q0 + CHAIN_QB + u) * LB_NC], chain_group<REV>(a1[u], b1[u], c));
             }
         } else {
-            for (int q = 0; q < cnt; ++q) {   // the partial block (the sequence's last)
+            // the partial block (the sequence's last): one chunk at a time
+            const float* fA = bufs + (size_t)st * 2 * CHAIN_BLK_FLOATS;
+            const float* fB = fA + CHAIN_BLK_FLOATS;
+            float* fC = p.dC + colbase + (size_t)blk * CHAIN_BLK * LB_NC;
+            for (int q = 0; q < cnt; ++q) {
                 const int i = REV ? cnt - 1 - q : q;
-                c = __fmaf_rn(sA[i * LB_NC], c, sB[i * LB_NC]);
-                __stcg(&dC[(size_t)i * LB_NC], c);
+                const int o = ((i >> 2) * LB_NC + lane) * 4 + (i & 3);
+                c = __fmaf_rn(fA[o], c, fB[o]);
+                __stcg(&fC[o], c);
             }
         }
-#undef SN_CHAIN_IX
+#undef SN_CHAIN_GX
         __syncwarp();                                 // the stage is read
         if (lane == 0 && issued < nblk) issue(issued);
         if (issued < nblk) ++issued;

@@ -68,6 +68,7 @@ cudaError_t set_smem_attr_once(const void* kern, size_t bytes);
 // Resident CTAs per SM of `kern` on the current device (cached per device).
 cudaError_t occupancy_once(const void* kern, int threads, size_t smem, int* out);
 
+
 // tensor-map encoder (driver entry point fetched through the runtime)
 bool encode_tiled(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
                   const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box, bool swizzle128 = false);

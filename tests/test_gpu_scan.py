@@ -277,6 +277,28 @@ def test_lookback_forced_without_workspace_is_nomem(sr, ctx):
     assert bool((out == 7.0).all())                     # untouched
 
 
+@pytest.mark.parametrize("kernel", ["lookback", "reduce_scan"])
+@pytest.mark.parametrize("shape", [(1, 70000, 64), (2, 1000, 64), (1, 256, 32)])
+def test_chunked_in_place_continuation(sr, ctx, kernel, shape):
+    """s_final may be s0's buffer.  The chunked kernels read s0 before any tile
+    writes a final state (the first chunk only; the output pass reads the
+    chain's copy), so in place gives the out-of-place bits."""
+    B, T, N = shape
+    ctx.ensure_workspace(B, T, N)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK if kernel == "lookback"
+                   else sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    a, b, _, s0 = _inputs(B, T, N, 71 + T % 7)
+    a, b, s0 = a.cuda(), b.cuda(), s0.cuda()
+    so1, sf1 = torch.empty_like(a), torch.empty_like(s0)
+    assert sr.sn_scan_fma(ctx.handle, B, T, N, a, b, s0, sf1, so1) == sr.SN_OK
+    st = s0.clone()
+    so2 = torch.empty_like(a)
+    assert sr.sn_scan_fma(ctx.handle, B, T, N, a, b, st, st, so2) == sr.SN_OK
+    torch.cuda.synchronize()
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    assert torch.equal(so1, so2) and torch.equal(sf1, st)
+
+
 def test_auto_choice_by_channel_count(sr, ctx):
     """With a workspace set, the automatic choice chunks along T only when the
     channels leave most SMs idle: one channel tile takes reduce-then-scan, eight
