@@ -162,7 +162,7 @@ cudaError_t run_decode_kind(const RecurArgs& x, const DecodeParams& p, int sm_co
     if constexpr (KIND == RK_DELTA) {
         return run_decode_rows<KIND, 8>(x, p, sm_count, s);
     } else {
-        if (seq_warps(x, 8, 4) >= 4 * (int64_t)sm_count) return run_decode_rows<KIND, 8>(x, p, sm_count, s);
+        if (diag_eight_rows(x, sm_count)) return run_decode_rows<KIND, 8>(x, p, sm_count, s);
         return run_decode_rows<KIND, 4>(x, p, sm_count, s);
     }
 }

@@ -6,12 +6,11 @@
 namespace sn {
 
 namespace {
-// 8 rows per lane when the problem yields at least 4 warps per SM; otherwise
-// 4 rows per lane, which doubles the warps of a small problem.
+// 8 or 4 rows per lane by diag_eight_rows (recur_seq.cuh).
 template <int KIND>
 cudaError_t diag_dispatch(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
                           cudaStream_t stream) {
-    const bool many = seq_warps(x, 8, 4) >= 4 * (int64_t)sm_count;
+    const bool many = diag_eight_rows(x, sm_count);
     if (x.dk == 128)
         return many ? run_seq_width<KIND, 128, 8, 4>(x, st, wait_ns, sm_count, force_w, stream)
                     : run_seq_width<KIND, 128, 4, 4>(x, st, wait_ns, sm_count, force_w, stream);

@@ -12,7 +12,7 @@ namespace {
 template <int KIND>
 cudaError_t gated_dispatch(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
                            cudaStream_t stream) {
-    const bool many = seq_warps(x, 8, 4) >= 4 * (int64_t)sm_count;
+    const bool many = diag_eight_rows(x, sm_count);
     if (x.dk == 128)
         return many ? run_seq_width<KIND, 128, 8, 4>(x, st, wait_ns, sm_count, force_w, stream)
                     : run_seq_width<KIND, 128, 4, 4>(x, st, wait_ns, sm_count, force_w, stream);

@@ -453,4 +453,14 @@ inline int64_t seq_warps(const RecurArgs& x, int R, int C) {
     return (int64_t)x.B * x.H * (x.dv / C) * (x.dk / R) / 32;
 }
 
+// Rows per lane of the diagonal-decay kinds: 8 when the problem yields at
+// least DIAG_R8_WARPS warps per SM with 8 rows, else 4 rows, which doubles the
+// warps of a small problem (measured at B4 H4 128x128, 256 warps with 8 rows:
+// GLA 0.346 ms with 4 rows, 0.498 ms with 8).  The single-step decode follows
+// the same rule, so a decode step has the bits of a one-step sequence call.
+constexpr int DIAG_R8_WARPS = 4;
+inline bool diag_eight_rows(const RecurArgs& x, int sm_count) {
+    return seq_warps(x, 8, 4) >= (int64_t)DIAG_R8_WARPS * sm_count;
+}
+
 }  // namespace sn
