@@ -127,6 +127,13 @@ def test_workspace_bytes(abi):
     tiles = 8 * (2048 // 32) * (8192 // 128)
     # flags, the A and B aggregates (f32) and the tagged carry words (u64)
     assert nb == ((tiles * 4 + 255) // 256) * 256 + tiles * (2 * 32 * 4 + 32 * 8)
+    # fewer than ten chunks: the reduce-then-scan arrays (chunks in groups of
+    # four per column, three arrays, plus the columns' initial carries) set it
+    cols, chunks = 2 * (64 // 32), 5
+    flags = ((cols * chunks * 4 + 255) // 256) * 256
+    rs = 3 * cols * ((chunks + 3) // 4) * 32 * 4 * 4 + cols * 32 * 4
+    assert rs > cols * chunks * 512
+    assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 2, 5 * 128, 64) == flags + rs
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_GATED, 1, 1, 1) > 0
     assert abi.sn_workspace_bytes(99, 1, 1, 1) == -1
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 0, 1, 1) == -1
