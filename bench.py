@@ -40,7 +40,12 @@ def scan_bytes(B, T, N, has_s0=True):
     return 12 * B * T * N + (8 if has_s0 else 4) * B * N
 
 
-# per-workload algorithmic bytes and flops ("Roofline accounting")
+# Per-workload algorithmic bytes and flops: every input read once and every
+# output written once per token and head (q, k, per-key decays, v in; o out;
+# per-head scalars 4 bytes; grouped k and q shared by H / G heads), plus the
+# final state written (and, for a decode, the initial state read).  Flops per
+# state entry and step: diag 5 (k v product, decay FMA, readout FMA), delta 6
+# (two dot-product FMAs and the update FMA), RWKV-7 7 (plus the decay).
 def matrix_cost(name):
     c = synth.CONFIGS[name]
     B, T, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
