@@ -80,8 +80,7 @@ scan_lookback(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     __shared__ int s_fold[2];                       // chunks [lo, hi) of a staged fold; hi = 0: none
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = lane & 7, sub = lane >> 3;
-    const int seg = warp * 4 + sub;                 // 0..31, rows [seg*LB_SEG, (seg+1)*LB_SEG)
+    const int quad = lane & 7;
 
     // The launch epoch lives in device memory: lb_epoch holds the last launch's
     // (0 = none yet), this launch uses the next one, and the launch's last CTA
