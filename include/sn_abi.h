@@ -27,9 +27,11 @@
  *     default stream.  Calls are asynchronous: they validate, enqueue the
  *     kernel on `stream` and return.  Outputs are valid once the stream has
  *     reached that point;
- *   - compute calls never allocate device memory.  The only device memory the
- *     library owns is a 256-byte status block per context (allocated by
- *     sn_ctx_create) plus what the caller hands over with
+ *   - compute calls never allocate device memory and never create streams or
+ *     events.  The only device memory the library owns is a 256-byte status
+ *     block per context (allocated by sn_ctx_create, which also creates the
+ *     context's side streams and events) and the static scratch array of
+ *     sn_scan_lookback_noalloc; the caller hands over the rest with
  *     sn_ctx_set_workspace;
  *   - an initial-state pointer may be NULL (zero initial state); a final-state
  *     or per-step output pointer may be NULL (not written);
@@ -104,7 +106,8 @@ typedef int32_t sn_status;
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
 #define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
 #define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA;
-                                      a width the value dimension does not divide fails with SN_E_DEVICE */
+                                      a width whose CTA columns the value dimension does not divide makes
+                                      the sequence-kernel call fail with SN_E_INVAL before any launch */
 #define SN_OPT_DELTA_SEGMENTS   7  /* sn_recur_delta_chunked: 0 auto (default), or 1..8 segments of the
                                       chunk sequence run as a pipeline (same bits for every value) */
 
@@ -137,7 +140,10 @@ const char* sn_status_str(sn_status s);
 /* ---------------------------------------------------------------- context */
 
 /* Create a context bound to CUDA device `device`.  Allocates the context's
- * 256-byte device status block on that device.  Errors: SN_E_INVAL (NULL
+ * 256-byte device status block on that device and creates the CUDA objects
+ * the pipelined chunked delta rule runs on (three non-blocking streams and 20
+ * events, see sn_recur_delta_chunked), so that no compute call creates CUDA
+ * objects.  sn_ctx_free releases all of them.  Errors: SN_E_INVAL (NULL
  * out_ctx, bad device index), SN_E_UNSUPPORTED (device is not sm_103),
  * SN_E_DEVICE (CUDA failure).  On error *out_ctx is set to NULL. */
 sn_status sn_ctx_create(int32_t device, SnCtx** out_ctx);
@@ -342,7 +348,8 @@ int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_
  * SN_E_NOMEM), which the call overwrites.
  * Streams: for more than a few chunks the call splits the sequence into
  * segments (SN_OPT_DELTA_SEGMENTS) and runs the chain of one segment beside
- * the preparation of the next on two side streams the context owns.  The
+ * the preparation of the next on side streams the context created with it
+ * (sn_ctx_create); the call itself creates no stream or event.  The
  * side streams wait for `stream`'s earlier work and `stream` waits for them
  * before its later work, so to the caller the call is ordered on `stream`
  * like any other (also under stream capture).  A context is not for use from
@@ -408,10 +415,13 @@ sn_status sn_readout_dskip(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t 
  * out during this call.
  *
  * The first call on a device sets the device up (it looks up the array's
- * device address and clears its flag area with a cudaMemsetAsync on `stream`),
- * so that first call should come before any stream capture.  Every later call
- * enqueues one small memset, the kernel and, if status_out is given, a 4-byte
- * device-to-device copy.  All calls on a device share the one array, which
+ * device address and clears the array's status words with a cudaMemsetAsync
+ * on `stream`), so that first call should come before any stream capture.  A
+ * call whose tile count differs from the previous call's on that device (and
+ * every 2^24-th call) also clears the flag and carry-word areas: two more
+ * memsets on `stream`.  Every call enqueues one small memset (this call's
+ * error word, error site and abort tag), the kernel and, if status_out is
+ * given, a 4-byte device-to-device copy.  All calls on a device share the one array, which
  * keeps the last call's contents: calls that may overlap on the GPU (other
  * streams, other host threads) race on it and must be serialised by the
  * caller.  No cudaMalloc, cudaFree or other allocating routine is called. */

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -25,6 +26,18 @@ constexpr int kDefaultWaitUs = 1000000;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+
+// True when the product of positive dimensions stays within kMaxElems.  Each
+// factor is checked by division before it is multiplied in, so the product of
+// int32 dimensions never overflows int64.
+bool within_elems(std::initializer_list<int64_t> dims) {
+    int64_t prod = 1;
+    for (int64_t d : dims) {
+        if (d <= 0 || d > kMaxElems / prod) return false;
+        prod *= d;
+    }
+    return true;
+}
 
 bool overlaps(const void* p, int64_t pbytes, const void* q, int64_t qbytes) {
     if (p == nullptr || q == nullptr || pbytes <= 0 || qbytes <= 0) return false;
@@ -73,6 +86,32 @@ struct DeviceGuard {
 };
 
 uint64_t wait_ns(const SnCtx* c) { return (uint64_t)c->wait_limit_us * 1000ull; }
+
+// The side streams and events of the pipelined chunked delta rule, created
+// with the context so that no compute call creates CUDA objects.  Priorities:
+// chain > preparation > output, so the serial chain starts as soon as SMs free
+// up and the preparation that feeds it runs ahead of the outputs.
+bool create_delta_pipe(SnCtx* c) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
+    const int mid = greatest < least - 1 ? greatest + 1 : greatest;
+    cudaStream_t* sts[3] = {&c->pipe_chain, &c->pipe_prep, &c->pipe_out};
+    const int prio[3] = {greatest, mid, least};
+    int made_s = 0;
+    for (; made_s < 3; ++made_s)
+        if (cudaStreamCreateWithPriority(sts[made_s], cudaStreamNonBlocking, prio[made_s]) != cudaSuccess) break;
+    int made_e = 0;
+    if (made_s == 3)
+        for (; made_e < 20; ++made_e)
+            if (cudaEventCreateWithFlags(&c->pipe_ev[made_e], cudaEventDisableTiming) != cudaSuccess) break;
+    if (made_e < 20) {
+        for (int i = 0; i < made_e; ++i) cudaEventDestroy(c->pipe_ev[i]);
+        for (int i = 0; i < made_s; ++i) cudaStreamDestroy(*sts[i]);
+        return false;
+    }
+    c->pipe_ready = true;
+    return true;
+}
 
 }  // namespace
 
@@ -184,7 +223,8 @@ sn_status sn_ctx_create(int32_t device, SnCtx** out_ctx) {
         delete c;
         return SN_E_DEVICE;
     }
-    if (cudaMemset(c->dstatus, 0, sizeof(SnDevStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    if (cudaMemset(c->dstatus, 0, sizeof(SnDevStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        !create_delta_pipe(c)) {
         cudaFree(c->dstatus);
         delete c;
         return SN_E_DEVICE;
@@ -222,7 +262,7 @@ sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes) {
 }
 
 int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N) {
-    if ((op != SN_OP_SCAN_FMA && op != SN_OP_SCAN_GATED) || B <= 0 || T <= 0 || N <= 0) return -1;
+    if ((op != SN_OP_SCAN_FMA && op != SN_OP_SCAN_GATED) || !within_elems({B, T, N})) return -1;
     return lookback_ws_bytes(B, T, N);
 }
 
@@ -289,8 +329,8 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
                              const float* s0, float* s_final, float* s_out, void* stream, bool gated) {
     if (ctx == nullptr || a == nullptr || b == nullptr) return SN_E_INVAL;
     if (B <= 0 || T <= 0 || N <= 0) return SN_E_INVAL;
+    if (!within_elems({B, T, N})) return SN_E_INVAL;
     const int64_t elems = (int64_t)B * T * N;
-    if (elems > kMaxElems) return SN_E_INVAL;
     const void* ptrs[5] = {a, b, s0, s_final, s_out};
     for (const void* p : ptrs)
         if (p != nullptr && !aligned(p, 4)) return SN_E_INVAL;
@@ -364,8 +404,8 @@ static sn_status scan_backward_common(SnCtx* ctx, BwdArgs& x, bool gated, void* 
     if (ctx == nullptr || x.a == nullptr || x.s == nullptr || x.gs == nullptr || (gated && x.u == nullptr))
         return SN_E_INVAL;
     if (x.B <= 0 || x.T <= 0 || x.N <= 0) return SN_E_INVAL;
+    if (!within_elems({x.B, x.T, x.N})) return SN_E_INVAL;
     const int64_t elems = (int64_t)x.B * x.T * x.N;
-    if (elems > kMaxElems) return SN_E_INVAL;
     const void* ptrs[9] = {x.a, x.u, x.s0, x.s, x.gs, x.gf, x.da, x.dbu, x.ds0};
     for (const void* p : ptrs)
         if (p != nullptr && !aligned(p, 4)) return SN_E_INVAL;
@@ -425,8 +465,10 @@ static sn_status recur_validate(SnCtx* ctx, const RecurArgs& x) {
     if (x.B <= 0 || x.T <= 0 || x.H <= 0 || x.G <= 0 || x.dk <= 0 || x.dv <= 0) return SN_E_INVAL;
     if (x.H % x.G != 0) return SN_E_INVAL;
     if (!head_dim_ok(x.dk) || !head_dim_ok(x.dv)) return SN_E_UNSUPPORTED;
+    if (!within_elems({x.B, x.T, x.H, x.dk}) || !within_elems({x.B, x.T, x.H, x.dv}) ||
+        !within_elems({x.B, x.H, x.dk, x.dv}))
+        return SN_E_INVAL;
     const int64_t rows = (int64_t)x.B * x.T;
-    if (rows * x.H * x.dk > kMaxElems || rows * x.H * x.dv > kMaxElems) return SN_E_INVAL;
     const void* ptrs[7] = {x.q, x.k, x.v, x.g, x.S_in, x.S_out, x.o};
     for (const void* p : ptrs)
         if (p != nullptr && !aligned(p, 16)) return SN_E_INVAL;
@@ -448,6 +490,7 @@ static sn_status recur_common(SnCtx* ctx, RecurArgs& x, void* stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (x.T == 1 && ctx->recur_kernel == 0 && recur_decode_supported(x))
         return from_cuda(launch_recur_decode(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+    if (!recur_seq_width_ok(x, ctx->sm_count, ctx->recur_tile)) return SN_E_INVAL;
     return from_cuda(launch_recur_sequence(x, ctx->dstatus, wait_ns(ctx), ctx->sm_count, ctx->recur_tile, s));
 }
 
@@ -532,37 +575,13 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, in
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
     ctx->ws_dirty = true;   // the chunk tiles overwrite the look-back flag area
-    const int nseg = delta_segments((T + 127) / 128, B * H, ctx->sm_count, ctx->delta_segments);
-    if (nseg > 1 && !ctx->pipe_ready) {
-        // priorities: chain > preparation > output, so the serial chain starts as soon as SMs
-        // free up and the preparation that feeds it runs ahead of the outputs
-        int least = 0, greatest = 0;
-        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return SN_E_DEVICE;
-        const int mid = greatest < least - 1 ? greatest + 1 : greatest;
-        cudaStream_t* sts[3] = {&ctx->pipe_chain, &ctx->pipe_prep, &ctx->pipe_out};
-        const int prio[3] = {greatest, mid, least};
-        int made_s = 0;
-        for (; made_s < 3; ++made_s)
-            if (cudaStreamCreateWithPriority(sts[made_s], cudaStreamNonBlocking, prio[made_s]) != cudaSuccess) break;
-        int made_e = 0;
-        if (made_s == 3)
-            for (; made_e < 20; ++made_e)
-                if (cudaEventCreateWithFlags(&ctx->pipe_ev[made_e], cudaEventDisableTiming) != cudaSuccess) break;
-        if (made_e < 20) {
-            for (int i = 0; i < made_e; ++i) cudaEventDestroy(ctx->pipe_ev[i]);
-            for (int i = 0; i < made_s; ++i) cudaStreamDestroy(*sts[i]);
-            return SN_E_DEVICE;
-        }
-        ctx->pipe_ready = true;
-    }
-    DeltaPipe pipe{};
-    if (ctx->pipe_ready) pipe = DeltaPipe{ctx->pipe_prep, ctx->pipe_chain, ctx->pipe_out, ctx->pipe_ev, 20};
+    const DeltaPipe pipe{ctx->pipe_prep, ctx->pipe_chain, ctx->pipe_out, ctx->pipe_ev, 20};
     return from_cuda(launch_delta_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, ctx->delta_segments, pipe,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {
-    if (B <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (!within_elems({B, T, H, dk}) || !within_elems({B, T, H, dv}) || dk > 4096 || dv > 4096) return -1;
     return delta_chunked_ws_bytes(B, T, H, dk, dv);
 }
 
@@ -570,7 +589,7 @@ int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, 
 static sn_status readout_check(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t dv, const void* const* ptrs,
                                int nptr) {
     if (ctx == nullptr || B <= 0 || T <= 0 || H <= 0 || dv <= 0) return SN_E_INVAL;
-    if ((int64_t)B * T * H * dv > kMaxElems) return SN_E_INVAL;
+    if (!within_elems({B, T, H, dv})) return SN_E_INVAL;
     if (dv != 64 && dv != 128) return SN_E_UNSUPPORTED;
     for (int i = 0; i < nptr; ++i)
         if (ptrs[i] != nullptr && !aligned(ptrs[i], 16)) return SN_E_INVAL;
@@ -609,7 +628,7 @@ sn_status sn_readout_dskip(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t 
 }
 
 int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {
-    if (B <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (!within_elems({B, T, H, dk}) || !within_elems({B, T, H, dv}) || dk > 4096 || dv > 4096) return -1;
     return chunked_ws_bytes(B, T, H, dk, dv);
 }
 

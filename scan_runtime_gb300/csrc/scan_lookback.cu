@@ -559,6 +559,7 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int po
 // Flags and carry words stay at fixed offsets, so such a word only ever holds
 // a tagged value or zero.
 #include <atomic>
+#include <cstddef>
 #include <mutex>
 
 namespace {
@@ -574,11 +575,20 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 constexpr int kNoallocMaxDevices = 64;
 
+// Calls between two clears of the flag and carry areas at one tile count.
+// Every launch rewrites the flags and carry words of all its tiles, so with an
+// unchanged tile count a stale word holds the previous launch's tag, never the
+// current one; the periodic clear bounds the case in which a launch that gave
+// up left some words unwritten, well before the epoch can wrap (2^29 - 1).
+constexpr uint64_t kNoallocClearEvery = uint64_t(1) << 24;
+
 struct NoallocDevice {
     bool ready = false;
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
     int sm_count = 0;
     int occ[2] = {0, 0};
+    int64_t last_tiles = -1;            // tile count of the previous call (-1: areas need a clear)
+    uint64_t calls_since_clear = 0;
 };
 NoallocDevice g_noalloc[kNoallocMaxDevices];
 std::mutex g_noalloc_mutex;
@@ -601,8 +611,11 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
     const void* ptrs[6] = {a, b, s0, s_final, s_out, status_out};
     for (const void* q : ptrs)
         if (q != nullptr && (reinterpret_cast<uintptr_t>(q) & 3u) != 0) return SN_E_INVAL;
+    // element-count bound checked by division first: B * T * N itself can
+    // exceed the int64 range for int32 dimensions
+    constexpr int64_t kMaxElems = int64_t(1) << 40;
+    if ((int64_t)T > kMaxElems / B / N) return SN_E_INVAL;
     const int64_t big = (int64_t)B * T * N * 4, small = (int64_t)B * N * 4;
-    if ((int64_t)B * T * N > (int64_t(1) << 40)) return SN_E_INVAL;
     const void* ins[3] = {a, b, s0};
     const int64_t insz[3] = {big, big, small};
     void* outs[3] = {s_final, s_out, status_out};
@@ -643,14 +656,25 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
                 d.occ[g] < 1)
                 return SN_E_DEVICE;
         }
-        if (cudaMemsetAsync(sym, 0, (size_t)kNoallocDataOff, s) != cudaSuccess ||
-            cudaMemsetAsync(static_cast<unsigned char*>(sym) + kNoallocCwOff, 0,
-                            (size_t)(kNoallocScratchBytes - kNoallocCwOff), s) != cudaSuccess)
-            return SN_E_DEVICE;
+        if (cudaMemsetAsync(sym, 0, sizeof(SnDevStatus), s) != cudaSuccess) return SN_E_DEVICE;
         d.scratch = static_cast<unsigned char*>(sym);
         d.sm_count = prop.multiProcessorCount;
+        d.last_tiles = -1;
         d.ready = true;
     }
+    if (tiles != d.last_tiles || d.calls_since_clear >= kNoallocClearEvery) {
+        // A different tile count maps tiles onto flag and carry words that an
+        // older call of another shape may have tagged: clear both areas (in
+        // stream order, before the launch), as the context path does.
+        if (cudaMemsetAsync(d.scratch + kNoallocFlagsOff, 0, (size_t)(kNoallocDataOff - kNoallocFlagsOff), s) !=
+                cudaSuccess ||
+            cudaMemsetAsync(d.scratch + kNoallocCwOff, 0, (size_t)(kNoallocScratchBytes - kNoallocCwOff), s) !=
+                cudaSuccess)
+            return SN_E_DEVICE;
+        d.last_tiles = tiles;
+        d.calls_since_clear = 0;
+    }
+    ++d.calls_since_clear;
 
     CUtensorMap ma, mb;
     if (!make_scan_map(&ma, a, B, T, N, LB_NC, LB_TC) || !make_scan_map(&mb, b, B, T, N, LB_NC, LB_TC))
@@ -674,8 +698,12 @@ extern "C" sn_status sn_scan_lookback_noalloc(int32_t gated, int32_t B, int32_t 
     p.poison = 0;
     p.st = st;                                    // also holds the launch epoch
     p.wait_ns = 1000000000ull;                    // 1 s bound on every device-side wait
-    // this call's error word starts at zero
-    if (cudaMemsetAsync(st, 0, 2 * sizeof(int), s) != cudaSuccess) return SN_E_DEVICE;
+    // this call's error word, error site and abort tag start at zero (the
+    // launch epoch after them is kept)
+    static_assert(offsetof(SnDevStatus, abort_tag) == 2 * sizeof(int) &&
+                      offsetof(SnDevStatus, lb_epoch) == 3 * sizeof(int),
+                  "error, site and abort tag precede the epoch");
+    if (cudaMemsetAsync(st, 0, 3 * sizeof(int), s) != cudaSuccess) return SN_E_DEVICE;
     const int grid = (int)std::min<int64_t>(tiles, (int64_t)d.occ[gated] * d.sm_count);
     void* args[] = {(void*)&ma, (void*)&mb, (void*)&p};
     if (cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(LB_THREADS), args, LB_SMEM, s) !=

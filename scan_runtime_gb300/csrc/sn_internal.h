@@ -44,7 +44,7 @@ struct SnCtx {
     int recur_kernel;
     int recur_tile;             // forced consumer warps per CTA of the sequence kernel (0 = auto)
     int delta_segments;         // segments of the pipelined chunked delta rule (0 = auto)
-    // side streams and events of the pipelined chunked delta rule (created on first use)
+    // side streams and events of the pipelined chunked delta rule (created with the context)
     cudaStream_t pipe_prep, pipe_chain, pipe_out;
     cudaEvent_t pipe_ev[20];
     bool pipe_ready;
@@ -142,6 +142,9 @@ struct RecurArgs {
 
 cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                   int force_width, cudaStream_t stream);
+// Whether a forced CTA width (SN_OPT_RECUR_TILE; 0 = auto) suits the problem:
+// the value dimension must be a multiple of the columns a CTA of that width covers.
+bool recur_seq_width_ok(const RecurArgs& x, int sm_count, int width);
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);

@@ -138,6 +138,20 @@ def test_workspace_bytes(abi):
     assert abi.sn_workspace_bytes(99, 1, 1, 1) == -1
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 0, 1, 1) == -1
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 1, -5, 1) == -1
+    # dimensions whose product exceeds the element bound (or int64): -1, no overflow
+    big = 2 ** 31 - 1
+    assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, big, big, big) == -1
+    assert abi.sn_recur_chunked_workspace_bytes(big, big, big, 128, 128) == -1
+    assert abi.sn_recur_delta_chunked_workspace_bytes(big, big, 1, 128, 128) == -1
+
+
+def test_noalloc_rejects_oversized_problems_before_any_device_work(abi):
+    """Dimensions whose element count overflows int64 are an argument error,
+    found before the device is touched (the pointers are never read)."""
+    big = 2 ** 31 - 1
+    fake = 1 << 20
+    for B, T, N in ((big, big, big), (4, big, big), (1, 1 << 20, 1 << 21)):
+        assert abi.sn_scan_lookback_noalloc(0, B, T, N, fake, fake, None, None, None, None, 0) == abi.SN_E_INVAL
 
 
 def test_product_package_does_not_touch_the_oracle():

@@ -413,3 +413,21 @@ def test_cta_widths_give_identical_bits(sr, ctx, kind):
         assert np.array_equal(o, outs[0][0]) and np.array_equal(S, outs[0][1])
     ro, rS = ref(x, S0)
     assert _nrel(outs[0][0], ro) <= TOL and _nrel(outs[0][1], rS) <= TOL
+
+
+def test_forced_width_that_does_not_tile_the_columns_is_rejected(sr, ctx):
+    """A forced CTA width whose columns the value dimension does not divide
+    (RWKV-7 64 x 64: 16 columns per warp, so 8 warps need 128) is an argument
+    error found on the host, before any launch; outputs stay untouched."""
+    x = make("rwkv", 1, 8, 2, 64, 64, seed=9)
+    o = torch.full((1, 8, 2, 64), 7.0, device="cuda")
+    S = torch.full((1, 2, 64, 64), 7.0, device="cuda")
+    ctx.set_option(sr.SN_OPT_RECUR_TILE, 8)
+    try:
+        st = sr.sn_recur_rwkv7(ctx.handle, 1, 8, 2, 64, 64, *(cu(x[n]) for n in ("q", "k", "v", "w")), None, S, o)
+    finally:
+        ctx.set_option(sr.SN_OPT_RECUR_TILE, 0)
+    torch.cuda.synchronize()
+    assert st == sr.SN_E_INVAL
+    assert bool((o == 7.0).all()) and bool((S == 7.0).all())
+
