@@ -105,9 +105,10 @@ typedef int32_t sn_status;
 #define SN_OPT_DEBUG_POISON     3  /* 1: look-back waits for a flag no chunk publishes (tests the bound) */
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
 #define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
-#define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA;
-                                      a width whose CTA columns the value dimension does not divide makes
-                                      the sequence-kernel call fail with SN_E_INVAL before any launch */
+#define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA
+                                      (the same bits for every width); a width whose CTA columns the value
+                                      dimension does not divide would fail with SN_E_INVAL before any
+                                      launch (no compiled tile and head size has such a width) */
 #define SN_OPT_DELTA_SEGMENTS   7  /* sn_recur_delta_chunked: 0 auto (default), or 1..8 segments of the
                                       chunk sequence run as a pipeline (same bits for every value) */
 

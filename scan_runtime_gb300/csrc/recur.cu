@@ -10,21 +10,10 @@ cudaError_t launch_recur_diag_gated_seq(const RecurArgs&, SnDevStatus*, uint64_t
 cudaError_t launch_recur_delta_seq(const RecurArgs&, SnDevStatus*, uint64_t, int, int, cudaStream_t);
 cudaError_t launch_recur_rwkv7_seq(const RecurArgs&, SnDevStatus*, uint64_t, int, int, cudaStream_t);
 
-// Value columns one consumer warp of the sequence kernel covers for this
-// problem (the dispatch's choice of rows per lane; 4 columns per lane group).
-namespace {
-int seq_cols_per_warp(const RecurArgs& x, int sm_count) {
-    const bool diag = x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_HEAD || x.kind == RK_DIAG_KEY_GATED ||
-                      x.kind == RK_DIAG_HEAD_GATED;
-    const int R = (!diag || diag_eight_rows(x, sm_count)) ? 8 : 4;
-    return (32 / (x.dk / R)) * 4;
-}
-}  // namespace
-
 bool recur_seq_width_ok(const RecurArgs& x, int sm_count, int width) {
     if (width == 0) return true;
     if (width != 2 && width != 4 && width != 8) return false;
-    return x.dv % (width * seq_cols_per_warp(x, sm_count)) == 0;
+    return x.dv % (width * seq_cols_per_warp(x, sm_count)) == 0;   // the tile of recur_seq.cuh
 }
 
 cudaError_t launch_recur_sequence(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,

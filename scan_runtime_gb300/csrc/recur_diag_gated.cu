@@ -8,24 +8,13 @@
 
 namespace sn {
 
-namespace {
-template <int KIND>
-cudaError_t gated_dispatch(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
-                           cudaStream_t stream) {
-    const bool many = diag_eight_rows(x, sm_count);
-    if (x.dk == 128)
-        return many ? run_seq_width<KIND, 128, 8, 4>(x, st, wait_ns, sm_count, force_w, stream)
-                    : run_seq_width<KIND, 128, 4, 4>(x, st, wait_ns, sm_count, force_w, stream);
-    return many ? run_seq_width<KIND, 64, 8, 4>(x, st, wait_ns, sm_count, force_w, stream)
-                : run_seq_width<KIND, 64, 4, 4>(x, st, wait_ns, sm_count, force_w, stream);
-}
-}  // namespace
-
 cudaError_t launch_recur_diag_gated_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                         int force_w, cudaStream_t stream) {
     if (x.kind == RK_DIAG_KEY_GATED)
-        return gated_dispatch<RK_DIAG_KEY_GATED>(x, st, wait_ns, sm_count, force_w, stream);
-    return gated_dispatch<RK_DIAG_HEAD_GATED>(x, st, wait_ns, sm_count, force_w, stream);
+        return x.dk == 128 ? run_seq_diag<RK_DIAG_KEY_GATED, 128>(x, st, wait_ns, sm_count, force_w, stream)
+                           : run_seq_diag<RK_DIAG_KEY_GATED, 64>(x, st, wait_ns, sm_count, force_w, stream);
+    return x.dk == 128 ? run_seq_diag<RK_DIAG_HEAD_GATED, 128>(x, st, wait_ns, sm_count, force_w, stream)
+                       : run_seq_diag<RK_DIAG_HEAD_GATED, 64>(x, st, wait_ns, sm_count, force_w, stream);
 }
 
 }  // namespace sn

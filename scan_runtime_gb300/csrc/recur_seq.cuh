@@ -1,5 +1,7 @@
 // recur_seq.cuh -- the sequence kernel shared by the three matrix recurrences
-// (instantiated per kind in recur_diag.cu, recur_delta.cu, recur_rwkv7.cu).
+// (instantiated per kind in recur_diag.cu, recur_diag_gated.cu,
+// recur_delta.cu, recur_rwkv7.cu; the tile of each problem is chosen at the
+// end of this file).
 //
 // All recurrences are written for the state P in R^{dk x dv} (row = key index
 // i, column = value index j), whose columns evolve independently:
@@ -14,18 +16,26 @@
 //
 // Work split: one CTA per (batch, head, tile of JT value columns).  A lane
 // holds R rows x C columns of P in registers for the whole sequence; LPC =
-// dk / R lanes share a group of C columns.  Column pairs are packed into
-// f32x2 operations, so every k / decay / q value read from shared memory
-// feeds C state entries.  q, k, per-key decay and the v slice arrive through a
-// 3-stage TMA ring fed by a producer warp (per-head scalars by 4-byte cp.async
-// on the same mbarrier); o leaves through TMA stores.
+// dk / R lanes share a group of C columns; W consumer warps take different
+// column groups.  Column pairs are packed into f32x2 operations, so every k /
+// decay / q value read feeds C state entries.  q, k, per-key decay and the v
+// slice arrive through a 3-stage TMA ring fed by a producer warp (per-head
+// scalars by 4-byte cp.async on the same mbarrier); o leaves through TMA
+// stores.  Each step's operands are read from shared memory PF steps ahead of
+// its arithmetic.
 //
-// Arithmetic per column is fixed: the diag update is fma(d_i, P_ij, k_i * v_j)
-// with the product rounded first (the single-precision definition's order);
-// a lane's dot products run four chains over its rows (row index mod 4) and
-// join as (c0 + c1) + (c2 + c3); lane partials join over xor partners LPC/2 ..
-// 1.  The result therefore depends only on the state and the inputs: segment
-// splits are bit-exact, and the CTA width does not change the bits.
+// Arithmetic per column is fixed by R (rows per lane):
+//   * the diag update is fma(d_i, P_ij, k_i * v_j) with the product rounded
+//     first (the single-precision definition's order), so the diagonal-decay
+//     state has the definition's bits whatever the tile;
+//   * a dot product over rows (the delta rule's P^T k and every readout) runs
+//     four chains over a lane's rows (row index mod 4) joined as
+//     (c0 + c1) + (c2 + c3); the LPC lane partials join over xor partners
+//     LPC/2 .. 1.
+// The result therefore depends only on the state, the inputs and R: segment
+// splits are bit-exact, C, W and PF do not change the bits, and the
+// single-step decode kernels reproduce the same order (recur_decode.cu,
+// recur_rwkv7.cu).
 #pragma once
 
 #include <algorithm>
@@ -38,7 +48,6 @@ namespace sn {
 constexpr int RS_TS = 16;       // time steps per stage
 constexpr int RS_STAGES = 3;
 constexpr int RS_OBUF = 3;      // output staging buffers
-constexpr int RS_RB = 8;        // steps per readout reduction batch
 
 template <int KIND>
 constexpr bool per_key_gate() { return KIND == RK_DIAG_KEY || KIND == RK_RWKV7 || KIND == RK_DIAG_KEY_GATED; }
@@ -50,6 +59,10 @@ constexpr bool diag_kind() {
 }
 template <int KIND>
 constexpr bool gated_injection() { return KIND == RK_DIAG_KEY_GATED || KIND == RK_DIAG_HEAD_GATED; }
+
+// Steps per readout reduction batch: 8, or 16 when 8 steps of C columns do
+// not fill a reduction over LPC lanes.
+constexpr int readout_batch(int C, int LPC) { return (8 * C) % LPC == 0 ? 8 : 16; }
 
 template <int KIND, int DK, int JT>
 struct SeqLayout {
@@ -119,28 +132,43 @@ __device__ __forceinline__ void load_rows(float (&x)[R], const float* row, int s
     }
 }
 
-// One time step for one lane: rows (m * LPC + sub) * 4 + e (m < R/4, e < 4),
-// columns c < C of its group (packed as C/2 pairs).  kr, gr, qr point at the
-// step's k, per-key gate and q rows; vr at the group's C values; gsc is the
-// per-head scalar (dA or beta).  opart receives this lane's readout partials.
+// Operands of one time step for one lane: its rows of k, the per-key gate and
+// q, its group's C values of v, and the per-head scalar (dA or beta).
+template <int KIND, int R, int C>
+struct StepOps {
+    float k[R];
+    float g[per_key_gate<KIND>() ? R : 1];
+    float q[R];
+    float2 v[C / 2];
+    float s;
+};
+
+// Read one step's operands: rows (m * LPC + sub) * 4 + e (m < R/4, e < 4) of
+// the row slice kr, gr, qr point into, and the group's C values at vr.
 template <int KIND, int R, int C, int LPC>
-__device__ __forceinline__ void lane_step(float2 (&P)[R][C / 2], const float* kr, const float* gr,
-                                          const float* qr, const float* vr, float gsc, int sub,
-                                          float2 (&opart)[C / 2], bool want_o) {
+__device__ __forceinline__ void load_step(StepOps<KIND, R, C>& x, const float* kr, const float* gr, const float* qr,
+                                          const float* vr, float gsc, int sub, bool want_o) {
+    load_rows<R, LPC>(x.k, kr, sub);
+    if constexpr (per_key_gate<KIND>()) load_rows<R, LPC>(x.g, gr, sub);
+    if (want_o) load_rows<R, LPC>(x.q, qr, sub);
+#pragma unroll
+    for (int c = 0; c < C / 2; ++c) x.v[c] = *reinterpret_cast<const float2*>(vr + 2 * c);
+    x.s = gsc;
+}
+
+// One time step for one lane on its R rows x C columns (packed as C/2 pairs)
+// from the step's operands; opart receives this lane's readout partials.
+template <int KIND, int R, int C, int LPC>
+__device__ __forceinline__ void step_compute(float2 (&P)[R][C / 2], const StepOps<KIND, R, C>& x,
+                                             float2 (&opart)[C / 2], bool want_o) {
     constexpr int C2 = C / 2;
     float kv[R];
-    load_rows<R, LPC>(kv, kr, sub);
-    float2 v2[C2];
 #pragma unroll
-    for (int c = 0; c < C2; ++c) v2[c] = *reinterpret_cast<const float2*>(vr + 2 * c);
+    for (int r = 0; r < R; ++r) kv[r] = x.k[r];
     if constexpr (diag_kind<KIND>()) {
         float dv_[R];
-        if constexpr (per_key_gate<KIND>()) {
-            load_rows<R, LPC>(dv_, gr, sub);
-        } else {
 #pragma unroll
-            for (int r = 0; r < R; ++r) dv_[r] = gsc;
-        }
+        for (int r = 0; r < R; ++r) dv_[r] = per_key_gate<KIND>() ? x.g[per_key_gate<KIND>() ? r : 0] : x.s;
         if constexpr (gated_injection<KIND>()) {
             // convex combination: the injection k_i v_j enters with weight 1 - p_i
 #pragma unroll
@@ -149,10 +177,8 @@ __device__ __forceinline__ void lane_step(float2 (&P)[R][C / 2], const float* kr
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int c = 0; c < C2; ++c) P[r][c] = __ffma2_rn(f2(dv_[r]), P[r][c], __fmul2_rn(f2(kv[r]), v2[c]));
+            for (int c = 0; c < C2; ++c) P[r][c] = __ffma2_rn(f2(dv_[r]), P[r][c], __fmul2_rn(f2(kv[r]), x.v[c]));
     } else {
-        float wv[R];
-        if constexpr (KIND == RK_RWKV7) load_rows<R, LPC>(wv, gr, sub);
 #pragma unroll
         for (int c = 0; c < C2; ++c) {
             float2 u0 = f2(0.f), u1 = f2(0.f), u2 = f2(0.f), u3 = f2(0.f);
@@ -164,52 +190,78 @@ __device__ __forceinline__ void lane_step(float2 (&P)[R][C / 2], const float* kr
                 u3 = __ffma2_rn(P[4 * m + 3][c], f2(kv[4 * m + 3]), u3);
             }
             const float2 u = group_sum2(__fadd2_rn(__fadd2_rn(u0, u1), __fadd2_rn(u2, u3)), LPC);
-            float2 delta = __fadd2_rn(v2[c], make_float2(-u.x, -u.y));   // v - u, exactly
+            float2 delta = __fadd2_rn(x.v[c], make_float2(-u.x, -u.y));   // v - u, exactly
             if constexpr (KIND == RK_DELTA) {
-                delta = __fmul2_rn(delta, f2(gsc));
+                delta = __fmul2_rn(delta, f2(x.s));
 #pragma unroll
                 for (int r = 0; r < R; ++r) P[r][c] = __ffma2_rn(f2(kv[r]), delta, P[r][c]);
             } else {
 #pragma unroll
-                for (int r = 0; r < R; ++r) P[r][c] = __ffma2_rn(f2(kv[r]), delta, __fmul2_rn(P[r][c], f2(wv[r])));
+                for (int r = 0; r < R; ++r)
+                    P[r][c] = __ffma2_rn(f2(kv[r]), delta, __fmul2_rn(P[r][c], f2(x.g[per_key_gate<KIND>() ? r : 0])));
             }
         }
     }
     if (!want_o) return;
-    float qv[R];
-    load_rows<R, LPC>(qv, qr, sub);
 #pragma unroll
     for (int c = 0; c < C2; ++c) {
         float2 a0 = f2(0.f), a1 = f2(0.f), a2 = f2(0.f), a3 = f2(0.f);
 #pragma unroll
         for (int m = 0; m < R / 4; ++m) {
-            a0 = __ffma2_rn(P[4 * m][c], f2(qv[4 * m]), a0);
-            a1 = __ffma2_rn(P[4 * m + 1][c], f2(qv[4 * m + 1]), a1);
-            a2 = __ffma2_rn(P[4 * m + 2][c], f2(qv[4 * m + 2]), a2);
-            a3 = __ffma2_rn(P[4 * m + 3][c], f2(qv[4 * m + 3]), a3);
+            a0 = __ffma2_rn(P[4 * m][c], f2(x.q[4 * m]), a0);
+            a1 = __ffma2_rn(P[4 * m + 1][c], f2(x.q[4 * m + 1]), a1);
+            a2 = __ffma2_rn(P[4 * m + 2][c], f2(x.q[4 * m + 2]), a2);
+            a3 = __ffma2_rn(P[4 * m + 3][c], f2(x.q[4 * m + 3]), a3);
         }
         opart[c] = __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
     }
 }
 
-template <int KIND, int DK, int R, int C, int W>
-__global__ void __launch_bounds__((W + 1) * 32)
+// One time step for one lane: load the operands, then compute.  kr, gr, qr
+// point at the row slice's k, per-key gate and q rows; vr at the group's C
+// values; gsc is the per-head scalar (dA or beta).
+template <int KIND, int R, int C, int LPC>
+__device__ __forceinline__ void lane_step(float2 (&P)[R][C / 2], const float* kr, const float* gr,
+                                          const float* qr, const float* vr, float gsc, int sub,
+                                          float2 (&opart)[C / 2], bool want_o) {
+    StepOps<KIND, R, C> x;
+    load_step<KIND, R, C, LPC>(x, kr, gr, qr, vr, gsc, sub, want_o);
+    step_compute<KIND, R, C, LPC>(P, x, opart, want_o);
+}
+
+// Tile of the sequence kernel for key dimension DK: R rows x C columns per
+// lane, LPC = DK / R lanes per column group, W consumer warps; GEN reads the
+// staged operands through generic pointers (see smem_align_generic); PF > 0
+// reads each step's operands PF steps ahead of its arithmetic (registers as a
+// ring).
+template <int DK, int R_, int C_, int W_, bool GEN_, int PF_>
+struct SeqTile {
+    static constexpr int R = R_, C = C_, LPC = DK / R_, W = W_;
+    static constexpr bool GEN = GEN_;
+    static constexpr int PF = PF_;                       // steps whose operands are read ahead
+    static constexpr int CPW = 32 / LPC;                 // column groups per warp
+    static constexpr int JT = W * CPW * C;               // columns per CTA
+    static constexpr int NCONS = W;                      // consumer warps
+    static constexpr int THREADS = (NCONS + 1) * 32;
+    static constexpr int RB = readout_batch(C, LPC);
+};
+
+template <int KIND, int DK, class TL>
+__global__ void __launch_bounds__(TL::THREADS)
 recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
           const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_v,
           const __grid_constant__ CUtensorMap map_o, const SeqParams p) {
-    constexpr int LPC = DK / R;            // lanes per column group
-    constexpr int CPW = 32 / LPC;          // column groups per warp
-    constexpr int JT = W * CPW * C;        // columns per CTA
+    constexpr int R = TL::R, C = TL::C, LPC = TL::LPC, CPW = TL::CPW, JT = TL::JT;
+    constexpr int NCONS = TL::NCONS, RB = TL::RB;
     constexpr int C2 = C / 2;
-    constexpr int NV = RS_RB * C;          // readout values per lane per batch
+    constexpr int NV = RB * C;             // readout values per lane per batch
     using L = SeqLayout<KIND, DK, JT>;
-    static_assert(R % 4 == 0 && C % 2 == 0 && LPC <= 32 && NV % LPC == 0, "tile shape");
+    static_assert(R % 4 == 0 && C % 2 == 0 && LPC >= 1 && LPC <= 32 && (LPC & (LPC - 1)) == 0 && R * LPC == DK,
+                  "tile shape");
+    static_assert(NV % LPC == 0 && RS_TS % RB == 0, "reduction shape");
 
     extern __shared__ unsigned char smem_raw[];
-    // With 4 rows per lane a step has little arithmetic to hide its operand
-    // loads behind, and the kernel measured faster with the loads scheduled as
-    // generic (long-latency) ones; with 8 rows, shared-memory loads are faster.
-    unsigned char* smem = R >= 8 ? smem_align<128>(smem_raw) : smem_align_generic<128>(smem_raw);
+    unsigned char* smem = TL::GEN ? smem_align_generic<128>(smem_raw) : smem_align<128>(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar_off);
     uint64_t* empty = full + RS_STAGES;
 
@@ -222,13 +274,13 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         for (int s = 0; s < RS_STAGES; ++s) {
             mbar_init(&full[s], scalar_gate<KIND>() ? 33 : 1);
-            mbar_init(&empty[s], W);
+            mbar_init(&empty[s], NCONS);
         }
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == W) {
+    if (warp == NCONS) {
         // ------------------------------------------------ producer warp
         for (int kk = 0; kk < nst; ++kk) {
             const int slot = kk % RS_STAGES;
@@ -260,7 +312,7 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
 
     // ---------------------------------------------------- consumer warps
     const int gcol = lane / LPC, sub = lane % LPC;
-    const int jl0 = (warp * CPW + gcol) * C;           // first column of the group within the tile
+    const int jl0 = (warp * CPW + gcol) * C;             // first column of the group within the tile
     const int j0 = jt0 + jl0;
     const size_t sbase = ((size_t)b * p.H + h) * (size_t)DK * p.dv;
 
@@ -290,39 +342,54 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     }
 
     const bool want_o = p.has_o != 0;
+    // A warp whose stage wait runs out records the error and from then on
+    // skips the waits and the arithmetic, but keeps passing the named
+    // barriers with the other consumer warps, so none of them is left waiting
+    // at a barrier (the other warps time out on the same stage or finish).
     bool failed = false;
     for (int kk = 0; kk < nst; ++kk) {
         const int slot = kk % RS_STAGES;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (kk / RS_STAGES) & 1, p.wait_ns));
-        if (!ok) {
+        if (!failed && !__all_sync(0xffffffffu, mbar_wait(&full[slot], (kk / RS_STAGES) & 1, p.wait_ns))) {
             if (lane == 0) record_error(p.st, SN_E_TIMEOUT, (SN_K_RECUR_SEQ << 16) | 2);
             failed = true;
-            break;
         }
         const unsigned char* sb = smem + slot * L::stage_bytes;
         const float* qs = reinterpret_cast<const float*>(sb + L::q_off);
         const float* ks = reinterpret_cast<const float*>(sb + L::k_off);
         const float* gs = reinterpret_cast<const float*>(sb + L::g_off);
+        const float* gks = gs;
         const float* vs = reinterpret_cast<const float*>(sb + L::v_off);
         float* os = reinterpret_cast<float*>(smem + L::o_off + (kk % RS_OBUF) * L::o_bytes);
         const int tn = min(RS_TS, T - kk * RS_TS);
 
-        if (tn == RS_TS) {
-            // Readout partials of RS_RB steps stay in registers and are reduced
+        // a column's readout sum, scaled, into the output staging
+        auto put = [&](int t, int col, float x) { os[t * JT + col] = __fmul_rn(x, p.scale); };
+        if (failed) {
+            // no arithmetic: fall through to the stage's barriers
+        } else if (tn == RS_TS) {
+            // Readout partials of RB steps stay in registers and are reduced
             // once over the lane group (no per-step shuffle chain or store).
+            constexpr int PF = TL::PF;
+            StepOps<KIND, R, C> ring[PF + 1];
+            auto fetch = [&](int t) {
+                load_step<KIND, R, C, LPC>(ring[t % (PF + 1)], ks + t * DK, gks + t * DK, qs + t * DK,
+                                           vs + t * JT + jl0, scalar_gate<KIND>() ? gs[t] : 0.f, sub, want_o);
+            };
 #pragma unroll
-            for (int rb = 0; rb < RS_TS / RS_RB; ++rb) {
-                float2 ov[RS_RB][C2];
+            for (int t = 0; t < PF; ++t) fetch(t);
 #pragma unroll
-                for (int i = 0; i < RS_RB; ++i) {
-                    const int t = rb * RS_RB + i;
-                    lane_step<KIND, R, C, LPC>(P, ks + t * DK, gs + t * DK, qs + t * DK, vs + t * JT + jl0,
-                                               scalar_gate<KIND>() ? gs[t] : 0.f, sub, ov[i], want_o);
+            for (int rb = 0; rb < RS_TS / RB; ++rb) {
+                float2 ov[RB][C2];
+#pragma unroll
+                for (int i = 0; i < RB; ++i) {
+                    const int t = rb * RB + i;
+                    if (t + PF < RS_TS) fetch(t + PF);
+                    step_compute<KIND, R, C, LPC>(P, ring[t % (PF + 1)], ov[i], want_o);
                 }
                 if (want_o) {
                     float fl[NV];                      // [step][column] readout partials
 #pragma unroll
-                    for (int i = 0; i < RS_RB; ++i)
+                    for (int i = 0; i < RB; ++i)
 #pragma unroll
                         for (int c = 0; c < C2; ++c) {
                             fl[i * C + 2 * c] = ov[i][c].x;
@@ -333,34 +400,34 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
 #pragma unroll
                     for (int e = 0; e < PER; ++e) {
                         const int idx = sub * PER + e;
-                        os[(rb * RS_RB + idx / C) * JT + jl0 + idx % C] = __fmul_rn(fl[e], p.scale);
+                        put(rb * RB + idx / C, jl0 + idx % C, fl[e]);
                     }
                 }
             }
         } else {
             for (int t = 0; t < tn; ++t) {
-                float2 part[C2];
-                lane_step<KIND, R, C, LPC>(P, ks + t * DK, gs + t * DK, qs + t * DK, vs + t * JT + jl0,
-                                           scalar_gate<KIND>() ? gs[t] : 0.f, sub, part, want_o);
+                float2 part2[C2];
+                lane_step<KIND, R, C, LPC>(P, ks + t * DK, gks + t * DK, qs + t * DK, vs + t * JT + jl0,
+                                           scalar_gate<KIND>() ? gs[t] : 0.f, sub, part2, want_o);
                 if (want_o) {
 #pragma unroll
                     for (int c = 0; c < C2; ++c) {
-                        const float2 acc = group_sum2(part[c], LPC);
+                        const float2 acc = group_sum2(part2[c], LPC);
                         if (sub == 0) {
-                            os[t * JT + jl0 + 2 * c] = __fmul_rn(acc.x, p.scale);
-                            os[t * JT + jl0 + 2 * c + 1] = __fmul_rn(acc.y, p.scale);
+                            put(t, jl0 + 2 * c, acc.x);
+                            put(t, jl0 + 2 * c + 1, acc.y);
                         }
                     }
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0 && !failed) mbar_arrive(&empty[slot]);
         if (want_o) {
             fence_proxy_async_smem();
             // the store two stages back read the buffer the next stage writes
             if (threadIdx.x == 0) bulk_wait_read_allbut1();
-            named_bar_sync(1, W * 32);
+            named_bar_sync(1, NCONS * 32);
             if (threadIdx.x == 0) {
                 tma_store_4d(&map_o, os, jt0, h, kk * RS_TS, b);
                 bulk_commit();
@@ -388,12 +455,11 @@ recur_seq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     }
 }
 
-template <int KIND, int DK, int R, int C, int W>
+template <int KIND, int DK, class TL>
 cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaStream_t stream) {
-    constexpr int LPC = DK / R;
-    constexpr int JT = W * (32 / LPC) * C;
+    constexpr int JT = TL::JT;
     using L = SeqLayout<KIND, DK, JT>;
-    if (x.dv % JT != 0) return cudaErrorInvalidValue;
+    if (x.dv % JT != 0 || x.dk != DK) return cudaErrorInvalidValue;
     const int gdim = diag_kind<KIND>() ? x.G : x.H;
     CUtensorMap mq, mk, mg, mv, mo;
     const uint64_t dqk[4] = {(uint64_t)DK, (uint64_t)gdim, (uint64_t)x.T, (uint64_t)x.B};
@@ -418,35 +484,30 @@ cudaError_t run_seq(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, cudaS
         mo = mv;   // unused
     }
     SeqParams p{x.T, x.H, x.G, x.dk, x.dv, x.scale, x.g, x.S_in, x.S_out, x.o != nullptr ? 1 : 0, st, wait_ns};
-    auto kern = recur_seq<KIND, DK, R, C, W>;
+    auto kern = recur_seq<KIND, DK, TL>;
     cudaError_t e = set_smem_attr_once((const void*)kern, L::smem);
     if (e != cudaSuccess) return e;
     dim3 grid(x.dv / JT, x.H, x.B);
-    kern<<<grid, (W + 1) * 32, L::smem, stream>>>(mq, mk, mg, mv, mo, p);
+    kern<<<grid, TL::THREADS, L::smem, stream>>>(mq, mk, mg, mv, mo, p);
     return cudaGetLastError();
 }
 
-// Pick the CTA width (consumer warps): 4-warp CTAs while they fit in one wave
-// (at most one per SM), else 2-warp CTAs for more CTAs per SM; measured on the
-// GLA, Mamba-2, DeltaNet and RWKV-7 workloads, 8 warps never won.  A forced
-// width (SN_OPT_RECUR_TILE) overrides the choice.
-template <int KIND, int DK, int R, int C>
-cudaError_t run_seq_width(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
-                          cudaStream_t stream) {
-    constexpr int COLS_PER_WARP = (32 / (DK / R)) * C;
-    int w = force_w;
-    if (w == 0) {
-        const bool fits4 = x.dv % (4 * COLS_PER_WARP) == 0 &&
-                           (int64_t)x.B * x.H * (x.dv / (4 * COLS_PER_WARP)) <= sm_count;
-        w = (fits4 || x.dv % (2 * COLS_PER_WARP) != 0) ? 4 : 2;
-    }
-    switch (w) {
-        case 2: return run_seq<KIND, DK, R, C, 2>(x, st, wait_ns, stream);
-        case 4: return run_seq<KIND, DK, R, C, 4>(x, st, wait_ns, stream);
-        case 8: return run_seq<KIND, DK, R, C, 8>(x, st, wait_ns, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
+}  // namespace sn
+
+namespace sn {
+
+// Tile choices, measured on the GLA, Mamba-2, DeltaNet and RWKV-7 workloads
+// (a sweep of rows and columns per lane, CTA width and operand read-ahead):
+//   * diagonal kinds with few warps (the GLA shape): 4 rows x 4 columns,
+//     generic operand reads, read-ahead 1; 4-warp CTAs while they fit in one
+//     wave, else 2-warp CTAs;
+//   * diagonal kinds otherwise (the Mamba-2 shape): 8 rows x 2 columns,
+//     4-warp CTAs, read-ahead 1;
+//   * the delta rule: 8 rows x 2 columns, 2-warp CTAs, read-ahead 1;
+//   * RWKV-7: 8 rows x 2 columns, 4-warp CTAs.
+// Only the rows per lane fix the summation order, and they are the ones the
+// earlier tiles used, so these tiles give the same bits.  A forced width
+// (SN_OPT_RECUR_TILE: 2, 4 or 8 warps) replaces the width.
 
 // Warps the sequence kernel would run with R rows x C columns per lane.
 inline int64_t seq_warps(const RecurArgs& x, int R, int C) {
@@ -454,13 +515,48 @@ inline int64_t seq_warps(const RecurArgs& x, int R, int C) {
 }
 
 // Rows per lane of the diagonal-decay kinds: 8 when the problem yields at
-// least DIAG_R8_WARPS warps per SM with 8 rows, else 4 rows, which doubles the
-// warps of a small problem (measured at B4 H4 128x128, 256 warps with 8 rows:
-// GLA 0.346 ms with 4 rows, 0.498 ms with 8).  The single-step decode follows
-// the same rule, so a decode step has the bits of a one-step sequence call.
+// least DIAG_R8_WARPS warps per SM with 8 rows x 4 columns per lane, else 4
+// rows, which keeps small problems (B4 H4 128 x 128) at more warps.  The
+// single-step decode follows the same rule, so a decode step has the bits of
+// a one-step sequence call.
 constexpr int DIAG_R8_WARPS = 4;
 inline bool diag_eight_rows(const RecurArgs& x, int sm_count) {
     return seq_warps(x, 8, 4) >= (int64_t)DIAG_R8_WARPS * sm_count;
+}
+
+// Value columns one consumer warp covers under the tile the dispatch picks.
+inline int seq_cols_per_warp(const RecurArgs& x, int sm_count) {
+    const bool diag = x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_HEAD || x.kind == RK_DIAG_KEY_GATED ||
+                      x.kind == RK_DIAG_HEAD_GATED;
+    const bool small = diag && !diag_eight_rows(x, sm_count);
+    const int R = small ? 4 : 8, C = small ? 4 : 2;
+    return (32 / (x.dk / R)) * C;
+}
+
+template <int KIND, int DK, int R, int C, bool GEN, int PF>
+cudaError_t run_seq_w(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int w, cudaStream_t stream) {
+    switch (w) {
+        case 2: return run_seq<KIND, DK, SeqTile<DK, R, C, 2, GEN, PF>>(x, st, wait_ns, stream);
+        case 4: return run_seq<KIND, DK, SeqTile<DK, R, C, 4, GEN, PF>>(x, st, wait_ns, stream);
+        case 8: return run_seq<KIND, DK, SeqTile<DK, R, C, 8, GEN, PF>>(x, st, wait_ns, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// The diagonal kinds (plain and gated) for key dimension DK.
+template <int KIND, int DK>
+cudaError_t run_seq_diag(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count, int force_w,
+                         cudaStream_t stream) {
+    if (diag_eight_rows(x, sm_count))
+        return run_seq_w<KIND, DK, 8, 2, false, 1>(x, st, wait_ns, force_w ? force_w : 4, stream);
+    int w = force_w;
+    if (w == 0) {
+        constexpr int COLS_PER_WARP = (32 / (DK / 4)) * 4;
+        const bool fits4 = x.dv % (4 * COLS_PER_WARP) == 0 &&
+                           (int64_t)x.B * x.H * (x.dv / (4 * COLS_PER_WARP)) <= sm_count;
+        w = (fits4 || x.dv % (2 * COLS_PER_WARP) != 0) ? 4 : 2;
+    }
+    return run_seq_w<KIND, DK, 4, 4, true, 1>(x, st, wait_ns, w, stream);
 }
 
 }  // namespace sn

@@ -13,6 +13,8 @@
 //    streaming stores.
 //    The LDG variant serves layouts TMA cannot describe (N % 4 != 0 or
 //    unaligned base pointers).
+//  * scan_step -- the single step (T = 1) of every channel, the same
+//    arithmetic, elementwise without the pipeline.
 //  * the chunked look-back kernel lives in scan_lookback.cu.
 #include <algorithm>
 #include <cstdio>
@@ -193,8 +195,67 @@ scan_seq_ldg(int T, int N, const float* __restrict__ a, const float* __restrict_
 
 // ============================================================ launchers
 
+// ============================================================ single step (T = 1)
+// One step of every channel, s = fma(a, s0, inj(a, b)), written to s_out and
+// s_final: the sequential kernel's arithmetic for T = 1, without its
+// pipeline (a single row would fill one stage of its ring).  Elementwise over
+// the B * N channels, VEC channels per thread per iteration, one wave of
+// grid-stride CTAs.
+template <bool GATED, int VEC>
+__global__ void __launch_bounds__(256) scan_step(int64_t n, const float* __restrict__ a,
+                                                 const float* __restrict__ b, const float* s0, float* s_final,
+                                                 float* __restrict__ s_out) {
+    const int64_t nv = n / VEC;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+        float av[VEC], bv[VEC], sv[VEC];
+        if constexpr (VEC == 4) {
+            const float4 ta = __ldcs(reinterpret_cast<const float4*>(a) + i);
+            const float4 tb = __ldcs(reinterpret_cast<const float4*>(b) + i);
+            const float4 ts = s0 != nullptr ? *(reinterpret_cast<const float4*>(s0) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            av[0] = ta.x; av[1] = ta.y; av[2] = ta.z; av[3] = ta.w;
+            bv[0] = tb.x; bv[1] = tb.y; bv[2] = tb.z; bv[3] = tb.w;
+            sv[0] = ts.x; sv[1] = ts.y; sv[2] = ts.z; sv[3] = ts.w;
+        } else {
+            av[0] = __ldcs(a + i);
+            bv[0] = __ldcs(b + i);
+            sv[0] = s0 != nullptr ? s0[i] : 0.f;
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) sv[v] = __fmaf_rn(av[v], sv[v], inj<GATED>(av[v], bv[v]));
+        if constexpr (VEC == 4) {
+            const float4 r = make_float4(sv[0], sv[1], sv[2], sv[3]);
+            if (s_out != nullptr) st_cs(reinterpret_cast<float4*>(s_out) + i, r);
+            if (s_final != nullptr) st_cs(reinterpret_cast<float4*>(s_final) + i, r);
+        } else {
+            if (s_out != nullptr) st_cs(s_out + i, sv[0]);
+            if (s_final != nullptr) st_cs(s_final + i, sv[0]);
+        }
+    }
+}
+
+static cudaError_t launch_scan_step(const ScanArgs& x, bool gated, cudaStream_t stream) {
+    const int64_t n = (int64_t)x.B * x.N;
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool vec = n % 4 == 0 && al16(x.a) && al16(x.b) && al16(x.s0) && al16(x.s_final) && al16(x.s_out);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t items = vec ? n / 4 : n;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((items + 255) / 256, (int64_t)sms * 8));
+    if (vec) {
+        if (gated) scan_step<true, 4><<<grid, 256, 0, stream>>>(n, x.a, x.b, x.s0, x.s_final, x.s_out);
+        else scan_step<false, 4><<<grid, 256, 0, stream>>>(n, x.a, x.b, x.s0, x.s_final, x.s_out);
+    } else {
+        if (gated) scan_step<true, 1><<<grid, 256, 0, stream>>>(n, x.a, x.b, x.s0, x.s_final, x.s_out);
+        else scan_step<false, 1><<<grid, 256, 0, stream>>>(n, x.a, x.b, x.s0, x.s_final, x.s_out);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scan_sequential(const ScanArgs& x, bool gated, SnDevStatus* st, uint64_t wait_ns,
                                    cudaStream_t stream) {
+    if (x.T == 1) return launch_scan_step(x, gated, stream);
     if (scan_tma_ok(x)) {
         CUtensorMap ma, mb;
         if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, S1_NC, S1_TS) ||

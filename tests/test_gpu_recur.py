@@ -285,13 +285,12 @@ def test_decode_matches_sequence_kernel_at_t1(sr, ctx):
     assert _nrel(o1, ro) <= TOL and _nrel(o2, ro) <= TOL and _nrel(S2, rS) <= TOL
 
 
-@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "gated_key", "gated_head"])
-@pytest.mark.parametrize("dims", [(128, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "gated_key", "gated_head", "rwkv"])
+@pytest.mark.parametrize("dims", [(128, 128), (128, 64), (64, 64), (64, 128)])
 def test_column_decode_matches_sequence_kernel_bit_for_bit(sr, ctx, kind, dims):
-    """T = 1 of the diagonal kinds and the delta rule runs the column decode
-    kernel, which sums in the sequence kernel's 8-rows-per-lane order; at this
-    batch the sequence kernel runs 8 rows per lane too, so a forced one-step
-    sequence call must give the same bits for o and the state."""
+    """T = 1 of every kind runs the column decode kernel, which sums in the
+    sequence kernel's order for the same call (rows per lane); a forced
+    one-step sequence call must give the same bits for o and the state."""
     dk, dv = dims
     B, H = 64, 4
     x = make(kind, B, 1, H, dk, dv, G=2 if kind == "mamba2" else None, seed=11)
@@ -415,19 +414,23 @@ def test_cta_widths_give_identical_bits(sr, ctx, kind):
     assert _nrel(outs[0][0], ro) <= TOL and _nrel(outs[0][1], rS) <= TOL
 
 
-def test_forced_width_that_does_not_tile_the_columns_is_rejected(sr, ctx):
-    """A forced CTA width whose columns the value dimension does not divide
-    (RWKV-7 64 x 64: 16 columns per warp, so 8 warps need 128) is an argument
-    error found on the host, before any launch; outputs stay untouched."""
-    x = make("rwkv", 1, 8, 2, 64, 64, seed=9)
-    o = torch.full((1, 8, 2, 64), 7.0, device="cuda")
-    S = torch.full((1, 2, 64, 64), 7.0, device="cuda")
-    ctx.set_option(sr.SN_OPT_RECUR_TILE, 8)
+@pytest.mark.parametrize("kind", ["gla", "mamba2", "delta", "rwkv"])
+def test_forced_widths_on_64_value_columns(sr, ctx, kind):
+    """Every CTA width (2, 4, 8 warps) tiles a 64-column value dimension, is
+    accepted on the host and gives the automatic width's bits."""
+    B, T, H, dv = 2, 37, 2, 64
+    dk = 64 if kind == "rwkv" else 128
+    x = make(kind, B, T, H, dk, dv, G=1 if kind == "mamba2" else None, seed=9)
+    S0 = synth.normal(state_shape(kind, B, H, dk, dv), 5401)
+    run, ref = RUN[kind]
+    outs = []
     try:
-        st = sr.sn_recur_rwkv7(ctx.handle, 1, 8, 2, 64, 64, *(cu(x[n]) for n in ("q", "k", "v", "w")), None, S, o)
+        for w in (0, 2, 4, 8):
+            ctx.set_option(sr.SN_OPT_RECUR_TILE, w)
+            outs.append(run(ctx, x, S0))
     finally:
         ctx.set_option(sr.SN_OPT_RECUR_TILE, 0)
-    torch.cuda.synchronize()
-    assert st == sr.SN_E_INVAL
-    assert bool((o == 7.0).all()) and bool((S == 7.0).all())
-
+    for o, S in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(S, outs[0][1])
+    ro, rS = ref(x, S0)
+    assert _nrel(outs[0][0], ro) <= TOL and _nrel(outs[0][1], rS) <= TOL

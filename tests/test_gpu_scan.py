@@ -75,6 +75,33 @@ def test_sequential_bit_exact_and_within_tolerance(ctx, form, shape):
 
 
 @pytest.mark.parametrize("form", ["fma", "gated"])
+@pytest.mark.parametrize("shape", [(1024, 1, 2048), (1, 1, 2048), (3, 1, 7), (5, 1, 130)])
+def test_single_step_bit_exact_in_place_and_views(ctx, form, shape):
+    """T = 1 (the single-step entry) runs its own elementwise kernel with the
+    sequential kernel's arithmetic: the fp32 definition's bits, in place
+    (s_final == s0), without s0, and on unaligned views (plain-load path)."""
+    B, T, N = shape
+    a, b, u, s0 = _inputs(B, T, N, 40 + N % 11)
+    rhs = b if form == "fma" else u
+    so, sf = _run(ctx, form, a, rhs, s0)
+    r32, f32 = _ref(form, a, rhs, s0, "f32")
+    assert np.array_equal(so, r32) and np.array_equal(sf, f32)
+    fn = ctx.scan_fma if form == "fma" else ctx.scan_gated
+    st = s0.cuda().clone()
+    fn(a.cuda(), rhs.cuda(), st, s_out=None, s_final=st)
+    torch.cuda.synchronize()
+    assert np.array_equal(st.cpu().numpy(), f32)
+    so0, _ = _run(ctx, form, a, rhs, None)
+    assert np.array_equal(so0, _ref(form, a, rhs, None, "f32")[0])
+    big_a, big_r = torch.zeros(B * N + 1), torch.zeros(B * N + 1)
+    big_a[1:] = a.reshape(-1)
+    big_r[1:] = rhs.reshape(-1)
+    so1, sf1 = fn(big_a.cuda()[1:].view(B, T, N), big_r.cuda()[1:].view(B, T, N), s0.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(so1.cpu().numpy(), r32) and np.array_equal(sf1.cpu().numpy(), f32)
+
+
+@pytest.mark.parametrize("form", ["fma", "gated"])
 def test_small_workload_config(ctx, form):
     """B=2 T=128 N=128, a = sigmoid(N(0,1)), s0 = 0 (the pages' parity size)."""
     x = synth.config_inputs("scan_small")
