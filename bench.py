@@ -175,28 +175,255 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "in_timed_region": bool(inwin)}
 
 
-# ---------------------------------------------------------------- CPU baseline
-def cpu_oracle_scan(a, b, u, s0, threads, prec="f64"):
-    """Time the CPU oracle (fp64 or fp32) on both scan forms; the batch rows
-    are independent, so they run on `threads` Python threads (ctypes releases
-    the GIL).  Returns seconds."""
-    import concurrent.futures as cf
+# ---------------------------------------------------------------- CPU oracle record
+# The oracle runs on the machine's host cores in two ways (the pages time their C
+# scan single-threaded, one subprocess per cell with the median of repeated
+# runs, "SunnyNet 工程化实录" §2.3):
+#   * all cores: the workload split into independent units -- (batch row,
+#     block of 128 channels) for the scans, (batch, head) for the matrix
+#     recurrences, batch blocks for single-step decodes -- on one thread per
+#     logical CPU (ctypes releases the GIL inside the oracle);
+#   * one thread: the median of repeated runs of one unit.
+# The fp64 all-core run also supplies the reference the GPU outputs are
+# measured against.
+SCAN_BLOCK = 128
+PAGES_ERR = {   # the pages' own accuracy figures (max |diff| on O(1) data), for context
+    "scan": (7.63e-06, "SunnyNet 工程化实录 §2.3 (C scan against torch)"),
+    "deltanet": (4.6e-05, "SunnyNet 工程化实录 §4.2 (DeltaNet against its reference)"),
+    "gla": (2.05e-05, "SunnyNet 工程化实录 §4.3 (GLA against its reference)"),
+}
 
+
+def host_cores():
+    return os.cpu_count() or 1
+
+
+def run_pool(tasks, threads):
+    """Run zero-argument callables on `threads` threads; results in order and
+    wall seconds."""
+    import concurrent.futures as cf
+    t0 = time.perf_counter()
+    if threads <= 1:
+        res = [t() for t in tasks]
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            res = list(ex.map(lambda f: f(), tasks))
+    return res, time.perf_counter() - t0
+
+
+class OracleJob:
+    """A workload cut into independent oracle units.  `units` is a list of
+    (slices, fn) with fn(prec) running the oracle on that unit; `place`
+    copies a unit's fp64 result into the full reference arrays; `nbytes` and
+    `tok_heads` are the algorithmic bytes and token-heads of the whole job and
+    `unit_share` the fraction one unit holds."""
+
+    def __init__(self, units, outputs, place, nbytes, tok_heads=None, what=""):
+        self.units, self.outputs, self.place = units, outputs, place
+        self.nbytes, self.tok_heads, self.what = nbytes, tok_heads, what
+        self.unit_share = 1.0 / len(units)
+
+    def run_all(self, prec, threads):
+        res, secs = run_pool([(lambda f=f: f(prec)) for _, f in self.units], threads)
+        return res, secs
+
+    def reference(self, threads):
+        """fp64 all-core run: (reference arrays, seconds)."""
+        import numpy as np
+        res, secs = self.run_all("f64", threads)
+        ref = {k: np.empty(shape, np.float64) for k, shape in self.outputs.items()}
+        for (sl, _), r in zip(self.units, res):
+            self.place(ref, sl, r)
+        return ref, secs
+
+    def one_thread(self, prec, reps):
+        f = self.units[0][1]
+        f(prec)                                  # warm (library loaded, pages touched)
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            f(prec)
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts)
+
+    def rate(self, secs, share=1.0):
+        r = {"GBps": round(self.nbytes * share / secs / GB, 4), "s": round(secs, 4)}
+        if self.tok_heads is not None:
+            r["tok_heads_per_s"] = round(self.tok_heads * share / secs, 1)
+        return r
+
+
+def scan_job(a, rhs, s0, forms=("fma", "gated"), block=SCAN_BLOCK):
+    """The elementwise scans cut into (batch row, block of channels) units; a
+    unit runs every form in `forms` (rhs maps a form to its b or u array).
+    Single steps (T = 1) are cut into blocks of batch rows instead."""
     import numpy as np
 
     import oracle
-    B = a.shape[0]
-    s0p = s0.astype(np.float64) if prec == "f64" else s0
+    B, T, N = a.shape
+    fns = {"fma": oracle.scan_fma, "gated": oracle.scan_gated}
+    units = []
 
-    def one(i):
-        oracle.scan_fma(a[i:i + 1], b[i:i + 1], s0p[i:i + 1], prec=prec)
-        oracle.scan_gated(a[i:i + 1], u[i:i + 1], s0p[i:i + 1], prec=prec)
+    def make(sl, au, ru, su):
+        return lambda prec: [fns[f](au, ru[f], su, prec=prec) for f in forms]
 
-    oracle.scan_fma(a[:1, :8], b[:1, :8], s0p[:1], prec=prec)   # load the library outside the timing
-    t0 = time.perf_counter()
-    with cf.ThreadPoolExecutor(threads) as ex:
-        list(ex.map(one, range(B)))
-    return time.perf_counter() - t0
+    if T == 1:
+        step = max(1, B // 64)
+        for b0 in range(0, B, step):
+            b1 = min(B, b0 + step)
+            sl = (b0, b1, 0, N)
+            units.append((sl, make(sl, a[b0:b1], {f: rhs[f][b0:b1] for f in forms},
+                                   None if s0 is None else s0[b0:b1])))
+    else:
+        for b in range(B):
+            for n0 in range(0, N, block):
+                n1 = min(N, n0 + block)
+                sl = (b, b + 1, n0, n1)
+                au = np.ascontiguousarray(a[b:b + 1, :, n0:n1])
+                ru = {f: np.ascontiguousarray(rhs[f][b:b + 1, :, n0:n1]) for f in forms}
+                su = None if s0 is None else np.ascontiguousarray(s0[b:b + 1, n0:n1])
+                units.append((sl, make(sl, au, ru, su)))
+
+    def place(ref, sl, r):
+        b0, b1, n0, n1 = sl
+        for f, (so, sf) in zip(forms, r):
+            ref[f"s_{f}"][b0:b1, :, n0:n1] = so
+            ref[f"s_final_{f}"][b0:b1, n0:n1] = sf
+
+    outputs = {}
+    for f in forms:
+        outputs[f"s_{f}"] = (B, T, N)
+        outputs[f"s_final_{f}"] = (B, N)
+    unit_what = "batch-row blocks" if T == 1 else f"(batch row, {block}-channel block) units"
+    return OracleJob(units, outputs, place, len(forms) * scan_bytes(B, T, N, s0 is not None),
+                     what=f"{unit_what}, forms {'+'.join(forms)}")
+
+
+def scan_bwd_job(a, s, s0, gs, u=None, block=SCAN_BLOCK):
+    """The reverse scan of one form (gated when u is given), cut like the
+    forward scans; used for its fp64 reference only."""
+    import numpy as np
+
+    import oracle
+    B, T, N = a.shape
+    kind = "fma" if u is None else "gated"
+    units = []
+    for b in range(B):
+        for n0 in range(0, N, block):
+            n1 = min(N, n0 + block)
+            cut = lambda x: None if x is None else np.ascontiguousarray(x[b:b + 1, ..., n0:n1])
+            args = (cut(a), cut(s), cut(s0), cut(gs), cut(u))
+            units.append(((b, n0, n1), lambda prec, q=args: oracle.scan_backward(
+                kind, q[0], q[1], q[2], q[3], None, q[4], prec=prec)))
+
+    def place(ref, sl, r):
+        b, n0, n1 = sl
+        ref["grad_a"][b, :, n0:n1] = r[0][0]
+        ref["grad_bu"][b, :, n0:n1] = r[1][0]
+        ref["grad_s0"][b, n0:n1] = r[2][0]
+
+    nb = (20 if u is None else 24) * B * T * N + 8 * B * N
+    return OracleJob(units, {"grad_a": (B, T, N), "grad_bu": (B, T, N), "grad_s0": (B, N)}, place, nb,
+                     what=f"(batch row, {block}-channel block) units")
+
+
+def matrix_job(kind, x, B, T, H, dk, dv, nbytes, G=None):
+    """A matrix recurrence cut into (batch, head) units, or into batch blocks
+    of all heads for a single step.  kind: diag | delta | rwkv7; x holds host
+    float32 arrays q, k, v, g (decays, beta or w) and optional S0, plus
+    decay_kind and scale for diag."""
+    import numpy as np
+
+    import oracle
+    G = G or H
+    S_shape = (B, H, dv, dk) if kind == "rwkv7" else (B, H, dk, dv)
+    S0 = x.get("S0")
+
+    def call(q, k, v, g, s0, Hu, Gu, prec):
+        if kind == "diag":
+            return oracle.recur_diag(q, k, v, g, s0, H=Hu, G=Gu, decay_kind=x["decay_kind"], scale=x["scale"],
+                                     prec=prec)
+        if kind == "delta":
+            return oracle.recur_delta(q, k, v, g, s0, scale=x["scale"], prec=prec)
+        return oracle.recur_rwkv7(q, k, v, g, s0, prec=prec)
+
+    units = []
+    if T == 1:
+        step = max(1, B // 64)
+        for b0 in range(0, B, step):
+            b1 = min(B, b0 + step)
+            args = [x[n][b0:b1] for n in ("q", "k", "v", "g")] + [None if S0 is None else S0[b0:b1]]
+            units.append((("b", b0, b1), lambda prec, a=args: call(*a, H, G, prec)))
+    else:
+        for b in range(B):
+            for h in range(H):
+                gi = h // (H // G)
+                qk = [np.ascontiguousarray(x[n][b:b + 1, :, gi:gi + 1]) for n in ("q", "k")]
+                vu = np.ascontiguousarray(x["v"][b:b + 1, :, h:h + 1])
+                gu = np.ascontiguousarray(x["g"][b:b + 1, :, h:h + 1])   # per key (B,T,H,dk) or per head (B,T,H)
+                su = None if S0 is None else np.ascontiguousarray(S0[b:b + 1, h:h + 1])
+                units.append((("bh", b, h), lambda prec, a=(qk[0], qk[1], vu, gu, su): call(*a, 1, 1, prec)))
+
+    def place(ref, sl, r):
+        o, S = r
+        if sl[0] == "b":
+            ref["o"][sl[1]:sl[2]] = o
+            ref["S"][sl[1]:sl[2]] = S
+        else:
+            ref["o"][sl[1]:sl[1] + 1, :, sl[2]:sl[2] + 1] = o
+            ref["S"][sl[1]:sl[1] + 1, sl[2]:sl[2] + 1] = S
+
+    what = "batch blocks of all heads" if T == 1 else "(batch, head) units"
+    return OracleJob(units, {"o": (B, T, H, dv), "S": S_shape}, place, nbytes, tok_heads=B * T * H, what=what)
+
+
+def err_pair(y, r):
+    """(normwise, elementwise) error of y against the fp64 reference r:
+    max|y - r| / max|r|, and max |y - r| / max(|r|, 1e-3 max|r|)."""
+    import numpy as np
+    y = np.asarray(y, np.float64)
+    r = np.asarray(r, np.float64)
+    m = float(np.max(np.abs(r))) if r.size else 0.0
+    d = np.abs(y - r)
+    nw = float(np.max(d)) / max(m, 1e-300)
+    ew = float(np.max(d / np.maximum(np.abs(r), 1e-3 * m + 1e-300)))
+    return nw, ew
+
+
+def errors(outs, ref, tol, pages=None):
+    """Per-output error figures against the fp64 oracle, with the bound."""
+    rec = {"err_normwise": {}, "err_elementwise": {}, "tolerance": tol}
+    for k, y in outs.items():
+        nw, ew = err_pair(y, ref[k])
+        rec["err_normwise"][k] = float(f"{nw:.3e}")
+        rec["err_elementwise"][k] = float(f"{ew:.3e}")
+    rec["within_tolerance"] = all(v <= tol for v in rec["err_normwise"].values())
+    if pages is not None:
+        rec["pages_max_abs_diff"] = {"value": pages[0], "where": pages[1]}
+    return rec
+
+
+def cpu_record(job, reps_1t=3, want_ref=True):
+    """The four CPU oracle figures of one workload and (optionally) its fp64
+    reference.  Returns (record, reference or None)."""
+    cores = host_cores()
+    threads = min(len(job.units), cores)
+    ref, s64 = job.reference(threads) if want_ref else (None, None)
+    if s64 is None:
+        _, s64 = job.run_all("f64", threads)
+    _, s32 = job.run_all("f32", threads)
+    t64 = job.one_thread("f64", reps_1t)
+    t32 = job.one_thread("f32", reps_1t)
+    hinfo = {"threads": threads, "logical_cpus": cores, "cpu_model": cpu_model()}
+    rec = {
+        "cpu_fp64_all": dict(job.rate(s64), **hinfo, sample=f"the whole workload, {len(job.units)} {job.what}"),
+        "cpu_fp32_all": dict(job.rate(s32), **hinfo, sample=f"the whole workload, {len(job.units)} {job.what}"),
+        "cpu_fp64_1t": dict(job.rate(t64, job.unit_share), threads=1, cpu_model=hinfo["cpu_model"],
+                            sample=f"one unit ({job.unit_share:.3g} of the workload), median of {reps_1t}"),
+        "cpu_fp32_1t": dict(job.rate(t32, job.unit_share), threads=1, cpu_model=hinfo["cpu_model"],
+                            sample=f"one unit ({job.unit_share:.3g} of the workload), median of {reps_1t}"),
+    }
+    return rec, ref
 
 
 def cpu_model():
@@ -221,21 +448,24 @@ def cpu_model():
 
 def run_reference(args):
     """The reference arm: the CPU oracle as it stands, on this arm's workload
-    (the full B=8 T=8192 N=2048 scan, both forms, inputs drawn on the CPU)."""
+    (the full B=8 T=8192 N=2048 scan, both forms, inputs drawn on the CPU),
+    fp64, the workload's independent units on every host core."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     x = synth.config_inputs("scan_large")
     a, b, u, s0 = (x[n].numpy() for n in ("a", "b", "u", "s0"))
     B, T, N = a.shape
-    threads = min(B, os.cpu_count() or 1)
+    job = scan_job(a, {"fma": b, "gated": u}, s0)
+    threads = min(len(job.units), host_cores())
     for _ in range(args.warmup):
-        cpu_oracle_scan(a, b, u, s0, threads)
-    times = [cpu_oracle_scan(a, b, u, s0, threads) for _ in range(args.steps)]
+        job.run_all("f64", threads)
+    times = [job.run_all("f64", threads)[1] for _ in range(args.steps)]
     per_step_bytes = 2 * scan_bytes(B, T, N)
     total = sum(times)
     value = args.steps * per_step_bytes / total / GB
-    sample = f"the full workload B=8 T=8192 N=2048 per step, both forms, fp64 oracle, batch rows on {threads} threads"
+    sample = (f"the full workload B=8 T=8192 N=2048 per step, both forms, fp64 oracle, {len(job.units)} "
+              f"{job.what} on {threads} threads ({cpu_model()})")
     line = {
         "impl": "reference", "metric": "recurrence_scan_GBps", "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -309,38 +539,64 @@ def time_form(torch, fn, warmup, reps, stream, flush=None):
 GRAPH_CALLS = 16   # scan calls captured in one CUDA graph for the small-workload latency
 
 
-def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=3, reps=20):
+def host(t):
+    """A device tensor's values as a host numpy array (None stays None)."""
+    return None if t is None else t.detach().cpu().numpy()
+
+
+def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, cpu=True, scan_ref=None,
+                warmup=3, reps=20):
     """Every other workload, each on its own inputs, outside the main timed
-    region.  Returns a dict of per-form results."""
+    region.  With `cpu`, each workload also gets its CPU-oracle figures and
+    the error of every GPU output against the fp64 oracle (`scan_ref` is the
+    large scan's fp64 reference, computed by the caller).  Returns a dict of
+    per-form results."""
+    import numpy as np
     out = {}
     s = stream
+    flush = torch.empty(64 << 20, device=dev)          # 256 MB, larger than L2
     with torch.cuda.stream(stream):
         # the small scan workload (0.4 MB, fits in L2): per-call latency of both
         # forms, launched directly and replayed from a CUDA graph of GRAPH_CALLS
-        # calls; L2 is flushed before every timed call or replay
+        # calls; L2 is flushed before every timed call or replay.  The
+        # single-step scans (T = 1) are measured the same way.
         c = synth.CONFIGS["scan_small"]
-        Bs, Ts, Ns = c["B"], c["T"], c["N"]
-        xs = synth.config_inputs("scan_small", device=dev)
-        sos = torch.empty((Bs, Ts, Ns), device=dev)
-        sfs = torch.empty((Bs, Ns), device=dev)
-        flush = torch.empty(64 << 20, device=dev)          # 256 MB
-        small = {"workload": f"B={Bs} T={Ts} N={Ns}", "bytes_per_call": scan_bytes(Bs, Ts, Ns), "l2": "flushed",
-                 "graph_calls": GRAPH_CALLS}
-        for form, rhs in (("fma", "b"), ("gated", "u")):
-            f = sr.sn_scan_fma if form == "fma" else sr.sn_scan_gated
-            call = lambda: f(ctx.handle, Bs, Ts, Ns, xs["a"], xs[rhs], xs["s0"], sfs, sos, s)
-            direct = time_form(torch, call, warmup, reps, s, flush=flush)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                for _ in range(GRAPH_CALLS):
-                    call()
-            replay = time_form(torch, g.replay, warmup, reps, s, flush=flush)
-            small[form] = {"us_per_call": round(direct * 1e3, 2),
-                           "us_per_call_graph": round(replay * 1e3 / GRAPH_CALLS, 2)}
-            del g
-        out["scan_small"] = small
-        del flush, xs, sos, sfs
+        for label, (Bs, Ts, Ns), maker in (
+                ("scan_small", (c["B"], c["T"], c["N"]), lambda: synth.config_inputs("scan_small", device=dev)),
+                ("scan_step_B1024", (1024, 1, 2048),
+                 lambda: synth.scan_inputs(1024, 1, 2048, large=True, cid=31, device=dev)),
+                ("scan_step_B1", (1, 1, 2048), lambda: synth.scan_inputs(1, 1, 2048, large=True, cid=32, device=dev))):
+            xs = maker()
+            sos = {f: torch.empty((Bs, Ts, Ns), device=dev) for f in ("fma", "gated")}
+            sfs = {f: torch.empty((Bs, Ns), device=dev) for f in ("fma", "gated")}
+            nb = scan_bytes(Bs, Ts, Ns, xs["s0"] is not None)
+            rec = {"workload": f"B={Bs} T={Ts} N={Ns}", "bytes_per_call": nb, "l2": "flushed",
+                   "graph_calls": GRAPH_CALLS}
+            for form, rhs in (("fma", "b"), ("gated", "u")):
+                f = sr.sn_scan_fma if form == "fma" else sr.sn_scan_gated
+                call = lambda: f(ctx.handle, Bs, Ts, Ns, xs["a"], xs[rhs], xs["s0"], sfs[form], sos[form], s)
+                direct = time_form(torch, call, warmup, reps, s, flush=flush)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    for _ in range(GRAPH_CALLS):
+                        call()
+                replay = time_form(torch, g.replay, warmup, reps, s, flush=flush)
+                rec[form] = {"us_per_call": round(direct * 1e3, 2),
+                             "us_per_call_graph": round(replay * 1e3 / GRAPH_CALLS, 2),
+                             "GBps": round(nb / direct / 1e6, 1),
+                             "GBps_graph": round(nb / (replay / GRAPH_CALLS) / 1e6, 1)}
+                del g
+            if cpu:
+                xh = {n: host(xs[n]) for n in ("a", "b", "u", "s0")}
+                job = scan_job(xh["a"], {"fma": xh["b"], "gated": xh["u"]}, xh["s0"])
+                crec, ref = cpu_record(job, reps_1t=10)
+                rec.update(crec)
+                rec.update(errors({f"s_{f}": host(sos[f]) for f in ("fma", "gated")} |
+                                  {f"s_final_{f}": host(sfs[f]) for f in ("fma", "gated")}, ref, 1e-5,
+                                  PAGES_ERR["scan"]))
+            out[label] = rec
+            del xs, sos, sfs
         # the chunked look-back kernel on the same large scan workload
         x = synth.config_inputs("scan_large", device=dev)
         B, T, N = SCAN["B"], SCAN["T"], SCAN["N"]
@@ -352,11 +608,16 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
             f = sr.sn_scan_fma if form == "fma" else sr.sn_scan_gated
             ms = time_form(torch, lambda: f(ctx.handle, B, T, N, x["a"], x[rhs], x["s0"], sf, so, s), warmup, reps, s)
             nb = scan_bytes(B, T, N)
-            out[f"scan_{form}_lookback"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
-                                           "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
+            r = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
+                 "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
+            if scan_ref is not None:
+                r.update(errors({"s": host(so), "s_final": host(sf)},
+                                {"s": scan_ref[f"s_{form}"], "s_final": scan_ref[f"s_final_{form}"]}, 1e-5))
+            out[f"scan_{form}_lookback"] = r
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
         # few channels, long T (B=1 T=262144 N=64, the chunked kernels' regime):
-        # the automatic choice (reduce-then-scan) and the look-back kernel
+        # the automatic choice (reduce-then-scan), the look-back kernel and the
+        # sequential kernel
         Bf, Tf, Nf = 1, 262144, 64
         xf = synth.scan_inputs(Bf, Tf, Nf, large=True, cid=6)
         af, bf, s0f = xf["a"].to(dev), xf["b"].to(dev), xf["s0"].to(dev)
@@ -364,6 +625,10 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
         sff = torch.empty_like(s0f)
         ctx.ensure_workspace(Bf, Tf, Nf)
         few = {"workload": f"B={Bf} T={Tf} N={Nf}", "bytes_per_call": scan_bytes(Bf, Tf, Nf)}
+        fref = None
+        if cpu:
+            fjob = scan_job(xf["a"].numpy(), {"fma": xf["b"].numpy()}, xf["s0"].numpy(), forms=("fma",), block=1)
+            fref, _ = fjob.reference(min(len(fjob.units), host_cores()))
         for label, kern in (("reduce_scan", sr.SN_SCAN_KERNEL_REDUCE_SCAN), ("lookback", sr.SN_SCAN_KERNEL_LOOKBACK),
                             ("sequential", sr.SN_SCAN_KERNEL_SEQUENTIAL)):
             ctx.set_option(sr.SN_OPT_SCAN_KERNEL, kern)
@@ -371,6 +636,9 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                            reps, s)
             few[label] = {"ms": round(ms, 4), "GBps": round(scan_bytes(Bf, Tf, Nf) / ms / 1e6, 1),
                           "hbm_frac": round(scan_bytes(Bf, Tf, Nf) / ms / 1e6 / hbm_peak, 3)}
+            if fref is not None:
+                few[label].update(errors({"s": host(sof), "s_final": host(sff)},
+                                         {"s": fref["s_fma"], "s_final": fref["s_final_fma"]}, 1e-5))
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
         few["auto_picks"] = "reduce_scan"
         out["scan_fma_few_channels"] = few
@@ -380,34 +648,50 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
         daf, dbf, d0f = torch.empty_like(af), torch.empty_like(af), torch.empty_like(s0f)
         nbb = 20 * Bf * Tf * Nf + 8 * Bf * Nf
         fewb = {"workload": f"B={Bf} T={Tf} N={Nf}", "bytes_per_call": nbb}
+        bref = None
+        if cpu:
+            bjob = scan_bwd_job(host(af), host(sof), host(s0f), host(gsf), block=1)
+            bref, _ = bjob.reference(min(len(bjob.units), host_cores()))
         for label, kern in (("chunked", sr.SN_SCAN_KERNEL_REDUCE_SCAN), ("sequential", sr.SN_SCAN_KERNEL_SEQUENTIAL)):
             ctx.set_option(sr.SN_OPT_SCAN_KERNEL, kern)
             ms = time_form(torch, lambda: sr.sn_scan_fma_backward(ctx.handle, Bf, Tf, Nf, af, s0f, sof, gsf, None,
                                                                    daf, dbf, d0f, s), warmup, reps, s)
             fewb[label] = {"ms": round(ms, 4), "GBps": round(nbb / ms / 1e6, 1),
                            "hbm_frac": round(nbb / ms / 1e6 / hbm_peak, 3)}
+            if bref is not None:
+                fewb[label].update(errors({"grad_a": host(daf), "grad_b": host(dbf), "grad_s0": host(d0f)},
+                                          {"grad_a": bref["grad_a"], "grad_b": bref["grad_bu"],
+                                           "grad_s0": bref["grad_s0"]}, 1e-5))
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
         fewb["auto_picks"] = "chunked"
         out["scan_fma_backward_few_channels"] = fewb
-        del xf, af, bf, s0f, sof, sff, gsf, daf, dbf, d0f
+        del xf, af, bf, s0f, sof, sff, gsf, daf, dbf, d0f, fref, bref
         # reverse scans (backward pass) on the same workload: read a, s, ds (+u),
         # write da, db|du
         gs_ = torch.empty((B, T, N), device=dev).normal_(generator=torch.Generator(dev).manual_seed(77))
         da = torch.empty((B, T, N), device=dev)
         db = torch.empty((B, T, N), device=dev)
         d0 = torch.empty((B, N), device=dev)
-        sr.sn_scan_fma(ctx.handle, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
         for form in ("fma", "gated"):
             if form == "fma":
+                sr.sn_scan_fma(ctx.handle, B, T, N, x["a"], x["b"], x["s0"], sf, so, s)
                 f = lambda: sr.sn_scan_fma_backward(ctx.handle, B, T, N, x["a"], x["s0"], so, gs_, None, da, db, d0, s)
                 nb = 20 * B * T * N + 8 * B * N
             else:
+                sr.sn_scan_gated(ctx.handle, B, T, N, x["a"], x["u"], x["s0"], sf, so, s)
                 f = lambda: sr.sn_scan_gated_backward(ctx.handle, B, T, N, x["a"], x["u"], x["s0"], so, gs_, None, da,
                                                       db, d0, s)
                 nb = 24 * B * T * N + 8 * B * N
             ms = time_form(torch, f, warmup, reps, s)
-            out[f"scan_{form}_backward"] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
-                                            "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
+            r = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
+                 "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm"}
+            if cpu:
+                bjob = scan_bwd_job(host(x["a"]), host(so), host(x["s0"]), host(gs_),
+                                    u=host(x["u"]) if form == "gated" else None)
+                bref, _ = bjob.reference(min(len(bjob.units), host_cores()))
+                r.update(errors({"grad_a": host(da), "grad_bu": host(db), "grad_s0": host(d0)}, bref, 1e-5))
+                del bref
+            out[f"scan_{form}_backward"] = r
         del x, so, sf, gs_, da, db, d0
         for name in ("gla", "mamba2", "deltanet", "rwkv7_prefill", "rwkv7_decode", "gated_memory"):
             c = synth.CONFIGS[name]
@@ -415,14 +699,17 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
             Bc, Tc, H, dk, dv = c["B"], c["T"], c["H"], c["dk"], c["dv"]
             o = torch.empty((Bc, Tc, H, dv), device=dev)
             if name in ("gla", "mamba2", "gated_memory"):
+                kind, gname = "diag", "d"
                 S = torch.empty((Bc, H, dk, dv), device=dev)
                 fn = lambda: sr.sn_recur_diag(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"], x["scale"],
                                               x["q"], x["k"], x["v"], x["d"], None, S, o, s)
             elif name == "deltanet":
+                kind, gname = "delta", "beta"
                 S = torch.empty((Bc, H, dk, dv), device=dev)
                 fn = lambda: sr.sn_recur_delta(ctx.handle, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"], x["v"],
                                                x["beta"], None, S, o, s)
             else:
+                kind, gname = "rwkv7", "w"
                 S = torch.empty((Bc, H, dv, dk), device=dev)
                 fn = lambda: sr.sn_recur_rwkv7(ctx.handle, Bc, Tc, H, dk, dv, x["q"], x["k"], x["v"], x["w"],
                                                x["S0"], S, o, s)
@@ -439,43 +726,48 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                  "fp32_frac": round(tflops / fp32_peak_tflops, 3)}
             r["bound"] = "hbm" if name == "rwkv7_decode" else "alu"
             out[name] = r
-            if name == "deltanet":
-                # the chunked tensor-core delta rule on the same workload (tf32 operands)
-                ctx.ensure_workspace_bytes(sr.sn_recur_delta_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
-                fc = lambda: sr.sn_recur_delta_chunked(ctx.handle, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"],
-                                                       x["v"], x["beta"], None, S, o, s)
-                st = fc()
-                if st != sr.SN_OK:
-                    out["deltanet_chunked_tc"] = {"error": sr.sn_status_str(st)}
-                else:
-                    ms = time_form(torch, fc, warmup, reps, s)
-                    tf = delta_tensor_flops(Bc, Tc, H, dk, dv) / ms / 1e9
-                    out["deltanet_chunked_tc"] = {
-                        "ms": round(ms, 4), "tok_heads_per_s": round(th / ms * 1e3, 1),
-                        "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
-                        "TFLOPs_tf32": round(tf, 2), "tf32_frac": round(tf / tf32_peak_tflops(), 4),
-                        "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "latency",
-                        "tolerance": 2e-3}
-                assert ctx.last_error() == sr.SN_OK
-            if name in ("gla", "mamba2", "gated_memory"):
+            torch.cuda.synchronize()
+            got = {"o": host(o), "S": host(S)}
+            chunked = None
+            if name in ("gla", "mamba2", "gated_memory", "deltanet"):
                 # the chunked tensor-core form of the same workload (tf32 operands)
-                ctx.ensure_workspace_bytes(sr.sn_recur_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
-                fc = lambda: sr.sn_recur_diag_chunked(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"],
-                                                      x["scale"], x["q"], x["k"], x["v"], x["d"], None, S, o, s)
+                if name == "deltanet":
+                    ctx.ensure_workspace_bytes(sr.sn_recur_delta_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
+                    fc = lambda: sr.sn_recur_delta_chunked(ctx.handle, Bc, Tc, H, dk, dv, x["scale"], x["q"], x["k"],
+                                                           x["v"], x["beta"], None, S, o, s)
+                    tflop = delta_tensor_flops(Bc, Tc, H, dk, dv)
+                else:
+                    ctx.ensure_workspace_bytes(sr.sn_recur_chunked_workspace_bytes(Bc, Tc, H, dk, dv))
+                    fc = lambda: sr.sn_recur_diag_chunked(ctx.handle, Bc, Tc, H, x["G"], dk, dv, x["decay_kind"],
+                                                          x["scale"], x["q"], x["k"], x["v"], x["d"], None, S, o, s)
+                    tflop = chunked_tensor_flops(Bc, Tc, H, dk, dv)
                 st = fc()
                 if st != sr.SN_OK:
                     out[name + "_chunked_tc"] = {"error": sr.sn_status_str(st)}
                 else:
                     ms = time_form(torch, fc, warmup, reps, s)
-                    tf = chunked_tensor_flops(Bc, Tc, H, dk, dv) / ms / 1e9
+                    tf = tflop / ms / 1e9
                     out[name + "_chunked_tc"] = {
                         "ms": round(ms, 4), "tok_heads_per_s": round(th / ms * 1e3, 1),
                         "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
                         "TFLOPs_tf32": round(tf, 2), "tf32_frac": round(tf / tf32_peak_tflops(), 4),
                         "speedup_vs_sequence_kernel": round(r["ms"] / ms, 2), "bound": "latency",
                         "tolerance": 2e-3}
+                    torch.cuda.synchronize()
+                    chunked = {"o": host(o), "S": host(S)}
                 assert ctx.last_error() == sr.SN_OK
-            del x, o, S
+            if cpu:
+                xh = {"q": host(x["q"]), "k": host(x["k"]), "v": host(x["v"]), "g": host(x[gname]),
+                      "S0": host(x.get("S0")), "scale": x.get("scale", 1.0), "decay_kind": x.get("decay_kind")}
+                job = matrix_job(kind, xh, Bc, Tc, H, dk, dv, nb, G=x.get("G", H))
+                crec, ref = cpu_record(job)
+                r.update(crec)
+                pages = PAGES_ERR.get("gla" if name == "gla" else name)
+                r.update(errors(got, ref, 1e-4, pages))
+                if chunked is not None:
+                    out[name + "_chunked_tc"].update(errors(chunked, ref, 2e-3))
+                del ref, xh, job
+            del x, o, S, got, chunked
         # single-step decode of the other kinds (column decode kernel), B=1024 T=1,
         # random states: each step reads and writes every state once
         for name, maker, (Bc, H, G, dk, dv) in (
@@ -485,26 +777,40 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                 ("deltanet_decode", lambda c: synth.deltanet_inputs(1024, 1, 8, 128, 128, cid=c, device=dev),
                  (1024, 8, 8, 128, 128))):
             x = maker(97)
-            S = torch.empty((Bc, H, dk, dv), device=dev).normal_(generator=torch.Generator(dev).manual_seed(98))
+            S0 = torch.empty((Bc, H, dk, dv), device=dev).normal_(generator=torch.Generator(dev).manual_seed(98))
+            S = S0.clone()
             o = torch.empty((Bc, 1, H, dv), device=dev)
             if name == "deltanet_decode":
-                fn = lambda: sr.sn_recur_delta(ctx.handle, Bc, 1, H, dk, dv, x["scale"], x["q"], x["k"], x["v"],
-                                               x["beta"], S, S, o, s)
-                gbytes = x["beta"].numel() * 4
+                call = lambda Si, So: sr.sn_recur_delta(ctx.handle, Bc, 1, H, dk, dv, x["scale"], x["q"], x["k"],
+                                                        x["v"], x["beta"], Si, So, o, s)
+                gname, kind = "beta", "delta"
             else:
-                fn = lambda: sr.sn_recur_diag(ctx.handle, Bc, 1, H, G, dk, dv, x["decay_kind"], x["scale"], x["q"],
-                                              x["k"], x["v"], x["d"], S, S, o, s)
-                gbytes = x["d"].numel() * 4
+                call = lambda Si, So: sr.sn_recur_diag(ctx.handle, Bc, 1, H, G, dk, dv, x["decay_kind"], x["scale"],
+                                                       x["q"], x["k"], x["v"], x["d"], Si, So, o, s)
+                gname, kind = "d", "diag"
+            gbytes = x[gname].numel() * 4
             nb = 2 * S.numel() * 4 + (x["q"].numel() + x["k"].numel() + x["v"].numel() + o.numel()) * 4 + gbytes
-            ms = time_form(torch, fn, warmup, reps, s)   # in place: the states (>= 268 MB) exceed L2
-            out[name] = {"ms": round(ms, 4), "tok_heads_per_s": round(Bc * H / ms * 1e3, 1),
-                         "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
-                         "bound": "hbm", "workload": f"B={Bc} T=1 H={H} dk={dk} dv={dv}"}
+            ms = time_form(torch, lambda: call(S, S), warmup, reps, s)   # in place: the states (>= 268 MB) exceed L2
+            r = {"ms": round(ms, 4), "tok_heads_per_s": round(Bc * H / ms * 1e3, 1),
+                 "GBps": round(nb / ms / 1e6, 1), "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3),
+                 "bound": "hbm", "workload": f"B={Bc} T=1 H={H} dk={dk} dv={dv}"}
             assert ctx.last_error() == sr.SN_OK
-            del x, S, o
+            if cpu:
+                # one step from the stored initial states (out of place) against the oracle
+                call(S0, S)
+                torch.cuda.synchronize()
+                got = {"o": host(o), "S": host(S)}
+                xh = {"q": host(x["q"]), "k": host(x["k"]), "v": host(x["v"]), "g": host(x[gname]),
+                      "S0": host(S0), "scale": x["scale"], "decay_kind": x.get("decay_kind")}
+                job = matrix_job(kind, xh, Bc, 1, H, dk, dv, nb, G=G)
+                crec, ref = cpu_record(job)
+                r.update(crec)
+                r.update(errors(got, ref, 1e-4))
+                del ref, xh, job, got
+            out[name] = r
+            del x, S, S0, o
         # readout epilogues on the GLA and Mamba-2 output shapes (12 B per element);
         # L2 is flushed before each timed launch (the GLA tensors fit in it)
-        flush = torch.empty(64 << 20, device=dev)          # 256 MB
         gen = torch.Generator(dev).manual_seed(91)
         for name, (Bc, Tc, H, dv) in (("gla_readout_norm_gate", (4, 4096, 4, 128)),
                                       ("mamba2_readout_dskip", (4, 4096, 24, 64))):
@@ -523,8 +829,20 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, warmup=
                 continue
             ms = time_form(torch, fn, warmup, reps, s, flush=flush)
             nb = 12 * o.numel()
-            out[name] = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
-                         "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm", "l2": "flushed"}
+            r = {"ms": round(ms, 4), "GBps": round(nb / ms / 1e6, 1),
+                 "hbm_frac": round(nb / ms / 1e6 / hbm_peak, 3), "bound": "hbm", "l2": "flushed"}
+            if cpu:
+                import oracle
+                torch.cuda.synchronize()
+                oh, zh = host(o), host(z)
+                if name.endswith("norm_gate"):
+                    tasks = [lambda b=b: oracle.readout_norm_gate(oh[b:b + 1], zh[b:b + 1], host(w), eps=1e-6)
+                             for b in range(Bc)]
+                else:
+                    tasks = [lambda b=b: oracle.readout_dskip(oh[b:b + 1], zh[b:b + 1], host(D)) for b in range(Bc)]
+                parts, _ = run_pool(tasks, min(Bc, host_cores()))
+                r.update(errors({"y": host(y)}, {"y": np.concatenate(parts, axis=0)}, 1e-5))
+            out[name] = r
             del o, z, y
         del flush
     return out
@@ -638,14 +956,14 @@ def run_ours(args):
     # in, both forms' s_t and s_final out, every step; wall clock per step
     e2e = None
     if not args.no_e2e:
-        host = {n: torch.empty_like(x[n], device="cpu").pin_memory() for n in ("a", "b", "u", "s0")}
-        for n in host:
-            host[n].copy_(x[n])
+        hbuf = {n: torch.empty_like(x[n], device="cpu").pin_memory() for n in ("a", "b", "u", "s0")}
+        for n in hbuf:
+            hbuf[n].copy_(x[n])
         hout = {f: (torch.empty((B, T, N), pin_memory=True), torch.empty((B, N), pin_memory=True))
                 for f in ("fma", "gated")}
 
         def e2e_step():
-            ctx.scan_host(host["a"], host["b"], host["u"], host["s0"], out=hout, rows_per_chunk=1, nstreams=3)
+            ctx.scan_host(hbuf["a"], hbuf["b"], hbuf["u"], hbuf["s0"], out=hout, rows_per_chunk=1, nstreams=3)
 
         n_e2e = max(3, min(args.steps, 20))
         for _ in range(2):
@@ -668,37 +986,40 @@ def run_ours(args):
                "api": "Context.scan_host (3 streams, one batch row per chunk)",
                "link": link, "link_bound_ms_per_step": round(bound_ms, 3),
                "link_frac": round(bound_ms / e2e_ms, 3)}
-        del host, hout
+        del hbuf, hout
+
+    # CPU baseline: the oracle on this run's own inputs (the full workload,
+    # copied to the host), rank 0 at N=1 only: fp64 and fp32, on every host
+    # core and on one thread.  The fp64 run is also the reference the GPU
+    # outputs are measured against (here and in the forms).
+    cpu = None
+    scan_rec = scan_ref = None
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu
+    if do_cpu:
+        xh = {n: x[n].cpu().numpy() for n in ("a", "b", "u", "s0")}
+        job = scan_job(xh["a"], {"fma": xh["b"], "gated": xh["u"]}, xh["s0"])
+        crec, scan_ref = cpu_record(job, reps_1t=5)
+        got = {"s_fma": host(so_f), "s_final_fma": host(sf_f), "s_gated": host(so_g), "s_final_gated": host(sf_g)}
+        scan_rec = dict(crec)
+        scan_rec.update(errors(got, scan_ref, 1e-5, PAGES_ERR["scan"]))
+        a64 = crec["cpu_fp64_all"]
+        cpu = {"value": a64["GBps"], "unit": "GB/s", "cores": a64["threads"], "kind": "oracle",
+               "sample": f"the full workload B=8 T=8192 N=2048 (this run's inputs), both forms, fp64 oracle, "
+                         f"{len(job.units)} {job.what} on {a64['threads']} threads, {a64['s']:.2f} s",
+               "detail": {"cpu_model": a64["cpu_model"], "logical_cpus": a64["logical_cpus"],
+                          "fp64_all_threads_GBps": a64["GBps"],
+                          "fp64_1_thread_GBps": crec["cpu_fp64_1t"]["GBps"],
+                          "fp32_all_threads_GBps": crec["cpu_fp32_all"]["GBps"],
+                          "fp32_1_thread_GBps": crec["cpu_fp32_1t"]["GBps"],
+                          "sample_1_thread": crec["cpu_fp64_1t"]["sample"]}}
+        del xh, job, got
 
     forms = None
     if not args.no_forms:
-        forms = bench_forms(torch, sr, ctx, dev, stream, fp32_peak, hbm_peak)
-
-    # CPU baseline: the fp64 oracle on this run's own inputs (the full
-    # workload, copied to the host), rank 0 at N=1 only
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        a, b, u, s0 = (x[n].cpu().numpy() for n in ("a", "b", "u", "s0"))
-        threads = min(B, os.cpu_count() or 1)
-        secs = cpu_oracle_scan(a, b, u, s0, threads)
-        cpu = {"value": round(2 * scan_bytes(B, T, N) / secs / GB, 4), "unit": "GB/s", "cores": threads,
-               "kind": "oracle",
-               "sample": f"the full workload B=8 T=8192 N=2048 (this run's inputs), both forms, fp64 oracle, "
-                         f"batch rows on {threads} threads, {secs:.2f} s"}
-        # the same oracle single-threaded (one batch row) and in fp32 (all rows,
-        # and one row), with the host it ran on
-        row = (a[:1], b[:1], u[:1], s0[:1])
-        s1 = cpu_oracle_scan(*row, 1)
-        s32 = cpu_oracle_scan(a, b, u, s0, threads, prec="f32")
-        s321 = cpu_oracle_scan(*row, 1, prec="f32")
-        cpu["detail"] = {
-            "cpu_model": cpu_model(), "logical_cpus": os.cpu_count(),
-            "fp64_all_threads_GBps": cpu["value"],
-            "fp64_1_thread_GBps": round(2 * scan_bytes(1, T, N) / s1 / GB, 4),
-            "fp32_all_threads_GBps": round(2 * scan_bytes(B, T, N) / s32 / GB, 4),
-            "fp32_1_thread_GBps": round(2 * scan_bytes(1, T, N) / s321 / GB, 4),
-            "sample_1_thread": "one batch row (T=8192 N=2048), both forms"}
-        del a, b, u, s0, row
+        forms = bench_forms(torch, sr, ctx, dev, stream, fp32_peak, hbm_peak, cpu=do_cpu, scan_ref=scan_ref)
+        if scan_rec is not None:
+            forms["scan_large"] = scan_rec
+    scan_ref = None
 
     assert ctx.last_error() == sr.SN_OK
     clocks = clk.summary()
