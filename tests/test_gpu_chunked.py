@@ -4,8 +4,9 @@
 Bar: o and the final state within 2e-3 normwise of the fp64 oracle (the
 operands of the tensor-core products are tf32); splits at multiples of the
 128-token chunk are bit-exact within the GPU path (the chunk grid does not
-move); the range limit of the per-key factors and non-positive decays are
-reported as SN_E_RANGE, never as silently wrong numbers.
+move); per-key decays strong enough to leave the single-anchor range are
+evaluated exactly; non-positive decays are reported as SN_E_RANGE, never as
+silently wrong numbers.
 """
 import numpy as np
 import pytest
@@ -161,12 +162,72 @@ def test_full_size_sampled_heads(ctx, name):
         assert _nrel(S[b:b + 1, h:h + 1], rS) <= TOL
 
 
+# ------------------------------------------------------------------ strong per-key decays
+def _strong(x, mode, seed):
+    """Per-key decays whose in-chunk products leave the single-anchor range:
+    d = 2^-4 at every token, GLA decays exp(logsigmoid(N(0,1))) without the
+    /16 (a product of about 2^-74 over half a chunk), or chunks that
+    alternate between the workload's mild decays and 2^-4 (flagged and
+    unflagged chunks in one call)."""
+    d = x["d"]
+    if mode == "pow2":
+        d = torch.full_like(d, 2.0 ** -4)
+    elif mode == "logsigmoid":
+        d = torch.exp(torch.nn.functional.logsigmoid(synth.normal(tuple(d.shape), 9900 + seed)))
+    else:
+        d = d.clone()
+        for n0 in range(CHUNK, d.shape[1], 2 * CHUNK):
+            d[:, n0:n0 + CHUNK] = 2.0 ** -4
+    return dict(x, d=d.contiguous())
+
+
+@pytest.mark.parametrize("mode", ["pow2", "logsigmoid", "mixed"])
+@pytest.mark.parametrize("dv", [128, 64])
+@pytest.mark.parametrize("T", [128, 300, 640])
+def test_strong_per_key_decays_within_tolerance(ctx, mode, dv, T):
+    """Chunks beyond the single-anchor range are evaluated step by step from
+    their start state: within the chunked form's tolerance of the fp64
+    oracle, with a start state, and no error recorded."""
+    B, H = 2, 3
+    x = _strong(make("gla", B, T, H, dv, seed=T % 5), mode, T)
+    S0 = synth.normal((B, H, 128, dv), 9950 + T) * 0.5
+    o, S = run_chunked(ctx, x, S0)
+    ro, rS = ref(x, S0)
+    assert _nrel(o, ro) <= TOL
+    assert _nrel(S, rS) <= TOL
+
+
+@pytest.mark.parametrize("mode", ["pow2", "mixed"])
+def test_strong_gated_per_key_decays(ctx, mode):
+    B, T, H, dv = 2, 300, 2, 128
+    x = synth.gated_memory_inputs(B, T, H, 128, dv, per_key=True, cid=360)
+    x = _strong(x, mode, 7)
+    o, S = run_chunked(ctx, x)
+    ro, rS = ref(x)
+    assert _nrel(o, ro) <= TOL and _nrel(S, rS) <= TOL
+
+
+def test_strong_decays_split_at_chunk_multiple_bit_exact(ctx):
+    """The flagged chunks' step-by-step outputs depend only on the chunk's
+    start state and its tokens, so splits at chunk multiples stay bit-exact."""
+    B, T, H, dv = 1, 512, 2, 64
+    x = _strong(make("gla", B, T, H, dv, seed=3), "mixed", 11)
+    o, S = run_chunked(ctx, x)
+    cut = 2 * CHUNK
+    x1 = {k: (v[:, :cut].contiguous() if torch.is_tensor(v) and v.dim() == 4 else v) for k, v in x.items()}
+    x2 = {k: (v[:, cut:].contiguous() if torch.is_tensor(v) and v.dim() == 4 else v) for k, v in x.items()}
+    o1, S1 = run_chunked(ctx, x1)
+    o2, S2 = run_chunked(ctx, x2, torch.from_numpy(S1))
+    assert np.array_equal(np.concatenate([o1, o2], axis=1), o) and np.array_equal(S2, S)
+
+
 # ------------------------------------------------------------------ errors
-def test_per_key_range_limit_is_reported(ctx, sr):
+def test_non_positive_decay_is_reported(ctx, sr):
     B, T, H, dv = 1, 128, 1, 64
     x = make("gla", B, T, H, dv, seed=0)
-    x = dict(x, d=torch.full_like(x["d"], 2.0 ** -4))      # 2^-252 between token 0 and the anchor
-    run_chunked(ctx, x)
+    d = x["d"].clone()
+    d[0, 5, 0, 17] = 0.0
+    run_chunked(ctx, dict(x, d=d))
     assert ctx.last_error() == sr.SN_E_RANGE
     assert ctx.last_error() == sr.SN_OK                    # read once, cleared
 
