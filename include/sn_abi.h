@@ -100,7 +100,7 @@ typedef int32_t sn_status;
 
 /* Context options (sn_ctx_set_option / sn_ctx_get_option). */
 #define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back,
-                                      3 chunked reduce-then-scan */
+                                      3 chunked reduce-then-scan, 4 chunked fused (forward scans) */
 #define SN_OPT_WAIT_LIMIT_US    2  /* bound on any device-side wait, microseconds (default 1e6) */
 #define SN_OPT_DEBUG_POISON     3  /* 1: look-back waits for a flag no chunk publishes (tests the bound) */
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
@@ -116,6 +116,8 @@ typedef int32_t sn_status;
 #define SN_SCAN_KERNEL_SEQUENTIAL 1
 #define SN_SCAN_KERNEL_LOOKBACK   2
 #define SN_SCAN_KERNEL_REDUCE_SCAN 3   /* the look-back kernel's results in three flag-free passes */
+#define SN_SCAN_KERNEL_FUSED       4   /* the same results in one launch: aggregates, per-column carry
+                                          chains and outputs at once (forward scans, T >= 1024) */
 
 /* Operation ids for sn_workspace_bytes(). */
 #define SN_OP_SCAN_FMA   1
@@ -191,9 +193,10 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value);
  * same bits as the single-precision definition at every t, so splitting a
  * sequence into segments and carrying s_final -> s0 reproduces the full run
  * bit for bit ([P1] §4).  For few channels and long T the call chunks T
- * instead: the reduce-then-scan path (chosen automatically there) or the
- * decoupled look-back kernel (SN_OPT_SCAN_KERNEL); the two give the same bits,
- * are deterministic and are bit-exact under splits at multiples of
+ * instead: the fused path (chosen automatically there when the workspace
+ * covers it, else reduce-then-scan), or the reduce-then-scan path or the
+ * decoupled look-back kernel (SN_OPT_SCAN_KERNEL); all three give the same
+ * bits, are deterministic and are bit-exact under splits at multiples of
  * SN_OPT_LOOKBACK_CHUNK.  Calls may be captured in a CUDA graph and replayed:
  * the look-back kernel keeps its launch epoch in device memory, so every
  * replay tags its chunk flags afresh.
@@ -316,11 +319,14 @@ sn_status sn_recur_rwkv7(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
  * Requirements: dk == 128, dv in {64, 128} (else SN_E_UNSUPPORTED); 16-byte aligned pointers; a
  * context workspace of at least sn_recur_chunked_workspace_bytes() bytes
  * (else SN_E_NOMEM), which the call overwrites (a later look-back scan on the
- * same context clears its flag area again).  Decays must be positive; with
- * per-key decays the product of the decays between any token of a chunk and
- * the chunk's token 63 must lie in [2^-60, 2^60] -- a chunk outside that
- * range records SN_E_RANGE in the context's status block (outputs are then
- * unspecified; use sn_recur_diag). */
+ * same context clears its flag area again).  Decays must be positive: a
+ * decay <= 0 (or NaN) records SN_E_RANGE in the context's status block
+ * (outputs are then unspecified; use sn_recur_diag).  Per-key decays enter
+ * the products through factors anchored at the chunk's token 63; a chunk in
+ * which the decay product between some token and the anchor leaves
+ * [2^-60, 2^60] has its outputs evaluated step by step in fp32 from the
+ * chunk's start state instead (exact per step; slower than the tensor-core
+ * products, so strong decays cost time, not accuracy). */
 sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int32_t G,
                                 int32_t dk, int32_t dv, int32_t decay_kind, float scale,
                                 const float* q, const float* k, const float* v,
@@ -328,8 +334,8 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
                                 float* o, void* stream);
 
 /* Workspace bytes sn_recur_diag_chunked needs: B * H * ceil(T / 128) chunk
- * states of dk x dv floats plus one decay vector of dk floats per chunk
- * (each part rounded up to 256 bytes); -1 on invalid arguments. */
+ * states of dk x dv floats, two vectors of dk floats per chunk and one int32
+ * per chunk (each part rounded up to 256 bytes); -1 on invalid arguments. */
 int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* Chunked tensor-core form of sn_recur_delta: the same delta rule and readout

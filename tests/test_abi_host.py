@@ -145,6 +145,15 @@ def test_workspace_bytes(abi):
     assert abi.sn_recur_delta_chunked_workspace_bytes(big, big, 1, 128, 128) == -1
 
 
+def test_chunked_workspace_bytes(abi):
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, T, H, dv in ((4, 4096, 4, 128), (1, 300, 3, 64), (2, 1, 1, 128)):
+        nc = (T + 127) // 128
+        # chunk states, the chunk decays and anchor factors, and one flag per chunk
+        want = r256(B * H * nc * 128 * dv * 4) + 2 * r256(B * H * nc * 128 * 4) + r256(B * H * nc * 4)
+        assert abi.sn_recur_chunked_workspace_bytes(B, T, H, 128, dv) == want
+
+
 def test_noalloc_rejects_oversized_problems_before_any_device_work(abi):
     """Dimensions whose element count overflows int64 are an argument error,
     found before the device is touched (the pointers are never read)."""
