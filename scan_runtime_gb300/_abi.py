@@ -29,6 +29,7 @@ SN_OPT_SCAN_KERNEL, SN_OPT_WAIT_LIMIT_US, SN_OPT_DEBUG_POISON, SN_OPT_LOOKBACK_C
 SN_OPT_RECUR_TILE = 6
 SN_OPT_DELTA_SEGMENTS = 7
 SN_SCAN_KERNEL_AUTO, SN_SCAN_KERNEL_SEQUENTIAL, SN_SCAN_KERNEL_LOOKBACK, SN_SCAN_KERNEL_REDUCE_SCAN = 0, 1, 2, 3
+SN_SCAN_KERNEL_FUSED = 4
 SN_OP_SCAN_FMA, SN_OP_SCAN_GATED = 1, 2
 
 # every symbol the header declares

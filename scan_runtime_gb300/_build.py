@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsn.so")
-SOURCES = ["abi.cu", "scan.cu", "scan_lookback.cu", "scan_bwd.cu", "scan_bwd_chunked.cu", "recur.cu", "recur_diag.cu", "recur_diag_gated.cu", "recur_delta.cu",
+SOURCES = ["abi.cu", "scan.cu", "scan_lookback.cu", "scan_fused.cu", "scan_bwd.cu", "scan_bwd_chunked.cu", "recur.cu", "recur_diag.cu", "recur_diag_gated.cu", "recur_delta.cu",
            "recur_rwkv7.cu", "recur_decode.cu", "recur_chunked.cu", "recur_delta_chunked.cu", "readout.cu"]
 HEADERS = ["sn_internal.h", "ptx.cuh", "scan_common.cuh", "scan_tile.cuh", "recur_seq.cuh", "tc.cuh", "chunk_common.cuh"]
 

@@ -7,6 +7,7 @@
 // bits, int32 status codes and dimensions).
 #include <cstdint>
 #include <cmath>
+#include <algorithm>
 #include <cstring>
 #include <initializer_list>
 #include <map>
@@ -283,7 +284,7 @@ sn_status sn_ctx_set_option(SnCtx* ctx, int32_t key, int32_t value) {
     if (ctx == nullptr) return SN_E_INVAL;
     switch (key) {
         case SN_OPT_SCAN_KERNEL:
-            if (value < SN_SCAN_KERNEL_AUTO || value > SN_SCAN_KERNEL_REDUCE_SCAN) return SN_E_INVAL;
+            if (value < SN_SCAN_KERNEL_AUTO || value > SN_SCAN_KERNEL_FUSED) return SN_E_INVAL;
             ctx->scan_kernel = value;
             return SN_OK;
         case SN_OPT_WAIT_LIMIT_US:
@@ -343,9 +344,13 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     ScanArgs x{B, T, N, a, b, s0, s_final, s_out};
     int kernel = ctx->scan_kernel;
     const int64_t need = lookback_ws_bytes(B, T, N);
+    const int64_t need_fused = scan_fused_ws_bytes(B, T, N);
     if (kernel == SN_SCAN_KERNEL_LOOKBACK || kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
         if (!lookback_supported(x)) return SN_E_UNSUPPORTED;
         if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
+    } else if (kernel == SN_SCAN_KERNEL_FUSED) {
+        if (!lookback_supported(x)) return SN_E_UNSUPPORTED;
+        if (ctx->ws == nullptr || ctx->ws_bytes < std::max(need, need_fused)) return SN_E_NOMEM;
     } else if (kernel == SN_SCAN_KERNEL_AUTO) {
         // The sequential kernel keeps the exact per-step bits and is HBM-bound
         // once there are enough channels; chunking along T pays only when the
@@ -360,6 +365,8 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         kernel = (few && T >= 8 * LB_TC && lookback_supported(x) && ctx->ws != nullptr && ctx->ws_bytes >= need)
                      ? SN_SCAN_KERNEL_REDUCE_SCAN
                      : SN_SCAN_KERNEL_SEQUENTIAL;
+        // the same results in one launch where the workspace also covers its block flags
+        if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN && ctx->ws_bytes >= need_fused) kernel = SN_SCAN_KERNEL_FUSED;
     }
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
@@ -381,6 +388,22 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         }
         return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->debug_poison, ctx->dstatus, wait_ns(ctx),
                                               ctx->sm_count, s));
+    }
+    if (kernel == SN_SCAN_KERNEL_FUSED) {
+        // tagged flags as the look-back kernel's (same launch epoch), in other
+        // places: cleared when the workspace, the geometry or the user changes
+        const int64_t sig = -lookback_flag_count(B, T, N);
+        if (ctx->ws_dirty || ctx->lb_last_flags != sig) {
+            int64_t fa, fb, fc;
+            scan_fused_flag_areas(B, T, N, &fa, &fb, &fc);
+            if (cudaMemsetAsync(ctx->ws, 0, (size_t)fa, s) != cudaSuccess ||
+                cudaMemsetAsync(static_cast<char*>(ctx->ws) + fb, 0, (size_t)fc, s) != cudaSuccess ||
+                cudaMemsetAsync(&ctx->dstatus->abort_tag, 0, sizeof(unsigned int), s) != cudaSuccess)
+                return SN_E_DEVICE;
+            ctx->ws_dirty = false;
+            ctx->lb_last_flags = sig;
+        }
+        return from_cuda(launch_scan_fused(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
     }
     if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
         ctx->ws_dirty = true;   // its carries overwrite the look-back's carry words

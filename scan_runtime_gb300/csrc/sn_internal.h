@@ -36,7 +36,8 @@ struct SnCtx {
     void* ws;
     int64_t ws_bytes;
     bool ws_dirty;              // flag area must be cleared before next use
-    int64_t lb_last_flags;      // flag count of the last look-back launch
+    int64_t lb_last_flags;      // layout of the tagged flags last cleared: the look-back kernel's flag
+                                // count, or minus the fused path's tile count
     // options
     int scan_kernel;
     int wait_limit_us;
@@ -116,6 +117,15 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int po
 // launches without flags, for few channel tiles and long T; same workspace.
 cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
                                     int sm_count, cudaStream_t stream);
+// The same results in one cooperative launch (scan_fused.cu): tile aggregates,
+// one chain CTA per column of tiles folding its carries, and the outputs run
+// at once.  Workspace bytes it needs,
+// and the two tagged flag areas a change of geometry must clear ([0, a) and
+// [b, b + c)).
+int64_t scan_fused_ws_bytes(int B, int T, int N);
+void scan_fused_flag_areas(int B, int T, int N, int64_t* a, int64_t* b, int64_t* c);
+cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
+                              int sm_count, cudaStream_t stream);
 
 enum RecurKind : int {
     RK_DIAG_KEY = 0,

@@ -257,10 +257,10 @@ def test_lookback_bounded_wait_reports_timeout(sr, lbctx):
 @pytest.mark.parametrize("shape", [(1, 4096, 32), (2, 1000, 64), (3, 257, 96), (2, 5, 8), (1, 70000, 64),
                                    (1, 40000, 36)])
 def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
-    """The reduce-then-scan path runs the look-back kernel's local scans,
-    aggregates and carry chain in the same order, so its results equal the
-    look-back's bit for bit; T = 70000 and 40000 span several blocks of the
-    carry chain, N = 36 a ragged channel tile."""
+    """The reduce-then-scan path and the fused path run the look-back kernel's
+    local scans, aggregates and carry chain in the same order, so their
+    results equal the look-back's bit for bit; T = 70000 and 40000 span
+    several blocks of the carry chains, N = 36 a ragged channel tile."""
     B, T, N = shape
     ctx.ensure_workspace(B, T, N)
     a, b, u, s0 = _inputs(B, T, N, 40 + T % 11)
@@ -270,8 +270,12 @@ def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
     ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
     ro, rf = _run(ctx, form, a, rhs, s0)
     ro0, rf0 = _run(ctx, form, a, rhs, None)
+    ctx.ensure_workspace_bytes(sr.sn_workspace_bytes(sr.SN_OP_SCAN_FMA, B, T, N) + 4096)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_FUSED)
+    fo, ff = _run(ctx, form, a, rhs, s0)
     ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
     assert np.array_equal(ro, lo) and np.array_equal(rf, lf)
+    assert np.array_equal(fo, lo) and np.array_equal(ff, lf)
     r64, f64 = _ref(form, a, rhs, s0, "f64")
     assert _nrel(ro, r64) <= TOL and _nrel(rf, f64) <= TOL
     z64, zf64 = _ref(form, a, rhs, None, "f64")
@@ -304,16 +308,17 @@ def test_lookback_forced_without_workspace_is_nomem(sr, ctx):
     assert bool((out == 7.0).all())                     # untouched
 
 
-@pytest.mark.parametrize("kernel", ["lookback", "reduce_scan"])
+@pytest.mark.parametrize("kernel", ["lookback", "reduce_scan", "fused"])
 @pytest.mark.parametrize("shape", [(1, 70000, 64), (2, 1000, 64), (1, 256, 32)])
 def test_chunked_in_place_continuation(sr, ctx, kernel, shape):
     """s_final may be s0's buffer.  The chunked kernels read s0 before any tile
     writes a final state (the first chunk only; the output pass reads the
     chain's copy), so in place gives the out-of-place bits."""
     B, T, N = shape
-    ctx.ensure_workspace(B, T, N)
-    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK if kernel == "lookback"
-                   else sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    ctx.ensure_workspace_bytes(sr.sn_workspace_bytes(sr.SN_OP_SCAN_FMA, B, T, N) + 4096)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, {"lookback": sr.SN_SCAN_KERNEL_LOOKBACK,
+                                           "reduce_scan": sr.SN_SCAN_KERNEL_REDUCE_SCAN,
+                                           "fused": sr.SN_SCAN_KERNEL_FUSED}[kernel])
     a, b, _, s0 = _inputs(B, T, N, 71 + T % 7)
     a, b, s0 = a.cuda(), b.cuda(), s0.cuda()
     so1, sf1 = torch.empty_like(a), torch.empty_like(s0)
@@ -324,6 +329,54 @@ def test_chunked_in_place_continuation(sr, ctx, kernel, shape):
     torch.cuda.synchronize()
     ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
     assert torch.equal(so1, so2) and torch.equal(sf1, st)
+
+
+def test_fused_interleaved_with_other_chunked_calls_and_shapes(sr, ctx):
+    """The fused path keeps tagged flags where the look-back kernel keeps its
+    own: calls of both kernels, reduce-then-scan calls and changes of shape
+    on one context all give the look-back's bits."""
+    shapes = ((1, 20000, 64), (2, 3000, 32), (1, 20000, 64))
+    ins = [_inputs(*sh, 60 + i) for i, sh in enumerate(shapes)]
+    ctx.ensure_workspace_bytes(max(sr.sn_workspace_bytes(sr.SN_OP_SCAN_FMA, *sh) for sh in shapes) + 4096)
+    ref = []
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_LOOKBACK)
+    for (a, b, _, s0) in ins:
+        ref.append(_run(ctx, "fma", a, b, s0))
+    order = [(0, sr.SN_SCAN_KERNEL_FUSED), (1, sr.SN_SCAN_KERNEL_FUSED), (1, sr.SN_SCAN_KERNEL_LOOKBACK),
+             (1, sr.SN_SCAN_KERNEL_FUSED), (2, sr.SN_SCAN_KERNEL_REDUCE_SCAN), (2, sr.SN_SCAN_KERNEL_FUSED),
+             (0, sr.SN_SCAN_KERNEL_FUSED), (0, sr.SN_SCAN_KERNEL_FUSED)]
+    for i, kern in order:
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, kern)
+        a, b, _, s0 = ins[i]
+        so, sf = _run(ctx, "fma", a, b, s0)
+        assert np.array_equal(so, ref[i][0]) and np.array_equal(sf, ref[i][1]), (i, kern)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+
+
+def test_fused_replayed_from_a_cuda_graph(sr, ctx):
+    """A fused call captured in a CUDA graph and replayed on new inputs: the
+    launch epoch advances on the device, so each replay equals an uncaptured
+    call bit for bit."""
+    B, T, N = 1, 16384, 64
+    ctx.ensure_workspace_bytes(sr.sn_workspace_bytes(sr.SN_OP_SCAN_FMA, B, T, N) + 4096)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_FUSED)
+    ins = [tuple(t.cuda() for t in _inputs(B, T, N, 80 + i)) for i in range(3)]
+    expect = [_run(ctx, "fma", a.cpu(), b.cpu(), s0.cpu()) for a, b, _, s0 in ins]
+    a_d, b_d = torch.empty((B, T, N), device="cuda"), torch.empty((B, T, N), device="cuda")
+    s0_d, so, sf = torch.empty((B, N), device="cuda"), torch.empty((B, T, N), device="cuda"), torch.empty((B, N), device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert sr.sn_scan_fma(ctx.handle, B, T, N, a_d, b_d, s0_d, sf, so) == sr.SN_OK
+    for _ in range(2):
+        for (a, b, _, s0), (eo, ef) in zip(ins, expect):
+            a_d.copy_(a)
+            b_d.copy_(b)
+            s0_d.copy_(s0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(so.cpu().numpy(), eo) and np.array_equal(sf.cpu().numpy(), ef)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
 
 
 def test_auto_choice_by_channel_count(sr, ctx):
