@@ -33,8 +33,8 @@ struct ChunkArgs {
     float* o;
     float* W;       // per (b, h, chunk) a dv x dk tile in operand layout: dS^T, then S'^T
     float* gam;     // (B, H, NC, dk): chunk decay gamma_n per key
-    float* anc;     // (B, H, NC, dk): anchor factor 2^{lam_m} (1 for per-head decays and flagged chunks)
-    int* bad;       // (B, H, NC): per-key decays whose anchor factors leave 2^{+-RANGE_LOG2} (chunk_fix)
+    float* anc;     // (B, H, NC, dk): anchor factor 2^{lam_m} (1 for per-head decays, -1 for flagged chunks)
+    int* bad;       // (B, H, NC): per-key decays whose anchor factors leave 2^{+-RANGE_LOG2}
     const float* vt;   // optional: per chunk a v^T operand tile (rows value, K = token, tf32)
                        // that replaces v in the output stage (bulk-loaded)
     SnDevStatus* st;

@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
         }
         gam = ex2(m);                       // half 0: the whole chunk's log2 decay
         // A key whose factors would leave 2^{+-RANGE_LOG2} flags the chunk: its
-        // outputs are then evaluated step by step (chunk_fix), and its state
-        // operand is kept unscaled and unrounded (anchor 1).  A non-finite sum
+        // outputs are then evaluated step by step (fix_unit), and its state
+        // operand is kept unscaled and unrounded (anchor -1 marks it).  A non-finite sum
         // means a decay <= 0, which no evaluation here supports.
         const float mm = tot[DKC + i];
         float* ext = Ds;                    // the decays are consumed: [2][2][DKC] extremes
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
         }
         const bool flagged = __syncthreads_or(wide);
         if (tid == 0) a.bad[c.bh * a.NC + c.n] = flagged ? 1 : 0;
-        anc = flagged ? 1.f : ex2(tot[i]);  // 2^{lam at the anchor token C/2 - 1}
+        anc = flagged ? -1.f : ex2(tot[i]); // 2^{lam at the anchor token C/2 - 1}; -1 marks the flag
     } else {
         const float total = total_s[0];
 #pragma unroll 4
@@ -410,11 +410,9 @@ __global__ void __launch_bounds__(256) chunk_carry(const ChunkArgs a, int dv) {
     float* w = a.W + bh * a.NC * per_head + f;
     const float* gm = a.gam + bh * a.NC * DKC + i;
     const float* an = a.anc + bh * a.NC * DKC + i;
-    const int* bd = a.bad != nullptr ? a.bad + bh * a.NC : nullptr;
-    // a flagged chunk (chunk_state) keeps its start state in fp32 for chunk_fix
-    auto operand = [&](float anchor, float st, int n) {
-        return (bd != nullptr && __ldg(bd + n) != 0) ? st : tc::to_tf32(anchor * st);
-    };
+    // a flagged chunk (chunk_state marks it with anchor -1) keeps its start
+    // state in fp32 for the step-by-step evaluation
+    auto operand = [&](float anchor, float st, int) { return anchor < 0.f ? st : tc::to_tf32(anchor * st); };
     constexpr int U = 8;
     int n = 0;
     for (; n + U <= a.NC; n += U) {
@@ -437,6 +435,131 @@ __global__ void __launch_bounds__(256) chunk_carry(const ChunkArgs a, int dv) {
         s = fmaf(__ldg(gm + (size_t)n * DKC), s, ds);
     }
     if (a.S_out != nullptr) a.S_out[nat] = s;
+}
+
+// ------------------------------------------------------------------ flagged chunks
+// Per-key decays strong enough that a chunk's anchor factors would leave
+// 2^{+-RANGE_LOG2} (chunk_state flags the chunk): the chunk's outputs are
+// evaluated step by step from its start state, which chunk_carry kept in fp32.
+// Each step is the sequence kernel's single-precision update
+// S_ij = fma(d_i, S_ij, k_i v_j) (k_i weighted by 1 - d_i when gated) and the
+// readout o_tj = scale sum_i S_ij q_i, so no factor other than the decays
+// themselves appears and any positive decay is exact.  The CTA of chunk_output
+// that owns the unit runs this after its tensor-core units (it skipped the
+// unit's stores there), in the same shared memory; a thread owns four value
+// columns over 16 key rows, the eight threads of a column quad sum the
+// readout by xor shuffles.  The tokens stream through shared memory FB at a
+// time, double-buffered.
+constexpr int FB = 32;               // tokens per staged batch
+
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+template <int DV>
+struct FixSmem {
+    static constexpr int per_batch = FB * (3 * DKC + DV);   // q, k, d rows, then v rows
+    static constexpr size_t bytes = (size_t)2 * per_batch * 4 + 128;
+};
+
+// Evaluate the flagged unit of chunk c (whole CTA; `base` holds FixSmem bytes).
+template <int DV>
+__device__ __forceinline__ void fix_unit(const ChunkArgs& a, const ChunkIdx& c, float* base) {
+    constexpr int QUADS = DV / 4, TPG = DKC / 16;
+    const int tid = threadIdx.x;
+    const int tau = tid % TPG, qd = tid / TPG;              // quad qd < QUADS holds columns 4 qd .. 4 qd + 3
+    const bool owner = qd < QUADS;
+    const int r0 = 16 * tau, j0 = 4 * qd;
+    {
+        const size_t u = c.bh * a.NC + c.n;
+        const int b = c.b, h = c.h, g = c.g;
+        const int t0 = c.t0, nval = c.nval;
+        // start state: column c's rows r0 .. r0 + 15 are four 16-byte runs of the operand tile
+        float2 S[16][2];
+        const float* w = a.W + (size_t)u * DV * DKC;
+        if (owner) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) {
+                    const float4 x = ld4(w + off128(j0 + c, r0 + 4 * r4));
+                    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (c & 1) S[4 * r4 + e][c >> 1].y = xs[e];
+                        else S[4 * r4 + e][c >> 1].x = xs[e];
+                    }
+                }
+        }
+        const size_t krs = (size_t)a.G * DKC, drs = (size_t)a.H * DKC, vrs = (size_t)a.H * DV;
+        auto stage = [&](int bt, float* buf) {               // tokens [bt, bt + FB) of the chunk
+            for (int f = tid; f < FB * (3 * DKC + DV) / 4; f += NT) {
+                const int e4 = 4 * f;
+                const int tt = e4 / (3 * DKC + DV), col = e4 % (3 * DKC + DV);
+                const size_t row = (size_t)b * a.T + t0 + bt + tt;
+                const bool ok = bt + tt < nval;
+                const float* src;
+                if (col < DKC) src = a.q + row * krs + (size_t)g * DKC + col;
+                else if (col < 2 * DKC) src = a.k + row * krs + (size_t)g * DKC + (col - DKC);
+                else if (col < 3 * DKC) src = a.d + row * drs + (size_t)h * DKC + (col - 2 * DKC);
+                else src = a.v + row * vrs + (size_t)h * DV + (col - 3 * DKC);
+                cp_async16(buf + e4, ok ? src : a.q, ok);
+            }
+            cp_async_commit();
+        };
+        const int nb = (nval + FB - 1) / FB;
+        __syncthreads();                                     // the shared memory is free
+        stage(0, base);
+        for (int bi = 0; bi < nb; ++bi) {
+            float* cur = base + (bi & 1) * FixSmem<DV>::per_batch;
+            if (bi + 1 < nb) {
+                stage((bi + 1) * FB, base + ((bi + 1) & 1) * FixSmem<DV>::per_batch);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                cp_async_wait_all();
+            }
+            __syncthreads();
+            const int tn = min(FB, nval - bi * FB);
+            for (int tt = 0; tt < tn; ++tt) {
+                const float* row = cur + tt * (3 * DKC + DV);
+                float qv[16], kv[16], dv[16];
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) {
+                    const float4 q4 = ld4(row + r0 + 4 * r4), k4 = ld4(row + DKC + r0 + 4 * r4),
+                                 d4 = ld4(row + 2 * DKC + r0 + 4 * r4);
+                    qv[4 * r4] = q4.x; qv[4 * r4 + 1] = q4.y; qv[4 * r4 + 2] = q4.z; qv[4 * r4 + 3] = q4.w;
+                    kv[4 * r4] = k4.x; kv[4 * r4 + 1] = k4.y; kv[4 * r4 + 2] = k4.z; kv[4 * r4 + 3] = k4.w;
+                    dv[4 * r4] = d4.x; dv[4 * r4 + 1] = d4.y; dv[4 * r4 + 2] = d4.z; dv[4 * r4 + 3] = d4.w;
+                }
+                const float4 v4 = owner ? ld4(row + 3 * DKC + j0) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float2 vlo = make_float2(v4.x, v4.y), vhi = make_float2(v4.z, v4.w);
+                float2 alo[4], ahi[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) alo[e] = ahi[e] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float ki = a.gated ? __fmul_rn(__fsub_rn(1.0f, dv[r]), kv[r]) : kv[r];
+                    S[r][0] = __ffma2_rn(f2(dv[r]), S[r][0], __fmul2_rn(f2(ki), vlo));
+                    S[r][1] = __ffma2_rn(f2(dv[r]), S[r][1], __fmul2_rn(f2(ki), vhi));
+                    alo[r & 3] = __ffma2_rn(S[r][0], f2(qv[r]), alo[r & 3]);
+                    ahi[r & 3] = __ffma2_rn(S[r][1], f2(qv[r]), ahi[r & 3]);
+                }
+                float2 slo = __fadd2_rn(__fadd2_rn(alo[0], alo[1]), __fadd2_rn(alo[2], alo[3]));
+                float2 shi = __fadd2_rn(__fadd2_rn(ahi[0], ahi[1]), __fadd2_rn(ahi[2], ahi[3]));
+#pragma unroll
+                for (int o = TPG / 2; o > 0; o >>= 1) {
+                    slo.x = __fadd_rn(slo.x, __shfl_xor_sync(FULL, slo.x, o));
+                    slo.y = __fadd_rn(slo.y, __shfl_xor_sync(FULL, slo.y, o));
+                    shi.x = __fadd_rn(shi.x, __shfl_xor_sync(FULL, shi.x, o));
+                    shi.y = __fadd_rn(shi.y, __shfl_xor_sync(FULL, shi.y, o));
+                }
+                if (owner && tau == 0 && a.o != nullptr) {
+                    float* orow = a.o + (((size_t)b * a.T + t0 + bi * FB + tt) * a.H + h) * DV + j0;
+                    st_cs(reinterpret_cast<float4*>(orow), make_float4(a.scale * slo.x, a.scale * slo.y,
+                                                                        a.scale * shi.x, a.scale * shi.y));
+                }
+            }
+            __syncthreads();                                 // batch `bi` is read: its buffer can refill
+        }
+    }
 }
 
 // ------------------------------------------------------------------ chunk_output
@@ -595,7 +718,7 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                 lam[tb] = x;
             }
             // a chunk chunk_state flagged (factors beyond 2^{+-RANGE_LOG2}) runs
-            // through here on anchor 1; its outputs are replaced by chunk_fix
+            // through here too; its stores are skipped and fix_unit writes them
         } else if (warp == 0) {
             // inclusive prefix sums of log2 d (per head) into lam_s
             float lg[4], sm = 0.f;
@@ -726,7 +849,7 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         if (has_next && tid == 0) issue_qk(cn);
         {
             const float fp = PER_KEY ? 1.f : ex2(lam_s[t]);
-            const bool store = t < c.nval && a.o != nullptr;
+            const bool store = t < c.nval && a.o != nullptr && !(PER_KEY && __ldg(a.bad + c.bh * a.NC + c.n) != 0);
             float* orow = a.o + (row0 + t) * a.H * DV + (size_t)c.h * DV;
 #pragma unroll
             for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
@@ -748,6 +871,17 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
+    }
+    if constexpr (PER_KEY) {
+        // this CTA's flagged units, step by step (their stores were skipped above)
+        if (ok) {
+            static_assert(FixSmem<DV>::bytes <= (size_t)L::misc_off * 4,
+                          "the fix reuses the operand buffers, not the barriers");
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                const ChunkIdx c = chunk_index(a, u);
+                if (__ldg(a.bad + c.bh * a.NC + c.n) != 0) fix_unit<DV>(a, c, base);
+            }
+        }
     }
     if (!ok && tid == 0) {
         record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
@@ -1012,134 +1146,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-// ------------------------------------------------------------------ chunk_fix
-// Per-key decays strong enough that a chunk's anchor factors would leave
-// 2^{+-RANGE_LOG2} (chunk_state flags the chunk): the chunk's outputs are
-// evaluated step by step from its start state, which chunk_carry kept in fp32.
-// Each step is the sequence kernel's single-precision update
-// S_ij = fma(d_i, S_ij, k_i v_j) (k_i weighted by 1 - d_i when gated) and the
-// readout o_tj = scale sum_i S_ij q_i, so no factor other than the decays
-// themselves appears and any positive decay is exact.  A CTA takes flagged
-// chunks in turn (persistent); a thread owns four value columns over 16 key
-// rows, the eight threads of a column quad sum the readout by xor shuffles.
-// The tokens stream through shared memory FB at a time, double-buffered.
-constexpr int FB = 32;               // tokens per staged batch
-
-__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
-
-template <int DV>
-struct FixSmem {
-    static constexpr int per_batch = FB * (3 * DKC + DV);   // q, k, d rows, then v rows
-    static constexpr size_t bytes = (size_t)2 * per_batch * 4 + 128;
-};
-
-template <int DV>
-__global__ void __launch_bounds__(NT, 1) chunk_fix(const ChunkArgs a) {
-    extern __shared__ unsigned char smem_raw[];
-    float* base = align128(smem_raw);
-    constexpr int QUADS = DV / 4, TPG = DKC / 16;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int tau = tid % TPG, qd = tid / TPG;              // quad qd < QUADS holds columns 4 qd .. 4 qd + 3
-    const bool owner = qd < QUADS;
-    const int r0 = 16 * tau, j0 = 4 * qd;
-    const int units = a.B * a.H * a.NC;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        if (__ldg(a.bad + u) == 0) continue;                 // uniform over the CTA
-        const int n = u % a.NC;
-        const size_t bh = (size_t)(u / a.NC);
-        const int b = (int)(bh / a.H), h = (int)(bh % a.H), g = h / (a.H / a.G);
-        const int t0 = n * CH, nval = min(CH, a.T - t0);
-        // start state: column c's rows r0 .. r0 + 15 are four 16-byte runs of the operand tile
-        float2 S[16][2];
-        const float* w = a.W + (size_t)u * DV * DKC;
-        if (owner) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int r4 = 0; r4 < 4; ++r4) {
-                    const float4 x = ld4(w + off128(j0 + c, r0 + 4 * r4));
-                    const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (c & 1) S[4 * r4 + e][c >> 1].y = xs[e];
-                        else S[4 * r4 + e][c >> 1].x = xs[e];
-                    }
-                }
-        }
-        const size_t krs = (size_t)a.G * DKC, drs = (size_t)a.H * DKC, vrs = (size_t)a.H * DV;
-        auto stage = [&](int bt, float* buf) {               // tokens [bt, bt + FB) of the chunk
-            for (int f = tid; f < FB * (3 * DKC + DV) / 4; f += NT) {
-                const int e4 = 4 * f;
-                const int tt = e4 / (3 * DKC + DV), col = e4 % (3 * DKC + DV);
-                const size_t row = (size_t)b * a.T + t0 + bt + tt;
-                const bool ok = bt + tt < nval;
-                const float* src;
-                if (col < DKC) src = a.q + row * krs + (size_t)g * DKC + col;
-                else if (col < 2 * DKC) src = a.k + row * krs + (size_t)g * DKC + (col - DKC);
-                else if (col < 3 * DKC) src = a.d + row * drs + (size_t)h * DKC + (col - 2 * DKC);
-                else src = a.v + row * vrs + (size_t)h * DV + (col - 3 * DKC);
-                cp_async16(buf + e4, ok ? src : a.q, ok);
-            }
-            cp_async_commit();
-        };
-        const int nb = (nval + FB - 1) / FB;
-        __syncthreads();                                     // the previous unit's readers are done
-        stage(0, base);
-        for (int bi = 0; bi < nb; ++bi) {
-            float* cur = base + (bi & 1) * FixSmem<DV>::per_batch;
-            if (bi + 1 < nb) {
-                stage((bi + 1) * FB, base + ((bi + 1) & 1) * FixSmem<DV>::per_batch);
-                asm volatile("cp.async.wait_group 1;" ::: "memory");
-            } else {
-                cp_async_wait_all();
-            }
-            __syncthreads();
-            const int tn = min(FB, nval - bi * FB);
-            for (int tt = 0; tt < tn; ++tt) {
-                const float* row = cur + tt * (3 * DKC + DV);
-                float qv[16], kv[16], dv[16];
-#pragma unroll
-                for (int r4 = 0; r4 < 4; ++r4) {
-                    const float4 q4 = ld4(row + r0 + 4 * r4), k4 = ld4(row + DKC + r0 + 4 * r4),
-                                 d4 = ld4(row + 2 * DKC + r0 + 4 * r4);
-                    qv[4 * r4] = q4.x; qv[4 * r4 + 1] = q4.y; qv[4 * r4 + 2] = q4.z; qv[4 * r4 + 3] = q4.w;
-                    kv[4 * r4] = k4.x; kv[4 * r4 + 1] = k4.y; kv[4 * r4 + 2] = k4.z; kv[4 * r4 + 3] = k4.w;
-                    dv[4 * r4] = d4.x; dv[4 * r4 + 1] = d4.y; dv[4 * r4 + 2] = d4.z; dv[4 * r4 + 3] = d4.w;
-                }
-                const float4 v4 = owner ? ld4(row + 3 * DKC + j0) : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float2 vlo = make_float2(v4.x, v4.y), vhi = make_float2(v4.z, v4.w);
-                float2 alo[4], ahi[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) alo[e] = ahi[e] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float ki = a.gated ? __fmul_rn(__fsub_rn(1.0f, dv[r]), kv[r]) : kv[r];
-                    S[r][0] = __ffma2_rn(f2(dv[r]), S[r][0], __fmul2_rn(f2(ki), vlo));
-                    S[r][1] = __ffma2_rn(f2(dv[r]), S[r][1], __fmul2_rn(f2(ki), vhi));
-                    alo[r & 3] = __ffma2_rn(S[r][0], f2(qv[r]), alo[r & 3]);
-                    ahi[r & 3] = __ffma2_rn(S[r][1], f2(qv[r]), ahi[r & 3]);
-                }
-                float2 slo = __fadd2_rn(__fadd2_rn(alo[0], alo[1]), __fadd2_rn(alo[2], alo[3]));
-                float2 shi = __fadd2_rn(__fadd2_rn(ahi[0], ahi[1]), __fadd2_rn(ahi[2], ahi[3]));
-#pragma unroll
-                for (int o = TPG / 2; o > 0; o >>= 1) {
-                    slo.x = __fadd_rn(slo.x, __shfl_xor_sync(FULL, slo.x, o));
-                    slo.y = __fadd_rn(slo.y, __shfl_xor_sync(FULL, slo.y, o));
-                    shi.x = __fadd_rn(shi.x, __shfl_xor_sync(FULL, shi.x, o));
-                    shi.y = __fadd_rn(shi.y, __shfl_xor_sync(FULL, shi.y, o));
-                }
-                if (owner && tau == 0 && a.o != nullptr) {
-                    float* orow = a.o + (((size_t)b * a.T + t0 + bi * FB + tt) * a.H + h) * DV + j0;
-                    st_cs(reinterpret_cast<float4*>(orow), make_float4(a.scale * slo.x, a.scale * slo.y,
-                                                                        a.scale * shi.x, a.scale * shi.y));
-                }
-            }
-            __syncthreads();                                 // batch `bi` is read: its buffer can refill
-        }
-        (void)lane;
-    }
-}
-
 // Heads per CTA of chunk_output_heads: the largest block of one group's heads
 // that still gives every SM two CTAs.
 int heads_per_cta(const ChunkArgs& a, int sm_count) {
@@ -1202,14 +1208,6 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
         CUtensorMap mq, mk;
         if (!make_qk_maps(a, &mq, &mk)) return cudaErrorInvalidValue;
         chunk_output<PER_KEY, DV><<<(unsigned)std::min<size_t>(chunks, (size_t)sm_count), NT, out_bytes, s>>>(mq, mk, a);
-    }
-    if constexpr (PER_KEY) {
-        // flagged chunks (usually none: every CTA checks its flags and leaves)
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        e = set_smem_attr_once((const void*)chunk_fix<DV>, FixSmem<DV>::bytes);
-        if (e != cudaSuccess) return e;
-        chunk_fix<DV><<<(unsigned)std::min<size_t>(chunks, (size_t)sm_count), NT, FixSmem<DV>::bytes, s>>>(a);
     }
     return cudaGetLastError();
 }
