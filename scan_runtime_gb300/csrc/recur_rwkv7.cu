@@ -15,8 +15,9 @@ cudaError_t launch_recur_rwkv7_seq(const RecurArgs& x, SnDevStatus* st, uint64_t
 
 bool recur_decode_supported(const RecurArgs& x) { return recur_decode_cols_supported(x); }
 
-cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus*, uint64_t, int sm_count, cudaStream_t stream) {
-    return launch_recur_decode_cols(x, sm_count, stream);   // recur_decode.cu
+cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                cudaStream_t stream) {
+    return launch_recur_decode_cols(x, st, wait_ns, sm_count, stream);   // recur_decode.cu
 }
 
 }  // namespace sn
