@@ -616,8 +616,8 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, cpu=Tru
             out[f"scan_{form}_lookback"] = r
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
         # few channels, long T (B=1 T=262144 N=64, the chunked kernels' regime):
-        # the automatic choice (reduce-then-scan), the look-back kernel and the
-        # sequential kernel
+        # the automatic choice (the fused one-launch kernel), reduce-then-scan,
+        # the look-back kernel and the sequential kernel
         Bf, Tf, Nf = 1, 262144, 64
         xf = synth.scan_inputs(Bf, Tf, Nf, large=True, cid=6)
         af, bf, s0f = xf["a"].to(dev), xf["b"].to(dev), xf["s0"].to(dev)
@@ -629,8 +629,8 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, cpu=Tru
         if cpu:
             fjob = scan_job(xf["a"].numpy(), {"fma": xf["b"].numpy()}, xf["s0"].numpy(), forms=("fma",), block=1)
             fref, _ = fjob.reference(min(len(fjob.units), host_cores()))
-        for label, kern in (("reduce_scan", sr.SN_SCAN_KERNEL_REDUCE_SCAN), ("lookback", sr.SN_SCAN_KERNEL_LOOKBACK),
-                            ("sequential", sr.SN_SCAN_KERNEL_SEQUENTIAL)):
+        for label, kern in (("fused", sr.SN_SCAN_KERNEL_FUSED), ("reduce_scan", sr.SN_SCAN_KERNEL_REDUCE_SCAN),
+                            ("lookback", sr.SN_SCAN_KERNEL_LOOKBACK), ("sequential", sr.SN_SCAN_KERNEL_SEQUENTIAL)):
             ctx.set_option(sr.SN_OPT_SCAN_KERNEL, kern)
             ms = time_form(torch, lambda: sr.sn_scan_fma(ctx.handle, Bf, Tf, Nf, af, bf, s0f, sff, sof, s), warmup,
                            reps, s)
@@ -640,7 +640,7 @@ def bench_forms(torch, sr, ctx, dev, stream, fp32_peak_tflops, hbm_peak, cpu=Tru
                 few[label].update(errors({"s": host(sof), "s_final": host(sff)},
                                          {"s": fref["s_fma"], "s_final": fref["s_final_fma"]}, 1e-5))
         ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
-        few["auto_picks"] = "reduce_scan"
+        few["auto_picks"] = "fused"
         out["scan_fma_few_channels"] = few
         # and its reverse scan (read a, s, ds; write da, db): sequential against chunked
         sr.sn_scan_fma(ctx.handle, Bf, Tf, Nf, af, bf, s0f, sff, sof, s)
@@ -1056,7 +1056,7 @@ PROFILE_CASES = {
     "scan_seq": "sequential scan (FMA), B=8 T=2048 N=2048 (402 MB moved, > L2)",
     "scan_seq_full": "sequential scan (FMA), full workload B=8 T=8192 N=2048 (1.61 GB moved)",
     "scan_lookback": "look-back scan (FMA), B=8 T=2048 N=2048",
-    "scan_few_channels": "reduce-then-scan (FMA, the automatic choice), few channels B=1 T=262144 N=64",
+    "scan_few_channels": "fused chunked scan (FMA, the automatic choice), few channels B=1 T=262144 N=64",
     "scan_bwd_fma": "reverse scan (FMA form), B=8 T=2048 N=2048 (20 B per element)",
     "scan_bwd_gated": "reverse scan (gated form), B=8 T=2048 N=2048 (24 B per element)",
     "gla": "diag per-key, full GLA workload B=4 T=4096 H=4 dk=dv=128",

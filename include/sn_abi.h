@@ -116,8 +116,9 @@ typedef int32_t sn_status;
 #define SN_SCAN_KERNEL_SEQUENTIAL 1
 #define SN_SCAN_KERNEL_LOOKBACK   2
 #define SN_SCAN_KERNEL_REDUCE_SCAN 3   /* the look-back kernel's results in three flag-free passes */
-#define SN_SCAN_KERNEL_FUSED       4   /* the same results in one launch: aggregates, per-column carry
-                                          chains and outputs at once (forward scans, T >= 1024) */
+#define SN_SCAN_KERNEL_FUSED       4   /* the same results in two launches: the aggregate pass, then the
+                                          per-column carry chains inside the state pass (forward scans;
+                                          T < 1024 runs reduce-then-scan) */
 
 /* Operation ids for sn_workspace_bytes(). */
 #define SN_OP_SCAN_FMA   1
@@ -165,11 +166,13 @@ sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes);
 
 /* Workspace bytes the chunked scans need for this problem (op =
  * SN_OP_SCAN_FMA or SN_OP_SCAN_GATED): with columns = B * ceil(N / 32),
- * chunks = ceil(T / 128) and tiles = columns * chunks, a flag word per tile
- * rounded up to 256 bytes, plus the larger of 512 bytes per tile and
- * columns * (1536 * ceil(chunks / 4) + 128) bytes (the second only for
- * sequences of fewer than ten chunks); 0 for an op that needs none, -1 on
- * invalid arguments. */
+ * chunks = ceil(T / 128) and tiles = columns * chunks, the larger of
+ *   a flag word per tile rounded up to 256 bytes, plus the larger of 512
+ *   bytes per tile and columns * (1536 * ceil(chunks / 4) + 128) bytes
+ *   (the look-back and reduce-then-scan kernels), and
+ *   columns * (2048 * ceil(chunks / 4) + 256) bytes from eight chunks on
+ *   (the fused kernel);
+ * 0 for an op that needs none, -1 on invalid arguments. */
 int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N);
 
 /* Return and clear the first device-side error recorded in the context's
@@ -193,13 +196,13 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value);
  * same bits as the single-precision definition at every t, so splitting a
  * sequence into segments and carrying s_final -> s0 reproduces the full run
  * bit for bit ([P1] §4).  For few channels and long T the call chunks T
- * instead: the fused path (chosen automatically there when the workspace
- * covers it, else reduce-then-scan), or the reduce-then-scan path or the
- * decoupled look-back kernel (SN_OPT_SCAN_KERNEL); all three give the same
+ * instead: automatically the fused path where B * ceil(N / 32) >= 2 and the
+ * workspace covers it, else reduce-then-scan; or, by SN_OPT_SCAN_KERNEL, any
+ * of those two or the decoupled look-back kernel; all three give the same
  * bits, are deterministic and are bit-exact under splits at multiples of
  * SN_OPT_LOOKBACK_CHUNK.  Calls may be captured in a CUDA graph and replayed:
- * the look-back kernel keeps its launch epoch in device memory, so every
- * replay tags its chunk flags afresh.
+ * the look-back and fused kernels keep their launch epoch in device memory,
+ * so every replay tags its flags and carry words afresh.
  * Pointers need 4-byte alignment; N % 4 == 0 with 16-byte aligned a, b and
  * s_out enables the TMA path.  Errors: SN_E_INVAL, SN_E_NOMEM (look-back
  * forced without enough workspace), SN_E_DEVICE. */

@@ -264,7 +264,7 @@ sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes) {
 
 int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N) {
     if ((op != SN_OP_SCAN_FMA && op != SN_OP_SCAN_GATED) || !within_elems({B, T, N})) return -1;
-    return lookback_ws_bytes(B, T, N);
+    return std::max(lookback_ws_bytes(B, T, N), scan_fused_applies(T) ? scan_fused_ws_bytes(B, T, N) : 0);
 }
 
 sn_status sn_ctx_last_error(SnCtx* ctx) {
@@ -344,7 +344,7 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     ScanArgs x{B, T, N, a, b, s0, s_final, s_out};
     int kernel = ctx->scan_kernel;
     const int64_t need = lookback_ws_bytes(B, T, N);
-    const int64_t need_fused = scan_fused_ws_bytes(B, T, N);
+    const int64_t need_fused = scan_fused_applies(T) ? scan_fused_ws_bytes(B, T, N) : need;
     if (kernel == SN_SCAN_KERNEL_LOOKBACK || kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
         if (!lookback_supported(x)) return SN_E_UNSUPPORTED;
         if (ctx->ws == nullptr || ctx->ws_bytes < need) return SN_E_NOMEM;
@@ -365,8 +365,12 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         kernel = (few && T >= 8 * LB_TC && lookback_supported(x) && ctx->ws != nullptr && ctx->ws_bytes >= need)
                      ? SN_SCAN_KERNEL_REDUCE_SCAN
                      : SN_SCAN_KERNEL_SEQUENTIAL;
-        // the same results in one launch where the workspace also covers its block flags
-        if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN && ctx->ws_bytes >= need_fused) kernel = SN_SCAN_KERNEL_FUSED;
+        // the same results in two launches (the chain inside the state pass)
+        // where there are two columns of channel tiles or more and the
+        // workspace covers the fused path's arrays
+        if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN && (int64_t)B * ((N + 31) / 32) >= 2 && scan_fused_applies(T) &&
+            ctx->ws_bytes >= need_fused)
+            kernel = SN_SCAN_KERNEL_FUSED;
     }
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
@@ -389,15 +393,15 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         return from_cuda(launch_scan_lookback(x, gated, ctx->ws, ctx->debug_poison, ctx->dstatus, wait_ns(ctx),
                                               ctx->sm_count, s));
     }
+    if (kernel == SN_SCAN_KERNEL_FUSED && !scan_fused_applies(T)) kernel = SN_SCAN_KERNEL_REDUCE_SCAN;   // same bits
     if (kernel == SN_SCAN_KERNEL_FUSED) {
-        // tagged flags as the look-back kernel's (same launch epoch), in other
+        // carry words tagged with the look-back kernel's launch epoch, in other
         // places: cleared when the workspace, the geometry or the user changes
         const int64_t sig = -lookback_flag_count(B, T, N);
         if (ctx->ws_dirty || ctx->lb_last_flags != sig) {
-            int64_t fa, fb, fc;
-            scan_fused_flag_areas(B, T, N, &fa, &fb, &fc);
-            if (cudaMemsetAsync(ctx->ws, 0, (size_t)fa, s) != cudaSuccess ||
-                cudaMemsetAsync(static_cast<char*>(ctx->ws) + fb, 0, (size_t)fc, s) != cudaSuccess ||
+            int64_t ta, tb;
+            scan_fused_tag_area(B, T, N, &ta, &tb);
+            if (cudaMemsetAsync(static_cast<char*>(ctx->ws) + ta, 0, (size_t)tb, s) != cudaSuccess ||
                 cudaMemsetAsync(&ctx->dstatus->abort_tag, 0, sizeof(unsigned int), s) != cudaSuccess)
                 return SN_E_DEVICE;
             ctx->ws_dirty = false;

@@ -1,28 +1,33 @@
 // scan_fused.cu -- the chunked scans of tier 1 for few channels and long T in
-// one launch ("SunnyNet 工程化实录" §2.1 forms; §4 bit-exact continuation).
+// two launches ("SunnyNet 工程化实录" §2.1 forms; §4 bit-exact continuation).
 //
 // The reduce-then-scan path (scan_lookback.cu) runs three launches: every
-// tile's aggregate, then a carry chain per column, then every tile's states
-// from its carry.  The chain is a serial fold over all chunks of a column, so
-// between the two passes the GPU waits for it, and the output pass starts on
-// tiles long gone from L2.  This kernel runs the same three steps at once:
-//   * worker CTAs first compute the aggregates of their tiles (chunk-major,
-//     like the aggregate pass) and raise a tagged flag per tile;
-//   * one chain CTA per column (blockIdx.x < columns, warp 0, lane = channel)
-//     folds C_k = fma(A_k, C_{k-1}, B_k) over the chunks in order, a block of
-//     FU_CB chunks at a time as soon as the block's flags are up (the
-//     aggregates arrive by bulk copies, up to FU_CSTAGES blocks in flight), and
-//     raises a tagged flag per block once its carries are written;
-//   * after their last aggregate the workers compute the states of their
-//     tiles in reverse order (the tiles they read last are still in L2), each
-//     waiting for the flag of the block that holds its incoming carry.
-// Every operation is the reduce-then-scan path's in the same order (the tile
-// local scan, the aggregate, the fold, the outputs), so all chunked paths
-// give the same bits.  Workers never wait during their aggregates, and the
-// chain waits only on aggregates, so the waits always end; the grid is
-// launched cooperatively (every CTA resident), and every wait is bounded
+// tile's aggregate, a carry chain per column, then every tile's states from
+// its carry.  The chain is a serial fold over all chunks of a column (one
+// dependent FMA per chunk and channel), so the GPU idles for its length
+// between the two passes.  Here the chain runs inside the state pass:
+//   1. the aggregate pass (scan_lookback.cu), last tile first, writes every
+//      tile's (A_k, B_k);
+//   2. one cooperative launch: CTA col < columns is the chain of column col
+//      (warp 0, lane = channel), folding C_k = fma(A_k, C_{k-1}, B_k) over the
+//      chunks in order with the aggregates staged by bulk copies (FU_CSTAGES
+//      blocks of FU_CB chunks in flight), and storing each carry as a 64-bit
+//      word that holds the launch's tag beside the carry's bits; the other
+//      CTAs compute the states of the tiles first to last (the first ones
+//      are the last the aggregate pass read, still in L2), each waiting for
+//      the carry word of the chunk before its own.
+// A single-copy-atomic 64-bit access reads or writes tag and value together,
+// so the chain needs no fence and a state tile no flag: it polls its own
+// carry words.  Sharing its SM with state CTAs, a chain folds a chunk in about
+// 30 cycles (10 alone), so a column of chunks takes about as long as the
+// state tiles of two columns: the path pays where a launch has two columns or
+// more, and a single column keeps the reduce-then-scan launches.
+// Every operation is the reduce-then-scan path's in the same order (tile local
+// scan, aggregate, fold, outputs), so all chunked paths give the same bits.
+// The chain waits only on its bulk copies and the state tiles only on the
+// chain, every CTA is resident (cooperative launch), and every wait is bounded
 // (SN_OPT_WAIT_LIMIT_US): a CTA that gives up records SN_E_TIMEOUT and tags
-// the launch, and the others stop waiting at once.  Flags carry the launch
+// the launch, and the others stop waiting at once.  The tags carry the launch
 // epoch (kept in device memory, shared with the look-back kernel), so no call
 // needs a memset while the geometry stays the same.
 #include <algorithm>
@@ -32,11 +37,11 @@
 namespace sn {
 namespace {
 
-constexpr int FU_CB = 64;                          // chunks per carry block
-constexpr int FU_CSTAGES = 4;                      // carry blocks in flight in a chain CTA
-constexpr int FU_STAGES = 2;                       // tiles in flight in a worker CTA
-constexpr uint32_t FU_AGG = 1u;                    // tile flag state: aggregate written
-constexpr uint32_t FU_READY = 2u;                  // block flag state: carries written
+constexpr int FU_CB = 64;                          // chunks per block of a chain's ring
+constexpr int FU_CSTAGES = 4;                      // blocks in flight in a chain CTA
+constexpr int FU_STAGES = 2;                       // tiles in flight in a state CTA (2 CTAs per SM: the
+                                                   // chain keeps its registers; 3 per SM measured slower)
+constexpr uint32_t FU_CARRY = 3u;                  // tag state of a carry word
 constexpr uint32_t FU_EPOCH_WRAP = 1u << 29;
 constexpr uint32_t FU_CBLK_FLOATS = FU_CB * LB_NC;  // one block of one array (agg_index layout)
 constexpr size_t FU_RING = FU_STAGES * (size_t)LB_TILE_BYTES;
@@ -44,22 +49,21 @@ static_assert((size_t)FU_CSTAGES * 2 * FU_CBLK_FLOATS * 4 <= FU_RING, "the chain
 constexpr size_t FU_SMEM = FU_RING + (FU_STAGES + FU_CSTAGES) * 8 + 16;
 
 struct FusedParams {
-    int B, T, N, ncb, nbcb, nchunks, ntiles, nblk;
+    int B, T, N, ncb, nbcb, nchunks, ntiles;
     const float* s0;
     float* s_final;
     float* s_out;
-    uint32_t* tflag;     // per tile ti = k * nbcb + col: tag | FU_AGG
-    uint32_t* bflag;     // per (col, carry block): tag | FU_READY
-    float* dA;           // aggregates and carries at agg_index (per column, chunks in groups of four)
-    float* dB;
-    float* dC;
-    float* cin0;         // [col][channel]: the initial carry as the chain read it
-    SnDevStatus* st;     // error word, abort tag and the launch epoch
+    const float* dA;              // aggregates at agg_index (per column, chunks in groups of four)
+    const float* dB;
+    unsigned long long* cw;       // carries at agg_index: (tag | FU_CARRY) << 32 | bits of C_k
+    unsigned long long* cw0;      // [col][channel]: the same for the initial carry
+    SnDevStatus* st;              // error word, abort tag and the launch epoch
     uint64_t wait_ns;
 };
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+__device__ __forceinline__ void st_relaxed_gpu_v2u64(unsigned long long* p, unsigned long long a,
+                                                     unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
 template <bool GATED>
@@ -83,6 +87,7 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
     __syncthreads();
     const uint32_t epoch = s_epoch;
     const uint32_t tag = epoch << 2;
+    const unsigned long long hi = (unsigned long long)(tag | FU_CARRY) << 32;
     auto aborted = [&]() { return *reinterpret_cast<volatile const uint32_t*>(&p.st->abort_tag) == tag; };
     auto give_up = [&](int site) {
         record_error(p.st, SN_E_TIMEOUT, (SN_K_SCAN_LOOKBACK << 16) | site);
@@ -107,75 +112,100 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
         float* ring = reinterpret_cast<float*>(smem);             // [stage][A | B][FU_CBLK_FLOATS]
         uint64_t* cbar = bar + FU_STAGES;
         const size_t colbase = agg_index(col, nq, 0, 0);
-        float c = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
-        // the first chunk's carry comes from here, not from s0: a call may
-        // write its final states over s0
-        p.cin0[col * LB_NC + lane] = c;
-        // block j's aggregates are all written: every tile flag of it carries this launch's tag
-        auto ready = [&](int j) {
-            const int k0 = j * FU_CB, cnt = min(FU_CB, p.nchunks - k0);
-            bool ok = true;
-            for (int i = lane; i < cnt; i += 32)
-                ok = ok && ld_acquire_gpu(p.tflag + (size_t)(k0 + i) * p.nbcb + col) == (tag | FU_AGG);
-            return __all_sync(0xffffffffu, ok);
-        };
-        auto issue = [&](int j) {   // after `ready`: the aggregates of block j into stage j % FU_CSTAGES
-            __syncwarp();                 // every lane's acquire before lane 0's copies
-            fence_proxy_async_global();   // the flags' acquire before the bulk copies' reads
-            if (lane == 0) {
-                const int k0 = j * FU_CB, st = j % FU_CSTAGES;
-                const uint32_t bytes = (uint32_t)chunk_quads(min(FU_CB, p.nchunks - k0)) * LB_NC * 16;
-                mbar_arrive_expect_tx(&cbar[st], 2 * bytes);
-                bulk_load(ring + (size_t)st * 2 * FU_CBLK_FLOATS, p.dA + colbase + (size_t)k0 * LB_NC, bytes, &cbar[st]);
-                bulk_load(ring + (size_t)st * 2 * FU_CBLK_FLOATS + FU_CBLK_FLOATS, p.dB + colbase + (size_t)k0 * LB_NC,
-                          bytes, &cbar[st]);
-            }
+        const int nblk = (p.nchunks + FU_CB - 1) / FU_CB;
+        auto issue = [&](int j) {   // lane 0: block j's aggregates into stage j % FU_CSTAGES
+            const int k0 = j * FU_CB, st = j % FU_CSTAGES;
+            const uint32_t bytes = (uint32_t)chunk_quads(min(FU_CB, p.nchunks - k0)) * LB_NC * 16;
+            mbar_arrive_expect_tx(&cbar[st], 2 * bytes);
+            bulk_load(ring + (size_t)st * 2 * FU_CBLK_FLOATS, p.dA + colbase + (size_t)k0 * LB_NC, bytes, &cbar[st]);
+            bulk_load(ring + (size_t)st * 2 * FU_CBLK_FLOATS + FU_CBLK_FLOATS, p.dB + colbase + (size_t)k0 * LB_NC,
+                      bytes, &cbar[st]);
         };
         int issued = 0;
+        if (lane == 0)
+            for (; issued < min(nblk, FU_CSTAGES); ++issued) issue(issued);
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        // the first chunk's carry is published from here, not read from s0 by
+        // the state tiles: a call may write its final states over s0
+        float c = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
+        st_relaxed_gpu_u64(p.cw0 + col * LB_NC + lane, hi | __float_as_uint(c));
+        unsigned long long* cwc = p.cw + colbase;
+        // four carries of the lane's channel (chunks 4 q .. 4 q + 3) as two 16-byte stores
+        auto put4 = [&](int q, float4 r) {
+            unsigned long long* d = cwc + ((size_t)q * LB_NC + lane) * 4;
+            st_relaxed_gpu_v2u64(d, hi | __float_as_uint(r.x), hi | __float_as_uint(r.y));
+            st_relaxed_gpu_v2u64(d + 2, hi | __float_as_uint(r.z), hi | __float_as_uint(r.w));
+        };
         bool ok = true;
-        for (int j = 0; j < p.nblk && ok; ++j) {
-            // blocks j .. j + FU_CSTAGES - 1 go out as their aggregates appear; block j must
-            const int limit = min(p.nblk, j + FU_CSTAGES);
-            const uint64_t t0 = global_ns();
-            while (issued < limit) {
-                if (ready(issued)) {
-                    issue(issued);
-                    ++issued;
-                    continue;
-                }
-                if (issued > j) break;                                 // something to fold meanwhile
-                if (global_ns() - t0 > p.wait_ns || aborted()) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (!ok) break;
+        for (int j = 0; j < nblk; ++j) {
             const int st = j % FU_CSTAGES;
             ok = __all_sync(0xffffffffu, mbar_wait(&cbar[st], (uint32_t)(j / FU_CSTAGES) & 1, p.wait_ns));
             if (!ok) break;
             const int k0 = j * FU_CB, cnt = min(FU_CB, p.nchunks - k0);
-            const float* fA = ring + (size_t)st * 2 * FU_CBLK_FLOATS;
-            const float* fB = fA + FU_CBLK_FLOATS;
-            float* fC = p.dC + colbase + (size_t)k0 * LB_NC;
-            for (int g = 0; g < (cnt >> 2); ++g) {                  // whole groups of four chunks
-                const float4 a4 = reinterpret_cast<const float4*>(fA)[g * LB_NC + lane];
-                const float4 b4 = reinterpret_cast<const float4*>(fB)[g * LB_NC + lane];
-                float4 r;
-                c = __fmaf_rn(a4.x, c, b4.x); r.x = c;
-                c = __fmaf_rn(a4.y, c, b4.y); r.y = c;
-                c = __fmaf_rn(a4.z, c, b4.z); r.z = c;
-                c = __fmaf_rn(a4.w, c, b4.w); r.w = c;
-                __stcg(reinterpret_cast<float4*>(fC) + g * LB_NC + lane, r);
+            const float4* sA = reinterpret_cast<const float4*>(ring + (size_t)st * 2 * FU_CBLK_FLOATS) + lane;
+            const float4* sB = sA + FU_CBLK_FLOATS / 4;
+            const int q0 = k0 >> 2;
+            if (cnt == FU_CB) {
+                // a full block: the groups are read a batch of four ahead of the
+                // FMAs that consume them, so the dependent chain waits on no load
+                constexpr int NG = FU_CB / 4, QB = 4;
+                float4 a0[QB], b0[QB], a1[QB], b1[QB];
+#pragma unroll
+                for (int u = 0; u < QB; ++u) {
+                    a0[u] = sA[u * LB_NC];
+                    b0[u] = sB[u * LB_NC];
+                }
+#pragma unroll
+                for (int g = 0; g < NG; g += 2 * QB) {
+#pragma unroll
+                    for (int u = 0; u < QB; ++u) {
+                        a1[u] = sA[(g + QB + u) * LB_NC];
+                        b1[u] = sB[(g + QB + u) * LB_NC];
+                    }
+#pragma unroll
+                    for (int u = 0; u < QB; ++u) {
+                        float4 r;
+                        c = __fmaf_rn(a0[u].x, c, b0[u].x); r.x = c;
+                        c = __fmaf_rn(a0[u].y, c, b0[u].y); r.y = c;
+                        c = __fmaf_rn(a0[u].z, c, b0[u].z); r.z = c;
+                        c = __fmaf_rn(a0[u].w, c, b0[u].w); r.w = c;
+                        put4(q0 + g + u, r);
+                    }
+                    if (g + 2 * QB < NG) {
+#pragma unroll
+                        for (int u = 0; u < QB; ++u) {
+                            a0[u] = sA[(g + 2 * QB + u) * LB_NC];
+                            b0[u] = sB[(g + 2 * QB + u) * LB_NC];
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < QB; ++u) {
+                        float4 r;
+                        c = __fmaf_rn(a1[u].x, c, b1[u].x); r.x = c;
+                        c = __fmaf_rn(a1[u].y, c, b1[u].y); r.y = c;
+                        c = __fmaf_rn(a1[u].z, c, b1[u].z); r.z = c;
+                        c = __fmaf_rn(a1[u].w, c, b1[u].w); r.w = c;
+                        put4(q0 + g + QB + u, r);
+                    }
+                }
+            } else {
+                // the sequence's last, partial block: one chunk at a time
+                const float* fA = ring + (size_t)st * 2 * FU_CBLK_FLOATS;
+                const float* fB = fA + FU_CBLK_FLOATS;
+                for (int i = 0; i < cnt; ++i) {
+                    const int o = ((i >> 2) * LB_NC + lane) * 4 + (i & 3);
+                    c = __fmaf_rn(fA[o], c, fB[o]);
+                    st_relaxed_gpu_u64(cwc + ((size_t)(q0 + (i >> 2)) * LB_NC + lane) * 4 + (i & 3),
+                                       hi | __float_as_uint(c));
+                }
             }
-            for (int i = cnt & ~3; i < cnt; ++i) {                  // the sequence's last, partial group
-                const int o = ((i >> 2) * LB_NC + lane) * 4 + (i & 3);
-                c = __fmaf_rn(fA[o], c, fB[o]);
-                __stcg(&fC[o], c);
-            }
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence();
-                st_release_gpu(p.bflag + col * p.nblk + j, tag | FU_READY);
+            __syncwarp();                                 // the stage is read
+            if (issued < nblk) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();             // those reads before the copy's writes
+                    issue(issued);
+                }
+                ++issued;
             }
         }
         if (!ok && lane == 0) {
@@ -189,45 +219,39 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
         return;
     }
 
-    // ---------------------------------------------------- worker CTAs
+    // ---------------------------------------------------- state CTAs
     const int w = (int)blockIdx.x - p.nbcb, nw = (int)gridDim.x - p.nbcb;
-    const int ni = w < p.ntiles ? (p.ntiles - 1 - w) / nw + 1 : 0;   // tiles w, w + nw, ...
+    const int ni = w < p.ntiles ? (p.ntiles - 1 - w) / nw + 1 : 0;   // tiles w, w + nw, ... (chunk order)
     float* bufs = reinterpret_cast<float*>(smem);
-    // load idx < ni: aggregate of tile w + idx nw; idx >= ni: states of the tiles in reverse
-    auto tile_of = [&](int idx) { return w + (idx < ni ? idx : 2 * ni - 1 - idx) * nw; };
     auto coords = [&](int ti, int& k, int& bi, int& cb) {
         k = ti / p.nbcb;
         const int r = ti - k * p.nbcb;
         bi = r / p.ncb;
         cb = r - bi * p.ncb;
     };
-    auto issue = [&](int idx, int buf) {
+    auto issue = [&](int i, int buf) {
         int k, bi, cb;
-        coords(tile_of(idx), k, bi, cb);
+        coords(w + i * nw, k, bi, cb);
         mbar_arrive_expect_tx(&bar[buf], LB_TILE_BYTES);
         float* dst = bufs + buf * 2 * LB_TILE;
         tma_load_3d(dst, &map_a, &bar[buf], cb * LB_NC, k * LB_TC, bi);
         tma_load_3d(dst + LB_TILE, &map_b, &bar[buf], cb * LB_NC, k * LB_TC, bi);
     };
-    const int nload = 2 * ni;
     if (tid == 0)
-        for (int s = 0; s < FU_STAGES - 1 && s < nload; ++s) issue(s, s);
-    bool ok = true;
-    for (int idx = 0; idx < nload; ++idx) {
-        const int buf = idx % FU_STAGES;
-        if (tid == 0 && idx + FU_STAGES - 1 < nload) issue(idx + FU_STAGES - 1, (idx + FU_STAGES - 1) % FU_STAGES);
-        const int ti = tile_of(idx);
+        for (int s = 0; s < FU_STAGES - 1 && s < ni; ++s) issue(s, s);
+    for (int i = 0; i < ni; ++i) {
+        const int buf = i % FU_STAGES;
+        if (tid == 0 && i + FU_STAGES - 1 < ni) issue(i + FU_STAGES - 1, (i + FU_STAGES - 1) % FU_STAGES);
         int k, bi, cb;
-        coords(ti, k, bi, cb);
+        coords(w + i * nw, k, bi, cb);
         const int t0 = k * LB_TC, n0 = cb * LB_NC;
         const int rows = min(LB_TC, p.T - t0);
-        if (!__syncthreads_and(mbar_wait(&bar[buf], (uint32_t)(idx / FU_STAGES) & 1, p.wait_ns))) {
+        if (!__syncthreads_and(mbar_wait(&bar[buf], (uint32_t)(i / FU_STAGES) & 1, p.wait_ns))) {
             if (tid == 0) {
                 give_up(6);
-                for (int j = idx; j < min(nload, idx + FU_STAGES); ++j)
+                for (int j = i; j < min(ni, i + FU_STAGES); ++j)
                     (void)mbar_wait(&bar[j % FU_STAGES], (uint32_t)(j / FU_STAGES) & 1, p.wait_ns);
             }
-            ok = false;
             break;
         }
         const float* sa = bufs + buf * 2 * LB_TILE;
@@ -238,71 +262,64 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
         if (warp == 0) {
             float CA, CB;
             tile_aggregate(wA, wB, lane, CA, CB);
-            if (idx < ni) {
-                const size_t me = agg_index(col, nq, k, lane);
-                p.dA[me] = CA;
-                p.dB[me] = CB;
-                __syncwarp();
-                if (lane == 0) st_release_gpu(p.tflag + ti, tag | FU_AGG);
-            } else {
-                // the incoming carry: chunk k - 1's, in carry block (k - 1) / FU_CB
-                const int kb = k == 0 ? 0 : (k - 1) / FU_CB;
-                const uint32_t* bf = p.bflag + col * p.nblk + kb;
+            // the incoming carry: chunk k - 1's word (the initial carry's for k = 0)
+            const unsigned long long* src =
+                k == 0 ? p.cw0 + col * LB_NC + lane : p.cw + agg_index(col, nq, k - 1, lane);
+            unsigned long long v = ld_relaxed_gpu_u64(src);
+            bool got = true;
+            if ((v & 0xffffffff00000000ull) != hi) {
                 const uint64_t t0w = global_ns();
-                bool got = true;
-                while (ld_acquire_gpu(bf) != (tag | FU_READY)) {
+                do {
                     if (global_ns() - t0w > p.wait_ns || aborted()) {
                         got = false;
                         break;
                     }
-                }
-                got = __all_sync(0xffffffffu, got);
-                if (!got && lane == 0) give_up(7);
-                const float cin = !got ? 0.f
-                                  : k == 0 ? __ldcg(p.cin0 + col * LB_NC + lane)
-                                           : __ldcg(p.dC + agg_index(col, nq, k - 1, lane));
-                const float Ck = __fmaf_rn(CA, cin, CB);
-                carry[lane] = cin;
-                cfin[lane] = Ck;
-                const int n = n0 + lane;
-                if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
+                    // back off: a chain CTA may share this SM, and its warp
+                    // folds fastest with the issue slots to itself
+                    __nanosleep(200);
+                    v = ld_relaxed_gpu_u64(src);
+                } while ((v & 0xffffffff00000000ull) != hi);
             }
+            got = __all_sync(0xffffffffu, got);
+            if (!got && lane == 0) give_up(7);
+            const float cin = got ? __uint_as_float((uint32_t)v) : 0.f;
+            const float Ck = __fmaf_rn(CA, cin, CB);
+            carry[lane] = cin;
+            cfin[lane] = Ck;
+            const int n = n0 + lane;
+            if (k == p.nchunks - 1 && p.s_final != nullptr && n < p.N) p.s_final[(size_t)bi * p.N + n] = Ck;
         }
-        if (idx >= ni) {
-            __syncthreads();
-            tile_outputs<GATED>(sa, sb, rows, carry, cfin, EA, EB, p.s_out + ((size_t)bi * p.T + t0) * p.N + n0,
-                                p.N, p.s_out != nullptr && n0 + 4 * quad < p.N);
-        }
+        __syncthreads();
+        tile_outputs<GATED>(sa, sb, rows, carry, cfin, EA, EB, p.s_out + ((size_t)bi * p.T + t0) * p.N + n0, p.N,
+                            p.s_out != nullptr && n0 + 4 * quad < p.N);
         __syncthreads();                              // buffer `buf` free for the next load
     }
-    (void)ok;
-    __syncthreads();
     if (tid == 0) finish();
 }
 
 }  // namespace
 
-// Workspace of the fused path: the tile flags at the start (where the
-// look-back kernel keeps its flags), the reduce-then-scan arrays after them,
-// then the block flags.  Returns the bytes it needs (at most the look-back
-// workspace in every case it is chosen for: T >= 8 chunks).
+// The fused path runs for eight chunks or more (shorter scans take the
+// reduce-then-scan launches, which give the same bits).
+bool scan_fused_applies(int T) { return (T + LB_TC - 1) / LB_TC >= 8; }
+
+// Workspace of the fused path: the A and B arrays of the aggregate pass, the
+// tagged carry words (one per chunk and channel, same layout), the tagged
+// initial carries.  Returns the bytes it needs.
 int64_t scan_fused_ws_bytes(int B, int T, int N) {
     const int64_t ncb = (N + LB_NC - 1) / LB_NC, nbcb = (int64_t)B * ncb;
-    const int64_t nch = (T + LB_TC - 1) / LB_TC, tiles = nbcb * nch;
-    const int64_t flag_bytes = ((tiles * 4 + 255) / 256) * 256;
-    const int64_t arr = nbcb * chunk_quads((int)nch) * LB_NC * 4 * 4;   // bytes per array
-    const int64_t nblk = (nch + FU_CB - 1) / FU_CB;
-    return flag_bytes + 3 * arr + nbcb * LB_NC * 4 + nbcb * nblk * 4;
+    const int64_t nch = (T + LB_TC - 1) / LB_TC;
+    const int64_t arr = nbcb * chunk_quads((int)nch) * LB_NC * 4 * 4;   // bytes per f32 array
+    return 4 * arr + nbcb * LB_NC * 8;
 }
 
-// the bytes of the two flag areas a change of geometry must clear: [0, a) and [b, b + c)
-void scan_fused_flag_areas(int B, int T, int N, int64_t* a, int64_t* b, int64_t* c) {
+// the tagged words' bytes [a, a + b), which a change of geometry clears
+void scan_fused_tag_area(int B, int T, int N, int64_t* a, int64_t* b) {
     const int64_t ncb = (N + LB_NC - 1) / LB_NC, nbcb = (int64_t)B * ncb;
-    const int64_t nch = (T + LB_TC - 1) / LB_TC, tiles = nbcb * nch;
-    const int64_t nblk = (nch + FU_CB - 1) / FU_CB;
-    *a = ((tiles * 4 + 255) / 256) * 256;
-    *c = nbcb * nblk * 4;
-    *b = scan_fused_ws_bytes(B, T, N) - *c;
+    const int64_t nch = (T + LB_TC - 1) / LB_TC;
+    const int64_t arr = nbcb * chunk_quads((int)nch) * LB_NC * 4 * 4;
+    *a = 2 * arr;
+    *b = 2 * arr + nbcb * LB_NC * 8;
 }
 
 cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
@@ -319,20 +336,16 @@ cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStat
     p.nbcb = x.B * p.ncb;
     p.nchunks = (x.T + LB_TC - 1) / LB_TC;
     p.ntiles = p.nbcb * p.nchunks;
-    p.nblk = (p.nchunks + FU_CB - 1) / FU_CB;
     p.s0 = x.s0;
     p.s_final = x.s_final;
     p.s_out = x.s_out;
-    int64_t fa, fb, fc;
-    scan_fused_flag_areas(x.B, x.T, x.N, &fa, &fb, &fc);
-    char* base = static_cast<char*>(ws);
     const int64_t arr = (int64_t)p.nbcb * chunk_quads(p.nchunks) * LB_NC * 4;   // floats per array
-    p.tflag = reinterpret_cast<uint32_t*>(base);
-    p.dA = reinterpret_cast<float*>(base + fa);
-    p.dB = p.dA + arr;
-    p.dC = p.dB + arr;
-    p.cin0 = p.dC + arr;
-    p.bflag = reinterpret_cast<uint32_t*>(base + fb);
+    float* dA = static_cast<float*>(ws);
+    float* dB = dA + arr;
+    p.dA = dA;
+    p.dB = dB;
+    p.cw = reinterpret_cast<unsigned long long*>(dB + arr);
+    p.cw0 = p.cw + arr;
     p.st = st;
     p.wait_ns = wait_ns;
 
@@ -340,9 +353,11 @@ cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStat
     int occ = 0;
     cudaError_t e = occupancy_once((const void*)kern, LB_THREADS, FU_SMEM, &occ);
     if (e != cudaSuccess) return e;
-    // every column's chain CTA plus the workers, all resident (cooperative launch)
+    // every column's chain CTA plus the state CTAs, all resident (cooperative launch)
     const int64_t resident = (int64_t)occ * sm_count;
     if (resident <= p.nbcb) return cudaErrorInvalidConfiguration;
+    e = launch_scan_aggregates(x, gated, dA, dB, st, wait_ns, sm_count, stream);
+    if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(resident, p.nbcb + (int64_t)p.ntiles);
     void* args[] = {(void*)&ma, (void*)&mb, (void*)&p};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(LB_THREADS), args, FU_SMEM, stream);

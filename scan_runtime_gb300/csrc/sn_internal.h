@@ -117,13 +117,17 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int po
 // launches without flags, for few channel tiles and long T; same workspace.
 cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
                                     int sm_count, cudaStream_t stream);
-// The same results in one cooperative launch (scan_fused.cu): tile aggregates,
-// one chain CTA per column of tiles folding its carries, and the outputs run
-// at once.  Workspace bytes it needs,
-// and the two tagged flag areas a change of geometry must clear ([0, a) and
-// [b, b + c)).
+// The reduce-then-scan path's aggregate pass alone, last tile first (scan_lookback.cu).
+cudaError_t launch_scan_aggregates(const ScanArgs& x, bool gated, float* dA, float* dB, SnDevStatus* st,
+                                   uint64_t wait_ns, int sm_count, cudaStream_t stream);
+// The same results in two launches (scan_fused.cu): the aggregate pass, then
+// one cooperative launch in which a chain CTA per column of tiles folds the
+// carries while the other CTAs compute the states.  Whether it runs (eight
+// chunks or more; else the reduce-then-scan launches run), the workspace
+// bytes it needs, and the tagged area [a, a + b) a change of geometry clears.
+bool scan_fused_applies(int T);
 int64_t scan_fused_ws_bytes(int B, int T, int N);
-void scan_fused_flag_areas(int B, int T, int N, int64_t* a, int64_t* b, int64_t* c);
+void scan_fused_tag_area(int B, int T, int N, int64_t* a, int64_t* b);
 cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
                               int sm_count, cudaStream_t stream);
 
@@ -158,9 +162,10 @@ bool recur_seq_width_ok(const RecurArgs& x, int sm_count, int width);
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);
-// recur_decode.cu: T == 1 of the diagonal-decay kinds and the delta rule
+// recur_decode.cu: T == 1 of every kind (diagonal decays, the delta rule, RWKV-7)
 bool recur_decode_cols_supported(const RecurArgs& x);
-cudaError_t launch_recur_decode_cols(const RecurArgs& x, int sm_count, cudaStream_t stream);
+cudaError_t launch_recur_decode_cols(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+                                     cudaStream_t stream);
 
 // Chunked tensor-core form of the delta rule (recur_delta_chunked.cu).
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv);

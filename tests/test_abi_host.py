@@ -127,6 +127,15 @@ def test_workspace_bytes(abi):
     tiles = 8 * (2048 // 32) * (8192 // 128)
     # flags, the A and B aggregates (f32) and the tagged carry words (u64)
     assert nb == ((tiles * 4 + 255) // 256) * 256 + tiles * (2 * 32 * 4 + 32 * 8)
+    # the fused kernel's arrays (from eight chunks on): A and B, a tagged
+    # 8-byte carry word per chunk and channel, the tagged initial carries
+    cols, chunks = 8 * (2048 // 32), 8192 // 128
+    assert nb == max(nb, cols * (2048 * ((chunks + 3) // 4) + 256))
+    cols, chunks = 3 * (64 // 32), 9
+    fused = cols * (2048 * ((chunks + 3) // 4) + 256)
+    lb = ((cols * chunks * 4 + 255) // 256) * 256 + cols * chunks * 512
+    assert fused > lb
+    assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 3, 9 * 128, 64) == fused
     # fewer than ten chunks: the reduce-then-scan arrays (chunks in groups of
     # four per column, three arrays, plus the columns' initial carries) set it
     cols, chunks = 2 * (64 // 32), 5
