@@ -126,7 +126,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20",
                  "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -165,14 +165,20 @@ class ClockSampler:
         if not rows:
             return None
         inwin = [r for r in rows if self.t_on and self.t_off and self.t_on <= r["ts"] <= self.t_off]
-        use = inwin or rows
+        # a timed region shorter than the sampling period may hold no sample:
+        # then the samples within 0.1 s of it (warm-up and the region itself
+        # keep the GPU loaded), else all
+        near = [r for r in rows if self.t_on and self.t_off and self.t_on - 0.1 <= r["ts"] <= self.t_off + 0.1]
+        use = inwin or near or rows
         reasons = []
         for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
                           ("pcap", "sw_power_cap")):
             if any(r[key].lower() == "active" for r in use):
                 reasons.append(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in use),
-                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inwin)}
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inwin),
+                "within_0.1s_of_timed_region": bool(inwin or near),
+                "timed_region_ms": round((self.t_off - self.t_on) * 1e3, 1) if self.t_on and self.t_off else None}
 
 
 # ---------------------------------------------------------------- CPU oracle record
