@@ -337,8 +337,9 @@ sn_status sn_recur_diag_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, int
                                 float* o, void* stream);
 
 /* Workspace bytes sn_recur_diag_chunked needs: B * H * ceil(T / 128) chunk
- * states of dk x dv floats, two vectors of dk floats per chunk and one int32
- * per chunk (each part rounded up to 256 bytes); -1 on invalid arguments. */
+ * states of dk x dv floats, two vectors of dk floats per chunk, one int32 per
+ * chunk and a 128 x dv tile of v per chunk (each part rounded up to 256
+ * bytes); -1 on invalid arguments. */
 int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* Chunked tensor-core form of sn_recur_delta: the same delta rule and readout

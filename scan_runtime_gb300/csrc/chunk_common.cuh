@@ -37,6 +37,7 @@ struct ChunkArgs {
     int* bad;       // (B, H, NC): per-key decays whose anchor factors leave 2^{+-RANGE_LOG2}
     const float* vt;   // optional: per chunk a v^T operand tile (rows value, K = token, tf32)
                        // that replaces v in the output stage (bulk-loaded)
+    float* vt_out;     // optional: where chunk_state stores its rounded v^T tile per chunk
     SnDevStatus* st;
     uint64_t wait_ns;
     int n0, nsg;       // the output kernel alone: chunks [n0, n0 + nsg) (nsg = 0: all NC chunks)

@@ -225,6 +225,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
         // dS^T (M = dv rows c, N = dk columns i) = v^T (K = t) x Khat^T (K = t)
         tc::gemm_tf32(tmem, Vs, Ks, CH, tc::idesc_tf32(DV, DKC), false);
         tc::commit(bar);
+        // the same v^T tile is the output stage's operand: one bulk copy out
+        if (a.vt_out != nullptr) {
+            bulk_store(a.vt_out + (c.bh * a.NC + c.n) * (size_t)DV * CH, Vs, DV * CH * 4);
+            bulk_commit();
+        }
     }
     const bool ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
     tc::fence_after_sync();
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     } else if (tid == 0) {
         record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_STATE_WAIT);
     }
+    if (tid == 0 && a.vt_out != nullptr) bulk_wait_all();   // the v^T copy is done before the CTA leaves
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, DKC);
@@ -1237,7 +1243,7 @@ size_t chunk::output_unit_decay_smem() { return OutSmem<128>::bytes; }
 int64_t chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;
     return round256((int64_t)B * H * nc * dk * dv * 4) + 2 * round256((int64_t)B * H * nc * dk * 4) +
-           round256((int64_t)B * H * nc * 4);
+           round256((int64_t)B * H * nc * 4) + round256((int64_t)B * H * nc * dv * CH * 4);
 }
 
 bool chunked_supported(const RecurArgs& x) {
@@ -1263,6 +1269,10 @@ cudaError_t launch_recur_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     p += round256((int64_t)x.B * x.H * a.NC * x.dk * 4);
     const bool per_key = x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_KEY_GATED;
     a.bad = per_key ? reinterpret_cast<int*>(p) : nullptr;   // written by chunk_state every call
+    p += round256((int64_t)x.B * x.H * a.NC * 4);
+    // per key: chunk_state leaves its rounded v^T tiles for the output stage
+    a.vt_out = per_key ? reinterpret_cast<float*>(p) : nullptr;
+    a.vt = a.vt_out;
     a.st = st;
     a.wait_ns = wait_ns;
     a.gated = x.kind == RK_DIAG_KEY_GATED || x.kind == RK_DIAG_HEAD_GATED;

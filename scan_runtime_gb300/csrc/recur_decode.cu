@@ -51,14 +51,16 @@ struct DecodeParams {
     uint64_t wait_ns;
 };
 
-// The tile: 256 threads, ROWS = 16 key rows x 4 value columns per thread, so
-// a step covers SPC = 256 / ((dv / 4) (dk / 16)) states = 64 KB, and three
-// such stages are in flight.  (Eight rows at dk = 64, 32 KB steps in six
+// The tile: ROWS = 16 key rows x 4 value columns per thread, so a step covers
+// SPC = THREADS / ((dv / 4) (dk / 16)) states, and 192 KB of such stages are
+// in flight.  256 threads (64 KB steps, three stages), except 64 x 64 states:
+// 192 threads, three states (48 KB) per step in four stages, so the steps
+// split more evenly over the SMs.  (Eight rows at dk = 64, 32 KB steps in six
 // stages, measured slower: RWKV-7 decode 0.814 against 0.837 of HBM.)
 template <int DK, int DV>
 struct RingShape {
     static constexpr int ROWS = 16;
-    static constexpr int THREADS = 256;
+    static constexpr int THREADS = DK == 64 && DV == 64 ? 192 : 256;
     static constexpr int TPG = DK / ROWS;               // threads per column quad
     static constexpr int QUADS = DV / 4;                // column quads per state
     static constexpr int PER_STATE = QUADS * TPG;       // threads per state
@@ -130,7 +132,7 @@ __device__ __forceinline__ float4 quad_dot(const float4 (&P)[ROWS], const float*
 }
 
 template <int KIND, int DK, int DV, int R>
-__global__ void __launch_bounds__(256, 1) recur_decode_ring(const DecodeParams p) {
+__global__ void __launch_bounds__(RingShape<DK, DV>::THREADS, 1) recur_decode_ring(const DecodeParams p) {
     using S = RingShape<DK, DV>;
     constexpr int ROWS = S::ROWS, TPG = S::TPG, SPC = S::SPC, QPW = S::QPW, NS = S::NS;
     using Q = QuadRows<DK, R, ROWS>;
@@ -317,18 +319,19 @@ __global__ void __launch_bounds__(256, 1) recur_decode_ring(const DecodeParams p
 template <int KIND, int R>
 cudaError_t run_decode_rows(const RecurArgs& x, const DecodeParams& p, int sm_count, cudaStream_t s) {
     const int BH = x.B * x.H;
-    auto go = [&](auto kern, int spc, size_t smem) -> cudaError_t {
-        cudaError_t e = set_smem_attr_once((const void*)kern, smem);
+    auto go = [&](auto kern, auto shape) -> cudaError_t {
+        using S = decltype(shape);
+        cudaError_t e = set_smem_attr_once((const void*)kern, S::smem);
         if (e != cudaSuccess) return e;
-        const int grid = std::min((BH + spc - 1) / spc, sm_count);
-        kern<<<grid, 256, smem, s>>>(p);
+        const int grid = std::min((BH + S::SPC - 1) / S::SPC, sm_count);
+        kern<<<grid, S::THREADS, S::smem, s>>>(p);
         return cudaGetLastError();
     };
     if (x.dk == 128)
-        return x.dv == 128 ? go(recur_decode_ring<KIND, 128, 128, R>, RingShape<128, 128>::SPC, RingShape<128, 128>::smem)
-                           : go(recur_decode_ring<KIND, 128, 64, R>, RingShape<128, 64>::SPC, RingShape<128, 64>::smem);
-    return x.dv == 128 ? go(recur_decode_ring<KIND, 64, 128, R>, RingShape<64, 128>::SPC, RingShape<64, 128>::smem)
-                       : go(recur_decode_ring<KIND, 64, 64, R>, RingShape<64, 64>::SPC, RingShape<64, 64>::smem);
+        return x.dv == 128 ? go(recur_decode_ring<KIND, 128, 128, R>, RingShape<128, 128>{})
+                           : go(recur_decode_ring<KIND, 128, 64, R>, RingShape<128, 64>{});
+    return x.dv == 128 ? go(recur_decode_ring<KIND, 64, 128, R>, RingShape<64, 128>{})
+                       : go(recur_decode_ring<KIND, 64, 64, R>, RingShape<64, 64>{});
 }
 
 // The rows per lane whose summation order the decode reproduces: the sequence

@@ -158,8 +158,10 @@ def test_chunked_workspace_bytes(abi):
     r256 = lambda x: (x + 255) // 256 * 256
     for B, T, H, dv in ((4, 4096, 4, 128), (1, 300, 3, 64), (2, 1, 1, 128)):
         nc = (T + 127) // 128
-        # chunk states, the chunk decays and anchor factors, and one flag per chunk
-        want = r256(B * H * nc * 128 * dv * 4) + 2 * r256(B * H * nc * 128 * 4) + r256(B * H * nc * 4)
+        # chunk states, the chunk decays and anchor factors, one flag per chunk,
+        # and the chunk's v tile (transposed once, for the output stage)
+        want = (r256(B * H * nc * 128 * dv * 4) + 2 * r256(B * H * nc * 128 * 4) + r256(B * H * nc * 4) +
+                r256(B * H * nc * dv * 128 * 4))
         assert abi.sn_recur_chunked_workspace_bytes(B, T, H, 128, dv) == want
 
 
