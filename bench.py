@@ -398,7 +398,7 @@ def err_pair(y, r):
 
 def errors(outs, ref, tol, pages=None):
     """Per-output error figures against the fp64 oracle, with the bound."""
-    rec = {"err_normwise": {}, "err_elementwise": {}, "tolerance": tol}
+    rec = {"err_normwise": {}, "err_elementwise": {}, "tolerance": tol, "tolerance_on": "err_normwise"}
     for k, y in outs.items():
         nw, ew = err_pair(y, ref[k])
         rec["err_normwise"][k] = float(f"{nw:.3e}")
