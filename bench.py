@@ -958,7 +958,7 @@ def run_ours(args):
     value = whole_job_gbps(step_bytes, args.steps, world, ms_total)
     achieved = per_form_bytes / (avg_launch_ms / 1e3) / GB
 
-    # end to end through the public API (Context.scan_host): pinned host inputs
+    # end to end through the C ABI's host-buffer call (sn_scan_host): pinned host inputs
     # in, both forms' s_t and s_final out, every step; wall clock per step
     e2e = None
     if not args.no_e2e:
@@ -969,7 +969,7 @@ def run_ours(args):
                 for f in ("fma", "gated")}
 
         def e2e_step():
-            ctx.scan_host(hbuf["a"], hbuf["b"], hbuf["u"], hbuf["s0"], out=hout, rows_per_chunk=1, nstreams=3)
+            ctx.scan_host(hbuf["a"], hbuf["b"], hbuf["u"], hbuf["s0"], out=hout, rows_per_chunk=1)
 
         n_e2e = max(3, min(args.steps, 20))
         for _ in range(2):
@@ -989,7 +989,7 @@ def run_ours(args):
         bound_ms = max(h2d, d2h) / (link["concurrent_each_GBps"] * 1e6)
         e2e = {"value": round(whole_job_gbps(step_bytes, 1, world, e2e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-               "api": "Context.scan_host (3 streams, one batch row per chunk)",
+               "api": "sn_scan_host (C ABI, host buffers; 3 pipeline streams, one batch row per chunk)",
                "link": link, "link_bound_ms_per_step": round(bound_ms, 3),
                "link_frac": round(bound_ms / e2e_ms, 3)}
         del hbuf, hout

@@ -219,6 +219,39 @@ sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N,
                         const float* a, const float* u, const float* s0,
                         float* s_final, float* s_out, void* stream);
 
+/* Device staging bytes sn_scan_host needs: forms_mask 1 (FMA), 2 (gated) or
+ * 3 (both); three slots of rows = min(rows_per_chunk, B) batch rows, each
+ * slot r256(rows T N 4) + r256(rows N 4) + forms * (2 r256(rows T N 4) +
+ * r256(rows N 4)) bytes with r256 rounding up to a multiple of 256.  -1 on
+ * invalid arguments. */
+int64_t sn_scan_host_staging_bytes(int32_t B, int32_t T, int32_t N, int32_t forms_mask, int32_t rows_per_chunk);
+
+/* Both scan forms over HOST buffers, the transfers part of the call
+ * ([P1] §2.1 forms; §2.4, the call overhead that a batch-wide call must
+ * amortise).  a, b, u, s0 (host, same shapes as sn_scan_fma / sn_scan_gated;
+ * b = NULL skips the FMA form, u = NULL the gated form, at least one given;
+ * s0 NULL = zeros) are copied to the device in chunks of rows_per_chunk batch
+ * rows, scanned there, and each given output (s_out_*: (B, T, N), s_final_*:
+ * (B, N), host, may be NULL) is copied back.  Three chunks are in flight at
+ * once on the context's three pipeline streams (the host-to-device copy of
+ * one, the kernels of another and the device-to-host copy of a third
+ * overlap), each chunk in its own slot of `staging` (caller-owned device
+ * memory, 256-byte aligned, at least sn_scan_host_staging_bytes bytes).
+ * Every chunk runs the sequential kernel, so the results have the bits of
+ * sn_scan_fma / sn_scan_gated with that kernel (the fp32 definition's) and
+ * no context workspace is used.  The call is asynchronous: the pipeline
+ * starts after the earlier work on `stream`, and `stream` waits for all of
+ * it, so synchronise `stream` before reading the outputs.  Pinned host
+ * memory lets the copies overlap; pageable memory works, slower.  One call
+ * at a time per context (the pipeline streams are the context's).
+ * Outputs may not overlap any other buffer.  Errors: SN_E_INVAL (NULL a,
+ * neither b nor u, dims, alignment, overlap, staging too small or not
+ * 256-byte aligned), SN_E_DEVICE. */
+sn_status sn_scan_host(SnCtx* ctx, int32_t B, int32_t T, int32_t N, int32_t rows_per_chunk,
+                       const float* a, const float* b, const float* u, const float* s0,
+                       float* s_out_fma, float* s_final_fma, float* s_out_gated, float* s_final_gated,
+                       void* staging, int64_t staging_bytes, void* stream);
+
 /* Reverse (adjoint) scan of the FMA form: the backward pass of sn_scan_fma
  * (the pages' kernels pair a forward scan with a reverse scan, [P1] §8).
  * Given the forward states and gs_t = dL/ds_t, gf = dL/ds_final:

@@ -104,20 +104,16 @@ class Context:
         _check(_abi.sn_scan_gated(self.handle, B, T, N, a, u, s0, sf, so, stream), "sn_scan_gated")
         return so, sf
 
-    def scan_host(self, a, b=None, u=None, s0=None, *, out=None, rows_per_chunk=1, nstreams=3):
-        """Scan host (CPU, ideally pinned) tensors through the GPU.
-
-        Runs the FMA form when ``b`` is given and the gated form when ``u`` is
-        given, sharing the upload of ``a``.  Batch rows are independent, so
-        they stream through the device in chunks of ``rows_per_chunk`` on
-        ``nstreams`` rotating streams: the host-to-device copy of one chunk,
-        the kernels of another and the device-to-host copy of a third
-        overlap.  Returns ``{"fma": (s_out, s_final), "gated": (...)}`` as
-        CPU tensors, filled once the call returns; pass ``out`` (the same
+    def scan_host(self, a, b=None, u=None, s0=None, *, out=None, rows_per_chunk=1):
+        """Scan host (CPU, ideally pinned) tensors through the GPU with
+        ``sn_scan_host``: the FMA form when ``b`` is given, the gated form when
+        ``u`` is given, sharing the upload of ``a``; batch rows stream through
+        the device in chunks of ``rows_per_chunk`` on the context's three
+        pipeline streams.  Returns ``{"fma": (s_out, s_final), "gated": (...)}``
+        as CPU tensors, filled once the call returns; pass ``out`` (the same
         dict shape, pinned tensors) to reuse buffers across calls."""
         torch = self._torch
         B, T, N = a.shape
-        dev = torch.device(f"cuda:{self.device}")
         forms = [f for f, x in (("fma", b), ("gated", u)) if x is not None]
         if not forms:
             raise ValueError("give b (FMA form), u (gated form) or both")
@@ -125,39 +121,17 @@ class Context:
         for f in forms:
             if f not in outs:
                 outs[f] = (torch.empty((B, T, N), pin_memory=True), torch.empty((B, N), pin_memory=True))
-        R = max(1, min(rows_per_chunk, B))
-        streams = [torch.cuda.Stream(dev) for _ in range(nstreams)]
-        bufs = []
-        for _ in range(nstreams):
-            d = {"a": torch.empty((R, T, N), device=dev), "s0": torch.empty((R, N), device=dev)}
-            for f in forms:
-                d[f] = torch.empty((R, T, N), device=dev)             # b or u
-                d[f + "_out"] = torch.empty((R, T, N), device=dev)
-                d[f + "_fin"] = torch.empty((R, N), device=dev)
-            bufs.append(d)
-        rhs = {"fma": b, "gated": u}
-        prev = torch.cuda.current_stream(dev)
-        start = torch.cuda.Event()
-        start.record(prev)
-        for ci, b0 in enumerate(range(0, B, R)):
-            r = min(R, B - b0)
-            st, d = streams[ci % nstreams], bufs[ci % nstreams]
-            st.wait_event(start)
-            with torch.cuda.stream(st):
-                d["a"][:r].copy_(a[b0:b0 + r], non_blocking=True)
-                s0d = None
-                if s0 is not None:
-                    d["s0"][:r].copy_(s0[b0:b0 + r], non_blocking=True)
-                    s0d = d["s0"][:r]
-                for f in forms:
-                    d[f][:r].copy_(rhs[f][b0:b0 + r], non_blocking=True)
-                    fn = _abi.sn_scan_fma if f == "fma" else _abi.sn_scan_gated
-                    _check(fn(self.handle, r, T, N, d["a"][:r], d[f][:r], s0d, d[f + "_fin"][:r], d[f + "_out"][:r],
-                              st), f"sn_scan_{f}")
-                    outs[f][0][b0:b0 + r].copy_(d[f + "_out"][:r], non_blocking=True)
-                    outs[f][1][b0:b0 + r].copy_(d[f + "_fin"][:r], non_blocking=True)
-        for st in streams:
-            st.synchronize()
+        mask = (1 if b is not None else 0) | (2 if u is not None else 0)
+        need = _abi.sn_scan_host_staging_bytes(B, T, N, mask, rows_per_chunk)
+        if need < 0:
+            raise ValueError("invalid dimensions for sn_scan_host")
+        if getattr(self, "_staging", None) is None or self._staging.numel() < need:
+            self._staging = torch.empty(max(need, 256), dtype=torch.uint8, device=f"cuda:{self.device}")
+        fo, go = outs.get("fma", (None, None)), outs.get("gated", (None, None))
+        stream = torch.cuda.current_stream(torch.device(f"cuda:{self.device}"))
+        _check(_abi.sn_scan_host(self.handle, B, T, N, rows_per_chunk, a, b, u, s0, fo[0], fo[1], go[0], go[1],
+                                 self._staging, self._staging.numel(), stream), "sn_scan_host")
+        stream.synchronize()
         return outs
 
     def scan_backward(self, form, a, s, grad_s, *, s0=None, grad_final=None, u=None, stream=None):

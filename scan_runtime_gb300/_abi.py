@@ -39,6 +39,7 @@ EXPORTS = (
     "sn_ctx_last_error", "sn_ctx_set_option", "sn_ctx_get_option",
     "sn_scan_fma", "sn_scan_gated", "sn_scan_fma_backward", "sn_scan_gated_backward",
     "sn_recur_diag", "sn_recur_delta", "sn_recur_rwkv7", "sn_scan_lookback_noalloc",
+    "sn_scan_host_staging_bytes", "sn_scan_host",
     "sn_recur_diag_chunked", "sn_recur_chunked_workspace_bytes", "sn_readout_norm_gate", "sn_readout_dskip",
     "sn_recur_delta_chunked", "sn_recur_delta_chunked_workspace_bytes",
 )
@@ -79,6 +80,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "sn_recur_delta": ([p, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_rwkv7": ([p, i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p], i32),
             "sn_scan_lookback_noalloc": ([i32, i32, i32, i32, p, p, p, p, p, p, p], i32),
+            "sn_scan_host_staging_bytes": ([i32, i32, i32, i32, i32], i64),
+            "sn_scan_host": ([p, i32, i32, i32, i32] + [p] * 9 + [i64, p], i32),
             "sn_recur_diag_chunked": ([p, i32, i32, i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p], i32),
             "sn_recur_chunked_workspace_bytes": ([i32, i32, i32, i32, i32], i64),
             "sn_readout_norm_gate": ([p, i32, i32, i32, i32, p, p, p, f32, p, p], i32),
@@ -95,7 +98,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 
 
 def ptr(x) -> int | None:
-    """Device pointer of a tensor (or an int address); None stays NULL."""
+    """Address of a tensor's data (device or host) or an int address; None stays NULL."""
     if x is None:
         return None
     if isinstance(x, int):
@@ -208,6 +211,17 @@ def sn_recur_rwkv7(ctx, B, T, H, dk, dv, q, k, v, w, S_in, S_out, o, stream=None
 def sn_scan_lookback_noalloc(gated, B, T, N, a, b, s0, s_final, s_out, status_out=None, stream=None) -> int:
     return load().sn_scan_lookback_noalloc(gated, B, T, N, ptr(a), ptr(b), ptr(s0), ptr(s_final), ptr(s_out),
                                            ptr(status_out), stream_handle(stream))
+
+
+def sn_scan_host_staging_bytes(B, T, N, forms_mask, rows_per_chunk) -> int:
+    return load().sn_scan_host_staging_bytes(B, T, N, forms_mask, rows_per_chunk)
+
+
+def sn_scan_host(ctx, B, T, N, rows_per_chunk, a, b, u, s0, s_out_fma, s_final_fma, s_out_gated, s_final_gated,
+                 staging, staging_bytes, stream=None) -> int:
+    return load().sn_scan_host(ctx, B, T, N, rows_per_chunk, ptr(a), ptr(b), ptr(u), ptr(s0), ptr(s_out_fma),
+                               ptr(s_final_fma), ptr(s_out_gated), ptr(s_final_gated), ptr(staging), staging_bytes,
+                               stream_handle(stream))
 
 
 def sn_recur_diag_chunked(ctx, B, T, H, G, dk, dv, decay_kind, scale, q, k, v, d, S_in, S_out, o,

@@ -426,6 +426,104 @@ sn_status sn_scan_gated(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const float
     return scan_common(ctx, B, T, N, a, u, s0, s_final, s_out, stream, true);
 }
 
+// ------------------------------------------------------------------ host buffers
+// Device staging of sn_scan_host: SN_HOST_SLOTS slots, each holding one chunk
+// of `rows` batch rows: a, s0, then per form its input, states and final
+// states, every part rounded up to 256 bytes.
+namespace {
+constexpr int SN_HOST_SLOTS = 3;
+int64_t r256(int64_t x) { return (x + 255) / 256 * 256; }
+int64_t host_slot_bytes(int64_t rows, int64_t T, int64_t N, int forms) {
+    const int64_t big = r256(rows * T * N * 4), small = r256(rows * N * 4);
+    return big + small + forms * (2 * big + small);
+}
+}  // namespace
+
+int64_t sn_scan_host_staging_bytes(int32_t B, int32_t T, int32_t N, int32_t forms_mask, int32_t rows_per_chunk) {
+    if (!within_elems({B, T, N}) || forms_mask < 1 || forms_mask > 3 || rows_per_chunk < 1) return -1;
+    const int forms = (forms_mask & 1) + ((forms_mask >> 1) & 1);
+    const int64_t rows = std::min<int64_t>(rows_per_chunk, B);
+    return SN_HOST_SLOTS * host_slot_bytes(rows, T, N, forms);
+}
+
+sn_status sn_scan_host(SnCtx* ctx, int32_t B, int32_t T, int32_t N, int32_t rows_per_chunk, const float* a,
+                       const float* b, const float* u, const float* s0, float* s_out_fma, float* s_final_fma,
+                       float* s_out_gated, float* s_final_gated, void* staging, int64_t staging_bytes,
+                       void* stream) {
+    if (ctx == nullptr || a == nullptr || (b == nullptr && u == nullptr) || staging == nullptr) return SN_E_INVAL;
+    if (B <= 0 || T <= 0 || N <= 0 || rows_per_chunk < 1 || !within_elems({B, T, N})) return SN_E_INVAL;
+    const int mask = (b != nullptr ? 1 : 0) | (u != nullptr ? 2 : 0);
+    if (staging_bytes < sn_scan_host_staging_bytes(B, T, N, mask, rows_per_chunk) || !aligned(staging, 256))
+        return SN_E_INVAL;
+    const void* ptrs[9] = {a, b, u, s0, s_out_fma, s_final_fma, s_out_gated, s_final_gated, staging};
+    for (const void* p : ptrs)
+        if (p != nullptr && !aligned(p, 4)) return SN_E_INVAL;
+    const int64_t big = (int64_t)B * T * N * 4, small = (int64_t)B * N * 4;
+    const Buf bufs[8] = {{a, big, false},          {b, big, false},           {u, big, false},
+                         {s0, small, false},       {s_out_fma, big, true},    {s_final_fma, small, true},
+                         {s_out_gated, big, true}, {s_final_gated, small, true}};
+    if (any_bad_overlap(bufs, 8, nullptr, nullptr)) return SN_E_INVAL;
+    if (!ctx->pipe_ready) return SN_E_DEVICE;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SN_E_DEVICE;
+
+    const int64_t R = std::min<int64_t>(rows_per_chunk, B);
+    const int forms = (mask & 1) + ((mask >> 1) & 1);
+    const int64_t slot_bytes = host_slot_bytes(R, T, N, forms);
+    const int64_t bigR = r256(R * T * N * 4), smallR = r256(R * N * 4);
+    cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t st[SN_HOST_SLOTS] = {ctx->pipe_prep, ctx->pipe_chain, ctx->pipe_out};
+    cudaEvent_t fork = ctx->pipe_ev[0];
+    // the pipeline starts after the caller's earlier work on `stream`
+    if (cudaEventRecord(fork, caller) != cudaSuccess) return SN_E_DEVICE;
+    for (int i = 0; i < SN_HOST_SLOTS; ++i)
+        if (cudaStreamWaitEvent(st[i], fork, 0) != cudaSuccess) return SN_E_DEVICE;
+    const float* rhs[2] = {b, u};
+    float* outs[2] = {s_out_fma, s_out_gated};
+    float* fins[2] = {s_final_fma, s_final_gated};
+    auto h2d = [](void* d, const void* h, int64_t n, cudaStream_t s) {
+        return cudaMemcpyAsync(d, h, (size_t)n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    };
+    auto d2h = [](void* h, const void* d, int64_t n, cudaStream_t s) {
+        return cudaMemcpyAsync(h, d, (size_t)n, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+    };
+    // chunk ci on stream ci mod 3, in slot ci mod 3: the slot's previous chunk
+    // (same stream) has been copied out before this one's copies land
+    int ci = 0;
+    for (int64_t b0 = 0; b0 < B; b0 += R, ++ci) {
+        const int64_t r = std::min<int64_t>(R, B - b0);
+        cudaStream_t s = st[ci % SN_HOST_SLOTS];
+        char* slot = static_cast<char*>(staging) + (ci % SN_HOST_SLOTS) * slot_bytes;
+        float* da = reinterpret_cast<float*>(slot);
+        float* ds0 = reinterpret_cast<float*>(slot + bigR);
+        const int64_t rb = r * T * N * 4, rs = r * N * 4;
+        if (!h2d(da, a + b0 * T * N, rb, s)) return SN_E_DEVICE;
+        if (s0 != nullptr && !h2d(ds0, s0 + b0 * N, rs, s)) return SN_E_DEVICE;
+        char* p = slot + bigR + smallR;
+        for (int f = 0; f < 2; ++f) {
+            if (rhs[f] == nullptr) continue;
+            float* din = reinterpret_cast<float*>(p);
+            float* dout = reinterpret_cast<float*>(p + bigR);
+            float* dfin = reinterpret_cast<float*>(p + 2 * bigR);
+            p += 2 * bigR + smallR;
+            if (!h2d(din, rhs[f] + b0 * T * N, rb, s)) return SN_E_DEVICE;
+            // the sequential kernel: exact per-step bits, no workspace (chunks
+            // in flight on different streams never share one)
+            ScanArgs x{(int)r, T, N, da, din, s0 != nullptr ? ds0 : nullptr, dfin, dout};
+            if (launch_scan_sequential(x, f == 1, ctx->dstatus, wait_ns(ctx), s) != cudaSuccess) return SN_E_DEVICE;
+            if (outs[f] != nullptr && !d2h(outs[f] + b0 * T * N, dout, rb, s)) return SN_E_DEVICE;
+            if (fins[f] != nullptr && !d2h(fins[f] + b0 * N, dfin, rs, s)) return SN_E_DEVICE;
+        }
+    }
+    // the caller's later work on `stream` waits for every chunk
+    for (int i = 0; i < SN_HOST_SLOTS; ++i) {
+        if (cudaEventRecord(ctx->pipe_ev[1 + i], st[i]) != cudaSuccess ||
+            cudaStreamWaitEvent(caller, ctx->pipe_ev[1 + i], 0) != cudaSuccess)
+            return SN_E_DEVICE;
+    }
+    return SN_OK;
+}
+
 // ------------------------------------------------------------------ reverse scans
 static sn_status scan_backward_common(SnCtx* ctx, BwdArgs& x, bool gated, void* stream) {
     if (ctx == nullptr || x.a == nullptr || x.s == nullptr || x.gs == nullptr || (gated && x.u == nullptr))

@@ -258,6 +258,197 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, DKC);
 }
 
+// ------------------------------------------------------------------ chunk_state_key
+// chunk_state for per-key decays with its tiles by TMA: k, d and v arrive as
+// natural [token][feature] boxes (128 tokens x 128 or dv features, rows past
+// T filled with zeros), three copies instead of 4-byte transposing copies.
+// The threads transpose while they compute: thread (key i, half of the
+// tokens) reads its column of k and d (consecutive keys, conflict-free),
+// takes log2 d in place, forms Khat in registers, and after a barrier writes
+// it in the operand layout over k; v goes the same way (rounded to tf32)
+// over its own box.  The product's dS^T leaves tensor memory for shared
+// memory (over the consumed decays) and goes out by one bulk copy.  The
+// arithmetic and its order are chunk_state's, so are the results.
+template <int DV>
+struct StateKeySmem {
+    static constexpr int k_off = 0;                    // k [t][i], then Khat^T (rows i, K = t)
+    static constexpr int d_off = OPF;                  // d [t][i] (log2 d in place), then dS^T
+    static constexpr int v_off = 2 * OPF;              // v [t][j], then v^T (rows j, K = t)
+    static constexpr int tot_off = v_off + DV * CH;    // [2][DKC] half sums, [2][2][DKC] extremes
+    static constexpr int misc_off = tot_off + 6 * DKC; // barriers (k and d, v, product), tmem slot
+    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+    static_assert(DV * DKC <= OPF, "dS^T fits over the decays");
+};
+
+template <int DV>
+__global__ void __launch_bounds__(NT, 1)
+chunk_state_key(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_d,
+                const __grid_constant__ CUtensorMap map_v, const ChunkArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    using L = StateKeySmem<DV>;
+    float* base = align128(smem_raw);
+    float* Kn = base + L::k_off;
+    float* Dn = base + L::d_off;
+    float* Vn = base + L::v_off;
+    float* tot = base + L::tot_off;
+    float* ext = tot + 2 * DKC;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::misc_off);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 6);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const ChunkIdx c = chunk_index(a);
+    if (warp == 0) tc::tmem_alloc(slot, DKC);
+    if (tid == 0) {
+        for (int q = 0; q < 3; ++q) mbar_init(&bars[q], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bars[0], 2 * OPF * 4);
+        tma_load_3d(Kn, &map_k, &bars[0], c.g * DKC, c.t0, c.b);
+        tma_load_3d(Dn, &map_d, &bars[0], c.h * DKC, c.t0, c.b);
+        mbar_arrive_expect_tx(&bars[1], DV * CH * 4);
+        tma_load_3d(Vn, &map_v, &bars[1], c.h * DV, c.t0, c.b);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+
+    const int i = tid & (DKC - 1), half = tid >> 7;
+    const int tbeg = (CH / 2) * half;
+    bool ok = __syncthreads_and(mbar_wait(&bars[0], 0, a.wait_ns));
+    int site = SITE_STATE_WAIT;
+    float gam = 1.f, anc = 1.f;
+    if (ok) {
+        // log2 of the decays in place; gated keys take the weight 1 - d
+        float sum = 0.f;
+#pragma unroll 4
+        for (int t4 = 0; t4 < CH / 8; ++t4) {
+            const int tb = tbeg + 4 * t4;
+            float lg[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int o = (tb + r) * DKC + i;
+                const float dd = Dn[o];
+                lg[r] = tb + r < c.nval ? lg2(dd) : 0.f;
+                Dn[o] = lg[r];
+                if (a.gated) Kn[o] = Kn[o] * (1.f - dd);
+            }
+            sum += (lg[0] + lg[1]) + (lg[2] + lg[3]);
+        }
+        tot[half * DKC + i] = sum;
+        __syncthreads();
+        // Khat_t = k_t 2^{m_t}, m_t the log2 decay of the tokens after t
+        float m = half == 0 ? tot[DKC + i] : 0.f;
+        float mhi = -INFINITY, mlo = INFINITY;
+        float kh[CH / 2];
+#pragma unroll
+        for (int t4 = CH / 8 - 1; t4 >= 0; --t4) {
+            const int tb = tbeg + 4 * t4;
+#pragma unroll
+            for (int r = 3; r >= 0; --r) {
+                const int o = (tb + r) * DKC + i;
+                kh[4 * t4 + r] = Kn[o] * ex2(m);
+                mhi = fmaxf(mhi, m);
+                mlo = fminf(mlo, m);
+                m += Dn[o];
+            }
+        }
+        gam = ex2(m);                       // half 0: the whole chunk's log2 decay
+        ext[(half * 2 + 0) * DKC + i] = mhi;
+        ext[(half * 2 + 1) * DKC + i] = mlo;
+        __syncthreads();                    // k and d are read: Khat^T goes over k
+#pragma unroll
+        for (int t4 = 0; t4 < CH / 8; ++t4)
+            st4(Kn + off128(i, tbeg + 4 * t4),
+                tf32x4(kh[4 * t4], kh[4 * t4 + 1], kh[4 * t4 + 2], kh[4 * t4 + 3]));
+        // the range test of chunk_state (flagged chunks run step by step in the output stage)
+        bool wide = false;
+        if (half == 0) {
+            const float mm = tot[DKC + i];
+            const float hi2 = fmaxf(mhi, ext[(2 + 0) * DKC + i]), lo2 = fminf(mlo, ext[(2 + 1) * DKC + i]);
+            if (!isfinite(tot[i]) || !isfinite(mm))
+                record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_KEY);
+            wide = !(hi2 - mm <= RANGE_LOG2 && mm - lo2 <= RANGE_LOG2);
+        }
+        const bool flagged = __syncthreads_or(wide);
+        if (tid == 0) a.bad[c.bh * a.NC + c.n] = flagged ? 1 : 0;
+        anc = flagged ? -1.f : ex2(tot[i]); // 2^{lam at the anchor token C/2 - 1}; -1 marks the flag
+        if (half == 0) {
+            const size_t gi = (c.bh * a.NC + c.n) * DKC + i;
+            a.gam[gi] = gam;
+            a.anc[gi] = anc;
+        }
+    }
+    if (ok) {
+        // v^T rounded, over v: thread = value column j, a run of TPV tokens
+        ok = __syncthreads_and(mbar_wait(&bars[1], 0, a.wait_ns));
+        if (ok) {
+            constexpr int TPV = CH * DV / NT;
+            const int j = tid % DV, t0 = (tid / DV) * TPV;
+            float vv[TPV];
+#pragma unroll
+            for (int r = 0; r < TPV; ++r) vv[r] = Vn[(t0 + r) * DV + j];
+            __syncthreads();
+#pragma unroll
+            for (int t4 = 0; t4 < TPV / 4; ++t4)
+                st4(Vn + off128(j, t0 + 4 * t4), tf32x4(vv[4 * t4], vv[4 * t4 + 1], vv[4 * t4 + 2], vv[4 * t4 + 3]));
+        }
+    }
+    if (ok) {
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            // dS^T (M = dv rows c, N = dk columns i) = v^T (K = t) x Khat^T (K = t)
+            tc::gemm_tf32(tmem, Vn, Kn, CH, tc::idesc_tf32(DV, DKC), false);
+            tc::commit(&bars[2]);
+            if (a.vt_out != nullptr) {   // the output stage's v operand
+                bulk_store(a.vt_out + (c.bh * a.NC + c.n) * (size_t)DV * CH, Vn, DV * CH * 4);
+                bulk_commit();
+            }
+        }
+        ok = __syncthreads_and(mbar_wait(&bars[2], 0, a.wait_ns));
+        tc::fence_after_sync();
+        if (ok) {
+            // M = 128: row c in lane c.  M = 64: rows 16q..16q+15 in lanes 32q..32q+15.
+            const int lq = warp & 3, ih = warp >> 2;
+            const int row = DV == 128 ? 32 * lq + lane : 16 * lq + (lane & 15);
+            const bool mine = DV == 128 || lane < 16;
+#pragma unroll
+            for (int i0 = 64 * ih; i0 < 64 * ih + 64; i0 += 16) {
+                float x[16];
+                tc::ld16(tmem + ((uint32_t)(32 * lq) << 16) + i0, x);
+                if (mine) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st4(Dn + off128(row, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_store(a.W + (c.bh * a.NC + c.n) * (size_t)DV * DKC, Dn, DV * DKC * 4);
+                bulk_commit();
+            }
+        } else {
+            site = SITE_STATE_WAIT;
+        }
+    }
+    if (tid == 0) {
+        if (!ok) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
+            // the copies still in flight land before the CTA leaves
+            (void)mbar_wait(&bars[0], 0, a.wait_ns);
+            (void)mbar_wait(&bars[1], 0, a.wait_ns);
+        }
+        bulk_wait_all();   // the bulk copies out have read shared memory and landed
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, DKC);
+}
+
 // ------------------------------------------------------------------ chunk_state_heads
 // Per-head decays with heads sharing k (Mamba-2's groups): the token weight
 // 2^{mu_t} is a scalar per token, so it is applied to v instead of k,
@@ -1172,6 +1363,22 @@ bool make_qk_maps(const ChunkArgs& a, CUtensorMap* mq, CUtensorMap* mk) {
     return encode_tiled(mq, 3, a.q, dims, strides, box, true) && encode_tiled(mk, 3, a.k, dims, strides, box, true);
 }
 
+// TMA maps of k, d and v for chunk_state_key: (B, T, features) row-major,
+// boxes of 128 tokens x all of a head's features (k: 128 keys of the group,
+// d: 128 keys of the head, v: dv values of the head), no swizzle.
+template <int DV>
+bool make_natural_maps(const ChunkArgs& a, CUtensorMap* mk, CUtensorMap* md, CUtensorMap* mv) {
+    const uint64_t dk_[3] = {(uint64_t)a.G * DKC, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t sk_[2] = {(uint64_t)a.G * DKC * 4, (uint64_t)a.T * a.G * DKC * 4};
+    const uint64_t dd_[3] = {(uint64_t)a.H * DKC, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t sd_[2] = {(uint64_t)a.H * DKC * 4, (uint64_t)a.T * a.H * DKC * 4};
+    const uint64_t dv_[3] = {(uint64_t)a.H * DV, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t sv_[2] = {(uint64_t)a.H * DV * 4, (uint64_t)a.T * a.H * DV * 4};
+    const uint32_t bk[3] = {DKC, (uint32_t)CH, 1}, bv[3] = {DV, (uint32_t)CH, 1};
+    return encode_tiled(mk, 3, a.k, dk_, sk_, bk, false) && encode_tiled(md, 3, a.d, dd_, sd_, bk, false) &&
+           encode_tiled(mv, 3, a.v, dv_, sv_, bv, false);
+}
+
 template <bool PER_KEY, int DV>
 cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     constexpr bool HEADS = !PER_KEY && DV == 64;   // per-head decays: heads of a group share Q K^T
@@ -1181,6 +1388,9 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     if constexpr (HEADS) {
         st_bytes = StateHeadsSmem<DV>::bytes;
         e = set_smem_attr_once((const void*)chunk_state_heads<DV>, st_bytes);
+    } else if constexpr (PER_KEY) {
+        st_bytes = StateKeySmem<DV>::bytes;
+        e = set_smem_attr_once((const void*)chunk_state_key<DV>, st_bytes);
     } else {
         st_bytes = StateSmem<PER_KEY, DV>::bytes;
         e = set_smem_attr_once((const void*)chunk_state<PER_KEY, DV>, st_bytes);
@@ -1198,6 +1408,10 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     if constexpr (HEADS) {
         const int hb = heads_per_cta(a, sm_count);
         chunk_state_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, st_bytes, s>>>(a, hb);
+    } else if constexpr (PER_KEY) {
+        CUtensorMap mk, md, mv;
+        if (!make_natural_maps<DV>(a, &mk, &md, &mv)) return cudaErrorInvalidValue;
+        chunk_state_key<DV><<<chunks, NT, st_bytes, s>>>(mk, md, mv, a);
     } else {
         chunk_state<PER_KEY, DV><<<chunks, NT, st_bytes, s>>>(a);
     }

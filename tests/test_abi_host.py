@@ -154,6 +154,19 @@ def test_workspace_bytes(abi):
     assert abi.sn_recur_delta_chunked_workspace_bytes(big, big, 1, 128, 128) == -1
 
 
+def test_scan_host_staging_bytes(abi):
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B, T, N, mask, rows in ((8, 8192, 2048, 3, 1), (5, 300, 192, 1, 2), (3, 7, 5, 2, 9)):
+        forms = (mask & 1) + ((mask >> 1) & 1)
+        r = min(rows, B)
+        slot = r256(r * T * N * 4) + r256(r * N * 4) + forms * (2 * r256(r * T * N * 4) + r256(r * N * 4))
+        assert abi.sn_scan_host_staging_bytes(B, T, N, mask, rows) == 3 * slot
+    assert abi.sn_scan_host_staging_bytes(1, 1, 1, 0, 1) == -1
+    assert abi.sn_scan_host_staging_bytes(1, 1, 1, 4, 1) == -1
+    assert abi.sn_scan_host_staging_bytes(1, 1, 1, 1, 0) == -1
+    assert abi.sn_scan_host_staging_bytes(2 ** 31 - 1, 2 ** 31 - 1, 2 ** 31 - 1, 1, 1) == -1
+
+
 def test_chunked_workspace_bytes(abi):
     r256 = lambda x: (x + 255) // 256 * 256
     for B, T, H, dv in ((4, 4096, 4, 128), (1, 300, 3, 64), (2, 1, 1, 128)):

@@ -497,3 +497,28 @@ def test_scan_host_pipeline_matches_device_path(ctx):
     only = ctx.scan_host(a, u=u, s0=None)
     r32, _ = _ref("gated", a, u, None, "f32")
     assert set(only) == {"gated"} and np.array_equal(only["gated"][0].numpy(), r32)
+
+
+def test_scan_host_rejects_bad_arguments_before_any_transfer(sr, ctx):
+    """sn_scan_host checks its arguments on the host: no form, a staging
+    buffer smaller than the query or not 256-byte aligned, an output that
+    overlaps an input."""
+    B, T, N = 3, 64, 32
+    a, b, u, s0 = _inputs(B, T, N, 13)
+    so = torch.zeros((B, T, N))
+    sf = torch.zeros((B, N))
+    need = sr.sn_scan_host_staging_bytes(B, T, N, 1, 1)
+    need2 = sr.sn_scan_host_staging_bytes(B, T, N, 1, 2)
+    stg = torch.empty(max(need, need2) + 512, dtype=torch.uint8, device="cuda")
+    h = ctx.handle
+    assert sr.sn_scan_host(h, B, T, N, 1, a, None, None, s0, so, sf, None, None, stg, need) == sr.SN_E_INVAL
+    assert sr.sn_scan_host(h, B, T, N, 1, a, b, None, s0, so, sf, None, None, stg, need - 1) == sr.SN_E_INVAL
+    assert sr.sn_scan_host(h, B, T, N, 1, a, b, None, s0, so, sf, None, None, stg[16:], need) == sr.SN_E_INVAL
+    assert sr.sn_scan_host(h, B, T, N, 1, a, b, None, s0, a, sf, None, None, stg, need) == sr.SN_E_INVAL
+    assert torch.count_nonzero(so) == 0 and torch.count_nonzero(sf) == 0
+    # and a valid call on the caller's stream, pageable buffers, ragged last chunk
+    s = torch.cuda.Stream()
+    assert sr.sn_scan_host(h, B, T, N, 2, a, b, None, s0, so, sf, None, None, stg, need2, s) == sr.SN_OK
+    s.synchronize()
+    ref_so, ref_sf = _run(ctx, "fma", a, b, s0)
+    assert np.array_equal(so.numpy(), ref_so) and np.array_equal(sf.numpy(), ref_sf)
