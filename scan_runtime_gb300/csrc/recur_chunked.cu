@@ -27,8 +27,10 @@
 // Qt = q 2^{lam_t - lam_m}, Kt = k 2^{lam_m - lam_j}, S' = diag(2^{lam_m}) S_n
 // and f_t = 1.  Those factors stay within 2^{+-60} as long as the decay
 // product between any token of the chunk and the anchor is at least 2^-60 (and
-// every decay is positive); a launch that sees a chunk outside that range
-// records SN_E_RANGE.  Per-head decays are scalars per token, so Qt = q, Kt =
+// every decay is positive); a chunk outside that range is flagged by the
+// state kernel and its outputs are evaluated step by step in fp32 by the
+// output kernel instead (a decay <= 0 records SN_E_RANGE).  Per-head decays
+// are scalars per token, so Qt = q, Kt =
 // k, S' = S_n, the exact weight 2^{lam_t - lam_j} multiplies A after the
 // product and f_t = 2^{lam_t}; they only need positive decays.
 //
@@ -37,13 +39,15 @@
 // instead of the sequence kernel's exact per-step fp32 arithmetic.
 //
 // Data movement: every tile a CTA needs is requested before any of it is
-// used.  Tiles whose layout matches the operand (q, k rows) arrive by 16-byte
-// cp.async straight into the operand layout; tiles that must be transposed
-// (k, d and v in chunk_state, the v slice of chunk_output) arrive by 4-byte
-// cp.async or plain loads, with lanes covering 8 operand rows x 4 tokens so
-// the scattered shared-memory writes are conflict-free; the chunk's S'
-// operand is one contiguous bulk copy, because chunk_state and chunk_carry
-// keep the chunk states in the operand layout.
+// used.  q and k of the output stage arrive by TMA in the 128-byte-swizzled
+// operand layout.  The per-key state kernel takes k, d and v by TMA as
+// natural [token][feature] tiles and transposes them in shared memory while
+// it computes; it also leaves its rounded v^T tile for the output stage,
+// which takes it by one bulk copy.  The per-head kernels transpose k and v
+// with 4-byte cp.async (lanes covering 8 operand rows x 4 tokens, so the
+// scattered shared-memory writes are conflict-free).  The chunk's S' operand
+// is one contiguous bulk copy, because the state kernels and chunk_carry keep
+// the chunk states in the operand layout.
 //
 // Shared-memory operands use the K-major no-swizzle core-matrix layout of
 // tc.cuh with K extent 128 (every contraction here has K = 128: keys, or the
@@ -56,27 +60,25 @@ namespace {
 using namespace chunk;
 
 // ------------------------------------------------------------------ chunk_state
-template <bool PER_KEY, int DV>
+// Per-head decays (one CTA per chunk and head; chunk_state_key below takes the
+// per-key decays, chunk_state_heads the heads of a group that share k).
+template <int DV>
 struct StateSmem {
     static constexpr int k_off = 0;                                   // k^T, then Khat^T: rows i, K = t
-    static constexpr int d_off = OPF;                                 // d^T (per key): rows i, K = t
-    static constexpr int v_off = d_off + (PER_KEY ? OPF : 0);         // v^T: rows c, K = t
-    static constexpr int tot_off = v_off + DV * CH;                   // [2][DKC] half sums
-    static constexpr int mu_off = tot_off + 2 * DKC;                  // [CH] suffix sums (per head)
-    static constexpr int om_off = mu_off + CH;                        // [CH] injection weights (per head)
+    static constexpr int v_off = OPF;                                 // v^T: rows c, K = t
+    static constexpr int mu_off = v_off + DV * CH;                    // [CH] suffix sums
+    static constexpr int om_off = mu_off + CH;                        // [CH] injection weights
     static constexpr int misc_off = om_off + CH;                      // total, barrier, tmem slot
     static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
 };
 
-template <bool PER_KEY, int DV>
+template <int DV>
 __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
-    using L = StateSmem<PER_KEY, DV>;
+    using L = StateSmem<DV>;
     float* base = align128(smem_raw);
     float* Ks = base + L::k_off;
-    float* Ds = base + L::d_off;
     float* Vs = base + L::v_off;
-    float* tot = base + L::tot_off;
     float* mu = base + L::mu_off;
     float* om = base + L::om_off;
     float* total_s = base + L::misc_off;
@@ -92,14 +94,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
         fence_mbar_init();
     }
 
-    const size_t krs = (size_t)a.G * DKC, drs = (size_t)a.H * DKC, vrs = (size_t)a.H * DV;
+    const size_t krs = (size_t)a.G * DKC, vrs = (size_t)a.H * DV;
     const size_t row0 = (size_t)c.b * a.T + c.t0;
     copy_transposed<DKC>(Ks, a.k + row0 * krs + (size_t)c.g * DKC, krs, c.nval, warp, lane);
-    if (PER_KEY) copy_transposed<DKC>(Ds, a.d + row0 * drs + (size_t)c.h * DKC, drs, c.nval, warp, lane);
     copy_transposed<DV>(Vs, a.v + row0 * vrs + (size_t)c.h * DV, vrs, c.nval, warp, lane);
     cp_async_commit();
 
-    if (!PER_KEY && warp == 0) {
+    if (warp == 0) {
         // exclusive suffix sums mu[t] = sum_{s > t} log2 d_s of the per-head decays
         float lg[4], s = 0.f;
 #pragma unroll
@@ -130,73 +131,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     cp_async_wait_all();
     __syncthreads();
 
-    // Khat^T in place: thread = key row i, half of the tokens
+    // Khat^T in place: thread = key row i, half of the tokens; the token
+    // weight 2^{mu_t} (times 1 - d_t when gated) is a scalar per token
     const int i = tid & (DKC - 1), half = tid >> 7;
     const int tbeg = (CH / 2) * half;
-    float gam, anc;
-    if (PER_KEY) {
-        // log2 of the decays, kept in place of the decays
-        float sum = 0.f;
-#pragma unroll 4
-        for (int t4 = 0; t4 < CH / 8; ++t4) {
-            const int tb = tbeg + 4 * t4;
-            const int o = off128(i, tb);
-            const float4 dd = ld4(Ds + o);
-            const float4 lg = make_float4(tb + 0 < c.nval ? lg2(dd.x) : 0.f, tb + 1 < c.nval ? lg2(dd.y) : 0.f,
-                                          tb + 2 < c.nval ? lg2(dd.z) : 0.f, tb + 3 < c.nval ? lg2(dd.w) : 0.f);
-            st4(Ds + o, lg);
-            if (a.gated) {   // the injection k_i v_j enters with weight 1 - d_i
-                const float4 kk = ld4(Ks + o);
-                st4(Ks + o, make_float4(kk.x * (1.f - dd.x), kk.y * (1.f - dd.y), kk.z * (1.f - dd.z),
-                                        kk.w * (1.f - dd.w)));
-            }
-            sum += (lg.x + lg.y) + (lg.z + lg.w);
-        }
-        tot[half * DKC + i] = sum;
-        __syncthreads();
-        float m = half == 0 ? tot[DKC + i] : 0.f;   // sum over the later tokens
-        // lam_t - lam_m = m_m - m_t with m_t the sum over the tokens after t
-        // (m_m = the second half's sum): the extremes of m_t bound the anchor
-        // factors of the output stage
-        float mhi = -INFINITY, mlo = INFINITY;
-#pragma unroll 4
-        for (int t4 = CH / 8 - 1; t4 >= 0; --t4) {
-            const int tb = tbeg + 4 * t4;
-            const int o = off128(i, tb);
-            const float4 dd = ld4(Ds + o), kk = ld4(Ks + o);
-            float out[4];
-            const float dv4[4] = {dd.x, dd.y, dd.z, dd.w}, kv4[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-            for (int r = 3; r >= 0; --r) {
-                out[r] = kv4[r] * ex2(m);
-                mhi = fmaxf(mhi, m);
-                mlo = fminf(mlo, m);
-                m += dv4[r];
-            }
-            st4(Ks + o, tf32x4(out[0], out[1], out[2], out[3]));
-        }
-        gam = ex2(m);                       // half 0: the whole chunk's log2 decay
-        // A key whose factors would leave 2^{+-RANGE_LOG2} flags the chunk: its
-        // outputs are then evaluated step by step (fix_unit), and its state
-        // operand is kept unscaled and unrounded (anchor -1 marks it).  A non-finite sum
-        // means a decay <= 0, which no evaluation here supports.
-        const float mm = tot[DKC + i];
-        float* ext = Ds;                    // the decays are consumed: [2][2][DKC] extremes
-        __syncthreads();
-        ext[(half * 2 + 0) * DKC + i] = mhi;
-        ext[(half * 2 + 1) * DKC + i] = mlo;
-        __syncthreads();
-        bool wide = false;
-        if (half == 0) {
-            const float hi2 = fmaxf(mhi, ext[(2 + 0) * DKC + i]), lo2 = fminf(mlo, ext[(2 + 1) * DKC + i]);
-            if (!isfinite(tot[i]) || !isfinite(mm)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_KEY);
-            wide = !(hi2 - mm <= RANGE_LOG2 && mm - lo2 <= RANGE_LOG2);
-        }
-        const bool flagged = __syncthreads_or(wide);
-        if (tid == 0) a.bad[c.bh * a.NC + c.n] = flagged ? 1 : 0;
-        anc = flagged ? -1.f : ex2(tot[i]); // 2^{lam at the anchor token C/2 - 1}; -1 marks the flag
-    } else {
-        const float total = total_s[0];
+    {
 #pragma unroll 4
         for (int t4 = 0; t4 < CH / 8; ++t4) {
             const int tb = tbeg + 4 * t4;
@@ -205,13 +144,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
             st4(Ks + o, tf32x4(kk.x * ex2(mu[tb]) * om[tb], kk.y * ex2(mu[tb + 1]) * om[tb + 1],
                                kk.z * ex2(mu[tb + 2]) * om[tb + 2], kk.w * ex2(mu[tb + 3]) * om[tb + 3]));
         }
-        gam = ex2(total);
-        anc = 1.f;
     }
     if (half == 0) {
         const size_t gi = (c.bh * a.NC + c.n) * DKC + i;
-        a.gam[gi] = gam;
-        a.anc[gi] = anc;
+        a.gam[gi] = ex2(total_s[0]);
+        a.anc[gi] = 1.f;
     }
     // v^T rounded in place
     for (int f = tid; f < DV * CH / 4; f += NT) st4(Vs + 4 * f, tf32x4(ld4(Vs + 4 * f)));
@@ -225,11 +162,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
         // dS^T (M = dv rows c, N = dk columns i) = v^T (K = t) x Khat^T (K = t)
         tc::gemm_tf32(tmem, Vs, Ks, CH, tc::idesc_tf32(DV, DKC), false);
         tc::commit(bar);
-        // the same v^T tile is the output stage's operand: one bulk copy out
-        if (a.vt_out != nullptr) {
-            bulk_store(a.vt_out + (c.bh * a.NC + c.n) * (size_t)DV * CH, Vs, DV * CH * 4);
-            bulk_commit();
-        }
     }
     const bool ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
     tc::fence_after_sync();
@@ -252,7 +184,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_state(const ChunkArgs a) {
     } else if (tid == 0) {
         record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_STATE_WAIT);
     }
-    if (tid == 0 && a.vt_out != nullptr) bulk_wait_all();   // the v^T copy is done before the CTA leaves
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, DKC);
@@ -1392,8 +1323,8 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
         st_bytes = StateKeySmem<DV>::bytes;
         e = set_smem_attr_once((const void*)chunk_state_key<DV>, st_bytes);
     } else {
-        st_bytes = StateSmem<PER_KEY, DV>::bytes;
-        e = set_smem_attr_once((const void*)chunk_state<PER_KEY, DV>, st_bytes);
+        st_bytes = StateSmem<DV>::bytes;
+        e = set_smem_attr_once((const void*)chunk_state<DV>, st_bytes);
     }
     if (e != cudaSuccess) return e;
     if constexpr (HEADS) {
@@ -1413,7 +1344,7 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
         if (!make_natural_maps<DV>(a, &mk, &md, &mv)) return cudaErrorInvalidValue;
         chunk_state_key<DV><<<chunks, NT, st_bytes, s>>>(mk, md, mv, a);
     } else {
-        chunk_state<PER_KEY, DV><<<chunks, NT, st_bytes, s>>>(a);
+        chunk_state<DV><<<chunks, NT, st_bytes, s>>>(a);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
