@@ -385,29 +385,43 @@ chunk_state_key(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 // 2^{mu_t} is a scalar per token, so it is applied to v instead of k,
 // dS^T = (v (.) 2^{mu})^T k, and the transposed k tile is the same for every
 // head of the group.  One CTA per (batch, chunk, block of hb heads of one
-// group) loads it once and loops over the heads.  dv = 64.
+// group).  k and the heads' v tiles arrive by TMA in their natural
+// [token][feature] layout (rows past T read as zeros) and the threads
+// transpose them: k once, into the operand layout; each head's v tile,
+// scaled by its token weights and rounded, into one of two operand buffers,
+// while the next head's tile is already on its way into the other staging
+// half.  A head's dS^T goes from tensor memory into the operand buffer its v
+// used and out by one bulk copy.  dv = 64.
 template <int DV>
 struct StateHeadsSmem {
-    static constexpr int k_off = 0;                  // k^T (rows key, K = t), tf32
-    static constexpr int v_off = OPF;                // the head's v^T (rows value, K = t), scaled, tf32
-    static constexpr int mu_off = v_off + DV * CH;   // [CH] suffix sums of log2 d of the head
-    static constexpr int om_off = mu_off + CH;       // [CH] injection weights of the head
-    static constexpr int misc_off = om_off + CH;     // total, barrier, tmem slot
+    static constexpr int k_off = 0;                    // k^T operand (rows key, K = t), tf32
+    static constexpr int st_off = OPF;                 // staging: k [t][i], then two v tiles [t][j]
+    static constexpr int v_off = 2 * OPF;              // [2] (v 2^mu)^T operand (rows value, K = t), then dS^T
+    static constexpr int mu_off = v_off + 2 * DV * CH; // [CH] suffix sums of log2 d of the head
+    static constexpr int om_off = mu_off + CH;         // [CH] injection weights of the head
+    static constexpr int misc_off = om_off + CH;       // total, barriers (k, v0, v1, product), tmem slot
     static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+    static_assert(2 * DV * CH <= OPF && DV * DKC <= DV * CH, "buffer sizes");
 };
 
 template <int DV>
-__global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, int hb) {
+__global__ void __launch_bounds__(NT, 1)
+chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                  const ChunkArgs a, int hb) {
     extern __shared__ unsigned char smem_raw[];
     using L = StateHeadsSmem<DV>;
     float* base = align128(smem_raw);
     float* Ks = base + L::k_off;
-    float* Vs = base + L::v_off;
+    float* Sg = base + L::st_off;
     float* mu = base + L::mu_off;
     float* om = base + L::om_off;
     float* total_s = base + L::misc_off;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+    uint64_t* bk = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
+    uint64_t* bv = bk + 1;                              // [2]
+    uint64_t* bm = bk + 3;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 10);
+    auto stg = [&](int q) { return Sg + q * DV * CH; };
+    auto vop = [&](int q) { return base + L::v_off + q * DV * CH; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nhb = a.H / hb;
@@ -418,37 +432,68 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, in
     const int g = h0 / (a.H / a.G);
     const int t0 = n * CH, nval = min(CH, a.T - t0);
     const size_t row0 = (size_t)b * a.T + t0;
-    const size_t krs = (size_t)a.G * DKC, vrs = (size_t)a.H * DV;
 
     if (warp == 0) tc::tmem_alloc(slot, DKC);
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&bk[q], 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(bk, OPF * 4);
+        tma_load_3d(Sg, &map_k, bk, g * DKC, t0, b);
     }
-    copy_transposed<DKC>(Ks, a.k + row0 * krs + (size_t)g * DKC, krs, nval, warp, lane);
-    cp_async_commit();
-    cp_async_wait_all();
+    tc::fence_before_sync();
     __syncthreads();
-    for (int f = tid; f < OPF / 4; f += NT) st4(Ks + 4 * f, tf32x4(ld4(Ks + 4 * f)));
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    auto issue_v = [&](int hi) {   // thread 0: head h0 + hi's v tile into staging half hi & 1
+        mbar_arrive_expect_tx(&bv[hi & 1], DV * CH * 4);
+        tma_load_3d(stg(hi & 1), &map_v, &bv[hi & 1], (h0 + hi) * DV, t0, b);
+    };
+    int v_issued = 0;   // thread 0's count of v tiles requested
+    int v_used = 0;     // v tiles waited for
+    // warp 0: a head's decays, four tokens per lane, loaded a head ahead of
+    // their suffix sums so that the load latency hides behind the other work
+    float dr[4];
+    auto head_d = [&](int hh) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * lane + r;
+            dr[r] = (t < nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + hh) : 1.f;
+        }
+    };
+    if (warp == 0) head_d(h0);
 
-    uint32_t mpar = 0;
-    bool ok = true;
-    uint32_t tmem = 0;
+    // k^T, rounded: thread (key i, half of the tokens) reads its column
+    bool ok = __syncthreads_and(mbar_wait(bk, 0, a.wait_ns));
+    int site = SITE_STATE_WAIT;
+    if (ok) {
+        const int i = tid & (DKC - 1), tb0 = (CH / 2) * (tid >> 7);
+        float kr[CH / 2];
+#pragma unroll
+        for (int r = 0; r < CH / 2; ++r) kr[r] = Sg[(tb0 + r) * DKC + i];
+        __syncthreads();                                // the staging area is read: the v tiles go there
+        if (tid == 0) {
+            fence_proxy_async_smem();                   // those reads before the copies' writes
+            for (; v_issued < min(2, hb); ++v_issued) issue_v(v_issued);
+        }
+#pragma unroll
+        for (int t4 = 0; t4 < CH / 8; ++t4)
+            st4(Ks + off128(i, tb0 + 4 * t4), tf32x4(kr[4 * t4], kr[4 * t4 + 1], kr[4 * t4 + 2], kr[4 * t4 + 3]));
+    }
     for (int hi = 0; hi < hb && ok; ++hi) {
-        const int h = h0 + hi;
-        copy_transposed<DV>(Vs, a.v + row0 * vrs + (size_t)h * DV, vrs, nval, warp, lane);
-        cp_async_commit();
+        const int h = h0 + hi, p = hi & 1;
+        // the bulk copy out of two heads ago has read operand buffer p
+        if (tid == 0) bulk_wait_read_allbut1();
         if (warp == 0) {
             // exclusive suffix sums mu[t] = sum_{s > t} log2 d_s of this head
             float lg[4], sm = 0.f;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * lane + r;
-                const float dt = (t < nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + h) : 1.f;
-                lg[r] = (t < nval && a.d != nullptr) ? lg2(dt) : 0.f;
-                om[t] = a.gated ? 1.f - dt : 1.f;
+                lg[r] = (t < nval && a.d != nullptr) ? lg2(dr[r]) : 0.f;
+                om[t] = a.gated ? 1.f - dr[r] : 1.f;
                 sm += lg[r];
             }
+            if (hi + 1 < hb) head_d(h + 1);
             float x = sm;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -466,35 +511,44 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, in
                 if (!isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
             }
         }
-        cp_async_wait_all();
-        __syncthreads();
-        // v^T (.) 2^{mu_t}, rounded: a float4 of the operand holds four consecutive tokens
-        for (int f = tid; f < DV * CH / 4; f += NT) {
-            const int tq = ((4 * f) >> 5 & 31) * 4;
-            const float4 x = ld4(Vs + 4 * f);
-            st4(Vs + 4 * f, tf32x4(x.x * ex2(mu[tq]) * om[tq], x.y * ex2(mu[tq + 1]) * om[tq + 1],
-                                   x.z * ex2(mu[tq + 2]) * om[tq + 2], x.w * ex2(mu[tq + 3]) * om[tq + 3]));
+        ok = __syncthreads_and(mbar_wait(&bv[p], (uint32_t)(hi >> 1) & 1u, a.wait_ns));
+        if (!ok) break;
+        v_used = hi + 1;
+        {
+            // (v^T (.) 2^{mu_t}), rounded, into operand buffer p: thread = value
+            // column j, a run of TPV tokens (a float4 of the operand holds four)
+            constexpr int TPV = CH * DV / NT;
+            const int j = tid % DV, tq0 = (tid / DV) * TPV;
+            const float* sv = stg(p);
+            float* vo = vop(p);
+#pragma unroll
+            for (int t4 = 0; t4 < TPV / 4; ++t4) {
+                const int tq = tq0 + 4 * t4;
+                const float v0 = sv[tq * DV + j], v1 = sv[(tq + 1) * DV + j];
+                const float v2 = sv[(tq + 2) * DV + j], v3 = sv[(tq + 3) * DV + j];
+                st4(vo + off128(j, tq), tf32x4(v0 * ex2(mu[tq]) * om[tq], v1 * ex2(mu[tq + 1]) * om[tq + 1],
+                                               v2 * ex2(mu[tq + 2]) * om[tq + 2], v3 * ex2(mu[tq + 3]) * om[tq + 3]));
+            }
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
+        __syncthreads();                                // staging half p is read; operand p is written
         tc::fence_after_sync();
-        tmem = *slot;
         if (tid == 0) {
             // dS^T (M = dv rows value, N = dk columns key) = (v 2^mu)^T (K = t) x k^T (K = t)
-            tc::gemm_tf32(tmem, Vs, Ks, CH, tc::idesc_tf32(DV, DKC), false);
-            tc::commit(bar);
+            tc::gemm_tf32(tmem, vop(p), Ks, CH, tc::idesc_tf32(DV, DKC), false);
+            tc::commit(bm);
+            if (v_issued < hb) issue_v(v_issued++);     // two heads ahead, into the half just read
         }
-        ok = __syncthreads_and(mbar_wait(bar, mpar, a.wait_ns));
-        mpar ^= 1;
+        ok = __syncthreads_and(mbar_wait(bm, (uint32_t)hi & 1u, a.wait_ns));
         tc::fence_after_sync();
-        if (ok) {
-            // M = 64: rows 16q .. 16q + 15 in lanes 32q .. 32q + 15
+        if (!ok) break;
+        {
+            // M = 64: rows 16q .. 16q + 15 in lanes 32q .. 32q + 15; dS^T over the operand it consumed
             const int lq = warp & 3, ih = warp >> 2;
             const int row = 16 * lq + (lane & 15);
             const bool mine = lane < 16;
-            const size_t bh = (size_t)b * a.H + h;
-            float* wt = a.W + (bh * a.NC + n) * (size_t)DV * DKC;
+            float* ds = vop(p);
 #pragma unroll
             for (int i0 = 64 * ih; i0 < 64 * ih + 64; i0 += 16) {
                 float x[16];
@@ -502,24 +556,36 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_heads(const ChunkArgs a, in
                 if (mine) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        st4(wt + off128(row, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+                        st4(ds + off128(row, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
                 }
             }
+            const size_t bh = (size_t)b * a.H + h;
             if (tid < DKC) {
                 const size_t gi = (bh * a.NC + n) * DKC + tid;
                 a.gam[gi] = ex2(total_s[0]);
                 a.anc[gi] = 1.f;
             }
-        } else if (tid == 0) {
-            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_STATE_WAIT);
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncthreads();   // dS^T is in place; tensor memory, mu and the weights are free for the next head
+            if (tid == 0) {
+                bulk_store(a.W + (bh * a.NC + n) * (size_t)DV * DKC, ds, DV * DKC * 4);
+                bulk_commit();
+            }
         }
-        tc::fence_before_sync();
-        __syncthreads();   // tensor memory, the v buffer and mu are reused by the next head
+    }
+    if (tid == 0) {
+        if (!ok) {
+            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
+            // the tiles still in flight land before the CTA leaves
+            (void)mbar_wait(bk, 0, a.wait_ns);
+            for (int q = v_used; q < v_issued; ++q) (void)mbar_wait(&bv[q & 1], (uint32_t)(q >> 1) & 1u, a.wait_ns);
+        }
+        bulk_wait_all();
     }
     tc::fence_before_sync();
     __syncthreads();
-    tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(*slot, DKC);
+    if (warp == 0) tc::tmem_dealloc(tmem, DKC);
 }
 
 // ------------------------------------------------------------------ chunk_carry
@@ -1274,15 +1340,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-// Heads per CTA of chunk_output_heads: the largest block of one group's heads
-// that still gives every SM two CTAs.
+// Heads per CTA of the heads kernels (one CTA per SM each): a CTA costs its
+// set-up (about 1.3 heads' time in both kernels, from phase stamps) plus one
+// head after another, and CTAs run in waves of one per SM, so the block of a
+// group's heads with the fewest waves x (hb + 1.3) wins (Mamba-2's 24 heads:
+// one wave of 128 CTAs of 24 heads against three of 8).
 int heads_per_cta(const ChunkArgs& a, int sm_count) {
     const int per_group = a.H / a.G;
-    for (int hb : {8, 6, 4, 3, 2}) {
+    int best = 1;
+    double best_cost = 0.0;
+    for (int hb = 1; hb <= per_group; ++hb) {
         if (per_group % hb != 0) continue;
-        if ((int64_t)a.B * a.NC * (a.H / hb) >= 2 * (int64_t)sm_count) return hb;
+        const int64_t ctas = (int64_t)a.B * a.NC * (a.H / hb);
+        const double cost = (double)((ctas + sm_count - 1) / sm_count) * (hb + 1.3);
+        if (hb == 1 || cost < best_cost) {
+            best = hb;
+            best_cost = cost;
+        }
     }
-    return 1;
+    return best;
 }
 
 // TMA maps of q and k for the output kernel: (B, T, G * dk) row-major, boxes
@@ -1308,6 +1384,18 @@ bool make_natural_maps(const ChunkArgs& a, CUtensorMap* mk, CUtensorMap* md, CUt
     const uint32_t bk[3] = {DKC, (uint32_t)CH, 1}, bv[3] = {DV, (uint32_t)CH, 1};
     return encode_tiled(mk, 3, a.k, dk_, sk_, bk, false) && encode_tiled(md, 3, a.d, dd_, sd_, bk, false) &&
            encode_tiled(mv, 3, a.v, dv_, sv_, bv, false);
+}
+
+// TMA maps of k and v for chunk_state_heads: natural boxes of 128 tokens x
+// 128 keys (k) and x dv values (v), no swizzle.
+template <int DV>
+bool make_heads_maps(const ChunkArgs& a, CUtensorMap* mk, CUtensorMap* mv) {
+    const uint64_t dk_[3] = {(uint64_t)a.G * DKC, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t sk_[2] = {(uint64_t)a.G * DKC * 4, (uint64_t)a.T * a.G * DKC * 4};
+    const uint64_t dv_[3] = {(uint64_t)a.H * DV, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t sv_[2] = {(uint64_t)a.H * DV * 4, (uint64_t)a.T * a.H * DV * 4};
+    const uint32_t bk[3] = {DKC, (uint32_t)CH, 1}, bv[3] = {DV, (uint32_t)CH, 1};
+    return encode_tiled(mk, 3, a.k, dk_, sk_, bk, false) && encode_tiled(mv, 3, a.v, dv_, sv_, bv, false);
 }
 
 template <bool PER_KEY, int DV>
@@ -1338,7 +1426,9 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     const unsigned chunks = (unsigned)((size_t)a.B * a.H * a.NC);
     if constexpr (HEADS) {
         const int hb = heads_per_cta(a, sm_count);
-        chunk_state_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, st_bytes, s>>>(a, hb);
+        CUtensorMap mk, mv;
+        if (!make_heads_maps<DV>(a, &mk, &mv)) return cudaErrorInvalidValue;
+        chunk_state_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, st_bytes, s>>>(mk, mv, a, hb);
     } else if constexpr (PER_KEY) {
         CUtensorMap mk, md, mv;
         if (!make_natural_maps<DV>(a, &mk, &md, &mv)) return cudaErrorInvalidValue;
@@ -1415,7 +1505,10 @@ cudaError_t launch_recur_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     const bool per_key = x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_KEY_GATED;
     a.bad = per_key ? reinterpret_cast<int*>(p) : nullptr;   // written by chunk_state every call
     p += round256((int64_t)x.B * x.H * a.NC * 4);
-    // per key: chunk_state leaves its rounded v^T tiles for the output stage
+    // per key: chunk_state_key leaves its rounded v^T tiles for the output
+    // stage (for the heads kernels this measured slower: 0.277 -> 0.289 ms
+    // on the Mamba-2 workload, the tiles' extra writes outweighing the
+    // 4-byte loads they replace)
     a.vt_out = per_key ? reinterpret_cast<float*>(p) : nullptr;
     a.vt = a.vt_out;
     a.st = st;
