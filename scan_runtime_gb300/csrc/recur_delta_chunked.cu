@@ -62,13 +62,13 @@ struct DeltaArgs {
 
 // ------------------------------------------------------------------ delta_prep
 struct PrepSmem {
-    static constexpr int b0 = 0;                 // K (hi), then K^T operand
-    static constexpr int b1 = OPF;               // K (lo), then V^T operand
+    static constexpr int b0 = 0;                 // K (hi, 128-byte swizzled), then k [t][i], then K^T operand
+    static constexpr int b1 = OPF;               // K (lo, swizzled), then v [t][j], then V^T operand
     static constexpr int b2 = 2 * OPF;           // A^T above the diagonal and X = (I + A)^{-1} on and
-                                                 // below it (fp32, stride LDX), then T operand
+                                                 // below it (fp32, stride LDX), then T operand, then W
     static constexpr int beta = b2 + CH * LDX;
-    static constexpr int misc = beta + CH;
-    static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
+    static constexpr int misc = beta + CH;       // barriers (products, K tile, k and v tiles), tmem slot
+    static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 1024;
 };
 
 // One doubling level of the lower-triangular inverse X = (I + A)^{-1}: for
@@ -142,16 +142,25 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
+// Tiles by TMA: K in the 128-byte-swizzled operand layout for the Gram
+// products (four boxes of 32 keys x 128 tokens), then k and v as natural
+// [token][feature] boxes, transposed by the threads into the K^T and V^T
+// operands once the inverse is done; W leaves through shared memory by a bulk
+// copy.  Rows past T read as zeros.
+__global__ void __launch_bounds__(NT, 1)
+delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
+           const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a) {
     extern __shared__ unsigned char smem_raw[];
     using L = PrepSmem;
-    float* base = align128(smem_raw);
+    float* base = reinterpret_cast<float*>(smem_align<1024>(smem_raw));
     float* buf0 = base + L::b0;
     float* buf1 = base + L::b1;
     float* buf2 = base + L::b2;
     float* beta_s = base + L::beta;
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 2);
+    uint64_t* barK = reinterpret_cast<uint64_t*>(base + L::misc + 4);    // the swizzled K tile
+    uint64_t* barT = reinterpret_cast<uint64_t*>(base + L::misc + 6);    // the natural k and v tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x % a.H;
@@ -162,63 +171,62 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
     const size_t bh = (size_t)b * a.H + h;
     const size_t row0 = (size_t)b * a.T + t0;
     const size_t tile = (bh * a.NC + n) * (size_t)OPF;
-    const size_t krs = (size_t)a.H * DKC;
 
     if (warp == 0) tc::tmem_alloc(slot, 256);
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(barK, 1);
+        mbar_init(barT, 1);
         fence_mbar_init();
-    }
-
-    // K rows straight into the operand layout (rows t, K = key); beta
-    const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
-    {
-        const float* kb = a.k + row0 * krs + (size_t)h * DKC + ic;
+        // K rows in the swizzled operand layout (rows t, K = key)
+        mbar_arrive_expect_tx(barK, OPF * 4);
 #pragma unroll
-        for (int tb = 0; tb < CH / 8; ++tb) {
-            const int t = 8 * tb + tl;
-            const bool ok = t < nval;
-            cp_async16(buf0 + off128(t, ic), kb + (size_t)(ok ? t : 0) * krs, ok);
-        }
-        cp_async_commit();
+        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(buf0 + at * 4096, &map_ks, barK, h * DKC + 32 * at, t0, b);
     }
     if (tid < CH) beta_s[tid] = tid < nval ? __ldg(a.beta + (row0 + tid) * a.H + h) : 0.f;
-    cp_async_wait_all();
-    __syncthreads();
+    __syncthreads();   // the barriers are initialised before any thread polls them
+    bool ok = __syncthreads_and(mbar_wait(barK, 0, a.wait_ns));
+    int site = SITE_PREP_WAIT1;
+    bool t_issued = false;   // thread 0: the natural k and v tiles were requested
 
-    // K = hi + lo, both tf32: K K^T ~ hi hi^T + hi lo^T + lo hi^T
-#pragma unroll
-    for (int tb = 0; tb < CH / 8; ++tb) {
-        const int o = off128(8 * tb + tl, ic);
-        const float4 x = ld4(buf0 + o);
-        const float4 hi = tf32x4(x);
-        st4(buf0 + o, hi);
-        st4(buf1 + o, tf32x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w));
+    // K = hi + lo, both tf32: K K^T ~ hi hi^T + hi lo^T + lo hi^T (elementwise,
+    // so the split keeps the swizzled layout)
+    if (ok) {
+        for (int f = tid; f < OPF / 4; f += NT) {
+            const float4 x = ld4(buf0 + 4 * f);
+            const float4 hi = tf32x4(x);
+            st4(buf0 + 4 * f, hi);
+            st4(buf1 + 4 * f, tf32x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w));
+        }
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *slot;
-    if (tid == 0) {
+    if (ok && tid == 0) {
         const uint32_t id = tc::idesc_tf32(128, 128);
-        tc::gemm_tf32(tmem, buf0, buf0, DKC, id, false);
-        tc::gemm_tf32(tmem, buf0, buf1, DKC, id, true);
-        tc::gemm_tf32(tmem, buf1, buf0, DKC, id, true);
+        tc::gemm_tf32_sw_sw(tmem, buf0, buf0, id, false);
+        tc::gemm_tf32_sw_sw(tmem, buf0, buf1, id, true);
+        tc::gemm_tf32_sw_sw(tmem, buf1, buf0, id, true);
         tc::commit(bar);
     }
-    bool ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
+    ok = __syncthreads_and(ok && mbar_wait(bar, 0, a.wait_ns));
+    const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
     tc::fence_after_sync();
     const int lq = warp & 3, hf = warp >> 2;
     const int tr = 32 * lq + lane;                           // tensor-memory row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     if (ok) {
-        // the K^T and V^T operands can stream in now (the Gram products have
+        // the natural k and v tiles can stream in now (the Gram products have
         // read the hi and lo parts of K) while the inverse runs
-        copy_transposed<DKC>(buf0, a.k + row0 * krs + (size_t)h * DKC, krs, nval, warp, lane);
-        copy_transposed<128>(buf1, a.v + row0 * (size_t)a.H * 128 + (size_t)h * 128, (size_t)a.H * 128, nval, warp,
-                             lane);
-        cp_async_commit();
+        if (tid == 0) {
+            t_issued = true;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(barT, 2 * OPF * 4);
+            tma_load_3d(buf0, &map_kn, barT, h * DKC, t0, b);
+            tma_load_3d(buf1, &map_vn, barT, h * 128, t0, b);
+        }
 
         // A = diag(beta) strict_lower(K K^T) in fp32, stored transposed: AT[j][t] = A[t][j]
         // (zeros on and below the diagonal, where X goes next)
@@ -278,14 +286,24 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
 #pragma unroll
         for (int tb = 0; tb < CH / 8; ++tb) st4(buf2 + off128(8 * tb + tl, ic), tv[tb]);
 
-        cp_async_wait_all();
-        __syncthreads();
-        for (int f = tid; f < OPF / 4; f += NT) {
-            st4(buf0 + 4 * f, tf32x4(ld4(buf0 + 4 * f)));
-            st4(buf1 + 4 * f, tf32x4(ld4(buf1 + 4 * f)));
+        // K^T and V^T, rounded, from the natural tiles: thread = feature
+        // column i, a half of the tokens, through registers
+        ok = __syncthreads_and(mbar_wait(barT, 0, a.wait_ns));
+        if (ok) {
+            const int i = tid & 127, tb0 = (CH / 2) * (tid >> 7);
+            float kr[CH / 2], vr[CH / 2];
+#pragma unroll
+            for (int r = 0; r < CH / 2; ++r) {
+                kr[r] = buf0[(tb0 + r) * DKC + i];
+                vr[r] = buf1[(tb0 + r) * 128 + i];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t4 = 0; t4 < CH / 8; ++t4) {
+                st4(buf0 + off128(i, tb0 + 4 * t4), tf32x4(kr[4 * t4], kr[4 * t4 + 1], kr[4 * t4 + 2], kr[4 * t4 + 3]));
+                st4(buf1 + off128(i, tb0 + 4 * t4), tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
+            }
         }
-    } else if (tid == 0) {
-        record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_PREP_WAIT1);
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
@@ -301,7 +319,8 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
         ok = __syncthreads_and(mbar_wait(bar, 1, a.wait_ns));
         tc::fence_after_sync();
         if (ok) {
-            float* wt = a.Wt + tile;
+            // W through shared memory (the T operand is consumed) and out by a
+            // bulk copy, with the K^T operand as it stands (tf32) for the chain
             float* ut = a.Ut + tile;
 #pragma unroll
             for (int i0 = 64 * hf; i0 < 64 * hf + 64; i0 += 16) {
@@ -309,20 +328,29 @@ __global__ void __launch_bounds__(NT, 1) delta_prep(const DeltaArgs a) {
                 tc::ld16(lane_base + i0, x);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    st4(wt + off128(tr, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+                    st4(buf2 + off128(tr, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
                 tc::ld16(lane_base + 128 + i0, x);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     st4(ut + tr * 128 + i0 + 4 * q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
             }
-            if (tid == 0) {   // the K^T operand as it stands (tf32) for the chain kernel
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_store(a.Wt + tile, buf2, OPF * 4);
                 bulk_store(a.KTt + tile, buf0, OPF * 4);
                 bulk_commit();
-                bulk_wait_read_all();
+                bulk_wait_all();
             }
-        } else if (tid == 0) {
-            record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_PREP_WAIT2);
+        } else {
+            site = SITE_PREP_WAIT2;
         }
+    }
+    if (!ok && tid == 0) {
+        record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
+        // the tiles still in flight land before the CTA leaves
+        (void)mbar_wait(barK, 0, a.wait_ns);
+        if (t_issued) (void)mbar_wait(barT, 0, a.wait_ns);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -534,6 +562,18 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     d.st = st;
     d.wait_ns = wait_ns;
 
+    // TMA maps of k (swizzled boxes of 32 keys for the Gram products, and the
+    // natural tile) and v (natural tile): (B, T, H * 128) row-major
+    CUtensorMap mks, mkn, mvn;
+    {
+        const uint64_t dims[3] = {(uint64_t)x.H * DKC, (uint64_t)x.T, (uint64_t)x.B};
+        const uint64_t strides[2] = {(uint64_t)x.H * DKC * 4, (uint64_t)x.T * x.H * DKC * 4};
+        const uint32_t box_sw[3] = {32, (uint32_t)CH, 1}, box_n[3] = {DKC, (uint32_t)CH, 1};
+        if (!encode_tiled(&mks, 3, x.k, dims, strides, box_sw, true) ||
+            !encode_tiled(&mkn, 3, x.k, dims, strides, box_n, false) ||
+            !encode_tiled(&mvn, 3, x.v, dims, strides, box_n, false))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = set_smem_attr_once((const void*)delta_prep, PrepSmem::bytes);
     if (e != cudaSuccess) return e;
     e = set_smem_attr_once((const void*)delta_chain, ChainSmem::bytes);
@@ -576,7 +616,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
         d.n0 = g * len;
         d.n1 = std::min(d.NC, d.n0 + len);
-        delta_prep<<<(unsigned)((size_t)x.B * x.H * (d.n1 - d.n0)), NT, PrepSmem::bytes, sp>>>(d);
+        delta_prep<<<(unsigned)((size_t)x.B * x.H * (d.n1 - d.n0)), NT, PrepSmem::bytes, sp>>>(mks, mkn, mvn, d);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = order(sp, sc);
         if (e != cudaSuccess) break;
