@@ -1070,6 +1070,8 @@ PROFILE_CASES = {
     "deltanet": "delta rule, full DeltaNet workload B=4 T=4096 H=8 dk=dv=128",
     "rwkv7_prefill": "RWKV-7 sequence kernel, full prefill workload B=16 T=4096 H=12 64x64",
     "rwkv7_decode": "RWKV-7 decode kernel, full decode workload B=1024 T=1 H=12 64x64",
+    "gla_decode": "decode ring kernel, GLA single step B=1024 T=1 H=4 128x128, states in place",
+    "deltanet_decode": "decode ring kernel, DeltaNet single step B=1024 T=1 H=8 128x128, states in place",
     "gla_chunked": "chunked tensor-core form, full GLA workload B=4 T=4096 H=4 dk=dv=128",
     "mamba2_chunked": "chunked tensor-core form, full Mamba-2 workload B=4 T=4096 H=24 dk=128 dv=64",
     "deltanet_chunked": "chunked tensor-core delta rule, full DeltaNet workload B=4 T=4096 H=8 dk=dv=128",
@@ -1138,6 +1140,24 @@ def run_profile_case(args):
             D = torch.ones(H, device=dev)
             fn = lambda: sr.sn_readout_dskip(h, Bc, Tc, H, dv, o, z, D, y, s)
         nbytes = 12 * o.numel()
+    elif name in ("gla_decode", "deltanet_decode"):
+        if name == "gla_decode":
+            Bc, H, dk, dv = 1024, 4, 128, 128
+            x = synth.gla_inputs(Bc, 1, H, dk, dv, cid=97, device=dev)
+        else:
+            Bc, H, dk, dv = 1024, 8, 128, 128
+            x = synth.deltanet_inputs(Bc, 1, H, dk, dv, cid=97, device=dev)
+        S = torch.empty((Bc, H, dk, dv), device=dev).normal_(generator=torch.Generator(dev).manual_seed(98))
+        o = torch.empty((Bc, 1, H, dv), device=dev)
+        if name == "gla_decode":
+            fn = lambda: sr.sn_recur_diag(h, Bc, 1, H, H, dk, dv, x["decay_kind"], x["scale"], x["q"], x["k"],
+                                          x["v"], x["d"], S, S, o, s)
+            gbytes = x["d"].numel() * 4
+        else:
+            fn = lambda: sr.sn_recur_delta(h, Bc, 1, H, dk, dv, x["scale"], x["q"], x["k"], x["v"], x["beta"],
+                                           S, S, o, s)
+            gbytes = x["beta"].numel() * 4
+        nbytes = 2 * S.numel() * 4 + (x["q"].numel() + x["k"].numel() + x["v"].numel() + o.numel()) * 4 + gbytes
     elif name == "deltanet_chunked":
         c = synth.CONFIGS["deltanet"]
         x = synth.config_inputs("deltanet", device=dev)
