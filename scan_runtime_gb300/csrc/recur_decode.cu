@@ -351,13 +351,13 @@ cudaError_t run_decode_kind(const RecurArgs& x, const DecodeParams& p, int sm_co
 
 }  // namespace
 
-bool recur_decode_cols_supported(const RecurArgs& x) {
+bool recur_decode_ring_supported(const RecurArgs& x) {
     const bool kind_ok = x.kind == RK_DIAG_KEY || x.kind == RK_DIAG_HEAD || x.kind == RK_DIAG_KEY_GATED ||
                          x.kind == RK_DIAG_HEAD_GATED || x.kind == RK_DELTA || x.kind == RK_RWKV7;
     return kind_ok && x.T == 1 && (x.dk == 64 || x.dk == 128) && (x.dv == 64 || x.dv == 128);
 }
 
-cudaError_t launch_recur_decode_cols(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+cudaError_t launch_recur_decode_ring(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                      cudaStream_t s) {
     DecodeParams p;
     p.st = st;

@@ -13,11 +13,11 @@ cudaError_t launch_recur_rwkv7_seq(const RecurArgs& x, SnDevStatus* st, uint64_t
     return run_seq_w<RK_RWKV7, 64, 8, 2, false, 0>(x, st, wait_ns, w, stream);
 }
 
-bool recur_decode_supported(const RecurArgs& x) { return recur_decode_cols_supported(x); }
+bool recur_decode_supported(const RecurArgs& x) { return recur_decode_ring_supported(x); }
 
 cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                 cudaStream_t stream) {
-    return launch_recur_decode_cols(x, st, wait_ns, sm_count, stream);   // recur_decode.cu
+    return launch_recur_decode_ring(x, st, wait_ns, sm_count, stream);   // recur_decode.cu
 }
 
 }  // namespace sn

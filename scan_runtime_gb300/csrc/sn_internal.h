@@ -163,8 +163,8 @@ cudaError_t launch_recur_decode(const RecurArgs& x, SnDevStatus* st, uint64_t wa
                                 cudaStream_t stream);
 bool recur_decode_supported(const RecurArgs& x);
 // recur_decode.cu: T == 1 of every kind (diagonal decays, the delta rule, RWKV-7)
-bool recur_decode_cols_supported(const RecurArgs& x);
-cudaError_t launch_recur_decode_cols(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
+bool recur_decode_ring_supported(const RecurArgs& x);
+cudaError_t launch_recur_decode_ring(const RecurArgs& x, SnDevStatus* st, uint64_t wait_ns, int sm_count,
                                      cudaStream_t stream);
 
 // Chunked tensor-core form of the delta rule (recur_delta_chunked.cu).
