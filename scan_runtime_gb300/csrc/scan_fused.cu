@@ -11,8 +11,9 @@
 //   2. one cooperative launch: CTA col < columns is the chain of column col
 //      (warp 0, lane = channel), folding C_k = fma(A_k, C_{k-1}, B_k) over the
 //      chunks in order with the aggregates staged by bulk copies (FU_CSTAGES
-//      blocks of FU_CB chunks in flight), and storing each carry as a 64-bit
-//      word that holds the launch's tag beside the carry's bits; the other
+//      blocks of FU_CB chunks in flight) into shared memory, while its warp 1
+//      publishes each carry as a 64-bit word that holds the launch's tag
+//      beside the carry's bits; the other
 //      CTAs compute the states of the tiles first to last (the first ones
 //      are the last the aggregate pass read, still in L2), each waiting for
 //      the carry word of the chunk before its own.
@@ -44,9 +45,12 @@ constexpr int FU_STAGES = 2;                       // tiles in flight in a state
 constexpr uint32_t FU_CARRY = 3u;                  // tag state of a carry word
 constexpr uint32_t FU_EPOCH_WRAP = 1u << 29;
 constexpr uint32_t FU_CBLK_FLOATS = FU_CB * LB_NC;  // one block of one array (agg_index layout)
+constexpr int FU_CQ = 4;                           // carry blocks between the folding and the storing warp
 constexpr size_t FU_RING = FU_STAGES * (size_t)LB_TILE_BYTES;
 static_assert((size_t)FU_CSTAGES * 2 * FU_CBLK_FLOATS * 4 <= FU_RING, "the chain ring reuses the tile ring");
-constexpr size_t FU_SMEM = FU_RING + (FU_STAGES + FU_CSTAGES) * 8 + 16;
+constexpr size_t FU_CBUF = (size_t)FU_CQ * FU_CBLK_FLOATS * 4;   // the folded carries, [block][group][lane][4]
+constexpr int FU_NBAR = FU_STAGES + FU_CSTAGES + 2 * FU_CQ;
+constexpr size_t FU_SMEM = FU_RING + FU_CBUF + FU_NBAR * 8 + 16;
 
 struct FusedParams {
     int B, T, N, ncb, nbcb, nchunks, ntiles;
@@ -70,7 +74,8 @@ template <bool GATED>
 __global__ void __launch_bounds__(LB_THREADS, 2)
 scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const FusedParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + FU_RING);   // [FU_STAGES] tiles | [FU_CSTAGES] chain
+    // [FU_STAGES] tiles | [FU_CSTAGES] chain ring | [FU_CQ] carries folded | [FU_CQ] carries stored
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + FU_RING + FU_CBUF);
     __shared__ float4 wA[8][8], wB[8][8];
     __shared__ float carry[LB_NC], cfin[LB_NC];
     __shared__ uint32_t s_epoch;
@@ -79,7 +84,7 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
     const int nq = chunk_quads(p.nchunks);
 
     if (tid == 0) {
-        for (int s = 0; s < FU_STAGES + FU_CSTAGES; ++s) mbar_init(&bar[s], 1);
+        for (int s = 0; s < FU_NBAR; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
         const uint32_t last = *reinterpret_cast<volatile const uint32_t*>(&p.st->lb_epoch);
         s_epoch = last + 1 >= FU_EPOCH_WRAP ? 1u : last + 1;
@@ -105,14 +110,50 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
 
     if ((int)blockIdx.x < p.nbcb) {
         // ------------------------------------------------ chain CTA of column blockIdx.x
-        if (warp != 0) return;
+        // Warp 0 folds the carries into shared memory (FU_CQ blocks deep) and
+        // warp 1 publishes them as tagged words, so the dependent FMA chain
+        // never waits behind global stores.
+        if (warp > 1) return;
         const size_t col = blockIdx.x;
         const int bi = (int)(col / p.ncb), cb = (int)(col % p.ncb);
         const int n = cb * LB_NC + lane;
         float* ring = reinterpret_cast<float*>(smem);             // [stage][A | B][FU_CBLK_FLOATS]
+        float* cbuf = reinterpret_cast<float*>(smem + FU_RING);   // [FU_CQ][group][lane][4] carries
         uint64_t* cbar = bar + FU_STAGES;
+        uint64_t* cfull = cbar + FU_CSTAGES;                      // [FU_CQ] a block is folded
+        uint64_t* cfree = cfull + FU_CQ;                          // [FU_CQ] a block is published
         const size_t colbase = agg_index(col, nq, 0, 0);
         const int nblk = (p.nchunks + FU_CB - 1) / FU_CB;
+        // bounded wait that also ends when another CTA or warp gave up
+        auto wait_or_abort = [&](uint64_t* b, uint32_t parity) {
+            if (mbar_try_wait(b, parity)) return true;
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(b, parity))
+                if (global_ns() - t0 > p.wait_ns || aborted()) return false;
+            return true;
+        };
+        if (warp == 1) {
+            unsigned long long* cwc = p.cw + colbase;
+            bool ok = true;
+            for (int j = 0; j < nblk; ++j) {
+                const int q = j % FU_CQ;
+                ok = __all_sync(0xffffffffu, wait_or_abort(&cfull[q], (uint32_t)(j / FU_CQ) & 1u));
+                if (!ok) break;
+                const int k0 = j * FU_CB, cnt = min(FU_CB, p.nchunks - k0);
+                const float4* src = reinterpret_cast<const float4*>(cbuf + (size_t)q * FU_CBLK_FLOATS) + lane;
+                for (int g = 0; g < (cnt + 3) >> 2; ++g) {   // four carries of the lane's channel per group
+                    const float4 r = src[g * LB_NC];
+                    unsigned long long* d = cwc + ((size_t)((k0 >> 2) + g) * LB_NC + lane) * 4;
+                    st_relaxed_gpu_v2u64(d, hi | __float_as_uint(r.x), hi | __float_as_uint(r.y));
+                    st_relaxed_gpu_v2u64(d + 2, hi | __float_as_uint(r.z), hi | __float_as_uint(r.w));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cfree[q]);
+            }
+            if (!ok && lane == 0) give_up(8);
+            named_bar_sync(1, 64);                        // the CTA finishes with the folding warp
+            return;
+        }
         auto issue = [&](int j) {   // lane 0: block j's aggregates into stage j % FU_CSTAGES
             const int k0 = j * FU_CB, st = j % FU_CSTAGES;
             const uint32_t bytes = (uint32_t)chunk_quads(min(FU_CB, p.nchunks - k0)) * LB_NC * 16;
@@ -129,22 +170,18 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
         // the state tiles: a call may write its final states over s0
         float c = (p.s0 != nullptr && n < p.N) ? p.s0[(size_t)bi * p.N + n] : 0.f;
         st_relaxed_gpu_u64(p.cw0 + col * LB_NC + lane, hi | __float_as_uint(c));
-        unsigned long long* cwc = p.cw + colbase;
-        // four carries of the lane's channel (chunks 4 q .. 4 q + 3) as two 16-byte stores
-        auto put4 = [&](int q, float4 r) {
-            unsigned long long* d = cwc + ((size_t)q * LB_NC + lane) * 4;
-            st_relaxed_gpu_v2u64(d, hi | __float_as_uint(r.x), hi | __float_as_uint(r.y));
-            st_relaxed_gpu_v2u64(d + 2, hi | __float_as_uint(r.z), hi | __float_as_uint(r.w));
-        };
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
-            const int st = j % FU_CSTAGES;
+            const int st = j % FU_CSTAGES, q = j % FU_CQ;
             ok = __all_sync(0xffffffffu, mbar_wait(&cbar[st], (uint32_t)(j / FU_CSTAGES) & 1, p.wait_ns));
+            // the carry buffer q is free once warp 1 has published block j - FU_CQ
+            if (ok && j >= FU_CQ)
+                ok = __all_sync(0xffffffffu, wait_or_abort(&cfree[q], (uint32_t)(j / FU_CQ - 1) & 1u));
             if (!ok) break;
             const int k0 = j * FU_CB, cnt = min(FU_CB, p.nchunks - k0);
             const float4* sA = reinterpret_cast<const float4*>(ring + (size_t)st * 2 * FU_CBLK_FLOATS) + lane;
             const float4* sB = sA + FU_CBLK_FLOATS / 4;
-            const int q0 = k0 >> 2;
+            float4* dst = reinterpret_cast<float4*>(cbuf + (size_t)q * FU_CBLK_FLOATS) + lane;
             if (cnt == FU_CB) {
                 // a full block: the groups are read a batch of four ahead of the
                 // FMAs that consume them, so the dependent chain waits on no load
@@ -169,7 +206,7 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
                         c = __fmaf_rn(a0[u].y, c, b0[u].y); r.y = c;
                         c = __fmaf_rn(a0[u].z, c, b0[u].z); r.z = c;
                         c = __fmaf_rn(a0[u].w, c, b0[u].w); r.w = c;
-                        put4(q0 + g + u, r);
+                        dst[(g + u) * LB_NC] = r;
                     }
                     if (g + 2 * QB < NG) {
 #pragma unroll
@@ -185,21 +222,22 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
                         c = __fmaf_rn(a1[u].y, c, b1[u].y); r.y = c;
                         c = __fmaf_rn(a1[u].z, c, b1[u].z); r.z = c;
                         c = __fmaf_rn(a1[u].w, c, b1[u].w); r.w = c;
-                        put4(q0 + g + QB + u, r);
+                        dst[(g + QB + u) * LB_NC] = r;
                     }
                 }
             } else {
                 // the sequence's last, partial block: one chunk at a time
                 const float* fA = ring + (size_t)st * 2 * FU_CBLK_FLOATS;
                 const float* fB = fA + FU_CBLK_FLOATS;
+                float* fC = cbuf + (size_t)q * FU_CBLK_FLOATS;
                 for (int i = 0; i < cnt; ++i) {
                     const int o = ((i >> 2) * LB_NC + lane) * 4 + (i & 3);
                     c = __fmaf_rn(fA[o], c, fB[o]);
-                    st_relaxed_gpu_u64(cwc + ((size_t)(q0 + (i >> 2)) * LB_NC + lane) * 4 + (i & 3),
-                                       hi | __float_as_uint(c));
+                    fC[o] = c;
                 }
             }
-            __syncwarp();                                 // the stage is read
+            __syncwarp();                                 // the stage is read, the carries are written
+            if (lane == 0) mbar_arrive(&cfull[q]);        // (release: warp 1 reads them after its wait)
             if (issued < nblk) {
                 if (lane == 0) {
                     fence_proxy_async_smem();             // those reads before the copy's writes
@@ -214,7 +252,7 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
             for (int j = max(0, issued - FU_CSTAGES); j < issued; ++j)
                 (void)mbar_wait(&cbar[j % FU_CSTAGES], (uint32_t)(j / FU_CSTAGES) & 1, p.wait_ns);
         }
-        __syncwarp();
+        named_bar_sync(1, 64);                            // and with the publishing warp
         if (lane == 0) finish();
         return;
     }
