@@ -116,9 +116,10 @@ typedef int32_t sn_status;
 #define SN_SCAN_KERNEL_SEQUENTIAL 1
 #define SN_SCAN_KERNEL_LOOKBACK   2
 #define SN_SCAN_KERNEL_REDUCE_SCAN 3   /* the look-back kernel's results in three flag-free passes */
-#define SN_SCAN_KERNEL_FUSED       4   /* the same results in two launches: the aggregate pass, then the
-                                          per-column carry chains inside the state pass (forward scans;
-                                          T < 1024 runs reduce-then-scan) */
+#define SN_SCAN_KERNEL_FUSED       4   /* the same results in one launch that reads a and b once, a
+                                          carry chain per column running beside the tiles (forward scans;
+                                          T < 1024, or more than (2 SMs - 17 columns) / 17 columns, runs
+                                          reduce-then-scan) */
 
 /* Operation ids for sn_workspace_bytes(). */
 #define SN_OP_SCAN_FMA   1
@@ -170,8 +171,8 @@ sn_status sn_ctx_set_workspace(SnCtx* ctx, void* dev_ptr, int64_t bytes);
  *   a flag word per tile rounded up to 256 bytes, plus the larger of 512
  *   bytes per tile and columns * (1536 * ceil(chunks / 4) + 128) bytes
  *   (the look-back and reduce-then-scan kernels), and
- *   columns * (2048 * ceil(chunks / 4) + 256) bytes from eight chunks on
- *   (the fused kernel);
+ *   columns * (2304 * ceil(chunks / 4) + 256) bytes from eight chunks on
+ *   (the fused kernel's tagged carry and aggregate words);
  * 0 for an op that needs none, -1 on invalid arguments. */
 int64_t sn_workspace_bytes(int32_t op, int32_t B, int32_t T, int32_t N);
 

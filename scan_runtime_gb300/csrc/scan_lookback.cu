@@ -347,7 +347,6 @@ constexpr size_t PASS_SMEM = PASS_STAGES * LB_TILE_BYTES + PASS_STAGES * 8 + 16;
 
 struct PassParams {
     int B, T, N, ncb, nbcb, nchunks, ntiles;
-    int agg_reverse;     // the aggregate pass visits the tiles last to first
     const float* s0;
     float* s_final;
     float* s_out;
@@ -379,7 +378,7 @@ scan_pass(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     // opposite order, so it starts on the tiles the aggregate pass read last,
     // which are still in L2
     auto tile_coords = [&](int ti, int& k, int& bi, int& cb) {
-        if (OUT || p.agg_reverse) ti = p.ntiles - 1 - ti;
+        if (OUT) ti = p.ntiles - 1 - ti;
         k = ti / p.nbcb;
         const int r = ti - k * p.nbcb;
         bi = r / p.ncb;
@@ -466,7 +465,6 @@ cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnD
     p.nbcb = x.B * p.ncb;
     p.nchunks = (x.T + LB_TC - 1) / LB_TC;
     p.ntiles = p.nbcb * p.nchunks;
-    p.agg_reverse = 0;
     p.s0 = x.s0;
     p.s_final = x.s_final;
     p.s_out = x.s_out;
@@ -498,38 +496,6 @@ cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnD
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k_out<<<grid, LB_THREADS, PASS_SMEM, stream>>>(ma, mb, p);
-    return cudaGetLastError();
-}
-
-
-
-// The aggregate pass alone, last tile first, into dA / dB at agg_index (the
-// first launch of the fused path, scan_fused.cu).
-cudaError_t launch_scan_aggregates(const ScanArgs& x, bool gated, float* dA, float* dB, SnDevStatus* st,
-                                   uint64_t wait_ns, int sm_count, cudaStream_t stream) {
-    CUtensorMap ma, mb;
-    if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, LB_NC, LB_TC) ||
-        !make_scan_map(&mb, x.b, x.B, x.T, x.N, LB_NC, LB_TC))
-        return cudaErrorInvalidValue;
-    PassParams p{};
-    p.B = x.B;
-    p.T = x.T;
-    p.N = x.N;
-    p.ncb = (x.N + LB_NC - 1) / LB_NC;
-    p.nbcb = x.B * p.ncb;
-    p.nchunks = (x.T + LB_TC - 1) / LB_TC;
-    p.ntiles = p.nbcb * p.nchunks;
-    p.agg_reverse = 1;
-    p.dA = dA;
-    p.dB = dB;
-    p.st = st;
-    p.wait_ns = wait_ns;
-    auto k_agg = gated ? scan_pass<true, false> : scan_pass<false, false>;
-    int occ = 0;
-    cudaError_t e = occupancy_once((const void*)k_agg, LB_THREADS, PASS_SMEM, &occ);
-    if (e != cudaSuccess) return e;
-    const int grid = (int)std::min<int64_t>(p.ntiles, (int64_t)occ * sm_count);
-    k_agg<<<grid, LB_THREADS, PASS_SMEM, stream>>>(ma, mb, p);
     return cudaGetLastError();
 }
 

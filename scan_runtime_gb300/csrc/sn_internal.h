@@ -117,14 +117,11 @@ cudaError_t launch_scan_lookback(const ScanArgs& x, bool gated, void* ws, int po
 // launches without flags, for few channel tiles and long T; same workspace.
 cudaError_t launch_scan_reduce_scan(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
                                     int sm_count, cudaStream_t stream);
-// The reduce-then-scan path's aggregate pass alone, last tile first (scan_lookback.cu).
-cudaError_t launch_scan_aggregates(const ScanArgs& x, bool gated, float* dA, float* dB, SnDevStatus* st,
-                                   uint64_t wait_ns, int sm_count, cudaStream_t stream);
-// The same results in two launches (scan_fused.cu): the aggregate pass, then
-// one cooperative launch in which a chain CTA per column of tiles folds the
-// carries while the other CTAs compute the states.  Whether it runs (eight
-// chunks or more; else the reduce-then-scan launches run), the workspace
-// bytes it needs, and the tagged area [a, a + b) a change of geometry clears.
+// The same results in one cooperative launch (scan_fused.cu) that reads a and
+// b once: state CTAs publish each tile's aggregate and wait for its carry,
+// which a chain CTA per column of tiles folds.  Whether it runs (eight chunks
+// or more; else the reduce-then-scan launches run), the workspace bytes it
+// needs, and the tagged area [a, a + b) a change of geometry clears.
 bool scan_fused_applies(int T);
 int64_t scan_fused_ws_bytes(int B, int T, int N);
 void scan_fused_tag_area(int B, int T, int N, int64_t* a, int64_t* b);

@@ -126,13 +126,14 @@ def test_workspace_bytes(abi):
     nb = abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 8, 8192, 2048)
     tiles = 8 * (2048 // 32) * (8192 // 128)
     # flags, the A and B aggregates (f32) and the tagged carry words (u64)
-    assert nb == ((tiles * 4 + 255) // 256) * 256 + tiles * (2 * 32 * 4 + 32 * 8)
-    # the fused kernel's arrays (from eight chunks on): A and B, a tagged
-    # 8-byte carry word per chunk and channel, the tagged initial carries
+    lb = ((tiles * 4 + 255) // 256) * 256 + tiles * (2 * 32 * 4 + 32 * 8)
+    # the fused kernel's tagged words (from eight chunks on), chunks padded to
+    # groups of four: 256 bytes of group-end carries and 2048 of aggregates
+    # per group and column, then the initial carries
     cols, chunks = 8 * (2048 // 32), 8192 // 128
-    assert nb == max(nb, cols * (2048 * ((chunks + 3) // 4) + 256))
+    assert nb == max(lb, cols * (2304 * ((chunks + 3) // 4) + 256))
     cols, chunks = 3 * (64 // 32), 9
-    fused = cols * (2048 * ((chunks + 3) // 4) + 256)
+    fused = cols * (2304 * ((chunks + 3) // 4) + 256)
     lb = ((cols * chunks * 4 + 255) // 256) * 256 + cols * chunks * 512
     assert fused > lb
     assert abi.sn_workspace_bytes(abi.SN_OP_SCAN_FMA, 3, 9 * 128, 64) == fused

@@ -255,12 +255,14 @@ def test_lookback_bounded_wait_reports_timeout(sr, lbctx):
 
 @pytest.mark.parametrize("form", ["fma", "gated"])
 @pytest.mark.parametrize("shape", [(1, 4096, 32), (2, 1000, 64), (3, 257, 96), (2, 5, 8), (1, 70000, 64),
-                                   (1, 40000, 36)])
+                                   (1, 40000, 36), (1, 70000, 32), (4, 4096, 1024), (2, 16384, 512)])
 def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
     """The reduce-then-scan path and the fused path run the look-back kernel's
     local scans, aggregates and carry chain in the same order, so their
     results equal the look-back's bit for bit; T = 70000 and 40000 span
-    several blocks of the carry chains, N = 36 a ragged channel tile."""
+    several blocks of the carry chains and wrap their rings, N = 36 is a
+    ragged channel tile, (1, 70000, 32) a single column, and the last two
+    have so many columns that the fused path's aggregates run far ahead."""
     B, T, N = shape
     ctx.ensure_workspace(B, T, N)
     a, b, u, s0 = _inputs(B, T, N, 40 + T % 11)
