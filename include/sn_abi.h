@@ -118,7 +118,7 @@ typedef int32_t sn_status;
 #define SN_SCAN_KERNEL_REDUCE_SCAN 3   /* the look-back kernel's results in three flag-free passes */
 #define SN_SCAN_KERNEL_FUSED       4   /* the same results in one launch that reads a and b once, a
                                           carry chain per column running beside the tiles (forward scans;
-                                          T < 1024, or more than (2 SMs - 17 columns) / 17 columns, runs
+                                          T < 1024, or B * ceil(N / 32) above about SMs / 9, runs
                                           reduce-then-scan) */
 
 /* Operation ids for sn_workspace_bytes(). */
@@ -197,8 +197,8 @@ sn_status sn_ctx_get_option(SnCtx* ctx, int32_t key, int32_t* value);
  * same bits as the single-precision definition at every t, so splitting a
  * sequence into segments and carrying s_final -> s0 reproduces the full run
  * bit for bit ([P1] §4).  For few channels and long T the call chunks T
- * instead: automatically the fused path where B * ceil(N / 32) >= 2 and the
- * workspace covers it, else reduce-then-scan; or, by SN_OPT_SCAN_KERNEL, any
+ * instead: automatically the fused path where the workspace covers it, else
+ * reduce-then-scan; or, by SN_OPT_SCAN_KERNEL, any
  * of those two or the decoupled look-back kernel; all three give the same
  * bits, are deterministic and are bit-exact under splits at multiples of
  * SN_OPT_LOOKBACK_CHUNK.  Calls may be captured in a CUDA graph and replayed:

@@ -365,11 +365,10 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
         kernel = (few && T >= 8 * LB_TC && lookback_supported(x) && ctx->ws != nullptr && ctx->ws_bytes >= need)
                      ? SN_SCAN_KERNEL_REDUCE_SCAN
                      : SN_SCAN_KERNEL_SEQUENTIAL;
-        // the same results in two launches (the chain inside the state pass)
-        // where there are two columns of channel tiles or more and the
-        // workspace covers the fused path's arrays
-        if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN && (int64_t)B * ((N + 31) / 32) >= 2 && scan_fused_applies(T) &&
-            ctx->ws_bytes >= need_fused)
+        // the same results in one launch that reads a and b once, where the
+        // workspace covers the fused path's words (it measured faster than
+        // reduce-then-scan at one column of channel tiles and at eight)
+        if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN && scan_fused_applies(T) && ctx->ws_bytes >= need_fused)
             kernel = SN_SCAN_KERNEL_FUSED;
     }
     DeviceGuard g(ctx->device);
