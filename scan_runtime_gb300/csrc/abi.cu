@@ -374,6 +374,15 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
     DeviceGuard g(ctx->device);
     if (!g.ok) return SN_E_DEVICE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kernel == SN_SCAN_KERNEL_LOOKBACK || kernel == SN_SCAN_KERNEL_FUSED) {
+        // The launch epoch wraps after 2^29 - 1 launches, when a tag could meet
+        // a stale word of the same value: the tagged words are cleared long
+        // before, every 2^24 tagged launches.
+        if (++ctx->tagged_calls >= (uint64_t(1) << 24)) {
+            ctx->ws_dirty = true;
+            ctx->tagged_calls = 1;
+        }
+    }
     if (kernel == SN_SCAN_KERNEL_LOOKBACK) {
         const int64_t nflags = lookback_flag_count(B, T, N);
         if (ctx->ws_dirty || nflags != ctx->lb_last_flags) {

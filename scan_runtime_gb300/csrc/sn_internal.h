@@ -38,6 +38,7 @@ struct SnCtx {
     bool ws_dirty;              // flag area must be cleared before next use
     int64_t lb_last_flags;      // layout of the tagged flags last cleared: the look-back kernel's flag
                                 // count, or minus the fused path's tile count
+    uint64_t tagged_calls;      // look-back and fused launches since the tagged words were last cleared
     // options
     int scan_kernel;
     int wait_limit_us;
