@@ -17,7 +17,7 @@
 //   chunk_state   one CTA per chunk: dS_n^T = V^T Khat with Khat_j = k_j
 //                 2^{lam_{C-1} - lam_j} (one tcgen05 product, M = dv), the chunk
 //                 decay gamma_n = 2^{lam_{C-1}} and the anchor factor below;
-//   chunk_carry   one thread per state entry: S_{n+1} = gamma_n S_n + dS_n over
+//   chunk_carry   one thread per four entries of a state column: S_{n+1} = gamma_n S_n + dS_n over
 //                 the chunks in order (fp32 FMA); the operand S'_n of the chunk
 //                 (below, rounded to tf32) is written over dS_n;
 //   chunk_output  one CTA per chunk: A = Qt Kt^T masked to j <= t, P = Qt S',
@@ -592,43 +592,51 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
 // One thread per entry of a head's dv x dk state tile, in the operand layout.
 // S_0 = S_in; for each chunk: W[n] <- tf32(anc_n (.) S_n), S_{n+1} = gamma_n (.) S_n + dS_n.
 __global__ void __launch_bounds__(256) chunk_carry(const ChunkArgs a, int dv) {
+    // a thread owns four entries of the operand tile: keys i0 .. i0 + 3 of
+    // one value column, 16 contiguous bytes of every chunk's tile
     const size_t per_head = (size_t)DKC * dv;
-    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= (size_t)a.B * a.H * per_head) return;
-    const size_t bh = e / per_head;
-    const int f = (int)(e % per_head);
-    const int i = ((f >> 5) & 31) * 4 + (f & 3);        // key (K index of the operand)
+    const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (e4 >= (size_t)a.B * a.H * per_head) return;
+    const size_t bh = e4 / per_head;
+    const int f = (int)(e4 % per_head);
+    const int i0 = ((f >> 5) & 31) * 4;                 // keys i0 .. i0 + 3 (K index of the operand)
     const int col = (f >> 10) * 8 + ((f >> 2) & 7);     // value (row of the operand)
-    const size_t nat = bh * per_head + (size_t)i * dv + col;
-    float s = a.S_in != nullptr ? a.S_in[nat] : 0.f;
+    float s[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s[q] = a.S_in != nullptr ? a.S_in[bh * per_head + (size_t)(i0 + q) * dv + col] : 0.f;
     float* w = a.W + bh * a.NC * per_head + f;
-    const float* gm = a.gam + bh * a.NC * DKC + i;
-    const float* an = a.anc + bh * a.NC * DKC + i;
+    const float* gm = a.gam + bh * a.NC * DKC + i0;
+    const float* an = a.anc + bh * a.NC * DKC + i0;
     // a flagged chunk (chunk_state marks it with anchor -1) keeps its start
     // state in fp32 for the step-by-step evaluation
-    auto operand = [&](float anchor, float st, int) { return anchor < 0.f ? st : tc::to_tf32(anchor * st); };
+    auto operand = [&](float anchor, float st) { return anchor < 0.f ? st : tc::to_tf32(anchor * st); };
+    auto step = [&](float4 ds, float4 gg, float4 aa, float* out) {
+        st4(out, make_float4(operand(aa.x, s[0]), operand(aa.y, s[1]), operand(aa.z, s[2]), operand(aa.w, s[3])));
+        s[0] = fmaf(gg.x, s[0], ds.x);
+        s[1] = fmaf(gg.y, s[1], ds.y);
+        s[2] = fmaf(gg.z, s[2], ds.z);
+        s[3] = fmaf(gg.w, s[3], ds.w);
+    };
     constexpr int U = 8;
     int n = 0;
     for (; n + U <= a.NC; n += U) {
-        float ds[U], gg[U], aa[U];
+        float4 ds[U], gg[U], aa[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            ds[u] = w[(size_t)(n + u) * per_head];
-            gg[u] = __ldg(gm + (size_t)(n + u) * DKC);
-            aa[u] = __ldg(an + (size_t)(n + u) * DKC);
+            ds[u] = ld4(w + (size_t)(n + u) * per_head);
+            gg[u] = ldg4(gm + (size_t)(n + u) * DKC);
+            aa[u] = ldg4(an + (size_t)(n + u) * DKC);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            w[(size_t)(n + u) * per_head] = operand(aa[u], s, n + u);
-            s = fmaf(gg[u], s, ds[u]);
-        }
+        for (int u = 0; u < U; ++u) step(ds[u], gg[u], aa[u], w + (size_t)(n + u) * per_head);
     }
-    for (; n < a.NC; ++n) {
-        const float ds = w[(size_t)n * per_head];
-        w[(size_t)n * per_head] = operand(__ldg(an + (size_t)n * DKC), s, n);
-        s = fmaf(__ldg(gm + (size_t)n * DKC), s, ds);
+    for (; n < a.NC; ++n)
+        step(ld4(w + (size_t)n * per_head), ldg4(gm + (size_t)n * DKC), ldg4(an + (size_t)n * DKC),
+             w + (size_t)n * per_head);
+    if (a.S_out != nullptr) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) a.S_out[bh * per_head + (size_t)(i0 + q) * dv + col] = s[q];
     }
-    if (a.S_out != nullptr) a.S_out[nat] = s;
 }
 
 // ------------------------------------------------------------------ flagged chunks
@@ -1439,7 +1447,7 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t entries = (size_t)a.B * a.H * DKC * DV;
-    chunk_carry<<<(unsigned)((entries + 255) / 256), 256, 0, s>>>(a, DV);
+    chunk_carry<<<(unsigned)((entries / 4 + 255) / 256), 256, 0, s>>>(a, DV);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if constexpr (HEADS) {
