@@ -415,7 +415,11 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
             ctx->ws_dirty = false;
             ctx->lb_last_flags = sig;
         }
-        return from_cuda(launch_scan_fused(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s));
+        bool fell_back = false;
+        const cudaError_t e = launch_scan_fused(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s,
+                                                &fell_back);
+        if (fell_back) ctx->ws_dirty = true;   // reduce-then-scan's arrays overwrote the tagged words
+        return from_cuda(e);
     }
     if (kernel == SN_SCAN_KERNEL_REDUCE_SCAN) {
         ctx->ws_dirty = true;   // its carries overwrite the look-back's carry words

@@ -453,7 +453,8 @@ void scan_fused_tag_area(int B, int T, int N, int64_t* a, int64_t* b) {
 }
 
 cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
-                              int sm_count, cudaStream_t stream) {
+                              int sm_count, cudaStream_t stream, bool* fell_back) {
+    *fell_back = false;
     CUtensorMap ma, mb;
     if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, LB_NC, LB_TC) ||
         !make_scan_map(&mb, x.b, x.B, x.T, x.N, LB_NC, LB_TC))
@@ -489,8 +490,10 @@ cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStat
     // aggregate out, and the carry needs those up to FU_PB - 2 chunks of its
     // column further on: more columns than that covers (or a grid without
     // room for them) take the reduce-then-scan launches, which give the same bits.
-    if (nw < 1 || (nw < p.ntiles && nw <= (int64_t)(FU_PB + 1) * p.nbcb))
+    if (nw < 1 || (nw < p.ntiles && nw <= (int64_t)(FU_PB + 1) * p.nbcb)) {
+        *fell_back = true;   // the caller's tagged area now holds the other path's arrays
         return launch_scan_reduce_scan(x, gated, ws, st, wait_ns, sm_count, stream);
+    }
     void* args[] = {(void*)&ma, (void*)&mb, (void*)&p};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(LB_THREADS), args, FU_SMEM, stream);
     if (e != cudaSuccess) return e;
