@@ -1130,6 +1130,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     uint64_t* barS = reinterpret_cast<uint64_t*>(base + L::misc_off);
     uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc_off + 2);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc_off + 4);
+    uint64_t* barO = reinterpret_cast<uint64_t*>(base + L::misc_off + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nhb = a.H / hb;
@@ -1143,10 +1144,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     const size_t tile_floats = (size_t)DV * DKC;
     auto tile = [&](int h) { return a.W + (((size_t)b * a.H + h) * a.NC + n) * tile_floats; };
 
-    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (warp == 0) tc::tmem_alloc(slot, 512);
     if (tid == 0) {
         mbar_init(barS, 1);
         mbar_init(barM, 1);
+        mbar_init(barO, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(barS, DV * DKC * 4);
         bulk_load(bufS, tile(h0), DV * DKC * 4, barS);
@@ -1237,7 +1239,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     bool ok = __syncthreads_and(mbar_wait(barS, 0, a.wait_ns));
     tc::fence_after_sync();
     const uint32_t tmem = *slot;
-    constexpr uint32_t COL_P = 128, COL_O = 128 + DV;   // tensor-memory columns: A, P, O
+    constexpr uint32_t COL_P = 128, COL_O = 128 + 2 * DV;   // tensor-memory columns: A, P[2], O[2]
     if (!ok) {
         if (tid == 0) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
@@ -1252,14 +1254,49 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     const int lq = warp & 3, hf = warp >> 2;
     const int t = 32 * lq + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    // head hi's state and value products go to P[hi & 1] and O[hi & 1], so
+    // that head hi's output product runs while head hi - 1's epilogue reads
+    // its own pair
+    auto col_p = [&](int hi) { return COL_P + (uint32_t)(hi & 1) * DV; };
+    auto col_o = [&](int hi) { return COL_O + (uint32_t)(hi & 1) * DV; };
+    float fp_prev = 0.f;   // 2^{lam_t} of the previous head (its epilogue's factor)
+    auto epilogue = [&](int hi, float fp) {   // o of head h0 + hi from its P and O
+        const bool store = t < nval && a.o != nullptr;
+        float* orow = a.o + (row0 + t) * a.H * DV + (size_t)(h0 + hi) * DV;
+#pragma unroll
+        for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
+            float pv[16], x[16];
+            tc::ld16(lane_base + col_p(hi) + c0, pv);
+            tc::ld16(lane_base + col_o(hi) + c0, x);
+            if (store) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st_cs(reinterpret_cast<float4*>(orow + c0 + 4 * q),
+                          make_float4(a.scale * fmaf(fp, pv[4 * q], x[4 * q]),
+                                      a.scale * fmaf(fp, pv[4 * q + 1], x[4 * q + 1]),
+                                      a.scale * fmaf(fp, pv[4 * q + 2], x[4 * q + 2]),
+                                      a.scale * fmaf(fp, pv[4 * q + 3], x[4 * q + 3])));
+            }
+        }
+    };
     uint32_t mpar = 0;
+    int last = -1;    // the last head whose output product was issued
+    int o_done = 0;   // output products waited for (barO phases)
     for (int hi = 0; hi < hb && ok; ++hi) {
         const int h = h0 + hi;
         const float* lam = lam2 + (hi & 1) * CH;
         const float* omh = om2 + (hi & 1) * CH;
         if (warp == 0 && hi + 1 < hb) head_d(h + 1);
-        ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
+        // this head's Q K^T (first head) and P are complete; so is the previous
+        // head's output product, which read the A and v^T buffers
+        bool w = mbar_wait(barM, mpar, a.wait_ns);
         mpar ^= 1;
+        if (hi > 0) {
+            const bool wo = __syncthreads_and(mbar_wait(barO, (uint32_t)o_done & 1u, a.wait_ns));
+            if (wo) ++o_done;
+            w = w && wo;
+        }
+        ok = __syncthreads_and(w);
         tc::fence_after_sync();
         if (!ok) {
             if (tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT1);
@@ -1292,41 +1329,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
         __syncthreads();
         tc::fence_after_sync();
         if (tid == 0) {
-            tc::gemm_tf32(tmem + COL_O, bufA, bufV, CH, tc::idesc_tf32(128, DV), false);
-            tc::commit(barM);
+            tc::gemm_tf32(tmem + col_o(hi), bufA, bufV, CH, tc::idesc_tf32(128, DV), false);
+            tc::commit(barO);
         }
-        if (hi + 1 < hb) {   // next head's v and decay sums while the product runs
+        last = hi;
+        if (hi > 0) epilogue(hi - 1, fp_prev);   // while this head's output product runs
+        fp_prev = ex2(lt);
+        if (hi + 1 < hb) {   // next head's v and decay sums, then its P once its S' tile is in
             load_v(h + 1);
             if (warp == 0) head_lam(lam2 + ((hi + 1) & 1) * CH);
-        }
-        ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
-        mpar ^= 1;
-        tc::fence_after_sync();
-        if (!ok) {
-            if (tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
-            break;
-        }
-        {
-            const float fp = ex2(lt);
-            const bool store = t < nval && a.o != nullptr;
-            float* orow = a.o + (row0 + t) * a.H * DV + (size_t)h * DV;
-#pragma unroll
-            for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
-                float p[16], x[16];
-                tc::ld16(lane_base + COL_P + c0, p);
-                tc::ld16(lane_base + COL_O + c0, x);
-                if (store) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_cs(reinterpret_cast<float4*>(orow + c0 + 4 * q),
-                              make_float4(a.scale * fmaf(fp, p[4 * q], x[4 * q]),
-                                          a.scale * fmaf(fp, p[4 * q + 1], x[4 * q + 1]),
-                                          a.scale * fmaf(fp, p[4 * q + 2], x[4 * q + 2]),
-                                          a.scale * fmaf(fp, p[4 * q + 3], x[4 * q + 3])));
-                }
-            }
-        }
-        if (hi + 1 < hb) {
             tc::fence_before_sync();
             ok = __syncthreads_and(mbar_wait(barS, (hi + 1) & 1, a.wait_ns));
             tc::fence_after_sync();
@@ -1337,15 +1348,23 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
                 }
                 break;
             }
-            if (tid == 0) {
-                tc::gemm_tf32(tmem + COL_P, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);
+            if (tid == 0) {   // P[(hi + 1) & 1] was read by the epilogue above
+                tc::gemm_tf32(tmem + col_p(hi + 1), bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);
                 tc::commit(barM);
             }
         }
     }
+    if (last >= o_done) {
+        // the last head's output product, then its epilogue; on an error the
+        // wait only drains the tensor pipe before the CTA frees its memory
+        const bool w = __syncthreads_and(mbar_wait(barO, (uint32_t)o_done & 1u, a.wait_ns));
+        tc::fence_after_sync();
+        if (ok && w) epilogue(last, fp_prev);
+        if (!w && tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
+    }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // Heads per CTA of the heads kernels (one CTA per SM each): a CTA costs its
