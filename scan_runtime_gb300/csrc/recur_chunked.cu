@@ -1309,12 +1309,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
         const float lt = lam[t];
 #pragma unroll
         for (int j0 = 64 * hf; j0 < 64 * hf + 64; j0 += 16) {
-            float x[16];
+            if (j0 > 32 * lq + 31) {   // above the diagonal for the whole warp: zeros
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st4(bufA + off128(t, j0 + 4 * q), make_float4(0.f, 0.f, 0.f, 0.f));
+                continue;
+            }
+            float x[16], lj[16], wj[16];
             tc::ld16(lane_base + j0, x);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int j = j0 + jj;
-                x[jj] *= j <= t ? ex2(lt - lam[j]) * omh[j] : 0.f;
+            for (int q = 0; q < 4; ++q) {   // the block's decay sums and weights, broadcast to the warp
+                const float4 l4 = ld4(lam + j0 + 4 * q), w4 = ld4(omh + j0 + 4 * q);
+                lj[4 * q] = l4.x; lj[4 * q + 1] = l4.y; lj[4 * q + 2] = l4.z; lj[4 * q + 3] = l4.w;
+                wj[4 * q] = w4.x; wj[4 * q + 1] = w4.y; wj[4 * q + 2] = w4.z; wj[4 * q + 3] = w4.w;
+            }
+            if (j0 + 15 <= 32 * lq) {   // below the diagonal for the whole warp
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) x[jj] *= ex2(lt - lj[jj]) * wj[jj];
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) x[jj] *= j0 + jj <= t ? ex2(lt - lj[jj]) * wj[jj] : 0.f;
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
