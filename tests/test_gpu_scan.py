@@ -284,6 +284,25 @@ def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
     assert _nrel(ro0, z64) <= TOL and _nrel(rf0, zf64) <= TOL
 
 
+@pytest.mark.parametrize("form", ["fma", "gated"])
+def test_fused_optional_outputs_match_reduce_scan(sr, ctx, form):
+    """The fused path without s0 (zeros), and with the final state alone (no
+    s_out), gives the reduce-then-scan path's bits."""
+    B, T, N = 1, 40000, 64
+    ctx.ensure_workspace(B, T, N)
+    a, b, u, _ = _inputs(B, T, N, 43)
+    rhs = b if form == "fma" else u
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+    ro, rf = _run(ctx, form, a, rhs, None)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_FUSED)
+    fo, ff = _run(ctx, form, a, rhs, None)
+    fnone, fonly = _run(ctx, form, a, rhs, None, s_out=False)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+    assert ctx.last_error() == sr.SN_OK
+    assert np.array_equal(fo, ro) and np.array_equal(ff, rf)
+    assert fnone is None and np.array_equal(fonly, rf)
+
+
 def test_reduce_scan_optional_outputs_and_split(sr, ctx):
     tc = ctx.get_option(sr.SN_OPT_LOOKBACK_CHUNK)
     B, T, N = 2, 300 * tc + 9, 64
