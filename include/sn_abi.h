@@ -102,7 +102,7 @@ typedef int32_t sn_status;
 #define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back,
                                       3 chunked reduce-then-scan, 4 chunked fused (forward scans) */
 #define SN_OPT_WAIT_LIMIT_US    2  /* bound on any device-side wait, microseconds (default 1e6) */
-#define SN_OPT_DEBUG_POISON     3  /* 1: look-back waits for a flag no chunk publishes (tests the bound) */
+#define SN_OPT_DEBUG_POISON     3  /* 1: the look-back and fused kernels wait for a word no CTA writes (tests the bound) */
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
 #define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
 #define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA

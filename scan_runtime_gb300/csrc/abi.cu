@@ -416,8 +416,8 @@ static sn_status scan_common(SnCtx* ctx, int32_t B, int32_t T, int32_t N, const 
             ctx->lb_last_flags = sig;
         }
         bool fell_back = false;
-        const cudaError_t e = launch_scan_fused(x, gated, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, s,
-                                                &fell_back);
+        const cudaError_t e = launch_scan_fused(x, gated, ctx->ws, ctx->debug_poison, ctx->dstatus, wait_ns(ctx),
+                                                ctx->sm_count, s, &fell_back);
         if (fell_back) ctx->ws_dirty = true;   // reduce-then-scan's arrays overwrote the tagged words
         return from_cuda(e);
     }

@@ -70,6 +70,7 @@ struct FusedParams {
     unsigned long long* cw0;      // [col][channel]: the same for the initial carry
     SnDevStatus* st;              // error word, abort tag and the launch epoch
     uint64_t wait_ns;
+    int poison;                   // 1: state tiles wait for a carry state no CTA writes (tests the bound)
 };
 
 __device__ __forceinline__ void st_relaxed_gpu_v2u64(unsigned long long* p, unsigned long long a,
@@ -287,7 +288,7 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
     const int ni = w < p.ntiles ? (p.ntiles - 1 - w) / nw + 1 : 0;   // tiles w, w + nw, ... (chunk order)
     const int nm = (p.nchunks + 7) >> 3;
     const unsigned long long hi_a = (unsigned long long)(L.tag | FU_AGG) << 32;
-    const unsigned long long hi_c = (unsigned long long)(L.tag | FU_CARRY) << 32;
+    const unsigned long long hi_c = (unsigned long long)(L.tag | (p.poison ? 1u : FU_CARRY)) << 32;
     float* bufs = reinterpret_cast<float*>(smem);
     auto coords = [&](int i, int& k, int& bi, int& cb) {
         const int ti = w + i * nw;
@@ -452,8 +453,8 @@ void scan_fused_tag_area(int B, int T, int N, int64_t* a, int64_t* b) {
     *b = fused_layout(B, T, N).total;
 }
 
-cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
-                              int sm_count, cudaStream_t stream, bool* fell_back) {
+cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,
+                              uint64_t wait_ns, int sm_count, cudaStream_t stream, bool* fell_back) {
     *fell_back = false;
     CUtensorMap ma, mb;
     if (!make_scan_map(&ma, x.a, x.B, x.T, x.N, LB_NC, LB_TC) ||
@@ -477,6 +478,7 @@ cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStat
     p.cw0 = reinterpret_cast<unsigned long long*>(base + l.cw0);
     p.st = st;
     p.wait_ns = wait_ns;
+    p.poison = poison;
 
     auto kern = gated ? scan_fused<true> : scan_fused<false>;
     int occ = 0;

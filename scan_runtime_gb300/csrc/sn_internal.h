@@ -128,8 +128,8 @@ int64_t scan_fused_ws_bytes(int B, int T, int N);
 void scan_fused_tag_area(int B, int T, int N, int64_t* a, int64_t* b);
 // *fell_back is set when the launch ran the reduce-then-scan launches instead
 // (too many columns for the fused path's progress rule).
-cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, SnDevStatus* st, uint64_t wait_ns,
-                              int sm_count, cudaStream_t stream, bool* fell_back);
+cudaError_t launch_scan_fused(const ScanArgs& x, bool gated, void* ws, int poison, SnDevStatus* st,
+                              uint64_t wait_ns, int sm_count, cudaStream_t stream, bool* fell_back);
 
 enum RecurKind : int {
     RK_DIAG_KEY = 0,

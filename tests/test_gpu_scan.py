@@ -284,6 +284,27 @@ def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
     assert _nrel(ro0, z64) <= TOL and _nrel(rf0, zf64) <= TOL
 
 
+def test_fused_bounded_wait_reports_timeout(sr, lbctx):
+    """The fused kernel's state tiles wait for a carry state no CTA writes:
+    the first wait runs out after the limit, the others stop at the abort,
+    the kernel returns and the context reports SN_E_TIMEOUT once; the next
+    call works."""
+    B, T, N = 1, 40000, 64
+    lbctx.ensure_workspace(B, T, N)
+    lbctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_FUSED)
+    lbctx.set_option(sr.SN_OPT_WAIT_LIMIT_US, 2000)
+    lbctx.set_option(sr.SN_OPT_DEBUG_POISON, 1)
+    a, b, _, s0 = _inputs(B, T, N, 10)
+    _run(lbctx, "fma", a, b, s0)
+    assert lbctx.last_error() == sr.SN_E_TIMEOUT
+    assert lbctx.last_error() == sr.SN_OK             # cleared
+    lbctx.set_option(sr.SN_OPT_DEBUG_POISON, 0)
+    so, sf = _run(lbctx, "fma", a, b, s0)              # context still usable
+    assert lbctx.last_error() == sr.SN_OK
+    r64, f64 = _ref("fma", a, b, s0, "f64")
+    assert _nrel(so, r64) <= TOL and _nrel(sf, f64) <= TOL
+
+
 @pytest.mark.parametrize("form", ["fma", "gated"])
 def test_fused_optional_outputs_match_reduce_scan(sr, ctx, form):
     """The fused path without s0 (zeros), and with the final state alone (no
