@@ -158,27 +158,103 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append(dict(ts=ts, sm=float(parts[1]), max=float(parts[2]), hw=parts[5], hwt=parts[6],
-                                 swt=parts[7], pcap=parts[8]))
+                rows.append(dict(ts=ts, sm=float(parts[1]), max=float(parts[2]),
+                                 hw=parts[5].lower() == "active", hwt=parts[6].lower() == "active",
+                                 swt=parts[7].lower() == "active", pcap=parts[8].lower() == "active"))
             except ValueError:
                 continue
-        if not rows:
-            return None
-        inwin = [r for r in rows if self.t_on and self.t_off and self.t_on <= r["ts"] <= self.t_off]
-        # a timed region shorter than the sampling period may hold no sample:
-        # then the samples within 0.1 s of it (warm-up and the region itself
-        # keep the GPU loaded), else all
-        near = [r for r in rows if self.t_on and self.t_off and self.t_on - 0.1 <= r["ts"] <= self.t_off + 0.1]
-        use = inwin or near or rows
-        reasons = []
-        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
-                          ("pcap", "sw_power_cap")):
-            if any(r[key].lower() == "active" for r in use):
-                reasons.append(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in use),
-                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inwin),
-                "within_0.1s_of_timed_region": bool(inwin or near),
-                "timed_region_ms": round((self.t_off - self.t_on) * 1e3, 1) if self.t_on and self.t_off else None}
+        return clock_summary(rows, self.t_on, self.t_off, "nvidia-smi, 20 ms")
+
+
+def clock_summary(rows, t_on, t_off, source):
+    """Median SM clock, its maximum and the throttle reasons seen, from the
+    samples inside the timed region [t_on, t_off] (else those within 0.1 s of
+    it, when the region is shorter than the sampling period, else all)."""
+    if not rows:
+        return None
+    inwin = [r for r in rows if t_on and t_off and t_on <= r["ts"] <= t_off]
+    near = [r for r in rows if t_on and t_off and t_on - 0.1 <= r["ts"] <= t_off + 0.1]
+    use = inwin or near or rows
+    reasons = [name for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                                      ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap"))
+               if any(r[key] for r in use)]
+    return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in use),
+            "reasons": reasons, "samples": len(use), "in_timed_region": bool(inwin),
+            "within_0.1s_of_timed_region": bool(inwin or near),
+            "timed_region_ms": round((t_off - t_on) * 1e3, 1) if t_on and t_off else None, "source": source}
+
+
+class NvmlClockSampler:
+    """The same record read in-process through NVML (read-only queries, by
+    ctypes) every PERIOD_S, so that samples fall inside a timed region of a
+    few milliseconds.  The device is found by the UUID CUDA reports for it."""
+    PERIOD_S = 0.002
+    # clock-event reason bits of NVML's current-clocks query
+    BITS = {"pcap": 0x4, "hw": 0x8, "swt": 0x20, "hwt": 0x40}
+
+    def __init__(self, torch, cuda_index):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML device with the CUDA device's UUID")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if self.reasons_fn is None:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.lib = lib
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) != 0:   # 1: the SM clock
+            raise OSError("max clock query failed")
+        self.max = float(mx.value)
+        self.rows = []
+        self.t_on = self.t_off = None
+        self.stop_flag = False
+        self.thread = None
+
+    def _sample(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) != 0 or \
+                self.reasons_fn(self.h, ct.byref(rs)) != 0:
+            return
+        r = dict(ts=time.time(), sm=float(clk.value), max=self.max)
+        r.update({k: bool(rs.value & bit) for k, bit in self.BITS.items()})
+        self.rows.append(r)
+
+    def _loop(self):
+        while not self.stop_flag:
+            self._sample()
+            time.sleep(self.PERIOD_S)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def mark(self, on):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        self.stop_flag = True
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        return clock_summary(self.rows, self.t_on, self.t_off, f"NVML, {self.PERIOD_S * 1e3:g} ms")
+
+
+def make_clock_sampler(torch, cuda_index, smi_index):
+    """The in-process NVML sampler, else the nvidia-smi one."""
+    try:
+        return NvmlClockSampler(torch, cuda_index)
+    except (OSError, AttributeError, TypeError, ValueError):
+        return ClockSampler(smi_index)
 
 
 # ---------------------------------------------------------------- CPU oracle record
@@ -933,7 +1009,7 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clk = ClockSampler(local)
+    clk = make_clock_sampler(torch, torch.cuda.current_device(), local)
     clk.start()
     time.sleep(0.3)
     if world > 1:
