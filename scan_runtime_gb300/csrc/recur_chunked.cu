@@ -52,6 +52,8 @@
 // Shared-memory operands use the K-major no-swizzle core-matrix layout of
 // tc.cuh with K extent 128 (every contraction here has K = 128: keys, or the
 // chunk's tokens).
+#include <type_traits>
+
 #include "chunk_common.cuh"
 
 namespace sn {
@@ -591,51 +593,66 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
 // ------------------------------------------------------------------ chunk_carry
 // One thread per entry of a head's dv x dk state tile, in the operand layout.
 // S_0 = S_in; for each chunk: W[n] <- tf32(anc_n (.) S_n), S_{n+1} = gamma_n (.) S_n + dS_n.
+// V entries per thread: keys i0 .. i0 + V - 1 of one value column, 4 V
+// contiguous bytes of every chunk's tile (V = 4 where the grid still fills
+// the GPU, else V = 1 for more threads to hide the load latency).
+template <int V>
 __global__ void __launch_bounds__(256) chunk_carry(const ChunkArgs a, int dv) {
-    // a thread owns four entries of the operand tile: keys i0 .. i0 + 3 of
-    // one value column, 16 contiguous bytes of every chunk's tile
+    static_assert(V == 1 || V == 4, "one entry or a 16-byte group");
+    using vec = typename std::conditional<V == 4, float4, float>::type;
     const size_t per_head = (size_t)DKC * dv;
-    const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (e4 >= (size_t)a.B * a.H * per_head) return;
-    const size_t bh = e4 / per_head;
-    const int f = (int)(e4 % per_head);
-    const int i0 = ((f >> 5) & 31) * 4;                 // keys i0 .. i0 + 3 (K index of the operand)
+    const size_t ev = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * V;
+    if (ev >= (size_t)a.B * a.H * per_head) return;
+    const size_t bh = ev / per_head;
+    const int f = (int)(ev % per_head);
+    const int i0 = ((f >> 5) & 31) * 4 + (f & 3);       // first key (K index of the operand)
     const int col = (f >> 10) * 8 + ((f >> 2) & 7);     // value (row of the operand)
-    float s[4];
+    float s[V];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) s[q] = a.S_in != nullptr ? a.S_in[bh * per_head + (size_t)(i0 + q) * dv + col] : 0.f;
+    for (int q = 0; q < V; ++q) s[q] = a.S_in != nullptr ? a.S_in[bh * per_head + (size_t)(i0 + q) * dv + col] : 0.f;
     float* w = a.W + bh * a.NC * per_head + f;
     const float* gm = a.gam + bh * a.NC * DKC + i0;
     const float* an = a.anc + bh * a.NC * DKC + i0;
+    auto ld = [](const float* p) -> vec {
+        if constexpr (V == 4) return ld4(p); else return *p;
+    };
+    auto ldg = [](const float* p) -> vec {
+        if constexpr (V == 4) return ldg4(p); else return __ldg(p);
+    };
     // a flagged chunk (chunk_state marks it with anchor -1) keeps its start
     // state in fp32 for the step-by-step evaluation
     auto operand = [&](float anchor, float st) { return anchor < 0.f ? st : tc::to_tf32(anchor * st); };
-    auto step = [&](float4 ds, float4 gg, float4 aa, float* out) {
-        st4(out, make_float4(operand(aa.x, s[0]), operand(aa.y, s[1]), operand(aa.z, s[2]), operand(aa.w, s[3])));
-        s[0] = fmaf(gg.x, s[0], ds.x);
-        s[1] = fmaf(gg.y, s[1], ds.y);
-        s[2] = fmaf(gg.z, s[2], ds.z);
-        s[3] = fmaf(gg.w, s[3], ds.w);
+    auto step = [&](vec ds, vec gg, vec aa, float* out) {
+        if constexpr (V == 4) {
+            st4(out, make_float4(operand(aa.x, s[0]), operand(aa.y, s[1]), operand(aa.z, s[2]), operand(aa.w, s[3])));
+            s[0] = fmaf(gg.x, s[0], ds.x);
+            s[1] = fmaf(gg.y, s[1], ds.y);
+            s[2] = fmaf(gg.z, s[2], ds.z);
+            s[3] = fmaf(gg.w, s[3], ds.w);
+        } else {
+            *out = operand(aa, s[0]);
+            s[0] = fmaf(gg, s[0], ds);
+        }
     };
     constexpr int U = 8;
     int n = 0;
     for (; n + U <= a.NC; n += U) {
-        float4 ds[U], gg[U], aa[U];
+        vec ds[U], gg[U], aa[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            ds[u] = ld4(w + (size_t)(n + u) * per_head);
-            gg[u] = ldg4(gm + (size_t)(n + u) * DKC);
-            aa[u] = ldg4(an + (size_t)(n + u) * DKC);
+            ds[u] = ld(w + (size_t)(n + u) * per_head);
+            gg[u] = ldg(gm + (size_t)(n + u) * DKC);
+            aa[u] = ldg(an + (size_t)(n + u) * DKC);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) step(ds[u], gg[u], aa[u], w + (size_t)(n + u) * per_head);
     }
     for (; n < a.NC; ++n)
-        step(ld4(w + (size_t)n * per_head), ldg4(gm + (size_t)n * DKC), ldg4(an + (size_t)n * DKC),
+        step(ld(w + (size_t)n * per_head), ldg(gm + (size_t)n * DKC), ldg(an + (size_t)n * DKC),
              w + (size_t)n * per_head);
     if (a.S_out != nullptr) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) a.S_out[bh * per_head + (size_t)(i0 + q) * dv + col] = s[q];
+        for (int q = 0; q < V; ++q) a.S_out[bh * per_head + (size_t)(i0 + q) * dv + col] = s[q];
     }
 }
 
@@ -1479,7 +1496,10 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t entries = (size_t)a.B * a.H * DKC * DV;
-    chunk_carry<<<(unsigned)((entries / 4 + 255) / 256), 256, 0, s>>>(a, DV);
+    if ((int64_t)(entries / 4 + 255) / 256 >= 4 * (int64_t)sm_count)   // four CTAs per SM with 16-byte groups
+        chunk_carry<4><<<(unsigned)((entries / 4 + 255) / 256), 256, 0, s>>>(a, DV);
+    else
+        chunk_carry<1><<<(unsigned)((entries + 255) / 256), 256, 0, s>>>(a, DV);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if constexpr (HEADS) {

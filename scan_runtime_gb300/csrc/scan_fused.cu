@@ -277,7 +277,7 @@ scan_fused(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CU
             if (!chain_poll(p, L, blockIdx.x, warp - 2, lane, ring, full, empty) && lane == 0) L.give_up(9);
             return;
         }
-        if (warp == 1) return;
+        if (warp == 1) return;   // (no part in a chain)
         if (!chain_fold(p, L, blockIdx.x, lane, ring, full, empty) && lane == 0) L.give_up(5);
         if (lane == 0) L.finish();
         return;
