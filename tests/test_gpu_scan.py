@@ -284,6 +284,31 @@ def test_reduce_scan_matches_lookback_bit_for_bit(sr, ctx, form, shape):
     assert _nrel(ro0, z64) <= TOL and _nrel(rf0, zf64) <= TOL
 
 
+def test_fused_random_shapes_repeated_bit_equal(sr, ctx):
+    """Seeded shapes across the fused path's regimes (one to several columns,
+    ragged T and N, with and without s0, both forms), each run three times in
+    a row: every run gives the reduce-then-scan bits (the carries are read
+    through tagged words with no fence, so a race would show as a
+    difference)."""
+    rng = np.random.default_rng(2024)
+    for case in range(10):
+        B = int(rng.integers(1, 4))
+        N = int(rng.integers(1, 41)) * 4
+        T = int(rng.integers(1024, 90000))
+        form = "fma" if case % 2 == 0 else "gated"
+        ctx.ensure_workspace(B, T, N)
+        a, b, u, s0 = _inputs(B, T, N, 500 + case)
+        rhs = b if form == "fma" else u
+        s0 = s0 if case % 3 else None
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_REDUCE_SCAN)
+        ro, rf = _run(ctx, form, a, rhs, s0)
+        ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_FUSED)
+        for _ in range(3):
+            fo, ff = _run(ctx, form, a, rhs, s0)
+            assert np.array_equal(fo, ro) and np.array_equal(ff, rf), (B, T, N, form)
+    ctx.set_option(sr.SN_OPT_SCAN_KERNEL, sr.SN_SCAN_KERNEL_AUTO)
+
+
 def test_fused_bounded_wait_reports_timeout(sr, lbctx):
     """The fused kernel's state tiles wait for a carry state no CTA writes:
     the first wait runs out after the limit, the others stop at the abort,
