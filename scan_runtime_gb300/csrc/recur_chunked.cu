@@ -1116,11 +1116,13 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
 
 // ------------------------------------------------------------------ chunk_output_heads
 // Per-head decays where several heads share q and k (Mamba-2's groups): one
-// CTA per (batch, chunk, block of hb heads of one group).  Q K^T does not
-// depend on the head, so the CTA forms it once in tensor memory and, head by
-// head, weights a copy of it with that head's decays, then adds the head's
-// state and value products.  The next head's S' tile, v slice and decay sums
-// are fetched while the current head's products run.  dv = 64.
+// CTA per SM, each taking an even share of the (batch, chunk, group, head)
+// items as one or more segments of consecutive heads of one (batch, chunk,
+// group).  Q K^T does not depend on the head, so a segment forms it once in
+// tensor memory and, head by head, weights a copy of it with that head's
+// decays, then adds the head's state and value products.  The next head's S'
+// tile, v slice and decay sums are fetched while the current head's products
+// run.  dv = 64.
 template <int DV>
 struct HeadsSmem {
     static constexpr int q_off = 0;                  // Q (tf32)
@@ -1134,7 +1136,7 @@ struct HeadsSmem {
 };
 
 template <int DV>
-__global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, int hb) {
+__global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     using L = HeadsSmem<DV>;
     float* base = align128(smem_raw);
@@ -1150,16 +1152,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     uint64_t* barO = reinterpret_cast<uint64_t*>(base + L::misc_off + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nhb = a.H / hb;
-    const int hblk = blockIdx.x % nhb;
-    const int bn = blockIdx.x / nhb;
-    const int n = bn % a.NC, b = bn / a.NC;
-    const int h0 = hblk * hb;
-    const int g = h0 / (a.H / a.G);
-    const int t0 = n * CH, nval = min(CH, a.T - t0);
-    const size_t row0 = (size_t)b * a.T + t0;
+    // The CTA's share of the (batch, chunk, group, head) items, in that order:
+    // segments of consecutive heads of one (batch, chunk, group) each.
+    const int hpg = a.H / a.G;
+    const int64_t total = (int64_t)a.B * a.NC * a.G * hpg;
+    int64_t it = (int64_t)blockIdx.x * total / gridDim.x;
+    const int64_t it_end = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
     const size_t tile_floats = (size_t)DV * DKC;
-    auto tile = [&](int h) { return a.W + (((size_t)b * a.H + h) * a.NC + n) * tile_floats; };
 
     if (warp == 0) tc::tmem_alloc(slot, 512);
     if (tid == 0) {
@@ -1167,10 +1166,30 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
         mbar_init(barM, 1);
         mbar_init(barO, 1);
         fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    uint32_t ps = 0, pm = 0, po = 0;   // phases of barS, barM and barO waited for
+    int o_pending = 0;                 // output products issued and not yet waited for
+    bool ok = true;
+    while (ok && it < it_end) {
+    const int64_t pair = it / hpg;
+    const int hin = (int)(it % hpg);
+    const int hb = (int)std::min<int64_t>(hpg - hin, it_end - it);   // heads h0 .. h0 + hb - 1
+    it += hb;
+    const int g = (int)(pair % a.G);
+    const int64_t bn = pair / a.G;
+    const int n = (int)(bn % a.NC), b = (int)(bn / a.NC);
+    const int h0 = g * hpg + hin;
+    const int t0 = n * CH, nval = min(CH, a.T - t0);
+    const size_t row0 = (size_t)b * a.T + t0;
+    auto tile = [&](int h) { return a.W + (((size_t)b * a.H + h) * a.NC + n) * tile_floats; };
+    if (tid == 0) {
         mbar_arrive_expect_tx(barS, DV * DKC * 4);
         bulk_load(bufS, tile(h0), DV * DKC * 4, barS);
     }
-    __syncthreads();
 
     // q, k rows straight into the operand layout
     {
@@ -1253,16 +1272,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
-    bool ok = __syncthreads_and(mbar_wait(barS, 0, a.wait_ns));
+    ok = __syncthreads_and(mbar_wait(barS, ps & 1u, a.wait_ns));
     tc::fence_after_sync();
-    const uint32_t tmem = *slot;
     constexpr uint32_t COL_P = 128, COL_O = 128 + 2 * DV;   // tensor-memory columns: A, P[2], O[2]
     if (!ok) {
         if (tid == 0) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
-            mbar_wait(barS, 0, a.wait_ns);
+            mbar_wait(barS, ps & 1u, a.wait_ns);   // the copy in flight lands before the CTA leaves
         }
-    } else if (tid == 0) {
+        break;
+    }
+    ++ps;
+    if (tid == 0) {
         tc::gemm_tf32(tmem, bufQ, bufA, DKC, tc::idesc_tf32(128, 128), false);        // Q K^T
         tc::gemm_tf32(tmem + COL_P, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false); // P of the first head
         tc::commit(barM);
@@ -1296,9 +1317,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
             }
         }
     };
-    uint32_t mpar = 0;
-    int last = -1;    // the last head whose output product was issued
-    int o_done = 0;   // output products waited for (barO phases)
+    int last = -1;    // the last head of the segment whose output product was issued
     for (int hi = 0; hi < hb && ok; ++hi) {
         const int h = h0 + hi;
         const float* lam = lam2 + (hi & 1) * CH;
@@ -1306,11 +1325,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
         if (warp == 0 && hi + 1 < hb) head_d(h + 1);
         // this head's Q K^T (first head) and P are complete; so is the previous
         // head's output product, which read the A and v^T buffers
-        bool w = mbar_wait(barM, mpar, a.wait_ns);
-        mpar ^= 1;
+        bool w = mbar_wait(barM, pm & 1u, a.wait_ns);
+        ++pm;
         if (hi > 0) {
-            const bool wo = __syncthreads_and(mbar_wait(barO, (uint32_t)o_done & 1u, a.wait_ns));
-            if (wo) ++o_done;
+            const bool wo = __syncthreads_and(mbar_wait(barO, po & 1u, a.wait_ns));
+            if (wo) {
+                ++po;
+                --o_pending;
+            }
             w = w && wo;
         }
         ok = __syncthreads_and(w);
@@ -1362,6 +1384,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
             tc::gemm_tf32(tmem + col_o(hi), bufA, bufV, CH, tc::idesc_tf32(128, DV), false);
             tc::commit(barO);
         }
+        ++o_pending;
         last = hi;
         if (hi > 0) epilogue(hi - 1, fp_prev);   // while this head's output product runs
         fp_prev = ex2(lt);
@@ -1369,29 +1392,38 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a, i
             load_v(h + 1);
             if (warp == 0) head_lam(lam2 + ((hi + 1) & 1) * CH);
             tc::fence_before_sync();
-            ok = __syncthreads_and(mbar_wait(barS, (hi + 1) & 1, a.wait_ns));
+            ok = __syncthreads_and(mbar_wait(barS, ps & 1u, a.wait_ns));
             tc::fence_after_sync();
             if (!ok) {
                 if (tid == 0) {
                     record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
-                    mbar_wait(barS, (hi + 1) & 1, a.wait_ns);
+                    mbar_wait(barS, ps & 1u, a.wait_ns);
                 }
                 break;
             }
+            ++ps;
             if (tid == 0) {   // P[(hi + 1) & 1] was read by the epilogue above
                 tc::gemm_tf32(tmem + col_p(hi + 1), bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);
                 tc::commit(barM);
             }
         }
     }
-    if (last >= o_done) {
-        // the last head's output product, then its epilogue; on an error the
-        // wait only drains the tensor pipe before the CTA frees its memory
-        const bool w = __syncthreads_and(mbar_wait(barO, (uint32_t)o_done & 1u, a.wait_ns));
+    if (o_pending > 0) {
+        // the segment's last output product, then its epilogue; on an error
+        // the wait only drains the tensor pipe before the CTA frees its memory
+        const bool w = __syncthreads_and(mbar_wait(barO, po & 1u, a.wait_ns));
         tc::fence_after_sync();
+        if (w) {
+            ++po;
+            --o_pending;
+        }
         if (ok && w) epilogue(last, fp_prev);
-        if (!w && tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
+        if (!w) {
+            if (tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT2);
+            ok = false;
+        }
     }
+    }   // segments
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
@@ -1503,8 +1535,9 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if constexpr (HEADS) {
-        const int hb = heads_per_cta(a, sm_count);
-        chunk_output_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, out_bytes, s>>>(a, hb);
+        // the (batch, chunk, group, head) items spread evenly over one CTA per SM
+        const int64_t items = (int64_t)a.B * a.NC * a.H;
+        chunk_output_heads<DV><<<(unsigned)std::min<int64_t>(items, sm_count), NT, out_bytes, s>>>(a);
     } else {
         CUtensorMap mq, mk;
         if (!make_qk_maps(a, &mq, &mk)) return cudaErrorInvalidValue;
