@@ -386,8 +386,9 @@ chunk_state_key(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 // Per-head decays with heads sharing k (Mamba-2's groups): the token weight
 // 2^{mu_t} is a scalar per token, so it is applied to v instead of k,
 // dS^T = (v (.) 2^{mu})^T k, and the transposed k tile is the same for every
-// head of the group.  One CTA per (batch, chunk, block of hb heads of one
-// group).  k and the heads' v tiles arrive by TMA in their natural
+// head of the group.  One CTA per SM, each taking an even share of the
+// (batch, chunk, group, head) items as segments of consecutive heads of one
+// (batch, chunk, group).  k and the heads' v tiles arrive by TMA in their natural
 // [token][feature] layout (rows past T read as zeros) and the threads
 // transpose them: k once, into the operand layout; each head's v tile,
 // scaled by its token weights and rounded, into one of two operand buffers,
@@ -409,7 +410,7 @@ struct StateHeadsSmem {
 template <int DV>
 __global__ void __launch_bounds__(NT, 1)
 chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                  const ChunkArgs a, int hb) {
+                  const ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     using L = StateHeadsSmem<DV>;
     float* base = align128(smem_raw);
@@ -426,32 +427,51 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     auto vop = [&](int q) { return base + L::v_off + q * DV * CH; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nhb = a.H / hb;
-    const int hblk = blockIdx.x % nhb;
-    const int bn = blockIdx.x / nhb;
-    const int n = bn % a.NC, b = bn / a.NC;
-    const int h0 = hblk * hb;
-    const int g = h0 / (a.H / a.G);
-    const int t0 = n * CH, nval = min(CH, a.T - t0);
-    const size_t row0 = (size_t)b * a.T + t0;
+    // The CTA's share of the (batch, chunk, group, head) items, in that order,
+    // as segments of consecutive heads of one (batch, chunk, group).  Heads
+    // are counted across segments (q): v staging half, operand buffer and
+    // barrier phases follow that count.
+    const int hpg = a.H / a.G;
+    const int64_t total = (int64_t)a.B * a.NC * a.G * hpg;
+    int64_t it = (int64_t)blockIdx.x * total / gridDim.x;
+    const int64_t it_end = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
 
     if (warp == 0) tc::tmem_alloc(slot, DKC);
     if (tid == 0) {
         for (int q = 0; q < 4; ++q) mbar_init(&bk[q], 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bk, OPF * 4);
-        tma_load_3d(Sg, &map_k, bk, g * DKC, t0, b);
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *slot;
-    auto issue_v = [&](int hi) {   // thread 0: head h0 + hi's v tile into staging half hi & 1
-        mbar_arrive_expect_tx(&bv[hi & 1], DV * CH * 4);
-        tma_load_3d(stg(hi & 1), &map_v, &bv[hi & 1], (h0 + hi) * DV, t0, b);
+    int v_issued = 0;   // thread 0's count of v tiles requested (all segments)
+    int v_used = 0;     // v tiles waited for (all segments)
+    int seg = 0;        // segments begun (k tiles requested)
+    bool ok = true;
+    int site = SITE_STATE_WAIT;
+    while (ok && it < it_end) {
+    const int64_t pair = it / hpg;
+    const int hin = (int)(it % hpg);
+    const int hb = (int)std::min<int64_t>(hpg - hin, it_end - it);   // heads h0 .. h0 + hb - 1
+    it += hb;
+    const int g = (int)(pair % a.G);
+    const int64_t bn = pair / a.G;
+    const int n = (int)(bn % a.NC), b = (int)(bn / a.NC);
+    const int h0 = g * hpg + hin;
+    const int t0 = n * CH, nval = min(CH, a.T - t0);
+    const size_t row0 = (size_t)b * a.T + t0;
+    const int q0 = v_used;   // the segment's first head in the CTA's count
+    if (tid == 0) {
+        fence_proxy_async_smem();   // the previous segment's reads of the staging area before this copy
+        mbar_arrive_expect_tx(bk, OPF * 4);
+        tma_load_3d(Sg, &map_k, bk, g * DKC, t0, b);
+    }
+    ++seg;
+    auto issue_v = [&](int q) {   // thread 0: the segment's head q - q0 v tile into staging half q & 1
+        mbar_arrive_expect_tx(&bv[q & 1], DV * CH * 4);
+        tma_load_3d(stg(q & 1), &map_v, &bv[q & 1], (h0 + q - q0) * DV, t0, b);
     };
-    int v_issued = 0;   // thread 0's count of v tiles requested
-    int v_used = 0;     // v tiles waited for
     // warp 0: a head's decays, four tokens per lane, loaded a head ahead of
     // their suffix sums so that the load latency hides behind the other work
     float dr[4];
@@ -465,8 +485,7 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     if (warp == 0) head_d(h0);
 
     // k^T, rounded: thread (key i, half of the tokens) reads its column
-    bool ok = __syncthreads_and(mbar_wait(bk, 0, a.wait_ns));
-    int site = SITE_STATE_WAIT;
+    ok = __syncthreads_and(mbar_wait(bk, (uint32_t)(seg - 1) & 1u, a.wait_ns));
     if (ok) {
         const int i = tid & (DKC - 1), tb0 = (CH / 2) * (tid >> 7);
         float kr[CH / 2];
@@ -475,14 +494,14 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
         __syncthreads();                                // the staging area is read: the v tiles go there
         if (tid == 0) {
             fence_proxy_async_smem();                   // those reads before the copies' writes
-            for (; v_issued < min(2, hb); ++v_issued) issue_v(v_issued);
+            for (; v_issued < q0 + min(2, hb); ++v_issued) issue_v(v_issued);
         }
 #pragma unroll
         for (int t4 = 0; t4 < CH / 8; ++t4)
             st4(Ks + off128(i, tb0 + 4 * t4), tf32x4(kr[4 * t4], kr[4 * t4 + 1], kr[4 * t4 + 2], kr[4 * t4 + 3]));
     }
     for (int hi = 0; hi < hb && ok; ++hi) {
-        const int h = h0 + hi, p = hi & 1;
+        const int h = h0 + hi, q = q0 + hi, p = q & 1;
         // the bulk copy out of two heads ago has read operand buffer p
         if (tid == 0) bulk_wait_read_allbut1();
         if (warp == 0) {
@@ -513,9 +532,9 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
                 if (!isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
             }
         }
-        ok = __syncthreads_and(mbar_wait(&bv[p], (uint32_t)(hi >> 1) & 1u, a.wait_ns));
+        ok = __syncthreads_and(mbar_wait(&bv[p], (uint32_t)(q >> 1) & 1u, a.wait_ns));
         if (!ok) break;
-        v_used = hi + 1;
+        v_used = q + 1;
         {
             // (v^T (.) 2^{mu_t}), rounded, into operand buffer p: thread = value
             // column j, a run of TPV tokens (a float4 of the operand holds four)
@@ -540,9 +559,9 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
             // dS^T (M = dv rows value, N = dk columns key) = (v 2^mu)^T (K = t) x k^T (K = t)
             tc::gemm_tf32(tmem, vop(p), Ks, CH, tc::idesc_tf32(DV, DKC), false);
             tc::commit(bm);
-            if (v_issued < hb) issue_v(v_issued++);     // two heads ahead, into the half just read
+            if (v_issued < q0 + hb) issue_v(v_issued++);   // two heads ahead, into the half just read
         }
-        ok = __syncthreads_and(mbar_wait(bm, (uint32_t)hi & 1u, a.wait_ns));
+        ok = __syncthreads_and(mbar_wait(bm, (uint32_t)q & 1u, a.wait_ns));
         tc::fence_after_sync();
         if (!ok) break;
         {
@@ -576,11 +595,12 @@ chunk_state_heads(const __grid_constant__ CUtensorMap map_k, const __grid_consta
             }
         }
     }
+    }   // segments
     if (tid == 0) {
         if (!ok) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
             // the tiles still in flight land before the CTA leaves
-            (void)mbar_wait(bk, 0, a.wait_ns);
+            if (seg > 0) (void)mbar_wait(bk, (uint32_t)(seg - 1) & 1u, a.wait_ns);
             for (int q = v_used; q < v_issued; ++q) (void)mbar_wait(&bv[q & 1], (uint32_t)(q >> 1) & 1u, a.wait_ns);
         }
         bulk_wait_all();
@@ -1429,27 +1449,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// Heads per CTA of the heads kernels (one CTA per SM each): a CTA costs its
-// set-up (about 1.3 heads' time in both kernels, from phase stamps) plus one
-// head after another, and CTAs run in waves of one per SM, so the block of a
-// group's heads with the fewest waves x (hb + 1.3) wins (Mamba-2's 24 heads:
-// one wave of 128 CTAs of 24 heads against three of 8).
-int heads_per_cta(const ChunkArgs& a, int sm_count) {
-    const int per_group = a.H / a.G;
-    int best = 1;
-    double best_cost = 0.0;
-    for (int hb = 1; hb <= per_group; ++hb) {
-        if (per_group % hb != 0) continue;
-        const int64_t ctas = (int64_t)a.B * a.NC * (a.H / hb);
-        const double cost = (double)((ctas + sm_count - 1) / sm_count) * (hb + 1.3);
-        if (hb == 1 || cost < best_cost) {
-            best = hb;
-            best_cost = cost;
-        }
-    }
-    return best;
-}
-
 // TMA maps of q and k for the output kernel: (B, T, G * dk) row-major, boxes
 // of 32 keys x 128 tokens, 128-byte swizzle.
 bool make_qk_maps(const ChunkArgs& a, CUtensorMap* mq, CUtensorMap* mk) {
@@ -1514,10 +1513,10 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned chunks = (unsigned)((size_t)a.B * a.H * a.NC);
     if constexpr (HEADS) {
-        const int hb = heads_per_cta(a, sm_count);
         CUtensorMap mk, mv;
         if (!make_heads_maps<DV>(a, &mk, &mv)) return cudaErrorInvalidValue;
-        chunk_state_heads<DV><<<(unsigned)((size_t)a.B * a.NC * (a.H / hb)), NT, st_bytes, s>>>(mk, mv, a, hb);
+        const int64_t items = (int64_t)a.B * a.NC * a.H;   // spread evenly over one CTA per SM
+        chunk_state_heads<DV><<<(unsigned)std::min<int64_t>(items, sm_count), NT, st_bytes, s>>>(mk, mv, a);
     } else if constexpr (PER_KEY) {
         CUtensorMap mk, md, mv;
         if (!make_natural_maps<DV>(a, &mk, &md, &mv)) return cudaErrorInvalidValue;
