@@ -84,12 +84,48 @@ struct PrepSmem {
 // sums skip X_A's and X_D's zero triangles in steps of four; the few entries
 // past the triangle that a step still touches sit in a diagonal 16 x 16 block
 // above its diagonal, where X holds exact zeros.
+// Which block of the level a thread owns: pair block at offset o, rows
+// RT rt .. RT rt + RT - 1, columns 4 ct .. 4 ct + 3.  The first product's sum
+// shortens with ct and the second's lengthens with rt, so for S = 32 and 64
+// each product has its own map (Y goes through shared memory in between): a
+// warp takes one or two adjacent values of the length-setting index, and the
+// warps sharing a scheduler (w, w + 4) take complementary lengths.  Each
+// output's sum keeps its order, so the map does not change the results.
+template <int S>
+__device__ __forceinline__ void level_map(int tid, bool by_rows, int& o, int& rt, int& ct) {
+    constexpr int NCT = S / 4;
+    const int w = tid >> 5, lane = tid & 31;
+    if constexpr (S == 64) {   // one pair block; a warp: one pair of the length-setting index x 16
+        const int kp = w < 4 ? w : 11 - w;
+        const int key = 2 * kp + (lane >> 4), other = lane & 15;
+        o = 0;
+        rt = by_rows ? key : other;
+        ct = by_rows ? other : key;
+    } else if constexpr (S == 32) {   // two pair blocks
+        if (!by_rows) {   // a warp: one pair of column groups x 16 row groups of one pair block
+            const int kp = w < 4 ? w : 7 - w;
+            ct = 2 * kp + (lane >> 4);
+            rt = lane & 15;
+            o = w < 4 ? 0 : 2 * S;
+        } else {          // a half warp: one pair of row groups x 8 column groups of one pair block
+            const int kp = w < 4 ? w : 11 - w;
+            rt = 2 * kp + ((lane >> 3) & 1);
+            ct = lane & 7;
+            o = 2 * S * (lane >> 4);
+        }
+    } else {
+        ct = tid % NCT;
+        rt = (tid / NCT) % 16;
+        o = 2 * S * (tid / (16 * NCT));
+    }
+}
+
 template <int S>
 __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int tid) {
-    constexpr int RT = S / 16, NCT = S / 4;
-    const int ct = tid % NCT, rt = (tid / NCT) % 16;
-    const int o = 2 * S * (tid / (16 * NCT));
-    const int r0 = RT * rt, c0 = 4 * ct;
+    constexpr int RT = S / 16;
+    int o, rt, ct;
+    level_map<S>(tid, false, o, rt, ct);
+    int r0 = RT * rt, c0 = 4 * ct;
     float acc[RT][4] = {};
     // Y[r][c] = sum_{m >= c} A[o + S + r][o + m] X[o + m][o + c]
     for (int m = c0; m < S; m += 4) {
@@ -120,6 +156,9 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
         st4(Xm + (o + r0 + j) * LDX + o + S + c0, make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
     __syncthreads();
     // X_C[r][c] = -sum_{m <= r} X[o + S + r][o + S + m] Y[m][c]
+    level_map<S>(tid, true, o, rt, ct);
+    r0 = RT * rt;
+    c0 = 4 * ct;
     float out[RT][4] = {};
     for (int m = 0; m < r0 + RT; m += 4) {
         float4 xd[RT];
