@@ -823,7 +823,8 @@ struct OutSmem {
 
 template <bool PER_KEY, int DV>
 __global__ void __launch_bounds__(NT, 1)
-chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, const ChunkArgs a) {
+chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+             const __grid_constant__ CUtensorMap map_o, const ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     using L = OutSmem<DV>;
     float* base = reinterpret_cast<float*>(smem_align<1024>(smem_raw));
@@ -876,14 +877,17 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         bulk_load(bufS, a.W + (c.bh * a.NC + c.n) * (size_t)DV * DKC, DV * DKC * 4, barS);
         ++s_loads;
     };
-    auto issue_qk = [&](const ChunkIdx& c) {   // thread 0: q and k tiles, four swizzled 32-key boxes each
+    // thread 0: the q and k tiles, four swizzled 32-key boxes each, on one
+    // barrier phase that expects both (k may be requested later than q)
+    auto issue_q = [&](const ChunkIdx& c) {
         mbar_arrive_expect_tx(barQ, 2 * OPF * 4);
 #pragma unroll
-        for (int at = 0; at < DKC / 32; ++at) {
-            tma_load_3d(bufQ + at * 4096, &map_q, barQ, c.g * DKC + 32 * at, c.t0, c.b);
-            tma_load_3d(bufK + at * 4096, &map_k, barQ, c.g * DKC + 32 * at, c.t0, c.b);
-        }
+        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(bufQ + at * 4096, &map_q, barQ, c.g * DKC + 32 * at, c.t0, c.b);
         ++q_loads;
+    };
+    auto issue_k = [&](const ChunkIdx& c) {
+#pragma unroll
+        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(bufK + at * 4096, &map_k, barQ, c.g * DKC + 32 * at, c.t0, c.b);
     };
     auto issue_v = [&](const ChunkIdx& c) {   // all threads: the v slice into registers
         if (a.vt != nullptr) return;
@@ -921,7 +925,8 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         const ChunkIdx c0 = chunk_index(a, blockIdx.x);
         if (tid == 0) {
             issue_s(c0);
-            issue_qk(c0);
+            issue_q(c0);
+            issue_k(c0);
         }
         issue_v(c0);
         issue_d(c0);
@@ -1084,27 +1089,38 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             site = SITE_OUT_WAIT2;
             break;
         }
-        // the Q and K buffers are free: the next unit's q and k stream in
-        if (has_next && tid == 0) issue_qk(cn);
-        {
+        // The Q buffer is free: the next unit's q streams in.  The unit's o
+        // tile goes through the K buffer (128-byte-swizzled 32-column boxes,
+        // written row by row without bank conflicts) and out by TMA stores,
+        // which clip the rows past T; the next unit's k follows once the
+        // stores have read it.  A flagged unit's outputs come from fix_unit.
+        if (has_next && tid == 0) issue_q(cn);
+        const bool out_unit = a.o != nullptr && !(PER_KEY && __ldg(a.bad + c.bh * a.NC + c.n) != 0);
+        if (out_unit) {
             const float fp = PER_KEY ? 1.f : ex2(lam_s[t]);
-            const bool store = t < c.nval && a.o != nullptr && !(PER_KEY && __ldg(a.bad + c.bh * a.NC + c.n) != 0);
-            float* orow = a.o + (row0 + t) * a.H * DV + (size_t)c.h * DV;
 #pragma unroll
             for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
                 float p[16], x[16];
                 tc::ld16(lane_base + 128 + c0, p);
                 tc::ld16(lane_base + c0, x);
-                if (store) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_cs(reinterpret_cast<float4*>(orow + c0 + 4 * q),
-                              make_float4(a.scale * fmaf(fp, p[4 * q], x[4 * q]),
-                                          a.scale * fmaf(fp, p[4 * q + 1], x[4 * q + 1]),
-                                          a.scale * fmaf(fp, p[4 * q + 2], x[4 * q + 2]),
-                                          a.scale * fmaf(fp, p[4 * q + 3], x[4 * q + 3])));
-                }
+                for (int q = 0; q < 4; ++q)
+                    st4(bufK + off_sw(t, c0 + 4 * q),
+                        make_float4(a.scale * fmaf(fp, p[4 * q], x[4 * q]), a.scale * fmaf(fp, p[4 * q + 1], x[4 * q + 1]),
+                                    a.scale * fmaf(fp, p[4 * q + 2], x[4 * q + 2]),
+                                    a.scale * fmaf(fp, p[4 * q + 3], x[4 * q + 3])));
             }
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            if (out_unit) {
+#pragma unroll
+                for (int at = 0; at < DV / 32; ++at) tma_store_3d(&map_o, bufK + at * 4096, c.h * DV + 32 * at, c.t0, c.b);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+            if (has_next) issue_k(cn);
         }
         // tensor memory and the per-head sums are reused by the next unit
         tc::fence_before_sync();
@@ -1458,6 +1474,18 @@ bool make_qk_maps(const ChunkArgs& a, CUtensorMap* mq, CUtensorMap* mk) {
     return encode_tiled(mq, 3, a.q, dims, strides, box, true) && encode_tiled(mk, 3, a.k, dims, strides, box, true);
 }
 
+// TMA map of o for the output kernel's stores: (B, T, H * dv) row-major,
+// boxes of 32 values x 128 tokens, 128-byte swizzle (the staging layout).
+// Without o the map is left zero: the kernel then stores nothing.
+bool make_o_map(const ChunkArgs& a, int dv, CUtensorMap* mo) {
+    *mo = CUtensorMap{};
+    if (a.o == nullptr) return true;
+    const uint64_t dims[3] = {(uint64_t)a.H * dv, (uint64_t)a.T, (uint64_t)a.B};
+    const uint64_t strides[2] = {(uint64_t)a.H * dv * 4, (uint64_t)a.T * a.H * dv * 4};
+    const uint32_t box[3] = {32, (uint32_t)CH, 1};
+    return encode_tiled(mo, 3, a.o, dims, strides, box, true);
+}
+
 // TMA maps of k, d and v for chunk_state_key: (B, T, features) row-major,
 // boxes of 128 tokens x all of a head's features (k: 128 keys of the group,
 // d: 128 keys of the head, v: dv values of the head), no swizzle.
@@ -1538,9 +1566,10 @@ cudaError_t run_chunked(const ChunkArgs& a, int sm_count, cudaStream_t s) {
         const int64_t items = (int64_t)a.B * a.NC * a.H;
         chunk_output_heads<DV><<<(unsigned)std::min<int64_t>(items, sm_count), NT, out_bytes, s>>>(a);
     } else {
-        CUtensorMap mq, mk;
-        if (!make_qk_maps(a, &mq, &mk)) return cudaErrorInvalidValue;
-        chunk_output<PER_KEY, DV><<<(unsigned)std::min<size_t>(chunks, (size_t)sm_count), NT, out_bytes, s>>>(mq, mk, a);
+        CUtensorMap mq, mk, mo;
+        if (!make_qk_maps(a, &mq, &mk) || !make_o_map(a, DV, &mo)) return cudaErrorInvalidValue;
+        chunk_output<PER_KEY, DV><<<(unsigned)std::min<size_t>(chunks, (size_t)sm_count), NT, out_bytes, s>>>(mq, mk, mo,
+                                                                                                             a);
     }
     return cudaGetLastError();
 }
@@ -1558,9 +1587,9 @@ cudaError_t chunk::launch_output_unit_decay(const ChunkArgs& a, int max_ctas, cu
     if (e != cudaSuccess) return e;
     const int nsg = a.nsg > 0 ? a.nsg : a.NC;
     const size_t units = (size_t)a.B * a.H * nsg;
-    CUtensorMap mq, mk;
-    if (!make_qk_maps(a, &mq, &mk)) return cudaErrorInvalidValue;
-    chunk_output<false, 128><<<(unsigned)std::min<size_t>(units, (size_t)max_ctas), NT, bytes, s>>>(mq, mk, a);
+    CUtensorMap mq, mk, mo;
+    if (!make_qk_maps(a, &mq, &mk) || !make_o_map(a, 128, &mo)) return cudaErrorInvalidValue;
+    chunk_output<false, 128><<<(unsigned)std::min<size_t>(units, (size_t)max_ctas), NT, bytes, s>>>(mq, mk, mo, a);
     return cudaGetLastError();
 }
 
