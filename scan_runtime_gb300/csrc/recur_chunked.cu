@@ -936,7 +936,6 @@ chunk_output(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         const ChunkIdx c = chunk_index(a, u);
         const bool has_next = u + (int)gridDim.x < units;
         const ChunkIdx cn = chunk_index(a, has_next ? u + (int)gridDim.x : u);
-        const size_t row0 = (size_t)c.b * a.T + c.t0;
         const uint32_t ph = (uint32_t)it & 1;
 
         // decay prefix sums: per key in registers (the q, k lane mapping), per head in shared memory
@@ -1168,7 +1167,8 @@ struct HeadsSmem {
     static constexpr int lam_off = v_off + DV * CH;  // [2][CH] decay prefix sums (two heads)
     static constexpr int om_off = lam_off + 2 * CH;  // [2][CH] injection weights (two heads)
     static constexpr int misc_off = om_off + 2 * CH;
-    static constexpr size_t bytes = (size_t)(misc_off + 16) * 4 + 128;
+    static constexpr int stage_off = misc_off + 16;  // [8 warps][32 rows][dv / 2] o staging
+    static constexpr size_t bytes = (size_t)(stage_off + 8 * 32 * (DV / 2)) * 4 + 128;
 };
 
 template <int DV>
@@ -1188,6 +1188,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
     uint64_t* barO = reinterpret_cast<uint64_t*>(base + L::misc_off + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* stage = base + L::stage_off + warp * 32 * (DV / 2);   // this warp's o rows
     // The CTA's share of the (batch, chunk, group, head) items, in that order:
     // segments of consecutive heads of one (batch, chunk, group) each.
     const int hpg = a.H / a.G;
@@ -1334,24 +1335,37 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
     auto col_p = [&](int hi) { return COL_P + (uint32_t)(hi & 1) * DV; };
     auto col_o = [&](int hi) { return COL_O + (uint32_t)(hi & 1) * DV; };
     float fp_prev = 0.f;   // 2^{lam_t} of the previous head (its epilogue's factor)
-    auto epilogue = [&](int hi, float fp) {   // o of head h0 + hi from its P and O
-        const bool store = t < nval && a.o != nullptr;
-        float* orow = a.o + (row0 + t) * a.H * DV + (size_t)(h0 + hi) * DV;
+    // o of head h0 + hi from its P and O.  A warp holds 32 rows x dv / 2
+    // values; it passes them through its own staging rows (16-byte slots
+    // XOR-swizzled by row, so that neither side conflicts on banks) and
+    // writes them back as whole 128-byte lines, eight lanes to a row.
+    static_assert(DV / 2 == 32, "one 128-byte line per row and warp");
+    auto epilogue = [&](int hi, float fp) {
+        if (a.o == nullptr) return;
 #pragma unroll
-        for (int c0 = hf * (DV / 2); c0 < (hf + 1) * (DV / 2); c0 += 16) {
+        for (int c = 0; c < 2; ++c) {
+            const int c0 = hf * (DV / 2) + 16 * c;
             float pv[16], x[16];
             tc::ld16(lane_base + col_p(hi) + c0, pv);
             tc::ld16(lane_base + col_o(hi) + c0, x);
-            if (store) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_cs(reinterpret_cast<float4*>(orow + c0 + 4 * q),
-                          make_float4(a.scale * fmaf(fp, pv[4 * q], x[4 * q]),
-                                      a.scale * fmaf(fp, pv[4 * q + 1], x[4 * q + 1]),
-                                      a.scale * fmaf(fp, pv[4 * q + 2], x[4 * q + 2]),
-                                      a.scale * fmaf(fp, pv[4 * q + 3], x[4 * q + 3])));
-            }
+            for (int q = 0; q < 4; ++q)
+                st4(stage + 32 * lane + 4 * ((4 * c + q) ^ (lane & 7)),
+                    make_float4(a.scale * fmaf(fp, pv[4 * q], x[4 * q]),
+                                a.scale * fmaf(fp, pv[4 * q + 1], x[4 * q + 1]),
+                                a.scale * fmaf(fp, pv[4 * q + 2], x[4 * q + 2]),
+                                a.scale * fmaf(fp, pv[4 * q + 3], x[4 * q + 3])));
         }
+        __syncwarp();
+        const size_t ors = (size_t)a.H * DV;
+        float* ob = a.o + (row0 + 32 * lq) * ors + (size_t)(h0 + hi) * DV + hf * (DV / 2) + 4 * (lane & 7);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const float4 v = ld4(stage + 32 * r + 4 * ((lane & 7) ^ (r & 7)));
+            if (32 * lq + r < nval) st_cs(reinterpret_cast<float4*>(ob + (size_t)r * ors), v);
+        }
+        __syncwarp();   // read back before the next head's epilogue writes the rows
     };
     int last = -1;    // the last head of the segment whose output product was issued
     for (int hi = 0; hi < hb && ok; ++hi) {
