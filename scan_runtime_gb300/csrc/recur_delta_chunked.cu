@@ -51,7 +51,7 @@ struct DeltaArgs {
     const float* beta;
     float* Wt;      // per chunk: W (rows t, K = key), operand layout, tf32
     float* KTt;     // per chunk: K^T (rows key, K = t), operand layout, tf32
-    float* Ut;      // per chunk: U, row-major [t][value]
+    float* Ut;      // per chunk: U, rows t of 128 values, 16-byte slots swizzled by row (off_u)
     float* DTt;     // per chunk: Delta^T (rows value, K = t), operand layout, tf32
     float* St;      // per chunk: S_n^T (rows value, K = key), operand layout, tf32
     const float* S_from;   // delta_chain: fp32 state entering chunk n0 (NULL = zeros)
@@ -59,6 +59,14 @@ struct DeltaArgs {
     SnDevStatus* st;
     uint64_t wait_ns;
 };
+
+// Float offset of U[t][i] in a chunk's U tile: rows of 128 values whose
+// 16-byte slots are XOR-swizzled by t mod 8 within each 128-byte line, so that
+// delta_prep stages a row per thread without bank conflicts and delta_chain
+// still reads a row a line at a time.
+__device__ __forceinline__ int off_u(int t, int i) {
+    return t * 128 + (i & ~31) + ((((i & 31) >> 2) ^ (t & 7)) << 2) + (i & 3);
+}
 
 // ------------------------------------------------------------------ delta_prep
 struct PrepSmem {
@@ -184,8 +192,11 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
 // Tiles by TMA: K in the 128-byte-swizzled operand layout for the Gram
 // products (four boxes of 32 keys x 128 tokens), then k and v as natural
 // [token][feature] boxes, transposed by the threads into the K^T and V^T
-// operands once the inverse is done; W leaves through shared memory by a bulk
-// copy.  Rows past T read as zeros.
+// operands once the inverse is done; W and U leave through shared memory by
+// bulk copies.  Rows past T read as zeros.  A CTA takes the units blockIdx.x,
+// blockIdx.x + gridDim.x, ... of the segment, so that a grid below the SM
+// count leaves SMs free for the kernels beside it; the next unit's K tile is
+// requested as soon as the copies out have read the buffer it lands in.
 __global__ void __launch_bounds__(NT, 1)
 delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
            const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a) {
@@ -202,14 +213,30 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
     uint64_t* barT = reinterpret_cast<uint64_t*>(base + L::misc + 6);    // the natural k and v tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % a.H;
-    const int bn = blockIdx.x / a.H;
     const int nsg = a.n1 - a.n0;
-    const int n = a.n0 + bn % nsg, b = bn / nsg;
-    const int t0 = n * CH, nval = min(CH, a.T - t0);
-    const size_t bh = (size_t)b * a.H + h;
-    const size_t row0 = (size_t)b * a.T + t0;
-    const size_t tile = (bh * a.NC + n) * (size_t)OPF;
+    const int units = a.B * a.H * nsg;   // unit ((b * nsg) + n - n0) * H + h
+    struct Unit {
+        int h, b, t0, nval;
+        size_t row0, tile;
+    };
+    auto unit = [&](int u) {
+        Unit c;
+        c.h = u % a.H;
+        const int bn = u / a.H;
+        const int n = a.n0 + bn % nsg;
+        c.b = bn / nsg;
+        c.t0 = n * CH;
+        c.nval = min(CH, a.T - c.t0);
+        c.row0 = (size_t)c.b * a.T + c.t0;
+        c.tile = (((size_t)c.b * a.H + c.h) * a.NC + n) * (size_t)OPF;
+        return c;
+    };
+    auto issue_k = [&](const Unit& c) {   // thread 0: K rows in the swizzled operand layout (rows t, K = key)
+        mbar_arrive_expect_tx(barK, OPF * 4);
+#pragma unroll
+        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(buf0 + at * 4096, &map_ks, barK, c.h * DKC + 32 * at, c.t0, c.b);
+    };
+    int k_loads = 0, t_loads = 0;   // thread 0: K tiles and k, v tile pairs requested
 
     if (warp == 0) tc::tmem_alloc(slot, 256);
     if (tid == 0) {
@@ -217,56 +244,59 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
         mbar_init(barK, 1);
         mbar_init(barT, 1);
         fence_mbar_init();
-        // K rows in the swizzled operand layout (rows t, K = key)
-        mbar_arrive_expect_tx(barK, OPF * 4);
-#pragma unroll
-        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(buf0 + at * 4096, &map_ks, barK, h * DKC + 32 * at, t0, b);
+        if ((int)blockIdx.x < units) {
+            issue_k(unit(blockIdx.x));
+            ++k_loads;
+        }
     }
-    if (tid < CH) beta_s[tid] = tid < nval ? __ldg(a.beta + (row0 + tid) * a.H + h) : 0.f;
+    tc::fence_before_sync();
     __syncthreads();   // the barriers are initialised before any thread polls them
-    bool ok = __syncthreads_and(mbar_wait(barK, 0, a.wait_ns));
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+    const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
+    const int lq = warp & 3, hf = warp >> 2;
+    const int tr = 32 * lq + lane;                           // tensor-memory row of this thread
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    bool ok = true;
     int site = SITE_PREP_WAIT1;
-    bool t_issued = false;   // thread 0: the natural k and v tiles were requested
+    for (int u = blockIdx.x, it = 0; u < units; u += gridDim.x, ++it) {
+        const Unit c = unit(u);
+        const uint32_t ph = (uint32_t)it & 1;
+        if (tid < CH) beta_s[tid] = tid < c.nval ? __ldg(a.beta + (c.row0 + tid) * a.H + c.h) : 0.f;
+        ok = __syncthreads_and(mbar_wait(barK, ph, a.wait_ns));
+        if (!ok) break;
 
-    // K = hi + lo, both tf32: K K^T ~ hi hi^T + hi lo^T + lo hi^T (elementwise,
-    // so the split keeps the swizzled layout)
-    if (ok) {
+        // K = hi + lo, both tf32: K K^T ~ hi hi^T + hi lo^T + lo hi^T (elementwise,
+        // so the split keeps the swizzled layout)
         for (int f = tid; f < OPF / 4; f += NT) {
             const float4 x = ld4(buf0 + 4 * f);
             const float4 hi = tf32x4(x);
             st4(buf0 + 4 * f, hi);
             st4(buf1 + 4 * f, tf32x4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w));
         }
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *slot;
-    if (ok && tid == 0) {
-        const uint32_t id = tc::idesc_tf32(128, 128);
-        tc::gemm_tf32_sw_sw(tmem, buf0, buf0, id, false);
-        tc::gemm_tf32_sw_sw(tmem, buf0, buf1, id, true);
-        tc::gemm_tf32_sw_sw(tmem, buf1, buf0, id, true);
-        tc::commit(bar);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(bar, 0, a.wait_ns));
-    const int tl = lane & 7, ic = 16 * warp + 4 * (lane >> 3);
-    tc::fence_after_sync();
-    const int lq = warp & 3, hf = warp >> 2;
-    const int tr = 32 * lq + lane;                           // tensor-memory row of this thread
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
-    if (ok) {
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            const uint32_t id = tc::idesc_tf32(128, 128);
+            tc::gemm_tf32_sw_sw(tmem, buf0, buf0, id, false);
+            tc::gemm_tf32_sw_sw(tmem, buf0, buf1, id, true);
+            tc::gemm_tf32_sw_sw(tmem, buf1, buf0, id, true);
+            tc::commit(bar);
+        }
+        ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
+        tc::fence_after_sync();
+        if (!ok) break;
         // the natural k and v tiles can stream in now (the Gram products have
         // read the hi and lo parts of K) while the inverse runs
         if (tid == 0) {
-            t_issued = true;
+            ++t_loads;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(barT, 2 * OPF * 4);
-            tma_load_3d(buf0, &map_kn, barT, h * DKC, t0, b);
-            tma_load_3d(buf1, &map_vn, barT, h * 128, t0, b);
+            tma_load_3d(buf0, &map_kn, barT, c.h * DKC, c.t0, c.b);
+            tma_load_3d(buf1, &map_vn, barT, c.h * 128, c.t0, c.b);
         }
-
         // A = diag(beta) strict_lower(K K^T) in fp32, stored transposed: AT[j][t] = A[t][j]
         // (zeros on and below the diagonal, where X goes next)
         float* AT = buf2;
@@ -327,8 +357,9 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
 
         // K^T and V^T, rounded, from the natural tiles: thread = feature
         // column i, a half of the tokens, through registers
-        ok = __syncthreads_and(mbar_wait(barT, 0, a.wait_ns));
-        if (ok) {
+        ok = __syncthreads_and(mbar_wait(barT, ph, a.wait_ns));
+        if (!ok) break;
+        {
             const int i = tid & 127, tb0 = (CH / 2) * (tid >> 7);
             float kr[CH / 2], vr[CH / 2];
 #pragma unroll
@@ -343,12 +374,10 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
                 st4(buf1 + off128(i, tb0 + 4 * t4), tf32x4(vr[4 * t4], vr[4 * t4 + 1], vr[4 * t4 + 2], vr[4 * t4 + 3]));
             }
         }
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (ok) {
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
         if (tid == 0) {
             const uint32_t id = tc::idesc_tf32(128, 128);
             tc::gemm_tf32(tmem, buf2, buf0, CH, id, false);          // W = T K   (cols 0..127)
@@ -357,40 +386,48 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
         }
         ok = __syncthreads_and(mbar_wait(bar, 1, a.wait_ns));
         tc::fence_after_sync();
-        if (ok) {
-            // W through shared memory (the T operand is consumed) and out by a
-            // bulk copy, with the K^T operand as it stands (tf32) for the chain
-            float* ut = a.Ut + tile;
-#pragma unroll
-            for (int i0 = 64 * hf; i0 < 64 * hf + 64; i0 += 16) {
-                float x[16];
-                tc::ld16(lane_base + i0, x);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st4(buf2 + off128(tr, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
-                tc::ld16(lane_base + 128 + i0, x);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st4(ut + tr * 128 + i0 + 4 * q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
-            }
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                bulk_store(a.Wt + tile, buf2, OPF * 4);
-                bulk_store(a.KTt + tile, buf0, OPF * 4);
-                bulk_commit();
-                bulk_wait_all();
-            }
-        } else {
+        if (!ok) {
             site = SITE_PREP_WAIT2;
+            break;
+        }
+        // W and U through shared memory (the T and V^T operands are
+        // consumed) and out by bulk copies, with the K^T operand as it
+        // stands (tf32) for the chain
+#pragma unroll
+        for (int i0 = 64 * hf; i0 < 64 * hf + 64; i0 += 16) {
+            float x[16];
+            tc::ld16(lane_base + i0, x);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st4(buf2 + off128(tr, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+            tc::ld16(lane_base + 128 + i0, x);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st4(buf1 + off_u(tr, i0 + 4 * q), make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(a.Wt + c.tile, buf2, OPF * 4);
+            bulk_store(a.KTt + c.tile, buf0, OPF * 4);
+            bulk_store(a.Ut + c.tile, buf1, OPF * 4);
+            bulk_commit();
+            if (u + (int)gridDim.x < units) {
+                bulk_wait_read_all();   // the copies out have read the buffers the next unit fills
+                issue_k(unit(u + gridDim.x));
+                ++k_loads;
+            }
         }
     }
     if (!ok && tid == 0) {
         record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
-        // the tiles still in flight land before the CTA leaves
-        (void)mbar_wait(barK, 0, a.wait_ns);
-        if (t_issued) (void)mbar_wait(barT, 0, a.wait_ns);
+        // the tiles still in flight land before the CTA leaves (a phase
+        // already waited for passes at once)
+        if (k_loads > 0) (void)mbar_wait(barK, (uint32_t)(k_loads - 1) & 1, a.wait_ns);
+        if (t_loads > 0) (void)mbar_wait(barT, (uint32_t)(t_loads - 1) & 1, a.wait_ns);
     }
+    if (tid == 0) bulk_wait_all();   // every copy out complete before the CTA exits
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -456,7 +493,7 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
     auto load_u = [&](int n) {
         const float* ut = tile(a.Ut, n);
 #pragma unroll
-        for (int r = 0; r < 64; ++r) u[r] = ut[(64 * part + r) * 128 + c];
+        for (int r = 0; r < 64; ++r) u[r] = ut[off_u(64 * part + r, c)];
     };
     put_state();
     load_u(a.n0);
@@ -566,8 +603,8 @@ bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && 
 
 // Auto: two segments when the chain (one CTA per head) leaves at least half
 // the SMs to the preparation and there are chunks enough to split; more
-// segments measured slower (each chain segment waits for SMs held by the
-// next segment's preparation, whose CTAs run about 30 us).
+// segments measured slower (each segment adds a chain launch, its setup and
+// a slower first chunk, about 15 us, to the serial path).
 int delta_segments(int NC, int BH, int sm_count, int requested) {
     int nseg = requested > 0 ? requested : (NC >= 8 && 2 * BH <= sm_count ? 2 : 1);
     nseg = std::min(nseg, NC);
@@ -625,6 +662,10 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     const int nseg = delta_segments(d.NC, x.B * x.H, sm_count, segments);
     const int len = (d.NC + nseg - 1) / nseg;
     const bool piped = nseg > 1;
+    // CTAs for a stage that runs beside a chain (one CTA per head): the SMs
+    // the chain leaves, when that is at least half of them
+    const int free_sms = sm_count - x.B * x.H;
+    const int side = 2 * free_sms >= sm_count ? free_sms : sm_count;
     if (piped && (pipe.prep == nullptr || pipe.chain == nullptr || pipe.out == nullptr || pipe.nev < 2 * nseg + 4))
         return cudaErrorInvalidValue;
     cudaStream_t sp = piped ? pipe.prep : s, sc = piped ? pipe.chain : s, so = piped ? pipe.out : s;
@@ -655,7 +696,11 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
         d.n0 = g * len;
         d.n1 = std::min(d.NC, d.n0 + len);
-        delta_prep<<<(unsigned)((size_t)x.B * x.H * (d.n1 - d.n0)), NT, PrepSmem::bytes, sp>>>(mks, mkn, mvn, d);
+        // persistent CTAs: the first segment's on every SM; a later one runs
+        // beside the chain of the segment before and leaves the chain's SMs
+        // free, so that the chain starts as soon as its inputs exist
+        const int units = x.B * x.H * (d.n1 - d.n0);
+        delta_prep<<<(unsigned)std::min(units, g > 0 ? side : sm_count), NT, PrepSmem::bytes, sp>>>(mks, mkn, mvn, d);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = order(sp, sc);
         if (e != cudaSuccess) break;
@@ -668,9 +713,9 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
         if (e != cudaSuccess) break;
         c.n0 = d.n0;
         c.nsg = d.n1 - d.n0;
-        // pipelined: one CTA per unit, so the output CTAs fill whatever SMs the other
-        // stages leave (persistent CTAs, assigned their units up front, measured slower)
-        e = launch_output_unit_decay(c, piped ? INT32_MAX : sm_count, so);
+        // persistent output CTAs; one of a segment whose successor's chain is
+        // still to run leaves that chain's SMs free as well
+        e = launch_output_unit_decay(c, g + 1 < nseg ? side : sm_count, so);
     }
     // join: the caller's stream waits for the side streams, also after an error
     for (cudaStream_t side : {sp, sc, so}) {
