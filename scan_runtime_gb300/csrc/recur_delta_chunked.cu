@@ -601,15 +601,27 @@ int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
 
 bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && x.dk == DKC && x.dv == 128; }
 
-// Auto: two segments when the chain (one CTA per head) leaves at least half
-// the SMs to the preparation and there are chunks enough to split; more
-// segments measured slower (each segment adds a chain launch, its setup and
-// a slower first chunk, about 15 us, to the serial path).
+// Auto: when the chain (one CTA per head) leaves at least half the SMs to
+// the other stages, three segments from 12 chunks on and two from 8; more
+// segments measured slower (each adds a chain launch, its setup and a slower
+// first chunk, about 15 us, to the serial path).
 int delta_segments(int NC, int BH, int sm_count, int requested) {
-    int nseg = requested > 0 ? requested : (NC >= 8 && 2 * BH <= sm_count ? 2 : 1);
+    const bool room = 2 * BH <= sm_count;
+    int nseg = requested > 0 ? requested : (room && NC >= 12 ? 3 : room && NC >= 8 ? 2 : 1);
     nseg = std::min(nseg, NC);
     const int len = (NC + nseg - 1) / nseg;
     return (NC + len - 1) / len;
+}
+
+// First chunk of segment g (g = nseg: NC).  Three segments split about
+// 5 : 7 : 4: a short first segment starts the chain early, a short last one
+// leaves little output after it, and the middle one's preparation hides
+// behind the first chain (32 chunks: 10, 14, 8, measured 3 % faster than
+// 16, 16).  Otherwise equal lengths.
+int delta_seg_start(int NC, int nseg, int g) {
+    if (g >= nseg) return NC;
+    if (nseg == 3) return g == 0 ? 0 : g == 1 ? (5 * NC + 8) / 16 : (12 * NC + 8) / 16;
+    return std::min(NC, g * ((NC + nseg - 1) / nseg));
 }
 
 // Segments of the chunk sequence run as a pipeline over three side streams:
@@ -660,7 +672,6 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     }
 
     const int nseg = delta_segments(d.NC, x.B * x.H, sm_count, segments);
-    const int len = (d.NC + nseg - 1) / nseg;
     const bool piped = nseg > 1;
     // CTAs for a stage that runs beside a chain (one CTA per head): the SMs
     // the chain leaves, when that is at least half of them
@@ -694,8 +705,8 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     c.wait_ns = wait_ns;
 
     for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
-        d.n0 = g * len;
-        d.n1 = std::min(d.NC, d.n0 + len);
+        d.n0 = delta_seg_start(d.NC, nseg, g);
+        d.n1 = delta_seg_start(d.NC, nseg, g + 1);
         // persistent CTAs: the first segment's on every SM; a later one runs
         // beside the chain of the segment before and leaves the chain's SMs
         // free, so that the chain starts as soon as its inputs exist
