@@ -1189,6 +1189,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float* stage = base + L::stage_off + warp * 32 * (DV / 2);   // this warp's o rows
+    // Warps 4 and 5 hold rows 0..63 of the right column half, above the
+    // diagonal: they weight no block of Q K^T.  Warp 4's first thread issues
+    // the products and copies (an issue of 16 products can stall it for a
+    // while), warp 5 loads the decays and forms their sums, so that neither
+    // delays the warps that weight the blocks.
+    constexpr int DWARP = 5;
+    const bool issuer = tid == 128;
     // The CTA's share of the (batch, chunk, group, head) items, in that order:
     // segments of consecutive heads of one (batch, chunk, group) each.
     const int hpg = a.H / a.G;
@@ -1223,7 +1230,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
     const int t0 = n * CH, nval = min(CH, a.T - t0);
     const size_t row0 = (size_t)b * a.T + t0;
     auto tile = [&](int h) { return a.W + (((size_t)b * a.H + h) * a.NC + n) * tile_floats; };
-    if (tid == 0) {
+    if (issuer) {
         mbar_arrive_expect_tx(barS, DV * DKC * 4);
         bulk_load(bufS, tile(h0), DV * DKC * 4, barS);
     }
@@ -1257,7 +1264,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
             vr[r] = t < nval ? __ldg(vcol + (size_t)t * vrs) : 0.f;
         }
     };
-    // warp 0: a head's decays, four tokens per lane, loaded one step ahead of
+    // warp DWARP: a head's decays, four tokens per lane, loaded one step ahead of
     // their prefix sums so that the load latency hides behind other work
     float dr[4];
     auto head_d = [&](int h) {
@@ -1267,7 +1274,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
             dr[r] = (t < nval && a.d != nullptr) ? __ldg(a.d + (row0 + t) * a.H + h) : 1.f;
         }
     };
-    // warp 0: inclusive prefix sums of log2 d of the loaded head into dst, and
+    // warp DWARP: inclusive prefix sums of log2 d of the loaded head into dst, and
     // the keys' injection weights (1 - d when gated) into dst + (om2 - lam2)
     auto head_lam = [&](float* dst) {
         float lg[4], s = 0.f;
@@ -1292,7 +1299,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
         if (lane == 31 && !isfinite(x)) record_error(a.st, SN_E_RANGE, (SN_K_RECUR_CHUNK << 16) | SITE_RANGE_HEAD);
     };
     load_v(h0);
-    if (warp == 0) {
+    if (warp == DWARP) {
         head_d(h0);
         head_lam(lam2);
     }
@@ -1313,14 +1320,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
     tc::fence_after_sync();
     constexpr uint32_t COL_P = 128, COL_O = 128 + 2 * DV;   // tensor-memory columns: A, P[2], O[2]
     if (!ok) {
-        if (tid == 0) {
+        if (issuer) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
             mbar_wait(barS, ps & 1u, a.wait_ns);   // the copy in flight lands before the CTA leaves
         }
         break;
     }
     ++ps;
-    if (tid == 0) {
+    if (issuer) {
         tc::gemm_tf32(tmem, bufQ, bufA, DKC, tc::idesc_tf32(128, 128), false);        // Q K^T
         tc::gemm_tf32(tmem + COL_P, bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false); // P of the first head
         tc::commit(barM);
@@ -1372,7 +1379,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
         const int h = h0 + hi;
         const float* lam = lam2 + (hi & 1) * CH;
         const float* omh = om2 + (hi & 1) * CH;
-        if (warp == 0 && hi + 1 < hb) head_d(h + 1);
+        if (warp == DWARP && hi + 1 < hb) head_d(h + 1);
         // this head's Q K^T (first head) and P are complete; so is the previous
         // head's output product, which read the A and v^T buffers
         bool w = mbar_wait(barM, pm & 1u, a.wait_ns);
@@ -1391,7 +1398,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
             if (tid == 0) record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_WAIT1);
             break;
         }
-        if (tid == 0 && hi + 1 < hb) {   // the S' buffer is free again
+        if (issuer && hi + 1 < hb) {   // the S' buffer is free again
             mbar_arrive_expect_tx(barS, DV * DKC * 4);
             bulk_load(bufS, tile(h + 1), DV * DKC * 4, barS);
         }
@@ -1430,7 +1437,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (tid == 0) {
+        if (issuer) {
             tc::gemm_tf32(tmem + col_o(hi), bufA, bufV, CH, tc::idesc_tf32(128, DV), false);
             tc::commit(barO);
         }
@@ -1440,19 +1447,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_output_heads(const ChunkArgs a) {
         fp_prev = ex2(lt);
         if (hi + 1 < hb) {   // next head's v and decay sums, then its P once its S' tile is in
             load_v(h + 1);
-            if (warp == 0) head_lam(lam2 + ((hi + 1) & 1) * CH);
+            if (warp == DWARP) head_lam(lam2 + ((hi + 1) & 1) * CH);
             tc::fence_before_sync();
             ok = __syncthreads_and(mbar_wait(barS, ps & 1u, a.wait_ns));
             tc::fence_after_sync();
             if (!ok) {
-                if (tid == 0) {
+                if (issuer) {
                     record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_COPY);
                     mbar_wait(barS, ps & 1u, a.wait_ns);
                 }
                 break;
             }
             ++ps;
-            if (tid == 0) {   // P[(hi + 1) & 1] was read by the epilogue above
+            if (issuer) {   // P[(hi + 1) & 1] was read by the epilogue above
                 tc::gemm_tf32(tmem + col_p(hi + 1), bufQ, bufS, DKC, tc::idesc_tf32(128, DV), false);
                 tc::commit(barM);
             }
