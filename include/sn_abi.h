@@ -102,15 +102,18 @@ typedef int32_t sn_status;
 #define SN_OPT_SCAN_KERNEL      1  /* 0 auto (default), 1 sequential-in-T, 2 chunked look-back,
                                       3 chunked reduce-then-scan, 4 chunked fused (forward scans) */
 #define SN_OPT_WAIT_LIMIT_US    2  /* bound on any device-side wait, microseconds (default 1e6) */
-#define SN_OPT_DEBUG_POISON     3  /* 1: the look-back and fused kernels wait for a word no CTA writes (tests the bound) */
+#define SN_OPT_DEBUG_POISON     3  /* 1: the look-back and fused scan kernels and the fused delta-rule kernel wait for a word no CTA writes (tests the bound) */
 #define SN_OPT_LOOKBACK_CHUNK   4  /* read-only: time steps per look-back chunk */
 #define SN_OPT_RECUR_KERNEL     5  /* 0 auto (default: T == 1 uses decode), 1 always the sequence kernel */
 #define SN_OPT_RECUR_TILE       6  /* sequence kernel: 0 auto (default), or 2, 4, 8 consumer warps per CTA
                                       (the same bits for every width); a width whose CTA columns the value
                                       dimension does not divide would fail with SN_E_INVAL before any
                                       launch (no compiled tile and head size has such a width) */
-#define SN_OPT_DELTA_SEGMENTS   7  /* sn_recur_delta_chunked: 0 auto (default), or 1..8 segments of the
-                                      chunk sequence run as a pipeline (same bits for every value) */
+#define SN_OPT_DELTA_SEGMENTS   7  /* sn_recur_delta_chunked: 0 auto (default): one cooperative launch of
+                                      the preparation and the chains, then the output stage, where the
+                                      chains (one CTA per head and batch row) leave at least half the SMs,
+                                      else a segmented pipeline; or 1..8 segments of the chunk sequence run
+                                      as a pipeline (same bits for every value) */
 
 #define SN_SCAN_KERNEL_AUTO       0
 #define SN_SCAN_KERNEL_SEQUENTIAL 1
@@ -391,10 +394,14 @@ int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_
  * = 128 (else SN_E_UNSUPPORTED), 16-byte aligned pointers and a context
  * workspace of at least sn_recur_delta_chunked_workspace_bytes() bytes (else
  * SN_E_NOMEM), which the call overwrites.
- * Streams: for more than a few chunks the call splits the sequence into
- * segments (SN_OPT_DELTA_SEGMENTS) and runs the chain of one segment beside
- * the preparation of the next on side streams the context created with it
- * (sn_ctx_create); the call itself creates no stream or event.  The
+ * Streams: by default (SN_OPT_DELTA_SEGMENTS 0, with B*H at most half the
+ * SMs) the call runs on `stream` alone: one cooperative launch whose chains
+ * wait, bounded, for the preparation of each chunk (SN_E_TIMEOUT past
+ * SN_OPT_WAIT_LIMIT_US), then the output stage.  Otherwise, for more than a
+ * few chunks, it splits the sequence into segments and runs the chain of one
+ * segment beside the preparation of the next on side streams the context
+ * created with it (sn_ctx_create); the call itself creates no stream or
+ * event.  The
  * side streams wait for `stream`'s earlier work and `stream` waits for them
  * before its later work, so to the caller the call is ordered on `stream`
  * like any other (also under stream capture).  A context is not for use from
@@ -407,8 +414,9 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
 
 /* Workspace bytes sn_recur_delta_chunked needs: five tiles of dk x dv floats
  * per chunk of 128 tokens and head (W, K^T, U, the chunk state and the
- * chunk's deltas) plus one fp32 dk x dv state per head (carried between
- * segments), each kind rounded up to 256 bytes; -1 on invalid arguments. */
+ * chunk's deltas), one fp32 dk x dv state per head (carried between
+ * segments) and 4 * (1 + B * H * chunks) bytes of control words, each kind
+ * rounded up to 256 bytes; -1 on invalid arguments. */
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* ---------------------------------------------------------------- readout epilogues */

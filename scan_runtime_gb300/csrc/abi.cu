@@ -713,8 +713,8 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H, in
     if (!g.ok) return SN_E_DEVICE;
     ctx->ws_dirty = true;   // the chunk tiles overwrite the look-back flag area
     const DeltaPipe pipe{ctx->pipe_prep, ctx->pipe_chain, ctx->pipe_out, ctx->pipe_ev, 20};
-    return from_cuda(launch_delta_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, ctx->delta_segments, pipe,
-                                          reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_delta_chunked(x, ctx->ws, ctx->dstatus, wait_ns(ctx), ctx->sm_count, ctx->delta_segments,
+                                          ctx->debug_poison != 0, pipe, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {

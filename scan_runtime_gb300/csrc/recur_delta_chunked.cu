@@ -58,6 +58,7 @@ struct DeltaArgs {
     float* S_to;           // delta_chain: fp32 state after chunk n1 - 1 (NULL = not written)
     SnDevStatus* st;
     uint64_t wait_ns;
+    int poison;            // fused kernel: the chains wait for a ready value no CTA writes (tests the bound)
 };
 
 // Float offset of U[t][i] in a chunk's U tile: rows of 128 values whose
@@ -193,13 +194,17 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
 // products (four boxes of 32 keys x 128 tokens), then k and v as natural
 // [token][feature] boxes, transposed by the threads into the K^T and V^T
 // operands once the inverse is done; W and U leave through shared memory by
-// bulk copies.  Rows past T read as zeros.  A CTA takes the units blockIdx.x,
-// blockIdx.x + gridDim.x, ... of the segment, so that a grid below the SM
-// count leaves SMs free for the kernels beside it; the next unit's K tile is
-// requested as soon as the copies out have read the buffer it lands in.
-__global__ void __launch_bounds__(NT, 1)
-delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
-           const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a) {
+// bulk copies.  Rows past T read as zeros.  Units are taken chunk by chunk:
+// unit u of the segment is chunk n0 + u / (B H) of head-batch u mod (B H).
+// Without a queue a CTA takes the units blockIdx.x, blockIdx.x + gridDim.x,
+// ..., so that a grid below the SM count leaves SMs free for the kernels
+// beside it; with one (the fused kernel) thread 0 claims units from it, and
+// once a unit's tiles are written it sets the unit's ready word.  The next
+// unit's K tile is requested as soon as the copies out have read the buffer
+// it lands in.
+__device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUtensorMap* map_kn,
+                                          const CUtensorMap* map_vn, const DeltaArgs& a, unsigned* queue,
+                                          unsigned* ready) {
     extern __shared__ unsigned char smem_raw[];
     using L = PrepSmem;
     float* base = reinterpret_cast<float*>(smem_align<1024>(smem_raw));
@@ -211,30 +216,38 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 2);
     uint64_t* barK = reinterpret_cast<uint64_t*>(base + L::misc + 4);    // the swizzled K tile
     uint64_t* barT = reinterpret_cast<uint64_t*>(base + L::misc + 6);    // the natural k and v tiles
+    int* s_next = reinterpret_cast<int*>(base + L::misc + 8);            // the next unit (thread 0 writes)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nsg = a.n1 - a.n0;
-    const int units = a.B * a.H * nsg;   // unit ((b * nsg) + n - n0) * H + h
+    const int BH = a.B * a.H;
+    const int units = BH * (a.n1 - a.n0);
     struct Unit {
         int h, b, t0, nval;
-        size_t row0, tile;
+        size_t row0, tile, word;
     };
     auto unit = [&](int u) {
         Unit c;
-        c.h = u % a.H;
-        const int bn = u / a.H;
-        const int n = a.n0 + bn % nsg;
-        c.b = bn / nsg;
+        const int bh = u % BH, n = a.n0 + u / BH;
+        c.h = bh % a.H;
+        c.b = bh / a.H;
         c.t0 = n * CH;
         c.nval = min(CH, a.T - c.t0);
         c.row0 = (size_t)c.b * a.T + c.t0;
-        c.tile = (((size_t)c.b * a.H + c.h) * a.NC + n) * (size_t)OPF;
+        c.word = (size_t)bh * a.NC + n;
+        c.tile = c.word * (size_t)OPF;
         return c;
+    };
+    auto next_unit = [&](int u) -> int {   // thread 0
+        if (queue != nullptr) {
+            const unsigned v = atomicAdd(queue, 1u);
+            return v < (unsigned)units ? (int)v : -1;
+        }
+        return u + (int)gridDim.x < units ? u + (int)gridDim.x : -1;
     };
     auto issue_k = [&](const Unit& c) {   // thread 0: K rows in the swizzled operand layout (rows t, K = key)
         mbar_arrive_expect_tx(barK, OPF * 4);
 #pragma unroll
-        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(buf0 + at * 4096, &map_ks, barK, c.h * DKC + 32 * at, c.t0, c.b);
+        for (int at = 0; at < DKC / 32; ++at) tma_load_3d(buf0 + at * 4096, map_ks, barK, c.h * DKC + 32 * at, c.t0, c.b);
     };
     int k_loads = 0, t_loads = 0;   // thread 0: K tiles and k, v tile pairs requested
 
@@ -244,10 +257,12 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
         mbar_init(barK, 1);
         mbar_init(barT, 1);
         fence_mbar_init();
-        if ((int)blockIdx.x < units) {
-            issue_k(unit(blockIdx.x));
+        const int u0 = queue != nullptr ? next_unit(-1) : ((int)blockIdx.x < units ? (int)blockIdx.x : -1);
+        if (u0 >= 0) {
+            issue_k(unit(u0));
             ++k_loads;
         }
+        *s_next = u0;
     }
     tc::fence_before_sync();
     __syncthreads();   // the barriers are initialised before any thread polls them
@@ -259,12 +274,13 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     bool ok = true;
     int site = SITE_PREP_WAIT1;
-    for (int u = blockIdx.x, it = 0; u < units; u += gridDim.x, ++it) {
+    for (int u = *s_next, it = 0; u >= 0; ++it) {
         const Unit c = unit(u);
         const uint32_t ph = (uint32_t)it & 1;
         if (tid < CH) beta_s[tid] = tid < c.nval ? __ldg(a.beta + (c.row0 + tid) * a.H + c.h) : 0.f;
         ok = __syncthreads_and(mbar_wait(barK, ph, a.wait_ns));
         if (!ok) break;
+        if (tid == 0) *s_next = next_unit(u);   // read by every thread at the end of the unit
 
         // K = hi + lo, both tf32: K K^T ~ hi hi^T + hi lo^T + lo hi^T (elementwise,
         // so the split keeps the swizzled layout)
@@ -294,8 +310,8 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
             ++t_loads;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(barT, 2 * OPF * 4);
-            tma_load_3d(buf0, &map_kn, barT, c.h * DKC, c.t0, c.b);
-            tma_load_3d(buf1, &map_vn, barT, c.h * 128, c.t0, c.b);
+            tma_load_3d(buf0, map_kn, barT, c.h * DKC, c.t0, c.b);
+            tma_load_3d(buf1, map_vn, barT, c.h * 128, c.t0, c.b);
         }
         // A = diag(beta) strict_lower(K K^T) in fp32, stored transposed: AT[j][t] = A[t][j]
         // (zeros on and below the diagonal, where X goes next)
@@ -413,12 +429,21 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
             bulk_store(a.KTt + c.tile, buf0, OPF * 4);
             bulk_store(a.Ut + c.tile, buf1, OPF * 4);
             bulk_commit();
-            if (u + (int)gridDim.x < units) {
+            const int un = *s_next;
+            if (un >= 0) {
                 bulk_wait_read_all();   // the copies out have read the buffers the next unit fills
-                issue_k(unit(u + gridDim.x));
+                issue_k(unit(un));
                 ++k_loads;
             }
+            if (ready != nullptr) {
+                // the tiles are written (the next K tile streams in meanwhile);
+                // then the unit's ready word, released at gpu scope
+                bulk_wait_all();
+                fence_proxy_async_global();
+                st_release_gpu(ready + c.word, 1u);
+            }
         }
+        u = *s_next;
     }
     if (!ok && tid == 0) {
         record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | site);
@@ -433,6 +458,12 @@ delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ C
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
+__global__ void __launch_bounds__(NT, 1)
+delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
+           const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a) {
+    prep_role(&map_ks, &map_kn, &map_vn, a, nullptr, nullptr);
+}
+
 // ------------------------------------------------------------------ delta_chain
 struct ChainSmem {
     static constexpr int w_off = 0;          // W_n (rows t, K = key)
@@ -442,7 +473,10 @@ struct ChainSmem {
     static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 128;
 };
 
-__global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
+// The chain of head-batch bh over chunks [n0, n1).  With ready words (the
+// fused kernel), thread 0 waits, bounded, for a chunk's word before it
+// requests the chunk's first tile.
+__device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, const unsigned* ready) {
     extern __shared__ unsigned char smem_raw[];
     using L = ChainSmem;
     float* base = align128(smem_raw);
@@ -453,13 +487,27 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
     uint64_t* barK = reinterpret_cast<uint64_t*>(base + L::misc + 2);
     uint64_t* barM = reinterpret_cast<uint64_t*>(base + L::misc + 4);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 6);
+    int* s_ok = reinterpret_cast<int*>(base + L::misc + 8);   // thread 0: the first chunk's tiles were requested
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const size_t bh = blockIdx.x;
+    const size_t bh = (size_t)bh_index;
     const int c = tid & 127, part = tid >> 7;     // value column, half of the keys / tokens
     const int lq = warp & 3;                      // tensor-memory lanes 32 lq .. : rows c
     const int NC = a.NC;
     auto tile = [&](const float* p, int n) { return p + (bh * NC + n) * (size_t)OPF; };
+    auto wait_ready = [&](int n) -> bool {   // thread 0: chunk n's W, K^T and U tiles are written
+        if (ready == nullptr) return true;
+        const uint32_t* w = ready + bh * NC + n;
+        const uint32_t want = a.poison ? 2u : 1u;   // poisoned: a value no CTA writes (tests the bound)
+        if (ld_acquire_gpu(w) != want) {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_gpu(w) != want)
+                if (global_ns() - t0 > a.wait_ns) return false;
+        }
+        fence_proxy_async_global();   // the bulk copies that follow read what the flag published
+        return true;
+    };
+    int w_loads = 0, k_loads = 0;   // bulk loads issued on barW / barK (thread 0's count)
 
     if (warp == 0) tc::tmem_alloc(slot, 256);
     if (tid == 0) {
@@ -467,10 +515,15 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         mbar_init(barK, 1);
         mbar_init(barM, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(barW, OPF * 4);
-        bulk_load(Wb, tile(a.Wt, a.n0), OPF * 4, barW);
-        mbar_arrive_expect_tx(barK, OPF * 4);
-        bulk_load(KTb, tile(a.KTt, a.n0), OPF * 4, barK);
+        const bool r0 = wait_ready(a.n0);
+        if (r0) {
+            mbar_arrive_expect_tx(barW, OPF * 4);
+            bulk_load(Wb, tile(a.Wt, a.n0), OPF * 4, barW);
+            mbar_arrive_expect_tx(barK, OPF * 4);
+            bulk_load(KTb, tile(a.KTt, a.n0), OPF * 4, barK);
+            w_loads = k_loads = 1;
+        }
+        *s_ok = r0 ? 1 : 0;
     }
 
     // S^T[c][i] for this part's 64 keys, fp32 in registers for the whole sequence
@@ -496,19 +549,18 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         for (int r = 0; r < 64; ++r) u[r] = ut[off_u(64 * part + r, c)];
     };
     put_state();
-    load_u(a.n0);
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    bool ok = *s_ok != 0;
+    if (ok) load_u(a.n0);
     if (tid == 0) store_tile(a.St, a.n0);
     const uint32_t tmem = *slot;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
     const uint32_t id = tc::idesc_tf32(128, 128);
     uint32_t mpar = 0;
-    int w_loads = 1, k_loads = 1;   // bulk loads issued on barW / barK (thread 0's count)
-    bool ok = true;
-    for (int n = a.n0; n < a.n1; ++n) {
+    for (int n = a.n0; ok && n < a.n1; ++n) {
         const uint32_t ph = (uint32_t)(n - a.n0) & 1;   // phase of this launch's n-th tile loads
         ok = __syncthreads_and(mbar_wait(barW, ph, a.wait_ns));
         if (!ok) break;
@@ -521,10 +573,14 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         mpar ^= 1;
         tc::fence_after_sync();
         if (!ok) break;
+        bool rdy = true;   // thread 0: the next chunk's tiles exist
         if (tid == 0 && n + 1 < a.n1) {
-            mbar_arrive_expect_tx(barW, OPF * 4);
-            bulk_load(Wb, tile(a.Wt, n + 1), OPF * 4, barW);
-            ++w_loads;
+            rdy = wait_ready(n + 1);
+            if (rdy) {
+                mbar_arrive_expect_tx(barW, OPF * 4);
+                bulk_load(Wb, tile(a.Wt, n + 1), OPF * 4, barW);
+                ++w_loads;
+            }
         }
         // Delta^T[c][t] = U[t][c] - P[c][t] for this part's tokens
 #pragma unroll
@@ -540,7 +596,7 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        ok = __syncthreads_and(mbar_wait(barK, ph, a.wait_ns));
+        ok = __syncthreads_and(rdy && mbar_wait(barK, ph, a.wait_ns));
         tc::fence_after_sync();
         if (!ok) break;
         if (tid == 0) {   // D[c][i] = sum_t Delta^T[c][t] K^T[i][t]  (= (K^T Delta)^T)
@@ -578,8 +634,8 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
         if (tid == 0) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_CHAIN_WAIT);
             // let copies still in flight land before the CTA exits
-            mbar_wait(barW, (w_loads - 1) & 1, a.wait_ns);
-            mbar_wait(barK, (k_loads - 1) & 1, a.wait_ns);
+            if (w_loads > 0) mbar_wait(barW, (w_loads - 1) & 1, a.wait_ns);
+            if (k_loads > 0) mbar_wait(barK, (k_loads - 1) & 1, a.wait_ns);
         }
     } else if (a.S_to != nullptr) {
 #pragma unroll
@@ -590,13 +646,34 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
+__global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) { chain_role(a, blockIdx.x, nullptr); }
+
+// ------------------------------------------------------------------ delta_fused
+// Preparation and chain in one cooperative launch: CTAs 0 .. B H - 1 run the
+// chains over the whole sequence, the others claim preparation units chunk
+// by chunk from ctrl[0] and set a unit's ready word (ctrl[1 + bh NC + n])
+// once its tiles are written.  A chain waits only on ready words and a
+// preparation unit waits on nothing but its own copies, and every CTA is
+// resident, so every wait ends (each is bounded all the same).  The
+// arithmetic of every unit and chain step is the segmented pipeline's, so the
+// bits are too.
+__global__ void __launch_bounds__(NT, 1)
+delta_fused(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
+            const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a, unsigned* ctrl) {
+    if ((int)blockIdx.x < a.B * a.H)
+        chain_role(a, blockIdx.x, ctrl + 1);
+    else
+        prep_role(&map_ks, &map_kn, &map_vn, a, ctrl, ctrl + 1);
+}
+
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;
-    return 5 * round256((int64_t)B * H * nc * dk * dv * 4) + round256((int64_t)B * H * dk * dv * 4);
+    return 5 * round256((int64_t)B * H * nc * dk * dv * 4) + round256((int64_t)B * H * dk * dv * 4) +
+           round256((1 + (int64_t)B * H * nc) * 4);
 }
 
 bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && x.dk == DKC && x.dv == 128; }
@@ -634,7 +711,7 @@ int delta_seg_start(int NC, int nseg, int g) {
 // Events order the stages (fork from and join to the caller's stream); no
 // kernel waits on another.
 cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
-                                 int segments, const DeltaPipe& pipe, cudaStream_t s) {
+                                 int segments, bool poison, const DeltaPipe& pipe, cudaStream_t s) {
     DeltaArgs d{};
     d.B = x.B; d.T = x.T; d.H = x.H;
     d.NC = (x.T + CH - 1) / CH;
@@ -647,6 +724,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     d.St = reinterpret_cast<float*>(p + 3 * tile_bytes);
     d.DTt = reinterpret_cast<float*>(p + 4 * tile_bytes);
     float* S_mid = reinterpret_cast<float*>(p + 5 * tile_bytes);
+    unsigned* ctrl = reinterpret_cast<unsigned*>(p + 5 * tile_bytes + round256((int64_t)x.B * x.H * DKC * 128 * 4));
     d.st = st;
     d.wait_ns = wait_ns;
 
@@ -669,6 +747,37 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     if (x.o != nullptr) {
         e = set_smem_attr_once(output_unit_decay_kernel(), output_unit_decay_smem());
         if (e != cudaSuccess) return e;
+    }
+
+    ChunkArgs c{};
+    c.B = x.B; c.T = x.T; c.H = x.H; c.G = x.H; c.NC = d.NC;
+    c.scale = x.scale;
+    c.q = x.q; c.k = x.k; c.v = nullptr; c.vt = d.DTt; c.d = nullptr;
+    c.S_in = nullptr; c.S_out = nullptr; c.o = x.o;
+    c.W = d.St; c.gam = nullptr; c.anc = nullptr;
+    c.st = st;
+    c.wait_ns = wait_ns;
+
+    // Auto: preparation and chain in one cooperative launch (delta_fused) when
+    // the chains leave at least half the SMs to the preparation, then the
+    // output stage over every chunk; all on the caller's stream.
+    if (segments == 0 && d.NC >= 2 && 2 * x.B * x.H <= sm_count) {
+        const size_t fused_bytes = std::max(PrepSmem::bytes, ChainSmem::bytes);
+        e = set_smem_attr_once((const void*)delta_fused, fused_bytes);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(ctrl, 0, (size_t)(1 + (int64_t)x.B * x.H * d.NC) * 4, s);
+        if (e != cudaSuccess) return e;
+        d.n0 = 0;
+        d.n1 = d.NC;
+        d.S_from = x.S_in;
+        d.S_to = x.S_out;
+        d.poison = poison ? 1 : 0;
+        void* args[] = {(void*)&mks, (void*)&mkn, (void*)&mvn, (void*)&d, (void*)&ctrl};
+        e = cudaLaunchCooperativeKernel((const void*)delta_fused, dim3((unsigned)sm_count), dim3(NT), args, fused_bytes, s);
+        if (e != cudaSuccess || x.o == nullptr) return e;
+        c.n0 = 0;
+        c.nsg = d.NC;
+        return launch_output_unit_decay(c, sm_count, s);
     }
 
     const int nseg = delta_segments(d.NC, x.B * x.H, sm_count, segments);
@@ -694,15 +803,6 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
         for (cudaStream_t side : {sp, sc, so})
             if (e == cudaSuccess) e = cudaStreamWaitEvent(side, pipe.ev[0], 0);
     }
-
-    ChunkArgs c{};
-    c.B = x.B; c.T = x.T; c.H = x.H; c.G = x.H; c.NC = d.NC;
-    c.scale = x.scale;
-    c.q = x.q; c.k = x.k; c.v = nullptr; c.vt = d.DTt; c.d = nullptr;
-    c.S_in = nullptr; c.S_out = nullptr; c.o = x.o;
-    c.W = d.St; c.gam = nullptr; c.anc = nullptr;
-    c.st = st;
-    c.wait_ns = wait_ns;
 
     for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
         d.n0 = delta_seg_start(d.NC, nseg, g);

@@ -181,7 +181,7 @@ struct DeltaPipe {
 };
 int delta_segments(int NC, int BH, int sm_count, int requested);
 cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, uint64_t wait_ns, int sm_count,
-                                 int segments, const DeltaPipe& pipe, cudaStream_t stream);
+                                 int segments, bool poison, const DeltaPipe& pipe, cudaStream_t stream);
 
 // Readout epilogues (readout.cu).
 cudaError_t launch_readout_norm_gate(int64_t rows, int dv, const float* o, const float* g, const float* w, float eps,

@@ -163,6 +163,51 @@ def test_segments_give_the_same_bits(ctx, sr, segments):
     ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
 
 
+def test_fused_on_the_deltanet_workload_gives_the_same_bits(ctx, sr):
+    """The default call on the DeltaNet workload shape (B4 T4096 H8: one
+    cooperative launch of preparation and chains, then the output stage)
+    against one pipelined segment, bit for bit."""
+    B, T, H = 4, 4096, 8
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=470)
+    S0 = synth.normal((B, H, 128, 128), 8310) * 0.5
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 1)
+    o1, S1 = run(ctx, x, S0)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
+    o, S = run(ctx, x, S0)
+    assert np.array_equal(o, o1) and np.array_equal(S, S1)
+
+
+def test_many_heads_fall_back_to_the_pipeline(ctx, sr):
+    """B*H above half the SMs: the default call takes the segmented pipeline
+    and still gives the bits of one segment."""
+    B, T, H = 8, 300, 10
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=480)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 1)
+    o1, S1 = run(ctx, x)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
+    o, S = run(ctx, x)
+    assert np.array_equal(o, o1) and np.array_equal(S, S1)
+
+
+def test_fused_bounded_wait_reports_timeout(ctx, sr):
+    """The chains of the fused call wait for a ready value no CTA writes: each
+    wait runs out after the limit, the kernel returns, the context reports
+    SN_E_TIMEOUT once, and the next call is exact again."""
+    B, T, H = 1, 640, 2
+    x = synth.deltanet_inputs(B, T, H, 128, 128, cid=490)
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
+    ctx.set_option(sr.SN_OPT_WAIT_LIMIT_US, 2000)
+    ctx.set_option(sr.SN_OPT_DEBUG_POISON, 1)
+    run(ctx, x)
+    assert ctx.last_error() == sr.SN_E_TIMEOUT
+    assert ctx.last_error() == sr.SN_OK             # cleared
+    ctx.set_option(sr.SN_OPT_DEBUG_POISON, 0)
+    o, S = run(ctx, x)
+    assert ctx.last_error() == sr.SN_OK
+    ro, rS = ref(x)
+    assert _nrel(o, ro) <= TOL and _nrel(S, rS) <= TOL
+
+
 def test_segments_in_place_on_a_side_stream(ctx, sr):
     """Pipelined call issued on a non-default stream, state in place: the
     results are ordered on that stream."""
