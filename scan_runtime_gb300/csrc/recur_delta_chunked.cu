@@ -76,7 +76,7 @@ struct PrepSmem {
     static constexpr int b2 = 2 * OPF;           // A^T above the diagonal and X = (I + A)^{-1} on and
                                                  // below it (fp32, stride LDX), then T operand, then W
     static constexpr int beta = b2 + CH * LDX;
-    static constexpr int misc = beta + CH;       // barriers (products, K tile, k and v tiles), tmem slot
+    static constexpr int misc = beta + CH;       // barriers (products, K tile, v tile), tmem slot
     static constexpr size_t bytes = (size_t)(misc + 16) * 4 + 1024;
 };
 
@@ -191,9 +191,10 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
 }
 
 // Tiles by TMA: K in the 128-byte-swizzled operand layout for the Gram
-// products (four boxes of 32 keys x 128 tokens), then k and v as natural
-// [token][feature] boxes, transposed by the threads into the K^T and V^T
-// operands once the inverse is done; W and U leave through shared memory by
+// products (four boxes of 32 keys x 128 tokens), then v as a natural
+// [token][feature] box; once the inverse is done the threads transpose v and
+// K's tf32 part (still in its buffer) into the V^T and K^T operands; W and U
+// leave through shared memory by
 // bulk copies.  Rows past T read as zeros.  Units are taken chunk by chunk:
 // unit u of the segment is chunk n0 + u / (B H) of head-batch u mod (B H).
 // Without a queue a CTA takes the units blockIdx.x, blockIdx.x + gridDim.x,
@@ -202,9 +203,8 @@ __device__ __forceinline__ void inverse_level(float* Xm, const float* AT, int ti
 // once a unit's tiles are written it sets the unit's ready word.  The next
 // unit's K tile is requested as soon as the copies out have read the buffer
 // it lands in.
-__device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUtensorMap* map_kn,
-                                          const CUtensorMap* map_vn, const DeltaArgs& a, unsigned* queue,
-                                          unsigned* ready) {
+__device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUtensorMap* map_vn, const DeltaArgs& a,
+                                          unsigned* queue, unsigned* ready) {
     extern __shared__ unsigned char smem_raw[];
     using L = PrepSmem;
     float* base = reinterpret_cast<float*>(smem_align<1024>(smem_raw));
@@ -215,7 +215,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + L::misc);
     uint32_t* slot = reinterpret_cast<uint32_t*>(base + L::misc + 2);
     uint64_t* barK = reinterpret_cast<uint64_t*>(base + L::misc + 4);    // the swizzled K tile
-    uint64_t* barT = reinterpret_cast<uint64_t*>(base + L::misc + 6);    // the natural k and v tiles
+    uint64_t* barT = reinterpret_cast<uint64_t*>(base + L::misc + 6);    // the natural v tile
     int* s_next = reinterpret_cast<int*>(base + L::misc + 8);            // the next unit (thread 0 writes)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -250,6 +250,14 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         for (int at = 0; at < DKC / 32; ++at) tma_load_3d(buf0 + at * 4096, map_ks, barK, c.h * DKC + 32 * at, c.t0, c.b);
     };
     int k_loads = 0, t_loads = 0;   // thread 0: K tiles and k, v tile pairs requested
+    int64_t pending = -1;           // thread 0: the ready word of the last unit whose tiles left
+    auto publish = [&]() {          // thread 0: the tiles are written, then the word (gpu-scope release)
+        if (pending < 0) return;
+        bulk_wait_all();
+        fence_proxy_async_global();
+        st_release_gpu(ready + pending, 1u);
+        pending = -1;
+    };
 
     if (warp == 0) tc::tmem_alloc(slot, 256);
     if (tid == 0) {
@@ -278,6 +286,9 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         const Unit c = unit(u);
         const uint32_t ph = (uint32_t)it & 1;
         if (tid < CH) beta_s[tid] = tid < c.nval ? __ldg(a.beta + (c.row0 + tid) * a.H + c.h) : 0.f;
+        // thread 0: the last unit's W and U copies out have read the buffers
+        // this unit fills (they drain while this unit's K tile arrives)
+        if (tid == 0) bulk_wait_read_all();
         ok = __syncthreads_and(mbar_wait(barK, ph, a.wait_ns));
         if (!ok) break;
         if (tid == 0) *s_next = next_unit(u);   // read by every thread at the end of the unit
@@ -304,13 +315,15 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         ok = __syncthreads_and(mbar_wait(bar, 0, a.wait_ns));
         tc::fence_after_sync();
         if (!ok) break;
-        // the natural k and v tiles can stream in now (the Gram products have
-        // read the hi and lo parts of K) while the inverse runs
+        // the natural v tile can stream in now (the Gram products have read
+        // the lo part of K, whose buffer it takes) while the inverse runs; the last
+        // unit's tiles, stored a few microseconds ago, are published (waiting
+        // for them at the end of that unit stalled the CTA)
         if (tid == 0) {
+            publish();
             ++t_loads;
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(barT, 2 * OPF * 4);
-            tma_load_3d(buf0, map_kn, barT, c.h * DKC, c.t0, c.b);
+            mbar_arrive_expect_tx(barT, OPF * 4);
             tma_load_3d(buf1, map_vn, barT, c.h * 128, c.t0, c.b);
         }
         // A = diag(beta) strict_lower(K K^T) in fp32, stored transposed: AT[j][t] = A[t][j]
@@ -371,8 +384,8 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
 #pragma unroll
         for (int tb = 0; tb < CH / 8; ++tb) st4(buf2 + off128(8 * tb + tl, ic), tv[tb]);
 
-        // K^T and V^T, rounded, from the natural tiles: thread = feature
-        // column i, a half of the tokens, through registers
+        // K^T and V^T, rounded, from K's tf32 part and the natural v tile:
+        // thread = feature column i, a half of the tokens, through registers
         ok = __syncthreads_and(mbar_wait(barT, ph, a.wait_ns));
         if (!ok) break;
         {
@@ -380,7 +393,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
             float kr[CH / 2], vr[CH / 2];
 #pragma unroll
             for (int r = 0; r < CH / 2; ++r) {
-                kr[r] = buf0[(tb0 + r) * DKC + i];
+                kr[r] = buf0[off_sw(tb0 + r, i)];   // K's hi part: tf32(k) itself
                 vr[r] = buf1[(tb0 + r) * 128 + i];
             }
             __syncthreads();
@@ -425,23 +438,20 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            bulk_store(a.Wt + c.tile, buf2, OPF * 4);
+            // K^T first, in a group of its own: the next unit's K tile lands in
+            // its buffer as soon as it is read; W and U drain meanwhile
             bulk_store(a.KTt + c.tile, buf0, OPF * 4);
+            bulk_commit();
+            bulk_store(a.Wt + c.tile, buf2, OPF * 4);
             bulk_store(a.Ut + c.tile, buf1, OPF * 4);
             bulk_commit();
             const int un = *s_next;
             if (un >= 0) {
-                bulk_wait_read_all();   // the copies out have read the buffers the next unit fills
+                bulk_wait_read_allbut1();
                 issue_k(unit(un));
                 ++k_loads;
             }
-            if (ready != nullptr) {
-                // the tiles are written (the next K tile streams in meanwhile);
-                // then the unit's ready word, released at gpu scope
-                bulk_wait_all();
-                fence_proxy_async_global();
-                st_release_gpu(ready + c.word, 1u);
-            }
+            if (ready != nullptr) pending = (int64_t)c.word;
         }
         u = *s_next;
     }
@@ -452,16 +462,18 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         if (k_loads > 0) (void)mbar_wait(barK, (uint32_t)(k_loads - 1) & 1, a.wait_ns);
         if (t_loads > 0) (void)mbar_wait(barT, (uint32_t)(t_loads - 1) & 1, a.wait_ns);
     }
-    if (tid == 0) bulk_wait_all();   // every copy out complete before the CTA exits
+    if (tid == 0) {
+        if (ok) publish();   // the last unit's word
+        bulk_wait_all();     // every copy out complete before the CTA exits
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 __global__ void __launch_bounds__(NT, 1)
-delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
-           const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a) {
-    prep_role(&map_ks, &map_kn, &map_vn, a, nullptr, nullptr);
+delta_prep(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a) {
+    prep_role(&map_ks, &map_vn, a, nullptr, nullptr);
 }
 
 // ------------------------------------------------------------------ delta_chain
@@ -658,12 +670,12 @@ __global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) { chain_
 // arithmetic of every unit and chain step is the segmented pipeline's, so the
 // bits are too.
 __global__ void __launch_bounds__(NT, 1)
-delta_fused(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_kn,
-            const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a, unsigned* ctrl) {
+delta_fused(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a,
+            unsigned* ctrl) {
     if ((int)blockIdx.x < a.B * a.H)
         chain_role(a, blockIdx.x, ctrl + 1);
     else
-        prep_role(&map_ks, &map_kn, &map_vn, a, ctrl, ctrl + 1);
+        prep_role(&map_ks, &map_vn, a, ctrl, ctrl + 1);
 }
 
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -728,15 +740,15 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     d.st = st;
     d.wait_ns = wait_ns;
 
-    // TMA maps of k (swizzled boxes of 32 keys for the Gram products, and the
-    // natural tile) and v (natural tile): (B, T, H * 128) row-major
-    CUtensorMap mks, mkn, mvn;
+    // TMA maps of k (swizzled boxes of 32 keys for the Gram products; K^T is
+    // transposed from that tile's tf32 part) and v (natural tile):
+    // (B, T, H * 128) row-major
+    CUtensorMap mks, mvn;
     {
         const uint64_t dims[3] = {(uint64_t)x.H * DKC, (uint64_t)x.T, (uint64_t)x.B};
         const uint64_t strides[2] = {(uint64_t)x.H * DKC * 4, (uint64_t)x.T * x.H * DKC * 4};
         const uint32_t box_sw[3] = {32, (uint32_t)CH, 1}, box_n[3] = {DKC, (uint32_t)CH, 1};
         if (!encode_tiled(&mks, 3, x.k, dims, strides, box_sw, true) ||
-            !encode_tiled(&mkn, 3, x.k, dims, strides, box_n, false) ||
             !encode_tiled(&mvn, 3, x.v, dims, strides, box_n, false))
             return cudaErrorInvalidValue;
     }
@@ -772,7 +784,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
         d.S_from = x.S_in;
         d.S_to = x.S_out;
         d.poison = poison ? 1 : 0;
-        void* args[] = {(void*)&mks, (void*)&mkn, (void*)&mvn, (void*)&d, (void*)&ctrl};
+        void* args[] = {(void*)&mks, (void*)&mvn, (void*)&d, (void*)&ctrl};
         e = cudaLaunchCooperativeKernel((const void*)delta_fused, dim3((unsigned)sm_count), dim3(NT), args, fused_bytes, s);
         if (e != cudaSuccess || x.o == nullptr) return e;
         c.n0 = 0;
@@ -811,7 +823,7 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
         // beside the chain of the segment before and leaves the chain's SMs
         // free, so that the chain starts as soon as its inputs exist
         const int units = x.B * x.H * (d.n1 - d.n0);
-        delta_prep<<<(unsigned)std::min(units, g > 0 ? side : sm_count), NT, PrepSmem::bytes, sp>>>(mks, mkn, mvn, d);
+        delta_prep<<<(unsigned)std::min(units, g > 0 ? side : sm_count), NT, PrepSmem::bytes, sp>>>(mks, mvn, d);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = order(sp, sc);
         if (e != cudaSuccess) break;
