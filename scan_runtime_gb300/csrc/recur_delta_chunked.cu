@@ -438,20 +438,27 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            // K^T first, in a group of its own: the next unit's K tile lands in
-            // its buffer as soon as it is read; W and U drain meanwhile
+            // The copy engine works in order: K^T first, then the next unit's
+            // K tile into its buffer as soon as it is read, then W.  U (staged
+            // in its global layout) leaves by the threads' own 16-byte stores
+            // meanwhile, beside the copy engine.
             bulk_store(a.KTt + c.tile, buf0, OPF * 4);
-            bulk_commit();
-            bulk_store(a.Wt + c.tile, buf2, OPF * 4);
-            bulk_store(a.Ut + c.tile, buf1, OPF * 4);
             bulk_commit();
             const int un = *s_next;
             if (un >= 0) {
-                bulk_wait_read_allbut1();
+                bulk_wait_read_all();
                 issue_k(unit(un));
                 ++k_loads;
             }
+            bulk_store(a.Wt + c.tile, buf2, OPF * 4);
+            bulk_commit();
             if (ready != nullptr) pending = (int64_t)c.word;
+        }
+        {
+            float4* ug = reinterpret_cast<float4*>(a.Ut + c.tile);
+            const float4* us = reinterpret_cast<const float4*>(buf1);
+#pragma unroll 4
+            for (int f = tid; f < OPF / 4; f += NT) ug[f] = us[f];
         }
         u = *s_next;
     }
