@@ -110,7 +110,7 @@ typedef int32_t sn_status;
                                       dimension does not divide would fail with SN_E_INVAL before any
                                       launch (no compiled tile and head size has such a width) */
 #define SN_OPT_DELTA_SEGMENTS   7  /* sn_recur_delta_chunked: 0 auto (default): one cooperative launch of
-                                      the preparation and the chains, then the output stage, where the
+                                      the preparation, the chains and the output stage, where the
                                       chains (one CTA per head and batch row) leave at least half the SMs,
                                       else a segmented pipeline; or 1..8 segments of the chunk sequence run
                                       as a pipeline (same bits for every value) */
@@ -395,9 +395,10 @@ int64_t sn_recur_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_
  * workspace of at least sn_recur_delta_chunked_workspace_bytes() bytes (else
  * SN_E_NOMEM), which the call overwrites.
  * Streams: by default (SN_OPT_DELTA_SEGMENTS 0, with B*H at most half the
- * SMs) the call runs on `stream` alone: one cooperative launch whose chains
- * wait, bounded, for the preparation of each chunk (SN_E_TIMEOUT past
- * SN_OPT_WAIT_LIMIT_US), then the output stage.  Otherwise, for more than a
+ * SMs) the call runs on `stream` alone as one cooperative launch, whose
+ * chains wait, bounded, for the preparation of each chunk and whose output
+ * units wait for their chains (SN_E_TIMEOUT past SN_OPT_WAIT_LIMIT_US).
+ * Otherwise, for more than a
  * few chunks, it splits the sequence into segments and runs the chain of one
  * segment beside the preparation of the next on side streams the context
  * created with it (sn_ctx_create); the call itself creates no stream or
@@ -415,8 +416,8 @@ sn_status sn_recur_delta_chunked(SnCtx* ctx, int32_t B, int32_t T, int32_t H,
 /* Workspace bytes sn_recur_delta_chunked needs: five tiles of dk x dv floats
  * per chunk of 128 tokens and head (W, K^T, U, the chunk state and the
  * chunk's deltas), one fp32 dk x dv state per head (carried between
- * segments) and 4 * (1 + B * H * chunks) bytes of control words, each kind
- * rounded up to 256 bytes; -1 on invalid arguments. */
+ * segments) and 4 * (2 + B * H * (chunks + 1)) bytes of control words,
+ * each kind rounded up to 256 bytes; -1 on invalid arguments. */
 int64_t sn_recur_delta_chunked_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
 
 /* ---------------------------------------------------------------- readout epilogues */

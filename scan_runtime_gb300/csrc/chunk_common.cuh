@@ -148,6 +148,8 @@ __device__ __forceinline__ void copy_transposed(float* dst, const float* base, s
 cudaError_t launch_output_unit_decay(const ChunkArgs& a, int max_ctas, cudaStream_t s);
 const void* output_unit_decay_kernel();
 size_t output_unit_decay_smem();
+// The output stage's TMA maps (q and k swizzled boxes; o, zero without o).
+bool output_maps(const ChunkArgs& a, int dv, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mo);
 
 }  // namespace chunk
 }  // namespace sn

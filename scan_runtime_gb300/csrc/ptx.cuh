@@ -65,6 +65,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Ends an mbarrier's life, before its shared memory serves another purpose.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -166,6 +171,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 
 // Wait until all but the most recent committed bulk store group have finished
 // reading shared memory.
+// Wait until all but the most recent committed bulk store group have
+// completed (writes performed).
+__device__ __forceinline__ void bulk_wait_allbut1() {
+    asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_wait_read_allbut1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }

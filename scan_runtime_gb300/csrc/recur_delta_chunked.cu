@@ -31,6 +31,7 @@
 // relative); splits at multiples of 128 tokens are bit-exact because the state
 // crosses chunks in fp32.
 #include "chunk_common.cuh"
+#include "chunk_output.cuh"
 
 #include <algorithm>
 
@@ -41,7 +42,7 @@ using namespace chunk;
 
 constexpr int LDX = CH + 4;         // row stride of A^T and X (rows of float4)
 constexpr int BSZ = 16;             // diagonal block size of the inverse
-constexpr int SITE_PREP_WAIT1 = 7, SITE_PREP_WAIT2 = 8, SITE_CHAIN_WAIT = 9;
+constexpr int SITE_PREP_WAIT1 = 7, SITE_PREP_WAIT2 = 8, SITE_CHAIN_WAIT = 9, SITE_OUT_READY = 10;
 
 struct DeltaArgs {
     int B, T, H, NC;
@@ -259,7 +260,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
         pending = -1;
     };
 
-    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (warp == 0) tc::tmem_alloc_keep(slot, 256);
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(barK, 1);
@@ -472,6 +473,9 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* map_ks, const CUten
     if (tid == 0) {
         if (ok) publish();   // the last unit's word
         bulk_wait_all();     // every copy out complete before the CTA exits
+        mbar_inval(bar);     // the fused kernel's output stage reuses this memory
+        mbar_inval(barK);
+        mbar_inval(barT);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -494,8 +498,10 @@ struct ChainSmem {
 
 // The chain of head-batch bh over chunks [n0, n1).  With ready words (the
 // fused kernel), thread 0 waits, bounded, for a chunk's word before it
-// requests the chunk's first tile.
-__device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, const unsigned* ready) {
+// requests the chunk's first tile, and publishes in progress[bh] how many
+// chunks have their state and delta tiles written.
+__device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, const unsigned* ready,
+                                           unsigned* progress) {
     extern __shared__ unsigned char smem_raw[];
     using L = ChainSmem;
     float* base = align128(smem_raw);
@@ -528,7 +534,7 @@ __device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, con
     };
     int w_loads = 0, k_loads = 0;   // bulk loads issued on barW / barK (thread 0's count)
 
-    if (warp == 0) tc::tmem_alloc(slot, 256);
+    if (warp == 0) tc::tmem_alloc_keep(slot, 256);
     if (tid == 0) {
         mbar_init(barW, 1);
         mbar_init(barK, 1);
@@ -587,6 +593,12 @@ __device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, con
             tc::gemm_tf32(tmem, SUb, Wb, DKC, id, false);
             tc::commit(barM);
             bulk_wait_read_all();   // the S_n tile store has read the buffer the deltas overwrite
+            if (progress != nullptr && n > a.n0) {
+                // every copy but S_n's is complete: chunks before n have their tiles
+                bulk_wait_allbut1();
+                fence_proxy_async_global();
+                st_release_gpu(progress + bh, (uint32_t)n);
+            }
         }
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
         mpar ^= 1;
@@ -648,7 +660,13 @@ __device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, con
         tc::fence_after_sync();
         if (tid == 0 && n + 1 < a.n1) store_tile(a.St, n + 1);
     }
-    if (tid == 0) bulk_wait_all();   // every tile store complete before the CTA exits
+    if (tid == 0) {
+        bulk_wait_all();   // every tile store complete before the CTA exits
+        if (ok && progress != nullptr) {
+            fence_proxy_async_global();
+            st_release_gpu(progress + bh, (uint32_t)a.n1);
+        }
+    }
     if (!ok) {
         if (tid == 0) {
             record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_CHAIN_WAIT);
@@ -660,29 +678,91 @@ __device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, con
 #pragma unroll
         for (int r = 0; r < 64; ++r) a.S_to[sbase + (size_t)(64 * part + r) * 128 + c] = sreg[r];
     }
+    if (tid == 0) {   // the fused kernel's output stage reuses this memory
+        mbar_inval(barW);
+        mbar_inval(barK);
+        mbar_inval(barM);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-__global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) { chain_role(a, blockIdx.x, nullptr); }
+__global__ void __launch_bounds__(NT, 1) delta_chain(const DeltaArgs a) {
+    chain_role(a, blockIdx.x, nullptr, nullptr);
+}
+
+// Output units of the fused kernel, chunk by chunk (all heads of chunk 0,
+// then chunk 1, ...), claimed from a counter; a unit's tiles may be read once
+// its chain's progress word has passed the unit's chunk.  A wait gives up
+// after the limit, or at once when an error is already recorded.
+struct QueueUnits {
+    int units, BH;
+    unsigned* queue;
+    const unsigned* progress;
+    static constexpr bool kDynamic = true;
+    __device__ int claim() const {
+        const unsigned v = atomicAdd(queue, 1u);
+        return v < (unsigned)units ? (int)v : -1;
+    }
+    __device__ int first() const { return claim(); }
+    __device__ int next(int) const { return claim(); }
+    __device__ ChunkIdx index(const ChunkArgs& a, int u) const {
+        ChunkIdx c;
+        const int bh = u % BH;
+        c.n = u / BH;
+        c.h = bh % a.H;
+        c.b = bh / a.H;
+        c.g = c.h / (a.H / a.G);
+        c.t0 = c.n * CH;
+        c.nval = min(CH, a.T - c.t0);
+        c.bh = (size_t)bh;
+        return c;
+    }
+    __device__ bool ready(const ChunkArgs& a, const ChunkIdx& c) const {
+        const uint32_t* w = progress + c.bh;
+        const uint32_t need = (uint32_t)c.n + 1;
+        if (ld_acquire_gpu(w) < need) {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_gpu(w) < need) {
+                if (*reinterpret_cast<volatile const int*>(&a.st->error) != 0 || global_ns() - t0 > a.wait_ns) {
+                    record_error(a.st, SN_E_TIMEOUT, (SN_K_RECUR_CHUNK << 16) | SITE_OUT_READY);
+                    return false;
+                }
+            }
+        }
+        fence_proxy_async_global();   // the bulk copies that follow read what the word published
+        return true;
+    }
+};
 
 // ------------------------------------------------------------------ delta_fused
-// Preparation and chain in one cooperative launch: CTAs 0 .. B H - 1 run the
-// chains over the whole sequence, the others claim preparation units chunk
-// by chunk from ctrl[0] and set a unit's ready word (ctrl[1 + bh NC + n])
-// once its tiles are written.  A chain waits only on ready words and a
-// preparation unit waits on nothing but its own copies, and every CTA is
-// resident, so every wait ends (each is bounded all the same).  The
-// arithmetic of every unit and chain step is the segmented pipeline's, so the
-// bits are too.
+// The whole call in one cooperative launch.  CTAs 0 .. B H - 1 run the chains
+// over the whole sequence; the others claim preparation units chunk by chunk
+// from ctrl[0] and set a unit's ready word (ctrl[2 + bh NC + n]) once its
+// tiles are written; a chain publishes in its progress word (after the ready
+// words) how many chunks have their state and delta tiles written.  Every CTA
+// then claims output units from ctrl[1], chunk by chunk, and computes each
+// once its chain's progress has passed it.  Preparation units wait on nothing
+// but their own copies, every one is claimed before any output unit, chains
+// wait only on ready words and every CTA is resident, so every wait ends
+// (each is bounded all the same).  The arithmetic of every unit and chain
+// step is the pipeline's, so the bits are too.
 __global__ void __launch_bounds__(NT, 1)
-delta_fused(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vn, const DeltaArgs a,
-            unsigned* ctrl) {
-    if ((int)blockIdx.x < a.B * a.H)
-        chain_role(a, blockIdx.x, ctrl + 1);
+delta_fused(const __grid_constant__ CUtensorMap map_ks, const __grid_constant__ CUtensorMap map_vn,
+            const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_o, const DeltaArgs a, const ChunkArgs oc, unsigned* ctrl) {
+    const int BH = a.B * a.H;
+    unsigned* ready = ctrl + 2;
+    unsigned* progress = ready + (size_t)BH * a.NC;
+    if ((int)blockIdx.x < BH)
+        chain_role(a, blockIdx.x, ready, progress);
     else
-        prep_role(&map_ks, &map_vn, a, ctrl, ctrl + 1);
+        prep_role(&map_ks, &map_vn, a, ctrl, ready);
+    if (oc.o != nullptr) {
+        QueueUnits sch{BH * a.NC, BH, ctrl + 1, progress};
+        output_loop<false, 128>(&map_q, &map_k, &map_o, oc, sch);
+    }
 }
 
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -692,7 +772,7 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 int64_t delta_chunked_ws_bytes(int B, int T, int H, int dk, int dv) {
     const int64_t nc = (T + CH - 1) / CH;
     return 5 * round256((int64_t)B * H * nc * dk * dv * 4) + round256((int64_t)B * H * dk * dv * 4) +
-           round256((1 + (int64_t)B * H * nc) * 4);
+           round256((2 + (int64_t)B * H * (nc + 1)) * 4);
 }
 
 bool delta_chunked_supported(const RecurArgs& x) { return x.kind == RK_DELTA && x.dk == DKC && x.dv == 128; }
@@ -777,26 +857,27 @@ cudaError_t launch_delta_chunked(const RecurArgs& x, void* ws, SnDevStatus* st, 
     c.st = st;
     c.wait_ns = wait_ns;
 
-    // Auto: preparation and chain in one cooperative launch (delta_fused) when
-    // the chains leave at least half the SMs to the preparation, then the
-    // output stage over every chunk; all on the caller's stream.
+    // Auto: the whole call in one cooperative launch (delta_fused) when the
+    // chains leave at least half the SMs to the other stages; on the caller's
+    // stream.
     if (segments == 0 && d.NC >= 2 && 2 * x.B * x.H <= sm_count) {
-        const size_t fused_bytes = std::max(PrepSmem::bytes, ChainSmem::bytes);
+        const size_t fused_bytes = std::max({PrepSmem::bytes, ChainSmem::bytes, output_unit_decay_smem()});
         e = set_smem_attr_once((const void*)delta_fused, fused_bytes);
         if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(ctrl, 0, (size_t)(1 + (int64_t)x.B * x.H * d.NC) * 4, s);
+        c.n0 = 0;
+        c.nsg = d.NC;
+        CUtensorMap mq, mk, mo;
+        if (!output_maps(c, 128, &mq, &mk, &mo)) return cudaErrorInvalidValue;
+        e = cudaMemsetAsync(ctrl, 0, (size_t)(2 + (int64_t)x.B * x.H * (d.NC + 1)) * 4, s);
         if (e != cudaSuccess) return e;
         d.n0 = 0;
         d.n1 = d.NC;
         d.S_from = x.S_in;
         d.S_to = x.S_out;
         d.poison = poison ? 1 : 0;
-        void* args[] = {(void*)&mks, (void*)&mvn, (void*)&d, (void*)&ctrl};
-        e = cudaLaunchCooperativeKernel((const void*)delta_fused, dim3((unsigned)sm_count), dim3(NT), args, fused_bytes, s);
-        if (e != cudaSuccess || x.o == nullptr) return e;
-        c.n0 = 0;
-        c.nsg = d.NC;
-        return launch_output_unit_decay(c, sm_count, s);
+        void* args[] = {(void*)&mks, (void*)&mvn, (void*)&mq, (void*)&mk, (void*)&mo, (void*)&d, (void*)&c, (void*)&ctrl};
+        return cudaLaunchCooperativeKernel((const void*)delta_fused, dim3((unsigned)sm_count), dim3(NT), args, fused_bytes,
+                                           s);
     }
 
     const int nseg = delta_segments(d.NC, x.B * x.H, sm_count, segments);

@@ -70,6 +70,15 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
 }
 
+// Whole warp: the same, keeping the CTA's permit to allocate again (a CTA
+// that frees its columns and allocates once more, as the roles of one fused
+// kernel do, must not have given it up; with one CTA per SM nothing waits on
+// it).
+__device__ __forceinline__ void tmem_alloc_keep(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols));
+}
+
 // Whole warp: release the allocation.
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
