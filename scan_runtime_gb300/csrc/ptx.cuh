@@ -171,10 +171,10 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 
 // Wait until all but the most recent committed bulk store group have finished
 // reading shared memory.
-// Wait until all but the most recent committed bulk store group have
+// Wait until all but the two most recent committed bulk store groups have
 // completed (writes performed).
-__device__ __forceinline__ void bulk_wait_allbut1() {
-    asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+__device__ __forceinline__ void bulk_wait_allbut2() {
+    asm volatile("cp.async.bulk.wait_group 2;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_read_allbut1() {

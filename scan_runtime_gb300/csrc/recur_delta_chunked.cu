@@ -593,11 +593,14 @@ __device__ __forceinline__ void chain_role(const DeltaArgs& a, int bh_index, con
             tc::gemm_tf32(tmem, SUb, Wb, DKC, id, false);
             tc::commit(barM);
             bulk_wait_read_all();   // the S_n tile store has read the buffer the deltas overwrite
-            if (progress != nullptr && n > a.n0) {
-                // every copy but S_n's is complete: chunks before n have their tiles
-                bulk_wait_allbut1();
+            if (progress != nullptr && n > a.n0 + 1 && ((n - 1 - a.n0) & 3) == 0) {
+                // every copy but the two newest (Delta_{n-1}, S_n) is complete:
+                // chunks before n - 1 have their tiles (issued microseconds ago,
+                // so this wait does not hold up the chain); every fourth chunk,
+                // since the release is thread 0's, which issues the products
+                bulk_wait_allbut2();
                 fence_proxy_async_global();
-                st_release_gpu(progress + bh, (uint32_t)n);
+                st_release_gpu(progress + bh, (uint32_t)(n - 1));
             }
         }
         ok = __syncthreads_and(mbar_wait(barM, mpar, a.wait_ns));
