@@ -208,6 +208,33 @@ def test_fused_bounded_wait_reports_timeout(ctx, sr):
     assert _nrel(o, ro) <= TOL and _nrel(S, rS) <= TOL
 
 
+def test_fused_replayed_from_a_cuda_graph(ctx, sr):
+    """The default one-launch call captured in a CUDA graph (with the memset
+    that clears its control words) and replayed on new inputs: each replay
+    equals an uncaptured call bit for bit."""
+    B, T, H = 2, 1100, 3
+    ins = [synth.deltanet_inputs(B, T, H, 128, 128, cid=500 + i) for i in range(2)]
+    ctx.set_option(sr.SN_OPT_DELTA_SEGMENTS, 0)
+    expect = [run(ctx, x) for x in ins]
+    d = {n: ins[0][n].cuda().clone() for n in ("q", "k", "v", "beta")}
+    o = torch.empty((B, T, H, 128), device="cuda")
+    S = torch.empty((B, H, 128, 128), device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = sr.sn_recur_delta_chunked(ctx.handle, B, T, H, 128, 128, ins[0]["scale"], d["q"], d["k"], d["v"],
+                                       d["beta"], None, S, o, torch.cuda.current_stream())
+    assert st == sr.SN_OK
+    for _ in range(2):
+        for x, (eo, eS) in zip(ins, expect):
+            assert x["scale"] == ins[0]["scale"]
+            for n in d:
+                d[n].copy_(x[n])
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(o.cpu().numpy(), eo) and np.array_equal(S.cpu().numpy(), eS)
+
+
 def test_segments_in_place_on_a_side_stream(ctx, sr):
     """Pipelined call issued on a non-default stream, state in place: the
     results are ordered on that stream."""
